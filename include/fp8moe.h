@@ -1,0 +1,220 @@
+/*
+ * fp8moe -- FP8 / MXFP8 quantization and scaled grouped GEMM for the
+ * Mixture-of-Experts training hot path, for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument is a plain device pointer unless marked
+ * "host"; sizes are element counts.  The caller owns and allocates every
+ * buffer.  The library allocates no device memory: its only device state is
+ * one status word in static device memory per device, and TMA descriptors
+ * are passed to kernels by value.
+ *
+ * Streams.  Every call is asynchronous on the given stream (NULL = legacy
+ * default stream) and never synchronizes, except fp8moe_get_device_status.
+ * No call reads the routing offsets on the host: grouped kernels schedule
+ * experts on the device.
+ *
+ * Errors.  A problem visible on the host (null pointer, bad size, alignment,
+ * an unsupported combination) makes the call return an error before any
+ * launch and leaves the outputs untouched.  A problem only visible on the
+ * device (offsets that decrease, exceed M, do not end at M, or break a
+ * multiple-of-32 rule; a pipeline wait that runs out) sets the sticky
+ * device status word; the outputs of that launch are then unspecified.
+ * Read and clear it with fp8moe_get_device_status.
+ *
+ * Alignment.  Every data pointer must be 16-byte aligned.
+ *
+ * Sources (the library follows the behaviour these pages describe):
+ *  [AMD-FP8]  "FP8 Training on AMD GPUs with TorchTitan and TorchAO:
+ *             Upstreaming Performance Improvements", as summarised by
+ *             aitrends.kr (Korean), aihirek.info (Hungarian) and aixai.ru
+ *             (Russian).
+ *  [SCOUT]    "Accelerating Llama4 Scout training with TorchAO MXFP8 MoE
+ *             primitives", as summarised by aitrends.kr (Korean).
+ */
+#ifndef FP8MOE_H
+#define FP8MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* fp8moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  FP8MOE_OK = 0,
+  FP8MOE_ERR_INVALID_ARG = 1,     /* null pointer, negative or inconsistent size */
+  FP8MOE_ERR_ALIGNMENT = 2,       /* pointer not 16-byte aligned, bad multiple */
+  FP8MOE_ERR_UNSUPPORTED = 3,     /* e.g. e4m3fnuz with MXFP8 or with the GEMM */
+  FP8MOE_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
+  FP8MOE_ERR_DEVICE_OFFSETS = 5,  /* device: offsets invalid (read via get_device_status) */
+  FP8MOE_ERR_TIMEOUT = 6          /* device: a bounded pipeline wait ran out */
+} fp8moe_status;
+
+typedef enum {
+  FP8MOE_E4M3FN = 0,   /* max 448, NaN = S.1111.111, signed zero      */
+  FP8MOE_E4M3FNUZ = 1  /* max 240, no NaN/Inf values, unsigned zero   */
+} fp8moe_fp8_kind;
+
+typedef enum {
+  FP8MOE_ROWWISE = 0,  /* fp32 scale per row / per (expert, column)   */
+  FP8MOE_MXFP8 = 1     /* e8m0 scale per 1x32 block, 128x4-tiled      */
+} fp8moe_recipe;
+
+enum { FP8MOE_NO_GROUPS = -1, FP8MOE_GROUP_ROWS = 0, FP8MOE_GROUP_COLS = 1 };
+
+/* ------------------------------------------------------------------------
+ * Rowwise FP8 quantization.  [AMD-FP8] aihirek.info "A Triton-kernelok
+ * csökkentették a kvantálás költségét"; aixai.ru "Три уровня оптимизации
+ * Triton-ядер": absmax per row -> scale -> apply -> clamp -> cast, fused in
+ * one pass (one read of x, one write of q).
+ *
+ * x      [R, C] bf16, row stride ldx elements (ldx >= C, ldx % 8 == 0)
+ * q      [R, C] fp8 codes of `kind`, dense (row stride C); C % 16 == 0
+ * scale_inv [R] fp32: the dequantization scale fl(1/s), where
+ *        s = fl(fp8_max / max(amax_row, 1e-12)) and q = enc(fl(x * s))
+ *        (round to nearest even, saturating at +-fp8_max).
+ * kind   FP8MOE_E4M3FN or FP8MOE_E4M3FNUZ (quantize-only mode; [AMD-FP8]
+ *        aixai.ru "Тихая порча градиентов": the wrong maximum silently clips).
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_quantize_rowwise(const void* x, int64_t R, int64_t C, int64_t ldx,
+                                      int kind, void* q, float* scale_inv,
+                                      fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Colwise FP8 quantization of 3D expert weights or of routed rows.
+ * [AMD-FP8] aixai.ru "MoE: почему DeepSeek-V3 ломал пайплайн" (a column
+ * scale per expert) and "Три уровня оптимизации" (the backward colwise
+ * scales kernel: transposed output written through on-chip staging, single
+ * pass, no .t().contiguous() copy).
+ *
+ * offs == NULL (dense): x is [E, R, C] bf16 contiguous; the absmax runs over
+ *   R for every (e, c).  scale_inv is [E, C].  q is [E, C, R] when
+ *   transpose_out (R contiguous: the K-major operand of a GEMM contracting
+ *   over R), else [E, R, C].
+ * offs != NULL (jagged): x is [R, C] bf16 contiguous; offs is a device int32
+ *   [E] of cumulative exclusive group ends (group e = rows
+ *   [offs[e-1], offs[e]), offs[-1] = 0, offs[E-1] must equal R).  The
+ *   absmax runs over each group's rows for every column; an empty group
+ *   gets scale_inv = fl(1 / fl(fp8_max / 1e-12)).  q is
+ *   [C, fp8moe_jagged_t_cols(R, E)] when transpose_out, with group e in
+ *   columns [P_e, P_e + g_e), P_e = sum_{j<e} round_up(g_j, 32), every
+ *   other column 0; else [R, C].
+ * C % 16 == 0; dense transposed output also needs R % 16 == 0.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, int64_t C,
+                                         const int32_t* offs, int transpose_out, int kind,
+                                         void* q, float* scale_inv, fp8moe_stream_t stream);
+
+/* Width (columns) of the transposed jagged colwise output: round_up(M + 31*E, 16). */
+int64_t fp8moe_jagged_t_cols(int64_t M, int64_t E);
+
+/* ------------------------------------------------------------------------
+ * MXFP8 quantization along dim 0 (the contiguous dimension).  [SCOUT] MXFP8
+ * layout diagram: e4m3 data, one e8m0 scale per 1x32 block.
+ * x [B*R, C] bf16 contiguous (B batches of R rows), C % 32 == 0.
+ * q [B*R, C] e4m3fn codes; scale [B*R, C/32] e8m0 bytes, row-major.
+ * Scale rule: e = clamp(floor(log2(amax)) - 8, -127, 127), byte = e + 127
+ * (amax = 0 gives byte 0); q = enc_e4m3fn(x * 2^-e), RNE, saturating.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_mxfp8_quantize_dim0(const void* x, int64_t B, int64_t R, int64_t C,
+                                         void* q, uint8_t* scale, fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * MXFP8 quantization along dim 1 with transposed output.  [SCOUT] section
+ * details: dynamic quantization in forward and backward, with the layout
+ * change along the contracting dimension of the weight gradient.
+ * x [B, R, C] bf16 contiguous, R % 32 == 0, C % 16 == 0.
+ * qt [B, C, R] e4m3fn codes; scale [B, C, R/32] e8m0 bytes (blocks of 32
+ * consecutive rows of one column).  Routed rows whose groups are multiples
+ * of 32 need no offsets here: no block straddles two groups.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, int64_t C,
+                                         void* qt, uint8_t* scale, fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * 128x4 tiled scale layout for tcgen05 block-scaled MMA.  [SCOUT] section
+ * details and the caption of its 128x4 tile layout table: a dedicated kernel
+ * converts row-major scales into 128x4 tiles.
+ *
+ * Input s: [B, R, Cs] bytes, row-major.  Output: for each batch, the matrix
+ * padded to whole tiles, tile (rb, cb) at byte ((rb * CB) + cb) * 512 and
+ * element (r, c) of a tile at (r % 32) * 16 + (r / 32) * 4 + c.
+ * group_axis:
+ *   FP8MOE_NO_GROUPS  plain, B >= 1 batches, offs ignored (may be NULL).
+ *   FP8MOE_GROUP_ROWS B == 1; offs [E] (device) splits the R rows; each
+ *                     group starts a new 128-row block (forward / dgrad).
+ *   FP8MOE_GROUP_COLS B == 1; offs [E] (device) splits the *contracting
+ *                     elements* (32 per scale column; boundaries multiples of
+ *                     32); each group starts a new 4-column block (wgrad).
+ * Every byte of the output (fp8moe_swizzled_scales_bytes) is written: pads
+ * and unused tiles are 0.
+ * ------------------------------------------------------------------------ */
+int64_t fp8moe_swizzled_scales_bytes(int64_t B, int64_t R, int64_t Cs, int64_t E, int group_axis);
+fp8moe_status fp8moe_swizzle_scales_128x4(const uint8_t* s, int64_t B, int64_t R, int64_t Cs,
+                                          const int32_t* offs, int64_t E, int group_axis,
+                                          uint8_t* out, fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Scaled grouped GEMM, one launch over all experts, groups from device
+ * offsets.  [AMD-FP8] aixai.ru "MoE: почему DeepSeek-V3 ломал пайплайн"
+ * (row scales for activations, column scales per expert for weights, an
+ * offsets tensor, one launch); [SCOUT] MoE forward diagram (2D input, 3D
+ * weights, grouped by offsets); aixai.ru "Что такое FP8-обучение" (three
+ * GEMMs per linear layer).  Output bf16, fp32 accumulation on tcgen05
+ * tensor cores.  Only e4m3fn operands.
+ *
+ * forward:  out[m, :] = A[m, :] . W[e]^T  for m in group e
+ *   a [M, K] e4m3, w [E, N, K] e4m3, out [M, N] bf16.
+ *   MXFP8:   a_scale = fp8moe_swizzle_scales_128x4 of [M, K/32], GROUP_ROWS;
+ *            w_scale = swizzle of [E, N, K/32], NO_GROUPS, B = E.
+ *   ROWWISE: a_scale fp32 [M]; w_scale fp32 [E, N].
+ * dgrad:    dA[m, :] = dY[m, :] . Wt[e]^T  (contraction over N)
+ *   dy [M, N], wt [E, K, N] (the transposed weight from colwise / dim1
+ *   quantization), out [M, K].  Scales as forward with (K <-> N).
+ * wgrad:    dW[e] = dYt[:, group e] . At[:, group e]^T (contraction over
+ *   the routed tokens of group e; an empty group gives dW[e] = 0)
+ *   dyt [N, Mt], at [K, Mt], out [E, N, K].
+ *   MXFP8:   Mt = M, offs multiples of 32; scales = swizzle of [N, M/32] and
+ *            [K, M/32] with GROUP_COLS.
+ *   ROWWISE: Mt = fp8moe_jagged_t_cols(M, E), the group-padded layout of
+ *            fp8moe_quantize_colwise_3d; scales fp32 [E, N] and [E, K].
+ * Sizes: M >= 0, N % 16 == 0, K % 32 == 0 (MXFP8) or K % 16 == 0 (rowwise),
+ * E >= 1.  MXFP8 offsets must be multiples of 32 (device-checked).
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_scaled_grouped_mm_fwd(int recipe, const void* a, const void* a_scale,
+                                           const void* w, const void* w_scale,
+                                           const int32_t* offs, int64_t E, int64_t M,
+                                           int64_t N, int64_t K, void* out,
+                                           fp8moe_stream_t stream);
+fp8moe_status fp8moe_scaled_grouped_mm_dgrad(int recipe, const void* dy, const void* dy_scale,
+                                             const void* wt, const void* wt_scale,
+                                             const int32_t* offs, int64_t E, int64_t M,
+                                             int64_t N, int64_t K, void* out,
+                                             fp8moe_stream_t stream);
+fp8moe_status fp8moe_scaled_grouped_mm_wgrad(int recipe, const void* dyt, const void* dyt_scale,
+                                             const void* at, const void* at_scale,
+                                             const int32_t* offs, int64_t E, int64_t M,
+                                             int64_t N, int64_t K, void* out,
+                                             fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Device status.  Synchronizes `stream`, returns the sticky device error
+ * code (an fp8moe_status value, 0 if none) in *out_code and clears it.
+ * The pages' failure mode is silent ([AMD-FP8] aixai.ru "Тихая порча
+ * градиентов"); this makes device-side problems visible instead.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_get_device_status(fp8moe_stream_t stream, int32_t* out_code);
+
+/* Static string for a status code. */
+const char* fp8moe_status_string(int status);
+
+/* Library version, (major << 16) | minor. */
+int fp8moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8MOE_H */

@@ -1,0 +1,248 @@
+"""Python binding of libfp8moe (FP8 / MXFP8 MoE quantization + grouped GEMM).
+
+Argument marshalling only: every function below passes device pointers,
+sizes and the current CUDA stream of PyTorch to the C ABI declared in
+``include/fp8moe.h`` and raises ``Fp8MoeError`` on any non-OK status.  PyTorch
+provides device memory and streams; all arithmetic runs in the library's CUDA
+kernels.  There is no CPU path: importing works without a GPU (so the host
+logic can be tested), but every call needs the built library and a CUDA
+device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+__all__ = [
+    "E4M3FN", "E4M3FNUZ", "ROWWISE", "MXFP8", "NO_GROUPS", "GROUP_ROWS", "GROUP_COLS",
+    "Fp8MoeError", "lib", "library_path", "SYMBOLS",
+    "fp8moe_quantize_rowwise", "fp8moe_quantize_colwise_3d", "fp8moe_jagged_t_cols",
+    "fp8moe_mxfp8_quantize_dim0", "fp8moe_mxfp8_quantize_dim1",
+    "fp8moe_swizzled_scales_bytes", "fp8moe_swizzle_scales_128x4",
+    "fp8moe_scaled_grouped_mm_fwd", "fp8moe_scaled_grouped_mm_dgrad",
+    "fp8moe_scaled_grouped_mm_wgrad", "fp8moe_get_device_status", "fp8moe_status_string",
+]
+
+E4M3FN, E4M3FNUZ = 0, 1
+ROWWISE, MXFP8 = 0, 1
+NO_GROUPS, GROUP_ROWS, GROUP_COLS = -1, 0, 1
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(HERE, "libfp8moe.so")
+
+_i64, _i32, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+
+# name -> (restype, argtypes), mirroring include/fp8moe.h
+SYMBOLS = {
+    "fp8moe_quantize_rowwise": (_i32, [_vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "fp8moe_quantize_colwise_3d": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp]),
+    "fp8moe_jagged_t_cols": (_i64, [_i64, _i64]),
+    "fp8moe_mxfp8_quantize_dim0": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "fp8moe_mxfp8_quantize_dim1": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "fp8moe_swizzled_scales_bytes": (_i64, [_i64, _i64, _i64, _i64, _i32]),
+    "fp8moe_swizzle_scales_128x4": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _vp]),
+    "fp8moe_scaled_grouped_mm_fwd": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "fp8moe_scaled_grouped_mm_dgrad": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "fp8moe_scaled_grouped_mm_wgrad": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "fp8moe_get_device_status": (_i32, [_vp, ctypes.POINTER(ctypes.c_int32)]),
+    "fp8moe_status_string": (ctypes.c_char_p, [_i32]),
+    "fp8moe_version": (_i32, []),
+}
+
+
+class Fp8MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        msg = _lib_raw().fp8moe_status_string(code).decode() if _LIB is not None else str(code)
+        super().__init__(f"{fn}: status {code} ({msg})")
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def _lib_raw() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(library_path):
+            raise ImportError(
+                f"libfp8moe.so is not built ({library_path}); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        l = ctypes.CDLL(library_path)
+        for name, (res, args) in SYMBOLS.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = l
+    return _LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it is not built)."""
+    return _lib_raw()
+
+
+# ----------------------------------------------------------------------------
+# marshalling helpers
+# ----------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise Fp8MoeError(fn, code)
+
+
+def _empty(shape, dtype, like):
+    return _torch().empty(shape, dtype=dtype, device=like.device)
+
+
+def _u8(t):
+    torch = _torch()
+    return t.view(torch.uint8) if t.dtype != torch.uint8 else t
+
+
+# ----------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# ----------------------------------------------------------------------------
+
+def fp8moe_jagged_t_cols(M: int, E: int) -> int:
+    return int(_lib_raw().fp8moe_jagged_t_cols(M, E))
+
+
+def fp8moe_swizzled_scales_bytes(B: int, R: int, Cs: int, E: int = 0, group_axis: int = NO_GROUPS) -> int:
+    return int(_lib_raw().fp8moe_swizzled_scales_bytes(B, R, Cs, E, group_axis))
+
+
+def fp8moe_quantize_rowwise(x, kind: int = E4M3FN, q=None, scale_inv=None, stream=None):
+    """x [R, C] bf16 (row stride may exceed C) -> (q uint8 [R, C], scale_inv fp32 [R])."""
+    torch = _torch()
+    R, C = x.shape
+    q = _empty((R, C), torch.uint8, x) if q is None else q
+    scale_inv = _empty((R,), torch.float32, x) if scale_inv is None else scale_inv
+    _check("fp8moe_quantize_rowwise", _lib_raw().fp8moe_quantize_rowwise(
+        _ptr(x), R, C, x.stride(0), kind, _ptr(q), _ptr(scale_inv), _stream(stream)))
+    return q, scale_inv
+
+
+def fp8moe_quantize_colwise_3d(x, offs=None, transpose_out: bool = True, kind: int = E4M3FN,
+                               E: Optional[int] = None, q=None, scale_inv=None, stream=None):
+    """Dense x [E, R, C] (offs None) or jagged x [R, C] with offs [E] int32 (device).
+
+    Returns (q, scale_inv [E, C]); q is [E, C, R] / [E, R, C] (dense) or
+    [C, fp8moe_jagged_t_cols(R, E)] / [R, C] (jagged).
+    """
+    torch = _torch()
+    if offs is None:
+        E_, R, C = x.shape
+        qshape = (E_, C, R) if transpose_out else (E_, R, C)
+    else:
+        R, C = x.shape
+        E_ = offs.numel() if E is None else E
+        qshape = (C, fp8moe_jagged_t_cols(R, E_)) if transpose_out else (R, C)
+    q = _empty(qshape, torch.uint8, x) if q is None else q
+    scale_inv = _empty((E_, C), torch.float32, x) if scale_inv is None else scale_inv
+    _check("fp8moe_quantize_colwise_3d", _lib_raw().fp8moe_quantize_colwise_3d(
+        _ptr(x), E_, R, C, _ptr(offs), int(bool(transpose_out)), kind, _ptr(q), _ptr(scale_inv),
+        _stream(stream)))
+    return q, scale_inv
+
+
+def fp8moe_mxfp8_quantize_dim0(x, q=None, scale=None, stream=None):
+    """x [..., C] bf16 contiguous -> (q uint8 [..., C], scale uint8 [..., C/32])."""
+    torch = _torch()
+    C = x.shape[-1]
+    rows = x.numel() // C if C else 0
+    q = _empty(x.shape, torch.uint8, x) if q is None else q
+    scale = _empty(tuple(x.shape[:-1]) + (C // 32,), torch.uint8, x) if scale is None else scale
+    _check("fp8moe_mxfp8_quantize_dim0", _lib_raw().fp8moe_mxfp8_quantize_dim0(
+        _ptr(x), 1, rows, C, _ptr(q), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
+def fp8moe_mxfp8_quantize_dim1(x, qt=None, scale=None, stream=None):
+    """x [B, R, C] or [R, C] bf16 -> (qt uint8 [B, C, R], scale uint8 [B, C, R/32])."""
+    torch = _torch()
+    squeeze = x.dim() == 2
+    B, R, C = (1,) + tuple(x.shape) if squeeze else tuple(x.shape)
+    qshape, sshape = (B, C, R), (B, C, R // 32)
+    if squeeze:
+        qshape, sshape = qshape[1:], sshape[1:]
+    qt = _empty(qshape, torch.uint8, x) if qt is None else qt
+    scale = _empty(sshape, torch.uint8, x) if scale is None else scale
+    _check("fp8moe_mxfp8_quantize_dim1", _lib_raw().fp8moe_mxfp8_quantize_dim1(
+        _ptr(x), B, R, C, _ptr(qt), _ptr(scale), _stream(stream)))
+    return qt, scale
+
+
+def fp8moe_swizzle_scales_128x4(s, offs=None, group_axis: int = NO_GROUPS, E: Optional[int] = None,
+                                out=None, stream=None):
+    """s [R, Cs] or [B, R, Cs] uint8 -> flat uint8 swizzled buffer."""
+    torch = _torch()
+    B, R, Cs = (1,) + tuple(s.shape) if s.dim() == 2 else tuple(s.shape)
+    E_ = (offs.numel() if offs is not None else 0) if E is None else E
+    n = fp8moe_swizzled_scales_bytes(B, R, Cs, E_, group_axis)
+    out = _empty((n,), torch.uint8, s) if out is None else out
+    _check("fp8moe_swizzle_scales_128x4", _lib_raw().fp8moe_swizzle_scales_128x4(
+        _ptr(s), B, R, Cs, _ptr(offs), E_, group_axis, _ptr(out), _stream(stream)))
+    return out
+
+
+def _gemm(name, recipe, a, a_scale, b, b_scale, offs, E, M, N, K, out, out_shape, stream):
+    torch = _torch()
+    out = _empty(out_shape, torch.bfloat16, a) if out is None else out
+    fn = getattr(_lib_raw(), name)
+    _check(name, fn(recipe, _ptr(a), _ptr(a_scale), _ptr(b), _ptr(b_scale), _ptr(offs),
+                    E, M, N, K, _ptr(out), _stream(stream)))
+    return out
+
+
+def fp8moe_scaled_grouped_mm_fwd(recipe, a, a_scale, w, w_scale, offs, out=None, stream=None):
+    """a [M, K] e4m3 (uint8), w [E, N, K] e4m3 -> out [M, N] bf16."""
+    M, K = a.shape
+    E, N, _ = w.shape
+    return _gemm("fp8moe_scaled_grouped_mm_fwd", recipe, a, a_scale, w, w_scale, offs, E, M, N, K,
+                 out, (M, N), stream)
+
+
+def fp8moe_scaled_grouped_mm_dgrad(recipe, dy, dy_scale, wt, wt_scale, offs, out=None, stream=None):
+    """dy [M, N], wt [E, K, N] -> dA [M, K] bf16."""
+    M, N = dy.shape
+    E, K, _ = wt.shape
+    return _gemm("fp8moe_scaled_grouped_mm_dgrad", recipe, dy, dy_scale, wt, wt_scale, offs, E, M, N, K,
+                 out, (M, K), stream)
+
+
+def fp8moe_scaled_grouped_mm_wgrad(recipe, dyt, dyt_scale, at, at_scale, offs, M: int, out=None,
+                                   stream=None):
+    """dyt [N, Mt], at [K, Mt] -> dW [E, N, K] bf16 (M = routed rows)."""
+    N = dyt.shape[0]
+    K = at.shape[0]
+    E = offs.numel()
+    return _gemm("fp8moe_scaled_grouped_mm_wgrad", recipe, dyt, dyt_scale, at, at_scale, offs, E, M, N, K,
+                 out, (E, N, K), stream)
+
+
+def fp8moe_get_device_status(stream=None) -> int:
+    """Synchronize the stream; return and clear the sticky device status code."""
+    v = ctypes.c_int32(0)
+    _check("fp8moe_get_device_status", _lib_raw().fp8moe_get_device_status(_stream(stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+def fp8moe_status_string(code: int) -> str:
+    return _lib_raw().fp8moe_status_string(code).decode()

@@ -1,0 +1,225 @@
+// C-ABI entry points of libfp8moe: argument checks on the host, then launches
+// on the caller's stream.  See include/fp8moe.h for the contract of each call.
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "launch.h"
+
+// Sticky device status word (static device memory: the library allocates
+// nothing).  Kernels receive its address; fp8moe_get_device_status reads and
+// clears it.
+static __device__ int g_fp8moe_status;
+
+namespace {
+
+struct DevInfo {
+  bool init = false;
+  int* status = nullptr;
+  int num_sms = 0;
+  int max_smem = 0;
+};
+
+constexpr int kMaxDevices = 128;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+fp8moe_status device_info(DevInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FP8MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    if (cudaGetSymbolAddress((void**)&d.status, g_fp8moe_status) != cudaSuccess) return FP8MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FP8MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return FP8MOE_ERR_CUDA;
+    d.init = true;
+  }
+  *out = &d;
+  return FP8MOE_OK;
+}
+
+inline bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+inline fp8moe_status cuda_result(cudaError_t e) { return e == cudaSuccess ? FP8MOE_OK : FP8MOE_ERR_CUDA; }
+
+inline bool valid_kind(int kind) { return kind == FP8MOE_E4M3FN || kind == FP8MOE_E4M3FNUZ; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8moe_status_string(int s) {
+  switch (s) {
+    case FP8MOE_OK: return "ok";
+    case FP8MOE_ERR_INVALID_ARG: return "invalid argument";
+    case FP8MOE_ERR_ALIGNMENT: return "misaligned pointer or size";
+    case FP8MOE_ERR_UNSUPPORTED: return "unsupported combination";
+    case FP8MOE_ERR_CUDA: return "CUDA error";
+    case FP8MOE_ERR_DEVICE_OFFSETS: return "invalid routing offsets (device)";
+    case FP8MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fp8moe_version(void) { return (1 << 16) | 0; }
+
+int64_t fp8moe_jagged_t_cols(int64_t M, int64_t E) { return (M + 31 * E + 15) / 16 * 16; }
+
+fp8moe_status fp8moe_quantize_rowwise(const void* x, int64_t R, int64_t C, int64_t ldx, int kind, void* q,
+                                      float* scale_inv, fp8moe_stream_t stream) {
+  if (R < 0 || C < 0 || ldx < C || !valid_kind(kind)) return FP8MOE_ERR_INVALID_ARG;
+  if (R == 0 || C == 0) return FP8MOE_OK;
+  if (!x || !q || !scale_inv) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(q) || C % 16 || ldx % 8 || ((uintptr_t)scale_inv & 3)) return FP8MOE_ERR_ALIGNMENT;
+  if (C > (int64_t)1 << 30) return FP8MOE_ERR_INVALID_ARG;
+  return cuda_result(fp8moe::launch_quant_rowwise(x, R, C, ldx, kind, q, scale_inv, (cudaStream_t)stream));
+}
+
+fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                                         int transpose_out, int kind, void* q, float* scale_inv,
+                                         fp8moe_stream_t stream) {
+  if (E < 0 || R < 0 || C < 0 || !valid_kind(kind)) return FP8MOE_ERR_INVALID_ARG;
+  if (offs && E == 0) return FP8MOE_ERR_INVALID_ARG;
+  if (E == 0 || C == 0) return FP8MOE_OK;
+  if (!x || !q || !scale_inv) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(q) || C % 16 || ((uintptr_t)scale_inv & 3)) return FP8MOE_ERR_ALIGNMENT;
+  if (!offs && transpose_out && R % 16) return FP8MOE_ERR_ALIGNMENT;
+  if (offs && ((uintptr_t)offs & 3)) return FP8MOE_ERR_ALIGNMENT;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  const int64_t ldt = offs ? fp8moe_jagged_t_cols(R, E) : 0;
+  return cuda_result(fp8moe::launch_colwise(x, E, R, C, offs, transpose_out, kind, ldt, q, scale_inv, d->status,
+                                            d->max_smem, (cudaStream_t)stream));
+}
+
+fp8moe_status fp8moe_mxfp8_quantize_dim0(const void* x, int64_t B, int64_t R, int64_t C, void* q, uint8_t* scale,
+                                         fp8moe_stream_t stream) {
+  if (B < 0 || R < 0 || C < 0) return FP8MOE_ERR_INVALID_ARG;
+  if (C % 32) return FP8MOE_ERR_ALIGNMENT;
+  if (B == 0 || R == 0 || C == 0) return FP8MOE_OK;
+  if (!x || !q || !scale) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(q)) return FP8MOE_ERR_ALIGNMENT;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  return cuda_result(fp8moe::launch_mx_dim0(x, B * R, C, q, scale, d->num_sms, (cudaStream_t)stream));
+}
+
+fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt,
+                                         uint8_t* scale, fp8moe_stream_t stream) {
+  if (B < 0 || R < 0 || C < 0) return FP8MOE_ERR_INVALID_ARG;
+  if (R % 32 || C % 16) return FP8MOE_ERR_ALIGNMENT;
+  if (B == 0 || R == 0 || C == 0) return FP8MOE_OK;
+  if (!x || !qt || !scale) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(qt)) return FP8MOE_ERR_ALIGNMENT;
+  if (C > 65535 * 64 || R > (int64_t)1 << 31 || B > 65535) return FP8MOE_ERR_INVALID_ARG;
+  return cuda_result(fp8moe::launch_mx_dim1(x, B, R, C, qt, scale, (cudaStream_t)stream));
+}
+
+int64_t fp8moe_swizzled_scales_bytes(int64_t B, int64_t R, int64_t Cs, int64_t E, int group_axis) {
+  if (B < 0 || R < 0 || Cs < 0 || E < 0) return -1;
+  if (group_axis != FP8MOE_NO_GROUPS && group_axis != FP8MOE_GROUP_ROWS && group_axis != FP8MOE_GROUP_COLS)
+    return -1;
+  const fp8moe::SwizzleGeom g = fp8moe::swizzle_geom(R, Cs, group_axis == FP8MOE_NO_GROUPS ? 0 : E, group_axis);
+  return B * g.Rp * g.Cp;
+}
+
+fp8moe_status fp8moe_swizzle_scales_128x4(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, const int32_t* offs,
+                                          int64_t E, int group_axis, uint8_t* out, fp8moe_stream_t stream) {
+  if (B < 0 || R < 0 || Cs < 0 || E < 0) return FP8MOE_ERR_INVALID_ARG;
+  if (group_axis != FP8MOE_NO_GROUPS && group_axis != FP8MOE_GROUP_ROWS && group_axis != FP8MOE_GROUP_COLS)
+    return FP8MOE_ERR_INVALID_ARG;
+  if (group_axis != FP8MOE_NO_GROUPS) {
+    if (B != 1 || E < 1 || E > 1024 || !offs) return FP8MOE_ERR_INVALID_ARG;
+    if ((uintptr_t)offs & 3) return FP8MOE_ERR_ALIGNMENT;
+  }
+  if (fp8moe_swizzled_scales_bytes(B, R, Cs, E, group_axis) == 0) return FP8MOE_OK;
+  if (!out || (!s && R * Cs > 0)) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(out)) return FP8MOE_ERR_ALIGNMENT;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  return cuda_result(fp8moe::launch_swizzle(s, B, R, Cs, offs, E, group_axis, out, d->status, d->num_sms,
+                                            (cudaStream_t)stream));
+}
+
+static fp8moe_status grouped_mm(int mode, int recipe, const void* a, const void* a_scale, const void* b,
+                                const void* b_scale, const int32_t* offs, int64_t E, int64_t M, int64_t N,
+                                int64_t K, void* out, fp8moe_stream_t stream) {
+  if (recipe != FP8MOE_ROWWISE && recipe != FP8MOE_MXFP8) return FP8MOE_ERR_INVALID_ARG;
+  if (E < 1 || M < 0 || N < 0 || K < 0 || E > 4096) return FP8MOE_ERR_INVALID_ARG;
+  if (!offs || ((uintptr_t)offs & 3)) return FP8MOE_ERR_INVALID_ARG;
+  if (N % 16 || K % 16) return FP8MOE_ERR_ALIGNMENT;
+  if (recipe == FP8MOE_MXFP8) {
+    // the contracting dimension must hold whole 32-element scale blocks
+    if (mode == fp8moe::GEMM_FWD && K % 32) return FP8MOE_ERR_ALIGNMENT;
+    if (mode == fp8moe::GEMM_DGRAD && N % 32) return FP8MOE_ERR_ALIGNMENT;
+    if (mode == fp8moe::GEMM_WGRAD && M % 32) return FP8MOE_ERR_ALIGNMENT;
+  }
+  if (!a || !b || !out || !a_scale || !b_scale) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(a) || !al16(b) || !al16(out) || !al16(a_scale) || !al16(b_scale)) return FP8MOE_ERR_ALIGNMENT;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  fp8moe::GemmArgs g{};
+  g.recipe = recipe;
+  g.mode = mode;
+  g.E = (int)E;
+  g.offs = offs;
+  g.out = (uint16_t*)out;
+  g.status = d->status;
+  g.num_sms = d->num_sms;
+  g.max_smem = d->max_smem;
+  g.M = M;
+  g.a = (const uint8_t*)a;
+  g.b = (const uint8_t*)b;
+  g.a_scale = a_scale;
+  g.b_scale = b_scale;
+  if (mode == fp8moe::GEMM_FWD) {          // [M,K] x [E,N,K] -> [M,N]
+    g.rows = M, g.cols = N, g.kk = K;
+  } else if (mode == fp8moe::GEMM_DGRAD) { // [M,N] x [E,K,N] -> [M,K]
+    g.rows = M, g.cols = K, g.kk = N;
+  } else {                                 // [N,Mt] x [K,Mt] -> [E,N,K]
+    g.rows = N, g.cols = K;
+    g.kk = recipe == FP8MOE_MXFP8 ? M : fp8moe_jagged_t_cols(M, E);
+  }
+  if (g.rows == 0 || g.cols == 0) return FP8MOE_OK;
+  cudaError_t e = fp8moe::launch_grouped_mm(g, (cudaStream_t)stream);
+  if (e == cudaErrorNotSupported) return FP8MOE_ERR_UNSUPPORTED;
+  return cuda_result(e);
+}
+
+fp8moe_status fp8moe_scaled_grouped_mm_fwd(int recipe, const void* a, const void* a_scale, const void* w,
+                                           const void* w_scale, const int32_t* offs, int64_t E, int64_t M,
+                                           int64_t N, int64_t K, void* out, fp8moe_stream_t stream) {
+  return grouped_mm(fp8moe::GEMM_FWD, recipe, a, a_scale, w, w_scale, offs, E, M, N, K, out, stream);
+}
+
+fp8moe_status fp8moe_scaled_grouped_mm_dgrad(int recipe, const void* dy, const void* dy_scale, const void* wt,
+                                             const void* wt_scale, const int32_t* offs, int64_t E, int64_t M,
+                                             int64_t N, int64_t K, void* out, fp8moe_stream_t stream) {
+  return grouped_mm(fp8moe::GEMM_DGRAD, recipe, dy, dy_scale, wt, wt_scale, offs, E, M, N, K, out, stream);
+}
+
+fp8moe_status fp8moe_scaled_grouped_mm_wgrad(int recipe, const void* dyt, const void* dyt_scale, const void* at,
+                                             const void* at_scale, const int32_t* offs, int64_t E, int64_t M,
+                                             int64_t N, int64_t K, void* out, fp8moe_stream_t stream) {
+  return grouped_mm(fp8moe::GEMM_WGRAD, recipe, dyt, dyt_scale, at, at_scale, offs, E, M, N, K, out, stream);
+}
+
+fp8moe_status fp8moe_get_device_status(fp8moe_stream_t stream, int32_t* out_code) {
+  if (!out_code) return FP8MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FP8MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fp8moe_status, sizeof(int)) != cudaSuccess) return FP8MOE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_fp8moe_status, &zero, sizeof(int)) != cudaSuccess) return FP8MOE_ERR_CUDA;
+  *out_code = v;
+  return FP8MOE_OK;
+}
+
+}  // extern "C"

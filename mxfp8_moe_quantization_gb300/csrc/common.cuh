@@ -1,0 +1,118 @@
+// Shared device helpers for the fp8moe kernels (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/fp8moe.h"
+
+#define FP8MOE_DEV __device__ __forceinline__
+
+namespace fp8moe {
+
+// Sticky device error word: the first error wins.
+FP8MOE_DEV void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+FP8MOE_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+FP8MOE_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 values -> two e4m3fn codes, round to nearest even, saturating to
+// +-448 (the hardware conversion).  Byte 0 of the result holds `lo`.
+FP8MOE_DEV uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// e4m3fnuz code of an fp32 value v (|v| may exceed 240: saturates).
+// fnuz (bias 8) has exactly half the value of the fn code with the same bits
+// for every finite code, so enc_fnuz(v) = enc_fn'(2v), where fn' extends
+// e4m3fn by the code 0x7F = 480: |2v| above the 448/480 midpoint 464 maps to
+// 0x7F; the tie at 464 goes to the even code 0x7E, as the hardware
+// conversion already does.  Zero is unsigned in fnuz.
+FP8MOE_DEV uint32_t enc_fnuz(float v) {
+  float v2 = 2.0f * v;  // exact
+  uint32_t c = cvt_e4m3x2(v2, 0.0f) & 0xFFu;
+  if (fabsf(v2) > 464.0f) c = 0x7Fu | (v2 < 0.0f ? 0x80u : 0u);
+  if ((c & 0x7Fu) == 0u) c = 0u;
+  return c;
+}
+
+template <bool FNUZ>
+FP8MOE_DEV uint32_t enc2(float lo, float hi) {
+  if constexpr (FNUZ) {
+    return enc_fnuz(lo) | (enc_fnuz(hi) << 8);
+  } else {
+    return cvt_e4m3x2(lo, hi);
+  }
+}
+
+// Four fp32 -> four codes packed little-endian into a 32-bit word.
+template <bool FNUZ>
+FP8MOE_DEV uint32_t enc4(float a, float b, float c, float d) {
+  return enc2<FNUZ>(a, b) | (enc2<FNUZ>(c, d) << 16);
+}
+
+// Encode 8 bf16 values (a uint4 of packed bf16 pairs) scaled by s.
+template <bool FNUZ>
+FP8MOE_DEV uint2 enc8_bf16(uint4 v, float s) {
+  uint2 r;
+  r.x = enc4<FNUZ>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s),
+                   __fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s));
+  r.y = enc4<FNUZ>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s),
+                   __fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s));
+  return r;
+}
+
+// max |x| over 8 bf16 values: works on the bit patterns (|x| is the pattern
+// with the sign bit cleared, and for non-negative IEEE values integer order
+// is value order), exact.
+FP8MOE_DEV uint32_t absmax8_bits(uint4 v) {
+  uint32_t m = 0;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    m = max(m, w[i] & 0x7FFFu);
+    m = max(m, (w[i] >> 16) & 0x7FFFu);
+  }
+  return m;  // a bf16 bit pattern without sign
+}
+
+FP8MOE_DEV float bf16bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// Rowwise / colwise scale from an absolute maximum (all IEEE fp32, RN).
+template <bool FNUZ>
+FP8MOE_DEV void rowwise_scale(float amax, float& s, float& inv) {
+  const float fmax = FNUZ ? 240.0f : 448.0f;
+  s = __fdiv_rn(fmax, fmaxf(amax, 1e-12f));
+  inv = __fdiv_rn(1.0f, s);
+}
+
+// e8m0 block exponent from the bf16 bit pattern (sign cleared) of the block
+// absolute maximum: e = clamp(floor(log2(amax)) - 8, -127, 127).
+// floor(log2) of a normal bf16 is its exponent field - 127; a subnormal
+// (exponent field 0, 7-bit mantissa m) has floor(log2) = msb(m) - 133.
+FP8MOE_DEV int e8m0_exponent(uint32_t amax_bits) {
+  if (amax_bits == 0) return -127;
+  int ef = (int)(amax_bits >> 7);
+  int E;
+  if (ef != 0) {
+    E = ef - 127;
+  } else {
+    E = (31 - __clz((int)(amax_bits & 0x7F))) - 133;
+  }
+  int e = E - 8;
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^-e as an fp32 (e in [-127, 127]): built from the exponent field; for
+// e = 127 (2^-127) the value is a subnormal.
+FP8MOE_DEV float exp2_neg(int e) {
+  int be = 127 - e;  // biased exponent of 2^-e
+  if (be >= 1) return __uint_as_float((uint32_t)be << 23);
+  return __uint_as_float(1u << (22 + be));  // subnormal: 2^(be-127) = 2^-149 * 2^(be+22)
+}
+
+}  // namespace fp8moe

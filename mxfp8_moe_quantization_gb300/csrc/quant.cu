@@ -1,0 +1,530 @@
+// Fused FP8 / MXFP8 quantization kernels (sm_103a).
+//
+// Every kernel reads its bf16 input once from HBM and writes codes and scales
+// once: absmax, scale, clamp and cast happen in one pass ("FP8 Training on AMD
+// GPUs with TorchTitan and TorchAO", aihirek.info section "A Triton-kernelok
+// csökkentették a kvantálás költségét"; aixai.ru section "Три уровня
+// оптимизации Triton-ядер": the unfused chain with HBM intermediates is what
+// the pages remove).  Transposed outputs are staged through shared memory so
+// that global stores are contiguous (same pages: the colwise-scales kernel
+// whose lanes wrote K bytes apart).
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace cg = cooperative_groups;
+
+namespace fp8moe {
+
+FP8MOE_DEV uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+FP8MOE_DEV void cp_async16(void* smem, const void* gmem) {
+  uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem));
+}
+FP8MOE_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// ============================================================================
+// Rowwise: TPR threads per row, each holding V 16-byte chunks in registers.
+// ============================================================================
+template <int TPR, int V, bool FNUZ>
+__global__ void __launch_bounds__(256) k_quant_rowwise(const uint16_t* __restrict__ x, int64_t R,
+                                                       int C, int64_t ldx, uint8_t* __restrict__ q,
+                                                       float* __restrict__ inv_out) {
+  constexpr int RPB = 256 / TPR;
+  const int t = threadIdx.x % TPR;
+  const int rloc = threadIdx.x / TPR;
+  const int64_t row = (int64_t)blockIdx.x * RPB + rloc;
+  const bool active = row < R;
+  const int nch = C / 8;
+  const uint16_t* xr = x + (active ? row : 0) * ldx;
+  uint4 v[V];
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int ch = t + i * TPR;
+    if (active && ch < nch) {
+      v[i] = ld_stream(xr + (int64_t)ch * 8);
+    } else {
+      v[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i) m = max(m, absmax8_bits(v[i]));
+#pragma unroll
+  for (int o = (TPR < 32 ? TPR : 32) / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if constexpr (TPR > 32) {
+    __shared__ uint32_t red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    constexpr int WPR = TPR / 32;
+    m = 0;
+#pragma unroll
+    for (int w = 0; w < WPR; ++w) m = max(m, red[rloc * WPR + w]);
+  }
+  float s, inv;
+  rowwise_scale<FNUZ>(bf16bits_to_float(m), s, inv);
+  if (!active) return;
+  uint8_t* qr = q + row * (int64_t)C;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int ch = t + i * TPR;
+    if (ch < nch) *reinterpret_cast<uint2*>(qr + (int64_t)ch * 8) = enc8_bf16<FNUZ>(v[i], s);
+  }
+  if (t == 0) inv_out[row] = inv;
+}
+
+// Rows too long for registers: two passes over the row (the second re-reads
+// it from L2), one row per 256-thread block.
+template <bool FNUZ>
+__global__ void __launch_bounds__(256) k_quant_rowwise_long(const uint16_t* __restrict__ x, int64_t R,
+                                                            int C, int64_t ldx, uint8_t* __restrict__ q,
+                                                            float* __restrict__ inv_out) {
+  const int64_t row = blockIdx.x;
+  const uint16_t* xr = x + row * ldx;
+  const int nch = C / 8;
+  uint32_t m = 0;
+  for (int ch = threadIdx.x; ch < nch; ch += 256) m = max(m, absmax8_bits(ld_stream(xr + (int64_t)ch * 8)));
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0;
+  for (int w = 0; w < 8; ++w) m = max(m, red[w]);
+  float s, inv;
+  rowwise_scale<FNUZ>(bf16bits_to_float(m), s, inv);
+  uint8_t* qr = q + row * (int64_t)C;
+  for (int ch = threadIdx.x; ch < nch; ch += 256) {
+    uint4 v = *reinterpret_cast<const uint4*>(xr + (int64_t)ch * 8);
+    *reinterpret_cast<uint2*>(qr + (int64_t)ch * 8) = enc8_bf16<FNUZ>(v, s);
+  }
+  if (threadIdx.x == 0) inv_out[row] = inv;
+}
+
+template <int TPR, int V, bool FNUZ>
+static cudaError_t launch_rowwise_t(const void* x, int64_t R, int C, int64_t ldx, void* q, float* inv,
+                                    cudaStream_t st) {
+  constexpr int RPB = 256 / TPR;
+  const int64_t blocks = (R + RPB - 1) / RPB;
+  k_quant_rowwise<TPR, V, FNUZ><<<(unsigned)blocks, 256, 0, st>>>(
+      (const uint16_t*)x, R, C, ldx, (uint8_t*)q, inv);
+  return cudaGetLastError();
+}
+
+template <bool FNUZ>
+static cudaError_t launch_rowwise_k(const void* x, int64_t R, int C, int64_t ldx, void* q, float* inv,
+                                    cudaStream_t st) {
+  const int nch = C / 8;
+  int tpr = 32;
+  while (tpr < 256 && tpr * 8 < nch) tpr *= 2;
+  const int v = (nch + tpr - 1) / tpr;
+#define FP8MOE_RW(T, VV) \
+  if (tpr == T && v <= VV) return launch_rowwise_t<T, VV, FNUZ>(x, R, C, ldx, q, inv, st);
+  FP8MOE_RW(32, 1) FP8MOE_RW(32, 2) FP8MOE_RW(32, 4) FP8MOE_RW(32, 8)
+  FP8MOE_RW(64, 8) FP8MOE_RW(128, 8) FP8MOE_RW(256, 8)
+#undef FP8MOE_RW
+  k_quant_rowwise_long<FNUZ><<<(unsigned)R, 256, 0, st>>>((const uint16_t*)x, R, C, ldx, (uint8_t*)q, inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rowwise(const void* x, int64_t R, int64_t C, int64_t ldx, int kind, void* q,
+                                 float* inv, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  return kind == FP8MOE_E4M3FNUZ ? launch_rowwise_k<true>(x, R, (int)C, ldx, q, inv, st)
+                                 : launch_rowwise_k<false>(x, R, (int)C, ldx, q, inv, st);
+}
+
+// ============================================================================
+// MXFP8 dim0: four lanes per 32-element block, 8 bf16 (16 bytes) per lane.
+// ============================================================================
+template <int U>
+__global__ void __launch_bounds__(256) k_mx_dim0(const uint16_t* __restrict__ x, int64_t nch,
+                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  for (int64_t wb = warp0 * 32 * U; wb < nch; wb += warps_total * 32 * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t ch = wb + u * 32 + lane;
+      v[u] = ch < nch ? ld_stream(x + ch * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t ch = wb + u * 32 + lane;
+      uint32_t m = absmax8_bits(v[u]);
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      const int e = e8m0_exponent(m);
+      const float p = exp2_neg(e);
+      if (ch < nch) {
+        *reinterpret_cast<uint2*>(q + ch * 8) = enc8_bf16<false>(v[u], p);
+        if ((lane & 3) == 0) sc[ch >> 2] = (uint8_t)(e + 127);
+      }
+    }
+  }
+}
+
+cudaError_t launch_mx_dim0(const void* x, int64_t rows, int64_t C, void* q, uint8_t* s, int num_sms,
+                           cudaStream_t st) {
+  const int64_t nch = rows * C / 8;
+  if (nch == 0) return cudaSuccess;
+  constexpr int U = 4;
+  int64_t blocks = (nch + 256 * U - 1) / (256 * U);
+  const int64_t cap = (int64_t)num_sms * 8 * 4;
+  if (blocks > cap) blocks = cap;
+  k_mx_dim0<U><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, nch, (uint8_t*)q, s);
+  return cudaGetLastError();
+}
+
+// ============================================================================
+// MXFP8 dim1: a 128-row x 64-column bf16 tile in shared memory; each thread
+// owns one (32-row block, column) pair and writes 32 contiguous output bytes
+// of the transposed result.
+// ============================================================================
+constexpr int D1_ROWS = 128, D1_COLS = 64, D1_PITCH = 144;  // 128 B data + 16 B pad
+
+__global__ void __launch_bounds__(256) k_mx_dim1(const uint16_t* __restrict__ x, int64_t R, int64_t C,
+                                                 uint8_t* __restrict__ qt, uint8_t* __restrict__ sc) {
+  __shared__ __align__(16) uint8_t tile[D1_ROWS * D1_PITCH];
+  const int64_t r0 = (int64_t)blockIdx.x * D1_ROWS;
+  const int64_t c0 = (int64_t)blockIdx.y * D1_COLS;
+  const int64_t b = blockIdx.z;
+  const uint16_t* xb = x + b * R * C;
+  const int tid = threadIdx.x;
+  // load: 8 threads x 16 B per row, 4 passes of 32 rows
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int k = tid + 256 * i;
+    const int rr = k >> 3, c16 = k & 7;
+    const int64_t r = r0 + rr, c = c0 + c16 * 8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < R && c < C) v = ld_stream(xb + r * C + c);
+    *reinterpret_cast<uint4*>(tile + rr * D1_PITCH + c16 * 16) = v;
+  }
+  __syncthreads();
+  const int cl = tid & 63, rb = tid >> 6;
+  const int64_t c = c0 + cl;
+  const int64_t rbase = r0 + rb * 32;
+  if (c >= C || rbase >= R) return;
+  float f[32];
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t h = *reinterpret_cast<const uint16_t*>(tile + (rb * 32 + i) * D1_PITCH + cl * 2);
+    m = max(m, h & 0x7FFFu);
+    f[i] = bf16bits_to_float(h);
+  }
+  const int e = e8m0_exponent(m);
+  const float p = exp2_neg(e);
+  uint32_t w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    w[j] = enc4<false>(__fmul_rn(f[4 * j], p), __fmul_rn(f[4 * j + 1], p), __fmul_rn(f[4 * j + 2], p),
+                       __fmul_rn(f[4 * j + 3], p));
+  uint8_t* dst = qt + (b * C + c) * R + rbase;
+  reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  sc[(b * C + c) * (R / 32) + rbase / 32] = (uint8_t)(e + 127);
+}
+
+cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s,
+                           cudaStream_t st) {
+  if (B == 0 || R == 0 || C == 0) return cudaSuccess;
+  dim3 grid((unsigned)((R + D1_ROWS - 1) / D1_ROWS), (unsigned)((C + D1_COLS - 1) / D1_COLS), (unsigned)B);
+  k_mx_dim1<<<grid, 256, 0, st>>>((const uint16_t*)x, R, C, (uint8_t*)qt, s);
+  return cudaGetLastError();
+}
+
+// ============================================================================
+// Colwise (per expert, per column) FP8: a 32-column strip of one group stays
+// resident in shared memory between the absmax and the cast.  Strips taller
+// than one CTA's shared memory are split over a thread-block cluster whose
+// CTAs exchange their partial column maxima through distributed shared
+// memory; groups taller than the whole cluster fall back to re-reading the
+// overflow from L2.
+// ============================================================================
+constexpr int CW_COLS = 32, CW_PITCH = 80;      // 64 B of bf16 + 16 B pad per row
+constexpr int CW_TCHUNK = 256;                  // rows per transposed output chunk
+constexpr int CW_TPITCH = CW_TCHUNK + 16;
+
+struct ColwiseArgs {
+  const uint16_t* x;
+  int64_t C;
+  int64_t R;          // dense: rows per expert; jagged: total rows
+  int E;
+  const int32_t* offs;  // NULL: dense
+  int transpose_out;
+  int64_t ldt;        // jagged transposed width
+  uint8_t* q;
+  float* inv;
+  int cap_rows;       // rows of the strip resident per CTA
+  int* status;
+};
+
+template <bool FNUZ>
+__global__ void __launch_bounds__(256) k_colwise(ColwiseArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint8_t* buf = smem;                                        // cap_rows x CW_PITCH
+  uint8_t* tbuf = smem + (size_t)a.cap_rows * CW_PITCH;       // 32 x CW_TPITCH
+  __shared__ uint32_t red[256][4];
+  __shared__ float s_col[CW_COLS];
+  __shared__ uint32_t amax_part[CW_COLS];
+  __shared__ int64_t grp[3];                                  // start, end, padded start
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t nstrips = (a.C + CW_COLS - 1) / CW_COLS;
+  const int64_t unit = blockIdx.x / CL;
+  const int e = (int)(unit / nstrips);
+  const int64_t c0 = (unit % nstrips) * CW_COLS;
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    int64_t g0 = 0, g1 = 0, P = 0;
+    bool bad = false;
+    if (a.offs == nullptr) {
+      g0 = (int64_t)e * a.R;
+      g1 = g0 + a.R;
+    } else {
+      // validate every group up to e (0 <= start <= end <= R) while summing the
+      // 32-padded sizes of the earlier ones
+      int64_t prev = 0;
+      for (int j = 0; j <= e; ++j) {
+        const int64_t end = a.offs[j];
+        if (end < prev || end > a.R) {
+          bad = true;
+          break;
+        }
+        if (j < e) P += (end - prev + 31) / 32 * 32;
+        g0 = prev;
+        g1 = end;
+        prev = end;
+      }
+      if (e == a.E - 1 && g1 != a.R) bad = true;
+    }
+    if (bad) {
+      set_status(a.status, FP8MOE_ERR_DEVICE_OFFSETS);
+      g0 = g1 = P = -1;
+    }
+    grp[0] = g0;
+    grp[1] = g1;
+    grp[2] = P;
+  }
+  __syncthreads();
+  if (grp[2] < 0) return;  // invalid offsets: nothing is written (uniform across the cluster)
+  const int64_t g0 = grp[0], g1 = grp[1], P = grp[2];
+  const int64_t gsz = g1 - g0;
+  int64_t per = (gsz + CL - 1) / CL;
+  per = (per + 15) / 16 * 16;
+  const int64_t rb = g0 + rank * per < g1 ? g0 + rank * per : g1;
+  const int64_t re = rb + per < g1 ? rb + per : g1;
+  const int64_t nrows = re - rb;
+  const int cap = a.cap_rows;
+  const int nwin = nrows == 0 ? 1 : (int)((nrows + cap - 1) / cap);
+
+  // ---- phase 1: column absmax over this CTA's rows, window by window ----
+  // load mapping: 4 threads per row (16 B each), 64 rows per pass
+  const int lsub = tid & 3, lrow = tid >> 2;
+  const bool col_ok = c0 + lsub * 8 < a.C;
+  uint4 mx = make_uint4(0, 0, 0, 0);
+  auto load_window = [&](int w) {
+    const int64_t wr0 = rb + (int64_t)w * cap;
+    const int64_t wn = (re - wr0) < cap ? (re - wr0) : cap;
+    for (int64_t r = lrow; r < wn; r += 64) {
+      uint8_t* d = buf + r * CW_PITCH + lsub * 16;
+      if (col_ok) {
+        cp_async16(d, a.x + (wr0 + r) * a.C + c0 + lsub * 8);
+      } else {
+        *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    return wn;
+  };
+  int64_t wn = 0;
+  for (int w = 0; w < nwin; ++w) {
+    if (w > 0) __syncthreads();
+    wn = load_window(w);
+    for (int64_t r = lrow; r < wn; r += 64) {
+      const uint4 v = *reinterpret_cast<const uint4*>(buf + r * CW_PITCH + lsub * 16);
+      mx.x = __vmaxu2(mx.x, v.x & 0x7FFF7FFFu);
+      mx.y = __vmaxu2(mx.y, v.y & 0x7FFF7FFFu);
+      mx.z = __vmaxu2(mx.z, v.z & 0x7FFF7FFFu);
+      mx.w = __vmaxu2(mx.w, v.w & 0x7FFF7FFFu);
+    }
+  }
+  red[tid][0] = mx.x;
+  red[tid][1] = mx.y;
+  red[tid][2] = mx.z;
+  red[tid][3] = mx.w;
+  __syncthreads();
+  if (tid < CW_COLS) {
+    // column tid lives in thread-sub tid/8, halfword tid%8
+    const int sub = tid >> 3, hw = tid & 7;
+    uint32_t m = 0;
+    for (int k = 0; k < 64; ++k) {
+      const uint32_t w2 = red[k * 4 + sub][hw >> 1];
+      m = max(m, (hw & 1) ? (w2 >> 16) : (w2 & 0xFFFFu));
+    }
+    amax_part[tid] = m;
+  }
+  if (CL > 1) {
+    cluster.sync();
+    if (tid < CW_COLS) {
+      uint32_t m = 0;
+      for (int k = 0; k < CL; ++k) m = max(m, *cluster.map_shared_rank(&amax_part[tid], k));
+      red[tid][0] = m;
+    }
+    cluster.sync();
+    if (tid < CW_COLS) amax_part[tid] = red[tid][0];
+  }
+  __syncthreads();
+  if (tid < CW_COLS) {
+    float s, inv;
+    rowwise_scale<FNUZ>(bf16bits_to_float(amax_part[tid]), s, inv);
+    s_col[tid] = s;
+    if (rank == 0 && c0 + tid < a.C) a.inv[(int64_t)e * a.C + c0 + tid] = inv;
+  }
+  __syncthreads();
+
+  // ---- phase 2: cast and store, last window first (it is still resident) ----
+  const int qsub = tid >> 6, qrow = tid & 63;      // quantize mapping: warp = 32 rows, fixed sub
+  const bool qcol_ok = c0 + qsub * 8 < a.C;
+  float sv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sv[i] = s_col[(qsub * 8 + i) & 31];
+  for (int w = nwin - 1; w >= 0; --w) {
+    if (w != nwin - 1) {
+      __syncthreads();
+      wn = load_window(w);
+    }
+    const int64_t wr0 = rb + (int64_t)w * cap;
+    if (!a.transpose_out) {
+      for (int64_t r = qrow; r < wn; r += 64) {
+        if (!qcol_ok) continue;
+        const uint4 v = *reinterpret_cast<const uint4*>(buf + r * CW_PITCH + qsub * 16);
+        uint2 o;
+        o.x = enc4<FNUZ>(__fmul_rn(bf16_lo(v.x), sv[0]), __fmul_rn(bf16_hi(v.x), sv[1]),
+                         __fmul_rn(bf16_lo(v.y), sv[2]), __fmul_rn(bf16_hi(v.y), sv[3]));
+        o.y = enc4<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
+                         __fmul_rn(bf16_lo(v.w), sv[6]), __fmul_rn(bf16_hi(v.w), sv[7]));
+        *reinterpret_cast<uint2*>(a.q + (wr0 + r) * a.C + c0 + qsub * 8) = o;
+      }
+      continue;
+    }
+    // transposed: chunks of CW_TCHUNK rows through the byte-transposed tbuf
+    for (int64_t t0 = 0; t0 < wn; t0 += CW_TCHUNK) {
+      const int64_t tn = (wn - t0) < CW_TCHUNK ? (wn - t0) : CW_TCHUNK;
+      __syncthreads();
+      for (int64_t r = qrow; r < tn; r += 64) {
+        const uint4 v = *reinterpret_cast<const uint4*>(buf + (t0 + r) * CW_PITCH + qsub * 16);
+        const uint32_t o0 = enc4<FNUZ>(__fmul_rn(bf16_lo(v.x), sv[0]), __fmul_rn(bf16_hi(v.x), sv[1]),
+                                       __fmul_rn(bf16_lo(v.y), sv[2]), __fmul_rn(bf16_hi(v.y), sv[3]));
+        const uint32_t o1 = enc4<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
+                                       __fmul_rn(bf16_lo(v.w), sv[6]), __fmul_rn(bf16_hi(v.w), sv[7]));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tbuf[(qsub * 8 + i) * CW_TPITCH + r] = (uint8_t)(o0 >> (8 * i));
+          tbuf[(qsub * 8 + 4 + i) * CW_TPITCH + r] = (uint8_t)(o1 >> (8 * i));
+        }
+      }
+      __syncthreads();
+      // write 32 output rows of tn bytes; tn is a multiple of 16 except at the
+      // end of a group, where the tail is written bytewise
+      const int64_t row_begin = wr0 + t0 - g0;  // offset inside the group
+      const int nv = (int)(tn / 16);
+      for (int k = tid; k < CW_COLS * nv; k += 256) {
+        const int cc = k / nv, j = k % nv;
+        if (c0 + cc >= a.C) continue;
+        uint8_t* dst = a.offs == nullptr ? a.q + ((int64_t)e * a.C + c0 + cc) * a.R + row_begin
+                                         : a.q + (c0 + cc) * a.ldt + P + row_begin;
+        reinterpret_cast<uint4*>(dst)[j] = *reinterpret_cast<const uint4*>(tbuf + cc * CW_TPITCH + j * 16);
+      }
+      const int tail = (int)(tn - nv * 16);
+      for (int k = tid; k < CW_COLS * tail; k += 256) {
+        const int cc = k / tail, j = nv * 16 + k % tail;
+        if (c0 + cc >= a.C) continue;
+        uint8_t* dst = a.offs == nullptr ? a.q + ((int64_t)e * a.C + c0 + cc) * a.R + row_begin
+                                         : a.q + (c0 + cc) * a.ldt + P + row_begin;
+        dst[j] = tbuf[cc * CW_TPITCH + j];
+      }
+    }
+  }
+  // jagged transposed: zero the group's padding columns (and the tail after
+  // the last group)
+  if (a.transpose_out && a.offs != nullptr && rank == CL - 1) {
+    const int64_t pad_end = (e == a.E - 1) ? a.ldt : P + (gsz + 31) / 32 * 32;
+    const int64_t pad0 = P + gsz;
+    const int64_t npad = pad_end - pad0;
+    for (int64_t k = tid; k < CW_COLS * npad; k += 256) {
+      const int cc = (int)(k / npad);
+      if (c0 + cc < a.C) a.q[(c0 + cc) * a.ldt + pad0 + k % npad] = 0;
+    }
+  }
+  if (CL > 1) cluster.sync();
+}
+
+cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                           int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
+                           int max_smem, cudaStream_t st) {
+  ColwiseArgs a;
+  a.x = (const uint16_t*)x;
+  a.C = C;
+  a.R = R;
+  a.E = (int)E;
+  a.offs = offs;
+  a.transpose_out = transpose_out;
+  a.ldt = ldt;
+  a.q = (uint8_t*)q;
+  a.inv = inv;
+  a.status = status;
+  const int64_t nstrips = (C + CW_COLS - 1) / CW_COLS;
+  if (E == 0 || nstrips == 0) return cudaSuccess;
+  const size_t fixed = sizeof(uint32_t) * 256 * 4 + 1024;  // static shared memory + slack
+  const size_t tbytes = (size_t)CW_COLS * CW_TPITCH;
+  int64_t cap = (int64_t)((max_smem - fixed - tbytes) / CW_PITCH) / 64 * 64;
+  int CL = 1;
+  if (offs == nullptr) {
+    // dense: pick the smallest cluster that keeps every row resident
+    while (CL < 8 && (R + CL - 1) / CL > cap) CL *= 2;
+    const int64_t per = ((R + CL - 1) / CL + 15) / 16 * 16;
+    if (per < cap) cap = (per + 63) / 64 * 64;
+  } else {
+    // jagged: the average group's strip, capped; bigger groups re-read the overflow
+    const int64_t avg = (R / (E > 0 ? E : 1) + 63) / 64 * 64;
+    const int64_t want = avg < 1024 ? 1024 : avg;
+    if (want < cap) cap = want;
+  }
+  if (cap < 64) cap = 64;
+  a.cap_rows = (int)cap;
+  const size_t smem = (size_t)cap * CW_PITCH + tbytes;
+  auto kern = kind == FP8MOE_E4M3FNUZ ? k_colwise<true> : k_colwise<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(E * nstrips * CL));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace fp8moe

@@ -1,0 +1,71 @@
+"""The C-ABI library loads and exports every symbol its header declares; host-side
+argument checks return their status before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp8_moe_quantization_gb300 import build as B
+    B.build()
+    import mxfp8_moe_quantization_gb300 as F
+    return F.lib()
+
+
+def _declared():
+    hdr = open(os.path.join(ROOT, "include", "fp8moe.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8moe_[a-z0-9_]+)\s*\(", hdr)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    import mxfp8_moe_quantization_gb300 as F
+    assert set(F.SYMBOLS) == set(names)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.fp8moe_status_string(code)
+    assert lib.fp8moe_version() >> 16 == 1
+
+
+def test_sizes(lib):
+    assert lib.fp8moe_jagged_t_cols(100, 4) == 224
+    assert lib.fp8moe_jagged_t_cols(49152, 64) == (49152 + 31 * 64 + 15) // 16 * 16
+    from oracle import swizzle as S, quant as Q
+    for (B, R, Cs, E, ax) in [(1, 1024, 8, 4, 0), (1, 512, 32, 4, 1), (16, 8192, 160, 0, -1),
+                              (1, 1, 1, 0, -1), (1, 0, 0, 0, -1)]:
+        rp, cp = S.swizzled_shape(R, Cs, E, ax)
+        assert lib.fp8moe_swizzled_scales_bytes(B, R, Cs, E, ax) == B * rp * cp
+    assert Q.jagged_t_cols(100, 4) == lib.fp8moe_jagged_t_cols(100, 4)
+
+
+def test_host_errors_before_launch(lib):
+    """Invalid arguments are rejected on the host (no CUDA call is made)."""
+    p = ctypes.c_void_p(1 << 20)     # aligned, never dereferenced
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    INVALID, ALIGN, UNSUP = 1, 2, 3
+    assert lib.fp8moe_quantize_rowwise(None, 4, 32, 32, 0, p, p, None) == INVALID
+    assert lib.fp8moe_quantize_rowwise(p, 4, 24, 24, 0, p, p, None) == ALIGN       # C % 16
+    assert lib.fp8moe_quantize_rowwise(mis, 4, 32, 32, 0, p, p, None) == ALIGN
+    assert lib.fp8moe_quantize_rowwise(p, 4, 32, 32, 7, p, p, None) == INVALID     # bad kind
+    assert lib.fp8moe_quantize_rowwise(p, 0, 32, 32, 0, p, p, None) == 0           # empty: no-op
+    assert lib.fp8moe_mxfp8_quantize_dim0(p, 1, 4, 48, p, p, None) == ALIGN         # C % 32
+    assert lib.fp8moe_mxfp8_quantize_dim1(p, 1, 48, 64, p, p, None) == ALIGN        # R % 32
+    assert lib.fp8moe_mxfp8_quantize_dim0(p, 1, 0, 64, p, p, None) == 0
+    assert lib.fp8moe_quantize_colwise_3d(p, 2, 24, 32, None, 1, 0, p, p, None) == ALIGN  # R % 16
+    assert lib.fp8moe_swizzle_scales_128x4(p, 2, 128, 4, p, 4, 0, p, None) == INVALID    # B > 1 grouped
+    assert lib.fp8moe_scaled_grouped_mm_fwd(1, p, p, p, p, p, 4, 64, 64, 48, p, None) == ALIGN  # K % 32
+    assert lib.fp8moe_scaled_grouped_mm_fwd(5, p, p, p, p, p, 4, 64, 64, 64, p, None) == INVALID
+    assert lib.fp8moe_scaled_grouped_mm_fwd(1, p, p, p, p, None, 4, 64, 64, 64, p, None) == INVALID
+    assert lib.fp8moe_scaled_grouped_mm_wgrad(1, p, p, p, p, p, 4, 48, 64, 64, p, None) == ALIGN  # M % 32
+    assert lib.fp8moe_get_device_status(None, None) == INVALID

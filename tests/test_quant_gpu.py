@@ -1,0 +1,254 @@
+"""GPU parity of the quantization and swizzle kernels against the CPU oracle.
+
+Codes and scales must match bit for bit.  Calls go through the C ABI (via the
+thin binding).  Inputs come from the seeded generators in ``workloads`` or are
+built here from e4m3 tie points.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import formats as OF, quant as OQ, swizzle as OS
+
+pytestmark = pytest.mark.gpu
+
+KINDS = [(0, OF.FN), (1, OF.FNUZ)]
+
+
+@pytest.fixture(scope="module")
+def F():
+    from mxfp8_moe_quantization_gb300 import build as B
+    B.build()
+    import mxfp8_moe_quantization_gb300 as m
+    torch.cuda.init()
+    return m
+
+
+DEV = "cuda"
+
+
+def _bf16(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * scale).to(torch.bfloat16)
+
+
+def _np(t):
+    return t.float().cpu().numpy()
+
+
+def _tie_rows(R, C, seed, kind=OF.FN):
+    """Rows whose scale is a power of two and whose elements sit on e4m3
+    rounding midpoints, plus -0 and zeros."""
+    rng = np.random.default_rng(seed)
+    tab = OF.decode_table(kind)
+    fin = np.sort(tab[np.isfinite(tab) & (tab >= 0)])
+    mids = (fin[:-1] + fin[1:]) / 2
+    cand = np.concatenate([fin, mids, [0.0]])
+    vmax = OF.FP8_MAX[kind]
+    x = np.empty((R, C))
+    for r in range(R):
+        j = int(rng.integers(-20, 20))
+        row = rng.choice(cand, size=C) * rng.choice([-1.0, 1.0], size=C)
+        row[int(rng.integers(0, C))] = vmax * (1 if r % 2 else -1)
+        x[r] = row * 2.0 ** j
+    x[0, 1] = -0.0
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    assert np.array_equal(t.float().numpy(), x.astype(np.float32)), "tie rows must be bf16-exact"
+    return t
+
+
+# ----------------------------------------------------------------------------
+# rowwise
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind,okind", KINDS)
+@pytest.mark.parametrize("R,C", [(1024, 256), (1024, 512), (37, 16), (5, 4096), (3, 14336), (2, 32768),
+                                 (129, 1408), (64, 2048)])
+def test_rowwise_parity(F, kind, okind, R, C):
+    x = _bf16((R, C), R * 7 + C, 3.0)
+    x[min(2, R - 1)] = 0.0
+    q, inv = F.fp8moe_quantize_rowwise(x.to(DEV), kind)
+    rq, rinv = OQ.quantize_rowwise(_np(x), okind)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+
+
+@pytest.mark.parametrize("kind,okind", KINDS)
+def test_rowwise_tie_points_and_stride(F, kind, okind):
+    x = _tie_rows(64, 256, 5, okind)
+    big = torch.zeros(64, 320, dtype=torch.bfloat16)
+    big[:, :256] = x
+    xv = big.to(DEV)[:, :256]                     # row stride 320 != C
+    q, inv = F.fp8moe_quantize_rowwise(xv, kind)
+    rq, rinv = OQ.quantize_rowwise(_np(x), okind)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+
+
+def test_rowwise_tiny_workload(F):
+    wl = W.get_workload("tiny")
+    for which in ["A", "dY"]:
+        x = W.make_activations(wl, which)
+        for kind, okind in KINDS:
+            q, inv = F.fp8moe_quantize_rowwise(x.to(DEV), kind)
+            rq, rinv = OQ.quantize_rowwise(_np(x), okind)
+            assert np.array_equal(q.cpu().numpy(), rq) and np.array_equal(inv.cpu().numpy(), rinv)
+
+
+# ----------------------------------------------------------------------------
+# colwise (dense 3D and jagged)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("kind,okind", KINDS)
+@pytest.mark.parametrize("E,R,C", [(4, 256, 512), (2, 48, 32), (3, 64, 48), (1, 4096, 64),
+                                   (1, 14336, 32), (1, 24576, 16)])
+@pytest.mark.parametrize("trans", [True, False])
+def test_colwise_dense_parity(F, kind, okind, E, R, C, trans):
+    x = _bf16((E, R, C), E * 1000 + R + C, 0.02)
+    x[0, :, 1] = 0.0
+    q, inv = F.fp8moe_quantize_colwise_3d(x.to(DEV), None, trans, kind)
+    rq, rinv = OQ.quantize_colwise_3d(_np(x), okind, transpose_out=trans)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+@pytest.mark.parametrize("kind,okind", KINDS)
+@pytest.mark.parametrize("sizes", [[96, 0, 0, 928], [30, 0, 47, 23], [4000, 0, 1000], [1, 2, 3, 500, 7],
+                                   [0, 0, 64]])
+@pytest.mark.parametrize("trans", [True, False])
+def test_colwise_jagged_parity(F, kind, okind, sizes, trans):
+    M = sum(sizes)
+    C = 48
+    x = _bf16((M, C), M + len(sizes), 1.0)
+    offs = W.offsets_from_sizes(sizes)
+    ot = torch.from_numpy(offs).to(DEV)
+    q, inv = F.fp8moe_quantize_colwise_3d(x.to(DEV), ot, trans, kind)
+    rq, rinv = OQ.quantize_colwise_jagged(_np(x), offs, okind, transpose_out=trans)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert F.fp8moe_get_device_status() == 0
+
+
+def test_colwise_jagged_tiny_workload(F):
+    wl = W.get_workload("tiny")
+    offs = wl.offs()
+    x = W.make_activations(wl, "A")
+    q, inv = F.fp8moe_quantize_colwise_3d(x.to(DEV), torch.from_numpy(offs).to(DEV), True, 0)
+    rq, rinv = OQ.quantize_colwise_jagged(_np(x), offs, OF.FN, transpose_out=True)
+    assert np.array_equal(q.cpu().numpy(), rq) and np.array_equal(inv.cpu().numpy(), rinv)
+
+
+def test_colwise_bad_offsets_set_status(F):
+    x = torch.zeros(64, 32, dtype=torch.bfloat16, device=DEV)
+    for bad in [[40, 30, 64], [10, 20, 60], [10, 20, 70]]:
+        F.fp8moe_quantize_colwise_3d(x, torch.tensor(bad, dtype=torch.int32, device=DEV), True, 0)
+        assert F.fp8moe_get_device_status() == 5
+    assert F.fp8moe_get_device_status() == 0
+
+
+# ----------------------------------------------------------------------------
+# MXFP8
+# ----------------------------------------------------------------------------
+
+def _mx_tie_blocks(rows, C, seed):
+    rng = np.random.default_rng(seed)
+    tab = OF.decode_table(OF.FN)
+    fin = np.sort(tab[np.isfinite(tab) & (tab >= 0)])
+    mids = (fin[:-1] + fin[1:]) / 2
+    cand = np.concatenate([fin, mids, [464.0, 480.0, 500.0, 0.0]])
+    x = rng.choice(cand, size=(rows, C)) * rng.choice([-1.0, 1.0], size=(rows, C))
+    blocks = x.reshape(rows, C // 32, 32)
+    j = rng.integers(-30, 30, size=(rows, C // 32))
+    blocks[..., 0] = 256.0
+    x = (blocks * np.ldexp(1.0, j)[..., None]).reshape(rows, C)
+    x[0, :32] = 0.0
+    x[1, :32] = -0.0
+    x[2, 32:64] = np.ldexp(1.0, -133)       # bf16 subnormal block
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    assert np.array_equal(t.float().numpy(), x.astype(np.float32))
+    return t
+
+
+@pytest.mark.parametrize("shape", [(1024, 256), (4, 512, 256), (3, 32), (1, 5120), (333, 96)])
+def test_mx_dim0_parity(F, shape):
+    x = _bf16(shape, sum(shape), 2.0)
+    q, s = F.fp8moe_mxfp8_quantize_dim0(x.to(DEV))
+    rq, rs = OQ.mxfp8_quantize_dim0(_np(x))
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_mx_dim0_tie_points(F):
+    x = _mx_tie_blocks(64, 256, 3)
+    q, s = F.fp8moe_mxfp8_quantize_dim0(x.to(DEV))
+    rq, rs = OQ.mxfp8_quantize_dim0(_np(x))
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
+@pytest.mark.parametrize("shape", [(1024, 256), (4, 512, 256), (32, 16), (96, 80), (160, 128), (1, 256, 5120)])
+def test_mx_dim1_parity(F, shape):
+    x = _bf16(shape, sum(shape) + 1, 2.0)
+    qt, st = F.fp8moe_mxfp8_quantize_dim1(x.to(DEV))
+    rqt, rst = OQ.mxfp8_quantize_dim1(_np(x))
+    assert np.array_equal(st.cpu().numpy(), rst)
+    assert np.array_equal(qt.cpu().numpy(), rqt)
+
+
+def test_mx_dim1_tie_points(F):
+    x = _mx_tie_blocks(256, 64, 4).T.contiguous()    # blocks of 32 along dim 0 after transpose
+    qt, st = F.fp8moe_mxfp8_quantize_dim1(x.to(DEV))
+    rqt, rst = OQ.mxfp8_quantize_dim1(_np(x))
+    assert np.array_equal(st.cpu().numpy(), rst)
+    assert np.array_equal(qt.cpu().numpy(), rqt)
+
+
+def test_mx_tiny_workload(F):
+    wl = W.get_workload("tiny")
+    for x in [W.make_activations(wl, "A"), W.make_activations(wl, "dY"), W.make_weights(wl, "W1")]:
+        q, s = F.fp8moe_mxfp8_quantize_dim0(x.to(DEV))
+        rq, rs = OQ.mxfp8_quantize_dim0(_np(x))
+        assert np.array_equal(q.cpu().numpy(), rq) and np.array_equal(s.cpu().numpy(), rs)
+        qt, st = F.fp8moe_mxfp8_quantize_dim1(x.to(DEV))
+        rqt, rst = OQ.mxfp8_quantize_dim1(_np(x))
+        assert np.array_equal(qt.cpu().numpy(), rqt) and np.array_equal(st.cpu().numpy(), rst)
+
+
+# ----------------------------------------------------------------------------
+# swizzle
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,R,Cs", [(1, 1024, 8), (4, 512, 8), (1, 1, 1), (2, 200, 7), (1, 300, 160)])
+def test_swizzle_plain(F, B, R, Cs):
+    s = torch.randint(1, 255, (B, R, Cs), dtype=torch.uint8, generator=torch.Generator().manual_seed(R))
+    out = F.fp8moe_swizzle_scales_128x4(s.to(DEV))
+    ref = OS.swizzle(s.numpy() if B > 1 else s[0].numpy())
+    assert np.array_equal(out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("sizes", [[96, 0, 0, 928], [100, 0, 160, 40], [0, 0, 5], [300]])
+def test_swizzle_group_rows(F, sizes):
+    R = sum(sizes)
+    s = torch.randint(1, 255, (R, 6), dtype=torch.uint8, generator=torch.Generator().manual_seed(R))
+    offs = W.offsets_from_sizes(sizes)
+    out = F.fp8moe_swizzle_scales_128x4(s.to(DEV), torch.from_numpy(offs).to(DEV), F.GROUP_ROWS)
+    assert np.array_equal(out.cpu().numpy(), OS.swizzle(s.numpy(), offs, OS.GROUP_ROWS))
+
+
+@pytest.mark.parametrize("sizes", [[96, 0, 0, 928], [64, 0, 256], [32], [0, 320]])
+def test_swizzle_group_cols(F, sizes):
+    M = sum(sizes)
+    s = torch.randint(1, 255, (130, M // 32), dtype=torch.uint8, generator=torch.Generator().manual_seed(M))
+    offs = W.offsets_from_sizes(sizes)
+    out = F.fp8moe_swizzle_scales_128x4(s.to(DEV), torch.from_numpy(offs).to(DEV), F.GROUP_COLS)
+    assert np.array_equal(out.cpu().numpy(), OS.swizzle(s.numpy(), offs, OS.GROUP_COLS))
+
+
+def test_swizzle_bad_offsets_set_status(F):
+    s = torch.ones(64, 4, dtype=torch.uint8, device=DEV)
+    F.fp8moe_swizzle_scales_128x4(s, torch.tensor([40, 30, 64], dtype=torch.int32, device=DEV), F.GROUP_ROWS)
+    assert F.fp8moe_get_device_status() == 5
+    F.fp8moe_swizzle_scales_128x4(s, torch.tensor([40, 64], dtype=torch.int32, device=DEV), F.GROUP_COLS)
+    assert F.fp8moe_get_device_status() == 5     # 40 is not a multiple of 32
+    assert F.fp8moe_get_device_status() == 0
