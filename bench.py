@@ -1,0 +1,390 @@
+"""Benchmark: one MXFP8 MoE training step of the Llama4-Scout-shaped layer.
+
+A step is one pass of the whole hot path over one batch of synthetic routed
+tokens, for both expert weights of the layer (W1 [16, 8192, 5120] and
+W2 [16, 5120, 8192]):
+
+    MXFP8 quantize A (dim0) + swizzle, W (dim0) + swizzle  -> grouped GEMM fwd
+    MXFP8 quantize dY (dim0) + swizzle, W (dim1) + swizzle -> grouped GEMM dgrad
+    MXFP8 quantize dY, A (dim1) + column-grouped swizzle   -> grouped GEMM wgrad
+
+Prints one JSON line.  ``value`` is the effective MXFP8 grouped-GEMM
+throughput of the step (GEMM FLOPs over the step time, quantization
+included); the line also carries the GEMM-only TFLOP/s, the quantization
+GB/s, the dominant kernel's roofline, an end-to-end number through host
+buffers, and the CPU oracle timed on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "scout"
+METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the step
+# ----------------------------------------------------------------------------
+class ScoutStep:
+    """Buffers and launches of one step; every launch goes through the C ABI."""
+
+    def __init__(self, F, wl, device, seed_offset=0):
+        import torch
+        import workloads as W
+        self.F, self.wl, self.dev = F, wl, device
+        self.offs_np = wl.offs()
+        self.offs = torch.from_numpy(self.offs_np).to(device)
+        self.M = wl.M
+        self.E = wl.E
+        self.real_tokens = int(wl.group_plan()[0].sum())
+        self.layers = []
+        for wname, aname, dname in [("W1", "A", "dY"), ("W2", "A2", "dY2")]:
+            w = W.make_weights(wl, wname, device=device)
+            a = W.make_activations(wl, aname, device=device)
+            dy = W.make_activations(wl, dname, device=device)
+            self.layers.append(self._alloc(w, a, dy))
+        self.launches_per_step = 15 * len(self.layers)
+
+    def _alloc(self, w, a, dy):
+        import torch
+        F, dev, M, E = self.F, self.dev, self.M, self.E
+        _, N, K = w.shape
+        u8 = torch.uint8
+        L = dict(w=w, a=a, dy=dy, N=N, K=K)
+        L["qa"] = torch.empty(M, K, dtype=u8, device=dev)
+        L["sa"] = torch.empty(M, K // 32, dtype=u8, device=dev)
+        L["sa_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(1, M, K // 32, E, F.GROUP_ROWS), dtype=u8, device=dev)
+        L["qw"] = torch.empty(E, N, K, dtype=u8, device=dev)
+        L["sw"] = torch.empty(E, N, K // 32, dtype=u8, device=dev)
+        L["sw_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(E, N, K // 32), dtype=u8, device=dev)
+        L["out"] = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        L["qdy"] = torch.empty(M, N, dtype=u8, device=dev)
+        L["sdy"] = torch.empty(M, N // 32, dtype=u8, device=dev)
+        L["sdy_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(1, M, N // 32, E, F.GROUP_ROWS), dtype=u8, device=dev)
+        L["qwt"] = torch.empty(E, K, N, dtype=u8, device=dev)
+        L["swt"] = torch.empty(E, K, N // 32, dtype=u8, device=dev)
+        L["swt_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(E, K, N // 32), dtype=u8, device=dev)
+        L["da"] = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        L["qdyt"] = torch.empty(N, M, dtype=u8, device=dev)
+        L["sdyt"] = torch.empty(N, M // 32, dtype=u8, device=dev)
+        L["sdyt_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(1, N, M // 32, E, F.GROUP_COLS), dtype=u8, device=dev)
+        L["qat"] = torch.empty(K, M, dtype=u8, device=dev)
+        L["sat"] = torch.empty(K, M // 32, dtype=u8, device=dev)
+        L["sat_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(1, K, M // 32, E, F.GROUP_COLS), dtype=u8, device=dev)
+        L["dw"] = torch.empty(E, N, K, dtype=torch.bfloat16, device=dev)
+        return L
+
+    # accounting -------------------------------------------------------
+    def gemm_flops(self):
+        """Per step: 3 GEMMs per weight, 2*T*N*K each over the real routed tokens."""
+        return sum(3 * 2.0 * self.real_tokens * L["N"] * L["K"] for L in self.layers)
+
+    def quant_bytes(self):
+        """Algorithmic HBM bytes of the quantization + swizzle launches per step:
+        2 B read + 1 B written per element, + 1 scale byte per 32 (written, then
+        read and written again by the swizzle)."""
+        tot = 0.0
+        for L in self.layers:
+            M, N, K, E = self.M, L["N"], L["K"], self.E
+            elems = 2 * M * K + 2 * E * N * K + 2 * M * N   # A, W, dY each dim0 + dim1
+            tot += elems * 3 + elems / 32 * 3
+        return tot
+
+    # launches -------------------------------------------------------
+    def run(self, rec=None):
+        """One step.  ``rec(kind, fn)`` wraps each launch for timing."""
+        F, offs = self.F, self.offs
+        rec = rec or (lambda kind, fn: fn())
+        for L in self.layers:
+            rec("quant", lambda: F.fp8moe_mxfp8_quantize_dim0(L["a"], L["qa"], L["sa"]))
+            rec("quant", lambda: F.fp8moe_swizzle_scales_128x4(L["sa"], offs, F.GROUP_ROWS, out=L["sa_sw"]))
+            rec("quant", lambda: F.fp8moe_mxfp8_quantize_dim0(L["w"], L["qw"], L["sw"]))
+            rec("quant", lambda: F.fp8moe_swizzle_scales_128x4(L["sw"], out=L["sw_sw"]))
+            rec("gemm", lambda: F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, L["qa"], L["sa_sw"], L["qw"], L["sw_sw"],
+                                                               offs, out=L["out"]))
+            rec("quant", lambda: F.fp8moe_mxfp8_quantize_dim0(L["dy"], L["qdy"], L["sdy"]))
+            rec("quant", lambda: F.fp8moe_swizzle_scales_128x4(L["sdy"], offs, F.GROUP_ROWS, out=L["sdy_sw"]))
+            rec("quant", lambda: F.fp8moe_mxfp8_quantize_dim1(L["w"], L["qwt"], L["swt"]))
+            rec("quant", lambda: F.fp8moe_swizzle_scales_128x4(L["swt"], out=L["swt_sw"]))
+            rec("gemm", lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.MXFP8, L["qdy"], L["sdy_sw"], L["qwt"],
+                                                                 L["swt_sw"], offs, out=L["da"]))
+            rec("quant", lambda: F.fp8moe_mxfp8_quantize_dim1(L["dy"], L["qdyt"], L["sdyt"]))
+            rec("quant", lambda: F.fp8moe_swizzle_scales_128x4(L["sdyt"], offs, F.GROUP_COLS, out=L["sdyt_sw"]))
+            rec("quant", lambda: F.fp8moe_mxfp8_quantize_dim1(L["a"], L["qat"], L["sat"]))
+            rec("quant", lambda: F.fp8moe_swizzle_scales_128x4(L["sat"], offs, F.GROUP_COLS, out=L["sat_sw"]))
+            rec("gemm", lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.MXFP8, L["qdyt"], L["sdyt_sw"], L["qat"],
+                                                                 L["sat_sw"], offs, self.M, out=L["dw"]))
+
+
+def run_e2e(F, step, steps, warmup):
+    """Same step through host buffers: pinned host inputs are copied in and the
+    step's results (out, dA, dW of both weights) copied back every step."""
+    import torch
+    host_in, host_out = [], []
+    for L in step.layers:
+        for k in ("a", "w", "dy"):
+            host_in.append((L[k], torch.empty(L[k].shape, dtype=L[k].dtype, pin_memory=True).copy_(L[k].cpu())))
+        for k in ("out", "da", "dw"):
+            host_out.append((L[k], torch.empty(L[k].shape, dtype=L[k].dtype, pin_memory=True)))
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
+    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
+
+    def one():
+        for d, h in host_in:
+            d.copy_(h, non_blocking=True)
+        step.run()
+        for d, h in host_out:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return dt, h2d, d2h
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# ----------------------------------------------------------------------------
+def cpu_baseline(wl, budget_s=20.0):
+    """Time the oracle's MXFP8 quantization and float64 grouped GEMM on a slice
+    of the workload and scale to one step's work."""
+    import numpy as np
+    from oracle import quant as OQ, grouped_mm as OG
+    rng = np.random.default_rng(0)
+    # quantization rate (elements / s) on a 2048 x 5120 slice
+    x = rng.standard_normal((2048, 5120)).astype(np.float32)
+    t0 = time.perf_counter()
+    OQ.mxfp8_quantize_dim0(x)
+    q_rate = x.size / (time.perf_counter() - t0)
+    # GEMM rate (flop / s) on one group of 256 rows against a 512 x 5120 slice
+    a = rng.standard_normal((256, 5120))
+    w = rng.standard_normal((1, 512, 5120))
+    t0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < max(1.0, budget_s / 4) and reps < 50:
+        OG.grouped_mm_fwd(a, w, np.array([256]))
+        reps += 1
+    g_rate = reps * 2.0 * 256 * 512 * 5120 / (time.perf_counter() - t0)
+    return q_rate, g_rate, "oracle mxfp8_quantize_dim0 on 2048x5120 and fp64 grouped_mm_fwd on 256x512x5120"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    import workloads as W
+    wl = W.get_workload(WORKLOAD)
+
+    if args.impl == "reference":
+        # the reference arm is the CPU oracle (the pages ship no runnable code)
+        if rank != 0:
+            return
+        q_rate, g_rate, sample = cpu_baseline(wl)
+        import numpy as np
+        step_flops = sum(3 * 2.0 * int(wl.group_plan()[0].sum()) * n * k
+                         for n, k in [(wl.N, wl.K), (wl.K, wl.N)])
+        M = wl.M
+        elems = sum(2 * M * k + 2 * wl.E * n * k + 2 * M * n for n, k in [(wl.N, wl.K), (wl.K, wl.N)])
+        t_step = elems / q_rate + step_flops / g_rate
+        val = step_flops / t_step / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: {wl.description}"},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    import torch
+    from mxfp8_moe_quantization_gb300 import build as B
+    B.build()
+    import mxfp8_moe_quantization_gb300 as F
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    step = ScoutStep(F, wl, dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    assert F.fp8moe_get_device_status() == 0
+
+    # timed region: events around every launch on the launching stream
+    ev = {"gemm": [], "quant": []}
+
+    def rec(kind, fn):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        ev[kind].append((s, e))
+
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else 0) as clk:
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step.run(rec)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    if pg:
+        t = torch.tensor([ms_total], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    gemm_ms = sum(s.elapsed_time(e) for s, e in ev["gemm"]) / args.steps
+    quant_ms = sum(s.elapsed_time(e) for s, e in ev["quant"]) / args.steps
+    n_gemm = len(ev["gemm"]) // args.steps
+    flops = step.gemm_flops()
+    qbytes = step.quant_bytes()
+    assert F.fp8moe_get_device_status() == 0
+
+    peaks, peak_kind = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]          # nominal fp8:bf16 dense ratio 4.5 / 2.25
+    gemm_launch_ms = gemm_ms / n_gemm
+    achieved = flops / n_gemm / (gemm_launch_ms * 1e-3) / 1e12
+    value = flops * world / (ms_step * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        dt, h2d, d2h = run_e2e(F, step, max(2, args.steps // 3), 1)
+        e2e = {"value": flops * world / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        q_rate, g_rate, sample = cpu_baseline(wl)
+        t_cpu = qbytes / 3.1 / q_rate + flops / g_rate
+        cpu = {"value": flops / t_cpu / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": sample, "ms_per_step_extrapolated": t_cpu * 1e3}
+
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3 x e4m3 (e8m0 scales) -> fp32 accum -> bf16", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: {wl.description}", "experts": wl.E, "tokens": wl.tokens,
+                       "routed_rows_padded": wl.M, "hidden": wl.K, "ffn": wl.N, "weights": 2,
+                       "l2": "inputs larger than L2 (each expert weight is 1.34 GB bf16)"},
+            "gemm_tflops": flops / (gemm_ms * 1e-3) / 1e12,
+            "gemm_frac_fp8_peak": flops / (gemm_ms * 1e-3) / 1e12 / fp8_peak,
+            "quant_gbs": qbytes / (quant_ms * 1e-3) / 1e9,
+            "quant_frac_hbm": qbytes / (quant_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "gemm_ms_per_step": gemm_ms, "quant_ms_per_step": quant_ms,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                         "frac": achieved / fp8_peak, "traffic": None,
+                         "kernel": "k_grouped_mm<MX=true>", "peak_source":
+                             f"{peak_kind}: 2 x bf16_tflops (nominal fp8/bf16 dense ratio)"},
+            "clocks": clk.summary(),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": step.launches_per_step * args.steps,
+        }))
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

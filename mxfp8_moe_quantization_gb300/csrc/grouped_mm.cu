@@ -1,6 +1,632 @@
+// Scaled grouped GEMM on tcgen05 tensor cores (sm_103a): forward, dgrad and
+// wgrad of an MoE expert layer in one launch each, with experts scheduled on
+// the device from the routing offsets.
+//
+// What it computes ("FP8 Training on AMD GPUs with TorchTitan and TorchAO",
+// aixai.ru section "MoE: почему DeepSeek-V3 ломал пайплайн": row scales for
+// activations, per-expert column scales for weights, an offsets tensor, one
+// launch; "Accelerating Llama4 Scout training with TorchAO MXFP8 MoE
+// primitives": MXFP8 operands with e8m0 scales in the 128x4 layout for
+// tcgen05, a 2D input times a 3D expert weight grouped by offsets, and a weight
+// gradient that contracts over the routed-token dimension).
+//
+// Design (GB300-first; the pages' Triton / Composable-Kernel kernels are for
+// other hardware):
+//  * persistent kernel, one 192-thread CTA per SM, tiles of 128 x 256 outputs;
+//  * warp 0: TMA producer (A and B tiles with 128-byte swizzle, MXFP8 scale
+//    tiles as 512-byte bulk copies -- the 128x4 layout makes each one
+//    contiguous); warp 1: TMEM allocator and single-thread MMA issuer; warps
+//    2-5: epilogue (TMEM -> registers -> bf16 -> global);
+//  * 4-stage shared-memory ring with mbarriers; every wait is bounded and a
+//    timeout sets the device status word instead of hanging;
+//  * accumulator in TMEM (128 lanes x 256 fp32 columns); MXFP8 scales copied
+//    into TMEM per stage with tcgen05.cp and consumed by the block-scaled MMA
+//    (kind::mxf8f6f4, one e8m0 scale per 32 elements of K); the rowwise recipe
+//    uses kind::f8f6f4 and applies row x column fp32 scales in the epilogue;
+//  * the epilogue drains the accumulator to registers and releases TMEM before
+//    its global stores, so the next tile's MMAs overlap the stores.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "gemm.h"
 #include "launch.h"
+
 namespace fp8moe {
-cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) { return cudaErrorNotSupported; }
+
+constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int NUM_THREADS = 192;
+constexpr int A_STAGE_BYTES = BM * BK;            // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK;            // 32 KB
+constexpr int SFA_STAGE_BYTES = 512;              // one 128x4 scale tile
+constexpr int SFB_STAGE_BYTES = 1024;             // two 128x4 scale tiles (256 rows)
+constexpr int MAX_GROUPS = 1024;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_SF_BASE = 256;            // scale columns start after the accumulator
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull; // 2 s
+
+struct SmemLayout {
+  static constexpr int a = 0;
+  static constexpr int b = a + STAGES * A_STAGE_BYTES;
+  static constexpr int sfa = b + STAGES * B_STAGE_BYTES;
+  static constexpr int sfb = sfa + STAGES * SFA_STAGE_BYTES;
+  static constexpr int bars = sfb + STAGES * SFB_STAGE_BYTES;   // 2*STAGES + 2 mbarriers
+  static constexpr int misc = bars + (2 * STAGES + 2) * 8;      // tmem addr, abort, counts
+  static constexpr int colscale = misc + 64;                    // 256 floats
+  static constexpr int tiles_prefix = colscale + BN * 4;        // MAX_GROUPS + 1 ints
+  static constexpr int blk_prefix = tiles_prefix + (MAX_GROUPS + 1) * 4;
+  static constexpr int total = blk_prefix + (MAX_GROUPS + 1) * 4;
+};
+constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+FP8MOE_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+FP8MOE_DEV uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
+
+FP8MOE_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+FP8MOE_DEV void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+FP8MOE_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+FP8MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when the limit ran out or another role aborted.
+FP8MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+  }
+}
+
+FP8MOE_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+FP8MOE_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+FP8MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+FP8MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+FP8MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+FP8MOE_DEV void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand tile, 128-byte swizzle,
+// 8-row groups 1024 bytes apart.
+FP8MOE_DEV uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;              // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
+}
+// Descriptor of one 128x4 scale tile (32 rows of 16 bytes, no swizzle) as the
+// source of tcgen05.cp 32x128b.
+FP8MOE_DEV uint64_t sdesc_sf(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 32;     // 8 rows x 16 bytes between row groups
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptors.  Block-scaled e4m3 x e4m3 with e8m0 scales:
+// b scale id [4,6), A/B format E4M3 (0), K-major A and B, N>>3 at [17,23),
+// scale type UE8M0 (bit 23), M>>4 at [24,29), a scale id [29,31).
+FP8MOE_DEV uint32_t idesc_mx(uint32_t sf_id) {
+  return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+}
+// Plain e4m3 x e4m3 with an fp32 accumulator (D format F32 = 1 at [4,6)).
+FP8MOE_DEV uint32_t idesc_f8() {
+  return (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+FP8MOE_DEV void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                       uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb));
+}
+FP8MOE_DEV void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
+}
+FP8MOE_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns -> 32 registers per thread.
+FP8MOE_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+FP8MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+FP8MOE_DEV uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------
+// kernel
+// ---------------------------------------------------------------------------
+struct KParams {
+  GemmArgs g;
+  int64_t cpb;        // 128x4 scale tiles per scale row block (A side and, fwd, B side)
+  int64_t b_rows_pad; // fwd/dgrad: padded rows (cols of C) of one expert's scale matrix
+  int n_tiles;        // tiles along the output columns
+  int m_tiles_w;      // wgrad: tiles along the output rows
+};
+
+// Per-tile geometry, recomputed identically by every role.
+struct Tile {
+  int e;          // expert
+  int64_t row0;   // first output row (fwd: absolute row of A; wgrad: row of dYt)
+  int64_t rows;   // valid rows in this tile
+  int64_t col0;   // first output column
+  int64_t x0;     // first contracting element
+  int64_t kvalid; // contracting elements
+  int nk;         // k stages
+  int64_t sfa_blk; // scale row block on the A side (swizzled units)
+  int64_t sf_kblk; // first scale column block (in 128x4 tiles) of the contraction
+};
+
+template <bool WGRAD>
+FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* blk_prefix, int t) {
+  const GemmArgs& g = p.g;
+  // last group whose tile prefix is <= t
+  int lo = 0, hi = g.E - 1, e = 0;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (tiles_prefix[mid] <= t) {
+      e = mid;
+      lo = mid + 1;
+    } else {
+      hi = mid - 1;
+    }
+  }
+  const int local = t - tiles_prefix[e];
+  const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
+  const int64_t ge = g.offs[e];
+  Tile tl;
+  tl.e = e;
+  if (!WGRAD) {
+    const int mt = (int)((ge - gs + BM - 1) / BM);
+    const int ni = local / mt, mi = local % mt;   // n-major: neighbours share the B tile
+    tl.row0 = gs + (int64_t)mi * BM;
+    tl.rows = (ge - tl.row0) < BM ? (ge - tl.row0) : BM;
+    tl.col0 = (int64_t)ni * BN;
+    tl.x0 = 0;
+    tl.kvalid = g.kk;
+    tl.sfa_blk = blk_prefix[e] + mi;
+    tl.sf_kblk = 0;
+  } else {
+    const int ni = local / p.m_tiles_w, mi = local % p.m_tiles_w;
+    tl.row0 = (int64_t)mi * BM;
+    tl.rows = (g.rows - tl.row0) < BM ? (g.rows - tl.row0) : BM;
+    tl.col0 = (int64_t)ni * BN;
+    // MXFP8: groups are multiples of 32 and used in place; rowwise: the
+    // 32-padded layout (blk_prefix holds the padded start)
+    tl.x0 = g.recipe == FP8MOE_MXFP8 ? gs : (int64_t)blk_prefix[e];
+    tl.kvalid = ge - gs;
+    tl.sfa_blk = mi;
+    tl.sf_kblk = g.recipe == FP8MOE_MXFP8 ? (int64_t)blk_prefix[e] : 0;
+  }
+  tl.nk = (int)((tl.kvalid + BK - 1) / BK);
+  return tl;
+}
+
+template <bool MX, bool WGRAD>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_grouped_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, KParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem + SmemLayout::a;
+  uint8_t* sB = smem + SmemLayout::b;
+  uint8_t* sSFA = smem + SmemLayout::sfa;
+  uint8_t* sSFB = smem + SmemLayout::sfb;
+  uint64_t* full = (uint64_t*)(smem + SmemLayout::bars);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tmem_full = empty + STAGES;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint32_t* tmem_base_holder = (uint32_t*)(smem + SmemLayout::misc);
+  volatile int* abort_flag = (volatile int*)(smem + SmemLayout::misc + 4);
+  int* total_tiles_s = (int*)(smem + SmemLayout::misc + 8);
+  float* colscale = (float*)(smem + SmemLayout::colscale);
+  int* tiles_prefix = (int*)(smem + SmemLayout::tiles_prefix);
+  int* blk_prefix = (int*)(smem + SmemLayout::blk_prefix);
+
+  const GemmArgs& g = p.g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- setup: barriers, TMEM, the device-side group schedule ----
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 4);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_base_holder)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    tc_fence_before();
+  }
+  // per-group tile counts and scale-block counts, then an exclusive scan
+  for (int e = threadIdx.x; e < g.E; e += NUM_THREADS) {
+    const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
+    const int64_t ge = g.offs[e];
+    const int64_t sz = ge - gs;
+    int nt, nb;
+    if (!WGRAD) {
+      nt = (int)((sz + BM - 1) / BM) * p.n_tiles;
+      nb = (int)((sz + BM - 1) / BM);
+    } else {
+      nt = p.m_tiles_w * p.n_tiles;
+      nb = MX ? (int)((sz + 127) / 128) : (int)((sz + 31) / 32 * 32);
+    }
+    tiles_prefix[e + 1] = sz < 0 ? 0 : nt;
+    blk_prefix[e + 1] = sz < 0 ? 0 : nb;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // validate the offsets and scan (one warp, 32 groups per step)
+    int bad = 0;
+    int carry_t = 0, carry_b = 0;
+    for (int base = 0; base < g.E; base += 32) {
+      const int e = base + lane;
+      int vt = 0, vb = 0;
+      if (e < g.E) {
+        const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
+        const int64_t ge = g.offs[e];
+        if (ge < gs || ge > g.M || (e == g.E - 1 && ge != g.M)) bad = 1;
+        if (MX && (ge % 32)) bad = 1;
+        vt = tiles_prefix[e + 1];
+        vb = blk_prefix[e + 1];
+      }
+      for (int o = 1; o < 32; o <<= 1) {
+        const int ut = __shfl_up_sync(0xffffffffu, vt, o);
+        const int ub = __shfl_up_sync(0xffffffffu, vb, o);
+        if (lane >= o) {
+          vt += ut;
+          vb += ub;
+        }
+      }
+      if (e < g.E) {
+        tiles_prefix[e + 1] = carry_t + vt;
+        blk_prefix[e + 1] = carry_b + vb;
+      }
+      carry_t += __shfl_sync(0xffffffffu, vt, 31);
+      carry_b += __shfl_sync(0xffffffffu, vb, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      tiles_prefix[0] = 0;
+      blk_prefix[0] = 0;
+      *total_tiles_s = bad ? 0 : carry_t;
+      if (bad && blockIdx.x == 0) set_status(g.status, FP8MOE_ERR_DEVICE_OFFSETS);
+    }
+  }
+  // exclusive prefix: tiles_prefix[e] = tiles of groups < e (shift by reading e)
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_holder;
+  const int total_tiles = *total_tiles_s;
+
+  if (warp == 0 && lane == 0) {
+    // ======================= TMA producer =======================
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+      for (int ks = 0; ks < tl.nk; ++ks) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+          set_status(g.status, FP8MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES;
+        const uint8_t* sfa_src = nullptr;
+        const uint8_t* sfb_src0 = nullptr;
+        const uint8_t* sfb_src1 = nullptr;
+        if (MX) {
+          const int64_t kb = tl.sf_kblk + ks;
+          sfa_src = (const uint8_t*)g.a_scale + (tl.sfa_blk * p.cpb + kb) * 512;
+          const int64_t nb0 = tl.col0 / 128;
+          const int64_t nbl = WGRAD ? (g.cols + 127) / 128 : p.b_rows_pad / 128;
+          const uint8_t* bsf = (const uint8_t*)g.b_scale + (WGRAD ? 0 : (int64_t)tl.e * p.b_rows_pad * p.cpb * 4);
+          sfb_src0 = bsf + (nb0 * p.cpb + kb) * 512;
+          sfb_src1 = nb0 + 1 < nbl ? bsf + ((nb0 + 1) * p.cpb + kb) * 512 : nullptr;
+          bytes += 512 + 512 + (sfb_src1 ? 512 : 0);
+        }
+        mbar_expect_tx(&full[stage], bytes);
+        const int x = (int)(tl.x0 + (int64_t)ks * BK);
+        tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, &full[stage], x, (int)tl.row0);
+        if (WGRAD) {
+          tma_load_2d(sB + stage * B_STAGE_BYTES, &tmB, &full[stage], x, (int)tl.col0);
+        } else {
+          tma_load_3d(sB + stage * B_STAGE_BYTES, &tmB, &full[stage], x, (int)tl.col0, tl.e);
+        }
+        if (MX) {
+          bulk_load(sSFA + stage * SFA_STAGE_BYTES, sfa_src, 512, &full[stage]);
+          bulk_load(sSFB + stage * SFB_STAGE_BYTES, sfb_src0, 512, &full[stage]);
+          if (sfb_src1) bulk_load(sSFB + stage * SFB_STAGE_BYTES + 512, sfb_src1, 512, &full[stage]);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ======================= MMA issuer =======================
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+      if (tl.nk == 0) continue;
+      if (!mbar_wait(tmem_empty, acc_phase ^ 1, abort_flag)) {
+        set_status(g.status, FP8MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      acc_phase ^= 1;
+      tc_fence_after();
+      bool ok = true;
+      for (int ks = 0; ks < tl.nk; ++ks) {
+        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          set_status(g.status, FP8MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(sA + stage * A_STAGE_BYTES);
+        const uint32_t b_addr = smem_u32(sB + stage * B_STAGE_BYTES);
+        const uint32_t sf_col = tmem_base + TMEM_SF_BASE + stage * 16;
+        if (MX) {
+          tc_cp_sf(sf_col, sdesc_sf(smem_u32(sSFA + stage * SFA_STAGE_BYTES)));
+          tc_cp_sf(sf_col + 4, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES)));
+          tc_cp_sf(sf_col + 8, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES + 512)));
+        }
+        const int64_t rem = tl.kvalid - (int64_t)ks * BK;
+        const int nsub = rem >= BK ? 4 : (int)((rem + 31) / 32);
+        const uint64_t adesc = sdesc_sw128(a_addr), bdesc = sdesc_sw128(b_addr);
+        for (int k = 0; k < nsub; ++k) {
+          const uint32_t accum = (ks > 0 || k > 0) ? 1u : 0u;
+          if (MX) {
+            mma_mx(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_mx((uint32_t)k), sf_col,
+                   sf_col + 4, accum);
+          } else {
+            mma_f8(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8(), accum);
+          }
+        }
+        tc_commit(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      tc_commit(tmem_full);
+    }
+  } else if (warp >= 2) {
+    // ======================= epilogue =======================
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int et = threadIdx.x - 64;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+      const int64_t lrow = quarter * 32 + lane;
+      const bool row_ok = lrow < tl.rows;
+      const int64_t ncols = (g.cols - tl.col0) < BN ? (g.cols - tl.col0) : BN;
+      uint16_t* orow = WGRAD ? g.out + ((int64_t)tl.e * g.rows + tl.row0 + lrow) * g.cols + tl.col0
+                             : g.out + (tl.row0 + lrow) * g.cols + tl.col0;
+      if (tl.nk == 0) {  // empty group in wgrad: dW[e] = 0
+        if (row_ok)
+          for (int c = 0; c < ncols; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      float rscale = 1.0f;
+      if (!MX) {
+        // column scales of this tile into shared memory, row scale per thread
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const float* cs = (const float*)g.b_scale + (int64_t)tl.e * g.cols + tl.col0;
+        for (int c = et; c < BN; c += 128) colscale[c] = c < ncols ? cs[c] : 0.0f;
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (row_ok) {
+          const float* rs = (const float*)g.a_scale;
+          rscale = WGRAD ? rs[(int64_t)tl.e * g.rows + tl.row0 + lrow] : rs[tl.row0 + lrow];
+        }
+      }
+      if (!mbar_wait(tmem_full, acc_phase, abort_flag)) {
+        set_status(g.status, FP8MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      acc_phase ^= 1;
+      tc_fence_after();
+      uint32_t packed[BN / 2];
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
+          if (!MX) {
+            v0 = v0 * rscale * colscale[c + j];
+            v1 = v1 * rscale * colscale[c + j + 1];
+          }
+          packed[(c + j) / 2] = pack_bf16(v0, v1);
+        }
+      }
+      // accumulator drained: let the MMA warp start the next tile
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
+      if (row_ok) {
+#pragma unroll
+        for (int c = 0; c < BN; c += 8) {
+          if (c < ncols)
+            *reinterpret_cast<uint4*>(orow + c) =
+                make_uint4(packed[c / 2], packed[c / 2 + 1], packed[c / 2 + 2], packed[c / 2 + 3]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)ptr;
+  }
+  return fn;
+}
+
+static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                     const cuuint32_t* box) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool MX, bool WGRAD>
+static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& p, int grid,
+                            cudaStream_t st) {
+  auto kern = k_grouped_mm<MX, WGRAD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
+  if (g.E > MAX_GROUPS) return cudaErrorNotSupported;
+  if (g.kk > INT32_MAX || g.rows > INT32_MAX || g.cols > INT32_MAX || g.M > INT32_MAX) return cudaErrorInvalidValue;
+  if (SMEM_BYTES > g.max_smem) return cudaErrorNotSupported;
+  const bool mx = g.recipe == FP8MOE_MXFP8;
+  const bool wgrad = g.mode == GEMM_WGRAD;
+  KParams p;
+  p.g = g;
+  p.n_tiles = (int)((g.cols + BN - 1) / BN);
+  p.m_tiles_w = (int)((g.rows + BM - 1) / BM);
+  if (!wgrad) {
+    p.cpb = (g.kk / 32 + 3) / 4;
+    p.b_rows_pad = (g.cols + 127) / 128 * 128;
+  } else {
+    p.cpb = (g.kk / 32 + 3) / 4 + g.E;  // column-grouped scale layout
+    p.b_rows_pad = 0;
+  }
+  CUtensorMap ta, tb;
+  {
+    const int64_t arows = wgrad ? g.rows : g.M;
+    cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)(arows > 0 ? arows : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)g.kk};
+    cuuint32_t box[2] = {BK, BM};
+    if (!make_map(&ta, g.a, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  if (wgrad) {
+    cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)g.cols};
+    cuuint64_t strides[1] = {(cuuint64_t)g.kk};
+    cuuint32_t box[2] = {BK, BN};
+    if (!make_map(&tb, g.b, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  } else {
+    cuuint64_t dims[3] = {(cuuint64_t)g.kk, (cuuint64_t)g.cols, (cuuint64_t)g.E};
+    cuuint64_t strides[2] = {(cuuint64_t)g.kk, (cuuint64_t)(g.kk * g.cols)};
+    cuuint32_t box[3] = {BK, BN, 1};
+    if (!make_map(&tb, g.b, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  // tiles are only known on the device; size the grid by an upper bound
+  int64_t bound;
+  if (!wgrad) {
+    bound = ((g.M + BM - 1) / BM + g.E) * p.n_tiles;
+  } else {
+    bound = (int64_t)g.E * p.m_tiles_w * p.n_tiles;
+  }
+  int grid = (int)(bound < g.num_sms ? bound : g.num_sms);
+  if (grid < 1) grid = 1;
+  if (mx) {
+    return wgrad ? launch_t<true, true>(ta, tb, p, grid, st) : launch_t<true, false>(ta, tb, p, grid, st);
+  }
+  return wgrad ? launch_t<false, true>(ta, tb, p, grid, st) : launch_t<false, false>(ta, tb, p, grid, st);
+}
+
+}  // namespace fp8moe
