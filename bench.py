@@ -60,7 +60,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
         return self
@@ -101,7 +101,7 @@ class ClockSampler:
 class ScoutStep:
     """Buffers and launches of one step; every launch goes through the C ABI."""
 
-    def __init__(self, F, wl, device, seed_offset=0):
+    def __init__(self, F, wl, device, layers=2):
         import torch
         import workloads as W
         self.F, self.wl, self.dev = F, wl, device
@@ -111,7 +111,7 @@ class ScoutStep:
         self.E = wl.E
         self.real_tokens = int(wl.group_plan()[0].sum())
         self.layers = []
-        for wname, aname, dname in [("W1", "A", "dY"), ("W2", "A2", "dY2")]:
+        for wname, aname, dname in [("W1", "A", "dY"), ("W2", "A2", "dY2")][:layers]:
             w = W.make_weights(wl, wname, device=device)
             a = W.make_activations(wl, aname, device=device)
             dy = W.make_activations(wl, dname, device=device)
@@ -249,8 +249,10 @@ def cpu_baseline(wl, budget_s=20.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--layers", type=int, default=2, choices=[1, 2],
+                    help="expert weights per step (2 = W1 and W2; 1 = W1 only, for profiling)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -298,7 +300,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    step = ScoutStep(F, wl, dev)
+    step = ScoutStep(F, wl, dev, layers=args.layers)
     stream = torch.cuda.current_stream()
     for _ in range(max(3, args.warmup)):
         step.run()
@@ -366,7 +368,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3 x e4m3 (e8m0 scales) -> fp32 accum -> bf16", "data": "synthetic",
             "config": {"workload": f"{wl.name}: {wl.description}", "experts": wl.E, "tokens": wl.tokens,
-                       "routed_rows_padded": wl.M, "hidden": wl.K, "ffn": wl.N, "weights": 2,
+                       "routed_rows_padded": wl.M, "hidden": wl.K, "ffn": wl.N, "weights": args.layers,
                        "l2": "inputs larger than L2 (each expert weight is 1.34 GB bf16)"},
             "gemm_tflops": flops / (gemm_ms * 1e-3) / 1e12,
             "gemm_frac_fp8_peak": flops / (gemm_ms * 1e-3) / 1e12 / fp8_peak,

@@ -116,8 +116,11 @@ fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, in
   if (B == 0 || R == 0 || C == 0) return FP8MOE_OK;
   if (!x || !qt || !scale) return FP8MOE_ERR_INVALID_ARG;
   if (!al16(x) || !al16(qt)) return FP8MOE_ERR_ALIGNMENT;
-  if (C > 65535 * 64 || R > (int64_t)1 << 31 || B > 65535) return FP8MOE_ERR_INVALID_ARG;
-  return cuda_result(fp8moe::launch_mx_dim1(x, B, R, C, qt, scale, (cudaStream_t)stream));
+  if (C > ((int64_t)1 << 31) || R > ((int64_t)1 << 31) || B > 65535) return FP8MOE_ERR_INVALID_ARG;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  return cuda_result(fp8moe::launch_mx_dim1(x, B, R, C, qt, scale, d->num_sms, d->status, (cudaStream_t)stream));
 }
 
 int64_t fp8moe_swizzled_scales_bytes(int64_t B, int64_t R, int64_t Cs, int64_t E, int group_axis) {

@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace fp8moe {
 
@@ -42,7 +43,6 @@ constexpr int SFB_STAGE_BYTES = 1024;             // two 128x4 scale tiles (256 
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = 256;            // scale columns start after the accumulator
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull; // 2 s
 
 struct SmemLayout {
   static constexpr int a = 0;
@@ -54,72 +54,15 @@ struct SmemLayout {
   static constexpr int colscale = misc + 64;                    // 256 floats
   static constexpr int tiles_prefix = colscale + BN * 4;        // MAX_GROUPS + 1 ints
   static constexpr int blk_prefix = tiles_prefix + (MAX_GROUPS + 1) * 4;
-  static constexpr int total = blk_prefix + (MAX_GROUPS + 1) * 4;
+  static constexpr int stg = (blk_prefix + (MAX_GROUPS + 1) * 4 + 15) / 16 * 16;
+  static constexpr int total = stg + 4 * 32 * 144;                    // per-warp 32 x (128 + 16) B
 };
+static_assert(SmemLayout::stg % 16 == 0, "staging must be 16-byte aligned");
 constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
-FP8MOE_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-FP8MOE_DEV uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-FP8MOE_DEV void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-FP8MOE_DEV void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-FP8MOE_DEV void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-FP8MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: false when the limit ran out or another role aborted.
-FP8MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
-  }
-}
-
-FP8MOE_DEV void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-FP8MOE_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
-FP8MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
 FP8MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 FP8MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 FP8MOE_DEV void tc_commit(uint64_t* bar) {
@@ -296,7 +239,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, 4);
     *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_fence_init();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -468,17 +411,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ======================= epilogue =======================
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int et = threadIdx.x - 64;
+    uint8_t* stg = smem + SmemLayout::stg + (warp - 2) * 32 * 144;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
       const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
       const int64_t lrow = quarter * 32 + lane;
       const bool row_ok = lrow < tl.rows;
       const int64_t ncols = (g.cols - tl.col0) < BN ? (g.cols - tl.col0) : BN;
-      uint16_t* orow = WGRAD ? g.out + ((int64_t)tl.e * g.rows + tl.row0 + lrow) * g.cols + tl.col0
-                             : g.out + (tl.row0 + lrow) * g.cols + tl.col0;
+      // first element of this tile in the output
+      uint16_t* obase = WGRAD ? g.out + ((int64_t)tl.e * g.rows + tl.row0) * g.cols + tl.col0
+                              : g.out + tl.row0 * g.cols + tl.col0;
       if (tl.nk == 0) {  // empty group in wgrad: dW[e] = 0
-        if (row_ok)
-          for (int c = 0; c < ncols; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+        const int nc8 = (int)(ncols / 8);
+        for (int i = lane; i < 32 * nc8; i += 32) {
+          const int64_t trow = quarter * 32 + i / nc8;
+          if (trow < tl.rows)
+            *reinterpret_cast<uint4*>(obase + trow * g.cols + (i % nc8) * 8) = make_uint4(0, 0, 0, 0);
+        }
         continue;
       }
       float rscale = 1.0f;
@@ -521,12 +470,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty);
-      if (row_ok) {
+      // Coalesced stores: 64-column slices of this warp's 32 rows go through a
+      // padded shared-memory buffer (row pitch 144 B: conflict-free both ways),
+      // then each store instruction writes 4 rows x 128 contiguous bytes.
 #pragma unroll
-        for (int c = 0; c < BN; c += 8) {
-          if (c < ncols)
-            *reinterpret_cast<uint4*>(orow + c) =
-                make_uint4(packed[c / 2], packed[c / 2 + 1], packed[c / 2 + 2], packed[c / 2 + 3]);
+      for (int cc = 0; cc < BN; cc += 64) {
+        if (cc < ncols) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(stg + lane * 144 + j * 16) =
+                make_uint4(packed[(cc + j * 8) / 2], packed[(cc + j * 8) / 2 + 1], packed[(cc + j * 8) / 2 + 2],
+                           packed[(cc + j * 8) / 2 + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = i * 4 + (lane >> 3), ch = lane & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 144 + ch * 16);
+            const int64_t trow = quarter * 32 + r;
+            const int64_t col = cc + ch * 8;
+            if (trow < tl.rows && col < ncols) *reinterpret_cast<uint4*>(obase + trow * g.cols + col) = v;
+          }
+          __syncwarp();
         }
       }
     }
@@ -541,31 +505,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn get_encode() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiledFn)ptr;
-  }
-  return fn;
-}
-
 static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                      const cuuint32_t* box) {
-  EncodeTiledFn enc = get_encode();
-  if (!enc) return false;
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides, box);
 }
 
 template <bool MX, bool WGRAD>

@@ -9,8 +9,8 @@ cudaError_t launch_quant_rowwise(const void* x, int64_t R, int64_t C, int64_t ld
                                  float* inv, cudaStream_t st);
 cudaError_t launch_mx_dim0(const void* x, int64_t rows, int64_t C, void* q, uint8_t* s, int num_sms,
                            cudaStream_t st);
-cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s,
-                           cudaStream_t st);
+cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s, int num_sms,
+                           int* status, cudaStream_t st);
 cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                            int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
                            int max_smem, cudaStream_t st);

@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -186,61 +187,139 @@ cudaError_t launch_mx_dim0(const void* x, int64_t rows, int64_t C, void* q, uint
 }
 
 // ============================================================================
-// MXFP8 dim1: a 128-row x 64-column bf16 tile in shared memory; each thread
-// owns one (32-row block, column) pair and writes 32 contiguous output bytes
-// of the transposed result.
+// MXFP8 dim1: persistent CTAs stream 128-row x 64-column bf16 tiles through a
+// 4-stage TMA ring (128-byte swizzle); each thread owns one (32-row block,
+// column) pair, computes its e8m0 scale and 32 codes, and writes them into a
+// swizzled 64 x 128-byte staging tile that a TMA store writes out as 64
+// contiguous 128-byte segments of the transposed output.
 // ============================================================================
-constexpr int D1_ROWS = 128, D1_COLS = 64, D1_PITCH = 144;  // 128 B data + 16 B pad
+constexpr int D1_ROWS = 128, D1_COLS = 64, D1_STAGES = 4;
+constexpr int D1_IN_BYTES = D1_ROWS * D1_COLS * 2;   // 16 KB
+constexpr int D1_OUT_BYTES = D1_COLS * D1_ROWS;      // 8 KB
+constexpr int D1_SMEM = D1_STAGES * D1_IN_BYTES + 2 * D1_OUT_BYTES + 64 + 1024;
 
-__global__ void __launch_bounds__(256) k_mx_dim1(const uint16_t* __restrict__ x, int64_t R, int64_t C,
-                                                 uint8_t* __restrict__ qt, uint8_t* __restrict__ sc) {
-  __shared__ __align__(16) uint8_t tile[D1_ROWS * D1_PITCH];
-  const int64_t r0 = (int64_t)blockIdx.x * D1_ROWS;
-  const int64_t c0 = (int64_t)blockIdx.y * D1_COLS;
-  const int64_t b = blockIdx.z;
-  const uint16_t* xb = x + b * R * C;
+struct Dim1Args {
+  int64_t B, R, C;
+  int64_t n_rt, n_ct, tiles;
+  uint8_t* scale;
+  int* status;
+};
+
+__global__ void __launch_bounds__(256) k_mx_dim1(const __grid_constant__ CUtensorMap tin,
+                                                 const __grid_constant__ CUtensorMap tout, Dim1Args a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* in = smem;
+  uint8_t* outb = smem + D1_STAGES * D1_IN_BYTES;
+  uint64_t* full = (uint64_t*)(outb + 2 * D1_OUT_BYTES);
+  volatile int* abort_s = (volatile int*)(full + D1_STAGES);
   const int tid = threadIdx.x;
-  // load: 8 threads x 16 B per row, 4 passes of 32 rows
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int k = tid + 256 * i;
-    const int rr = k >> 3, c16 = k & 7;
-    const int64_t r = r0 + rr, c = c0 + c16 * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < R && c < C) v = ld_stream(xb + r * C + c);
-    *reinterpret_cast<uint4*>(tile + rr * D1_PITCH + c16 * 16) = v;
+  auto coords = [&](int64_t t, int& rt, int& ct, int& b) {
+    rt = (int)(t % a.n_rt);
+    ct = (int)((t / a.n_rt) % a.n_ct);
+    b = (int)(t / (a.n_rt * a.n_ct));
+  };
+  if (tid == 0) {
+    for (int s = 0; s < D1_STAGES; ++s) mbar_init(&full[s], 1);
+    *abort_s = 0;
+    mbar_fence_init();
   }
   __syncthreads();
-  const int cl = tid & 63, rb = tid >> 6;
-  const int64_t c = c0 + cl;
-  const int64_t rbase = r0 + rb * 32;
-  if (c >= C || rbase >= R) return;
-  float f[32];
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint32_t h = *reinterpret_cast<const uint16_t*>(tile + (rb * 32 + i) * D1_PITCH + cl * 2);
-    m = max(m, h & 0x7FFFu);
-    f[i] = bf16bits_to_float(h);
+  if (tid == 0) {
+    for (int s = 0; s < D1_STAGES; ++s) {
+      const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
+      if (t >= a.tiles) break;
+      int rt, ct, b;
+      coords(t, rt, ct, b);
+      mbar_expect_tx(&full[s], D1_IN_BYTES);
+      tma_load_3d(in + s * D1_IN_BYTES, &tin, &full[s], ct * D1_COLS, rt * D1_ROWS, b);
+    }
   }
-  const int e = e8m0_exponent(m);
-  const float p = exp2_neg(e);
-  uint32_t w[8];
+  const int cl = tid & 63, rb = tid >> 6;
+  int it = 0;
+  for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
+    const int s = it % D1_STAGES, ob = it & 1;
+    int rt, ct, b;
+    coords(t, rt, ct, b);
+    if (tid == 0) bulk_wait_read<1>();  // the store issued two tiles ago has left staging buffer ob
+    __syncthreads();
+    if (!mbar_wait(&full[s], (uint32_t)((it / D1_STAGES) & 1), abort_s)) {
+      set_status(a.status, FP8MOE_ERR_TIMEOUT);
+      *abort_s = 1;
+    }
+    __syncthreads();
+    if (*abort_s) break;
+    const uint8_t* tile = in + s * D1_IN_BYTES;
+    float f[32];
+    uint32_t m = 0;
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    w[j] = enc4<false>(__fmul_rn(f[4 * j], p), __fmul_rn(f[4 * j + 1], p), __fmul_rn(f[4 * j + 2], p),
-                       __fmul_rn(f[4 * j + 3], p));
-  uint8_t* dst = qt + (b * C + c) * R + rbase;
-  reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  sc[(b * C + c) * (R / 32) + rbase / 32] = (uint8_t)(e + 127);
+    for (int i = 0; i < 32; ++i) {
+      const int r = rb * 32 + i;
+      const uint32_t h =
+          *reinterpret_cast<const uint16_t*>(tile + r * 128 + ((((cl >> 3) ^ (r & 7))) << 4) + ((cl & 7) << 1));
+      m = max(m, h & 0x7FFFu);
+      f[i] = bf16bits_to_float(h);
+    }
+    const int e = e8m0_exponent(m);
+    const float p = exp2_neg(e);
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      w[j] = enc4<false>(__fmul_rn(f[4 * j], p), __fmul_rn(f[4 * j + 1], p), __fmul_rn(f[4 * j + 2], p),
+                         __fmul_rn(f[4 * j + 3], p));
+    uint8_t* orow = outb + ob * D1_OUT_BYTES + cl * 128;
+    *reinterpret_cast<uint4*>(orow + (((rb * 2) ^ (cl & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(orow + (((rb * 2 + 1) ^ (cl & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    const int64_t c = (int64_t)ct * D1_COLS + cl;
+    const int64_t rbase = (int64_t)rt * D1_ROWS + rb * 32;
+    if (c < a.C && rbase < a.R) a.scale[((int64_t)b * a.C + c) * (a.R / 32) + rbase / 32] = (uint8_t)(e + 127);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tma_store_3d(&tout, outb + ob * D1_OUT_BYTES, rt * D1_ROWS, ct * D1_COLS, b);
+      bulk_commit();
+      const int64_t t2 = t + (int64_t)D1_STAGES * gridDim.x;
+      if (t2 < a.tiles) {
+        int rt2, ct2, b2;
+        coords(t2, rt2, ct2, b2);
+        mbar_expect_tx(&full[s], D1_IN_BYTES);
+        tma_load_3d(in + s * D1_IN_BYTES, &tin, &full[s], ct2 * D1_COLS, rt2 * D1_ROWS, b2);
+      }
+    }
+  }
+  if (tid == 0) bulk_wait_read<0>();
 }
 
-cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s,
-                           cudaStream_t st) {
+cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s, int num_sms,
+                           int* status, cudaStream_t st) {
   if (B == 0 || R == 0 || C == 0) return cudaSuccess;
-  dim3 grid((unsigned)((R + D1_ROWS - 1) / D1_ROWS), (unsigned)((C + D1_COLS - 1) / D1_COLS), (unsigned)B);
-  k_mx_dim1<<<grid, 256, 0, st>>>((const uint16_t*)x, R, C, (uint8_t*)qt, s);
+  CUtensorMap tin, tout;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)R, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)(C * 2), (cuuint64_t)(R * C * 2)};
+    cuuint32_t box[3] = {D1_COLS, D1_ROWS, 1};
+    if (!make_tmap(&tin, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)R, (cuuint64_t)C, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)R, (cuuint64_t)(C * R)};
+    cuuint32_t box[3] = {D1_ROWS, D1_COLS, 1};
+    if (!make_tmap(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT8, qt, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  Dim1Args a;
+  a.B = B;
+  a.R = R;
+  a.C = C;
+  a.n_rt = (R + D1_ROWS - 1) / D1_ROWS;
+  a.n_ct = (C + D1_COLS - 1) / D1_COLS;
+  a.tiles = a.n_rt * a.n_ct * B;
+  a.scale = s;
+  a.status = status;
+  cudaError_t err = cudaFuncSetAttribute(k_mx_dim1, cudaFuncAttributeMaxDynamicSharedMemorySize, D1_SMEM);
+  if (err != cudaSuccess) return err;
+  int64_t grid = (int64_t)num_sms * 2;
+  if (grid > a.tiles) grid = a.tiles;
+  k_mx_dim1<<<(unsigned)grid, 256, D1_SMEM, st>>>(tin, tout, a);
   return cudaGetLastError();
 }
 
@@ -475,6 +554,32 @@ __global__ void __launch_bounds__(256) k_colwise(ColwiseArgs a) {
   if (CL > 1) cluster.sync();
 }
 
+template <typename K>
+static cudaError_t launch_colwise_cl8(ColwiseArgs a, K kern, int64_t R, int64_t E, int64_t nstrips, int64_t max_cap,
+                                      cudaStream_t st) {
+  const int CL = 8;
+  const size_t tbytes = (size_t)CW_COLS * CW_TPITCH;
+  int64_t cap = (((R + CL - 1) / CL + 15) / 16 * 16 + 63) / 64 * 64;
+  if (cap > max_cap) cap = max_cap;
+  a.cap_rows = (int)cap;
+  const size_t smem = (size_t)cap * CW_PITCH + tbytes;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(E * nstrips * CL));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                            int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
                            int max_smem, cudaStream_t st) {
@@ -493,25 +598,33 @@ cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const
   if (E == 0 || nstrips == 0) return cudaSuccess;
   const size_t fixed = sizeof(uint32_t) * 256 * 4 + 1024;  // static shared memory + slack
   const size_t tbytes = (size_t)CW_COLS * CW_TPITCH;
-  int64_t cap = (int64_t)((max_smem - fixed - tbytes) / CW_PITCH) / 64 * 64;
+  const int64_t max_cap = (int64_t)((max_smem - fixed - tbytes) / CW_PITCH) / 64 * 64;
+  // ~640 resident rows per CTA keeps 3+ CTAs per SM, so one CTA's loads overlap
+  // another's casts and stores; taller strips are split over a cluster.
+  constexpr int64_t kTargetRows = 640;
   int CL = 1;
+  int64_t cap;
   if (offs == nullptr) {
-    // dense: pick the smallest cluster that keeps every row resident
-    while (CL < 8 && (R + CL - 1) / CL > cap) CL *= 2;
+    while (CL < 16 && (R + CL - 1) / CL > kTargetRows) CL *= 2;
     const int64_t per = ((R + CL - 1) / CL + 15) / 16 * 16;
-    if (per < cap) cap = (per + 63) / 64 * 64;
+    cap = (per + 63) / 64 * 64;
   } else {
-    // jagged: the average group's strip, capped; bigger groups re-read the overflow
-    const int64_t avg = (R / (E > 0 ? E : 1) + 63) / 64 * 64;
-    const int64_t want = avg < 1024 ? 1024 : avg;
-    if (want < cap) cap = want;
+    // jagged: groups up to ~3x the average size stay single-pass
+    const int64_t avg = R / (E > 0 ? E : 1);
+    while (CL < 8 && 3 * avg > CL * kTargetRows) CL *= 2;
+    cap = kTargetRows;
   }
+  if (cap > max_cap) cap = max_cap;
   if (cap < 64) cap = 64;
   a.cap_rows = (int)cap;
   const size_t smem = (size_t)cap * CW_PITCH + tbytes;
   auto kern = kind == FP8MOE_E4M3FNUZ ? k_colwise<true> : k_colwise<false>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
+  if (CL > 8) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err != cudaSuccess) return err;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(E * nstrips * CL));
   cfg.blockDim = dim3(256);
@@ -524,6 +637,14 @@ cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (CL > 8) {
+    // a 16-CTA cluster may not fit next to other work; fall back to 8 with more rows each
+    int ncl = 0;
+    if (cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg) != cudaSuccess || ncl < 1) {
+      (void)cudaGetLastError();
+      return launch_colwise_cl8(a, kern, R, E, nstrips, max_cap, st);
+    }
+  }
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
