@@ -101,10 +101,11 @@ class ClockSampler:
 class ScoutStep:
     """Buffers and launches of one step; every launch goes through the C ABI."""
 
-    def __init__(self, F, wl, device, layers=2):
+    def __init__(self, F, wl, device, layers=2, fused=True):
         import torch
         import workloads as W
         self.F, self.wl, self.dev = F, wl, device
+        self.fused = fused
         self.offs_np = wl.offs()
         self.offs = torch.from_numpy(self.offs_np).to(device)
         self.M = wl.M
@@ -116,7 +117,7 @@ class ScoutStep:
             a = W.make_activations(wl, aname, device=device)
             dy = W.make_activations(wl, dname, device=device)
             self.layers.append(self._alloc(w, a, dy))
-        self.launches_per_step = 15 * len(self.layers)
+        self.launches_per_step = (6 if fused else 15) * len(self.layers)
 
     def _alloc(self, w, a, dy):
         import torch
@@ -126,24 +127,26 @@ class ScoutStep:
         L = dict(w=w, a=a, dy=dy, N=N, K=K)
         L["qa"] = torch.empty(M, K, dtype=u8, device=dev)
         L["sa"] = torch.empty(M, K // 32, dtype=u8, device=dev)
-        L["sa_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(1, M, K // 32, E, F.GROUP_ROWS), dtype=u8, device=dev)
+        # swizzled scale buffers start zeroed: the fused kernels write only real
+        # scale bytes, so the padding stays 0
+        L["sa_sw"] = torch.zeros(F.fp8moe_swizzled_scales_bytes(1, M, K // 32, E, F.GROUP_ROWS), dtype=u8, device=dev)
         L["qw"] = torch.empty(E, N, K, dtype=u8, device=dev)
         L["sw"] = torch.empty(E, N, K // 32, dtype=u8, device=dev)
-        L["sw_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(E, N, K // 32), dtype=u8, device=dev)
+        L["sw_sw"] = torch.zeros(F.fp8moe_swizzled_scales_bytes(E, N, K // 32), dtype=u8, device=dev)
         L["out"] = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         L["qdy"] = torch.empty(M, N, dtype=u8, device=dev)
         L["sdy"] = torch.empty(M, N // 32, dtype=u8, device=dev)
-        L["sdy_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(1, M, N // 32, E, F.GROUP_ROWS), dtype=u8, device=dev)
+        L["sdy_sw"] = torch.zeros(F.fp8moe_swizzled_scales_bytes(1, M, N // 32, E, F.GROUP_ROWS), dtype=u8, device=dev)
         L["qwt"] = torch.empty(E, K, N, dtype=u8, device=dev)
         L["swt"] = torch.empty(E, K, N // 32, dtype=u8, device=dev)
-        L["swt_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(E, K, N // 32), dtype=u8, device=dev)
+        L["swt_sw"] = torch.zeros(F.fp8moe_swizzled_scales_bytes(E, K, N // 32), dtype=u8, device=dev)
         L["da"] = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
         L["qdyt"] = torch.empty(N, M, dtype=u8, device=dev)
         L["sdyt"] = torch.empty(N, M // 32, dtype=u8, device=dev)
-        L["sdyt_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(1, N, M // 32, E, F.GROUP_COLS), dtype=u8, device=dev)
+        L["sdyt_sw"] = torch.zeros(F.fp8moe_swizzled_scales_bytes(1, N, M // 32, E, F.GROUP_COLS), dtype=u8, device=dev)
         L["qat"] = torch.empty(K, M, dtype=u8, device=dev)
         L["sat"] = torch.empty(K, M // 32, dtype=u8, device=dev)
-        L["sat_sw"] = torch.empty(F.fp8moe_swizzled_scales_bytes(1, K, M // 32, E, F.GROUP_COLS), dtype=u8, device=dev)
+        L["sat_sw"] = torch.zeros(F.fp8moe_swizzled_scales_bytes(1, K, M // 32, E, F.GROUP_COLS), dtype=u8, device=dev)
         L["dw"] = torch.empty(E, N, K, dtype=torch.bfloat16, device=dev)
         return L
 
@@ -153,21 +156,51 @@ class ScoutStep:
         return sum(3 * 2.0 * self.real_tokens * L["N"] * L["K"] for L in self.layers)
 
     def quant_bytes(self):
-        """Algorithmic HBM bytes of the quantization + swizzle launches per step:
-        2 B read + 1 B written per element, + 1 scale byte per 32 (written, then
-        read and written again by the swizzle)."""
+        """Algorithmic HBM bytes of the quantization launches per step.
+
+        Fused: each of A, W, dY is read once (2 B/element) and written twice
+        (1 B of codes per direction) with one scale byte per 32 elements per
+        direction.  Unfused: dim0 and dim1 each read the tensor (2 + 1 B per
+        element + 1/32), and the swizzle reads and writes every scale byte.
+        """
         tot = 0.0
         for L in self.layers:
             M, N, K, E = self.M, L["N"], L["K"], self.E
-            elems = 2 * M * K + 2 * E * N * K + 2 * M * N   # A, W, dY each dim0 + dim1
-            tot += elems * 3 + elems / 32 * 3
+            elems = M * K + E * N * K + M * N               # A, W, dY
+            if self.fused:
+                tot += elems * (2 + 2 + 2 / 32)
+            else:
+                tot += elems * 2 * (3 + 1 / 32) + elems * 2 / 32 * 2
         return tot
+
+    def quant_elements(self):
+        """Elements quantized per step, counting each direction separately."""
+        return sum(2 * (self.M * L["K"] + self.E * L["N"] * L["K"] + self.M * L["N"]) for L in self.layers)
 
     # launches -------------------------------------------------------
     def run(self, rec=None):
         """One step.  ``rec(kind, fn)`` wraps each launch for timing."""
         F, offs = self.F, self.offs
         rec = rec or (lambda kind, fn: fn())
+        if self.fused:
+            for L in self.layers:
+                # A: dim0 (forward operand, row-grouped scales) + dim1 (wgrad operand,
+                # column-grouped scales); W: both directions, per-expert scales;
+                # dY: dim0 (dgrad) + dim1 (wgrad)
+                rec("quant", lambda: F.fp8moe_mxfp8_quantize_dual(
+                    L["a"], offs, F.GROUP_ROWS, F.GROUP_COLS, q0=L["qa"], s0=L["sa_sw"], q1=L["qat"], s1=L["sat_sw"]))
+                rec("quant", lambda: F.fp8moe_mxfp8_quantize_dual(
+                    L["w"], None, F.NO_GROUPS, F.NO_GROUPS, q0=L["qw"], s0=L["sw_sw"], q1=L["qwt"], s1=L["swt_sw"]))
+                rec("gemm", lambda: F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, L["qa"], L["sa_sw"], L["qw"], L["sw_sw"],
+                                                                   offs, out=L["out"]))
+                rec("quant", lambda: F.fp8moe_mxfp8_quantize_dual(
+                    L["dy"], offs, F.GROUP_ROWS, F.GROUP_COLS, q0=L["qdy"], s0=L["sdy_sw"], q1=L["qdyt"],
+                    s1=L["sdyt_sw"]))
+                rec("gemm", lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.MXFP8, L["qdy"], L["sdy_sw"], L["qwt"],
+                                                                     L["swt_sw"], offs, out=L["da"]))
+                rec("gemm", lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.MXFP8, L["qdyt"], L["sdyt_sw"], L["qat"],
+                                                                     L["sat_sw"], offs, self.M, out=L["dw"]))
+            return
         for L in self.layers:
             rec("quant", lambda: F.fp8moe_mxfp8_quantize_dim0(L["a"], L["qa"], L["sa"]))
             rec("quant", lambda: F.fp8moe_swizzle_scales_128x4(L["sa"], offs, F.GROUP_ROWS, out=L["sa_sw"]))
@@ -255,6 +288,8 @@ def main():
                     help="expert weights per step (2 = W1 and W2; 1 = W1 only, for profiling)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="separate dim0 / dim1 / swizzle launches instead of the fused dual-direction kernel")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
 
@@ -300,7 +335,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    step = ScoutStep(F, wl, dev, layers=args.layers)
+    step = ScoutStep(F, wl, dev, layers=args.layers, fused=not args.unfused)
     stream = torch.cuda.current_stream()
     for _ in range(max(3, args.warmup)):
         step.run()
@@ -358,7 +393,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         q_rate, g_rate, sample = cpu_baseline(wl)
-        t_cpu = qbytes / 3.1 / q_rate + flops / g_rate
+        t_cpu = step.quant_elements() / q_rate + flops / g_rate
         cpu = {"value": flops / t_cpu / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": sample, "ms_per_step_extrapolated": t_cpu * 1e3}
 
@@ -369,7 +404,8 @@ def main():
             "vs_baseline": None, "dtype": "e4m3 x e4m3 (e8m0 scales) -> fp32 accum -> bf16", "data": "synthetic",
             "config": {"workload": f"{wl.name}: {wl.description}", "experts": wl.E, "tokens": wl.tokens,
                        "routed_rows_padded": wl.M, "hidden": wl.K, "ffn": wl.N, "weights": args.layers,
-                       "l2": "inputs larger than L2 (each expert weight is 1.34 GB bf16)"},
+                       "l2": "inputs larger than L2 (each expert weight is 1.34 GB bf16)",
+                       "quant": "fused dual-direction" if step.fused else "separate dim0/dim1/swizzle"},
             "gemm_tflops": flops / (gemm_ms * 1e-3) / 1e12,
             "gemm_frac_fp8_peak": flops / (gemm_ms * 1e-3) / 1e12 / fp8_peak,
             "quant_gbs": qbytes / (quant_ms * 1e-3) / 1e9,

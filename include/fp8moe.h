@@ -63,7 +63,7 @@ typedef enum {
   FP8MOE_MXFP8 = 1     /* e8m0 scale per 1x32 block, 128x4-tiled      */
 } fp8moe_recipe;
 
-enum { FP8MOE_NO_GROUPS = -1, FP8MOE_GROUP_ROWS = 0, FP8MOE_GROUP_COLS = 1 };
+enum { FP8MOE_SCALES_ROWMAJOR = -2, FP8MOE_NO_GROUPS = -1, FP8MOE_GROUP_ROWS = 0, FP8MOE_GROUP_COLS = 1 };
 
 /* ------------------------------------------------------------------------
  * Rowwise FP8 quantization.  [AMD-FP8] aihirek.info "A Triton-kernelok
@@ -133,6 +133,34 @@ fp8moe_status fp8moe_mxfp8_quantize_dim0(const void* x, int64_t B, int64_t R, in
  * ------------------------------------------------------------------------ */
 fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, int64_t C,
                                          void* qt, uint8_t* scale, fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * MXFP8 quantization along both dimensions from one read of x, with the
+ * scales written directly in their final layout.  [SCOUT] section details:
+ * forward and backward each quantize the same tensors (activations, weights,
+ * gradients) along the dimension their GEMM contracts over, and the scales go
+ * to the 128x4 layout; [AMD-FP8] aixai.ru "Три уровня оптимизации": one fused
+ * kernel instead of separate passes through HBM.
+ *
+ * x [B, R, C] bf16 contiguous, R % 32 == 0 (when dim1 is produced), C % 32 == 0.
+ * Either direction may be skipped by passing NULL codes.
+ *   dim0: q0 [B, R, C] e4m3fn; s0 = scales of [B, R, C/32] in layout s0_layout:
+ *         FP8MOE_SCALES_ROWMAJOR (plain [B, R, C/32]), FP8MOE_NO_GROUPS
+ *         (128x4 tiles per batch, as fp8moe_swizzle_scales_128x4), or
+ *         FP8MOE_GROUP_ROWS (B == 1, offs [E] over R).
+ *   dim1: q1 [B, C, R] e4m3fn; s1 = scales of [B, C, R/32] in layout s1_layout:
+ *         FP8MOE_SCALES_ROWMAJOR, FP8MOE_NO_GROUPS, or FP8MOE_GROUP_COLS
+ *         (B == 1, offs [E] over R, multiples of 32).
+ * Codes and the scale bytes of real blocks are bit-identical to
+ * fp8moe_mxfp8_quantize_dim0 / dim1 followed by fp8moe_swizzle_scales_128x4;
+ * the padding bytes of a swizzled scale buffer are not written (the grouped
+ * GEMM never lets them reach a stored output; zero the buffer first if they
+ * must be zero).  Invalid device offsets set FP8MOE_ERR_DEVICE_OFFSETS and
+ * write nothing.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_mxfp8_quantize_dual(const void* x, int64_t B, int64_t R, int64_t C, const int32_t* offs,
+                                         int64_t E, void* q0, uint8_t* s0, int s0_layout, void* q1, uint8_t* s1,
+                                         int s1_layout, fp8moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * 128x4 tiled scale layout for tcgen05 block-scaled MMA.  [SCOUT] section

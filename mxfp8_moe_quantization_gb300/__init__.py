@@ -15,10 +15,10 @@ import os
 from typing import Optional, Tuple
 
 __all__ = [
-    "E4M3FN", "E4M3FNUZ", "ROWWISE", "MXFP8", "NO_GROUPS", "GROUP_ROWS", "GROUP_COLS",
+    "E4M3FN", "E4M3FNUZ", "ROWWISE", "MXFP8", "SCALES_ROWMAJOR", "NO_GROUPS", "GROUP_ROWS", "GROUP_COLS",
     "Fp8MoeError", "lib", "library_path", "SYMBOLS",
     "fp8moe_quantize_rowwise", "fp8moe_quantize_colwise_3d", "fp8moe_jagged_t_cols",
-    "fp8moe_mxfp8_quantize_dim0", "fp8moe_mxfp8_quantize_dim1",
+    "fp8moe_mxfp8_quantize_dim0", "fp8moe_mxfp8_quantize_dim1", "fp8moe_mxfp8_quantize_dual",
     "fp8moe_swizzled_scales_bytes", "fp8moe_swizzle_scales_128x4",
     "fp8moe_scaled_grouped_mm_fwd", "fp8moe_scaled_grouped_mm_dgrad",
     "fp8moe_scaled_grouped_mm_wgrad", "fp8moe_get_device_status", "fp8moe_status_string",
@@ -26,7 +26,7 @@ __all__ = [
 
 E4M3FN, E4M3FNUZ = 0, 1
 ROWWISE, MXFP8 = 0, 1
-NO_GROUPS, GROUP_ROWS, GROUP_COLS = -1, 0, 1
+SCALES_ROWMAJOR, NO_GROUPS, GROUP_ROWS, GROUP_COLS = -2, -1, 0, 1
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(HERE, "libfp8moe.so")
@@ -40,6 +40,7 @@ SYMBOLS = {
     "fp8moe_jagged_t_cols": (_i64, [_i64, _i64]),
     "fp8moe_mxfp8_quantize_dim0": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "fp8moe_mxfp8_quantize_dim1": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "fp8moe_mxfp8_quantize_dual": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _i32, _vp]),
     "fp8moe_swizzled_scales_bytes": (_i64, [_i64, _i64, _i64, _i64, _i32]),
     "fp8moe_swizzle_scales_128x4": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _vp]),
     "fp8moe_scaled_grouped_mm_fwd": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
@@ -187,6 +188,42 @@ def fp8moe_mxfp8_quantize_dim1(x, qt=None, scale=None, stream=None):
     _check("fp8moe_mxfp8_quantize_dim1", _lib_raw().fp8moe_mxfp8_quantize_dim1(
         _ptr(x), B, R, C, _ptr(qt), _ptr(scale), _stream(stream)))
     return qt, scale
+
+
+def _scale_buffer(layout, B, R, Cs, E, like):
+    torch = _torch()
+    if layout == SCALES_ROWMAJOR:
+        return _empty((B, R, Cs) if B > 1 else (R, Cs), torch.uint8, like)
+    return _torch().zeros(fp8moe_swizzled_scales_bytes(B, R, Cs, E, layout), dtype=torch.uint8, device=like.device)
+
+
+def fp8moe_mxfp8_quantize_dual(x, offs=None, s0_layout: int = NO_GROUPS, s1_layout: int = NO_GROUPS,
+                               dim0: bool = True, dim1: bool = True, q0=None, s0=None, q1=None, s1=None,
+                               stream=None):
+    """MXFP8 of x [B, R, C] (or [R, C]) along both dims from one read.
+
+    Returns (q0 [.., R, C], s0, q1 [.., C, R], s1); scales are allocated
+    zero-filled in the requested layouts when not given.  A direction with
+    ``dim0=False`` / ``dim1=False`` returns None for its outputs.
+    """
+    torch = _torch()
+    squeeze = x.dim() == 2
+    B, R, C = (1,) + tuple(x.shape) if squeeze else tuple(x.shape)
+    E = offs.numel() if offs is not None else 0
+    if dim0:
+        q0 = _empty(x.shape, torch.uint8, x) if q0 is None else q0
+        s0 = _scale_buffer(s0_layout, B, R, C // 32, E, x) if s0 is None else s0
+    else:
+        q0 = s0 = None
+    if dim1:
+        q1 = _empty((C, R) if squeeze else (B, C, R), torch.uint8, x) if q1 is None else q1
+        s1 = _scale_buffer(s1_layout, B, C, R // 32, E, x) if s1 is None else s1
+    else:
+        q1 = s1 = None
+    _check("fp8moe_mxfp8_quantize_dual", _lib_raw().fp8moe_mxfp8_quantize_dual(
+        _ptr(x), B, R, C, _ptr(offs), E, _ptr(q0), _ptr(s0), s0_layout, _ptr(q1), _ptr(s1), s1_layout,
+        _stream(stream)))
+    return q0, s0, q1, s1
 
 
 def fp8moe_swizzle_scales_128x4(s, offs=None, group_axis: int = NO_GROUPS, E: Optional[int] = None,

@@ -123,6 +123,31 @@ fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, in
   return cuda_result(fp8moe::launch_mx_dim1(x, B, R, C, qt, scale, d->num_sms, d->status, (cudaStream_t)stream));
 }
 
+fp8moe_status fp8moe_mxfp8_quantize_dual(const void* x, int64_t B, int64_t R, int64_t C, const int32_t* offs,
+                                         int64_t E, void* q0, uint8_t* s0, int s0_layout, void* q1, uint8_t* s1,
+                                         int s1_layout, fp8moe_stream_t stream) {
+  if (B < 0 || R < 0 || C < 0 || E < 0) return FP8MOE_ERR_INVALID_ARG;
+  if (!q0 && !q1) return FP8MOE_ERR_INVALID_ARG;
+  if (C % 32 || (q1 && R % 32)) return FP8MOE_ERR_ALIGNMENT;
+  if ((q0 && !s0) || (q1 && !s1)) return FP8MOE_ERR_INVALID_ARG;
+  const bool ok0 = !q0 || s0_layout == FP8MOE_SCALES_ROWMAJOR || s0_layout == FP8MOE_NO_GROUPS ||
+                   s0_layout == FP8MOE_GROUP_ROWS;
+  const bool ok1 = !q1 || s1_layout == FP8MOE_SCALES_ROWMAJOR || s1_layout == FP8MOE_NO_GROUPS ||
+                   s1_layout == FP8MOE_GROUP_COLS;
+  if (!ok0 || !ok1) return FP8MOE_ERR_INVALID_ARG;
+  const bool grouped = (q0 && s0_layout == FP8MOE_GROUP_ROWS) || (q1 && s1_layout == FP8MOE_GROUP_COLS);
+  if (grouped && (B != 1 || E < 1 || E > 1024 || !offs)) return FP8MOE_ERR_INVALID_ARG;
+  if (grouped && ((uintptr_t)offs & 3)) return FP8MOE_ERR_ALIGNMENT;
+  if (B == 0 || R == 0 || C == 0) return FP8MOE_OK;
+  if (!x || !al16(x) || (q0 && !al16(q0)) || (q1 && !al16(q1))) return x ? FP8MOE_ERR_ALIGNMENT : FP8MOE_ERR_INVALID_ARG;
+  if (B > 65535 || R > ((int64_t)1 << 31) || C > ((int64_t)1 << 31)) return FP8MOE_ERR_INVALID_ARG;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  return cuda_result(fp8moe::launch_mx_dual(x, B, R, C, offs, grouped ? E : 0, q0, s0, s0_layout, q1, s1, s1_layout,
+                                            d->num_sms, d->status, (cudaStream_t)stream));
+}
+
 int64_t fp8moe_swizzled_scales_bytes(int64_t B, int64_t R, int64_t Cs, int64_t E, int group_axis) {
   if (B < 0 || R < 0 || Cs < 0 || E < 0) return -1;
   if (group_axis != FP8MOE_NO_GROUPS && group_axis != FP8MOE_GROUP_ROWS && group_axis != FP8MOE_GROUP_COLS)

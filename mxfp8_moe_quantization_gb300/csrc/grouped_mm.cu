@@ -26,6 +26,7 @@
 //  * the epilogue drains the accumulator to registers and releases TMEM before
 //    its global stores, so the next tile's MMAs overlap the stores.
 #include <cuda.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -34,17 +35,24 @@
 
 namespace fp8moe {
 
-constexpr int BM = 128, BN = 256, BK = 128, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int NUM_THREADS = 192;
 constexpr int A_STAGE_BYTES = BM * BK;            // 16 KB
-constexpr int B_STAGE_BYTES = BN * BK;            // 32 KB
 constexpr int SFA_STAGE_BYTES = 512;              // one 128x4 scale tile
 constexpr int SFB_STAGE_BYTES = 1024;             // two 128x4 scale tiles (256 rows)
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = 256;            // scale columns start after the accumulator
 
+// TWO = false: 1-CTA MMAs (M = 128 per CTA), the pair shares B tiles by TMA
+//               multicast; each CTA's shared memory holds the whole B tile.
+// TWO = true:  2-CTA MMAs (cta_group::2, M = 256 across the pair); each CTA
+//               holds its own 128 rows of A and its own half of B, halving the
+//               operand bytes each SM receives per MMA.
+template <bool TWO>
 struct SmemLayout {
+  static constexpr int STAGES = TWO ? 5 : 4;
+  static constexpr int B_STAGE_BYTES = TWO ? BN * BK / 2 : BN * BK;
   static constexpr int a = 0;
   static constexpr int b = a + STAGES * A_STAGE_BYTES;
   static constexpr int sfa = b + STAGES * B_STAGE_BYTES;
@@ -57,12 +65,65 @@ struct SmemLayout {
   static constexpr int stg = (blk_prefix + (MAX_GROUPS + 1) * 4 + 15) / 16 * 16;
   static constexpr int total = stg + 4 * 32 * 144;                    // per-warp 32 x (128 + 16) B
 };
-static_assert(SmemLayout::stg % 16 == 0, "staging must be 16-byte aligned");
-constexpr int SMEM_BYTES = SmemLayout::total + 1024;  // + alignment slack
+static_assert(SmemLayout<false>::stg % 16 == 0 && SmemLayout<true>::stg % 16 == 0, "staging alignment");
+template <bool TWO>
+constexpr int smem_bytes() { return SmemLayout<TWO>::total + 1024; }  // + alignment slack
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
+FP8MOE_DEV void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+template <bool TWO>
+FP8MOE_DEV void tc_commit_pair(uint64_t* bar) {
+  if constexpr (TWO) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)0x3)
+        : "memory");
+  } else {
+    tc_commit_mc(bar, 0x3);
+  }
+}
+FP8MOE_DEV uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// arrive on the mbarrier at the same offset in CTA `rank` of the cluster
+FP8MOE_DEV void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa_rank(smem_u32(bar), rank))
+               : "memory");
+}
+FP8MOE_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait for arrivals that come from the peer CTA (cluster scope)
+FP8MOE_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+  }
+}
+FP8MOE_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 FP8MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 FP8MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 FP8MOE_DEV void tc_commit(uint64_t* bar) {
@@ -94,30 +155,54 @@ FP8MOE_DEV uint64_t sdesc_sf(uint32_t saddr) {
 // Instruction descriptors.  Block-scaled e4m3 x e4m3 with e8m0 scales:
 // b scale id [4,6), A/B format E4M3 (0), K-major A and B, N>>3 at [17,23),
 // scale type UE8M0 (bit 23), M>>4 at [24,29), a scale id [29,31).
+template <int MM>
 FP8MOE_DEV uint32_t idesc_mx(uint32_t sf_id) {
-  return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+  return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(MM >> 4) << 24) | (sf_id << 29);
 }
 // Plain e4m3 x e4m3 with an fp32 accumulator (D format F32 = 1 at [4,6)).
+template <int MM>
 FP8MOE_DEV uint32_t idesc_f8() {
-  return (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+  return (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(MM >> 4) << 24);
 }
 
+template <bool TWO>
 FP8MOE_DEV void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
                        uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::"r"(
-          d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb));
+  if constexpr (TWO) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::
+            "r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb));
+  } else {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::
+            "r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb));
+  }
 }
+template <bool TWO>
 FP8MOE_DEV void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
+  if constexpr (TWO) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
+  } else {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
+  }
 }
+template <bool TWO>
 FP8MOE_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
+  if constexpr (TWO) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
+  } else {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
+  }
 }
 
 // 32 lanes x 32 bits, 32 consecutive columns -> 32 registers per thread.
@@ -162,8 +247,12 @@ struct Tile {
   int64_t sf_kblk; // first scale column block (in 128x4 tiles) of the contraction
 };
 
+// Tiles come in pairs: the two CTAs of a cluster take m-tiles 2i and 2i+1 of
+// the same group against the same B tile (shared through TMA multicast).  A
+// pair whose second m-tile lies past the group ("phantom", rows == 0) still
+// loads and releases its half of B but computes and stores nothing.
 template <bool WGRAD>
-FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* blk_prefix, int t) {
+FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* blk_prefix, int t, int rank) {
   const GemmArgs& g = p.g;
   // last group whose tile prefix is <= t
   int lo = 0, hi = g.E - 1, e = 0;
@@ -183,82 +272,100 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
   tl.e = e;
   if (!WGRAD) {
     const int mt = (int)((ge - gs + BM - 1) / BM);
-    const int ni = local / mt, mi = local % mt;   // n-major: neighbours share the B tile
+    const int mp = (mt + 1) / 2;
+    const int ni = local / mp, mi = 2 * (local % mp) + rank;   // n-major: neighbours share the B tile
     tl.row0 = gs + (int64_t)mi * BM;
     tl.rows = (ge - tl.row0) < BM ? (ge - tl.row0) : BM;
+    if (tl.rows < 0) tl.rows = 0;
     tl.col0 = (int64_t)ni * BN;
     tl.x0 = 0;
     tl.kvalid = g.kk;
     tl.sfa_blk = blk_prefix[e] + mi;
     tl.sf_kblk = 0;
   } else {
-    const int ni = local / p.m_tiles_w, mi = local % p.m_tiles_w;
+    const int pw = (p.m_tiles_w + 1) / 2;
+    const int ni = local / pw, mi = 2 * (local % pw) + rank;
     tl.row0 = (int64_t)mi * BM;
     tl.rows = (g.rows - tl.row0) < BM ? (g.rows - tl.row0) : BM;
+    if (tl.rows < 0) tl.rows = 0;
     tl.col0 = (int64_t)ni * BN;
     // MXFP8: groups are multiples of 32 and used in place; rowwise: the
     // 32-padded layout (blk_prefix holds the padded start)
     tl.x0 = g.recipe == FP8MOE_MXFP8 ? gs : (int64_t)blk_prefix[e];
     tl.kvalid = ge - gs;
-    tl.sfa_blk = mi;
+    tl.sfa_blk = mi < p.m_tiles_w ? mi : p.m_tiles_w - 1;   // a phantom reads a valid block
     tl.sf_kblk = g.recipe == FP8MOE_MXFP8 ? (int64_t)blk_prefix[e] : 0;
   }
   tl.nk = (int)((tl.kvalid + BK - 1) / BK);
   return tl;
 }
 
-template <bool MX, bool WGRAD>
+template <bool MX, bool WGRAD, bool TWO>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    k_grouped_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, KParams p) {
+    k_grouped_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB, KParams p) {
+  using L = SmemLayout<TWO>;
+  constexpr int STAGES = L::STAGES;
+  constexpr int B_STAGE_BYTES = L::B_STAGE_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* sA = smem + SmemLayout::a;
-  uint8_t* sB = smem + SmemLayout::b;
-  uint8_t* sSFA = smem + SmemLayout::sfa;
-  uint8_t* sSFB = smem + SmemLayout::sfb;
-  uint64_t* full = (uint64_t*)(smem + SmemLayout::bars);
+  uint8_t* sA = smem + L::a;
+  uint8_t* sB = smem + L::b;
+  uint8_t* sSFA = smem + L::sfa;
+  uint8_t* sSFB = smem + L::sfb;
+  uint64_t* full = (uint64_t*)(smem + L::bars);
   uint64_t* empty = full + STAGES;
   uint64_t* tmem_full = empty + STAGES;
   uint64_t* tmem_empty = tmem_full + 1;
-  uint32_t* tmem_base_holder = (uint32_t*)(smem + SmemLayout::misc);
-  volatile int* abort_flag = (volatile int*)(smem + SmemLayout::misc + 4);
-  int* total_tiles_s = (int*)(smem + SmemLayout::misc + 8);
-  float* colscale = (float*)(smem + SmemLayout::colscale);
-  int* tiles_prefix = (int*)(smem + SmemLayout::tiles_prefix);
-  int* blk_prefix = (int*)(smem + SmemLayout::blk_prefix);
+  uint32_t* tmem_base_holder = (uint32_t*)(smem + L::misc);
+  volatile int* abort_flag = (volatile int*)(smem + L::misc + 4);
+  int* total_tiles_s = (int*)(smem + L::misc + 8);
+  float* colscale = (float*)(smem + L::colscale);
+  int* tiles_prefix = (int*)(smem + L::tiles_prefix);
+  int* blk_prefix = (int*)(smem + L::blk_prefix);
 
   const GemmArgs& g = p.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)(blockIdx.x & 1);
 
   // ---- setup: barriers, TMEM, the device-side group schedule ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      // 1-CTA: released by the MMAs of both CTAs; 2-CTA: by the leader's MMA
+      mbar_init(&empty[s], TWO ? 1 : 2);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 4);
+    // 2-CTA: the leader's accumulator is free once both CTAs' epilogues drained
+    mbar_init(tmem_empty, TWO ? 8 : 4);
     *abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_base_holder)),
-                 "r"(TMEM_COLS));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    if constexpr (TWO) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_base_holder)),
+                   "r"(TMEM_COLS));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_base_holder)),
+                   "r"(TMEM_COLS));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
     tc_fence_before();
   }
-  // per-group tile counts and scale-block counts, then an exclusive scan
+  // per-group tile counts and scale-block counts, then a scan
   for (int e = threadIdx.x; e < g.E; e += NUM_THREADS) {
     const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
     const int64_t ge = g.offs[e];
     const int64_t sz = ge - gs;
     int nt, nb;
     if (!WGRAD) {
-      nt = (int)((sz + BM - 1) / BM) * p.n_tiles;
+      nt = (int)(((sz + BM - 1) / BM + 1) / 2) * p.n_tiles;
       nb = (int)((sz + BM - 1) / BM);
     } else {
-      nt = p.m_tiles_w * p.n_tiles;
+      nt = ((p.m_tiles_w + 1) / 2) * p.n_tiles;
       nb = MX ? (int)((sz + 127) / 128) : (int)((sz + 31) / 32 * 32);
     }
     tiles_prefix[e + 1] = sz < 0 ? 0 : nt;
@@ -303,25 +410,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (bad && blockIdx.x == 0) set_status(g.status, FP8MOE_ERR_DEVICE_OFFSETS);
     }
   }
-  // exclusive prefix: tiles_prefix[e] = tiles of groups < e (shift by reading e)
   __syncthreads();
+  // barriers of both CTAs are initialised before any cross-CTA arrival
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_holder;
   const int total_tiles = *total_tiles_s;
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
 
   if (warp == 0 && lane == 0) {
     // ======================= TMA producer =======================
     int stage = 0;
     uint32_t phase = 0;
-    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+    for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
       for (int ks = 0; ks < tl.nk; ++ks) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
           set_status(g.status, FP8MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           break;
         }
-        uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES;
+        // 1-CTA: own A + both halves of B (one of them multicast by the peer);
+        // 2-CTA: own A + own half of B
+        uint32_t bytes = A_STAGE_BYTES + (TWO ? B_STAGE_BYTES : B_STAGE_BYTES);
         const uint8_t* sfa_src = nullptr;
         const uint8_t* sfb_src0 = nullptr;
         const uint8_t* sfb_src1 = nullptr;
@@ -331,22 +442,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int64_t nb0 = tl.col0 / 128;
           const int64_t nbl = WGRAD ? (g.cols + 127) / 128 : p.b_rows_pad / 128;
           const uint8_t* bsf = (const uint8_t*)g.b_scale + (WGRAD ? 0 : (int64_t)tl.e * p.b_rows_pad * p.cpb * 4);
+          // both 128-row scale tiles of B (in 2-CTA mode each CTA's TMEM holds
+          // the scales of all 256 columns)
           sfb_src0 = bsf + (nb0 * p.cpb + kb) * 512;
           sfb_src1 = nb0 + 1 < nbl ? bsf + ((nb0 + 1) * p.cpb + kb) * 512 : nullptr;
           bytes += 512 + 512 + (sfb_src1 ? 512 : 0);
         }
-        mbar_expect_tx(&full[stage], bytes);
         const int x = (int)(tl.x0 + (int64_t)ks * BK);
-        tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, &full[stage], x, (int)tl.row0);
-        if (WGRAD) {
-          tma_load_2d(sB + stage * B_STAGE_BYTES, &tmB, &full[stage], x, (int)tl.col0);
+        const int brow = (int)(tl.col0 + rank * (BN / 2));
+        if constexpr (TWO) {
+          // both CTAs' loads complete on the leader's full barrier, which
+          // expects the bytes of the pair (both CTAs load the same amounts)
+          const uint32_t fb = mapa_rank(smem_u32(&full[stage]), 0);
+          if (rank == 0) mbar_expect_tx(&full[stage], 2 * bytes);
+          tma_load_2d_cg2(sA + stage * A_STAGE_BYTES, &tmA, fb, x, (int)tl.row0);
+          uint8_t* bdst = sB + stage * B_STAGE_BYTES;
+          if (WGRAD) {
+            tma_load_2d_cg2(bdst, &tmB, fb, x, brow);
+          } else {
+            tma_load_3d_cg2(bdst, &tmB, fb, x, brow, tl.e);
+          }
+          if (MX) {
+            // scale tiles as 1-D boxes of 128 u32 (= one 512-byte 128x4 tile)
+            const uint8_t* sa0 = (const uint8_t*)g.a_scale;
+            const uint8_t* sb0 = (const uint8_t*)g.b_scale;
+            tma_load_1d_cg2(sSFA + stage * SFA_STAGE_BYTES, &tmSFA, fb, (int)((sfa_src - sa0) / 4));
+            tma_load_1d_cg2(sSFB + stage * SFB_STAGE_BYTES, &tmSFB, fb, (int)((sfb_src0 - sb0) / 4));
+            if (sfb_src1)
+              tma_load_1d_cg2(sSFB + stage * SFB_STAGE_BYTES + 512, &tmSFB, fb, (int)((sfb_src1 - sb0) / 4));
+          }
         } else {
-          tma_load_3d(sB + stage * B_STAGE_BYTES, &tmB, &full[stage], x, (int)tl.col0, tl.e);
-        }
-        if (MX) {
-          bulk_load(sSFA + stage * SFA_STAGE_BYTES, sfa_src, 512, &full[stage]);
-          bulk_load(sSFB + stage * SFB_STAGE_BYTES, sfb_src0, 512, &full[stage]);
-          if (sfb_src1) bulk_load(sSFB + stage * SFB_STAGE_BYTES + 512, sfb_src1, 512, &full[stage]);
+          mbar_expect_tx(&full[stage], bytes);
+          tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, &full[stage], x, (int)tl.row0);
+          // this CTA's half of the B tile goes to both CTAs of the pair
+          uint8_t* bdst = sB + stage * B_STAGE_BYTES + rank * (B_STAGE_BYTES / 2);
+          if (WGRAD) {
+            tma_load_2d_mc(bdst, &tmB, &full[stage], x, brow, 0x3);
+          } else {
+            tma_load_3d_mc(bdst, &tmB, &full[stage], x, brow, tl.e, 0x3);
+          }
+          if (MX) {
+            bulk_load(sSFA + stage * SFA_STAGE_BYTES, sfa_src, 512, &full[stage]);
+            bulk_load(sSFB + stage * SFB_STAGE_BYTES, sfb_src0, 512, &full[stage]);
+            if (sfb_src1) bulk_load(sSFB + stage * SFB_STAGE_BYTES + 512, sfb_src1, 512, &full[stage]);
+          }
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -354,15 +493,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
+    // drain: every release of this CTA's stages has arrived before the pair
+    // may exit (releases can come from the peer CTA)
+    for (int i = 0; i < STAGES && !*abort_flag; ++i) {
+      if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+        set_status(g.status, FP8MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+  } else if (warp == 1 && lane == 0 && TWO && rank == 1) {
+    // 2-CTA peer: the leader issues every MMA of the pair; nothing to do here
   } else if (warp == 1 && lane == 0) {
     // ======================= MMA issuer =======================
+    constexpr int MM = TWO ? 2 * BM : BM;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+    for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
       if (tl.nk == 0) continue;
-      if (!mbar_wait(tmem_empty, acc_phase ^ 1, abort_flag)) {
+      if (!TWO && tl.rows == 0) {
+        // phantom: release each stage for the pair without computing
+        bool ok = true;
+        for (int ks = 0; ks < tl.nk; ++ks) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            set_status(g.status, FP8MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_commit_mc(&empty[stage], 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        continue;
+      }
+      const bool acc_ok = TWO ? mbar_wait_cluster(tmem_empty, acc_phase ^ 1, abort_flag)
+                              : mbar_wait(tmem_empty, acc_phase ^ 1, abort_flag);
+      if (!acc_ok) {
         set_status(g.status, FP8MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -382,9 +557,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t b_addr = smem_u32(sB + stage * B_STAGE_BYTES);
         const uint32_t sf_col = tmem_base + TMEM_SF_BASE + stage * 16;
         if (MX) {
-          tc_cp_sf(sf_col, sdesc_sf(smem_u32(sSFA + stage * SFA_STAGE_BYTES)));
-          tc_cp_sf(sf_col + 4, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES)));
-          tc_cp_sf(sf_col + 8, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES + 512)));
+          tc_cp_sf<TWO>(sf_col, sdesc_sf(smem_u32(sSFA + stage * SFA_STAGE_BYTES)));
+          tc_cp_sf<TWO>(sf_col + 4, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES)));
+          tc_cp_sf<TWO>(sf_col + 8, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES + 512)));
         }
         const int64_t rem = tl.kvalid - (int64_t)ks * BK;
         const int nsub = rem >= BK ? 4 : (int)((rem + 31) / 32);
@@ -392,29 +567,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int k = 0; k < nsub; ++k) {
           const uint32_t accum = (ks > 0 || k > 0) ? 1u : 0u;
           if (MX) {
-            mma_mx(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_mx((uint32_t)k), sf_col,
-                   sf_col + 4, accum);
+            mma_mx<TWO>(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_mx<MM>((uint32_t)k),
+                        sf_col, sf_col + 4, accum);
           } else {
-            mma_f8(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8(), accum);
+            mma_f8<TWO>(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8<MM>(), accum);
           }
         }
-        tc_commit(&empty[stage]);
+        tc_commit_pair<TWO>(&empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
         }
       }
       if (!ok) break;
-      tc_commit(tmem_full);
+      if constexpr (TWO) {
+        tc_commit_pair<true>(tmem_full);
+      } else {
+        tc_commit(tmem_full);
+      }
     }
   } else if (warp >= 2) {
     // ======================= epilogue =======================
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int et = threadIdx.x - 64;
-    uint8_t* stg = smem + SmemLayout::stg + (warp - 2) * 32 * 144;
+    uint8_t* stg = smem + L::stg + (warp - 2) * 32 * 144;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+    auto release_acc = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (TWO && rank == 1) {
+          mbar_arrive_remote(tmem_empty, 0);
+        } else {
+          mbar_arrive(tmem_empty);
+        }
+      }
+    };
+    for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+      if (!TWO && tl.rows == 0) continue;  // phantom of a 1-CTA pair: nothing computed
       const int64_t lrow = quarter * 32 + lane;
       const bool row_ok = lrow < tl.rows;
       const int64_t ncols = (g.cols - tl.col0) < BN ? (g.cols - tl.col0) : BN;
@@ -431,7 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
       float rscale = 1.0f;
-      if (!MX) {
+      if (!MX && tl.rows > 0) {
         // column scales of this tile into shared memory, row scale per thread
         asm volatile("bar.sync 1, 128;" ::: "memory");
         const float* cs = (const float*)g.b_scale + (int64_t)tl.e * g.cols + tl.col0;
@@ -449,6 +640,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       acc_phase ^= 1;
       tc_fence_after();
+      if (tl.rows == 0) {  // 2-CTA phantom half: nothing to store
+        release_acc();
+        continue;
+      }
       uint32_t packed[BN / 2];
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
@@ -466,10 +661,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           packed[(c + j) / 2] = pack_bf16(v0, v1);
         }
       }
-      // accumulator drained: let the MMA warp start the next tile
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty);
+      // accumulator drained: let the MMA start the next tile
+      release_acc();
       // Coalesced stores: 64-column slices of this warp's 32 rows go through a
       // padded shared-memory buffer (row pitch 144 B: conflict-free both ways),
       // then each store instruction writes 4 rows x 128 contiguous bytes.
@@ -496,9 +689,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+    if constexpr (TWO) {
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+    } else {
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+    }
   }
 }
 
@@ -510,20 +708,32 @@ static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_
   return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides, box);
 }
 
-template <bool MX, bool WGRAD>
-static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& p, int grid,
-                            cudaStream_t st) {
-  auto kern = k_grouped_mm<MX, WGRAD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+template <bool MX, bool WGRAD, bool TWO>
+static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                            const CUtensorMap& tsb, const KParams& p, int grid, cudaStream_t st) {
+  auto kern = k_grouped_mm<MX, WGRAD, TWO>;
+  constexpr int SMEM = smem_bytes<TWO>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
 }
 
 cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   if (g.E > MAX_GROUPS) return cudaErrorNotSupported;
   if (g.kk > INT32_MAX || g.rows > INT32_MAX || g.cols > INT32_MAX || g.M > INT32_MAX) return cudaErrorInvalidValue;
-  if (SMEM_BYTES > g.max_smem) return cudaErrorNotSupported;
+  if (smem_bytes<true>() > g.max_smem || smem_bytes<false>() > g.max_smem) return cudaErrorNotSupported;
   const bool mx = g.recipe == FP8MOE_MXFP8;
   const bool wgrad = g.mode == GEMM_WGRAD;
   KParams p;
@@ -548,27 +758,61 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   if (wgrad) {
     cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)g.cols};
     cuuint64_t strides[1] = {(cuuint64_t)g.kk};
-    cuuint32_t box[2] = {BK, BN};
+    cuuint32_t box[2] = {BK, BN / 2};
     if (!make_map(&tb, g.b, 2, dims, strides, box)) return cudaErrorInvalidValue;
   } else {
     cuuint64_t dims[3] = {(cuuint64_t)g.kk, (cuuint64_t)g.cols, (cuuint64_t)g.E};
     cuuint64_t strides[2] = {(cuuint64_t)g.kk, (cuuint64_t)(g.kk * g.cols)};
-    cuuint32_t box[3] = {BK, BN, 1};
+    cuuint32_t box[3] = {BK, BN / 2, 1};
     if (!make_map(&tb, g.b, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
   // tiles are only known on the device; size the grid by an upper bound
   int64_t bound;
+  // (pairs of tiles; each pair runs on a 2-CTA cluster)
   if (!wgrad) {
-    bound = ((g.M + BM - 1) / BM + g.E) * p.n_tiles;
+    bound = ((g.M + 2 * BM - 1) / (2 * BM) + g.E) * p.n_tiles;
   } else {
-    bound = (int64_t)g.E * p.m_tiles_w * p.n_tiles;
+    bound = (int64_t)g.E * ((p.m_tiles_w + 1) / 2) * p.n_tiles;
   }
-  int grid = (int)(bound < g.num_sms ? bound : g.num_sms);
-  if (grid < 1) grid = 1;
+  const int64_t max_pairs = g.num_sms / 2;
+  int grid = 2 * (int)(bound < max_pairs ? bound : max_pairs);
+  if (grid < 2) grid = 2;
+  // MXFP8 scale buffers as 1-D u32 tensors (the 2-CTA producer loads scale
+  // tiles with TMA so that they can complete on the leader's barrier)
+  CUtensorMap tsa = ta, tsb = ta;
   if (mx) {
-    return wgrad ? launch_t<true, true>(ta, tb, p, grid, st) : launch_t<true, false>(ta, tb, p, grid, st);
+    int64_t sa_bytes, sb_bytes;
+    if (!wgrad) {
+      sa_bytes = ((g.M + 127) / 128 + g.E) * 128 * p.cpb * 4;
+      sb_bytes = (int64_t)g.E * p.b_rows_pad * p.cpb * 4;
+    } else {
+      sa_bytes = (g.rows + 127) / 128 * 128 * p.cpb * 4;
+      sb_bytes = (g.cols + 127) / 128 * 128 * p.cpb * 4;
+    }
+    cuuint64_t da[1] = {(cuuint64_t)(sa_bytes / 4)}, db[1] = {(cuuint64_t)(sb_bytes / 4)};
+    cuuint64_t unused_stride[1] = {(cuuint64_t)16};
+    cuuint32_t box[1] = {128};
+    if (!make_tmap(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.a_scale, 1, da, unused_stride, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.b_scale, 1, db, unused_stride, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
   }
-  return wgrad ? launch_t<false, true>(ta, tb, p, grid, st) : launch_t<false, false>(ta, tb, p, grid, st);
+  // 2-CTA MMAs unless FP8MOE_GEMM_1CTA=1 (the 1-CTA + multicast variant)
+  static const bool two = [] {
+    const char* v = getenv("FP8MOE_GEMM_1CTA");
+    return !(v && v[0] == '1');
+  }();
+  if (two) {
+    if (mx) return wgrad ? launch_t<true, true, true>(ta, tb, tsa, tsb, p, grid, st)
+                         : launch_t<true, false, true>(ta, tb, tsa, tsb, p, grid, st);
+    return wgrad ? launch_t<false, true, true>(ta, tb, tsa, tsb, p, grid, st)
+                 : launch_t<false, false, true>(ta, tb, tsa, tsb, p, grid, st);
+  }
+  if (mx) return wgrad ? launch_t<true, true, false>(ta, tb, tsa, tsb, p, grid, st)
+                       : launch_t<true, false, false>(ta, tb, tsa, tsb, p, grid, st);
+  return wgrad ? launch_t<false, true, false>(ta, tb, tsa, tsb, p, grid, st)
+               : launch_t<false, false, false>(ta, tb, tsa, tsb, p, grid, st);
 }
 
 }  // namespace fp8moe

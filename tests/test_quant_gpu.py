@@ -252,3 +252,74 @@ def test_swizzle_bad_offsets_set_status(F):
     F.fp8moe_swizzle_scales_128x4(s, torch.tensor([40, 64], dtype=torch.int32, device=DEV), F.GROUP_COLS)
     assert F.fp8moe_get_device_status() == 5     # 40 is not a multiple of 32
     assert F.fp8moe_get_device_status() == 0
+
+
+# ----------------------------------------------------------------------------
+# dual-direction MXFP8 with scales written in their final layout
+# ----------------------------------------------------------------------------
+
+def _mx_ref(x_np):
+    q0, s0 = OQ.mxfp8_quantize_dim0(x_np)
+    q1, s1 = OQ.mxfp8_quantize_dim1(x_np)
+    return q0, s0, q1, s1
+
+
+@pytest.mark.parametrize("shape", [(1024, 256), (96, 96), (32, 64), (160, 5120)])
+def test_mx_dual_rowmajor(F, shape):
+    x = _bf16(shape, sum(shape) + 7, 2.0)
+    q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), None, F.SCALES_ROWMAJOR, F.SCALES_ROWMAJOR)
+    r0, rs0, r1, rs1 = _mx_ref(_np(x))
+    assert np.array_equal(q0.cpu().numpy(), r0) and np.array_equal(s0.cpu().numpy(), rs0)
+    assert np.array_equal(q1.cpu().numpy(), r1) and np.array_equal(s1.cpu().numpy(), rs1)
+
+
+@pytest.mark.parametrize("shape", [(4, 512, 256), (3, 96, 160), (1, 256, 5120)])
+def test_mx_dual_batched_swizzled(F, shape):
+    x = _bf16(shape, sum(shape) + 8, 0.05)
+    q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), None, F.NO_GROUPS, F.NO_GROUPS)
+    r0, rs0, r1, rs1 = _mx_ref(_np(x))
+    assert np.array_equal(q0.cpu().numpy(), r0)
+    assert np.array_equal(q1.cpu().numpy(), r1)
+    assert np.array_equal(s0.cpu().numpy(), OS.swizzle(rs0))
+    assert np.array_equal(s1.cpu().numpy(), OS.swizzle(rs1))
+
+
+@pytest.mark.parametrize("sizes", [[96, 0, 0, 928], [64, 0, 352, 32, 160], [0, 0, 64], [32]])
+def test_mx_dual_grouped(F, sizes):
+    M = int(sum(sizes))
+    x = _bf16((M, 192), M + 9, 1.5)
+    offs = W.offsets_from_sizes(sizes)
+    q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), torch.from_numpy(offs).to(DEV), F.GROUP_ROWS,
+                                                  F.GROUP_COLS)
+    r0, rs0, r1, rs1 = _mx_ref(_np(x))
+    assert np.array_equal(q0.cpu().numpy(), r0)
+    assert np.array_equal(q1.cpu().numpy(), r1)
+    assert np.array_equal(s0.cpu().numpy(), OS.swizzle(rs0, offs, OS.GROUP_ROWS))
+    assert np.array_equal(s1.cpu().numpy(), OS.swizzle(rs1, offs, OS.GROUP_COLS))
+    assert F.fp8moe_get_device_status() == 0
+
+
+def test_mx_dual_single_direction(F):
+    x = _bf16((256, 128), 5, 1.0)
+    q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), None, F.SCALES_ROWMAJOR, F.NO_GROUPS, dim1=False)
+    r0, rs0, _, _ = _mx_ref(_np(x))
+    assert q1 is None and np.array_equal(q0.cpu().numpy(), r0) and np.array_equal(s0.cpu().numpy(), rs0)
+    q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), None, F.NO_GROUPS, F.SCALES_ROWMAJOR, dim0=False)
+    _, _, r1, rs1 = _mx_ref(_np(x))
+    assert q0 is None and np.array_equal(q1.cpu().numpy(), r1) and np.array_equal(s1.cpu().numpy(), rs1)
+
+
+def test_mx_dual_tie_points(F):
+    x = _mx_tie_blocks(256, 256, 6)
+    q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), None, F.SCALES_ROWMAJOR, F.SCALES_ROWMAJOR)
+    r0, rs0, r1, rs1 = _mx_ref(_np(x))
+    assert np.array_equal(q0.cpu().numpy(), r0) and np.array_equal(s0.cpu().numpy(), rs0)
+    assert np.array_equal(q1.cpu().numpy(), r1) and np.array_equal(s1.cpu().numpy(), rs1)
+
+
+def test_mx_dual_bad_offsets(F):
+    x = torch.zeros(128, 64, dtype=torch.bfloat16, device=DEV)
+    F.fp8moe_mxfp8_quantize_dual(x, torch.tensor([64, 32, 128], dtype=torch.int32, device=DEV), F.GROUP_ROWS,
+                                 F.GROUP_COLS)
+    assert F.fp8moe_get_device_status() == 5
+    assert F.fp8moe_get_device_status() == 0
