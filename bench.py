@@ -36,6 +36,25 @@ WORKLOAD = "scout"
 METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)"
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMM
+# kernel, averaged over one fwd, dgrad and wgrad launch of the Scout layer,
+# from the ncu capture summarised in profiles/k_grouped_mm_scout.md.  It is
+# reported only while the kernel source is the one that was captured.
+GEMM_TRAFFIC = {"source": "mxfp8_moe_quantization_gb300/csrc/grouped_mm.cu",
+                "sha256": "c1a50cf21246198e856f78c40b3320a0c6288d54c7fae215055d4eab99a11fd2",
+                "bytes_per_launch": (1031.354e6 + 1075.521e6 + 1569.749e6) / 3}
+
+
+def gemm_traffic():
+    import hashlib
+    path = os.path.join(ROOT, GEMM_TRAFFIC["source"])
+    try:
+        h = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return GEMM_TRAFFIC["bytes_per_launch"] if h == GEMM_TRAFFIC["sha256"] else None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -117,7 +136,9 @@ class ScoutStep:
             a = W.make_activations(wl, aname, device=device)
             dy = W.make_activations(wl, dname, device=device)
             self.layers.append(self._alloc(w, a, dy))
-        self.launches_per_step = (6 if fused else 15) * len(self.layers)
+        # fused: 3 quantize calls (2 kernels each: dim0 and dim1 with final-layout
+        # scales) + 3 GEMMs per weight; unfused: 6 quantize + 6 swizzle + 3 GEMMs
+        self.launches_per_step = (9 if fused else 15) * len(self.layers)
 
     def _alloc(self, w, a, dy):
         import torch
@@ -158,19 +179,18 @@ class ScoutStep:
     def quant_bytes(self):
         """Algorithmic HBM bytes of the quantization launches per step.
 
-        Fused: each of A, W, dY is read once (2 B/element) and written twice
-        (1 B of codes per direction) with one scale byte per 32 elements per
-        direction.  Unfused: dim0 and dim1 each read the tensor (2 + 1 B per
-        element + 1/32), and the swizzle reads and writes every scale byte.
+        Each of A, W, dY is quantized along both dimensions; each direction
+        reads the tensor (2 B/element) and writes codes (1 B) and one scale
+        byte per 32 elements.  Unfused, the swizzle additionally reads and
+        writes every scale byte.
         """
         tot = 0.0
         for L in self.layers:
             M, N, K, E = self.M, L["N"], L["K"], self.E
             elems = M * K + E * N * K + M * N               # A, W, dY
-            if self.fused:
-                tot += elems * (2 + 2 + 2 / 32)
-            else:
-                tot += elems * 2 * (3 + 1 / 32) + elems * 2 / 32 * 2
+            tot += elems * 2 * (3 + 1 / 32)
+            if not self.fused:
+                tot += elems * 2 / 32 * 2
         return tot
 
     def quant_elements(self):
@@ -412,7 +432,7 @@ def main():
             "quant_frac_hbm": qbytes / (quant_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "gemm_ms_per_step": gemm_ms, "quant_ms_per_step": quant_ms,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                         "frac": achieved / fp8_peak, "traffic": None,
+                         "frac": achieved / fp8_peak, "traffic": gemm_traffic(),
                          "kernel": "k_grouped_mm<MX=true>", "peak_source":
                              f"{peak_kind}: 2 x bf16_tflops (nominal fp8/bf16 dense ratio)"},
             "clocks": clk.summary(),

@@ -135,12 +135,13 @@ fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, in
                                          void* qt, uint8_t* scale, fp8moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * MXFP8 quantization along both dimensions from one read of x, with the
- * scales written directly in their final layout.  [SCOUT] section details:
- * forward and backward each quantize the same tensors (activations, weights,
- * gradients) along the dimension their GEMM contracts over, and the scales go
- * to the 128x4 layout; [AMD-FP8] aixai.ru "Три уровня оптимизации": one fused
- * kernel instead of separate passes through HBM.
+ * MXFP8 quantization along either or both dimensions, with the scales
+ * written directly in the layout the grouped GEMM consumes (no separate
+ * swizzle pass).  [SCOUT] section details: forward and backward quantize the
+ * same tensors (activations, weights, gradients) along the dimension their
+ * GEMM contracts over, and the scales go to the 128x4 layout; [AMD-FP8]
+ * aixai.ru "Три уровня оптимизации": fewer passes through HBM.  Each
+ * requested direction is one fused pass over x.
  *
  * x [B, R, C] bf16 contiguous, R % 32 == 0 (when dim1 is produced), C % 32 == 0.
  * Either direction may be skipped by passing NULL codes.

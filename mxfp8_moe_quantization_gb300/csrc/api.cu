@@ -106,7 +106,8 @@ fp8moe_status fp8moe_mxfp8_quantize_dim0(const void* x, int64_t B, int64_t R, in
   DevInfo* d;
   fp8moe_status st = device_info(&d);
   if (st) return st;
-  return cuda_result(fp8moe::launch_mx_dim0(x, B * R, C, q, scale, d->num_sms, (cudaStream_t)stream));
+  return cuda_result(fp8moe::launch_mx_dim0(x, B, R, C, q, scale, FP8MOE_SCALES_ROWMAJOR, nullptr, 0, d->num_sms,
+                                            d->status, (cudaStream_t)stream));
 }
 
 fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt,
@@ -120,7 +121,8 @@ fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, in
   DevInfo* d;
   fp8moe_status st = device_info(&d);
   if (st) return st;
-  return cuda_result(fp8moe::launch_mx_dim1(x, B, R, C, qt, scale, d->num_sms, d->status, (cudaStream_t)stream));
+  return cuda_result(fp8moe::launch_mx_dim1(x, B, R, C, qt, scale, FP8MOE_SCALES_ROWMAJOR, nullptr, 0, d->num_sms,
+                                            d->status, (cudaStream_t)stream));
 }
 
 fp8moe_status fp8moe_mxfp8_quantize_dual(const void* x, int64_t B, int64_t R, int64_t C, const int32_t* offs,
@@ -144,8 +146,21 @@ fp8moe_status fp8moe_mxfp8_quantize_dual(const void* x, int64_t B, int64_t R, in
   DevInfo* d;
   fp8moe_status st = device_info(&d);
   if (st) return st;
-  return cuda_result(fp8moe::launch_mx_dual(x, B, R, C, offs, grouped ? E : 0, q0, s0, s0_layout, q1, s1, s1_layout,
-                                            d->num_sms, d->status, (cudaStream_t)stream));
+  // one launch per direction: each reads x once; both write their scales in
+  // the final layout (measured faster than a single-read kernel producing
+  // both directions, whose per-tile work is twice as long)
+  const int64_t Eg = grouped ? E : 0;
+  if (q0) {
+    cudaError_t e = fp8moe::launch_mx_dim0(x, B, R, C, q0, s0, s0_layout, offs, Eg, d->num_sms, d->status,
+                                           (cudaStream_t)stream);
+    if (e != cudaSuccess) return FP8MOE_ERR_CUDA;
+  }
+  if (q1) {
+    cudaError_t e = fp8moe::launch_mx_dim1(x, B, R, C, q1, s1, s1_layout, offs, Eg, d->num_sms, d->status,
+                                           (cudaStream_t)stream);
+    if (e != cudaSuccess) return FP8MOE_ERR_CUDA;
+  }
+  return FP8MOE_OK;
 }
 
 int64_t fp8moe_swizzled_scales_bytes(int64_t B, int64_t R, int64_t Cs, int64_t E, int group_axis) {

@@ -36,7 +36,7 @@
 namespace fp8moe {
 
 constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 192;  // producer, MMA, 4 epilogue warps
 constexpr int A_STAGE_BYTES = BM * BK;            // 16 KB
 constexpr int SFA_STAGE_BYTES = 512;              // one 128x4 scale tile
 constexpr int SFB_STAGE_BYTES = 1024;             // two 128x4 scale tiles (256 rows)
@@ -513,6 +513,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_phase = 0;
+    auto stage_ready = [&]() -> bool { return mbar_wait(&full[stage], phase, abort_flag); };
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
       const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
       if (tl.nk == 0) continue;
@@ -520,7 +521,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // phantom: release each stage for the pair without computing
         bool ok = true;
         for (int ks = 0; ks < tl.nk; ++ks) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          if (!stage_ready()) {
             set_status(g.status, FP8MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             ok = false;
@@ -546,7 +547,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       bool ok = true;
       for (int ks = 0; ks < tl.nk; ++ks) {
-        if (!mbar_wait(&full[stage], phase, abort_flag)) {
+        if (!stage_ready()) {
           set_status(g.status, FP8MOE_ERR_TIMEOUT);
           *abort_flag = 1;
           ok = false;
@@ -798,10 +799,11 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
                    CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
-  // 2-CTA MMAs unless FP8MOE_GEMM_1CTA=1 (the 1-CTA + multicast variant)
+  // 1-CTA MMAs with B multicast by default (measured the faster of the two on
+  // the Scout shapes); FP8MOE_GEMM_2CTA=1 selects the cta_group::2 variant
   static const bool two = [] {
-    const char* v = getenv("FP8MOE_GEMM_1CTA");
-    return !(v && v[0] == '1');
+    const char* v = getenv("FP8MOE_GEMM_2CTA");
+    return v && v[0] == '1';
   }();
   if (two) {
     if (mx) return wgrad ? launch_t<true, true, true>(ta, tb, tsa, tsb, p, grid, st)

@@ -13,13 +13,12 @@ SwizzleGeom swizzle_geom(int64_t R, int64_t Cs, int64_t E, int group_axis);
 
 cudaError_t launch_quant_rowwise(const void* x, int64_t R, int64_t C, int64_t ldx, int kind, void* q,
                                  float* inv, cudaStream_t st);
-cudaError_t launch_mx_dim0(const void* x, int64_t rows, int64_t C, void* q, uint8_t* s, int num_sms,
-                           cudaStream_t st);
-cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s, int num_sms,
-                           int* status, cudaStream_t st);
-cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, const int32_t* offs, int64_t E, void* q0,
-                           uint8_t* s0, int s0_layout, void* q1, uint8_t* s1, int s1_layout, int num_sms, int* status,
-                           cudaStream_t st);
+// MXFP8 quantization; scales written in `layout` (FP8MOE_SCALES_ROWMAJOR,
+// FP8MOE_NO_GROUPS = 128x4 per batch, FP8MOE_GROUP_ROWS / _COLS with offs).
+cudaError_t launch_mx_dim0(const void* x, int64_t B, int64_t R, int64_t C, void* q, uint8_t* s, int layout,
+                           const int32_t* offs, int64_t E, int num_sms, int* status, cudaStream_t st);
+cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s, int layout,
+                           const int32_t* offs, int64_t E, int num_sms, int* status, cudaStream_t st);
 cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                            int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
                            int max_smem, cudaStream_t st);

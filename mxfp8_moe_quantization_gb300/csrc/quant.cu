@@ -143,11 +143,126 @@ cudaError_t launch_quant_rowwise(const void* x, int64_t R, int64_t C, int64_t ld
 }
 
 // ============================================================================
+// Scale output in its final layout (row-major, or the 128x4 tcgen05 tiles,
+// plain / batched or grouped by routing offsets).  Grouped layouts need, per
+// group, its end and its padded start: built per CTA in shared memory with a
+// block-wide scan of the offsets (which are also validated).
+// ============================================================================
+constexpr int QG_MAX = 1024;
+
+struct ScaleSpec {
+  uint8_t* p;
+  int layout;      // FP8MOE_SCALES_ROWMAJOR, FP8MOE_NO_GROUPS, FP8MOE_GROUP_ROWS / _COLS
+  int64_t Rp, Cp;  // padded geometry of one (batch's) swizzled matrix
+  const int32_t* offs;
+  int E;
+};
+
+struct GroupTable {
+  int64_t end[QG_MAX];
+  int64_t pad[QG_MAX];
+  int bad;
+};
+
+FP8MOE_DEV int64_t tile_off(int64_t r, int64_t c, int64_t Cp) {
+  return ((r >> 7) * (Cp >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
+}
+
+// first group whose end is > key
+FP8MOE_DEV int find_group(const int64_t* ends, int E, int64_t key) {
+  int lo = 0, hi = E - 1, g = E - 1;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (ends[mid] > key) {
+      g = mid;
+      hi = mid - 1;
+    } else {
+      lo = mid + 1;
+    }
+  }
+  return g;
+}
+
+// rows mode: pad = sum of earlier group sizes rounded up to 128 rows;
+// cols mode: pad = sum of earlier group sizes / 32 rounded up to 4 columns.
+// Call with all threads of a block of 256; ends with __syncthreads.
+__device__ void build_group_table(GroupTable& t, const int32_t* offs, int E, int64_t total, bool cols_mode,
+                                  int* status) {
+  __shared__ int64_t wsum[8];
+  const int tid = threadIdx.x;
+  const int per = (E + 255) / 256;  // <= 4
+  int64_t u[4] = {0, 0, 0, 0};
+  int64_t sum = 0;
+  int bad = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = tid * per + i;
+    if (e >= E) break;
+    const int64_t end = offs[e];
+    const int64_t start = e == 0 ? 0 : offs[e - 1];
+    if (end < start || end > total || (e == E - 1 && end != total)) bad = 1;
+    if (cols_mode && (end % 32)) bad = 1;
+    const int64_t sz = end - start;
+    u[i] = cols_mode ? ((sz / 32 + 3) / 4 * 4) : ((sz + 127) / 128 * 128);
+    sum += u[i];
+    t.end[e] = end;
+  }
+  // block exclusive scan of the per-thread sums
+  const int lane = tid & 31, warp = tid >> 5;
+  int64_t incl = sum;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  bad = __syncthreads_or(bad);
+  int64_t base = 0;
+  for (int w = 0; w < warp; ++w) base += wsum[w];
+  int64_t run = base + incl - sum;
+  for (int i = 0; i < per; ++i) {
+    const int e = tid * per + i;
+    if (e >= E) break;
+    t.pad[e] = run;
+    run += u[i];
+  }
+  if (tid == 0) {
+    t.bad = bad;
+    if (bad) set_status(status, FP8MOE_ERR_DEVICE_OFFSETS);
+  }
+  __syncthreads();
+}
+
+// Byte offset of scale (row, col) of batch b.  For GROUP_ROWS the row is an
+// element row of x (grouped over R); for GROUP_COLS the column is a 32-block
+// index along the grouped contracting dimension.
+FP8MOE_DEV int64_t scale_offset(const ScaleSpec& s, const GroupTable* gt, int64_t b, int64_t row, int64_t col,
+                                int64_t rows_per_batch, int64_t cols) {
+  if (s.layout == FP8MOE_SCALES_ROWMAJOR) return (b * rows_per_batch + row) * cols + col;
+  if (s.layout == FP8MOE_NO_GROUPS) return b * s.Rp * s.Cp + tile_off(row, col, s.Cp);
+  if (s.layout == FP8MOE_GROUP_ROWS) {
+    const int g = find_group(gt->end, s.E, row);
+    const int64_t gs = g == 0 ? 0 : gt->end[g - 1];
+    return tile_off(gt->pad[g] + (row - gs), col, s.Cp);
+  }
+  const int g = find_group(gt->end, s.E, col * 32);
+  const int64_t gs = g == 0 ? 0 : gt->end[g - 1];
+  return tile_off(row, gt->pad[g] + (col - gs / 32), s.Cp);
+}
+
+// ============================================================================
 // MXFP8 dim0: four lanes per 32-element block, 8 bf16 (16 bytes) per lane.
 // ============================================================================
-template <int U>
-__global__ void __launch_bounds__(256) k_mx_dim0(const uint16_t* __restrict__ x, int64_t nch,
-                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ sc) {
+// IDX32: every chunk index fits 32 bits, so the row / column of a scale come
+// from a 32-bit division (a 64-bit division per scale costs a third of the
+// kernel's time).  Row-major scales need no division at all.
+template <int U, bool IDX32>
+__global__ void __launch_bounds__(256) k_mx_dim0(const uint16_t* __restrict__ x, int64_t nch, int64_t R, int64_t C,
+                                                 uint8_t* __restrict__ q, ScaleSpec sc, int* status) {
+  __shared__ GroupTable gt;
+  if (sc.layout == FP8MOE_GROUP_ROWS) {
+    build_group_table(gt, sc.offs, sc.E, R, false, status);
+    if (gt.bad) return;
+  }
+  const int64_t Cs = C / 32, cpr = C / 8;  // scale columns, 16-byte chunks per row
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t warp0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -168,21 +283,59 @@ __global__ void __launch_bounds__(256) k_mx_dim0(const uint16_t* __restrict__ x,
       const float p = exp2_neg(e);
       if (ch < nch) {
         *reinterpret_cast<uint2*>(q + ch * 8) = enc8_bf16<false>(v[u], p);
-        if ((lane & 3) == 0) sc[ch >> 2] = (uint8_t)(e + 127);
+        if ((lane & 3) == 0) {
+          int64_t off;
+          if (sc.layout == FP8MOE_SCALES_ROWMAJOR) {
+            off = ch >> 2;
+          } else {
+            int64_t row, cb;
+            if (IDX32) {
+              const uint32_t c32 = (uint32_t)ch, p32 = (uint32_t)cpr;
+              const uint32_t r32 = c32 / p32;
+              row = r32;
+              cb = (c32 - r32 * p32) >> 2;
+            } else {
+              row = ch / cpr;
+              cb = (ch % cpr) >> 2;
+            }
+            int64_t b = 0;
+            if (sc.layout != FP8MOE_GROUP_ROWS) b = IDX32 ? (int64_t)((uint32_t)row / (uint32_t)R) : row / R;
+            off = scale_offset(sc, &gt, b, row - b * R, cb, R, Cs);
+          }
+          sc.p[off] = (uint8_t)(e + 127);
+        }
       }
     }
   }
 }
 
-cudaError_t launch_mx_dim0(const void* x, int64_t rows, int64_t C, void* q, uint8_t* s, int num_sms,
-                           cudaStream_t st) {
-  const int64_t nch = rows * C / 8;
+static ScaleSpec make_spec(uint8_t* p, int layout, int64_t R, int64_t Cs, const int32_t* offs, int64_t E) {
+  ScaleSpec o;
+  o.p = p;
+  o.layout = layout;
+  const bool grouped = layout == FP8MOE_GROUP_ROWS || layout == FP8MOE_GROUP_COLS;
+  const SwizzleGeom g = swizzle_geom(R, Cs, grouped ? E : 0, grouped ? layout : FP8MOE_NO_GROUPS);
+  o.Rp = g.Rp;
+  o.Cp = g.Cp;
+  o.offs = offs;
+  o.E = (int)E;
+  return o;
+}
+
+cudaError_t launch_mx_dim0(const void* x, int64_t B, int64_t R, int64_t C, void* q, uint8_t* s, int layout,
+                           const int32_t* offs, int64_t E, int num_sms, int* status, cudaStream_t st) {
+  const int64_t nch = B * R * C / 8;
   if (nch == 0) return cudaSuccess;
   constexpr int U = 4;
   int64_t blocks = (nch + 256 * U - 1) / (256 * U);
   const int64_t cap = (int64_t)num_sms * 8 * 4;
   if (blocks > cap) blocks = cap;
-  k_mx_dim0<U><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, nch, (uint8_t*)q, s);
+  const ScaleSpec spec = make_spec(s, layout, R, C / 32, offs, E);
+  if (nch < ((int64_t)1 << 32)) {
+    k_mx_dim0<U, true><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, nch, R, C, (uint8_t*)q, spec, status);
+  } else {
+    k_mx_dim0<U, false><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, nch, R, C, (uint8_t*)q, spec, status);
+  }
   return cudaGetLastError();
 }
 
@@ -201,7 +354,7 @@ constexpr int D1_SMEM = D1_STAGES * D1_IN_BYTES + 2 * D1_OUT_BYTES + 64 + 1024;
 struct Dim1Args {
   int64_t B, R, C;
   int64_t n_rt, n_ct, tiles;
-  uint8_t* scale;
+  ScaleSpec sc;
   int* status;
 };
 
@@ -213,12 +366,17 @@ __global__ void __launch_bounds__(256) k_mx_dim1(const __grid_constant__ CUtenso
   uint8_t* outb = smem + D1_STAGES * D1_IN_BYTES;
   uint64_t* full = (uint64_t*)(outb + 2 * D1_OUT_BYTES);
   volatile int* abort_s = (volatile int*)(full + D1_STAGES);
+  __shared__ GroupTable gt;
   const int tid = threadIdx.x;
   auto coords = [&](int64_t t, int& rt, int& ct, int& b) {
     rt = (int)(t % a.n_rt);
     ct = (int)((t / a.n_rt) % a.n_ct);
     b = (int)(t / (a.n_rt * a.n_ct));
   };
+  if (a.sc.layout == FP8MOE_GROUP_COLS) {
+    build_group_table(gt, a.sc.offs, a.sc.E, a.R, true, a.status);
+    if (gt.bad) return;
+  }
   if (tid == 0) {
     for (int s = 0; s < D1_STAGES; ++s) mbar_init(&full[s], 1);
     *abort_s = 0;
@@ -272,7 +430,8 @@ __global__ void __launch_bounds__(256) k_mx_dim1(const __grid_constant__ CUtenso
     *reinterpret_cast<uint4*>(orow + (((rb * 2 + 1) ^ (cl & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
     const int64_t c = (int64_t)ct * D1_COLS + cl;
     const int64_t rbase = (int64_t)rt * D1_ROWS + rb * 32;
-    if (c < a.C && rbase < a.R) a.scale[((int64_t)b * a.C + c) * (a.R / 32) + rbase / 32] = (uint8_t)(e + 127);
+    if (c < a.C && rbase < a.R)
+      a.sc.p[scale_offset(a.sc, &gt, b, c, rbase / 32, a.C, a.R / 32)] = (uint8_t)(e + 127);
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -290,8 +449,8 @@ __global__ void __launch_bounds__(256) k_mx_dim1(const __grid_constant__ CUtenso
   if (tid == 0) bulk_wait_read<0>();
 }
 
-cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s, int num_sms,
-                           int* status, cudaStream_t st) {
+cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s, int layout,
+                           const int32_t* offs, int64_t E, int num_sms, int* status, cudaStream_t st) {
   if (B == 0 || R == 0 || C == 0) return cudaSuccess;
   CUtensorMap tin, tout;
   {
@@ -313,287 +472,13 @@ cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void*
   a.n_rt = (R + D1_ROWS - 1) / D1_ROWS;
   a.n_ct = (C + D1_COLS - 1) / D1_COLS;
   a.tiles = a.n_rt * a.n_ct * B;
-  a.scale = s;
+  a.sc = make_spec(s, layout, C, R / 32, offs, E);
   a.status = status;
   cudaError_t err = cudaFuncSetAttribute(k_mx_dim1, cudaFuncAttributeMaxDynamicSharedMemorySize, D1_SMEM);
   if (err != cudaSuccess) return err;
   int64_t grid = (int64_t)num_sms * 2;
   if (grid > a.tiles) grid = a.tiles;
   k_mx_dim1<<<(unsigned)grid, 256, D1_SMEM, st>>>(tin, tout, a);
-  return cudaGetLastError();
-}
-
-// ============================================================================
-// MXFP8 in both directions from one read, scales written straight into their
-// final layout.  Every tensor of an MoE training step is needed along both
-// dimensions (activations: dim0 for the forward GEMM, dim1 for wgrad; weights:
-// dim0 forward, dim1 dgrad; gradients: dim0 dgrad, dim1 wgrad), so reading the
-// bf16 tile once and emitting both code layouts saves one of the two reads;
-// writing the e8m0 bytes directly in the 128x4 tcgen05 layout removes the
-// separate swizzle pass.  Same TMA ring as dim1; dim0 codes go through a
-// 64-byte-swizzled 128 x 64 staging tile, dim1 codes through a 128-byte-
-// swizzled 64 x 128 one, both written by TMA stores.
-// ============================================================================
-constexpr int DU_STAGES = 4;
-constexpr int DU_MAX_GROUPS = 1024;
-constexpr int DU_SMEM = DU_STAGES * D1_IN_BYTES + 4 * D1_OUT_BYTES + 64 + 3 * (DU_MAX_GROUPS + 1) * 8 + 1024;
-
-struct ScaleOut {
-  uint8_t* p;     // NULL: this direction is not produced
-  int layout;     // FP8MOE_SCALES_ROWMAJOR, FP8MOE_NO_GROUPS, FP8MOE_GROUP_ROWS / _COLS
-  int64_t Rp, Cp; // padded geometry of one (batch's) swizzled matrix
-};
-
-struct DualArgs {
-  int64_t B, R, C;
-  int64_t n_rt, n_ct, tiles;
-  const int32_t* offs;
-  int E;
-  ScaleOut s0, s1;
-  int do0, do1;
-  int* status;
-};
-
-FP8MOE_DEV int64_t tile_off(int64_t r, int64_t c, int64_t Cp) {
-  return ((r >> 7) * (Cp >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
-}
-
-// last group whose start (exclusive prefix of ends) is <= key; starts[] in smem
-FP8MOE_DEV int find_group(const int64_t* ends, int E, int64_t key) {
-  int lo = 0, hi = E - 1, g = E - 1;
-  while (lo <= hi) {
-    const int mid = (lo + hi) >> 1;
-    if (ends[mid] > key) {
-      g = mid;
-      hi = mid - 1;
-    } else {
-      lo = mid + 1;
-    }
-  }
-  return g;  // first group whose end is > key
-}
-
-__global__ void __launch_bounds__(256) k_mx_dual(const __grid_constant__ CUtensorMap tin,
-                                                 const __grid_constant__ CUtensorMap tout0,
-                                                 const __grid_constant__ CUtensorMap tout1, DualArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* in = smem;
-  uint8_t* out0 = smem + DU_STAGES * D1_IN_BYTES;         // 2 x 8 KB (128 rows x 64 B)
-  uint8_t* out1 = out0 + 2 * D1_OUT_BYTES;                 // 2 x 8 KB (64 rows x 128 B)
-  uint64_t* full = (uint64_t*)(out1 + 2 * D1_OUT_BYTES);
-  volatile int* flags = (volatile int*)(full + DU_STAGES);  // [0] abort, [1] bad offsets
-  int64_t* gend = (int64_t*)(full + DU_STAGES + 2);         // group ends (rows of x)
-  int64_t* gpad0 = gend + DU_MAX_GROUPS + 1;                // dim0 scales: padded start row (128-row blocks)
-  int64_t* gpad1 = gpad0 + DU_MAX_GROUPS + 1;               // dim1 scales: padded start column (4-column blocks)
-  const int tid = threadIdx.x;
-  const bool grouped = (a.do0 && a.s0.layout == FP8MOE_GROUP_ROWS) || (a.do1 && a.s1.layout == FP8MOE_GROUP_COLS);
-  if (tid == 0) {
-    for (int s = 0; s < DU_STAGES; ++s) mbar_init(&full[s], 1);
-    flags[0] = 0;
-    flags[1] = 0;
-    mbar_fence_init();
-    if (grouped) {
-      // group table: ends, and padded starts (rows in 128-row blocks for the
-      // dim0 scales; scale columns in 4-column blocks for the dim1 scales)
-      int64_t prev = 0, p0 = 0, p1 = 0;
-      int bad = 0;
-      for (int e = 0; e < a.E; ++e) {
-        const int64_t end = a.offs[e];
-        if (end < prev || end > a.R) bad = 1;
-        if (a.do1 && (end % 32)) bad = 1;
-        gend[e] = end;
-        gpad0[e] = p0;
-        gpad1[e] = p1;
-        p0 += (end - prev + 127) / 128 * 128;
-        p1 += ((end - prev) / 32 + 3) / 4 * 4;
-        prev = end;
-      }
-      if (prev != a.R) bad = 1;
-      flags[1] = bad;
-      if (bad) set_status(a.status, FP8MOE_ERR_DEVICE_OFFSETS);
-    }
-  }
-  __syncthreads();
-  if (flags[1]) return;
-  auto coords = [&](int64_t t, int& rt, int& ct, int& b) {
-    rt = (int)(t % a.n_rt);
-    ct = (int)((t / a.n_rt) % a.n_ct);
-    b = (int)(t / (a.n_rt * a.n_ct));
-  };
-  if (tid == 0) {
-    for (int s = 0; s < DU_STAGES; ++s) {
-      const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
-      if (t >= a.tiles) break;
-      int rt, ct, b;
-      coords(t, rt, ct, b);
-      mbar_expect_tx(&full[s], D1_IN_BYTES);
-      tma_load_3d(in + s * D1_IN_BYTES, &tin, &full[s], ct * D1_COLS, rt * D1_ROWS, b);
-    }
-  }
-  const int cl = tid & 63, rb = tid >> 6;     // dim1 role: column, 32-row block
-  const int r0 = tid >> 1, h = tid & 1;       // dim0 role: row, 32-column half
-  const int64_t Cs = a.C / 32, Rs = a.R / 32;
-  int it = 0;
-  for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
-    const int s = it % DU_STAGES, ob = it & 1;
-    int rt, ct, b;
-    coords(t, rt, ct, b);
-    if (tid == 0) bulk_wait_read<1>();
-    __syncthreads();
-    if (!mbar_wait(&full[s], (uint32_t)((it / DU_STAGES) & 1), flags)) {
-      set_status(a.status, FP8MOE_ERR_TIMEOUT);
-      flags[0] = 1;
-    }
-    __syncthreads();
-    if (flags[0]) break;
-    const uint8_t* tile = in + s * D1_IN_BYTES;
-    if (a.do1) {
-      float f[32];
-      uint32_t m = 0;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = rb * 32 + i;
-        const uint32_t hv =
-            *reinterpret_cast<const uint16_t*>(tile + r * 128 + ((((cl >> 3) ^ (r & 7))) << 4) + ((cl & 7) << 1));
-        m = max(m, hv & 0x7FFFu);
-        f[i] = bf16bits_to_float(hv);
-      }
-      const int e = e8m0_exponent(m);
-      const float pw = exp2_neg(e);
-      uint32_t w[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        w[j] = enc4<false>(__fmul_rn(f[4 * j], pw), __fmul_rn(f[4 * j + 1], pw), __fmul_rn(f[4 * j + 2], pw),
-                           __fmul_rn(f[4 * j + 3], pw));
-      uint8_t* orow = out1 + ob * D1_OUT_BYTES + cl * 128;
-      *reinterpret_cast<uint4*>(orow + (((rb * 2) ^ (cl & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(orow + (((rb * 2 + 1) ^ (cl & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-      const int64_t c = (int64_t)ct * D1_COLS + cl;
-      const int64_t sr = (int64_t)rt * 4 + rb;  // 32-row block index along R
-      if (c < a.C && sr < Rs) {
-        int64_t o;
-        if (a.s1.layout == FP8MOE_SCALES_ROWMAJOR) {
-          o = ((int64_t)b * a.C + c) * Rs + sr;
-        } else if (a.s1.layout == FP8MOE_NO_GROUPS) {
-          o = (int64_t)b * a.s1.Rp * a.s1.Cp + tile_off(c, sr, a.s1.Cp);
-        } else {
-          const int g = find_group(gend, a.E, sr * 32);
-          const int64_t gs = g == 0 ? 0 : gend[g - 1];
-          o = tile_off(c, gpad1[g] + (sr - gs / 32), a.s1.Cp);
-        }
-        a.s1.p[o] = (uint8_t)(e + 127);
-      }
-    }
-    if (a.do0) {
-      uint4 v[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = h * 4 + i;
-        v[i] = *reinterpret_cast<const uint4*>(tile + r0 * 128 + ((j ^ (r0 & 7)) << 4));
-      }
-      uint32_t m = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) m = max(m, absmax8_bits(v[i]));
-      const int e = e8m0_exponent(m);
-      const float pw = exp2_neg(e);
-      uint2 w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = enc8_bf16<false>(v[i], pw);
-      // 64-byte swizzle: 16-byte chunk index ^= (row / 2) % 4
-      uint8_t* orow = out0 + ob * D1_OUT_BYTES + r0 * 64;
-      const int sw = (r0 >> 1) & 3;
-      *reinterpret_cast<uint4*>(orow + (((2 * h) ^ sw) << 4)) = make_uint4(w[0].x, w[0].y, w[1].x, w[1].y);
-      *reinterpret_cast<uint4*>(orow + (((2 * h + 1) ^ sw) << 4)) = make_uint4(w[2].x, w[2].y, w[3].x, w[3].y);
-      const int64_t r = (int64_t)rt * D1_ROWS + r0;
-      const int64_t sc = (int64_t)ct * 2 + h;  // 32-column block index along C
-      if (r < a.R && sc < Cs) {
-        int64_t o;
-        if (a.s0.layout == FP8MOE_SCALES_ROWMAJOR) {
-          o = ((int64_t)b * a.R + r) * Cs + sc;
-        } else if (a.s0.layout == FP8MOE_NO_GROUPS) {
-          o = (int64_t)b * a.s0.Rp * a.s0.Cp + tile_off(r, sc, a.s0.Cp);
-        } else {
-          const int g = find_group(gend, a.E, r);
-          const int64_t gs = g == 0 ? 0 : gend[g - 1];
-          o = tile_off(gpad0[g] + (r - gs), sc, a.s0.Cp);
-        }
-        a.s0.p[o] = (uint8_t)(e + 127);
-      }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      if (a.do1) tma_store_3d(&tout1, out1 + ob * D1_OUT_BYTES, rt * D1_ROWS, ct * D1_COLS, b);
-      if (a.do0) tma_store_3d(&tout0, out0 + ob * D1_OUT_BYTES, ct * D1_COLS, rt * D1_ROWS, b);
-      bulk_commit();
-      const int64_t t2 = t + (int64_t)DU_STAGES * gridDim.x;
-      if (t2 < a.tiles) {
-        int rt2, ct2, b2;
-        coords(t2, rt2, ct2, b2);
-        mbar_expect_tx(&full[s], D1_IN_BYTES);
-        tma_load_3d(in + s * D1_IN_BYTES, &tin, &full[s], ct2 * D1_COLS, rt2 * D1_ROWS, b2);
-      }
-    }
-  }
-  if (tid == 0) bulk_wait_read<0>();
-}
-
-static ScaleOut scale_out(uint8_t* p, int layout, int64_t R, int64_t Cs, int64_t E) {
-  ScaleOut o;
-  o.p = p;
-  o.layout = layout;
-  const SwizzleGeom g = swizzle_geom(R, Cs, layout >= 0 ? E : 0, layout >= 0 ? layout : FP8MOE_NO_GROUPS);
-  o.Rp = g.Rp;
-  o.Cp = g.Cp;
-  return o;
-}
-
-cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, const int32_t* offs, int64_t E, void* q0,
-                           uint8_t* s0, int s0_layout, void* q1, uint8_t* s1, int s1_layout, int num_sms, int* status,
-                           cudaStream_t st) {
-  if (B == 0 || R == 0 || C == 0) return cudaSuccess;
-  CUtensorMap tin, t0, t1;
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)R, (cuuint64_t)B};
-    cuuint64_t strides[2] = {(cuuint64_t)(C * 2), (cuuint64_t)(R * C * 2)};
-    cuuint32_t box[3] = {D1_COLS, D1_ROWS, 1};
-    if (!make_tmap(&tin, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  t0 = tin;
-  t1 = tin;
-  if (q0) {
-    cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)R, (cuuint64_t)B};
-    cuuint64_t strides[2] = {(cuuint64_t)C, (cuuint64_t)(R * C)};
-    cuuint32_t box[3] = {D1_COLS, D1_ROWS, 1};
-    if (!make_tmap(&t0, CU_TENSOR_MAP_DATA_TYPE_UINT8, q0, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
-      return cudaErrorInvalidValue;
-  }
-  if (q1) {
-    cuuint64_t dims[3] = {(cuuint64_t)R, (cuuint64_t)C, (cuuint64_t)B};
-    cuuint64_t strides[2] = {(cuuint64_t)R, (cuuint64_t)(C * R)};
-    cuuint32_t box[3] = {D1_ROWS, D1_COLS, 1};
-    if (!make_tmap(&t1, CU_TENSOR_MAP_DATA_TYPE_UINT8, q1, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  DualArgs a;
-  a.B = B;
-  a.R = R;
-  a.C = C;
-  a.n_rt = (R + D1_ROWS - 1) / D1_ROWS;
-  a.n_ct = (C + D1_COLS - 1) / D1_COLS;
-  a.tiles = a.n_rt * a.n_ct * B;
-  a.offs = offs;
-  a.E = (int)E;
-  a.s0 = scale_out(s0, s0_layout, R, C / 32, E);
-  a.s1 = scale_out(s1, s1_layout, C, R / 32, E);
-  a.do0 = q0 != nullptr;
-  a.do1 = q1 != nullptr;
-  a.status = status;
-  cudaError_t err = cudaFuncSetAttribute(k_mx_dual, cudaFuncAttributeMaxDynamicSharedMemorySize, DU_SMEM);
-  if (err != cudaSuccess) return err;
-  int64_t grid = (int64_t)num_sms * 2;
-  if (grid > a.tiles) grid = a.tiles;
-  k_mx_dual<<<(unsigned)grid, 256, DU_SMEM, st>>>(tin, t0, t1, a);
   return cudaGetLastError();
 }
 
