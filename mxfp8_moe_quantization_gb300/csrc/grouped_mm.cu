@@ -16,7 +16,11 @@
 //  * warp 0: TMA producer (A and B tiles with 128-byte swizzle, MXFP8 scale
 //    tiles as 512-byte bulk copies -- the 128x4 layout makes each one
 //    contiguous); warp 1: TMEM allocator and single-thread MMA issuer; warps
-//    2-5: epilogue (TMEM -> registers -> bf16 -> global);
+//    2-5: epilogue (TMEM -> registers -> bf16 -> global); warp 6: scale-factor
+//    copier (MXFP8): moves each stage's scale tiles into TMEM with
+//    tcgen05.cp and signals the MMA thread through a second per-stage barrier.
+//    Issued from the MMA thread itself, the copies cost a quarter of the MMA
+//    rate (measured); from their own thread they overlap the MMAs;
 //  * 4-stage shared-memory ring with mbarriers; every wait is bounded and a
 //    timeout sets the device status word instead of hanging;
 //  * accumulator in TMEM (128 lanes x 256 fp32 columns); MXFP8 scales copied
@@ -36,11 +40,11 @@
 namespace fp8moe {
 
 constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int NUM_THREADS = 192;  // producer, MMA, 4 epilogue warps
+constexpr int NUM_THREADS = 224;  // producer, MMA, 4 epilogue warps, scale copier
 constexpr int A_STAGE_BYTES = BM * BK;            // 16 KB
 constexpr int SFA_STAGE_BYTES = 512;              // one 128x4 scale tile
 constexpr int SFB_STAGE_BYTES = 1024;             // two 128x4 scale tiles (256 rows)
-constexpr int MAX_GROUPS = 1024;
+constexpr int MAX_GROUPS = 1024;                  // 1-CTA variant; the 2-CTA one holds 512
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = 256;            // scale columns start after the accumulator
 
@@ -51,18 +55,21 @@ constexpr uint32_t TMEM_SF_BASE = 256;            // scale columns start after t
 //               operand bytes each SM receives per MMA.
 template <bool TWO>
 struct SmemLayout {
-  static constexpr int STAGES = TWO ? 5 : 4;
+  // 2-CTA: 32 KB per stage buys a 6-deep ring; its group tables are capped at
+  // 512 groups to fit (larger E runs the 1-CTA variant)
+  static constexpr int STAGES = TWO ? 6 : 4;
+  static constexpr int MAXG = TWO ? 512 : MAX_GROUPS;
   static constexpr int B_STAGE_BYTES = TWO ? BN * BK / 2 : BN * BK;
   static constexpr int a = 0;
   static constexpr int b = a + STAGES * A_STAGE_BYTES;
   static constexpr int sfa = b + STAGES * B_STAGE_BYTES;
   static constexpr int sfb = sfa + STAGES * SFA_STAGE_BYTES;
-  static constexpr int bars = sfb + STAGES * SFB_STAGE_BYTES;   // 2*STAGES + 2 mbarriers
-  static constexpr int misc = bars + (2 * STAGES + 2) * 8;      // tmem addr, abort, counts
+  static constexpr int bars = sfb + STAGES * SFB_STAGE_BYTES;   // 3*STAGES + 2 mbarriers
+  static constexpr int misc = bars + (3 * STAGES + 2) * 8;      // tmem addr, abort, counts
   static constexpr int colscale = misc + 64;                    // 256 floats
-  static constexpr int tiles_prefix = colscale + BN * 4;        // MAX_GROUPS + 1 ints
-  static constexpr int blk_prefix = tiles_prefix + (MAX_GROUPS + 1) * 4;
-  static constexpr int stg = (blk_prefix + (MAX_GROUPS + 1) * 4 + 15) / 16 * 16;
+  static constexpr int tiles_prefix = colscale + BN * 4;        // MAXG + 1 ints
+  static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
+  static constexpr int stg = (blk_prefix + (MAXG + 1) * 4 + 15) / 16 * 16;
   static constexpr int total = stg + 4 * 32 * 144;                    // per-warp 32 x (128 + 16) B
 };
 static_assert(SmemLayout<false>::stg % 16 == 0 && SmemLayout<true>::stg % 16 == 0, "staging alignment");
@@ -129,6 +136,17 @@ FP8MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_syn
 FP8MOE_DEV void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+// completion of this thread's earlier tcgen05 ops (of its own CTA group) on a
+// local barrier
+template <bool TWO>
+FP8MOE_DEV void tc_commit_local(uint64_t* bar) {
+  if constexpr (TWO) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+  } else {
+    tc_commit(bar);
+  }
 }
 
 // Shared-memory matrix descriptor: K-major operand tile, 128-byte swizzle,
@@ -306,6 +324,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB, KParams p) {
   using L = SmemLayout<TWO>;
   constexpr int STAGES = L::STAGES;
+  // MXFP8 scale copies run on their own warp (the 2-CTA leader's)
+  constexpr bool SFW = MX;
   constexpr int B_STAGE_BYTES = L::B_STAGE_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -317,6 +337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* tmem_full = empty + STAGES;
   uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* sf_full = tmem_empty + 1;  // per stage: scales are in TMEM (scale-copier commits)
   uint32_t* tmem_base_holder = (uint32_t*)(smem + L::misc);
   volatile int* abort_flag = (volatile int*)(smem + L::misc + 4);
   int* total_tiles_s = (int*)(smem + L::misc + 8);
@@ -335,6 +356,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // 1-CTA: released by the MMAs of both CTAs; 2-CTA: by the leader's MMA
       mbar_init(&empty[s], TWO ? 1 : 2);
     }
+    for (int s = 0; s < STAGES; ++s) mbar_init(&sf_full[s], 1);
     mbar_init(tmem_full, 1);
     // 2-CTA: the leader's accumulator is free once both CTAs' epilogues drained
     mbar_init(tmem_empty, TWO ? 8 : 4);
@@ -513,7 +535,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_phase = 0;
-    auto stage_ready = [&]() -> bool { return mbar_wait(&full[stage], phase, abort_flag); };
+    auto stage_ready = [&]() -> bool {
+      if (!mbar_wait(&full[stage], phase, abort_flag)) return false;
+      return !SFW || mbar_wait(&sf_full[stage], phase, abort_flag);
+    };
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
       const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
       if (tl.nk == 0) continue;
@@ -557,15 +582,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t a_addr = smem_u32(sA + stage * A_STAGE_BYTES);
         const uint32_t b_addr = smem_u32(sB + stage * B_STAGE_BYTES);
         const uint32_t sf_col = tmem_base + TMEM_SF_BASE + stage * 16;
-        if (MX) {
+        if (MX && !SFW) {
           tc_cp_sf<TWO>(sf_col, sdesc_sf(smem_u32(sSFA + stage * SFA_STAGE_BYTES)));
           tc_cp_sf<TWO>(sf_col + 4, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES)));
           tc_cp_sf<TWO>(sf_col + 8, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES + 512)));
         }
         const int64_t rem = tl.kvalid - (int64_t)ks * BK;
-        const int nsub = rem >= BK ? 4 : (int)((rem + 31) / 32);
         const uint64_t adesc = sdesc_sw128(a_addr), bdesc = sdesc_sw128(b_addr);
-        for (int k = 0; k < nsub; ++k) {
+        auto issue = [&](int k) {
           const uint32_t accum = (ks > 0 || k > 0) ? 1u : 0u;
           if (MX) {
             mma_mx<TWO>(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_mx<MM>((uint32_t)k),
@@ -573,6 +597,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             mma_f8<TWO>(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8<MM>(), accum);
           }
+        };
+        // Full stages issue their four K=32 MMAs as straight-line code: behind a
+        // loop with a run-time trip count the MMA rate dropped by a quarter
+        // (measured).  Only the last stage of a ragged contraction (wgrad
+        // groups, a multiple of 32 long) takes the counted path.
+        if (rem >= BK) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) issue(k);
+        } else {
+          const int nsub = (int)((rem + 31) / 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k < nsub) issue(k);
         }
         tc_commit_pair<TWO>(&empty[stage]);
         if (++stage == STAGES) {
@@ -585,6 +622,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_commit_pair<true>(tmem_full);
       } else {
         tc_commit(tmem_full);
+      }
+    }
+  } else if (warp == 6) {
+    // ======================= scale copier =======================
+    // Stage s's scale columns are free once the MMAs of its previous use
+    // completed: the producer refilled the stage only after that release, and
+    // the copies wait for the refill.  Phantom tiles copy nothing but still
+    // complete sf_full, so that its phase follows full.
+    if (SFW && lane == 0 && (!TWO || rank == 0)) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
+        const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+        bool ok = true;
+        for (int ks = 0; ks < tl.nk; ++ks) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            set_status(g.status, FP8MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // (a 2-CTA pair computes both halves even when one is a phantom)
+          if (TWO || tl.rows > 0) {
+            const uint32_t sf_col = tmem_base + TMEM_SF_BASE + stage * 16;
+            tc_cp_sf<TWO>(sf_col, sdesc_sf(smem_u32(sSFA + stage * SFA_STAGE_BYTES)));
+            tc_cp_sf<TWO>(sf_col + 4, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES)));
+            tc_cp_sf<TWO>(sf_col + 8, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES + 512)));
+          }
+          tc_commit_local<TWO>(&sf_full[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
       }
     }
   } else if (warp >= 2) {
@@ -799,13 +872,14 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
                    CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
-  // 1-CTA MMAs with B multicast by default (measured the faster of the two on
-  // the Scout shapes); FP8MOE_GEMM_2CTA=1 selects the cta_group::2 variant
+  // cta_group::2 MMAs by default (with its 6-deep ring, the faster of the two
+  // on the Scout shapes: 2,695 against 2,492 TFLOP/s fwd); FP8MOE_GEMM_1CTA=1
+  // selects the 1-CTA variant with B multicast, which also serves E > 512
   static const bool two = [] {
-    const char* v = getenv("FP8MOE_GEMM_2CTA");
-    return v && v[0] == '1';
+    const char* v = getenv("FP8MOE_GEMM_1CTA");
+    return !(v && v[0] == '1');
   }();
-  if (two) {
+  if (two && g.E <= SmemLayout<true>::MAXG) {
     if (mx) return wgrad ? launch_t<true, true, true>(ta, tb, tsa, tsb, p, grid, st)
                          : launch_t<true, false, true>(ta, tb, tsa, tsb, p, grid, st);
     return wgrad ? launch_t<false, true, true>(ta, tb, tsa, tsb, p, grid, st)

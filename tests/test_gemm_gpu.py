@@ -218,3 +218,34 @@ def test_bad_offsets_set_status(F):
     F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, bad)
     assert F.fp8moe_get_device_status() == 5
     assert F.fp8moe_get_device_status() == 0
+
+
+def test_many_groups_fwd(F):
+    """E = 600 groups (above the 2-CTA variant's 512-group table; the launch
+    falls back to the 1-CTA variant), many of them empty."""
+    rng = np.random.default_rng(5)
+    sizes = (rng.integers(0, 3, size=600) * 32).tolist()
+    offs = W.offsets_from_sizes(sizes)
+    M, N, K = int(sum(sizes)), 256, 128
+    a = _bf16((M, K), 81)
+    w = _bf16((len(sizes), N, K), 82, 0.05)
+    (qa, sa, qw, sw), ref, bound = mx_fwd_case(a, w, offs)
+    out = F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, _d(offs))
+    assert F.fp8moe_get_device_status() == 0
+    check(out, ref, bound, "mx fwd, 600 groups")
+
+
+def test_one_cta_variant():
+    """The other pair variant (1-CTA MMAs with B multicast, chosen per process
+    by FP8MOE_GEMM_1CTA=1) passes the same parity cases."""
+    import os
+    import subprocess
+    import sys
+    if os.environ.get("FP8MOE_GEMM_1CTA") == "1":
+        pytest.skip("this process already runs the 1-CTA variant")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, FP8MOE_GEMM_1CTA="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
+                        os.path.abspath(__file__), "-k", "not one_cta_variant"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
