@@ -47,6 +47,9 @@ constexpr int SFB_STAGE_BYTES = 1024;             // two 128x4 scale tiles (256 
 constexpr int MAX_GROUPS = 1024;                  // 1-CTA variant; the 2-CTA one holds 512
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = 256;            // scale columns start after the accumulator
+constexpr int STG_COLS = 32;                      // output columns per staged store (64 bytes of bf16)
+constexpr int STG_BYTES = 32 * STG_COLS * 2;      // one staging tile: 32 rows x 64 B
+constexpr int STG_WARP_BYTES = 2 * STG_BYTES;     // double-buffered per epilogue warp
 
 // TWO = false: 1-CTA MMAs (M = 128 per CTA), the pair shares B tiles by TMA
 //               multicast; each CTA's shared memory holds the whole B tile.
@@ -69,10 +72,11 @@ struct SmemLayout {
   static constexpr int colscale = misc + 64;                    // 256 floats
   static constexpr int tiles_prefix = colscale + BN * 4;        // MAXG + 1 ints
   static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
-  static constexpr int stg = (blk_prefix + (MAXG + 1) * 4 + 15) / 16 * 16;
-  static constexpr int total = stg + 4 * 32 * 144;                    // per-warp 32 x (128 + 16) B
+  // per epilogue warp two 32-row x 64-byte staging tiles (64-byte swizzle)
+  static constexpr int stg = (blk_prefix + (MAXG + 1) * 4 + 1023) / 1024 * 1024;
+  static constexpr int total = stg + 4 * STG_WARP_BYTES;
 };
-static_assert(SmemLayout<false>::stg % 16 == 0 && SmemLayout<true>::stg % 16 == 0, "staging alignment");
+static_assert(SmemLayout<false>::stg % 1024 == 0 && SmemLayout<true>::stg % 1024 == 0, "staging alignment");
 template <bool TWO>
 constexpr int smem_bytes() { return SmemLayout<TWO>::total + 1024; }  // + alignment slack
 
@@ -250,6 +254,7 @@ struct KParams {
   int64_t b_rows_pad; // fwd/dgrad: padded rows (cols of C) of one expert's scale matrix
   int n_tiles;        // tiles along the output columns
   int m_tiles_w;      // wgrad: tiles along the output rows
+  int tma_out;        // output stored by TMA (tmOut valid); else by thread stores
 };
 
 // Per-tile geometry, recomputed identically by every role.
@@ -321,7 +326,8 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
 template <bool MX, bool WGRAD, bool TWO>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB, KParams p) {
+                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                 const __grid_constant__ CUtensorMap tmOut, KParams p) {
   using L = SmemLayout<TWO>;
   constexpr int STAGES = L::STAGES;
   // MXFP8 scale copies run on their own warp (the 2-CTA leader's)
@@ -442,6 +448,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     // ======================= TMA producer =======================
+    // global sources of k-stage ks of a tile: MXFP8 scale tiles
+    auto sf_srcs = [&](const Tile& tl, int ks, const uint8_t*& sa, const uint8_t*& sb0, const uint8_t*& sb1) {
+      const int64_t kb = tl.sf_kblk + ks;
+      sa = (const uint8_t*)g.a_scale + (tl.sfa_blk * p.cpb + kb) * 512;
+      const int64_t nb0 = tl.col0 / 128;
+      const int64_t nbl = WGRAD ? (g.cols + 127) / 128 : p.b_rows_pad / 128;
+      const uint8_t* bsf = (const uint8_t*)g.b_scale + (WGRAD ? 0 : (int64_t)tl.e * p.b_rows_pad * p.cpb * 4);
+      // both 128-row scale tiles of B (in 2-CTA mode each CTA's TMEM holds
+      // the scales of all 256 columns)
+      sb0 = bsf + (nb0 * p.cpb + kb) * 512;
+      sb1 = nb0 + 1 < nbl ? bsf + ((nb0 + 1) * p.cpb + kb) * 512 : nullptr;
+    };
     int stage = 0;
     uint32_t phase = 0;
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
@@ -459,15 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint8_t* sfb_src0 = nullptr;
         const uint8_t* sfb_src1 = nullptr;
         if (MX) {
-          const int64_t kb = tl.sf_kblk + ks;
-          sfa_src = (const uint8_t*)g.a_scale + (tl.sfa_blk * p.cpb + kb) * 512;
-          const int64_t nb0 = tl.col0 / 128;
-          const int64_t nbl = WGRAD ? (g.cols + 127) / 128 : p.b_rows_pad / 128;
-          const uint8_t* bsf = (const uint8_t*)g.b_scale + (WGRAD ? 0 : (int64_t)tl.e * p.b_rows_pad * p.cpb * 4);
-          // both 128-row scale tiles of B (in 2-CTA mode each CTA's TMEM holds
-          // the scales of all 256 columns)
-          sfb_src0 = bsf + (nb0 * p.cpb + kb) * 512;
-          sfb_src1 = nb0 + 1 < nbl ? bsf + ((nb0 + 1) * p.cpb + kb) * 512 : nullptr;
+          sf_srcs(tl, ks, sfa_src, sfb_src0, sfb_src1);
           bytes += 512 + 512 + (sfb_src1 ? 512 : 0);
         }
         const int x = (int)(tl.x0 + (int64_t)ks * BK);
@@ -664,7 +674,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ======================= epilogue =======================
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const int et = threadIdx.x - 64;
-    uint8_t* stg = smem + L::stg + (warp - 2) * 32 * 144;
+    uint8_t* stg = smem + L::stg + (warp - 2) * STG_WARP_BYTES;
     uint32_t acc_phase = 0;
     auto release_acc = [&]() {
       tc_fence_before();
@@ -737,30 +747,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // accumulator drained: let the MMA start the next tile
       release_acc();
-      // Coalesced stores: 64-column slices of this warp's 32 rows go through a
-      // padded shared-memory buffer (row pitch 144 B: conflict-free both ways),
-      // then each store instruction writes 4 rows x 128 contiguous bytes.
+      // Stores in 32-column slices through two 32-row x 64-byte staging tiles
+      // per warp, laid out with the 64-byte swizzle (16-byte chunk c of row r
+      // at r*64 + (c ^ ((r >> 1) & 3))*16: conflict-free for the row-per-lane
+      // writes and for the 2-rows-per-8-lanes reads).  A warp whose 32 rows
+      // are all in the output (always for MXFP8 fwd/dgrad, whose groups are
+      // multiples of 32, and for wgrad, whose 3-D map clips rows past the
+      // expert) hands each slice to a TMA store; a partial slice is written by
+      // the lanes with bounds checks.
+      const bool tma = p.tma_out && (WGRAD ? (int64_t)quarter * 32 < tl.rows : (int64_t)(quarter + 1) * 32 <= tl.rows);
+      if (!tma && (int64_t)quarter * 32 >= tl.rows) continue;
 #pragma unroll
-      for (int cc = 0; cc < BN; cc += 64) {
+      for (int j = 0; j < BN / STG_COLS; ++j) {
+        const int cc = j * STG_COLS;
         if (cc < ncols) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(stg + lane * 144 + j * 16) =
-                make_uint4(packed[(cc + j * 8) / 2], packed[(cc + j * 8) / 2 + 1], packed[(cc + j * 8) / 2 + 2],
-                           packed[(cc + j * 8) / 2 + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = i * 4 + (lane >> 3), ch = lane & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 144 + ch * 16);
-            const int64_t trow = quarter * 32 + r;
-            const int64_t col = cc + ch * 8;
-            if (trow < tl.rows && col < ncols) *reinterpret_cast<uint4*>(obase + trow * g.cols + col) = v;
+          uint8_t* buf = stg + (j & 1) * STG_BYTES;
+          // the store that last read this buffer (two slices ago) is done reading
+          if (lane == 0) {
+            if (tma) {
+              bulk_wait_read<1>();
+            } else {
+              bulk_wait_read<0>();
+            }
           }
           __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int w = (cc + c * 8) / 2;
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(packed[w], packed[w + 1], packed[w + 2], packed[w + 3]);
+          }
+          if (tma) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (WGRAD) {
+                tma_store_3d(&tmOut, buf, (int)(tl.col0 + cc), (int)(tl.row0 + quarter * 32), tl.e);
+              } else {
+                tma_store_2d(&tmOut, buf, (int)(tl.col0 + cc), (int)(tl.row0 + quarter * 32));
+              }
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = i * 8 + (lane >> 2), ch = lane & 3;
+              const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+              const int64_t trow = quarter * 32 + r;
+              const int64_t col = cc + ch * 8;
+              if (trow < tl.rows && col < ncols) *reinterpret_cast<uint4*>(obase + trow * g.cols + col) = v;
+            }
+            __syncwarp();
+          }
         }
       }
     }
+    // the output stores have left shared memory and reached global memory
+    if (lane == 0) bulk_wait_all();
   }
   __syncthreads();
   cluster_sync();
@@ -784,7 +828,8 @@ static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_
 
 template <bool MX, bool WGRAD, bool TWO>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                            const CUtensorMap& tsb, const KParams& p, int grid, cudaStream_t st) {
+                            const CUtensorMap& tsb, const CUtensorMap& tout, const KParams& p, int grid,
+                            cudaStream_t st) {
   auto kern = k_grouped_mm<MX, WGRAD, TWO>;
   constexpr int SMEM = smem_bytes<TWO>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
@@ -801,7 +846,7 @@ static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, p);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tout, p);
 }
 
 cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
@@ -872,6 +917,25 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
                    CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
+  // bf16 output tiles stored by TMA: 32 columns x 32 rows per box, 64-byte
+  // swizzle; wgrad as [E, rows, cols] so that rows past an expert are clipped
+  CUtensorMap tout = ta;
+  p.tma_out = 0;
+  if (((uintptr_t)g.out % 16) == 0 && (g.cols * 2) % 16 == 0) {
+    bool ok;
+    if (wgrad) {
+      cuuint64_t dims[3] = {(cuuint64_t)g.cols, (cuuint64_t)g.rows, (cuuint64_t)g.E};
+      cuuint64_t strides[2] = {(cuuint64_t)(g.cols * 2), (cuuint64_t)(g.rows * g.cols * 2)};
+      cuuint32_t box[3] = {(cuuint32_t)STG_COLS, 32, 1};
+      ok = make_tmap(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.out, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    } else {
+      cuuint64_t dims[2] = {(cuuint64_t)g.cols, (cuuint64_t)(g.M > 0 ? g.M : 1)};
+      cuuint64_t strides[1] = {(cuuint64_t)(g.cols * 2)};
+      cuuint32_t box[2] = {(cuuint32_t)STG_COLS, 32};
+      ok = make_tmap(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.out, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    }
+    p.tma_out = ok ? 1 : 0;
+  }
   // cta_group::2 MMAs by default (with its 6-deep ring, the faster of the two
   // on the Scout shapes: 2,695 against 2,492 TFLOP/s fwd); FP8MOE_GEMM_1CTA=1
   // selects the 1-CTA variant with B multicast, which also serves E > 512
@@ -880,15 +944,15 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
     return !(v && v[0] == '1');
   }();
   if (two && g.E <= SmemLayout<true>::MAXG) {
-    if (mx) return wgrad ? launch_t<true, true, true>(ta, tb, tsa, tsb, p, grid, st)
-                         : launch_t<true, false, true>(ta, tb, tsa, tsb, p, grid, st);
-    return wgrad ? launch_t<false, true, true>(ta, tb, tsa, tsb, p, grid, st)
-                 : launch_t<false, false, true>(ta, tb, tsa, tsb, p, grid, st);
+    if (mx) return wgrad ? launch_t<true, true, true>(ta, tb, tsa, tsb, tout, p, grid, st)
+                         : launch_t<true, false, true>(ta, tb, tsa, tsb, tout, p, grid, st);
+    return wgrad ? launch_t<false, true, true>(ta, tb, tsa, tsb, tout, p, grid, st)
+                 : launch_t<false, false, true>(ta, tb, tsa, tsb, tout, p, grid, st);
   }
-  if (mx) return wgrad ? launch_t<true, true, false>(ta, tb, tsa, tsb, p, grid, st)
-                       : launch_t<true, false, false>(ta, tb, tsa, tsb, p, grid, st);
-  return wgrad ? launch_t<false, true, false>(ta, tb, tsa, tsb, p, grid, st)
-               : launch_t<false, false, false>(ta, tb, tsa, tsb, p, grid, st);
+  if (mx) return wgrad ? launch_t<true, true, false>(ta, tb, tsa, tsb, tout, p, grid, st)
+                       : launch_t<true, false, false>(ta, tb, tsa, tsb, tout, p, grid, st);
+  return wgrad ? launch_t<false, true, false>(ta, tb, tsa, tsb, tout, p, grid, st)
+               : launch_t<false, false, false>(ta, tb, tsa, tsb, tout, p, grid, st);
 }
 
 }  // namespace fp8moe

@@ -105,6 +105,11 @@ FP8MOE_DEV void tma_load_3d_cg2(void* dst, const CUtensorMap* map, uint32_t bar,
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
+FP8MOE_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+               "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
 FP8MOE_DEV void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(map),
                "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
@@ -115,6 +120,8 @@ template <int N>
 FP8MOE_DEV void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
+// every committed bulk group of this thread has completed (writes performed)
+FP8MOE_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 FP8MOE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 FP8MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
