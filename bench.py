@@ -41,8 +41,8 @@ METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)
 # from the ncu capture summarised in profiles/k_grouped_mm_scout.md.  It is
 # reported only while the kernel source is the one that was captured.
 GEMM_TRAFFIC = {"source": "mxfp8_moe_quantization_gb300/csrc/grouped_mm.cu",
-                "sha256": "c1a50cf21246198e856f78c40b3320a0c6288d54c7fae215055d4eab99a11fd2",
-                "bytes_per_launch": (1031.354e6 + 1075.521e6 + 1569.749e6) / 3}
+                "sha256": "f3238213d60e1d449dc0530ab2edc08602669c48771ea774a21525a161901779",
+                "bytes_per_launch": (1030.698e6 + 1079.303e6 + 1567.769e6) / 3}
 
 
 def gemm_traffic():

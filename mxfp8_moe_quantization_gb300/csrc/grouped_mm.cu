@@ -90,17 +90,28 @@ FP8MOE_DEV void tc_commit_mc(uint64_t* bar, uint16_t mask) {
       "h"(mask)
       : "memory");
 }
+// completion of this thread's MMAs on the barrier at the same offset in every
+// CTA of `mask`
 template <bool TWO>
-FP8MOE_DEV void tc_commit_pair(uint64_t* bar) {
+FP8MOE_DEV void tc_commit_pair(uint64_t* bar, uint16_t mask) {
   if constexpr (TWO) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             smem_u32(bar)),
-        "h"((uint16_t)0x3)
+        "h"(mask)
         : "memory");
   } else {
-    tc_commit_mc(bar, 0x3);
+    tc_commit_mc(bar, mask);
   }
+}
+// 2-SM TMA load multicast to the CTAs of `mask`; each destination's bytes
+// complete on the barrier at `bar`'s offset in that destination's pair leader
+FP8MOE_DEV void tma_load_2d_cg2_mc(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2 "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "h"(mask)
+      : "memory");
 }
 FP8MOE_DEV uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;
@@ -253,6 +264,7 @@ struct KParams {
   int64_t cpb;        // 128x4 scale tiles per scale row block (A side and, fwd, B side)
   int64_t b_rows_pad; // fwd/dgrad: padded rows (cols of C) of one expert's scale matrix
   int n_tiles;        // tiles along the output columns
+  int n_units;        // column units: n-tiles per cluster pass (quad mode: 2 n-tiles)
   int m_tiles_w;      // wgrad: tiles along the output rows
   int tma_out;        // output stored by TMA (tmOut valid); else by thread stores
 };
@@ -270,12 +282,16 @@ struct Tile {
   int64_t sf_kblk; // first scale column block (in 128x4 tiles) of the contraction
 };
 
-// Tiles come in pairs: the two CTAs of a cluster take m-tiles 2i and 2i+1 of
-// the same group against the same B tile (shared through TMA multicast).  A
-// pair whose second m-tile lies past the group ("phantom", rows == 0) still
-// loads and releases its half of B but computes and stores nothing.
-template <bool WGRAD>
-FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* blk_prefix, int t, int rank) {
+// Tiles come in pairs: the two CTAs of a pair take m-tiles 2i and 2i+1 of
+// the same group against the same B tile (1-CTA: shared through TMA multicast;
+// 2-CTA: one M = 256 MMA).  A pair whose second m-tile lies past the group
+// ("phantom", rows == 0) still loads and releases its share of the operands
+// but stores nothing.  In quad mode (NQ = 2) the two pairs of a 4-CTA cluster
+// take adjacent n-tiles 2j and 2j+1 of the same rows and share the A tile; an
+// n-tile past the output ("phantom", col0 >= cols) stores nothing either.
+// rank: CTA within its pair; pp: pair within the cluster.
+template <bool WGRAD, int NQ>
+FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* blk_prefix, int t, int rank, int pp) {
   const GemmArgs& g = p.g;
   // last group whose tile prefix is <= t
   int lo = 0, hi = g.E - 1, e = 0;
@@ -296,7 +312,7 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
   if (!WGRAD) {
     const int mt = (int)((ge - gs + BM - 1) / BM);
     const int mp = (mt + 1) / 2;
-    const int ni = local / mp, mi = 2 * (local % mp) + rank;   // n-major: neighbours share the B tile
+    const int ni = NQ * (local / mp) + pp, mi = 2 * (local % mp) + rank;   // n-major: neighbours share B tiles
     tl.row0 = gs + (int64_t)mi * BM;
     tl.rows = (ge - tl.row0) < BM ? (ge - tl.row0) : BM;
     if (tl.rows < 0) tl.rows = 0;
@@ -307,7 +323,7 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
     tl.sf_kblk = 0;
   } else {
     const int pw = (p.m_tiles_w + 1) / 2;
-    const int ni = local / pw, mi = 2 * (local % pw) + rank;
+    const int ni = NQ * (local / pw) + pp, mi = 2 * (local % pw) + rank;
     tl.row0 = (int64_t)mi * BM;
     tl.rows = (g.rows - tl.row0) < BM ? (g.rows - tl.row0) : BM;
     if (tl.rows < 0) tl.rows = 0;
@@ -323,13 +339,16 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
   return tl;
 }
 
-template <bool MX, bool WGRAD, bool TWO>
+template <bool MX, bool WGRAD, bool TWO, bool QUAD>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                  const __grid_constant__ CUtensorMap tmOut, KParams p) {
+  static_assert(!QUAD || TWO, "quad mode pairs 2-CTA MMAs");
   using L = SmemLayout<TWO>;
   constexpr int STAGES = L::STAGES;
+  constexpr int CL = QUAD ? 4 : 2;          // cluster size
+  constexpr int NQ = QUAD ? 2 : 1;          // n-tiles per cluster pass
   // MXFP8 scale copies run on their own warp (the 2-CTA leader's)
   constexpr bool SFW = MX;
   constexpr int B_STAGE_BYTES = L::B_STAGE_BYTES;
@@ -353,14 +372,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const GemmArgs& g = p.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = (int)(blockIdx.x & 1);
+  const int crank = (int)(blockIdx.x % CL);  // rank in the cluster
+  const int rank = crank & 1;                // rank in the pair
+  const int pp = crank >> 1;                 // pair in the cluster
+  const uint32_t lead = (uint32_t)(crank & ~1);
+  const uint16_t pair_mask = (uint16_t)(0x3u << (2 * pp));
 
   // ---- setup: barriers, TMEM, the device-side group schedule ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      // 1-CTA: released by the MMAs of both CTAs; 2-CTA: by the leader's MMA
-      mbar_init(&empty[s], TWO ? 1 : 2);
+      // 1-CTA: released by the MMAs of both CTAs; 2-CTA: by the leader's MMA;
+      // quad: by both pairs' leaders (either pair writes A into this CTA)
+      mbar_init(&empty[s], TWO ? (QUAD ? 2 : 1) : 2);
     }
     for (int s = 0; s < STAGES; ++s) mbar_init(&sf_full[s], 1);
     mbar_init(tmem_full, 1);
@@ -390,10 +414,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int64_t sz = ge - gs;
     int nt, nb;
     if (!WGRAD) {
-      nt = (int)(((sz + BM - 1) / BM + 1) / 2) * p.n_tiles;
+      nt = (int)(((sz + BM - 1) / BM + 1) / 2) * p.n_units;
       nb = (int)((sz + BM - 1) / BM);
     } else {
-      nt = ((p.m_tiles_w + 1) / 2) * p.n_tiles;
+      nt = ((p.m_tiles_w + 1) / 2) * p.n_units;
       nb = MX ? (int)((sz + 127) / 128) : (int)((sz + 31) / 32 * 32);
     }
     tiles_prefix[e + 1] = sz < 0 ? 0 : nt;
@@ -444,7 +468,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_holder;
   const int total_tiles = *total_tiles_s;
-  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  // clusters stride over the tile units
+  const int pair = (int)(blockIdx.x / CL), npairs = (int)(gridDim.x / CL);
 
   if (warp == 0 && lane == 0) {
     // ======================= TMA producer =======================
@@ -452,7 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto sf_srcs = [&](const Tile& tl, int ks, const uint8_t*& sa, const uint8_t*& sb0, const uint8_t*& sb1) {
       const int64_t kb = tl.sf_kblk + ks;
       sa = (const uint8_t*)g.a_scale + (tl.sfa_blk * p.cpb + kb) * 512;
-      const int64_t nb0 = tl.col0 / 128;
+      const int64_t nb0 = tl.col0 < g.cols ? tl.col0 / 128 : 0;   // a phantom n-tile reads a valid block
       const int64_t nbl = WGRAD ? (g.cols + 127) / 128 : p.b_rows_pad / 128;
       const uint8_t* bsf = (const uint8_t*)g.b_scale + (WGRAD ? 0 : (int64_t)tl.e * p.b_rows_pad * p.cpb * 4);
       // both 128-row scale tiles of B (in 2-CTA mode each CTA's TMEM holds
@@ -463,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+      const Tile tl = get_tile<WGRAD, NQ>(p, tiles_prefix, blk_prefix, t, rank, pp);
       for (int ks = 0; ks < tl.nk; ++ks) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
           set_status(g.status, FP8MOE_ERR_TIMEOUT);
@@ -485,9 +510,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if constexpr (TWO) {
           // both CTAs' loads complete on the leader's full barrier, which
           // expects the bytes of the pair (both CTAs load the same amounts)
-          const uint32_t fb = mapa_rank(smem_u32(&full[stage]), 0);
+          const uint32_t fb = mapa_rank(smem_u32(&full[stage]), lead);
           if (rank == 0) mbar_expect_tx(&full[stage], 2 * bytes);
-          tma_load_2d_cg2(sA + stage * A_STAGE_BYTES, &tmA, fb, x, (int)tl.row0);
+          if (QUAD) {
+            // this CTA's 64 rows of the A tile, multicast to the CTA of the
+            // other pair that holds the same rows
+            tma_load_2d_cg2_mc(sA + stage * A_STAGE_BYTES + pp * (A_STAGE_BYTES / 2), &tmA, fb, x,
+                               (int)tl.row0 + pp * (BM / 2), (uint16_t)((1u << crank) | (1u << (crank ^ 2))));
+          } else {
+            tma_load_2d_cg2(sA + stage * A_STAGE_BYTES, &tmA, fb, x, (int)tl.row0);
+          }
           uint8_t* bdst = sB + stage * B_STAGE_BYTES;
           if (WGRAD) {
             tma_load_2d_cg2(bdst, &tmB, fb, x, brow);
@@ -550,7 +582,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       return !SFW || mbar_wait(&sf_full[stage], phase, abort_flag);
     };
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+      const Tile tl = get_tile<WGRAD, NQ>(p, tiles_prefix, blk_prefix, t, rank, pp);
       if (tl.nk == 0) continue;
       if (!TWO && tl.rows == 0) {
         // phantom: release each stage for the pair without computing
@@ -562,7 +594,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          tc_commit_mc(&empty[stage], 0x3);
+          tc_commit_mc(&empty[stage], pair_mask);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -621,7 +653,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int k = 0; k < 4; ++k)
             if (k < nsub) issue(k);
         }
-        tc_commit_pair<TWO>(&empty[stage]);
+        tc_commit_pair<TWO>(&empty[stage], QUAD ? (uint16_t)0xF : pair_mask);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
@@ -629,7 +661,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok) break;
       if constexpr (TWO) {
-        tc_commit_pair<true>(tmem_full);
+        tc_commit_pair<true>(tmem_full, pair_mask);
       } else {
         tc_commit(tmem_full);
       }
@@ -644,7 +676,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-        const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+        const Tile tl = get_tile<WGRAD, NQ>(p, tiles_prefix, blk_prefix, t, rank, pp);
         bool ok = true;
         for (int ks = 0; ks < tl.nk; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
@@ -681,14 +713,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) {
         if (TWO && rank == 1) {
-          mbar_arrive_remote(tmem_empty, 0);
+          mbar_arrive_remote(tmem_empty, lead);
         } else {
           mbar_arrive(tmem_empty);
         }
       }
     };
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+      const Tile tl = get_tile<WGRAD, NQ>(p, tiles_prefix, blk_prefix, t, rank, pp);
       if (!TWO && tl.rows == 0) continue;  // phantom of a 1-CTA pair: nothing computed
       const int64_t lrow = quarter * 32 + lane;
       const bool row_ok = lrow < tl.rows;
@@ -826,26 +858,44 @@ static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_
   return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides, box);
 }
 
-template <bool MX, bool WGRAD, bool TWO>
+template <bool MX, bool WGRAD, bool TWO, bool QUAD>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                            const CUtensorMap& tsb, const CUtensorMap& tout, const KParams& p, int grid,
+                            const CUtensorMap& tsb, const CUtensorMap& tout, const KParams& p, int64_t units,
                             cudaStream_t st) {
-  auto kern = k_grouped_mm<MX, WGRAD, TWO>;
+  auto kern = k_grouped_mm<MX, WGRAD, TWO, QUAD>;
+  constexpr int CL = QUAD ? 4 : 2;
   constexpr int SMEM = smem_bytes<TWO>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = dim3((unsigned)CL);
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // persistent grid: as many clusters as can be resident at once (4-CTA
+  // clusters of this size fit on fewer SMs than pairs do)
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  static int max_clusters[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_clusters[dev] <= 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = p.g.num_sms / CL;
+    }
+    max_clusters[dev] = n > 0 ? n : 1;
+  }
+  int64_t nclu = units < max_clusters[dev] ? units : max_clusters[dev];
+  if (nclu < 1) nclu = 1;
+  cfg.gridDim = dim3((unsigned)(CL * nclu));
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tout, p);
 }
 
@@ -855,9 +905,28 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   if (smem_bytes<true>() > g.max_smem || smem_bytes<false>() > g.max_smem) return cudaErrorNotSupported;
   const bool mx = g.recipe == FP8MOE_MXFP8;
   const bool wgrad = g.mode == GEMM_WGRAD;
+  // Pair modes.  Default: cta_group::2 MMAs (M = 256 per pair, 6-deep ring)
+  // in 2-CTA clusters.  FP8MOE_GEMM_CLUSTER=4 groups two pairs into a 4-CTA
+  // cluster that takes adjacent n-tiles and shares the A tile by multicast
+  // (24 KB loaded per SM and k-stage instead of 32); on the Scout shapes it
+  // measured slower (2,547 against 2,652 TFLOP/s fwd: the loads were not
+  // bandwidth-bound, and 4-CTA clusters fit on 144 of the 152 SMs).
+  // FP8MOE_GEMM_1CTA=1 selects 1-CTA MMAs with B multicast inside a pair,
+  // which also serves E > 512.
+  static const bool want_two = [] {
+    const char* v = getenv("FP8MOE_GEMM_1CTA");
+    return !(v && v[0] == '1');
+  }();
+  static const bool want_quad = [] {
+    const char* v = getenv("FP8MOE_GEMM_CLUSTER");
+    return v && v[0] == '4';
+  }();
+  const bool two = want_two && g.E <= SmemLayout<true>::MAXG;
+  const bool quad = two && want_quad;
   KParams p;
   p.g = g;
   p.n_tiles = (int)((g.cols + BN - 1) / BN);
+  p.n_units = quad ? (p.n_tiles + 1) / 2 : p.n_tiles;
   p.m_tiles_w = (int)((g.rows + BM - 1) / BM);
   if (!wgrad) {
     p.cpb = (g.kk / 32 + 3) / 4;
@@ -871,7 +940,7 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
     const int64_t arows = wgrad ? g.rows : g.M;
     cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)(arows > 0 ? arows : 1)};
     cuuint64_t strides[1] = {(cuuint64_t)g.kk};
-    cuuint32_t box[2] = {BK, BM};
+    cuuint32_t box[2] = {BK, (cuuint32_t)(quad ? BM / 2 : BM)};   // quad: each pair loads half of A
     if (!make_map(&ta, g.a, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   if (wgrad) {
@@ -885,17 +954,14 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
     cuuint32_t box[3] = {BK, BN / 2, 1};
     if (!make_map(&tb, g.b, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  // tiles are only known on the device; size the grid by an upper bound
-  int64_t bound;
-  // (pairs of tiles; each pair runs on a 2-CTA cluster)
+  // tiles are only known on the device; size the grid by an upper bound on
+  // the tile units (a unit is one pass of a cluster)
+  int64_t units;
   if (!wgrad) {
-    bound = ((g.M + 2 * BM - 1) / (2 * BM) + g.E) * p.n_tiles;
+    units = ((g.M + 2 * BM - 1) / (2 * BM) + g.E) * p.n_units;
   } else {
-    bound = (int64_t)g.E * ((p.m_tiles_w + 1) / 2) * p.n_tiles;
+    units = (int64_t)g.E * ((p.m_tiles_w + 1) / 2) * p.n_units;
   }
-  const int64_t max_pairs = g.num_sms / 2;
-  int grid = 2 * (int)(bound < max_pairs ? bound : max_pairs);
-  if (grid < 2) grid = 2;
   // MXFP8 scale buffers as 1-D u32 tensors (the 2-CTA producer loads scale
   // tiles with TMA so that they can complete on the leader's barrier)
   CUtensorMap tsa = ta, tsb = ta;
@@ -936,23 +1002,15 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
     }
     p.tma_out = ok ? 1 : 0;
   }
-  // cta_group::2 MMAs by default (with its 6-deep ring, the faster of the two
-  // on the Scout shapes: 2,695 against 2,492 TFLOP/s fwd); FP8MOE_GEMM_1CTA=1
-  // selects the 1-CTA variant with B multicast, which also serves E > 512
-  static const bool two = [] {
-    const char* v = getenv("FP8MOE_GEMM_1CTA");
-    return !(v && v[0] == '1');
-  }();
-  if (two && g.E <= SmemLayout<true>::MAXG) {
-    if (mx) return wgrad ? launch_t<true, true, true>(ta, tb, tsa, tsb, tout, p, grid, st)
-                         : launch_t<true, false, true>(ta, tb, tsa, tsb, tout, p, grid, st);
-    return wgrad ? launch_t<false, true, true>(ta, tb, tsa, tsb, tout, p, grid, st)
-                 : launch_t<false, false, true>(ta, tb, tsa, tsb, tout, p, grid, st);
-  }
-  if (mx) return wgrad ? launch_t<true, true, false>(ta, tb, tsa, tsb, tout, p, grid, st)
-                       : launch_t<true, false, false>(ta, tb, tsa, tsb, tout, p, grid, st);
-  return wgrad ? launch_t<false, true, false>(ta, tb, tsa, tsb, tout, p, grid, st)
-               : launch_t<false, false, false>(ta, tb, tsa, tsb, tout, p, grid, st);
+#define FP8MOE_GMM_LAUNCH(TWO_, QUAD_)                                                                    \
+  (mx ? (wgrad ? launch_t<true, true, TWO_, QUAD_>(ta, tb, tsa, tsb, tout, p, units, st)                  \
+               : launch_t<true, false, TWO_, QUAD_>(ta, tb, tsa, tsb, tout, p, units, st))                \
+      : (wgrad ? launch_t<false, true, TWO_, QUAD_>(ta, tb, tsa, tsb, tout, p, units, st)                 \
+               : launch_t<false, false, TWO_, QUAD_>(ta, tb, tsa, tsb, tout, p, units, st)))
+  if (quad) return FP8MOE_GMM_LAUNCH(true, true);
+  if (two) return FP8MOE_GMM_LAUNCH(true, false);
+  return FP8MOE_GMM_LAUNCH(false, false);
+#undef FP8MOE_GMM_LAUNCH
 }
 
 }  // namespace fp8moe

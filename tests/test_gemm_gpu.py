@@ -235,17 +235,19 @@ def test_many_groups_fwd(F):
     check(out, ref, bound, "mx fwd, 600 groups")
 
 
-def test_one_cta_variant():
-    """The other pair variant (1-CTA MMAs with B multicast, chosen per process
-    by FP8MOE_GEMM_1CTA=1) passes the same parity cases."""
+@pytest.mark.parametrize("env", [{"FP8MOE_GEMM_1CTA": "1"}, {"FP8MOE_GEMM_CLUSTER": "4"}],
+                         ids=["1cta_pairs", "2cta_quads"])
+def test_pair_mode_variants(env):
+    """The other pair modes (chosen per process: 1-CTA MMAs with B multicast,
+    or 2-CTA pairs grouped into 4-CTA clusters that share A) pass the same
+    parity cases."""
     import os
     import subprocess
     import sys
-    if os.environ.get("FP8MOE_GEMM_1CTA") == "1":
-        pytest.skip("this process already runs the 1-CTA variant")
+    if any(os.environ.get(k) for k in ("FP8MOE_GEMM_1CTA", "FP8MOE_GEMM_CLUSTER")):
+        pytest.skip("this process already runs a non-default variant")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, FP8MOE_GEMM_1CTA="1")
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
-                        os.path.abspath(__file__), "-k", "not one_cta_variant"],
-                       cwd=root, env=env, capture_output=True, text=True, timeout=900)
+                        os.path.abspath(__file__), "-k", "not pair_mode_variants"],
+                       cwd=root, env=dict(os.environ, **env), capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
