@@ -138,7 +138,7 @@ class ScoutStep:
             self.layers.append(self._alloc(w, a, dy))
         # fused: 3 quantize calls (2 kernels each: dim0 and dim1 with final-layout
         # scales) + 3 GEMMs per weight; unfused: 6 quantize + 6 swizzle + 3 GEMMs
-        self.launches_per_step = (9 if fused else 15) * len(self.layers)
+        self.launches_per_step = (6 if fused else 15) * len(self.layers)
 
     def _alloc(self, w, a, dy):
         import torch
@@ -179,18 +179,20 @@ class ScoutStep:
     def quant_bytes(self):
         """Algorithmic HBM bytes of the quantization launches per step.
 
-        Each of A, W, dY is quantized along both dimensions; each direction
-        reads the tensor (2 B/element) and writes codes (1 B) and one scale
-        byte per 32 elements.  Unfused, the swizzle additionally reads and
-        writes every scale byte.
+        Each of A, W, dY is quantized along both dimensions.  Fused, one
+        launch reads the tensor once (2 B/element) and writes both codes
+        (2 x 1 B) and both scale sets (2 x 1 B per 32 elements).  Unfused,
+        each direction reads the tensor and writes its codes and scales, and
+        the swizzle reads and writes every scale byte once more.
         """
         tot = 0.0
         for L in self.layers:
             M, N, K, E = self.M, L["N"], L["K"], self.E
             elems = M * K + E * N * K + M * N               # A, W, dY
-            tot += elems * 2 * (3 + 1 / 32)
-            if not self.fused:
-                tot += elems * 2 / 32 * 2
+            if self.fused:
+                tot += elems * (2 + 2 + 2 / 32)
+            else:
+                tot += elems * 2 * (3 + 1 / 32) + elems * 2 / 32 * 2
         return tot
 
     def quant_elements(self):

@@ -140,8 +140,9 @@ fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, in
  * swizzle pass).  [SCOUT] section details: forward and backward quantize the
  * same tensors (activations, weights, gradients) along the dimension their
  * GEMM contracts over, and the scales go to the 128x4 layout; [AMD-FP8]
- * aixai.ru "Три уровня оптимизации": fewer passes through HBM.  Each
- * requested direction is one fused pass over x.
+ * aixai.ru "Три уровня оптимизации": fewer passes through HBM.  With both
+ * directions requested, one launch reads x once and writes both (4 bytes
+ * moved per element instead of 6); with one, that direction's own pass.
  *
  * x [B, R, C] bf16 contiguous, R % 32 == 0 (when dim1 is produced), C % 32 == 0.
  * Either direction may be skipped by passing NULL codes.

@@ -1,0 +1,261 @@
+// MXFP8 quantization of one bf16 tensor in both directions from a single read
+// of it: dim0 (blocks of 32 along a row, codes [B, R, C]) and dim1 (blocks of
+// 32 down a column, codes transposed to [B, C, R]), each with its e8m0 scales
+// written straight into their final layout.  This is the operand preparation
+// of the MXFP8 MoE layer ("Accelerating Llama4 Scout training with TorchAO
+// MXFP8 MoE primitives": a tensor is quantized along both dimensions for the
+// forward and the two backward GEMMs); doing both from one read moves 4 bytes
+// per element instead of the 6 of two separate passes.
+//
+// Layout of the work (no shared-memory staging): a warp owns a band of up to
+// 128 rows x 128 columns and sweeps it in 32-row sub-tiles, so that every
+// 128-byte line of the transposed codes and of the scales is completed by one
+// warp within a short time (while it is still in L2); small tensors use lower
+// bands so that every warp gets work.  In a sub-tile, lane l
+// holds rows 16*(l/16) .. +15 of the 8 columns 8*(l%16) .. +7 in registers
+// (16 loads of 16 bytes, each warp load covering two 256-byte row segments).
+//   dim0: the 32-element block of a row spans 4 lanes: two shuffles give its
+//         absolute maximum; each lane encodes and stores its 8 codes, so a
+//         warp store writes two 128-byte row segments.
+//   dim1: a lane has 16 rows of each of its columns; one shuffle with the
+//         lane holding the other 16 rows gives the column block's maximum;
+//         each lane stores 16 codes per column, the two halves of a column's
+//         32-byte output segment coming from the two lanes.
+#include "common.cuh"
+#include "launch.h"
+#include "scales.cuh"
+
+namespace fp8moe {
+
+namespace {
+
+FP8MOE_DEV uint4 ld_nc16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// lane-wise max of two pairs of non-negative bf16 values (sign bits cleared):
+// the result is one of the inputs, so the maximum is exact.  Only an all-zero
+// or all-subnormal block could see a subnormal flushed, and its scale byte is
+// 0 either way (its exponent field is 0).
+FP8MOE_DEV uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// The e8m0 byte of a block, clamp(floor(log2 amax) - 8, -127, 127) + 127, is
+// max(ef, 8) - 8 for the bf16 exponent field ef of the block maximum (a zero
+// or subnormal maximum has ef = 0 and gets byte 0, as the clamp gives); 2^-e
+// is then the bf16 with exponent field 262 - max(ef, 8), a normal number.
+// x * 2^-e on two bf16 values: exact (an 8-bit significand times a power of
+// two, below 2^9 in magnitude; only values far under the e4m3 range can
+// round, and they encode to a signed zero either way)
+FP8MOE_DEV uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// four fp32 values -> four e4m3fn codes (RNE, saturating), byte i from the
+// i-th argument, packed in one word
+FP8MOE_DEV uint32_t cvt4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n .reg .b16 l, h;\n cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n"
+      " mov.b32 %0, {l, h};\n}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+FP8MOE_DEV float lo_f32(uint32_t y) { return __uint_as_float(y << 16); }
+FP8MOE_DEV float hi_f32(uint32_t y) { return __uint_as_float(y & 0xFFFF0000u); }
+// 8 codes of one row chunk (4 bf16 pairs) scaled by the pair p2
+FP8MOE_DEV uint2 enc_row8(const uint4& v, uint32_t p2) {
+  const uint32_t y0 = mul_bf16x2(v.x, p2), y1 = mul_bf16x2(v.y, p2);
+  const uint32_t y2 = mul_bf16x2(v.z, p2), y3 = mul_bf16x2(v.w, p2);
+  return make_uint2(cvt4(lo_f32(y0), hi_f32(y0), lo_f32(y1), hi_f32(y1)),
+                    cvt4(lo_f32(y2), hi_f32(y2), lo_f32(y3), hi_f32(y3)));
+}
+
+struct DualArgs {
+  const uint16_t* x;    // [B, R, C] bf16
+  int64_t B, R, C;
+  uint32_t n_ct, n_band, tiles;  // 128 columns x bands of `nsub` 32-row sub-tiles
+  uint32_t n_rt;
+  int nsub;
+  uint8_t* q0;          // [B, R, C]
+  uint8_t* q1;          // [B, C, R]
+  ScaleSpec s0;         // [B, R, C/32] in its layout
+  ScaleSpec s1;         // [B, C, R/32] in its layout
+  int* status;
+};
+
+constexpr uint32_t FULL = 0xffffffffu;
+
+// the per-row scale offset of a routing group boundary inside a 16-row run
+// (kept out of line: the unrolled row loop would otherwise carry 16 copies)
+__device__ __noinline__ int64_t s0_offset_slow(const ScaleSpec& s, const GroupTable* gt, int64_t b, int64_t row,
+                                               int64_t col, int64_t R, int64_t cols) {
+  return scale_offset(s, gt, b, row, col, R, cols);
+}
+
+// dim1 of the column pair held in word K of this lane's 16 rows: 16 codes per
+// column (this half's rows) and, when s1b is given, the two scale bytes
+// (columns 2K and 2K+1 at s1b + column * st1)
+template <int K>
+FP8MOE_DEV void dim1_pair(const uint4 (&v)[16], uint32_t mw, bool ok, uint8_t* q1c, int64_t R, uint8_t* s1b,
+                          int64_t st1) {
+  // exponent fields of the two column maxima (sign bits are clear)
+  const uint32_t efl = max((mw >> 7) & 0xFFu, 8u), efh = max(mw >> 23, 8u);
+  const uint32_t blo = efl - 8u, bhi = efh - 8u;
+  const uint32_t p2 = ((262u - efl) << 7) | ((262u - efh) << 23);
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t y[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4& w = v[4 * k + i];
+      y[i] = mul_bf16x2(K == 0 ? w.x : (K == 1 ? w.y : (K == 2 ? w.z : w.w)), p2);
+    }
+    lo[k] = cvt4(lo_f32(y[0]), lo_f32(y[1]), lo_f32(y[2]), lo_f32(y[3]));
+    hi[k] = cvt4(hi_f32(y[0]), hi_f32(y[1]), hi_f32(y[2]), hi_f32(y[3]));
+  }
+  if (ok) {
+    *reinterpret_cast<uint4*>(q1c + (2 * K) * R) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(q1c + (2 * K + 1) * R) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    if (s1b) {
+      s1b[(2 * K) * st1] = (uint8_t)blo;
+      s1b[(2 * K + 1) * st1] = (uint8_t)bhi;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
+  __shared__ GroupTable gt0, gt1;
+  if (a.s0.layout == FP8MOE_GROUP_ROWS) {
+    build_group_table(gt0, a.s0.offs, a.s0.E, a.R, false, a.status);
+    if (gt0.bad) return;
+  }
+  if (a.s1.layout == FP8MOE_GROUP_COLS) {
+    build_group_table(gt1, a.s1.offs, a.s1.E, a.R, true, a.status);
+    if (gt1.bad) return;
+  }
+  const int lane = threadIdx.x & 31, half = lane >> 4, cl = lane & 15;
+  const uint32_t nwarps = gridDim.x * (blockDim.x >> 5);
+  for (uint32_t t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.tiles; t += nwarps) {
+    const uint32_t ct = t % a.n_ct;
+    const uint32_t rest = t / a.n_ct;
+    const uint32_t rt0 = (rest % a.n_band) * a.nsub;
+    const int64_t b = rest / a.n_band;
+    for (int sub = 0; sub < a.nsub && rt0 + sub < a.n_rt; ++sub) {
+      const int64_t rt = rt0 + sub;
+      const int64_t r = rt * 32 + half * 16;   // first of this lane's 16 rows
+      const int64_t c = (int64_t)ct * 128 + cl * 8;   // first of this lane's 8 columns
+      const bool ok = c < a.C;                 // C % 32 == 0: whole 4-lane groups are in or out
+      const uint16_t* xp = a.x + (b * a.R + r) * a.C + c;
+      uint4 v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = ok ? ld_nc16(xp + i * a.C) : make_uint4(0, 0, 0, 0);
+
+      // ---- dim0: blocks of 32 along each row (4 lanes x 8 columns).
+      // Scale byte of row r + i: rows r .. r + 15 share a 32-row group of the
+      // 128x4 layout (offset step 16) or are consecutive rows (step C/32) --
+      // unless a routing group ends inside them (grouped layout only).
+      int64_t s0_base = 0, s0_step = 0;
+      if ((cl & 3) == 0 && ok) {
+        s0_base = scale_offset(a.s0, &gt0, b, r, c >> 5, a.R, a.C >> 5);
+        if (a.s0.layout == FP8MOE_SCALES_ROWMAJOR) {
+          s0_step = a.C >> 5;
+        } else if (a.s0.layout == FP8MOE_NO_GROUPS) {
+          s0_step = 16;
+        } else {
+          // grouped rows: rows r .. r + 15 lie in one routing group and in
+          // one 32-row group of the layout (the group starts on a 16-row
+          // boundary)
+          const int g = find_group(gt0.end, a.s0.E, r);
+          const int64_t gs = g == 0 ? 0 : gt0.end[g - 1];
+          if (gt0.end[g] >= r + 16 && ((r - gs) & 15) == 0) s0_step = 16;
+        }
+      }
+      uint8_t* q0p = a.q0 + (b * a.R + r) * a.C + c;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uint32_t m2 = max_u16x2(max_u16x2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
+                                max_u16x2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
+        m2 = max_u16x2(m2, __byte_perm(m2, 0, 0x1032));   // both halves: the chunk's maximum
+        m2 = max_u16x2(m2, __shfl_xor_sync(FULL, m2, 1));
+        m2 = max_u16x2(m2, __shfl_xor_sync(FULL, m2, 2));
+        const uint32_t ef = max((m2 >> 7) & 0xFFu, 8u);   // exponent field of the block maximum
+        const uint32_t byte = ef - 8u;
+        const uint32_t p2 = (262u - ef) * 0x00800080u;    // 2^-e in both bf16 halves
+        if (ok) {
+          *reinterpret_cast<uint2*>(q0p + i * a.C) = enc_row8(v[i], p2);
+          if ((cl & 3) == 0) {
+            const int64_t off =
+                s0_step ? s0_base + i * s0_step : s0_offset_slow(a.s0, &gt0, b, r + i, c >> 5, a.R, a.C >> 5);
+            a.s0.p[off] = (uint8_t)byte;
+          }
+        }
+      }
+
+      // ---- dim1: blocks of 32 down each column (16 rows here + 16 in lane ^ 16)
+      uint32_t mw[4] = {0, 0, 0, 0};   // column pairs (2k, 2k+1) as packed 16-bit maxima
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        mw[0] = max_u16x2(mw[0], v[i].x & 0x7FFF7FFFu);
+        mw[1] = max_u16x2(mw[1], v[i].y & 0x7FFF7FFFu);
+        mw[2] = max_u16x2(mw[2], v[i].z & 0x7FFF7FFFu);
+        mw[3] = max_u16x2(mw[3], v[i].w & 0x7FFF7FFFu);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mw[k] = max_u16x2(mw[k], __shfl_xor_sync(FULL, mw[k], 16));
+      // q1[b][c + j][r .. r + 15]; columns c .. c + 7 share a 32-row group of
+      // the 128x4 layout (scale step 16) or are consecutive rows of the
+      // row-major [C, R/32] scales; one lane of each pair writes them
+      uint8_t* q1c = a.q1 + (b * a.C + c) * a.R + r;
+      uint8_t* s1b = (ok && half == 0) ? a.s1.p + scale_offset(a.s1, &gt1, b, c, rt, a.C, a.R >> 5) : nullptr;
+      const int64_t st1 = a.s1.layout == FP8MOE_SCALES_ROWMAJOR ? (a.R >> 5) : 16;
+      dim1_pair<0>(v, mw[0], ok, q1c, a.R, s1b, st1);
+      dim1_pair<1>(v, mw[1], ok, q1c, a.R, s1b, st1);
+      dim1_pair<2>(v, mw[2], ok, q1c, a.R, s1b, st1);
+      dim1_pair<3>(v, mw[3], ok, q1c, a.R, s1b, st1);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void* q0, uint8_t* s0, int s0_layout,
+                           void* q1, uint8_t* s1, int s1_layout, const int32_t* offs, int64_t E, int num_sms,
+                           int* status, cudaStream_t st) {
+  if (B == 0 || R == 0 || C == 0) return cudaSuccess;
+  DualArgs a;
+  a.x = (const uint16_t*)x;
+  a.B = B;
+  a.R = R;
+  a.C = C;
+  a.n_ct = (uint32_t)((C + 127) / 128);
+  a.n_rt = (uint32_t)(R / 32);
+  // bands of 4 sub-tiles when that leaves several bands per warp, else lower
+  const int64_t warps = (int64_t)num_sms * 2 * 8;
+  a.nsub = 4;
+  while (a.nsub > 1 && (int64_t)a.n_ct * ((a.n_rt + a.nsub - 1) / a.nsub) * B < 4 * warps) a.nsub >>= 1;
+  a.n_band = (a.n_rt + a.nsub - 1) / a.nsub;
+  const int64_t tiles = (int64_t)a.n_ct * a.n_band * B;
+  if (tiles >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+  a.tiles = (uint32_t)tiles;
+  a.q0 = (uint8_t*)q0;
+  a.q1 = (uint8_t*)q1;
+  a.s0 = make_spec(s0, s0_layout, R, C / 32, offs, E);
+  a.s1 = make_spec(s1, s1_layout, C, R / 32, offs, E);
+  a.status = status;
+  int64_t grid = (a.tiles + 7) / 8;
+  const int64_t cap = (int64_t)num_sms * 2;
+  if (grid > cap) grid = cap;
+  k_mx_dual<<<(unsigned)grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8moe

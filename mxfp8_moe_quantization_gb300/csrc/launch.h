@@ -19,6 +19,10 @@ cudaError_t launch_mx_dim0(const void* x, int64_t B, int64_t R, int64_t C, void*
                            const int32_t* offs, int64_t E, int num_sms, int* status, cudaStream_t st);
 cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s, int layout,
                            const int32_t* offs, int64_t E, int num_sms, int* status, cudaStream_t st);
+// Both directions from one read of x (R % 32 == 0, C % 32 == 0).
+cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void* q0, uint8_t* s0, int s0_layout,
+                           void* q1, uint8_t* s1, int s1_layout, const int32_t* offs, int64_t E, int num_sms,
+                           int* status, cudaStream_t st);
 cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                            int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
                            int max_smem, cudaStream_t st);

@@ -323,3 +323,45 @@ def test_mx_dual_bad_offsets(F):
                                  F.GROUP_COLS)
     assert F.fp8moe_get_device_status() == 5
     assert F.fp8moe_get_device_status() == 0
+
+
+@pytest.mark.parametrize("l0,l1", [("SCALES_ROWMAJOR", "GROUP_COLS"), ("GROUP_ROWS", "SCALES_ROWMAJOR"),
+                                   ("GROUP_ROWS", "NO_GROUPS"), ("NO_GROUPS", "GROUP_COLS")])
+def test_mx_dual_mixed_layouts(F, l0, l1):
+    """Each direction's scales in its own layout; all-zero blocks (scale byte
+    0, codes 0) in both directions."""
+    sizes = [64, 0, 160, 32]
+    offs = W.offsets_from_sizes(sizes)
+    x = _bf16((256, 320), 31, 1.0)
+    x[32:64, :] = 0.0          # zero dim1 blocks (and dim0 rows)
+    x[:, 96:128] = 0.0         # zero dim0 blocks
+    q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), torch.from_numpy(offs).to(DEV), getattr(F, l0),
+                                                  getattr(F, l1))
+    r0, rs0, r1, rs1 = _mx_ref(_np(x))
+
+    def lay(rs, name, axis):
+        if name == "SCALES_ROWMAJOR":
+            return rs
+        if name == "NO_GROUPS":
+            return OS.swizzle(rs)
+        return OS.swizzle(rs, offs, axis)
+
+    assert np.array_equal(q0.cpu().numpy(), r0) and np.array_equal(q1.cpu().numpy(), r1)
+    assert np.array_equal(s0.cpu().numpy(), lay(rs0, l0, OS.GROUP_ROWS))
+    assert np.array_equal(s1.cpu().numpy(), lay(rs1, l1, OS.GROUP_COLS))
+    assert F.fp8moe_get_device_status() == 0
+
+
+def test_mx_dual_unaligned_row_groups(F):
+    """dim0 scales grouped by rows whose groups start off 16-row boundaries
+    (allowed when dim1's scales are not grouped)."""
+    sizes = [40, 0, 200, 8, 72]          # sums to 320
+    offs = W.offsets_from_sizes(sizes)
+    x = _bf16((320, 96), 41, 1.0)
+    q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), torch.from_numpy(offs).to(DEV), F.GROUP_ROWS,
+                                                  F.SCALES_ROWMAJOR)
+    r0, rs0, r1, rs1 = _mx_ref(_np(x))
+    assert np.array_equal(q0.cpu().numpy(), r0) and np.array_equal(q1.cpu().numpy(), r1)
+    assert np.array_equal(s0.cpu().numpy(), OS.swizzle(rs0, offs, OS.GROUP_ROWS))
+    assert np.array_equal(s1.cpu().numpy(), rs1)
+    assert F.fp8moe_get_device_status() == 0
