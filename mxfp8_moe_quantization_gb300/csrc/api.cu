@@ -121,8 +121,9 @@ fp8moe_status fp8moe_mxfp8_quantize_dim1(const void* x, int64_t B, int64_t R, in
   DevInfo* d;
   fp8moe_status st = device_info(&d);
   if (st) return st;
-  return cuda_result(fp8moe::launch_mx_dim1(x, B, R, C, qt, scale, FP8MOE_SCALES_ROWMAJOR, nullptr, 0, d->num_sms,
-                                            d->status, (cudaStream_t)stream));
+  return cuda_result(fp8moe::launch_mx_dual(x, B, R, C, nullptr, nullptr, FP8MOE_SCALES_ROWMAJOR, qt, scale,
+                                            FP8MOE_SCALES_ROWMAJOR, nullptr, 0, d->num_sms, d->status,
+                                            (cudaStream_t)stream));
 }
 
 fp8moe_status fp8moe_mxfp8_quantize_dual(const void* x, int64_t B, int64_t R, int64_t C, const int32_t* offs,
@@ -147,18 +148,15 @@ fp8moe_status fp8moe_mxfp8_quantize_dual(const void* x, int64_t B, int64_t R, in
   fp8moe_status st = device_info(&d);
   if (st) return st;
   // both directions: one fused launch reading x once (4 bytes moved per
-  // element instead of 6); one direction: its own kernel.  Scales go straight
-  // to their final layout either way.
+  // element instead of 6); dim1 alone: the same kernel without dim0; dim0
+  // alone: its own kernel.  Scales go straight to their final layout.
   const int64_t Eg = grouped ? E : 0;
   cudaError_t e = cudaSuccess;
-  if (q0 && q1) {
-    e = fp8moe::launch_mx_dual(x, B, R, C, q0, s0, s0_layout, q1, s1, s1_layout, offs, Eg, d->num_sms, d->status,
-                               (cudaStream_t)stream);
-  } else if (q0) {
-    e = fp8moe::launch_mx_dim0(x, B, R, C, q0, s0, s0_layout, offs, Eg, d->num_sms, d->status,
-                               (cudaStream_t)stream);
+  if (q1) {
+    e = fp8moe::launch_mx_dual(x, B, R, C, q0, s0, q0 ? s0_layout : FP8MOE_SCALES_ROWMAJOR, q1, s1, s1_layout, offs,
+                               Eg, d->num_sms, d->status, (cudaStream_t)stream);
   } else {
-    e = fp8moe::launch_mx_dim1(x, B, R, C, q1, s1, s1_layout, offs, Eg, d->num_sms, d->status,
+    e = fp8moe::launch_mx_dim0(x, B, R, C, q0, s0, s0_layout, offs, Eg, d->num_sms, d->status,
                                (cudaStream_t)stream);
   }
   return e == cudaSuccess ? FP8MOE_OK : FP8MOE_ERR_CUDA;

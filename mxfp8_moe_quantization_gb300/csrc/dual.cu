@@ -21,6 +21,8 @@
 //         lane holding the other 16 rows gives the column block's maximum;
 //         each lane stores 16 codes per column, the two halves of a column's
 //         32-byte output segment coming from the two lanes.
+#include <stdlib.h>
+
 #include "common.cuh"
 #include "launch.h"
 #include "scales.cuh"
@@ -93,19 +95,22 @@ struct DualArgs {
 
 constexpr uint32_t FULL = 0xffffffffu;
 
-// the per-row scale offset of a routing group boundary inside a 16-row run
-// (kept out of line: the unrolled row loop would otherwise carry 16 copies)
+// scale offsets off the fast paths (kept out of line: the unrolled loops
+// would otherwise carry many copies)
 __device__ __noinline__ int64_t s0_offset_slow(const ScaleSpec& s, const GroupTable* gt, int64_t b, int64_t row,
+                                               int64_t col, int64_t R, int64_t cols) {
+  return scale_offset(s, gt, b, row, col, R, cols);
+}
+__device__ __noinline__ int64_t s1_offset_slow(const ScaleSpec& s, const GroupTable* gt, int64_t b, int64_t row,
                                                int64_t col, int64_t R, int64_t cols) {
   return scale_offset(s, gt, b, row, col, R, cols);
 }
 
 // dim1 of the column pair held in word K of this lane's 16 rows: 16 codes per
-// column (this half's rows) and, when s1b is given, the two scale bytes
-// (columns 2K and 2K+1 at s1b + column * st1)
+// column (this half's rows); the two scale bytes are returned
 template <int K>
-FP8MOE_DEV void dim1_pair(const uint4 (&v)[16], uint32_t mw, bool ok, uint8_t* q1c, int64_t R, uint8_t* s1b,
-                          int64_t st1) {
+FP8MOE_DEV void dim1_pair(const uint4 (&v)[16], uint32_t mw, bool ok, uint8_t* q1c, int64_t R, uint32_t& b_lo,
+                          uint32_t& b_hi) {
   // exponent fields of the two column maxima (sign bits are clear)
   const uint32_t efl = max((mw >> 7) & 0xFFu, 8u), efh = max(mw >> 23, 8u);
   const uint32_t blo = efl - 8u, bhi = efh - 8u;
@@ -125,20 +130,21 @@ FP8MOE_DEV void dim1_pair(const uint4 (&v)[16], uint32_t mw, bool ok, uint8_t* q
   if (ok) {
     *reinterpret_cast<uint4*>(q1c + (2 * K) * R) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     *reinterpret_cast<uint4*>(q1c + (2 * K + 1) * R) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    if (s1b) {
-      s1b[(2 * K) * st1] = (uint8_t)blo;
-      s1b[(2 * K + 1) * st1] = (uint8_t)bhi;
-    }
   }
+  b_lo = blo;
+  b_hi = bhi;
 }
 
+// D0 / D1: produce the dim0 / dim1 direction (the dim1-only instance serves
+// the standalone transposed quantization)
+template <bool D0, bool D1>
 __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
   __shared__ GroupTable gt0, gt1;
-  if (a.s0.layout == FP8MOE_GROUP_ROWS) {
+  if (D0 && a.s0.layout == FP8MOE_GROUP_ROWS) {
     build_group_table(gt0, a.s0.offs, a.s0.E, a.R, false, a.status);
     if (gt0.bad) return;
   }
-  if (a.s1.layout == FP8MOE_GROUP_COLS) {
+  if (D1 && a.s1.layout == FP8MOE_GROUP_COLS) {
     build_group_table(gt1, a.s1.offs, a.s1.E, a.R, true, a.status);
     if (gt1.bad) return;
   }
@@ -149,6 +155,10 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
     const uint32_t rest = t / a.n_ct;
     const uint32_t rt0 = (rest % a.n_band) * a.nsub;
     const int64_t b = rest / a.n_band;
+    // dim1 scale bytes of this lane's 8 columns over the band's row blocks
+    // (byte `sub` of each word): the row blocks of a band are consecutive
+    // scale bytes of a column in every layout, written as one word per column
+    uint32_t sacc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     for (int sub = 0; sub < a.nsub && rt0 + sub < a.n_rt; ++sub) {
       const int64_t rt = rt0 + sub;
       const int64_t r = rt * 32 + half * 16;   // first of this lane's 16 rows
@@ -159,6 +169,7 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = ok ? ld_nc16(xp + i * a.C) : make_uint4(0, 0, 0, 0);
 
+      if (D0) {
       // ---- dim0: blocks of 32 along each row (4 lanes x 8 columns).
       // Scale byte of row r + i: rows r .. r + 15 share a 32-row group of the
       // 128x4 layout (offset step 16) or are consecutive rows (step C/32) --
@@ -200,6 +211,8 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
         }
       }
 
+      }
+      if (D1) {
       // ---- dim1: blocks of 32 down each column (16 rows here + 16 in lane ^ 16)
       uint32_t mw[4] = {0, 0, 0, 0};   // column pairs (2k, 2k+1) as packed 16-bit maxima
 #pragma unroll
@@ -211,16 +224,58 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) mw[k] = max_u16x2(mw[k], __shfl_xor_sync(FULL, mw[k], 16));
-      // q1[b][c + j][r .. r + 15]; columns c .. c + 7 share a 32-row group of
-      // the 128x4 layout (scale step 16) or are consecutive rows of the
-      // row-major [C, R/32] scales; one lane of each pair writes them
+      // q1[b][c + j][r .. r + 15]
       uint8_t* q1c = a.q1 + (b * a.C + c) * a.R + r;
-      uint8_t* s1b = (ok && half == 0) ? a.s1.p + scale_offset(a.s1, &gt1, b, c, rt, a.C, a.R >> 5) : nullptr;
-      const int64_t st1 = a.s1.layout == FP8MOE_SCALES_ROWMAJOR ? (a.R >> 5) : 16;
-      dim1_pair<0>(v, mw[0], ok, q1c, a.R, s1b, st1);
-      dim1_pair<1>(v, mw[1], ok, q1c, a.R, s1b, st1);
-      dim1_pair<2>(v, mw[2], ok, q1c, a.R, s1b, st1);
-      dim1_pair<3>(v, mw[3], ok, q1c, a.R, s1b, st1);
+      uint32_t bl, bh;
+      dim1_pair<0>(v, mw[0], ok, q1c, a.R, bl, bh);
+      sacc[0] |= bl << (8 * sub);
+      sacc[1] |= bh << (8 * sub);
+      dim1_pair<1>(v, mw[1], ok, q1c, a.R, bl, bh);
+      sacc[2] |= bl << (8 * sub);
+      sacc[3] |= bh << (8 * sub);
+      dim1_pair<2>(v, mw[2], ok, q1c, a.R, bl, bh);
+      sacc[4] |= bl << (8 * sub);
+      sacc[5] |= bh << (8 * sub);
+      dim1_pair<3>(v, mw[3], ok, q1c, a.R, bl, bh);
+      sacc[6] |= bl << (8 * sub);
+      sacc[7] |= bh << (8 * sub);
+      }
+    }
+    if (D1) {
+      // dim1 scales of the band: columns c .. c + 7 share a 32-row group of
+      // the 128x4 layout (step 16) or are consecutive rows of the row-major
+      // [C, R/32] scales (step R/32)
+      const int64_t c = (int64_t)ct * 128 + cl * 8;
+      const int nv = (int)min((uint32_t)a.nsub, a.n_rt - rt0);
+      if (half == 0 && c < a.C) {
+        const int64_t base = scale_offset(a.s1, &gt1, b, c, rt0, a.C, a.R >> 5);
+        const bool rowmajor = a.s1.layout == FP8MOE_SCALES_ROWMAJOR;
+        const int64_t st1 = rowmajor ? (a.R >> 5) : 16;
+        // the band's row blocks are consecutive scale bytes of each column:
+        // always in row-major; in a 128x4 tile while they stay inside one
+        // 4-column group of it (and, grouped, inside one routing group)
+        bool contiguous = rowmajor || (base & 3) + nv <= 4;
+        if (contiguous && a.s1.layout == FP8MOE_GROUP_COLS && nv > 1)
+          contiguous = find_group(gt1.end, a.s1.E, rt0 * 32) == find_group(gt1.end, a.s1.E, (rt0 + nv - 1) * 32);
+        uint8_t* p0 = a.s1.p + base;
+        if (contiguous && nv == 4 && ((uintptr_t)p0 & 3) == 0 && (st1 & 3) == 0) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint32_t*>(p0 + j * st1) = sacc[j];
+        } else if (contiguous && nv == 2 && ((uintptr_t)p0 & 1) == 0 && (st1 & 1) == 0) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint16_t*>(p0 + j * st1) = (uint16_t)sacc[j];
+        } else if (contiguous) {
+          for (int j = 0; j < 8; ++j)
+            for (int sb = 0; sb < nv; ++sb) p0[j * st1 + sb] = (uint8_t)(sacc[j] >> (8 * sb));
+        } else {
+          // one offset per row block; the 8 columns step by st1 from it
+          for (int sb = 0; sb < nv; ++sb) {
+            uint8_t* pb = a.s1.p + s1_offset_slow(a.s1, &gt1, b, c, rt0 + sb, a.C, a.R >> 5);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pb[j * st1] = (uint8_t)(sacc[j] >> (8 * sb));
+          }
+        }
+      }
     }
   }
 }
@@ -230,6 +285,7 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
 cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void* q0, uint8_t* s0, int s0_layout,
                            void* q1, uint8_t* s1, int s1_layout, const int32_t* offs, int64_t E, int num_sms,
                            int* status, cudaStream_t st) {
+  if (!q1) return cudaErrorInvalidValue;
   if (B == 0 || R == 0 || C == 0) return cudaSuccess;
   DualArgs a;
   a.x = (const uint16_t*)x;
@@ -242,6 +298,14 @@ cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void*
   const int64_t warps = (int64_t)num_sms * 2 * 8;
   a.nsub = 4;
   while (a.nsub > 1 && (int64_t)a.n_ct * ((a.n_rt + a.nsub - 1) / a.nsub) * B < 4 * warps) a.nsub >>= 1;
+  // FP8MOE_DUAL_BAND=1|2|4 fixes the band height (tests use it to cover every
+  // band shape on small inputs)
+  static const int force_band = [] {
+    const char* v = getenv("FP8MOE_DUAL_BAND");
+    const int n = v ? atoi(v) : 0;
+    return (n == 1 || n == 2 || n == 4) ? n : 0;
+  }();
+  if (force_band) a.nsub = force_band;
   a.n_band = (a.n_rt + a.nsub - 1) / a.nsub;
   const int64_t tiles = (int64_t)a.n_ct * a.n_band * B;
   if (tiles >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
@@ -254,7 +318,11 @@ cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void*
   int64_t grid = (a.tiles + 7) / 8;
   const int64_t cap = (int64_t)num_sms * 2;
   if (grid > cap) grid = cap;
-  k_mx_dual<<<(unsigned)grid, 256, 0, st>>>(a);
+  if (q0) {
+    k_mx_dual<true, true><<<(unsigned)grid, 256, 0, st>>>(a);
+  } else {
+    k_mx_dual<false, true><<<(unsigned)grid, 256, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -17,9 +17,8 @@ cudaError_t launch_quant_rowwise(const void* x, int64_t R, int64_t C, int64_t ld
 // FP8MOE_NO_GROUPS = 128x4 per batch, FP8MOE_GROUP_ROWS / _COLS with offs).
 cudaError_t launch_mx_dim0(const void* x, int64_t B, int64_t R, int64_t C, void* q, uint8_t* s, int layout,
                            const int32_t* offs, int64_t E, int num_sms, int* status, cudaStream_t st);
-cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s, int layout,
-                           const int32_t* offs, int64_t E, int num_sms, int* status, cudaStream_t st);
-// Both directions from one read of x (R % 32 == 0, C % 32 == 0).
+// MXFP8 along both dims from one read of x (R % 32 == 0, C % 32 == 0), or
+// dim1 alone (q0 == NULL; C % 8 == 0); scales written in their layouts.
 cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void* q0, uint8_t* s0, int s0_layout,
                            void* q1, uint8_t* s1, int s1_layout, const int32_t* offs, int64_t E, int num_sms,
                            int* status, cudaStream_t st);

@@ -222,149 +222,6 @@ cudaError_t launch_mx_dim0(const void* x, int64_t B, int64_t R, int64_t C, void*
 }
 
 // ============================================================================
-// MXFP8 dim1: persistent CTAs stream 128-row x 64-column bf16 tiles through a
-// 4-stage TMA ring (128-byte swizzle); each thread owns one (32-row block,
-// column) pair, computes its e8m0 scale and 32 codes, and writes them into a
-// swizzled 64 x 128-byte staging tile that a TMA store writes out as 64
-// contiguous 128-byte segments of the transposed output.
-// ============================================================================
-constexpr int D1_ROWS = 128, D1_COLS = 64, D1_STAGES = 4;
-constexpr int D1_IN_BYTES = D1_ROWS * D1_COLS * 2;   // 16 KB
-constexpr int D1_OUT_BYTES = D1_COLS * D1_ROWS;      // 8 KB
-constexpr int D1_SMEM = D1_STAGES * D1_IN_BYTES + 2 * D1_OUT_BYTES + 64 + 1024;
-
-struct Dim1Args {
-  int64_t B, R, C;
-  int64_t n_rt, n_ct, tiles;
-  ScaleSpec sc;
-  int* status;
-};
-
-__global__ void __launch_bounds__(256) k_mx_dim1(const __grid_constant__ CUtensorMap tin,
-                                                 const __grid_constant__ CUtensorMap tout, Dim1Args a) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* in = smem;
-  uint8_t* outb = smem + D1_STAGES * D1_IN_BYTES;
-  uint64_t* full = (uint64_t*)(outb + 2 * D1_OUT_BYTES);
-  volatile int* abort_s = (volatile int*)(full + D1_STAGES);
-  __shared__ GroupTable gt;
-  const int tid = threadIdx.x;
-  auto coords = [&](int64_t t, int& rt, int& ct, int& b) {
-    rt = (int)(t % a.n_rt);
-    ct = (int)((t / a.n_rt) % a.n_ct);
-    b = (int)(t / (a.n_rt * a.n_ct));
-  };
-  if (a.sc.layout == FP8MOE_GROUP_COLS) {
-    build_group_table(gt, a.sc.offs, a.sc.E, a.R, true, a.status);
-    if (gt.bad) return;
-  }
-  if (tid == 0) {
-    for (int s = 0; s < D1_STAGES; ++s) mbar_init(&full[s], 1);
-    *abort_s = 0;
-    mbar_fence_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    for (int s = 0; s < D1_STAGES; ++s) {
-      const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
-      if (t >= a.tiles) break;
-      int rt, ct, b;
-      coords(t, rt, ct, b);
-      mbar_expect_tx(&full[s], D1_IN_BYTES);
-      tma_load_3d(in + s * D1_IN_BYTES, &tin, &full[s], ct * D1_COLS, rt * D1_ROWS, b);
-    }
-  }
-  const int cl = tid & 63, rb = tid >> 6;
-  int it = 0;
-  for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
-    const int s = it % D1_STAGES, ob = it & 1;
-    int rt, ct, b;
-    coords(t, rt, ct, b);
-    if (tid == 0) bulk_wait_read<1>();  // the store issued two tiles ago has left staging buffer ob
-    __syncthreads();
-    if (!mbar_wait(&full[s], (uint32_t)((it / D1_STAGES) & 1), abort_s)) {
-      set_status(a.status, FP8MOE_ERR_TIMEOUT);
-      *abort_s = 1;
-    }
-    __syncthreads();
-    if (*abort_s) break;
-    const uint8_t* tile = in + s * D1_IN_BYTES;
-    float f[32];
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int r = rb * 32 + i;
-      const uint32_t h =
-          *reinterpret_cast<const uint16_t*>(tile + r * 128 + ((((cl >> 3) ^ (r & 7))) << 4) + ((cl & 7) << 1));
-      m = max(m, h & 0x7FFFu);
-      f[i] = bf16bits_to_float(h);
-    }
-    const int e = e8m0_exponent(m);
-    const float p = exp2_neg(e);
-    uint32_t w[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      w[j] = enc4<false>(__fmul_rn(f[4 * j], p), __fmul_rn(f[4 * j + 1], p), __fmul_rn(f[4 * j + 2], p),
-                         __fmul_rn(f[4 * j + 3], p));
-    uint8_t* orow = outb + ob * D1_OUT_BYTES + cl * 128;
-    *reinterpret_cast<uint4*>(orow + (((rb * 2) ^ (cl & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(orow + (((rb * 2 + 1) ^ (cl & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-    const int64_t c = (int64_t)ct * D1_COLS + cl;
-    const int64_t rbase = (int64_t)rt * D1_ROWS + rb * 32;
-    if (c < a.C && rbase < a.R)
-      a.sc.p[scale_offset(a.sc, &gt, b, c, rbase / 32, a.C, a.R / 32)] = (uint8_t)(e + 127);
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tma_store_3d(&tout, outb + ob * D1_OUT_BYTES, rt * D1_ROWS, ct * D1_COLS, b);
-      bulk_commit();
-      const int64_t t2 = t + (int64_t)D1_STAGES * gridDim.x;
-      if (t2 < a.tiles) {
-        int rt2, ct2, b2;
-        coords(t2, rt2, ct2, b2);
-        mbar_expect_tx(&full[s], D1_IN_BYTES);
-        tma_load_3d(in + s * D1_IN_BYTES, &tin, &full[s], ct2 * D1_COLS, rt2 * D1_ROWS, b2);
-      }
-    }
-  }
-  if (tid == 0) bulk_wait_read<0>();
-}
-
-cudaError_t launch_mx_dim1(const void* x, int64_t B, int64_t R, int64_t C, void* qt, uint8_t* s, int layout,
-                           const int32_t* offs, int64_t E, int num_sms, int* status, cudaStream_t st) {
-  if (B == 0 || R == 0 || C == 0) return cudaSuccess;
-  CUtensorMap tin, tout;
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)R, (cuuint64_t)B};
-    cuuint64_t strides[2] = {(cuuint64_t)(C * 2), (cuuint64_t)(R * C * 2)};
-    cuuint32_t box[3] = {D1_COLS, D1_ROWS, 1};
-    if (!make_tmap(&tin, CU_TENSOR_MAP_DATA_TYPE_UINT16, x, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)R, (cuuint64_t)C, (cuuint64_t)B};
-    cuuint64_t strides[2] = {(cuuint64_t)R, (cuuint64_t)(C * R)};
-    cuuint32_t box[3] = {D1_ROWS, D1_COLS, 1};
-    if (!make_tmap(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT8, qt, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  Dim1Args a;
-  a.B = B;
-  a.R = R;
-  a.C = C;
-  a.n_rt = (R + D1_ROWS - 1) / D1_ROWS;
-  a.n_ct = (C + D1_COLS - 1) / D1_COLS;
-  a.tiles = a.n_rt * a.n_ct * B;
-  a.sc = make_spec(s, layout, C, R / 32, offs, E);
-  a.status = status;
-  cudaError_t err = cudaFuncSetAttribute(k_mx_dim1, cudaFuncAttributeMaxDynamicSharedMemorySize, D1_SMEM);
-  if (err != cudaSuccess) return err;
-  int64_t grid = (int64_t)num_sms * 2;
-  if (grid > a.tiles) grid = a.tiles;
-  k_mx_dim1<<<(unsigned)grid, 256, D1_SMEM, st>>>(tin, tout, a);
-  return cudaGetLastError();
-}
-
-// ============================================================================
 // Colwise (per expert, per column) FP8: a 32-column strip of one group stays
 // resident in shared memory between the absmax and the cast.  Strips taller
 // than one CTA's shared memory are split over a thread-block cluster whose

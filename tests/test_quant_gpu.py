@@ -365,3 +365,38 @@ def test_mx_dual_unaligned_row_groups(F):
     assert np.array_equal(s0.cpu().numpy(), OS.swizzle(rs0, offs, OS.GROUP_ROWS))
     assert np.array_equal(s1.cpu().numpy(), rs1)
     assert F.fp8moe_get_device_status() == 0
+
+
+def test_mx_dual_unaligned_scale_buffers(F):
+    """Scale buffers at odd byte offsets (views into larger buffers) and
+    row-major scales whose rows are not a multiple of 4 bytes."""
+    x = _bf16((160, 96), 51, 1.0)                 # C/32 = 3, R/32 = 5
+    r0, rs0, r1, rs1 = _mx_ref(_np(x))
+    big0 = torch.zeros(160 * 3 + 8, dtype=torch.uint8, device=DEV)
+    big1 = torch.zeros(96 * 5 + 8, dtype=torch.uint8, device=DEV)
+    s0 = big0[1:1 + 160 * 3].view(160, 3)
+    s1 = big1[3:3 + 96 * 5].view(96, 5)
+    q0, _, q1, _ = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), None, F.SCALES_ROWMAJOR, F.SCALES_ROWMAJOR, s0=s0,
+                                                s1=s1)
+    assert np.array_equal(q0.cpu().numpy(), r0) and np.array_equal(q1.cpu().numpy(), r1)
+    assert np.array_equal(s0.cpu().numpy(), rs0) and np.array_equal(s1.cpu().numpy(), rs1)
+    qt, st = F.fp8moe_mxfp8_quantize_dim1(x.to(DEV))
+    assert np.array_equal(qt.cpu().numpy(), r1) and np.array_equal(st.cpu().numpy(), rs1)
+    assert F.fp8moe_get_device_status() == 0
+
+
+@pytest.mark.parametrize("band", ["4", "2"])
+def test_mx_dual_band_heights(band):
+    """The fused kernel's band heights (chosen by tensor size) give identical
+    results: the dual / dim1 cases rerun with the height fixed."""
+    import os
+    import subprocess
+    import sys
+    if os.environ.get("FP8MOE_DUAL_BAND"):
+        pytest.skip("this process already fixes the band height")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
+                        os.path.abspath(__file__), "-k", "(mx_dual or mx_dim1) and not band_heights"],
+                       cwd=root, env=dict(os.environ, FP8MOE_DUAL_BAND=band), capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
