@@ -266,36 +266,58 @@ __global__ void __launch_bounds__(256) k_colwise(ColwiseArgs a) {
   const int64_t c0 = (unit % nstrips) * CW_COLS;
   const int tid = threadIdx.x;
 
-  if (tid == 0) {
+  if (tid < 32) {
+    // group bounds and the padded start of group e: warp 0 reads offsets
+    // 0..e 32 at a time (coalesced) and scans the 32-padded sizes with
+    // shuffles, validating 0 <= start <= end <= R on the way
     int64_t g0 = 0, g1 = 0, P = 0;
     bool bad = false;
     if (a.offs == nullptr) {
       g0 = (int64_t)e * a.R;
       g1 = g0 + a.R;
     } else {
-      // validate every group up to e (0 <= start <= end <= R) while summing the
-      // 32-padded sizes of the earlier ones
-      int64_t prev = 0;
-      for (int j = 0; j <= e; ++j) {
-        const int64_t end = a.offs[j];
-        if (end < prev || end > a.R) {
-          bad = true;
-          break;
+      int64_t carry = 0, prev_end = 0;
+      for (int base = 0; base <= e; base += 32) {
+        const int j = base + tid;
+        const int64_t end = j <= e ? (int64_t)a.offs[j] : 0;
+        const int64_t start = __shfl_up_sync(0xffffffffu, end, 1);
+        const int64_t st = tid == 0 ? prev_end : start;
+        int64_t padded = 0;
+        if (j <= e) {
+          if (end < st || end > a.R) bad = true;
+          if (j < e) padded = (end - st + 31) / 32 * 32;
+          if (j == e) {
+            g0 = st;
+            g1 = end;
+          }
         }
-        if (j < e) P += (end - prev + 31) / 32 * 32;
-        g0 = prev;
-        g1 = end;
-        prev = end;
+        // inclusive scan of padded sizes over the lanes
+        int64_t incl = padded;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (tid >= o) incl += u;
+        }
+        if (j == e) P = carry + incl - padded;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+        prev_end = __shfl_sync(0xffffffffu, end, 31);
       }
+      // the lane that held group e has its bounds; share them
+      const int owner = e % 32;
+      g0 = __shfl_sync(0xffffffffu, g0, owner);
+      g1 = __shfl_sync(0xffffffffu, g1, owner);
+      P = __shfl_sync(0xffffffffu, P, owner);
+      bad = __any_sync(0xffffffffu, bad);
       if (e == a.E - 1 && g1 != a.R) bad = true;
     }
-    if (bad) {
-      set_status(a.status, FP8MOE_ERR_DEVICE_OFFSETS);
-      g0 = g1 = P = -1;
+    if (tid == 0) {
+      if (bad) {
+        set_status(a.status, FP8MOE_ERR_DEVICE_OFFSETS);
+        g0 = g1 = P = -1;
+      }
+      grp[0] = g0;
+      grp[1] = g1;
+      grp[2] = P;
     }
-    grp[0] = g0;
-    grp[1] = g1;
-    grp[2] = P;
   }
   __syncthreads();
   if (grp[2] < 0) return;  // invalid offsets: nothing is written (uniform across the cluster)
@@ -376,7 +398,7 @@ __global__ void __launch_bounds__(256) k_colwise(ColwiseArgs a) {
   __syncthreads();
 
   // ---- phase 2: cast and store, last window first (it is still resident) ----
-  const int qsub = tid >> 6, qrow = tid & 63;      // quantize mapping: warp = 32 rows, fixed sub
+  const int qsub = tid >> 6, qrow = tid & 63;      // quantize mapping: 8 columns (qsub) per 64 threads
   const bool qcol_ok = c0 + qsub * 8 < a.C;
   float sv[8];
 #pragma unroll
@@ -404,16 +426,30 @@ __global__ void __launch_bounds__(256) k_colwise(ColwiseArgs a) {
     for (int64_t t0 = 0; t0 < wn; t0 += CW_TCHUNK) {
       const int64_t tn = (wn - t0) < CW_TCHUNK ? (wn - t0) : CW_TCHUNK;
       __syncthreads();
-      for (int64_t r = qrow; r < tn; r += 64) {
-        const uint4 v = *reinterpret_cast<const uint4*>(buf + (t0 + r) * CW_PITCH + qsub * 16);
-        const uint32_t o0 = enc4<FNUZ>(__fmul_rn(bf16_lo(v.x), sv[0]), __fmul_rn(bf16_hi(v.x), sv[1]),
-                                       __fmul_rn(bf16_lo(v.y), sv[2]), __fmul_rn(bf16_hi(v.y), sv[3]));
-        const uint32_t o1 = enc4<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
-                                       __fmul_rn(bf16_lo(v.w), sv[6]), __fmul_rn(bf16_hi(v.w), sv[7]));
+      {
+        // 4 consecutive rows x 8 columns per thread: each column's 4 codes
+        // go to the transposed tile as one word (consecutive words across a
+        // warp: conflict-free); rows past tn encode zeros that are never
+        // copied out
+        const int r = qrow * 4;
+        if (r < tn) {
+          uint32_t col[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          tbuf[(qsub * 8 + i) * CW_TPITCH + r] = (uint8_t)(o0 >> (8 * i));
-          tbuf[(qsub * 8 + 4 + i) * CW_TPITCH + r] = (uint8_t)(o1 >> (8 * i));
+          for (int k = 0; k < 4; ++k) {
+            const uint4 v = r + k < tn ? *reinterpret_cast<const uint4*>(buf + (t0 + r + k) * CW_PITCH + qsub * 16)
+                                       : make_uint4(0, 0, 0, 0);
+            const uint32_t o0 = enc4<FNUZ>(__fmul_rn(bf16_lo(v.x), sv[0]), __fmul_rn(bf16_hi(v.x), sv[1]),
+                                           __fmul_rn(bf16_lo(v.y), sv[2]), __fmul_rn(bf16_hi(v.y), sv[3]));
+            const uint32_t o1 = enc4<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
+                                           __fmul_rn(bf16_lo(v.w), sv[6]), __fmul_rn(bf16_hi(v.w), sv[7]));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              col[i] |= ((o0 >> (8 * i)) & 0xFFu) << (8 * k);
+              col[4 + i] |= ((o1 >> (8 * i)) & 0xFFu) << (8 * k);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) *reinterpret_cast<uint32_t*>(tbuf + (qsub * 8 + i) * CW_TPITCH + r) = col[i];
         }
       }
       __syncthreads();
