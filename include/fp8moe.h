@@ -59,8 +59,9 @@ typedef enum {
 } fp8moe_fp8_kind;
 
 typedef enum {
-  FP8MOE_ROWWISE = 0,  /* fp32 scale per row / per (expert, column)   */
-  FP8MOE_MXFP8 = 1     /* e8m0 scale per 1x32 block, 128x4-tiled      */
+  FP8MOE_ROWWISE = 0,   /* fp32 scale per row / per (expert, column)  */
+  FP8MOE_MXFP8 = 1,     /* e8m0 scale per 1x32 block, 128x4-tiled     */
+  FP8MOE_TENSORWISE = 2 /* one fp32 scale per tensor                  */
 } fp8moe_recipe;
 
 enum { FP8MOE_SCALES_ROWMAJOR = -2, FP8MOE_NO_GROUPS = -1, FP8MOE_GROUP_ROWS = 0, FP8MOE_GROUP_COLS = 1 };
@@ -107,6 +108,25 @@ fp8moe_status fp8moe_quantize_rowwise(const void* x, int64_t R, int64_t C, int64
 fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, int64_t C,
                                          const int32_t* offs, int transpose_out, int kind,
                                          void* q, float* scale_inv, fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Tensorwise FP8 quantization: one scale for the whole tensor.  [AMD-FP8]
+ * aixai.ru "Скейлы: от тензора до микроблока" (the coarsest of the four
+ * granularities; tensorwise, rowwise, blockwise, MXFP8).  Same arithmetic as
+ * rowwise with the absolute maximum over every element.
+ *
+ * x and the output layouts as fp8moe_quantize_colwise_3d: dense [E, R, C]
+ * (offs NULL) or routed rows [R, C] with offs [E] over R; transpose_out 0
+ * writes q in x's layout, 1 writes [E, C, R] (dense) or the group-padded
+ * [C, fp8moe_jagged_t_cols(R, E)] (jagged; zero padding), the operand
+ * layouts of the rowwise / tensorwise grouped GEMMs.  scale_inv: one fp32
+ * (4-byte aligned), the dequantization scale 1/s; it is used as scratch by
+ * the call (stream-ordered).  Alignment: x, q 16 bytes; C % 16 == 0 when
+ * transposed, (dense) R % 16 == 0 when transposed.  kind: e4m3fn or fnuz.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_quantize_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                                         int transpose_out, int kind, void* q, float* scale_inv,
+                                         fp8moe_stream_t stream);
 
 /* Width (columns) of the transposed jagged colwise output: round_up(M + 31*E, 16). */
 int64_t fp8moe_jagged_t_cols(int64_t M, int64_t E);
@@ -201,6 +221,8 @@ fp8moe_status fp8moe_swizzle_scales_128x4(const uint8_t* s, int64_t B, int64_t R
  *   MXFP8:   a_scale = fp8moe_swizzle_scales_128x4 of [M, K/32], GROUP_ROWS;
  *            w_scale = swizzle of [E, N, K/32], NO_GROUPS, B = E.
  *   ROWWISE: a_scale fp32 [M]; w_scale fp32 [E, N].
+ *   TENSORWISE: a_scale, w_scale one fp32 each (fp8moe_quantize_tensorwise);
+ *            operand layouts as ROWWISE in every mode.
  * dgrad:    dA[m, :] = dY[m, :] . Wt[e]^T  (contraction over N)
  *   dy [M, N], wt [E, K, N] (the transposed weight from colwise / dim1
  *   quantization), out [M, K].  Scales as forward with (K <-> N).

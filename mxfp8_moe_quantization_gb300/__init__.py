@@ -17,7 +17,8 @@ from typing import Optional, Tuple
 __all__ = [
     "E4M3FN", "E4M3FNUZ", "ROWWISE", "MXFP8", "SCALES_ROWMAJOR", "NO_GROUPS", "GROUP_ROWS", "GROUP_COLS",
     "Fp8MoeError", "lib", "library_path", "SYMBOLS",
-    "fp8moe_quantize_rowwise", "fp8moe_quantize_colwise_3d", "fp8moe_jagged_t_cols",
+    "fp8moe_quantize_rowwise", "fp8moe_quantize_colwise_3d", "fp8moe_quantize_tensorwise",
+    "fp8moe_jagged_t_cols",
     "fp8moe_mxfp8_quantize_dim0", "fp8moe_mxfp8_quantize_dim1", "fp8moe_mxfp8_quantize_dual",
     "fp8moe_swizzled_scales_bytes", "fp8moe_swizzle_scales_128x4",
     "fp8moe_scaled_grouped_mm_fwd", "fp8moe_scaled_grouped_mm_dgrad",
@@ -25,7 +26,7 @@ __all__ = [
 ]
 
 E4M3FN, E4M3FNUZ = 0, 1
-ROWWISE, MXFP8 = 0, 1
+ROWWISE, MXFP8, TENSORWISE = 0, 1, 2
 SCALES_ROWMAJOR, NO_GROUPS, GROUP_ROWS, GROUP_COLS = -2, -1, 0, 1
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,6 +38,7 @@ _i64, _i32, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
 SYMBOLS = {
     "fp8moe_quantize_rowwise": (_i32, [_vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp]),
     "fp8moe_quantize_colwise_3d": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp]),
+    "fp8moe_quantize_tensorwise": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp]),
     "fp8moe_jagged_t_cols": (_i64, [_i64, _i64]),
     "fp8moe_mxfp8_quantize_dim0": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "fp8moe_mxfp8_quantize_dim1": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
@@ -158,6 +160,27 @@ def fp8moe_quantize_colwise_3d(x, offs=None, transpose_out: bool = True, kind: i
     q = _empty(qshape, torch.uint8, x) if q is None else q
     scale_inv = _empty((E_, C), torch.float32, x) if scale_inv is None else scale_inv
     _check("fp8moe_quantize_colwise_3d", _lib_raw().fp8moe_quantize_colwise_3d(
+        _ptr(x), E_, R, C, _ptr(offs), int(bool(transpose_out)), kind, _ptr(q), _ptr(scale_inv),
+        _stream(stream)))
+    return q, scale_inv
+
+
+def fp8moe_quantize_tensorwise(x, offs=None, transpose_out: bool = False, kind: int = E4M3FN,
+                               E: Optional[int] = None, q=None, scale_inv=None, stream=None):
+    """One FP8 scale for the whole tensor.  Layouts as fp8moe_quantize_colwise_3d:
+    dense x [E, R, C] (or any 2-D x as E = 1 when not transposed) or jagged
+    x [R, C] with offs.  Returns (q, scale_inv float32 [1])."""
+    torch = _torch()
+    if offs is None:
+        E_, R, C = x.shape if x.dim() == 3 else (1,) + tuple(x.shape)
+        qshape = ((E_, C, R) if x.dim() == 3 else (C, R)) if transpose_out else tuple(x.shape)
+    else:
+        R, C = x.shape
+        E_ = offs.numel() if E is None else E
+        qshape = (C, fp8moe_jagged_t_cols(R, E_)) if transpose_out else (R, C)
+    q = _empty(qshape, torch.uint8, x) if q is None else q
+    scale_inv = _empty((1,), torch.float32, x) if scale_inv is None else scale_inv
+    _check("fp8moe_quantize_tensorwise", _lib_raw().fp8moe_quantize_tensorwise(
         _ptr(x), E_, R, C, _ptr(offs), int(bool(transpose_out)), kind, _ptr(q), _ptr(scale_inv),
         _stream(stream)))
     return q, scale_inv

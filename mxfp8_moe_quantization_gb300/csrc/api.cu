@@ -189,10 +189,35 @@ fp8moe_status fp8moe_swizzle_scales_128x4(const uint8_t* s, int64_t B, int64_t R
                                             (cudaStream_t)stream));
 }
 
+fp8moe_status fp8moe_quantize_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                                         int transpose_out, int kind, void* q, float* scale_inv,
+                                         fp8moe_stream_t stream) {
+  if (E < 0 || R < 0 || C < 0 || !valid_kind(kind)) return FP8MOE_ERR_INVALID_ARG;
+  if (offs && E == 0) return FP8MOE_ERR_INVALID_ARG;
+  if (!scale_inv) return FP8MOE_ERR_INVALID_ARG;
+  if ((uintptr_t)scale_inv & 3) return FP8MOE_ERR_ALIGNMENT;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  if (E == 0 || C == 0 || (R == 0 && !(offs && transpose_out))) {
+    // nothing to cast (the jagged transposed layout still gets its zero
+    // padding below); the scale is that of an all-zero tensor
+    return cuda_result(fp8moe::launch_tensorwise(nullptr, 0, 0, 0, nullptr, 0, kind, nullptr, scale_inv,
+                                                 d->num_sms, d->status, d->max_smem, (cudaStream_t)stream));
+  }
+  if (!q || (!x && R > 0)) return FP8MOE_ERR_INVALID_ARG;
+  if ((x && !al16(x)) || !al16(q)) return FP8MOE_ERR_ALIGNMENT;
+  if (transpose_out && (C % 16 || (!offs && R % 16))) return FP8MOE_ERR_ALIGNMENT;
+  if (offs && ((uintptr_t)offs & 3)) return FP8MOE_ERR_ALIGNMENT;
+  return cuda_result(fp8moe::launch_tensorwise(x, E, R, C, offs, transpose_out, kind, q, scale_inv, d->num_sms,
+                                               d->status, d->max_smem, (cudaStream_t)stream));
+}
+
 static fp8moe_status grouped_mm(int mode, int recipe, const void* a, const void* a_scale, const void* b,
                                 const void* b_scale, const int32_t* offs, int64_t E, int64_t M, int64_t N,
                                 int64_t K, void* out, fp8moe_stream_t stream) {
-  if (recipe != FP8MOE_ROWWISE && recipe != FP8MOE_MXFP8) return FP8MOE_ERR_INVALID_ARG;
+  if (recipe != FP8MOE_ROWWISE && recipe != FP8MOE_MXFP8 && recipe != FP8MOE_TENSORWISE)
+    return FP8MOE_ERR_INVALID_ARG;
   if (E < 1 || M < 0 || N < 0 || K < 0 || E > 4096) return FP8MOE_ERR_INVALID_ARG;
   if (!offs || ((uintptr_t)offs & 3)) return FP8MOE_ERR_INVALID_ARG;
   if (N % 16 || K % 16) return FP8MOE_ERR_ALIGNMENT;
@@ -203,7 +228,9 @@ static fp8moe_status grouped_mm(int mode, int recipe, const void* a, const void*
     if (mode == fp8moe::GEMM_WGRAD && M % 32) return FP8MOE_ERR_ALIGNMENT;
   }
   if (!a || !b || !out || !a_scale || !b_scale) return FP8MOE_ERR_INVALID_ARG;
-  if (!al16(a) || !al16(b) || !al16(out) || !al16(a_scale) || !al16(b_scale)) return FP8MOE_ERR_ALIGNMENT;
+  if (!al16(a) || !al16(b) || !al16(out)) return FP8MOE_ERR_ALIGNMENT;
+  if (recipe == FP8MOE_TENSORWISE ? (((uintptr_t)a_scale | (uintptr_t)b_scale) & 3) : (!al16(a_scale) || !al16(b_scale)))
+    return FP8MOE_ERR_ALIGNMENT;
   DevInfo* d;
   fp8moe_status st = device_info(&d);
   if (st) return st;

@@ -740,13 +740,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float rscale = 1.0f;
       if (!MX && tl.rows > 0) {
         // column scales of this tile into shared memory, row scale per thread
+        // (tensorwise: one scale per operand)
+        const bool tw = g.recipe == FP8MOE_TENSORWISE;
         asm volatile("bar.sync 1, 128;" ::: "memory");
-        const float* cs = (const float*)g.b_scale + (int64_t)tl.e * g.cols + tl.col0;
-        for (int c = et; c < BN; c += 128) colscale[c] = c < ncols ? cs[c] : 0.0f;
+        const float* cs = (const float*)g.b_scale + (tw ? 0 : (int64_t)tl.e * g.cols + tl.col0);
+        for (int c = et; c < BN; c += 128) colscale[c] = c < ncols ? cs[tw ? 0 : c] : 0.0f;
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (row_ok) {
           const float* rs = (const float*)g.a_scale;
-          rscale = WGRAD ? rs[(int64_t)tl.e * g.rows + tl.row0 + lrow] : rs[tl.row0 + lrow];
+          rscale = tw ? rs[0] : (WGRAD ? rs[(int64_t)tl.e * g.rows + tl.row0 + lrow] : rs[tl.row0 + lrow]);
         }
       }
       if (!mbar_wait(tmem_full, acc_phase, abort_flag)) {

@@ -26,6 +26,16 @@ cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const
                            int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
                            int max_smem, cudaStream_t st);
 
+// colwise transposed cast with one scale from the tensor's maximum (bf16
+// bits at amax_bits); no per-column scales
+cudaError_t launch_colwise_fixed(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs, int kind,
+                                 int64_t ldt, void* q, const uint32_t* amax_bits, int* status, int max_smem,
+                                 cudaStream_t st);
+// tensorwise FP8: plain layout, or transposed (dense [E, C, R] / jagged
+// [C, fp8moe_jagged_t_cols(R, E)]); scale_inv: one float
+cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                              int transpose_out, int kind, void* q, float* scale_inv, int num_sms, int* status,
+                              int max_smem, cudaStream_t st);
 cudaError_t launch_swizzle(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, const int32_t* offs,
                            int64_t E, int group_axis, uint8_t* out, int* status, int num_sms,
                            cudaStream_t st);

@@ -245,6 +245,9 @@ struct ColwiseArgs {
   float* inv;
   int cap_rows;       // rows of the strip resident per CTA
   int* status;
+  // tensorwise mode: the bf16 bit pattern of the whole tensor's maximum
+  // replaces the per-column maxima, and no per-column scale is written
+  const uint32_t* fixed_amax;
 };
 
 template <bool FNUZ>
@@ -352,7 +355,8 @@ __global__ void __launch_bounds__(256) k_colwise(ColwiseArgs a) {
     return wn;
   };
   int64_t wn = 0;
-  for (int w = 0; w < nwin; ++w) {
+  const bool fixed = a.fixed_amax != nullptr;
+  for (int w = 0; w < (fixed ? 0 : nwin); ++w) {
     if (w > 0) __syncthreads();
     wn = load_window(w);
     for (int64_t r = lrow; r < wn; r += 64) {
@@ -376,9 +380,9 @@ __global__ void __launch_bounds__(256) k_colwise(ColwiseArgs a) {
       const uint32_t w2 = red[k * 4 + sub][hw >> 1];
       m = max(m, (hw & 1) ? (w2 >> 16) : (w2 & 0xFFFFu));
     }
-    amax_part[tid] = m;
+    amax_part[tid] = fixed ? *a.fixed_amax : m;
   }
-  if (CL > 1) {
+  if (CL > 1 && !fixed) {
     cluster.sync();
     if (tid < CW_COLS) {
       uint32_t m = 0;
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(256) k_colwise(ColwiseArgs a) {
     float s, inv;
     rowwise_scale<FNUZ>(bf16bits_to_float(amax_part[tid]), s, inv);
     s_col[tid] = s;
-    if (rank == 0 && c0 + tid < a.C) a.inv[(int64_t)e * a.C + c0 + tid] = inv;
+    if (!fixed && rank == 0 && c0 + tid < a.C) a.inv[(int64_t)e * a.C + c0 + tid] = inv;
   }
   __syncthreads();
 
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(256) k_colwise(ColwiseArgs a) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) sv[i] = s_col[(qsub * 8 + i) & 31];
   for (int w = nwin - 1; w >= 0; --w) {
-    if (w != nwin - 1) {
+    if (w != nwin - 1 || fixed) {   // (phase 1 left the last window resident)
       __syncthreads();
       wn = load_window(w);
     }
@@ -514,10 +518,11 @@ static cudaError_t launch_colwise_cl8(ColwiseArgs a, K kern, int64_t R, int64_t 
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
-                           int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
-                           int max_smem, cudaStream_t st) {
+static cudaError_t launch_colwise_impl(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                                       int transpose_out, int kind, int64_t ldt, void* q, float* inv,
+                                       const uint32_t* fixed_amax, int* status, int max_smem, cudaStream_t st) {
   ColwiseArgs a;
+  a.fixed_amax = fixed_amax;
   a.x = (const uint16_t*)x;
   a.C = C;
   a.R = R;
@@ -580,6 +585,18 @@ cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const
     }
   }
   return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                           int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
+                           int max_smem, cudaStream_t st) {
+  return launch_colwise_impl(x, E, R, C, offs, transpose_out, kind, ldt, q, inv, nullptr, status, max_smem, st);
+}
+
+cudaError_t launch_colwise_fixed(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs, int kind,
+                                 int64_t ldt, void* q, const uint32_t* amax_bits, int* status, int max_smem,
+                                 cudaStream_t st) {
+  return launch_colwise_impl(x, E, R, C, offs, 1, kind, ldt, q, nullptr, amax_bits, status, max_smem, st);
 }
 
 }  // namespace fp8moe

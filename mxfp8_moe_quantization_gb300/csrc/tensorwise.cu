@@ -1,0 +1,112 @@
+// Tensorwise FP8 quantization: one scale for a whole tensor, the coarsest of
+// the four scaling granularities ("FP8-обучение на AMD", section "Скейлы: от
+// тензора до микроблока").  The arithmetic is the rowwise one (fp32:
+// s = fmax / max(amax, 1e-12), q = RNE_sat(x * s), stored inv = 1 / s) with
+// the absolute maximum taken over every element.
+//
+// Three stream-ordered launches around the caller's one-float scale buffer,
+// which holds the maximum's bf16 bit pattern until the last one replaces it
+// by the dequantization scale:
+//   1. k_tw_amax: grid-stride 16-byte loads, warp / block maxima, one
+//      atomicMax per block (bit patterns of non-negative values order like
+//      the values);
+//   2. the cast: k_tw_cast for the plain layout, or the colwise kernel in its
+//      fixed-scale mode for the transposed / jagged layouts;
+//   3. k_tw_finalize: one thread writes fl(1 / s).
+#include "common.cuh"
+#include "launch.h"
+
+namespace fp8moe {
+
+namespace {
+
+FP8MOE_DEV uint4 ld_nc(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__global__ void __launch_bounds__(256) k_tw_amax(const uint16_t* __restrict__ x, int64_t n,
+                                                 uint32_t* __restrict__ amax_bits) {
+  __shared__ uint32_t wmax[8];
+  const int64_t nch = n / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  uint32_t m = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nch; i += stride)
+    m = max(m, absmax8_bits(ld_nc(x + i * 8)));
+  // tail elements (n % 8)
+  for (int64_t i = nch * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    m = max(m, (uint32_t)x[i] & 0x7FFFu);
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max(m, wmax[w]);
+    if (m) atomicMax(amax_bits, m);
+  }
+}
+
+template <bool FNUZ>
+__global__ void __launch_bounds__(256) k_tw_cast(const uint16_t* __restrict__ x, int64_t n, uint8_t* __restrict__ q,
+                                                 const uint32_t* __restrict__ amax_bits) {
+  float s, inv;
+  rowwise_scale<FNUZ>(bf16bits_to_float(*amax_bits), s, inv);
+  const int64_t nch = n / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nch; i += stride)
+    *reinterpret_cast<uint2*>(q + i * 8) = enc8_bf16<FNUZ>(ld_nc(x + i * 8), s);
+  for (int64_t i = nch * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
+    q[i] = (uint8_t)(enc2<FNUZ>(__fmul_rn(bf16bits_to_float(x[i]), s), 0.0f) & 0xFFu);
+}
+
+template <bool FNUZ>
+__global__ void k_tw_finalize(float* scale) {
+  float s, inv;
+  rowwise_scale<FNUZ>(bf16bits_to_float(*reinterpret_cast<const uint32_t*>(scale)), s, inv);
+  *scale = inv;
+}
+
+}  // namespace
+
+cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                              int transpose_out, int kind, void* q, float* scale_inv, int num_sms, int* status,
+                              int max_smem, cudaStream_t st) {
+  const int64_t n = (offs ? 1 : E) * R * C;
+  cudaError_t e = cudaMemsetAsync(scale_inv, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  const bool fnuz = kind == FP8MOE_E4M3FNUZ;
+  const int64_t cap = (int64_t)num_sms * 8;
+  if (n > 0) {
+    int64_t blocks = (n / 8 + 255) / 256;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    k_tw_amax<<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, n, (uint32_t*)scale_inv);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (!transpose_out) {
+      if (fnuz) {
+        k_tw_cast<true><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, n, (uint8_t*)q, (const uint32_t*)scale_inv);
+      } else {
+        k_tw_cast<false><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, n, (uint8_t*)q,
+                                                           (const uint32_t*)scale_inv);
+      }
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  }
+  if (transpose_out) {
+    // the transposed (and, jagged, group-padded) layout of the colwise
+    // kernel, with the tensor's maximum in place of per-column maxima
+    const int64_t ldt = offs ? fp8moe_jagged_t_cols(R, E) : 0;
+    e = launch_colwise_fixed(x, E, R, C, offs, kind, ldt, q, (const uint32_t*)scale_inv, status, max_smem, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (fnuz) {
+    k_tw_finalize<true><<<1, 1, 0, st>>>(scale_inv);
+  } else {
+    k_tw_finalize<false><<<1, 1, 0, st>>>(scale_inv);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fp8moe

@@ -70,6 +70,23 @@ def quantize_rowwise(x, kind: str = FN):
     return q, inv
 
 
+def quantize_tensorwise(x, kind: str = FN):
+    """One FP8 scale for the whole tensor ``x`` (any shape, bf16 values as
+    float32): the coarsest of the four scaling granularities the pages list
+    ("FP8-обучение на AMD", section "Скейлы: от тензора до микроблока": one
+    scale for the whole tensor).  The arithmetic is the rowwise one with the
+    absolute maximum taken over every element.
+
+    Returns ``(q uint8 [x.shape], inv float32 scalar)``.
+    """
+    x = _f32(x)
+    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0.0)
+    s = np.float32(np.float32(FP8_MAX[kind]) / np.maximum(amax, EPS))   # fp32 divide
+    inv = np.float32(np.float32(1.0) / s)                               # fp32 divide
+    q = encode(x * s, kind)                                             # fp32 multiply
+    return q, inv
+
+
 def quantize_colwise_3d(x, kind: str = FN, transpose_out: bool = True):
     """Per-(expert, column) FP8 quantization of dense ``x [E, R, C]``.
 

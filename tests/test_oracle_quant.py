@@ -65,6 +65,58 @@ def test_rowwise_error_bound():
     assert np.all(scaled_err <= bound)
 
 
+@pytest.mark.parametrize("kind", [F.FN, F.FNUZ])
+def test_tensorwise_amax_and_nearest_code(kind):
+    """The element of largest magnitude encodes to +-max; every code is the
+    nearest entry of the code table to x * s (ties to the even code),
+    checked by brute force over all 256 codes."""
+    x = _rand((37, 53), 11, 2.5)
+    x[3, 7] = -9.5                                   # the tensor's maximum
+    q, inv = Q.quantize_tensorwise(x, kind)
+    top = 0x7E if kind == F.FN else 0x7F
+    assert q[3, 7] == (top | 0x80)
+    s = np.float32(F.FP8_MAX[kind]) / np.float32(9.5)
+    assert inv == np.float32(np.float32(1.0) / s)
+    codes = np.arange(256)
+    vals = F.decode(codes.astype(np.uint8), kind)
+    finite = np.isfinite(vals)
+    if kind == F.FNUZ:
+        finite &= codes != 0x80
+    for v, c in zip((x * s).ravel()[:400], q.ravel()[:400]):
+        d = np.abs(vals[finite] - np.float64(v))
+        best = codes[finite][d == d.min()]
+        if len(best) > 1:       # a tie: the even mantissa
+            best = best[(best & 1) == 0]
+        if best[0] & 0x7F == 0 and kind == F.FN:
+            assert c & 0x7F == 0
+        else:
+            assert c == best[0] or (c & 0x7F) == (best[0] & 0x7F) == 0
+
+
+@pytest.mark.parametrize("kind", [F.FN, F.FNUZ])
+def test_tensorwise_representable_roundtrip_and_zero(kind):
+    """A tensor of codes times 2^j whose maximum is the largest code comes
+    back exactly, with inv = 2^j; an all-zero tensor gives zero codes and
+    inv = 1 / (max / 1e-12)."""
+    rng = np.random.default_rng(12)
+    top = 0x7E if kind == F.FN else 0x7F
+    codes = rng.integers(0, top + 1, size=(16, 24)).astype(np.uint8)
+    codes |= (rng.integers(0, 2, size=codes.shape) * 0x80).astype(np.uint8)
+    if kind == F.FNUZ:
+        codes[codes == 0x80] = 0
+    codes[0, 0] = top
+    j = -3
+    x = F.decode(codes, kind) * 2.0 ** j
+    q, inv = Q.quantize_tensorwise(x.astype(np.float32), kind)
+    assert np.array_equal(q & 0x7F, codes & 0x7F)
+    assert np.array_equal(q[(codes & 0x7F) != 0], codes[(codes & 0x7F) != 0])
+    assert inv == np.float32(2.0 ** j)
+    z = np.zeros((4, 5), np.float32)
+    qz, invz = Q.quantize_tensorwise(z, kind)
+    assert np.all(qz == 0)
+    assert invz == np.float32(np.float32(1.0) / (np.float32(F.FP8_MAX[kind]) / np.float32(1e-12)))
+
+
 def test_colwise_3d_is_rowwise_of_transpose():
     x = _rand((3, 40, 24), 4)
     qt, inv = Q.quantize_colwise_3d(x, F.FN, transpose_out=True)
