@@ -253,6 +253,41 @@ fp8moe_status fp8moe_scaled_grouped_mm_wgrad(int recipe, const void* dyt, const 
                                              fp8moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Token routing into expert groups and back.  [AMD-FP8] aixai.ru "MoE:
+ * почему DeepSeek-V3 ломал пайплайн" (tokens are routed to their experts by
+ * an offsets tensor before the fused quantization and the one-launch grouped
+ * GEMM); the MoE layer configurations pad every group to a multiple of 32
+ * rows.
+ *
+ * fp8moe_route_permute: x [T, H] bf16, topk_idx [T, k] int32 expert ids in
+ * [0, E).  Writes a [fp8moe_route_rows(T, k, E), H] bf16: group e holds the
+ * (t, j) pairs with topk_idx[t, j] == e in increasing (t, j) order starting
+ * at a 32-aligned row, followed by zero rows up to the next multiple of 32;
+ * the last group also takes the remaining rows (all zero).  offs [E] int32:
+ * the cumulative ends (multiples of 32, offs[E-1] = the row count), the
+ * offsets of the grouped GEMMs and of the grouped MXFP8 scale layouts.
+ * row_of [T, k] int32: the row of each (t, j).  topk_w [T, k] fp32 or NULL:
+ * when given, the copied rows are bf16(w * x) (the backward of a weighted
+ * combine).  Ids outside [0, E) set FP8MOE_ERR_DEVICE_OFFSETS; their rows are
+ * not written (row_of = -1).  workspace: caller-owned device memory of
+ * fp8moe_route_workspace_bytes(T, k, E) bytes.  Alignment: x, a 16 bytes,
+ * H % 8 == 0; 1 <= E <= 1024.
+ *
+ * fp8moe_route_unpermute: y [rows, N] bf16 (a grouped GEMM output), row_of as
+ * above -> out [T, N] bf16 with out[t] = sum over j (in order, fp32) of
+ * w[t, j] * y[row_of[t, j]] (w = 1 when topk_w is NULL: the backward of
+ * permute).  Alignment: y, out 16 bytes, N % 8 == 0.
+ * ------------------------------------------------------------------------ */
+int64_t fp8moe_route_rows(int64_t T, int64_t k, int64_t E);
+int64_t fp8moe_route_workspace_bytes(int64_t T, int64_t k, int64_t E);
+fp8moe_status fp8moe_route_permute(const void* x, int64_t T, int64_t H, const int32_t* topk_idx,
+                                   const float* topk_w, int64_t k, int64_t E, void* a, int32_t* offs,
+                                   int32_t* row_of, void* workspace, int64_t workspace_bytes,
+                                   fp8moe_stream_t stream);
+fp8moe_status fp8moe_route_unpermute(const void* y, int64_t T, int64_t N, const int32_t* row_of,
+                                     const float* topk_w, int64_t k, void* out, fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Device status.  Synchronizes `stream`, returns the sticky device error
  * code (an fp8moe_status value, 0 if none) in *out_code and clears it.
  * The pages' failure mode is silent ([AMD-FP8] aixai.ru "Тихая порча

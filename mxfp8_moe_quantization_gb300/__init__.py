@@ -18,7 +18,8 @@ __all__ = [
     "E4M3FN", "E4M3FNUZ", "ROWWISE", "MXFP8", "SCALES_ROWMAJOR", "NO_GROUPS", "GROUP_ROWS", "GROUP_COLS",
     "Fp8MoeError", "lib", "library_path", "SYMBOLS",
     "fp8moe_quantize_rowwise", "fp8moe_quantize_colwise_3d", "fp8moe_quantize_tensorwise",
-    "fp8moe_jagged_t_cols",
+    "fp8moe_jagged_t_cols", "fp8moe_route_rows", "fp8moe_route_workspace_bytes",
+    "fp8moe_route_permute", "fp8moe_route_unpermute",
     "fp8moe_mxfp8_quantize_dim0", "fp8moe_mxfp8_quantize_dim1", "fp8moe_mxfp8_quantize_dual",
     "fp8moe_swizzled_scales_bytes", "fp8moe_swizzle_scales_128x4",
     "fp8moe_scaled_grouped_mm_fwd", "fp8moe_scaled_grouped_mm_dgrad",
@@ -40,6 +41,10 @@ SYMBOLS = {
     "fp8moe_quantize_colwise_3d": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp]),
     "fp8moe_quantize_tensorwise": (_i32, [_vp, _i64, _i64, _i64, _vp, _i32, _i32, _vp, _vp, _vp]),
     "fp8moe_jagged_t_cols": (_i64, [_i64, _i64]),
+    "fp8moe_route_rows": (_i64, [_i64, _i64, _i64]),
+    "fp8moe_route_workspace_bytes": (_i64, [_i64, _i64, _i64]),
+    "fp8moe_route_permute": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp]),
+    "fp8moe_route_unpermute": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp]),
     "fp8moe_mxfp8_quantize_dim0": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "fp8moe_mxfp8_quantize_dim1": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "fp8moe_mxfp8_quantize_dual": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _i32, _vp]),
@@ -184,6 +189,44 @@ def fp8moe_quantize_tensorwise(x, offs=None, transpose_out: bool = False, kind: 
         _ptr(x), E_, R, C, _ptr(offs), int(bool(transpose_out)), kind, _ptr(q), _ptr(scale_inv),
         _stream(stream)))
     return q, scale_inv
+
+
+def fp8moe_route_rows(T: int, k: int, E: int) -> int:
+    return int(_lib_raw().fp8moe_route_rows(T, k, E))
+
+
+def fp8moe_route_workspace_bytes(T: int, k: int, E: int) -> int:
+    return int(_lib_raw().fp8moe_route_workspace_bytes(T, k, E))
+
+
+def fp8moe_route_permute(x, topk_idx, E: int, topk_w=None, a=None, offs=None, row_of=None, workspace=None,
+                         stream=None):
+    """x [T, H] bf16, topk_idx [T, k] int32 -> (a [rows, H] bf16, offs [E] int32,
+    row_of [T, k] int32), every expert's group padded to 32 rows."""
+    torch = _torch()
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    rows = fp8moe_route_rows(T, k, E)
+    a = _empty((rows, H), torch.bfloat16, x) if a is None else a
+    offs = _empty((E,), torch.int32, x) if offs is None else offs
+    row_of = _empty((T, k), torch.int32, x) if row_of is None else row_of
+    nbytes = fp8moe_route_workspace_bytes(T, k, E)
+    workspace = _empty((max(nbytes, 4),), torch.uint8, x) if workspace is None else workspace
+    _check("fp8moe_route_permute", _lib_raw().fp8moe_route_permute(
+        _ptr(x), T, H, _ptr(topk_idx), _ptr(topk_w), k, E, _ptr(a), _ptr(offs), _ptr(row_of),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return a, offs, row_of
+
+
+def fp8moe_route_unpermute(y, row_of, topk_w=None, out=None, stream=None):
+    """y [rows, N] bf16, row_of [T, k] -> out [T, N] bf16 (sum over k, weighted)."""
+    torch = _torch()
+    T, k = row_of.shape
+    N = y.shape[1]
+    out = _empty((T, N), torch.bfloat16, y) if out is None else out
+    _check("fp8moe_route_unpermute", _lib_raw().fp8moe_route_unpermute(
+        _ptr(y), T, N, _ptr(row_of), _ptr(topk_w), k, _ptr(out), _stream(stream)))
+    return out
 
 
 def fp8moe_mxfp8_quantize_dim0(x, q=None, scale=None, stream=None):

@@ -280,6 +280,46 @@ fp8moe_status fp8moe_scaled_grouped_mm_wgrad(int recipe, const void* dyt, const 
   return grouped_mm(fp8moe::GEMM_WGRAD, recipe, dyt, dyt_scale, at, at_scale, offs, E, M, N, K, out, stream);
 }
 
+int64_t fp8moe_route_rows(int64_t T, int64_t k, int64_t E) {
+  if (T < 0 || k < 1 || E < 1) return -1;
+  return (T * k + 31 * E + 31) / 32 * 32;
+}
+
+int64_t fp8moe_route_workspace_bytes(int64_t T, int64_t k, int64_t E) {
+  if (T < 0 || k < 1 || E < 1) return -1;
+  return fp8moe::route_workspace_bytes(T, k, E);
+}
+
+fp8moe_status fp8moe_route_permute(const void* x, int64_t T, int64_t H, const int32_t* topk_idx,
+                                   const float* topk_w, int64_t k, int64_t E, void* a, int32_t* offs,
+                                   int32_t* row_of, void* workspace, int64_t workspace_bytes,
+                                   fp8moe_stream_t stream) {
+  if (T < 0 || H < 0 || k < 1 || E < 1 || E > 1024) return FP8MOE_ERR_INVALID_ARG;
+  if (T * k > ((int64_t)1 << 30)) return FP8MOE_ERR_INVALID_ARG;
+  if (!a || !offs || !workspace || (T > 0 && (!x || !topk_idx || !row_of))) return FP8MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < fp8moe::route_workspace_bytes(T, k, E)) return FP8MOE_ERR_INVALID_ARG;
+  if (H % 8 || (x && !al16(x)) || !al16(a)) return FP8MOE_ERR_ALIGNMENT;
+  if (((uintptr_t)topk_idx | (uintptr_t)offs | (uintptr_t)row_of | (uintptr_t)topk_w | (uintptr_t)workspace) & 3)
+    return FP8MOE_ERR_ALIGNMENT;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  return cuda_result(fp8moe::launch_route_permute(x, T, H, topk_idx, topk_w, k, E, fp8moe_route_rows(T, k, E), a,
+                                                  offs, row_of, workspace, d->status, (cudaStream_t)stream));
+}
+
+fp8moe_status fp8moe_route_unpermute(const void* y, int64_t T, int64_t N, const int32_t* row_of,
+                                     const float* topk_w, int64_t k, void* out, fp8moe_stream_t stream) {
+  if (T < 0 || N < 0 || k < 1) return FP8MOE_ERR_INVALID_ARG;
+  if (T == 0 || N == 0) return FP8MOE_OK;
+  if (!y || !row_of || !out) return FP8MOE_ERR_INVALID_ARG;
+  if (N % 8 || !al16(y) || !al16(out) || (((uintptr_t)row_of | (uintptr_t)topk_w) & 3)) return FP8MOE_ERR_ALIGNMENT;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  return cuda_result(fp8moe::launch_route_unpermute(y, N, row_of, topk_w, T, k, out, (cudaStream_t)stream));
+}
+
 fp8moe_status fp8moe_get_device_status(fp8moe_stream_t stream, int32_t* out_code) {
   if (!out_code) return FP8MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FP8MOE_ERR_CUDA;
