@@ -305,7 +305,8 @@ fp8moe_status fp8moe_route_permute(const void* x, int64_t T, int64_t H, const in
   fp8moe_status st = device_info(&d);
   if (st) return st;
   return cuda_result(fp8moe::launch_route_permute(x, T, H, topk_idx, topk_w, k, E, fp8moe_route_rows(T, k, E), a,
-                                                  offs, row_of, workspace, d->status, (cudaStream_t)stream));
+                                                  offs, row_of, workspace, d->num_sms, d->status,
+                                                  (cudaStream_t)stream));
 }
 
 fp8moe_status fp8moe_route_unpermute(const void* y, int64_t T, int64_t N, const int32_t* row_of,

@@ -40,7 +40,7 @@ cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, co
 int64_t route_workspace_bytes(int64_t T, int64_t k, int64_t E);
 cudaError_t launch_route_permute(const void* x, int64_t T, int64_t H, const int32_t* idx, const float* w, int64_t k,
                                  int64_t E, int64_t rows, void* a, int32_t* offs, int32_t* row_of, void* workspace,
-                                 int* status, cudaStream_t st);
+                                 int num_sms, int* status, cudaStream_t st);
 cudaError_t launch_route_unpermute(const void* y, int64_t N, const int32_t* row_of, const float* w, int64_t T,
                                    int64_t k, void* out, cudaStream_t st);
 cudaError_t launch_swizzle(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, const int32_t* offs,

@@ -10,12 +10,12 @@
 //      device status and are skipped;
 //   2. k_route_scan (one CTA): per expert, the exclusive prefix over chunks
 //      and the padded group starts; offs; the end of each group's real rows;
-//   3. k_route_scatter: warp 0 ranks the chunk's entries stably (a warp-wide
-//      match of expert ids, per-expert running counts in shared memory), then
-//      all warps copy the routed rows with 16-byte accesses, optionally
-//      weighted (bf16(fp32(w) * x));
-//   4. k_route_zero: the padding rows of every group (and the slack of the
-//      last one) are zeroed.
+//   3. k_route_rank: per chunk, one warp ranks the entries stably (a warp-wide
+//      match of expert ids, per-expert running counts in shared memory) and
+//      writes each entry's row;
+//   4. k_route_copy: the routed rows, one warp per row over the whole GPU,
+//      16-byte accesses, optionally weighted (bf16(fp32(w) * x)), and the
+//      padding rows of every group (and the slack of the last one) zeroed.
 // Unpermute: one warp per token sums its k rows in slot order in fp32.
 #include "common.cuh"
 #include "launch.h"
@@ -51,10 +51,11 @@ __global__ void __launch_bounds__(256) k_route_count(const int32_t* __restrict__
 }
 
 // counts [nchunks][E] -> in place the first row of each (chunk, expert);
-// offs [E]; real_end [E] (end of the real rows of each group)
+// offs [E]; real_end [E] (end of the real rows of each group); pad_prefix
+// [E + 1] (padding rows of the groups before e, and the total)
 __global__ void __launch_bounds__(1024) k_route_scan(int32_t* __restrict__ counts, int nchunks, int E,
                                                      int64_t rows, int32_t* __restrict__ offs,
-                                                     int32_t* __restrict__ real_end) {
+                                                     int32_t* __restrict__ real_end, int32_t* __restrict__ pad_prefix) {
   __shared__ int64_t part[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // one expert per thread (E <= 1024): its total and the prefix over chunks
@@ -78,75 +79,109 @@ __global__ void __launch_bounds__(1024) k_route_scan(int32_t* __restrict__ count
   int64_t base = 0;
   for (int w = 0; w < warp; ++w) base += part[w];
   const int64_t start = base + incl - padded;
+  const int64_t end = tid == E - 1 ? rows : start + padded;
   if (tid < E) {
     for (int c = 0; c < nchunks; ++c) counts[(int64_t)c * E + tid] += (int)start;
-    offs[tid] = tid == E - 1 ? (int32_t)rows : (int32_t)(start + padded);
+    offs[tid] = (int32_t)end;
     real_end[tid] = (int32_t)(start + total);
   }
+  // exclusive scan of the padding row counts
+  const int64_t pad = tid < E ? end - (start + total) : 0;
+  __syncthreads();
+  int64_t pincl = pad;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t u = __shfl_up_sync(0xffffffffu, pincl, o);
+    if (lane >= o) pincl += u;
+  }
+  if (lane == 31) part[warp] = pincl;
+  __syncthreads();
+  int64_t pbase = 0;
+  for (int w = 0; w < warp; ++w) pbase += part[w];
+  if (tid < E) pad_prefix[tid] = (int32_t)(pbase + pincl - pad);
+  if (tid == E - 1) pad_prefix[E] = (int32_t)(pbase + pincl);
 }
 
-__global__ void __launch_bounds__(256) k_route_scatter(const uint16_t* __restrict__ x, int64_t H,
-                                                       const int32_t* __restrict__ idx, const float* __restrict__ w,
-                                                       int64_t n, int k, int E, const int32_t* __restrict__ first,
-                                                       uint16_t* __restrict__ a, int32_t* __restrict__ row_of) {
+__global__ void __launch_bounds__(32) k_route_rank(const int32_t* __restrict__ idx, int64_t n, int E,
+                                                   const int32_t* __restrict__ first, int32_t* __restrict__ row_of) {
   __shared__ int next[RT_MAXE];
-  __shared__ int dst[RT_CHUNK];
   const int64_t c0 = (int64_t)blockIdx.x * RT_CHUNK;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) next[e] = first[(int64_t)blockIdx.x * E + e];
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) next[e] = first[(int64_t)blockIdx.x * E + e];
+  __syncwarp();
   const int cn = (int)((n - c0) < RT_CHUNK ? (n - c0) : RT_CHUNK);
-  if (warp == 0) {
-    // stable ranks: batches of 32 entries in order; lanes with the same
-    // expert take consecutive rows in lane order
-    for (int b = 0; b < cn; b += 32) {
-      const int i = b + lane;
-      int e = i < cn ? idx[c0 + i] : -1;
-      if (e >= E) e = -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      int row = -1;
-      if (e >= 0) row = next[e] + rank;
-      __syncwarp();
-      if (e >= 0 && rank == 0) next[e] += __popc(peers);
-      __syncwarp();
-      if (i < cn) {
-        dst[i] = row;
-        row_of[c0 + i] = row;
-      }
-    }
-  }
-  __syncthreads();
-  // copy: one warp per routed row, 16 bytes per lane access
-  const int64_t nv = H / 8;
-  for (int i = warp; i < cn; i += blockDim.x >> 5) {
-    const int r = dst[i];
-    if (r < 0) continue;
-    const int64_t t = (c0 + i) / k;
-    const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
-    uint4* out = reinterpret_cast<uint4*>(a + (int64_t)r * H);
-    if (w == nullptr) {
-      for (int64_t v = lane; v < nv; v += 32) out[v] = src[v];
-    } else {
-      const float wt = w[c0 + i];
-      for (int64_t v = lane; v < nv; v += 32) {
-        const uint4 s = src[v];
-        out[v] = make_uint4(bf16x2_scaled(s.x, wt), bf16x2_scaled(s.y, wt), bf16x2_scaled(s.z, wt),
-                            bf16x2_scaled(s.w, wt));
-      }
-    }
+  // the chunk's ids, loaded up front (one per lane and batch)
+  int ids[RT_CHUNK / 32];
+#pragma unroll
+  for (int b = 0; b < RT_CHUNK / 32; ++b) ids[b] = b * 32 + lane < cn ? idx[c0 + b * 32 + lane] : -1;
+  // batches of 32 entries in order; lanes with the same expert take
+  // consecutive rows in lane order (a stable placement)
+#pragma unroll
+  for (int bb = 0; bb < RT_CHUNK / 32; ++bb) {
+    const int b = bb * 32;
+    if (b >= cn) break;
+    const int i = b + lane;
+    int e = ids[bb];
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int row = -1;
+    if (e >= 0) row = next[e] + rank;
+    __syncwarp();
+    if (e >= 0 && rank == 0) next[e] += __popc(peers);
+    __syncwarp();
+    if (i < cn) row_of[c0 + i] = row;
   }
 }
 
-// zero rows [real_end[e], offs[e]) of every group: one CTA per group
-__global__ void __launch_bounds__(256) k_route_zero(uint16_t* __restrict__ a, int64_t H,
-                                                    const int32_t* __restrict__ offs,
-                                                    const int32_t* __restrict__ real_end) {
-  const int e = blockIdx.x;
-  const int64_t r0 = real_end[e], r1 = offs[e];
-  const int64_t nv = (r1 - r0) * H / 8;
-  uint4* p = reinterpret_cast<uint4*>(a + r0 * H);
-  for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) p[v] = make_uint4(0, 0, 0, 0);
+// one warp per routed row (then one per padding row), 16 bytes per access
+__global__ void __launch_bounds__(256) k_route_copy(const uint16_t* __restrict__ x, int64_t H, const float* __restrict__ w,
+                                                    int64_t n, int k, int E, const int32_t* __restrict__ row_of,
+                                                    const int32_t* __restrict__ real_end,
+                                                    const int32_t* __restrict__ pad_prefix, uint16_t* __restrict__ a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t nv = H / 8;
+  for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < n; i += nw) {
+    const int r = row_of[i];
+    if (r < 0) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (i / k) * H);
+    uint4* out = reinterpret_cast<uint4*>(a + (int64_t)r * H);
+    const float wt = w ? w[i] : 1.0f;
+    // four 16-byte loads in flight per lane
+    int64_t v = lane;
+    for (; v + 96 < nv; v += 128) {
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = src[v + 32 * u];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        out[v + 32 * u] = w ? make_uint4(bf16x2_scaled(q[u].x, wt), bf16x2_scaled(q[u].y, wt),
+                                         bf16x2_scaled(q[u].z, wt), bf16x2_scaled(q[u].w, wt))
+                            : q[u];
+    }
+    for (; v < nv; v += 32) {
+      const uint4 q = src[v];
+      out[v] = w ? make_uint4(bf16x2_scaled(q.x, wt), bf16x2_scaled(q.y, wt), bf16x2_scaled(q.z, wt),
+                              bf16x2_scaled(q.w, wt))
+                 : q;
+    }
+  }
+  // padding rows: the p-th one overall belongs to the group g whose
+  // pad_prefix[g] <= p < pad_prefix[g + 1], at row real_end[g] + p - pad_prefix[g]
+  const int64_t npad = pad_prefix[E];
+  for (int64_t pr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pr < npad; pr += nw) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pad_prefix[mid] <= pr) {
+        lo = mid;
+      } else {
+        hi = mid - 1;
+      }
+    }
+    uint4* out = reinterpret_cast<uint4*>(a + ((int64_t)real_end[lo] + (pr - pad_prefix[lo])) * H);
+    for (int64_t v = lane; v < nv; v += 32) out[v] = make_uint4(0, 0, 0, 0);
+  }
 }
 
 __global__ void __launch_bounds__(256) k_route_unpermute(const uint16_t* __restrict__ y, int64_t N,
@@ -186,30 +221,36 @@ __global__ void __launch_bounds__(256) k_route_unpermute(const uint16_t* __restr
 int64_t route_workspace_bytes(int64_t T, int64_t k, int64_t E) {
   const int64_t n = T * k;
   const int64_t nchunks = (n + RT_CHUNK - 1) / RT_CHUNK;
-  return (nchunks * E + E) * (int64_t)sizeof(int32_t);
+  return (nchunks * E + 2 * E + 1) * (int64_t)sizeof(int32_t);
 }
 
 cudaError_t launch_route_permute(const void* x, int64_t T, int64_t H, const int32_t* idx, const float* w, int64_t k,
                                  int64_t E, int64_t rows, void* a, int32_t* offs, int32_t* row_of, void* workspace,
-                                 int* status, cudaStream_t st) {
+                                 int num_sms, int* status, cudaStream_t st) {
   if (E < 1 || E > RT_MAXE) return cudaErrorInvalidValue;
   const int64_t n = T * k;
   const int64_t nchunks = (n + RT_CHUNK - 1) / RT_CHUNK;
   int32_t* counts = (int32_t*)workspace;
   int32_t* real_end = counts + nchunks * E;
+  int32_t* pad_prefix = real_end + E;
   cudaError_t e;
   if (nchunks > 0) {
     k_route_count<<<(unsigned)nchunks, 256, 0, st>>>(idx, n, (int)E, counts, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  k_route_scan<<<1, 1024, 0, st>>>(counts, (int)nchunks, (int)E, rows, offs, real_end);
+  k_route_scan<<<1, 1024, 0, st>>>(counts, (int)nchunks, (int)E, rows, offs, real_end, pad_prefix);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nchunks > 0) {
-    k_route_scatter<<<(unsigned)nchunks, 256, 0, st>>>((const uint16_t*)x, H, idx, w, n, (int)k, (int)E, counts,
-                                                        (uint16_t*)a, row_of);
+    k_route_rank<<<(unsigned)nchunks, 32, 0, st>>>(idx, n, (int)E, counts, row_of);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  k_route_zero<<<(unsigned)E, 256, 0, st>>>((uint16_t*)a, H, offs, real_end);
+  // rows to copy or zero: about n + 31 E; 8 warps per CTA, several CTAs per SM
+  int64_t blocks = (n + 31 * E + 7) / 8;
+  const int64_t cap = (int64_t)num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  k_route_copy<<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, H, w, n, (int)k, (int)E, row_of, real_end,
+                                                 pad_prefix, (uint16_t*)a);
   return cudaGetLastError();
 }
 
