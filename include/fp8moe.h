@@ -66,6 +66,9 @@ typedef enum {
 
 enum { FP8MOE_SCALES_ROWMAJOR = -2, FP8MOE_NO_GROUPS = -1, FP8MOE_GROUP_ROWS = 0, FP8MOE_GROUP_COLS = 1 };
 
+/* Largest number of groups (experts) a call with offsets accepts. */
+enum { FP8MOE_MAX_GROUPS = 1024 };
+
 /* ------------------------------------------------------------------------
  * Rowwise FP8 quantization.  [AMD-FP8] aihirek.info "A Triton-kernelok
  * csökkentették a kvantálás költségét"; aixai.ru "Три уровня оптимизации
@@ -102,8 +105,10 @@ fp8moe_status fp8moe_quantize_rowwise(const void* x, int64_t R, int64_t C, int64
  *   gets scale_inv = fl(1 / fl(fp8_max / 1e-12)).  q is
  *   [C, fp8moe_jagged_t_cols(R, E)] when transpose_out, with group e in
  *   columns [P_e, P_e + g_e), P_e = sum_{j<e} round_up(g_j, 32), every
- *   other column 0; else [R, C].
+ *   other column 0; else [R, C].  1 <= E <= FP8MOE_MAX_GROUPS.
  * C % 16 == 0; dense transposed output also needs R % 16 == 0.
+ * scale_inv doubles as the scratch of the column maxima during the call
+ * (stream-ordered; it holds the scales when the call's work completes).
  * ------------------------------------------------------------------------ */
 fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, int64_t C,
                                          const int32_t* offs, int transpose_out, int kind,
@@ -118,8 +123,8 @@ fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, in
  * x and the output layouts as fp8moe_quantize_colwise_3d: dense [E, R, C]
  * (offs NULL) or routed rows [R, C] with offs [E] over R; transpose_out 0
  * writes q in x's layout, 1 writes [E, C, R] (dense) or the group-padded
- * [C, fp8moe_jagged_t_cols(R, E)] (jagged; zero padding), the operand
- * layouts of the rowwise / tensorwise grouped GEMMs.  scale_inv: one fp32
+ * [C, fp8moe_jagged_t_cols(R, E)] (jagged, E <= FP8MOE_MAX_GROUPS; zero
+ * padding), the operand layouts of the rowwise / tensorwise grouped GEMMs.  scale_inv: one fp32
  * (4-byte aligned), the dequantization scale 1/s; it is used as scratch by
  * the call (stream-ordered).  Alignment: x, q 16 bytes; C % 16 == 0 when
  * transposed, (dense) R % 16 == 0 when transposed.  kind: e4m3fn or fnuz.

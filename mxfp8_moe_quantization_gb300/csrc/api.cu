@@ -83,6 +83,7 @@ fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, in
                                          fp8moe_stream_t stream) {
   if (E < 0 || R < 0 || C < 0 || !valid_kind(kind)) return FP8MOE_ERR_INVALID_ARG;
   if (offs && E == 0) return FP8MOE_ERR_INVALID_ARG;
+  if (offs && E > FP8MOE_MAX_GROUPS) return FP8MOE_ERR_INVALID_ARG;
   if (E == 0 || C == 0) return FP8MOE_OK;
   if (!x || !q || !scale_inv) return FP8MOE_ERR_INVALID_ARG;
   if (!al16(x) || !al16(q) || C % 16 || ((uintptr_t)scale_inv & 3)) return FP8MOE_ERR_ALIGNMENT;
@@ -93,7 +94,7 @@ fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, in
   if (st) return st;
   const int64_t ldt = offs ? fp8moe_jagged_t_cols(R, E) : 0;
   return cuda_result(fp8moe::launch_colwise(x, E, R, C, offs, transpose_out, kind, ldt, q, scale_inv, d->status,
-                                            d->max_smem, (cudaStream_t)stream));
+                                            d->num_sms, (cudaStream_t)stream));
 }
 
 fp8moe_status fp8moe_mxfp8_quantize_dim0(const void* x, int64_t B, int64_t R, int64_t C, void* q, uint8_t* scale,
@@ -194,6 +195,7 @@ fp8moe_status fp8moe_quantize_tensorwise(const void* x, int64_t E, int64_t R, in
                                          fp8moe_stream_t stream) {
   if (E < 0 || R < 0 || C < 0 || !valid_kind(kind)) return FP8MOE_ERR_INVALID_ARG;
   if (offs && E == 0) return FP8MOE_ERR_INVALID_ARG;
+  if (offs && transpose_out && E > FP8MOE_MAX_GROUPS) return FP8MOE_ERR_INVALID_ARG;
   if (!scale_inv) return FP8MOE_ERR_INVALID_ARG;
   if ((uintptr_t)scale_inv & 3) return FP8MOE_ERR_ALIGNMENT;
   DevInfo* d;
@@ -203,14 +205,14 @@ fp8moe_status fp8moe_quantize_tensorwise(const void* x, int64_t E, int64_t R, in
     // nothing to cast (the jagged transposed layout still gets its zero
     // padding below); the scale is that of an all-zero tensor
     return cuda_result(fp8moe::launch_tensorwise(nullptr, 0, 0, 0, nullptr, 0, kind, nullptr, scale_inv,
-                                                 d->num_sms, d->status, d->max_smem, (cudaStream_t)stream));
+                                                 d->num_sms, d->status, (cudaStream_t)stream));
   }
   if (!q || (!x && R > 0)) return FP8MOE_ERR_INVALID_ARG;
   if ((x && !al16(x)) || !al16(q)) return FP8MOE_ERR_ALIGNMENT;
   if (transpose_out && (C % 16 || (!offs && R % 16))) return FP8MOE_ERR_ALIGNMENT;
   if (offs && ((uintptr_t)offs & 3)) return FP8MOE_ERR_ALIGNMENT;
   return cuda_result(fp8moe::launch_tensorwise(x, E, R, C, offs, transpose_out, kind, q, scale_inv, d->num_sms,
-                                               d->status, d->max_smem, (cudaStream_t)stream));
+                                               d->status, (cudaStream_t)stream));
 }
 
 static fp8moe_status grouped_mm(int mode, int recipe, const void* a, const void* a_scale, const void* b,

@@ -141,11 +141,11 @@ template <bool D0, bool D1>
 __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
   __shared__ GroupTable gt0, gt1;
   if (D0 && a.s0.layout == FP8MOE_GROUP_ROWS) {
-    build_group_table(gt0, a.s0.offs, a.s0.E, a.R, false, a.status);
+    build_group_table(gt0, a.s0.offs, a.s0.E, a.R, GT_ROWS128, a.status);
     if (gt0.bad) return;
   }
   if (D1 && a.s1.layout == FP8MOE_GROUP_COLS) {
-    build_group_table(gt1, a.s1.offs, a.s1.E, a.R, true, a.status);
+    build_group_table(gt1, a.s1.offs, a.s1.E, a.R, GT_COLS, a.status);
     if (gt1.bad) return;
   }
   const int lane = threadIdx.x & 31, half = lane >> 4, cl = lane & 15;

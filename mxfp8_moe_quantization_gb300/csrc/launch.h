@@ -22,20 +22,21 @@ cudaError_t launch_mx_dim0(const void* x, int64_t B, int64_t R, int64_t C, void*
 cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void* q0, uint8_t* s0, int s0_layout,
                            void* q1, uint8_t* s1, int s1_layout, const int32_t* offs, int64_t E, int num_sms,
                            int* status, cudaStream_t st);
+// colwise FP8 (colwise.cu); jagged (offs != NULL) needs E <= 1024
 cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                            int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
-                           int max_smem, cudaStream_t st);
+                           int num_sms, cudaStream_t st);
 
 // colwise transposed cast with one scale from the tensor's maximum (bf16
 // bits at amax_bits); no per-column scales
 cudaError_t launch_colwise_fixed(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs, int kind,
-                                 int64_t ldt, void* q, const uint32_t* amax_bits, int* status, int max_smem,
+                                 int64_t ldt, void* q, const uint32_t* amax_bits, int* status, int num_sms,
                                  cudaStream_t st);
 // tensorwise FP8: plain layout, or transposed (dense [E, C, R] / jagged
 // [C, fp8moe_jagged_t_cols(R, E)]); scale_inv: one float
 cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                               int transpose_out, int kind, void* q, float* scale_inv, int num_sms, int* status,
-                              int max_smem, cudaStream_t st);
+                              cudaStream_t st);
 // token routing (routing.cu)
 int64_t route_workspace_bytes(int64_t T, int64_t k, int64_t E);
 cudaError_t launch_route_permute(const void* x, int64_t T, int64_t H, const int32_t* idx, const float* w, int64_t k,

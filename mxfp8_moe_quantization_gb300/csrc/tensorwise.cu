@@ -72,7 +72,7 @@ __global__ void k_tw_finalize(float* scale) {
 
 cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                               int transpose_out, int kind, void* q, float* scale_inv, int num_sms, int* status,
-                              int max_smem, cudaStream_t st) {
+                              cudaStream_t st) {
   const int64_t n = (offs ? 1 : E) * R * C;
   cudaError_t e = cudaMemsetAsync(scale_inv, 0, sizeof(float), st);
   if (e != cudaSuccess) return e;
@@ -98,7 +98,7 @@ cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, co
     // the transposed (and, jagged, group-padded) layout of the colwise
     // kernel, with the tensor's maximum in place of per-column maxima
     const int64_t ldt = offs ? fp8moe_jagged_t_cols(R, E) : 0;
-    e = launch_colwise_fixed(x, E, R, C, offs, kind, ldt, q, (const uint32_t*)scale_inv, status, max_smem, st);
+    e = launch_colwise_fixed(x, E, R, C, offs, kind, ldt, q, (const uint32_t*)scale_inv, status, num_sms, st);
     if (e != cudaSuccess) return e;
   }
   if (fnuz) {
