@@ -258,6 +258,40 @@ fp8moe_status fp8moe_scaled_grouped_mm_wgrad(int recipe, const void* dyt, const 
                                              fp8moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * MXFP8 MoE expert layer as two composites: dynamic MXFP8 quantization of
+ * the bf16 operands followed by the scaled grouped GEMMs.  [SCOUT] section
+ * details (the _to_mxfp8_then_scaled_grouped_mm primitive quantizes the
+ * input activations and the weights to MXFP8 on the fly and then runs the
+ * scaled grouped GEMM; dynamic quantization applies in forward and
+ * backward, the weight gradient along its contracting dimension);
+ * [AMD-FP8] aixai.ru "Три уровня оптимизации" (the backward reads operands
+ * already laid out for its GEMMs instead of transposed copies).
+ *
+ * Forward: A [M, K] bf16 routed rows (groups from offs [E], multiples of
+ * 32), W [E, N, K] bf16.  One dual-direction quantization of A and one of W
+ * (each reads its tensor once), then out [M, N] bf16 = the grouped GEMM
+ * forward.  The dim1 codes and scales of A and of W (the operands of wgrad
+ * and dgrad) are kept in the workspace for the backward.
+ * Backward: dY [M, N] bf16 -> one dual-direction quantization, then
+ * dA [M, K] = dgrad(dY, W^T saved) and dW [E, N, K] = wgrad(dY^T, A^T
+ * saved); either output may be NULL to skip its GEMM.
+ * Results are bit-identical to the same chain of fp8moe_mxfp8_quantize_dual
+ * and fp8moe_scaled_grouped_mm_* calls.
+ * workspace: caller-owned device memory of fp8moe_mxfp8_moe_workspace_bytes
+ * (16-byte aligned), passed unchanged from the forward to the backward on
+ * the same stream (or after it completes); the backward overwrites the
+ * forward-only part of it.  Sizes: M, N, K multiples of 32, 1 <= E <=
+ * FP8MOE_MAX_GROUPS.  Device-side offset errors as the calls it chains.
+ * ------------------------------------------------------------------------ */
+int64_t fp8moe_mxfp8_moe_workspace_bytes(int64_t E, int64_t M, int64_t N, int64_t K);
+fp8moe_status fp8moe_mxfp8_moe_fwd(const void* a, const void* w, const int32_t* offs, int64_t E, int64_t M,
+                                   int64_t N, int64_t K, void* out, void* workspace, int64_t workspace_bytes,
+                                   fp8moe_stream_t stream);
+fp8moe_status fp8moe_mxfp8_moe_bwd(const void* dy, const int32_t* offs, int64_t E, int64_t M, int64_t N,
+                                   int64_t K, void* workspace, int64_t workspace_bytes, void* da, void* dw,
+                                   fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Token routing into expert groups and back.  [AMD-FP8] aixai.ru "MoE:
  * почему DeepSeek-V3 ломал пайплайн" (tokens are routed to their experts by
  * an offsets tensor before the fused quantization and the one-launch grouped

@@ -24,6 +24,7 @@ __all__ = [
     "fp8moe_swizzled_scales_bytes", "fp8moe_swizzle_scales_128x4",
     "fp8moe_scaled_grouped_mm_fwd", "fp8moe_scaled_grouped_mm_dgrad",
     "fp8moe_scaled_grouped_mm_wgrad", "fp8moe_get_device_status", "fp8moe_status_string",
+    "fp8moe_mxfp8_moe_workspace_bytes", "fp8moe_mxfp8_moe_fwd", "fp8moe_mxfp8_moe_bwd",
 ]
 
 E4M3FN, E4M3FNUZ = 0, 1
@@ -53,6 +54,9 @@ SYMBOLS = {
     "fp8moe_scaled_grouped_mm_fwd": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "fp8moe_scaled_grouped_mm_dgrad": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "fp8moe_scaled_grouped_mm_wgrad": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "fp8moe_mxfp8_moe_workspace_bytes": (_i64, [_i64, _i64, _i64, _i64]),
+    "fp8moe_mxfp8_moe_fwd": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _vp]),
+    "fp8moe_mxfp8_moe_bwd": (_i32, [_vp, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp]),
     "fp8moe_get_device_status": (_i32, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "fp8moe_status_string": (ctypes.c_char_p, [_i32]),
     "fp8moe_version": (_i32, []),
@@ -338,6 +342,53 @@ def fp8moe_scaled_grouped_mm_wgrad(recipe, dyt, dyt_scale, at, at_scale, offs, M
     E = offs.numel()
     return _gemm("fp8moe_scaled_grouped_mm_wgrad", recipe, dyt, dyt_scale, at, at_scale, offs, E, M, N, K,
                  out, (E, N, K), stream)
+
+
+def fp8moe_mxfp8_moe_workspace_bytes(E: int, M: int, N: int, K: int) -> int:
+    """Bytes of the workspace the MXFP8 MoE layer composites keep between
+    forward and backward (-1 for unsupported sizes)."""
+    return int(_lib_raw().fp8moe_mxfp8_moe_workspace_bytes(E, M, N, K))
+
+
+def fp8moe_mxfp8_moe_fwd(a, w, offs, workspace=None, out=None, stream=None):
+    """a [M, K] bf16 routed rows, w [E, N, K] bf16, offs [E] int32 (device).
+
+    Quantizes both operands to MXFP8 (both directions) and runs the grouped
+    GEMM forward.  Returns (out [M, N] bf16, workspace); pass the workspace
+    to fp8moe_mxfp8_moe_bwd."""
+    torch = _torch()
+    M, K = a.shape
+    E, N, _ = w.shape
+    n = fp8moe_mxfp8_moe_workspace_bytes(E, M, N, K)
+    if n < 0:
+        raise Fp8MoeError("fp8moe_mxfp8_moe_fwd", 2)
+    workspace = _empty((n,), torch.uint8, a) if workspace is None else workspace
+    out = _empty((M, N), torch.bfloat16, a) if out is None else out
+    _check("fp8moe_mxfp8_moe_fwd", _lib_raw().fp8moe_mxfp8_moe_fwd(
+        _ptr(a), _ptr(w), _ptr(offs), E, M, N, K, _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out, workspace
+
+
+def fp8moe_mxfp8_moe_bwd(dy, offs, workspace, K: int, need_da: bool = True, need_dw: bool = True,
+                         da=None, dw=None, stream=None):
+    """dy [M, N] bf16 and the forward's workspace -> (dA [M, K], dW [E, N, K])
+    bf16; a result not asked for is returned as None."""
+    torch = _torch()
+    M, N = dy.shape
+    E = offs.numel()
+    if need_da:
+        da = _empty((M, K), torch.bfloat16, dy) if da is None else da
+    else:
+        da = None
+    if need_dw:
+        dw = _empty((E, N, K), torch.bfloat16, dy) if dw is None else dw
+    else:
+        dw = None
+    _check("fp8moe_mxfp8_moe_bwd", _lib_raw().fp8moe_mxfp8_moe_bwd(
+        _ptr(dy), _ptr(offs), E, M, N, K, _ptr(workspace), workspace.numel(), _ptr(da), _ptr(dw),
+        _stream(stream)))
+    return da, dw
 
 
 def fp8moe_get_device_status(stream=None) -> int:

@@ -259,6 +259,12 @@ static fp8moe_status grouped_mm(int mode, int recipe, const void* a, const void*
     g.kk = recipe == FP8MOE_MXFP8 ? M : fp8moe_jagged_t_cols(M, E);
   }
   if (g.rows == 0 || g.cols == 0) return FP8MOE_OK;
+  if (g.kk == 0) {
+    // nothing to contract (e.g. wgrad of a batch without routed tokens):
+    // every output element is an empty sum
+    const int64_t n = (mode == fp8moe::GEMM_WGRAD ? E : 1) * g.rows * g.cols;
+    return cuda_result(cudaMemsetAsync(out, 0, (size_t)n * 2, (cudaStream_t)stream));
+  }
   cudaError_t e = fp8moe::launch_grouped_mm(g, (cudaStream_t)stream);
   if (e == cudaErrorNotSupported) return FP8MOE_ERR_UNSUPPORTED;
   return cuda_result(e);

@@ -69,3 +69,30 @@ def test_host_errors_before_launch(lib):
     assert lib.fp8moe_scaled_grouped_mm_fwd(1, p, p, p, p, None, 4, 64, 64, 64, p, None) == INVALID
     assert lib.fp8moe_scaled_grouped_mm_wgrad(1, p, p, p, p, p, 4, 48, 64, 64, p, None) == ALIGN  # M % 32
     assert lib.fp8moe_get_device_status(None, None) == INVALID
+
+
+def test_layer_workspace_and_host_errors(lib):
+    """The MoE layer composites: workspace size = the kept A^T / W^T operands
+    plus the larger of the forward-only and backward-only operands (each
+    buffer rounded up to 256 bytes); host checks before any launch."""
+    lib.fp8moe_mxfp8_moe_workspace_bytes.restype = ctypes.c_int64
+    ws = lambda *a: lib.fp8moe_mxfp8_moe_workspace_bytes(*[ctypes.c_int64(v) for v in a])
+    sw = lambda B, R, Cs, E, ax: lib.fp8moe_swizzled_scales_bytes(B, R, Cs, E, ax)
+    up = lambda v: (v + 255) // 256 * 256
+    for E, M, N, K in [(16, 16640, 8192, 5120), (4, 1024, 512, 256), (3, 0, 64, 96), (1, 32, 32, 32)]:
+        kept = up(K * M) + up(sw(1, K, M // 32, E, 1)) + up(E * K * N) + up(sw(E, K, N // 32, 0, -1))
+        fwd = up(M * K) + up(sw(1, M, K // 32, E, 0)) + up(E * N * K) + up(sw(E, N, K // 32, 0, -1))
+        bwd = up(M * N) + up(sw(1, M, N // 32, E, 0)) + up(N * M) + up(sw(1, N, M // 32, E, 1))
+        assert ws(E, M, N, K) == kept + max(fwd, bwd)
+    assert ws(4, 64, 64, 48) == -1 and ws(0, 64, 64, 64) == -1 and ws(1025, 64, 64, 64) == -1
+    p = ctypes.c_void_p(1 << 20)
+    big = ctypes.c_int64(1 << 40)
+    INVALID, ALIGN = 1, 2
+    i64 = ctypes.c_int64
+    assert lib.fp8moe_mxfp8_moe_fwd(p, p, p, i64(4), i64(64), i64(64), i64(48), p, p, big, None) == ALIGN
+    assert lib.fp8moe_mxfp8_moe_fwd(p, p, p, i64(4), i64(64), i64(64), i64(64), p, p, i64(100), None) == INVALID
+    assert lib.fp8moe_mxfp8_moe_fwd(p, p, None, i64(4), i64(64), i64(64), i64(64), p, p, big, None) == INVALID
+    assert lib.fp8moe_mxfp8_moe_bwd(p, p, i64(4), i64(64), i64(64), i64(64), None, big, p, p, None) == INVALID
+    assert lib.fp8moe_mxfp8_moe_bwd(p, p, i64(4), i64(64), i64(64), i64(64), p, big, None, None, None) == 0
+    # jagged colwise takes at most FP8MOE_MAX_GROUPS groups
+    assert lib.fp8moe_quantize_colwise_3d(p, i64(1025), i64(64), i64(32), p, 1, 0, p, p, None) == INVALID
