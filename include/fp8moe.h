@@ -61,7 +61,8 @@ typedef enum {
 typedef enum {
   FP8MOE_ROWWISE = 0,   /* fp32 scale per row / per (expert, column)  */
   FP8MOE_MXFP8 = 1,     /* e8m0 scale per 1x32 block, 128x4-tiled     */
-  FP8MOE_TENSORWISE = 2 /* one fp32 scale per tensor                  */
+  FP8MOE_TENSORWISE = 2, /* one fp32 scale per tensor                 */
+  FP8MOE_BLOCKWISE = 3   /* fp32 scale per 1x128 / 128x128 tile        */
 } fp8moe_recipe;
 
 enum { FP8MOE_SCALES_ROWMAJOR = -2, FP8MOE_NO_GROUPS = -1, FP8MOE_GROUP_ROWS = 0, FP8MOE_GROUP_COLS = 1 };
@@ -132,6 +133,40 @@ fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, in
 fp8moe_status fp8moe_quantize_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                                          int transpose_out, int kind, void* q, float* scale_inv,
                                          fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Blockwise FP8 quantization: one fp32 scale per tile.  [AMD-FP8] aixai.ru
+ * "Скейлы: от тензора до микроблока" (blockwise: a scale per tile of fixed
+ * size, between rowwise and MXFP8).  The pages give no tile size; tiles are
+ * 1 x 128 along the contracting dimension for activations and gradients,
+ * 128 x 128 for expert weights, 128 tokens per group for the operands of
+ * wgrad.  Per tile, the rowwise arithmetic: s = fl(fp8_max / max(amax,
+ * 1e-12)), q = enc(fl(x * s)) (RNE, saturating), scale_inv = fl(1 / s).
+ *
+ * _rows:   x [R, C] bf16, C % 128 == 0 -> q [R, C], scale_inv [C/128, R]
+ *          (tile-index major: the scales of one tile column are contiguous).
+ *          The row operand of forward (A over K) and dgrad (dY over N).
+ * _weight: w [E, N, K] bf16, N % 128 == K % 128 == 0 -> q [E, N, K] (forward
+ *          operand) and / or qt [E, K, N] (the transposed dgrad operand; the
+ *          same codes), scale_inv [E, N/128, K/128] serving both.  Either
+ *          output may be NULL.
+ * _tokens: x [M, C] bf16 routed rows, offs [E] device (multiples of 32,
+ *          offs[E-1] = M), C % 16 == 0 -> qt [C, M] (tokens contiguous: the
+ *          wgrad operand) and scale_inv [fp8moe_blockwise_token_blocks(M, E),
+ *          C]: row b holds the scales of token block b, the blocks of group
+ *          0 first (block j of group e = tokens [start + 128 j, min(end,
+ *          start + 128 (j + 1)))); rows past the real block count are not
+ *          written.  scale_inv 16-byte aligned.  Invalid offsets set
+ *          FP8MOE_ERR_DEVICE_OFFSETS and write nothing.
+ * kind: e4m3fn or fnuz (the GEMM takes e4m3fn).
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_quantize_blockwise_rows(const void* x, int64_t R, int64_t C, int kind, void* q,
+                                             float* scale_inv, fp8moe_stream_t stream);
+fp8moe_status fp8moe_quantize_blockwise_weight(const void* w, int64_t E, int64_t N, int64_t K, int kind, void* q,
+                                               void* qt, float* scale_inv, fp8moe_stream_t stream);
+int64_t fp8moe_blockwise_token_blocks(int64_t M, int64_t E);
+fp8moe_status fp8moe_quantize_blockwise_tokens(const void* x, int64_t M, int64_t C, const int32_t* offs, int64_t E,
+                                               int kind, void* qt, float* scale_inv, fp8moe_stream_t stream);
 
 /* Width (columns) of the transposed jagged colwise output: round_up(M + 31*E, 16). */
 int64_t fp8moe_jagged_t_cols(int64_t M, int64_t E);
@@ -238,6 +273,14 @@ fp8moe_status fp8moe_swizzle_scales_128x4(const uint8_t* s, int64_t B, int64_t R
  *            [K, M/32] with GROUP_COLS.
  *   ROWWISE: Mt = fp8moe_jagged_t_cols(M, E), the group-padded layout of
  *            fp8moe_quantize_colwise_3d; scales fp32 [E, N] and [E, K].
+ * BLOCKWISE (N % 128 == K % 128 == 0): operands and scales from
+ *   fp8moe_quantize_blockwise_*: forward a = _rows(A) with a_scale
+ *   [K/128, M], w = _weight q with w_scale [E, N/128, K/128]; dgrad dy =
+ *   _rows(dY) with [N/128, M], wt = _weight qt with the same w_scale; wgrad
+ *   (M % 32 == 0, offsets multiples of 32) dyt, at = _tokens(dY), _tokens(A)
+ *   with [blocks, N] and [blocks, K] (16-byte aligned).  Each 128-element
+ *   k-block's product is scaled by its row and column scales and summed in
+ *   fp32.
  * Sizes: M >= 0, N % 16 == 0, K % 32 == 0 (MXFP8) or K % 16 == 0 (rowwise),
  * E >= 1.  MXFP8 offsets must be multiples of 32 (device-checked).
  * ------------------------------------------------------------------------ */

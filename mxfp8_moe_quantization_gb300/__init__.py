@@ -25,10 +25,12 @@ __all__ = [
     "fp8moe_scaled_grouped_mm_fwd", "fp8moe_scaled_grouped_mm_dgrad",
     "fp8moe_scaled_grouped_mm_wgrad", "fp8moe_get_device_status", "fp8moe_status_string",
     "fp8moe_mxfp8_moe_workspace_bytes", "fp8moe_mxfp8_moe_fwd", "fp8moe_mxfp8_moe_bwd",
+    "fp8moe_quantize_blockwise_rows", "fp8moe_quantize_blockwise_weight", "fp8moe_blockwise_token_blocks",
+    "fp8moe_quantize_blockwise_tokens",
 ]
 
 E4M3FN, E4M3FNUZ = 0, 1
-ROWWISE, MXFP8, TENSORWISE = 0, 1, 2
+ROWWISE, MXFP8, TENSORWISE, BLOCKWISE = 0, 1, 2, 3
 SCALES_ROWMAJOR, NO_GROUPS, GROUP_ROWS, GROUP_COLS = -2, -1, 0, 1
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -54,6 +56,10 @@ SYMBOLS = {
     "fp8moe_scaled_grouped_mm_fwd": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "fp8moe_scaled_grouped_mm_dgrad": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "fp8moe_scaled_grouped_mm_wgrad": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "fp8moe_quantize_blockwise_rows": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
+    "fp8moe_quantize_blockwise_weight": (_i32, [_vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
+    "fp8moe_blockwise_token_blocks": (_i64, [_i64, _i64]),
+    "fp8moe_quantize_blockwise_tokens": (_i32, [_vp, _i64, _i64, _vp, _i64, _i32, _vp, _vp, _vp]),
     "fp8moe_mxfp8_moe_workspace_bytes": (_i64, [_i64, _i64, _i64, _i64]),
     "fp8moe_mxfp8_moe_fwd": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _vp]),
     "fp8moe_mxfp8_moe_bwd": (_i32, [_vp, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp]),
@@ -342,6 +348,50 @@ def fp8moe_scaled_grouped_mm_wgrad(recipe, dyt, dyt_scale, at, at_scale, offs, M
     E = offs.numel()
     return _gemm("fp8moe_scaled_grouped_mm_wgrad", recipe, dyt, dyt_scale, at, at_scale, offs, E, M, N, K,
                  out, (E, N, K), stream)
+
+
+def fp8moe_quantize_blockwise_rows(x, kind: int = E4M3FN, q=None, scale_inv=None, stream=None):
+    """1 x 128 tiles along the rows of x [R, C] -> (q [R, C], scale_inv [C/128, R])."""
+    torch = _torch()
+    R, C = x.shape
+    q = _empty((R, C), torch.uint8, x) if q is None else q
+    scale_inv = _empty((C // 128, R), torch.float32, x) if scale_inv is None else scale_inv
+    _check("fp8moe_quantize_blockwise_rows", _lib_raw().fp8moe_quantize_blockwise_rows(
+        _ptr(x), R, C, kind, _ptr(q), _ptr(scale_inv), _stream(stream)))
+    return q, scale_inv
+
+
+def fp8moe_quantize_blockwise_weight(w, kind: int = E4M3FN, plain: bool = True, transposed: bool = True,
+                                     q=None, qt=None, scale_inv=None, stream=None):
+    """128 x 128 tiles of w [E, N, K] -> (q [E, N, K] or None, qt [E, K, N] or
+    None, scale_inv [E, N/128, K/128])."""
+    torch = _torch()
+    E, N, K = w.shape
+    q = (_empty((E, N, K), torch.uint8, w) if q is None else q) if plain else None
+    qt = (_empty((E, K, N), torch.uint8, w) if qt is None else qt) if transposed else None
+    scale_inv = _empty((E, N // 128, K // 128), torch.float32, w) if scale_inv is None else scale_inv
+    _check("fp8moe_quantize_blockwise_weight", _lib_raw().fp8moe_quantize_blockwise_weight(
+        _ptr(w), E, N, K, kind, _ptr(q), _ptr(qt), _ptr(scale_inv), _stream(stream)))
+    return q, qt, scale_inv
+
+
+def fp8moe_blockwise_token_blocks(M: int, E: int) -> int:
+    """Rows of the token-tile scale buffer (an upper bound on the blocks)."""
+    return int(_lib_raw().fp8moe_blockwise_token_blocks(M, E))
+
+
+def fp8moe_quantize_blockwise_tokens(x, offs, kind: int = E4M3FN, qt=None, scale_inv=None, stream=None):
+    """128-token tiles per group of x [M, C] -> (qt [C, M], scale_inv
+    [fp8moe_blockwise_token_blocks(M, E), C])."""
+    torch = _torch()
+    M, C = x.shape
+    E = offs.numel()
+    qt = _empty((C, M), torch.uint8, x) if qt is None else qt
+    scale_inv = (_empty((fp8moe_blockwise_token_blocks(M, E), C), torch.float32, x)
+                 if scale_inv is None else scale_inv)
+    _check("fp8moe_quantize_blockwise_tokens", _lib_raw().fp8moe_quantize_blockwise_tokens(
+        _ptr(x), M, C, _ptr(offs), E, kind, _ptr(qt), _ptr(scale_inv), _stream(stream)))
+    return qt, scale_inv
 
 
 def fp8moe_mxfp8_moe_workspace_bytes(E: int, M: int, N: int, K: int) -> int:

@@ -215,10 +215,54 @@ fp8moe_status fp8moe_quantize_tensorwise(const void* x, int64_t E, int64_t R, in
                                                d->status, (cudaStream_t)stream));
 }
 
+fp8moe_status fp8moe_quantize_blockwise_rows(const void* x, int64_t R, int64_t C, int kind, void* q,
+                                             float* scale_inv, fp8moe_stream_t stream) {
+  if (R < 0 || C < 0 || !valid_kind(kind)) return FP8MOE_ERR_INVALID_ARG;
+  if (C % 128) return FP8MOE_ERR_ALIGNMENT;
+  if (R == 0 || C == 0) return FP8MOE_OK;
+  if (!x || !q || !scale_inv) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(q) || ((uintptr_t)scale_inv & 3)) return FP8MOE_ERR_ALIGNMENT;
+  if (R > ((int64_t)1 << 35)) return FP8MOE_ERR_INVALID_ARG;
+  return cuda_result(fp8moe::launch_bw_rows(x, R, C, kind, q, scale_inv, (cudaStream_t)stream));
+}
+
+fp8moe_status fp8moe_quantize_blockwise_weight(const void* w, int64_t E, int64_t N, int64_t K, int kind, void* q,
+                                               void* qt, float* scale_inv, fp8moe_stream_t stream) {
+  if (E < 0 || N < 0 || K < 0 || !valid_kind(kind) || (!q && !qt)) return FP8MOE_ERR_INVALID_ARG;
+  if (N % 128 || K % 128) return FP8MOE_ERR_ALIGNMENT;
+  if (E == 0 || N == 0 || K == 0) return FP8MOE_OK;
+  if (!w || !scale_inv) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(w) || (q && !al16(q)) || (qt && !al16(qt)) || ((uintptr_t)scale_inv & 3)) return FP8MOE_ERR_ALIGNMENT;
+  if (E * (N / 128) * (K / 128) >= ((int64_t)1 << 31)) return FP8MOE_ERR_INVALID_ARG;
+  return cuda_result(fp8moe::launch_bw_weight(w, E, N, K, kind, q, qt, scale_inv, (cudaStream_t)stream));
+}
+
+int64_t fp8moe_blockwise_token_blocks(int64_t M, int64_t E) {
+  if (M < 0 || E < 1) return -1;
+  return (M + 127) / 128 + E;
+}
+
+fp8moe_status fp8moe_quantize_blockwise_tokens(const void* x, int64_t M, int64_t C, const int32_t* offs, int64_t E,
+                                               int kind, void* qt, float* scale_inv, fp8moe_stream_t stream) {
+  if (M < 0 || C < 0 || E < 1 || E > FP8MOE_MAX_GROUPS || !valid_kind(kind) || !offs) return FP8MOE_ERR_INVALID_ARG;
+  if (M % 32 || C % 16) return FP8MOE_ERR_ALIGNMENT;
+  if (((uintptr_t)offs & 3)) return FP8MOE_ERR_ALIGNMENT;
+  if (M == 0 || C == 0) return FP8MOE_OK;
+  if (!x || !qt || !scale_inv) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(qt) || !al16(scale_inv)) return FP8MOE_ERR_ALIGNMENT;
+  if (fp8moe_blockwise_token_blocks(M, E) * ((C + 127) / 128) >= ((int64_t)1 << 31)) return FP8MOE_ERR_INVALID_ARG;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  return cuda_result(fp8moe::launch_bw_tokens(x, M, C, offs, E, kind, qt, scale_inv, d->status,
+                                              (cudaStream_t)stream));
+}
+
 static fp8moe_status grouped_mm(int mode, int recipe, const void* a, const void* a_scale, const void* b,
                                 const void* b_scale, const int32_t* offs, int64_t E, int64_t M, int64_t N,
                                 int64_t K, void* out, fp8moe_stream_t stream) {
-  if (recipe != FP8MOE_ROWWISE && recipe != FP8MOE_MXFP8 && recipe != FP8MOE_TENSORWISE)
+  if (recipe != FP8MOE_ROWWISE && recipe != FP8MOE_MXFP8 && recipe != FP8MOE_TENSORWISE &&
+      recipe != FP8MOE_BLOCKWISE)
     return FP8MOE_ERR_INVALID_ARG;
   if (E < 1 || M < 0 || N < 0 || K < 0 || E > 4096) return FP8MOE_ERR_INVALID_ARG;
   if (!offs || ((uintptr_t)offs & 3)) return FP8MOE_ERR_INVALID_ARG;
@@ -229,9 +273,16 @@ static fp8moe_status grouped_mm(int mode, int recipe, const void* a, const void*
     if (mode == fp8moe::GEMM_DGRAD && N % 32) return FP8MOE_ERR_ALIGNMENT;
     if (mode == fp8moe::GEMM_WGRAD && M % 32) return FP8MOE_ERR_ALIGNMENT;
   }
+  if (recipe == FP8MOE_BLOCKWISE) {
+    // weight tiles are 128 x 128; wgrad's token tiles are cut at 32-multiple
+    // group boundaries
+    if (N % 128 || K % 128 || (mode == fp8moe::GEMM_WGRAD && M % 32)) return FP8MOE_ERR_ALIGNMENT;
+  }
   if (!a || !b || !out || !a_scale || !b_scale) return FP8MOE_ERR_INVALID_ARG;
   if (!al16(a) || !al16(b) || !al16(out)) return FP8MOE_ERR_ALIGNMENT;
-  if (recipe == FP8MOE_TENSORWISE ? (((uintptr_t)a_scale | (uintptr_t)b_scale) & 3) : (!al16(a_scale) || !al16(b_scale)))
+  if (recipe == FP8MOE_TENSORWISE || (recipe == FP8MOE_BLOCKWISE && mode != fp8moe::GEMM_WGRAD)
+          ? (((uintptr_t)a_scale | (uintptr_t)b_scale) & 3)
+          : (!al16(a_scale) || !al16(b_scale)))
     return FP8MOE_ERR_ALIGNMENT;
   DevInfo* d;
   fp8moe_status st = device_info(&d);
@@ -256,7 +307,7 @@ static fp8moe_status grouped_mm(int mode, int recipe, const void* a, const void*
     g.rows = M, g.cols = K, g.kk = N;
   } else {                                 // [N,Mt] x [K,Mt] -> [E,N,K]
     g.rows = N, g.cols = K;
-    g.kk = recipe == FP8MOE_MXFP8 ? M : fp8moe_jagged_t_cols(M, E);
+    g.kk = recipe == FP8MOE_MXFP8 || recipe == FP8MOE_BLOCKWISE ? M : fp8moe_jagged_t_cols(M, E);
   }
   if (g.rows == 0 || g.cols == 0) return FP8MOE_OK;
   if (g.kk == 0) {
@@ -265,7 +316,8 @@ static fp8moe_status grouped_mm(int mode, int recipe, const void* a, const void*
     const int64_t n = (mode == fp8moe::GEMM_WGRAD ? E : 1) * g.rows * g.cols;
     return cuda_result(cudaMemsetAsync(out, 0, (size_t)n * 2, (cudaStream_t)stream));
   }
-  cudaError_t e = fp8moe::launch_grouped_mm(g, (cudaStream_t)stream);
+  cudaError_t e = recipe == FP8MOE_BLOCKWISE ? fp8moe::launch_blockwise_mm(g, (cudaStream_t)stream)
+                                             : fp8moe::launch_grouped_mm(g, (cudaStream_t)stream);
   if (e == cudaErrorNotSupported) return FP8MOE_ERR_UNSUPPORTED;
   return cuda_result(e);
 }

@@ -1,0 +1,472 @@
+// Blockwise-scaled grouped GEMM on tcgen05 (sm_103a): forward, dgrad and
+// wgrad of an MoE expert layer whose FP8 operands carry one fp32 scale per
+// tile ("FP8-обучение на AMD", section "Скейлы: от тензора до микроблока":
+// blockwise scaling, a scale per tile of fixed size; 1 x 128 tiles along the
+// contracting dimension for the row operand, 128 x 128 tiles for the
+// weights, 128-token tiles per group for both wgrad operands).
+//
+// The scales change every 128 elements of the contraction, so the tensor
+// core cannot accumulate across k-blocks: each k-block's product goes to its
+// own TMEM partial and is promoted into an fp32 accumulator held in
+// registers, scaled by (row scale x column scale) of that k-block.
+//  * persistent kernel, one 320-thread CTA per SM, output tiles 128 x 256;
+//  * warp 0: TMA producer (A 128 x 128 and B 256 x 128 byte tiles, 128-byte
+//    swizzle, 4-stage ring); warp 1: TMEM allocator and MMA issuer
+//    (kind::f8f6f4, M = 128, N = 256, four K = 32 steps per k-block);
+//  * two TMEM partials of 256 columns: the MMAs of k-block i + 1 run while
+//    the epilogue promotes k-block i;
+//  * warps 2-9: epilogue; warp w reads TMEM lanes 32 (w % 4) .. +31 and
+//    columns 128 ((w - 2) / 4) .. +127, holds 128 fp32 accumulators per
+//    thread (half of one output row) and writes bf16 at the end.  Ten warps
+//    leave 168 registers a thread (each SM sub-partition holds 16K registers
+//    and three of the warps); the promotion reads TMEM 16 columns at a time;
+//  * wgrad's per-column scales change with every k-block: the producer
+//    bulk-copies each k-block's 256 of them into a ring slot that the
+//    epilogue warps release;
+//  * every wait is bounded; a timeout sets the device status word.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "launch.h"
+#include "tcgen05.cuh"
+#include "tma.cuh"
+
+namespace fp8moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int STAGES = 4;
+constexpr int THREADS = 320;
+constexpr int EPI_THREADS = 256;
+constexpr int EPI_COLS = 128;  // columns per epilogue thread
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MAXG = 1024;
+constexpr uint32_t TMEM_COLS = 512;
+
+struct Layout {
+  // full, empty, cs_full, cs_empty per stage; pfull[2], pempty[2]
+  static constexpr int bars = STAGES * STAGE_BYTES;
+  static constexpr int misc = bars + (4 * STAGES + 4) * 8;          // tmem base, abort flag, total tiles
+  static constexpr int colsc = misc + 16;                           // wgrad column scales [STAGES][BN]
+  static constexpr int tiles_prefix = colsc + STAGES * BN * 4;
+  static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
+  static constexpr int total = blk_prefix + (MAXG + 1) * 4;
+};
+constexpr int SMEM_BYTES = Layout::total + 1024;
+
+struct BwParams {
+  GemmArgs g;
+  int n_tiles;    // output column tiles
+  int m_tiles_w;  // wgrad: output row tiles per group
+};
+
+struct BwTile {
+  int e;
+  int64_t row0, rows;    // output rows
+  int64_t col0, ncols;   // output columns
+  int64_t x0, kvalid;    // contraction start and length
+  int nk;                // k-blocks
+  int64_t blk0;          // wgrad: first token block of the group
+};
+
+template <bool WGRAD>
+FP8MOE_DEV BwTile bw_tile(const BwParams& p, const int* tiles_prefix, const int* blk_prefix, int t) {
+  const GemmArgs& g = p.g;
+  int lo = 0, hi = g.E - 1, e = 0;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (tiles_prefix[mid] <= t) {
+      e = mid;
+      lo = mid + 1;
+    } else {
+      hi = mid - 1;
+    }
+  }
+  const int local = t - tiles_prefix[e];
+  const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
+  const int64_t ge = g.offs[e];
+  BwTile tl;
+  tl.e = e;
+  if (!WGRAD) {
+    // m-tiles of the group fastest: CTAs running together share the B tile
+    const int mt = (int)((ge - gs + BM - 1) / BM);
+    const int ni = local / mt, mi = local % mt;
+    tl.row0 = gs + (int64_t)mi * BM;
+    tl.rows = min((int64_t)BM, ge - tl.row0);
+    tl.col0 = (int64_t)ni * BN;
+    tl.x0 = 0;
+    tl.kvalid = g.kk;
+    tl.blk0 = 0;
+  } else {
+    const int ni = local / p.m_tiles_w, mi = local % p.m_tiles_w;
+    tl.row0 = (int64_t)mi * BM;
+    tl.rows = min((int64_t)BM, g.rows - tl.row0);
+    tl.col0 = (int64_t)ni * BN;
+    tl.x0 = gs;
+    tl.kvalid = ge - gs;
+    tl.blk0 = blk_prefix[e];
+  }
+  tl.ncols = min((int64_t)BN, g.cols - tl.col0);
+  tl.nk = (int)((tl.kvalid + BK - 1) / BK);
+  return tl;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_blockwise_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, BwParams p) {
+  constexpr bool WGRAD = MODE == GEMM_WGRAD;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = (uint64_t*)(smem + Layout::bars);
+  uint64_t* empty = full + STAGES;
+  uint64_t* cs_full = empty + STAGES;
+  uint64_t* cs_empty = cs_full + STAGES;
+  uint64_t* pfull = cs_empty + STAGES;
+  uint64_t* pempty = pfull + 2;
+  uint32_t* tmem_holder = (uint32_t*)(smem + Layout::misc);
+  volatile int* abort_flag = (volatile int*)(smem + Layout::misc + 4);
+  int* total_s = (int*)(smem + Layout::misc + 8);
+  float* colsc = (float*)(smem + Layout::colsc);
+  int* tiles_prefix = (int*)(smem + Layout::tiles_prefix);
+  int* blk_prefix = (int*)(smem + Layout::blk_prefix);
+  const GemmArgs& g = p.g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&cs_full[s], 1);
+      mbar_init(&cs_empty[s], EPI_THREADS / 32);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pfull[b], 1);
+      mbar_init(&pempty[b], EPI_THREADS / 32);
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    tc_fence_before();
+  }
+  // per-group tile and token-block counts, then one warp scans them and
+  // validates the offsets
+  for (int e = threadIdx.x; e < g.E; e += THREADS) {
+    const int64_t sz = (int64_t)g.offs[e] - (e == 0 ? 0 : g.offs[e - 1]);
+    int nt, nb = 0;
+    if (!WGRAD) {
+      nt = (int)((sz + BM - 1) / BM) * p.n_tiles;
+    } else {
+      nt = p.m_tiles_w * p.n_tiles;
+      nb = (int)((sz + 127) / 128);
+    }
+    tiles_prefix[e + 1] = sz < 0 ? 0 : nt;
+    blk_prefix[e + 1] = sz < 0 ? 0 : nb;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int bad = 0, carry_t = 0, carry_b = 0;
+    for (int base = 0; base < g.E; base += 32) {
+      const int e = base + lane;
+      int vt = 0, vb = 0;
+      if (e < g.E) {
+        const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
+        const int64_t ge = g.offs[e];
+        if (ge < gs || ge > g.M || (e == g.E - 1 && ge != g.M)) bad = 1;
+        if (WGRAD && (ge % 32)) bad = 1;
+        vt = tiles_prefix[e + 1];
+        vb = blk_prefix[e + 1];
+      }
+      for (int o = 1; o < 32; o <<= 1) {
+        const int ut = __shfl_up_sync(0xffffffffu, vt, o);
+        const int ub = __shfl_up_sync(0xffffffffu, vb, o);
+        if (lane >= o) {
+          vt += ut;
+          vb += ub;
+        }
+      }
+      if (e < g.E) {
+        tiles_prefix[e + 1] = carry_t + vt;
+        blk_prefix[e + 1] = carry_b + vb;
+      }
+      carry_t += __shfl_sync(0xffffffffu, vt, 31);
+      carry_b += __shfl_sync(0xffffffffu, vb, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      tiles_prefix[0] = 0;
+      blk_prefix[0] = 0;
+      *total_s = bad ? 0 : carry_t;
+      if (bad && blockIdx.x == 0) set_status(g.status, FP8MOE_ERR_DEVICE_OFFSETS);
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = *total_s;
+
+  if (warp == 0 && lane == 0) {
+    // ======================= TMA producer =======================
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      const BwTile tl = bw_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+      for (int ks = 0; ks < tl.nk; ++ks) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+          set_status(g.status, FP8MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* sa = smem + stage * STAGE_BYTES;
+        mbar_expect_tx(&full[stage], STAGE_BYTES);
+        const int x = (int)(tl.x0 + (int64_t)ks * BK);
+        tma_load_2d(sa, &tmA, &full[stage], x, (int)tl.row0);
+        if (WGRAD) {
+          tma_load_2d(sa + A_BYTES, &tmB, &full[stage], x, (int)tl.col0);
+          // this k-block's column scales (the epilogue released the slot)
+          if (!mbar_wait(&cs_empty[stage], phase ^ 1, abort_flag)) {
+            set_status(g.status, FP8MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          const uint32_t nbytes = (uint32_t)(tl.ncols * 4);
+          mbar_expect_tx(&cs_full[stage], nbytes);
+          bulk_load(colsc + stage * BN, (const float*)g.b_scale + (tl.blk0 + ks) * g.cols + tl.col0, nbytes,
+                    &cs_full[stage]);
+        } else {
+          tma_load_3d(sa + A_BYTES, &tmB, &full[stage], x, (int)tl.col0, tl.e);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    // every stage's MMAs have completed (their loads landed), and the
+    // epilogue has read every column-scale slot, before exit
+    for (int i = 0; i < STAGES && !*abort_flag; ++i) {
+      if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag) ||
+          (WGRAD && !mbar_wait(&cs_empty[stage], phase ^ 1, abort_flag))) {
+        set_status(g.status, FP8MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ======================= MMA issuer =======================
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t np = 0;  // partials issued
+    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      const BwTile tl = bw_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+      bool ok = true;
+      for (int ks = 0; ks < tl.nk; ++ks) {
+        const uint32_t buf = np & 1, use = np >> 1;
+        if (!mbar_wait(&full[stage], phase, abort_flag) || !mbar_wait(&pempty[buf], (use & 1) ^ 1, abort_flag)) {
+          set_status(g.status, FP8MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+        const uint64_t adesc = sdesc_sw128(a_addr), bdesc = sdesc_sw128(a_addr + A_BYTES);
+        const uint32_t d = tmem_base + buf * BN;
+        const int64_t rem = tl.kvalid - (int64_t)ks * BK;
+        if (rem >= BK) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8<false>(d, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8n<BM, BN>(), k > 0);
+        } else {
+          const int nsub = (int)((rem + 31) / 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k < nsub)
+              mma_f8<false>(d, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8n<BM, BN>(), k > 0);
+        }
+        tc_commit(&empty[stage]);
+        tc_commit(&pfull[buf]);
+        ++np;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+    }
+  } else if (warp >= 2) {
+    // ======================= epilogue: promotion and stores =======================
+    const int quarter = warp & 3;
+    const int part = (warp - 2) >> 2;  // 128-column half of the tile
+    const int lrow = quarter * 32 + lane;
+    const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + part * EPI_COLS;
+    const float* sa_p = (const float*)g.a_scale;
+    const float* sb_p = (const float*)g.b_scale;
+    uint32_t np = 0;
+    for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+      const BwTile tl = bw_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+      const bool row_ok = lrow < tl.rows;
+      const int64_t c0 = part * EPI_COLS;  // first column of this thread inside the tile
+      uint16_t* orow = WGRAD ? g.out + ((int64_t)tl.e * g.rows + tl.row0 + lrow) * g.cols + tl.col0
+                             : g.out + (tl.row0 + lrow) * g.cols + tl.col0;
+      if (tl.nk == 0) {
+        // an empty group in wgrad: dW[e] = 0
+        if (row_ok)
+          for (int c = (int)c0; c < c0 + EPI_COLS && c < tl.ncols; c += 8)
+            *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      // scale of k-block ks: row part (per thread) and column part (one per
+      // 128-column half for forward / dgrad, per column for wgrad)
+      auto row_scale = [&](int ks) -> float {
+        if (!row_ok) return 0.0f;
+        if (WGRAD) return sa_p[(tl.blk0 + ks) * g.rows + tl.row0 + lrow];
+        return sa_p[(int64_t)ks * g.M + tl.row0 + lrow];
+      };
+      auto col_scale = [&](int ks) -> float {
+        if (WGRAD) return 1.0f;  // per column, from the ring
+        const int64_t cb = (tl.col0 + c0) / 128;
+        if (cb * 128 >= g.cols) return 0.0f;
+        if (MODE == GEMM_FWD) return sb_p[((int64_t)tl.e * (g.cols / 128) + cb) * (g.kk / 128) + ks];
+        return sb_p[((int64_t)tl.e * (g.kk / 128) + ks) * (g.cols / 128) + cb];   // dgrad: W^T tiles
+      };
+      float acc[EPI_COLS];
+#pragma unroll
+      for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
+      float rs_next = row_scale(0), cs_next = col_scale(0);
+      bool ok = true;
+      for (int ks = 0; ks < tl.nk; ++ks) {
+        const float rs = rs_next, cs = cs_next;
+        if (ks + 1 < tl.nk) {
+          rs_next = row_scale(ks + 1);
+          cs_next = col_scale(ks + 1);
+        }
+        const float* csv = nullptr;
+        const int slot = (int)(np % STAGES);
+        if (WGRAD) {
+          if (!mbar_wait(&cs_full[slot], (np / STAGES) & 1, abort_flag)) {
+            set_status(g.status, FP8MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          csv = colsc + slot * BN + c0;
+        }
+        const uint32_t pb = np & 1, use = np >> 1;
+        if (!mbar_wait(&pfull[pb], use & 1, abort_flag)) {
+          set_status(g.status, FP8MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float f = WGRAD ? rs : rs * cs;
+#pragma unroll
+        for (int c = 0; c < EPI_COLS; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(taddr + pb * BN + c, r);
+          tmem_ld_wait();
+          if constexpr (WGRAD) {
+            // the product times its column scale, then times the row scale
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              const float4 cv = *reinterpret_cast<const float4*>(csv + c + j);
+              acc[c + j] = fmaf(__uint_as_float(r[j]) * cv.x, f, acc[c + j]);
+              acc[c + j + 1] = fmaf(__uint_as_float(r[j + 1]) * cv.y, f, acc[c + j + 1]);
+              acc[c + j + 2] = fmaf(__uint_as_float(r[j + 2]) * cv.z, f, acc[c + j + 2]);
+              acc[c + j + 3] = fmaf(__uint_as_float(r[j + 3]) * cv.w, f, acc[c + j + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[c + j] = fmaf(__uint_as_float(r[j]), f, acc[c + j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&pempty[pb]);
+          if (WGRAD) mbar_arrive(&cs_empty[slot]);
+        }
+        ++np;
+      }
+      if (!ok) break;
+      if (!row_ok) continue;
+#pragma unroll
+      for (int c = 0; c < EPI_COLS; c += 8) {
+        if (c0 + c < tl.ncols) {
+          uint4 v;
+          v.x = pack_bf16(acc[c], acc[c + 1]);
+          v.y = pack_bf16(acc[c + 2], acc[c + 3]);
+          v.z = pack_bf16(acc[c + 4], acc[c + 5]);
+          v.w = pack_bf16(acc[c + 6], acc[c + 7]);
+          *reinterpret_cast<uint4*>(orow + c0 + c) = v;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+  }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const BwParams& p, int64_t tiles,
+                        cudaStream_t st) {
+  auto kern = k_blockwise_mm<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = tiles < p.g.num_sms ? tiles : p.g.num_sms;
+  kern<<<(unsigned)(grid > 0 ? grid : 1), THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_blockwise_mm(const GemmArgs& g, cudaStream_t st) {
+  if (g.E > MAXG) return cudaErrorNotSupported;
+  if (g.kk > INT32_MAX || g.rows > INT32_MAX || g.cols > INT32_MAX || g.M > INT32_MAX) return cudaErrorInvalidValue;
+  if (SMEM_BYTES > g.max_smem) return cudaErrorNotSupported;
+  const bool wgrad = g.mode == GEMM_WGRAD;
+  BwParams p;
+  p.g = g;
+  p.n_tiles = (int)((g.cols + BN - 1) / BN);
+  p.m_tiles_w = (int)((g.rows + BM - 1) / BM);
+  CUtensorMap ta, tb;
+  {
+    const int64_t arows = wgrad ? g.rows : g.M;
+    cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)(arows > 0 ? arows : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)g.kk};
+    cuuint32_t box[2] = {BK, BM};
+    if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.a, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  if (wgrad) {
+    cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)g.cols};
+    cuuint64_t strides[1] = {(cuuint64_t)g.kk};
+    cuuint32_t box[2] = {BK, BN};
+    if (!make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  } else {
+    cuuint64_t dims[3] = {(cuuint64_t)g.kk, (cuuint64_t)g.cols, (cuuint64_t)g.E};
+    cuuint64_t strides[2] = {(cuuint64_t)g.kk, (cuuint64_t)(g.kk * g.cols)};
+    cuuint32_t box[3] = {BK, BN, 1};
+    if (!make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  // an upper bound on the tiles (the exact count needs the offsets)
+  const int64_t tiles = wgrad ? (int64_t)g.E * p.m_tiles_w * p.n_tiles
+                              : ((g.M + BM - 1) / BM + g.E) * (int64_t)p.n_tiles;
+  if (g.mode == GEMM_FWD) return launch_mode<GEMM_FWD>(ta, tb, p, tiles, st);
+  if (g.mode == GEMM_DGRAD) return launch_mode<GEMM_DGRAD>(ta, tb, p, tiles, st);
+  return launch_mode<GEMM_WGRAD>(ta, tb, p, tiles, st);
+}
+
+}  // namespace fp8moe

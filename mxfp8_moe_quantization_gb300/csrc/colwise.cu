@@ -102,14 +102,7 @@ FP8MOE_DEV int64_t total_subs(const CwArgs& a, const GroupTable& gt) {
   }
 }
 
-// read-only, streamed past L1
-FP8MOE_DEV uint4 ld16(const uint16_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+FP8MOE_DEV uint4 ld16(const uint16_t* p) { return ld_nc16(p); }
 
 // The rows of a lane (rows at or past r1 read as zeros); all loads are
 // issued before any is consumed.
@@ -195,18 +188,6 @@ __global__ void __launch_bounds__(256) k_cw_amax(CwArgs a) {
   }
 }
 
-// Column t (0..3) of four row words (byte t of each) as one word, rows in
-// byte order.
-FP8MOE_DEV void transpose4x4(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3, uint32_t (&col)[4]) {
-  const uint32_t a01 = __byte_perm(r0, r1, 0x5140);  // c0 r0, c0 r1, c1 r0, c1 r1
-  const uint32_t a23 = __byte_perm(r2, r3, 0x5140);
-  const uint32_t b01 = __byte_perm(r0, r1, 0x7362);  // c2 r0, c2 r1, c3 r0, c3 r1
-  const uint32_t b23 = __byte_perm(r2, r3, 0x7362);
-  col[0] = __byte_perm(a01, a23, 0x5410);
-  col[1] = __byte_perm(a01, a23, 0x7632);
-  col[2] = __byte_perm(b01, b23, 0x5410);
-  col[3] = __byte_perm(b01, b23, 0x7632);
-}
 
 template <bool JAG, bool TRANS, bool FNUZ>
 __global__ void __launch_bounds__(256) k_cw_cast(CwArgs a) {

@@ -15,7 +15,7 @@ namespace fp8moe {
 enum GemmMode { GEMM_FWD = 0, GEMM_DGRAD = 1, GEMM_WGRAD = 2 };
 
 struct GemmArgs {
-  int recipe;            // FP8MOE_ROWWISE / FP8MOE_MXFP8
+  int recipe;            // FP8MOE_ROWWISE / _MXFP8 / _TENSORWISE / _BLOCKWISE
   int mode;              // GemmMode
   const uint8_t* a;      // [rows or M, kk]
   const void* a_scale;

@@ -35,6 +35,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "launch.h"
+#include "tcgen05.cuh"
 #include "tma.cuh"
 
 namespace fp8moe {
@@ -146,12 +147,6 @@ FP8MOE_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* 
 FP8MOE_DEV void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-FP8MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-FP8MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-FP8MOE_DEV void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
 // completion of this thread's earlier tcgen05 ops (of its own CTA group) on a
 // local barrier
 template <bool TWO>
@@ -164,17 +159,6 @@ FP8MOE_DEV void tc_commit_local(uint64_t* bar) {
   }
 }
 
-// Shared-memory matrix descriptor: K-major operand tile, 128-byte swizzle,
-// 8-row groups 1024 bytes apart.
-FP8MOE_DEV uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
-  d |= (uint64_t)1 << 46;              // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;              // 128-byte swizzle
-  return d;
-}
 // Descriptor of one 128x4 scale tile (32 rows of 16 bytes, no swizzle) as the
 // source of tcgen05.cp 32x128b.
 FP8MOE_DEV uint64_t sdesc_sf(uint32_t saddr) {
@@ -192,10 +176,9 @@ template <int MM>
 FP8MOE_DEV uint32_t idesc_mx(uint32_t sf_id) {
   return (sf_id << 4) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) | ((uint32_t)(MM >> 4) << 24) | (sf_id << 29);
 }
-// Plain e4m3 x e4m3 with an fp32 accumulator (D format F32 = 1 at [4,6)).
 template <int MM>
 FP8MOE_DEV uint32_t idesc_f8() {
-  return (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(MM >> 4) << 24);
+  return idesc_f8n<MM, BN>();
 }
 
 template <bool TWO>
@@ -216,20 +199,6 @@ FP8MOE_DEV void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t
   }
 }
 template <bool TWO>
-FP8MOE_DEV void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
-  if constexpr (TWO) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
-  } else {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
-  }
-}
-template <bool TWO>
 FP8MOE_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
   if constexpr (TWO) {
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
@@ -238,23 +207,7 @@ FP8MOE_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
   }
 }
 
-// 32 lanes x 32 bits, 32 consecutive columns -> 32 registers per thread.
-FP8MOE_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-FP8MOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-FP8MOE_DEV uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 
 // ---------------------------------------------------------------------------
 // kernel

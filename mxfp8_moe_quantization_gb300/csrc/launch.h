@@ -37,6 +37,13 @@ cudaError_t launch_colwise_fixed(const void* x, int64_t E, int64_t R, int64_t C,
 cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                               int transpose_out, int kind, void* q, float* scale_inv, int num_sms, int* status,
                               cudaStream_t st);
+// blockwise FP8 (blockwise.cu): 1 x 128 row tiles, 128 x 128 weight tiles,
+// per-group 128-token tiles (transposed codes)
+cudaError_t launch_bw_rows(const void* x, int64_t R, int64_t C, int kind, void* q, float* inv, cudaStream_t st);
+cudaError_t launch_bw_weight(const void* w, int64_t E, int64_t N, int64_t K, int kind, void* q, void* qt,
+                             float* inv, cudaStream_t st);
+cudaError_t launch_bw_tokens(const void* x, int64_t M, int64_t C, const int32_t* offs, int64_t E, int kind,
+                             void* qt, float* inv, int* status, cudaStream_t st);
 // token routing (routing.cu)
 int64_t route_workspace_bytes(int64_t T, int64_t k, int64_t E);
 cudaError_t launch_route_permute(const void* x, int64_t T, int64_t H, const int32_t* idx, const float* w, int64_t k,
@@ -50,5 +57,7 @@ cudaError_t launch_swizzle(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, c
 
 struct GemmArgs;
 cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st);
+// blockwise-scaled grouped GEMM (blockwise_mm.cu)
+cudaError_t launch_blockwise_mm(const GemmArgs& g, cudaStream_t st);
 
 }  // namespace fp8moe

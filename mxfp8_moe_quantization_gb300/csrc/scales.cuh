@@ -54,8 +54,10 @@ FP8MOE_DEV int find_group(const int64_t* ends, int E, int64_t key) {
 //   GT_ROWS128: group sizes rounded up to 128 rows (scale tiles of the rows);
 //   GT_COLS:    group sizes / 32 rounded up to 4 (scale tile columns; every
 //               group size must be a multiple of 32);
-//   GT_SUB32:   group sizes in 32-row sub-tiles, ceil(size / 32).
-enum { GT_ROWS128 = 0, GT_COLS = 1, GT_SUB32 = 2 };
+//   GT_SUB32:   group sizes in 32-row sub-tiles, ceil(size / 32);
+//   GT_BLK128:  group sizes in 128-row blocks, ceil(size / 128) (every group
+//               size must be a multiple of 32).
+enum { GT_ROWS128 = 0, GT_COLS = 1, GT_SUB32 = 2, GT_BLK128 = 3 };
 
 // Call with all threads of a block of 256; ends with __syncthreads.
 static __device__ void build_group_table(GroupTable& t, const int32_t* offs, int E, int64_t total, int mode,
@@ -72,9 +74,12 @@ static __device__ void build_group_table(GroupTable& t, const int32_t* offs, int
     const int64_t end = offs[e];
     const int64_t start = e == 0 ? 0 : offs[e - 1];
     if (end < start || end > total || (e == E - 1 && end != total)) bad = 1;
-    if (mode == GT_COLS && (end % 32)) bad = 1;
+    if ((mode == GT_COLS || mode == GT_BLK128) && (end % 32)) bad = 1;
     const int64_t sz = end - start;
-    u[i] = mode == GT_COLS ? ((sz / 32 + 3) / 4 * 4) : mode == GT_SUB32 ? (sz + 31) / 32 : ((sz + 127) / 128 * 128);
+    u[i] = mode == GT_COLS     ? ((sz / 32 + 3) / 4 * 4)
+           : mode == GT_SUB32  ? (sz + 31) / 32
+           : mode == GT_BLK128 ? (sz + 127) / 128
+                               : ((sz + 127) / 128 * 128);
     sum += u[i];
     t.end[e] = end;
   }

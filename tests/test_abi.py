@@ -96,3 +96,20 @@ def test_layer_workspace_and_host_errors(lib):
     assert lib.fp8moe_mxfp8_moe_bwd(p, p, i64(4), i64(64), i64(64), i64(64), p, big, None, None, None) == 0
     # jagged colwise takes at most FP8MOE_MAX_GROUPS groups
     assert lib.fp8moe_quantize_colwise_3d(p, i64(1025), i64(64), i64(32), p, 1, 0, p, p, None) == INVALID
+
+
+def test_blockwise_host_errors(lib):
+    p = ctypes.c_void_p(1 << 20)
+    i64 = ctypes.c_int64
+    INVALID, ALIGN = 1, 2
+    assert lib.fp8moe_quantize_blockwise_rows(p, i64(4), i64(192), 0, p, p, None) == ALIGN        # C % 128
+    assert lib.fp8moe_quantize_blockwise_rows(p, i64(0), i64(128), 0, p, p, None) == 0
+    assert lib.fp8moe_quantize_blockwise_weight(p, i64(2), i64(128), i64(64), 0, p, p, p, None) == ALIGN
+    assert lib.fp8moe_quantize_blockwise_weight(p, i64(2), i64(128), i64(128), 0, None, None, p, None) == INVALID
+    assert lib.fp8moe_quantize_blockwise_tokens(p, i64(48), i64(32), p, i64(2), 0, p, p, None) == ALIGN  # M % 32
+    assert lib.fp8moe_quantize_blockwise_tokens(p, i64(64), i64(32), None, i64(2), 0, p, p, None) == INVALID
+    assert lib.fp8moe_blockwise_token_blocks(i64(16640), i64(16)) == 130 + 16
+    assert lib.fp8moe_blockwise_token_blocks(i64(0), i64(0)) == -1
+    # GEMM: weight tiles need N, K multiples of 128
+    assert lib.fp8moe_scaled_grouped_mm_fwd(3, p, p, p, p, p, i64(4), i64(64), i64(256), i64(192), p, None) == ALIGN
+    assert lib.fp8moe_scaled_grouped_mm_wgrad(3, p, p, p, p, p, i64(4), i64(48), i64(256), i64(256), p, None) == ALIGN
