@@ -17,7 +17,9 @@
 //    the epilogue promotes k-block i;
 //  * warps 2-9: epilogue; warp w reads TMEM lanes 32 (w % 4) .. +31 and
 //    columns 128 ((w - 2) / 4) .. +127, holds 128 fp32 accumulators per
-//    thread (half of one output row) and writes bf16 at the end.  Ten warps
+//    thread (half of one output row) and writes bf16 at the end through a
+//    2 KB staging tile per warp (32 rows x 32 columns, 64-byte swizzle)
+//    handed to TMA stores, so the LSU is not the bottleneck.  Ten warps
 //    leave 168 registers a thread (each SM sub-partition holds 16K registers
 //    and three of the warps); the promotion reads TMEM 16 columns at a time;
 //  * wgrad's per-column scales change with every k-block: the producer
@@ -36,7 +38,6 @@ namespace fp8moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int STAGES = 4;
 constexpr int THREADS = 320;
 constexpr int EPI_THREADS = 256;
 constexpr int EPI_COLS = 128;  // columns per epilogue thread
@@ -46,6 +47,11 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MAXG = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 
+// Forward / dgrad: 4 stages and one staging tile per epilogue warp.  Wgrad
+// (tiles of ~8 k-blocks, so the stores recur 5x as often): 3 stages and two
+// staging tiles per warp, so that a slice is written while the previous
+// one's TMA store still reads.
+template <int STAGES, int NSTG>
 struct Layout {
   // full, empty, cs_full, cs_empty per stage; pfull[2], pempty[2]
   static constexpr int bars = STAGES * STAGE_BYTES;
@@ -53,14 +59,22 @@ struct Layout {
   static constexpr int colsc = misc + 16;                           // wgrad column scales [STAGES][BN]
   static constexpr int tiles_prefix = colsc + STAGES * BN * 4;
   static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
-  static constexpr int total = blk_prefix + (MAXG + 1) * 4;
+  static constexpr int stg = (blk_prefix + (MAXG + 1) * 4 + 1023) / 1024 * 1024;  // [8 warps][2 KB]
+  static constexpr int total = stg + (EPI_THREADS / 32) * 2048 * NSTG;
 };
-constexpr int SMEM_BYTES = Layout::total + 1024;
+template <int MODE>
+struct Cfg {
+  static constexpr int STAGES = MODE == GEMM_WGRAD ? 3 : 4;
+  static constexpr int NSTG = MODE == GEMM_WGRAD ? 2 : 1;
+  using L = Layout<STAGES, NSTG>;
+  static constexpr int SMEM_BYTES = L::total + 1024;
+};
 
 struct BwParams {
   GemmArgs g;
   int n_tiles;    // output column tiles
   int m_tiles_w;  // wgrad: output row tiles per group
+  int tma_out;    // output stored by TMA (tmOut valid)
 };
 
 struct BwTile {
@@ -116,8 +130,12 @@ FP8MOE_DEV BwTile bw_tile(const BwParams& p, const int* tiles_prefix, const int*
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_blockwise_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, BwParams p) {
+    k_blockwise_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmOut, BwParams p) {
   constexpr bool WGRAD = MODE == GEMM_WGRAD;
+  constexpr int STAGES = Cfg<MODE>::STAGES;
+  constexpr int NSTG = Cfg<MODE>::NSTG;
+  using Layout = typename Cfg<MODE>::L;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* full = (uint64_t*)(smem + Layout::bars);
@@ -309,6 +327,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int part = (warp - 2) >> 2;  // 128-column half of the tile
     const int lrow = quarter * 32 + lane;
     const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + part * EPI_COLS;
+    uint8_t* stg0 = smem + Layout::stg + (warp - 2) * 2048 * NSTG;
+    int slice = 0;  // slices staged by this warp (alternating tiles when NSTG == 2)
     const float* sa_p = (const float*)g.a_scale;
     const float* sb_p = (const float*)g.b_scale;
     uint32_t np = 0;
@@ -339,9 +359,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (MODE == GEMM_FWD) return sb_p[((int64_t)tl.e * (g.cols / 128) + cb) * (g.kk / 128) + ks];
         return sb_p[((int64_t)tl.e * (g.kk / 128) + ks) * (g.cols / 128) + cb];   // dgrad: W^T tiles
       };
-      float acc[EPI_COLS];
+      // column pairs: the promotion runs on packed fp32x2 multiplies / FMAs
+      float2 acc[EPI_COLS / 2];
 #pragma unroll
-      for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < EPI_COLS / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
       float rs_next = row_scale(0), cs_next = col_scale(0);
       bool ok = true;
       for (int ks = 0; ks < tl.nk; ++ks) {
@@ -375,19 +396,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint32_t r[16];
           tmem_ld16(taddr + pb * BN + c, r);
           tmem_ld_wait();
+          const float2 f2 = make_float2(f, f);
           if constexpr (WGRAD) {
             // the product times its column scale, then times the row scale
 #pragma unroll
             for (int j = 0; j < 16; j += 4) {
               const float4 cv = *reinterpret_cast<const float4*>(csv + c + j);
-              acc[c + j] = fmaf(__uint_as_float(r[j]) * cv.x, f, acc[c + j]);
-              acc[c + j + 1] = fmaf(__uint_as_float(r[j + 1]) * cv.y, f, acc[c + j + 1]);
-              acc[c + j + 2] = fmaf(__uint_as_float(r[j + 2]) * cv.z, f, acc[c + j + 2]);
-              acc[c + j + 3] = fmaf(__uint_as_float(r[j + 3]) * cv.w, f, acc[c + j + 3]);
+              const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                           make_float2(cv.x, cv.y));
+              const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                                           make_float2(cv.z, cv.w));
+              acc[(c + j) / 2] = __ffma2_rn(p0, f2, acc[(c + j) / 2]);
+              acc[(c + j) / 2 + 1] = __ffma2_rn(p1, f2, acc[(c + j) / 2 + 1]);
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[c + j] = fmaf(__uint_as_float(r[j]), f, acc[c + j]);
+            for (int j = 0; j < 16; j += 2)
+              acc[(c + j) / 2] =
+                  __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), f2, acc[(c + j) / 2]);
           }
         }
         tc_fence_before();
@@ -399,19 +425,68 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++np;
       }
       if (!ok) break;
-      if (!row_ok) continue;
+      // 32-column slices through the warp's staging tile: 16-byte chunk ch
+      // of row r at r * 64 + ((ch ^ ((r >> 1) & 3)) << 4) (the 64-byte
+      // swizzle of the output map; conflict-free for the row-per-lane writes
+      // and the 2-rows-per-8-lanes reads).  A warp whose 32 rows all belong
+      // to the tile hands the slice to a TMA store (wgrad's 3-D map clips
+      // rows past N); otherwise the lanes store with bounds checks.
+      const bool tma = p.tma_out && (WGRAD ? quarter * 32 < tl.rows : (quarter + 1) * 32 <= tl.rows);
+      if (!tma && quarter * 32 >= tl.rows) continue;
 #pragma unroll
-      for (int c = 0; c < EPI_COLS; c += 8) {
-        if (c0 + c < tl.ncols) {
-          uint4 v;
-          v.x = pack_bf16(acc[c], acc[c + 1]);
-          v.y = pack_bf16(acc[c + 2], acc[c + 3]);
-          v.z = pack_bf16(acc[c + 4], acc[c + 5]);
-          v.w = pack_bf16(acc[c + 6], acc[c + 7]);
-          *reinterpret_cast<uint4*>(orow + c0 + c) = v;
+      for (int j = 0; j < EPI_COLS / 32; ++j) {
+        const int64_t cc = c0 + j * 32;  // tile column of the slice
+        if (cc < tl.ncols) {
+          uint8_t* stg = stg0 + (slice % NSTG) * 2048;
+          ++slice;
+          // the store that last read this staging tile is done with it
+          if (lane == 0) {
+            if (tma && NSTG == 2) {
+              bulk_wait_read<1>();
+            } else {
+              bulk_wait_read<0>();
+            }
+          }
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int a0 = j * 32 + c * 8;
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(pack_bf16(acc[a0 / 2].x, acc[a0 / 2].y), pack_bf16(acc[a0 / 2 + 1].x, acc[a0 / 2 + 1].y),
+                           pack_bf16(acc[a0 / 2 + 2].x, acc[a0 / 2 + 2].y),
+                           pack_bf16(acc[a0 / 2 + 3].x, acc[a0 / 2 + 3].y));
+          }
+          if (tma) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (WGRAD) {
+                tma_store_3d(&tmOut, stg, (int)(tl.col0 + cc), (int)(tl.row0 + quarter * 32), tl.e);
+              } else {
+                tma_store_2d(&tmOut, stg, (int)(tl.col0 + cc), (int)(tl.row0 + quarter * 32));
+              }
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = i * 8 + (lane >> 2), ch = lane & 3;
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+              const int64_t trow = quarter * 32 + r, col = cc + ch * 8;
+              if (trow < tl.rows && col < tl.ncols) {
+                uint16_t* o = WGRAD ? g.out + ((int64_t)tl.e * g.rows + tl.row0 + trow) * g.cols + tl.col0 + col
+                                    : g.out + (tl.row0 + trow) * g.cols + tl.col0 + col;
+                *reinterpret_cast<uint4*>(o) = v;
+              }
+            }
+            __syncwarp();
+          }
         }
       }
     }
+    // the staged stores have left shared memory before the CTA exits
+    if (lane == 0) bulk_wait_all();
   }
   __syncthreads();
   if (warp == 1) {
@@ -421,13 +496,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int MODE>
-cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const BwParams& p, int64_t tiles,
-                        cudaStream_t st) {
+cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const BwParams& p,
+                        int64_t tiles, cudaStream_t st) {
   auto kern = k_blockwise_mm<MODE>;
+  constexpr int SMEM_BYTES = Cfg<MODE>::SMEM_BYTES;
+  if (SMEM_BYTES > p.g.max_smem) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int64_t grid = tiles < p.g.num_sms ? tiles : p.g.num_sms;
-  kern<<<(unsigned)(grid > 0 ? grid : 1), THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  kern<<<(unsigned)(grid > 0 ? grid : 1), THREADS, SMEM_BYTES, st>>>(ta, tb, to, p);
   return cudaGetLastError();
 }
 
@@ -436,7 +513,6 @@ cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const BwPa
 cudaError_t launch_blockwise_mm(const GemmArgs& g, cudaStream_t st) {
   if (g.E > MAXG) return cudaErrorNotSupported;
   if (g.kk > INT32_MAX || g.rows > INT32_MAX || g.cols > INT32_MAX || g.M > INT32_MAX) return cudaErrorInvalidValue;
-  if (SMEM_BYTES > g.max_smem) return cudaErrorNotSupported;
   const bool wgrad = g.mode == GEMM_WGRAD;
   BwParams p;
   p.g = g;
@@ -461,12 +537,31 @@ cudaError_t launch_blockwise_mm(const GemmArgs& g, cudaStream_t st) {
     cuuint32_t box[3] = {BK, BN, 1};
     if (!make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
+  // bf16 output slices of 32 columns x 32 rows, 64-byte swizzle; wgrad as
+  // [E, rows, cols] so that rows past an expert are clipped
+  CUtensorMap to = ta;
+  p.tma_out = 0;
+  if (((uintptr_t)g.out % 16) == 0) {
+    bool ok;
+    if (wgrad) {
+      cuuint64_t dims[3] = {(cuuint64_t)g.cols, (cuuint64_t)g.rows, (cuuint64_t)g.E};
+      cuuint64_t strides[2] = {(cuuint64_t)(g.cols * 2), (cuuint64_t)(g.rows * g.cols * 2)};
+      cuuint32_t box[3] = {32, 32, 1};
+      ok = make_tmap(&to, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.out, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    } else {
+      cuuint64_t dims[2] = {(cuuint64_t)g.cols, (cuuint64_t)(g.M > 0 ? g.M : 1)};
+      cuuint64_t strides[1] = {(cuuint64_t)(g.cols * 2)};
+      cuuint32_t box[2] = {32, 32};
+      ok = make_tmap(&to, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.out, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    }
+    p.tma_out = ok ? 1 : 0;
+  }
   // an upper bound on the tiles (the exact count needs the offsets)
   const int64_t tiles = wgrad ? (int64_t)g.E * p.m_tiles_w * p.n_tiles
                               : ((g.M + BM - 1) / BM + g.E) * (int64_t)p.n_tiles;
-  if (g.mode == GEMM_FWD) return launch_mode<GEMM_FWD>(ta, tb, p, tiles, st);
-  if (g.mode == GEMM_DGRAD) return launch_mode<GEMM_DGRAD>(ta, tb, p, tiles, st);
-  return launch_mode<GEMM_WGRAD>(ta, tb, p, tiles, st);
+  if (g.mode == GEMM_FWD) return launch_mode<GEMM_FWD>(ta, tb, to, p, tiles, st);
+  if (g.mode == GEMM_DGRAD) return launch_mode<GEMM_DGRAD>(ta, tb, to, p, tiles, st);
+  return launch_mode<GEMM_WGRAD>(ta, tb, to, p, tiles, st);
 }
 
 }  // namespace fp8moe
