@@ -41,8 +41,8 @@ METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)
 # from the ncu capture summarised in profiles/k_grouped_mm_scout.md.  It is
 # reported only while the kernel source is the one that was captured.
 GEMM_TRAFFIC = {"source": "mxfp8_moe_quantization_gb300/csrc/grouped_mm.cu",
-                "sha256": "f3238213d60e1d449dc0530ab2edc08602669c48771ea774a21525a161901779",
-                "bytes_per_launch": (1030.698e6 + 1079.303e6 + 1567.769e6) / 3}
+                "sha256": "c8c5f80c4714b0a9d43f8400cfb810f6a1f73a33023173519ecb6882dcda08c2",
+                "bytes_per_launch": (1029.789e6 + 1072.055e6 + 1563.509e6) / 3}
 
 
 def gemm_traffic():
@@ -365,21 +365,21 @@ def bench_rows(F, iters=10):
     q = torch.empty(wll.shape[::-1], dtype=torch.uint8, device=dev)
     inv = torch.empty(1, ll.K, dtype=torch.float32, device=dev)
     ms = timed(lambda: F.fp8moe_quantize_colwise_3d(wll[None], None, True, q=q, scale_inv=inv))
-    emit("a2", "k_colwise", "llama3_8b W^T [1,14336,4096] transposed", ms, nbytes=wll.numel() * 3 + ll.K * 4)
+    emit("a2", "k_cw_amax + k_cw_cast", "llama3_8b W^T [1,14336,4096] transposed", ms, nbytes=wll.numel() * 3 + ll.K * 4)
     dsoffs = torch.from_numpy(ds.offs()).to(dev)
     for which in ("W1", "W2"):
         wds = W.make_weights(ds, which, device=dev)
         q = torch.empty((wds.shape[0], wds.shape[2], wds.shape[1]), dtype=torch.uint8, device=dev)
         inv = torch.empty(wds.shape[0], wds.shape[2], dtype=torch.float32, device=dev)
         ms = timed(lambda: F.fp8moe_quantize_colwise_3d(wds, None, True, q=q, scale_inv=inv))
-        emit("a2", "k_colwise", f"dsmoe_16b {which} {list(wds.shape)} transposed", ms,
+        emit("a2", "k_cw_amax + k_cw_cast", f"dsmoe_16b {which} {list(wds.shape)} transposed", ms,
              nbytes=wds.numel() * 3 + wds.shape[0] * wds.shape[2] * 4)
         del wds
     ads = W.make_activations(ds, "A", device=dev)
     q = torch.empty((ds.K, F.fp8moe_jagged_t_cols(ds.M, ds.E)), dtype=torch.uint8, device=dev)
     inv = torch.empty(ds.E, ds.K, dtype=torch.float32, device=dev)
     ms = timed(lambda: F.fp8moe_quantize_colwise_3d(ads, dsoffs, True, q=q, scale_inv=inv))
-    emit("a2", "k_colwise", f"dsmoe_16b jagged A [{ds.M},{ds.K}] transposed", ms,
+    emit("a2", "k_cw_amax + k_cw_cast", f"dsmoe_16b jagged A [{ds.M},{ds.K}] transposed", ms,
          nbytes=ads.numel() * 3 + ds.E * ds.K * 4)
     qa = torch.empty(ads.shape, dtype=torch.uint8, device=dev)
     ia = torch.empty(ds.M, dtype=torch.float32, device=dev)
@@ -478,6 +478,44 @@ def bench_rows(F, iters=10):
         ms = timed(lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.ROWWISE, qdyt, s_en, qat, s_ek, offs, M, out=dw))
         emit("a8", "k_grouped_mm<rowwise,wgrad>", cfg, ms, flops=flops)
         del qa, qw, qdy, qwt, qdyt, qat, out, da, dw
+
+    # ---- MoE layer composites (next1) and blockwise scaling (next3) on the
+    # Scout W1 layer
+    soffs = torch.from_numpy(sc.offs()).to(dev)
+    M, E, N, K = sc.M, sc.E, sc.N, sc.K
+    T = int(sc.group_plan()[0].sum())
+    flops = 2.0 * T * N * K
+    a = W.make_activations(sc, "A", device=dev)
+    w = W.make_weights(sc, "W1", device=dev)
+    dy = torch.randn(M, N, device=dev).to(torch.bfloat16)
+    ws = torch.empty(F.fp8moe_mxfp8_moe_workspace_bytes(E, M, N, K), dtype=torch.uint8, device=dev)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    da = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    dw = torch.empty(E, N, K, dtype=torch.bfloat16, device=dev)
+    cfg = f"scout W1 M={M} N={N} K={K} E={E}"
+    ms = timed(lambda: F.fp8moe_mxfp8_moe_fwd(a, w, soffs, workspace=ws, out=out))
+    emit("next1", "fp8moe_mxfp8_moe_fwd (2 dual quant + fwd GEMM)", cfg, ms, flops=flops)
+    ms = timed(lambda: F.fp8moe_mxfp8_moe_bwd(dy, soffs, ws, K, da=da, dw=dw))
+    emit("next1", "fp8moe_mxfp8_moe_bwd (dual quant + dgrad + wgrad)", cfg, ms, flops=2 * flops)
+    del ws
+    qa, sa = F.fp8moe_quantize_blockwise_rows(a)
+    ms = timed(lambda: F.fp8moe_quantize_blockwise_rows(a, q=qa, scale_inv=sa))
+    emit("next3", "k_bw_rows", f"scout A [{M},{K}] 1x128", ms, nbytes=a.numel() * (3 + 4 / 128))
+    qw, qwt, sw = F.fp8moe_quantize_blockwise_weight(w)
+    ms = timed(lambda: F.fp8moe_quantize_blockwise_weight(w, q=qw, qt=qwt, scale_inv=sw))
+    emit("next3", "k_bw_weight (both layouts)", f"scout W1 {list(w.shape)} 128x128", ms, nbytes=w.numel() * 4)
+    qat, sat = F.fp8moe_quantize_blockwise_tokens(a, soffs)
+    ms = timed(lambda: F.fp8moe_quantize_blockwise_tokens(a, soffs, qt=qat, scale_inv=sat))
+    emit("next3", "k_bw_tokens", f"scout A [{M},{K}] 128-token tiles", ms, nbytes=a.numel() * (3 + 4 / 128))
+    qdy, sdy = F.fp8moe_quantize_blockwise_rows(dy)
+    qdyt, sdyt = F.fp8moe_quantize_blockwise_tokens(dy, soffs)
+    ms = timed(lambda: F.fp8moe_scaled_grouped_mm_fwd(F.BLOCKWISE, qa, sa, qw, sw, soffs, out=out))
+    emit("next3", "k_blockwise_mm<fwd>", cfg, ms, flops=flops)
+    ms = timed(lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.BLOCKWISE, qdy, sdy, qwt, sw, soffs, out=da))
+    emit("next3", "k_blockwise_mm<dgrad>", cfg, ms, flops=flops)
+    ms = timed(lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.BLOCKWISE, qdyt, sdyt, qat, sat, soffs, M, out=dw))
+    emit("next3", "k_blockwise_mm<wgrad>", cfg, ms, flops=flops)
+    del a, w, dy, out, da, dw, qa, qw, qwt, qat, qdy, qdyt
 
     # ---- routing (next2) on the Scout and DeepSeek-V3 token counts
     for wl, k in ((sc, 1), (v3, 8)):
