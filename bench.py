@@ -316,6 +316,7 @@ def bench_rows(F, iters=10):
     peaks, peak_kind = load_peaks()
     hbm, fp8 = peaks["hbm_gbs"], 2.0 * peaks["bf16_tflops"]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clean = torch.zeros(64 << 20, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
     def timed(fn):
@@ -324,9 +325,16 @@ def bench_rows(F, iters=10):
         torch.cuda.synchronize()
         ts = []
         for _ in range(iters):
+            # L2 flush: write a buffer twice the size of L2, then read another
+            # one, so that the write-backs of the flush's dirty lines finish
+            # before the timed region (the kernel starts from a cold, clean L2)
             flush.fill_(1)
+            clean.max()
             s = torch.cuda.Event(enable_timing=True)
             e = torch.cuda.Event(enable_timing=True)
+            # keep the GPU busy while the host enqueues the timed call, so
+            # that its launch latency is not inside the events
+            torch.cuda._sleep(200000)
             s.record(stream)
             fn()
             e.record(stream)

@@ -50,9 +50,26 @@ FP8MOE_DEV uint32_t enc2(float lo, float hi) {
 }
 
 // Four fp32 -> four codes packed little-endian into a 32-bit word.
+// fnuz, four at a time: the packed fn conversion of 2v, then two byte-wise
+// fix-ups.  A byte can need the 0x7F (= 240) code only where the fn
+// conversion gave +-448 (0x7E / 0xFE: |v| >= 216, within 10% of the fnuz
+// maximum), so the per-value check runs only when such a byte is present;
+// -0 (0x80) becomes the unsigned zero.
 template <bool FNUZ>
 FP8MOE_DEV uint32_t enc4(float a, float b, float c, float d) {
-  return enc2<FNUZ>(a, b) | (enc2<FNUZ>(c, d) << 16);
+  if constexpr (FNUZ) {
+    uint32_t w = cvt_e4m3x2(2.0f * a, 2.0f * b) | (cvt_e4m3x2(2.0f * c, 2.0f * d) << 16);
+    if (__vcmpeq4(w & 0x7F7F7F7Fu, 0x7E7E7E7Eu)) {
+      const float v[4] = {a, b, c, d};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (fabsf(2.0f * v[i]) > 464.0f)
+          w = (w & ~(0xFFu << (8 * i))) | ((0x7Fu | (v[i] < 0.0f ? 0x80u : 0u)) << (8 * i));
+    }
+    return w & ~__vcmpeq4(w, 0x80808080u);
+  } else {
+    return enc2<false>(a, b) | (enc2<false>(c, d) << 16);
+  }
 }
 
 // Encode 8 bf16 values (a uint4 of packed bf16 pairs) scaled by s.

@@ -7,13 +7,16 @@
 // (r, c) at (r % 32) * 16 + (r / 32) * 4 + c, i.e. 32 rows of 16 bytes, each
 // holding rows r, r+32, r+64, r+96 -- one 16-byte row per TMEM lane.
 //
-// The kernel is output-driven: each thread produces one 16-byte row of a tile
-// (so every output byte, padding included, is written exactly once and the
-// stores are contiguous) and gathers its 16 source bytes.  Group boundaries
-// come from device offsets: each group starts a new 128-row block (rows) or
-// 4-column block (columns).
+// A 128-row block of the tiled output is one contiguous region, and its
+// source rows are contiguous too (groups are padded to whole tiles), so each
+// CTA stages the block's source rows (a chunk of up to 128 scale columns) in
+// shared memory with coalesced loads and writes the tiles with contiguous
+// 16-byte stores; every output byte, padding included, is written once.
+// Group boundaries come from device offsets: each group starts a new 128-row
+// block (rows) or 4-column block (columns).
 #include "common.cuh"
 #include "launch.h"
+#include "scales.cuh"
 
 namespace fp8moe {
 
@@ -24,7 +27,8 @@ SwizzleGeom swizzle_geom(int64_t R, int64_t Cs, int64_t E, int group_axis) {
   return SwizzleGeom{rb * 128, cb * 4};
 }
 
-constexpr int SWZ_MAX_GROUPS = 1024;
+constexpr int SW_CC = 128;             // padded scale columns per chunk
+constexpr int SW_PITCH = SW_CC + 4;    // staged row: 33 words, so the 32 rows a warp reads hit 32 banks
 
 struct SwizzleArgs {
   const uint8_t* s;
@@ -37,96 +41,127 @@ struct SwizzleArgs {
   int* status;
 };
 
+// Source column of padded column pc in GROUP_COLS mode (-1 in a padding
+// column), and the source position the chunk boundary pc maps to.
+FP8MOE_DEV int find_last_le(const int64_t* pad, int E, int64_t key) {
+  int lo = 0, hi = E - 1, g = 0;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (pad[mid] <= key) {
+      g = mid;
+      lo = mid + 1;
+    } else {
+      hi = mid - 1;
+    }
+  }
+  return g;
+}
+
 __global__ void __launch_bounds__(256) k_swizzle(SwizzleArgs a) {
-  // padded start / real start / size of each group, in rows (GROUP_ROWS) or
-  // scale columns (GROUP_COLS)
-  __shared__ int64_t gp[SWZ_MAX_GROUPS + 1];
-  __shared__ int64_t gs[SWZ_MAX_GROUPS];
-  __shared__ int64_t gz[SWZ_MAX_GROUPS];
-  __shared__ int bad;
+  __shared__ GroupTable gt;
+  __shared__ __align__(16) uint8_t tile[128 * SW_PITCH];
   const bool grouped = a.group_axis != FP8MOE_NO_GROUPS;
-  if (grouped) {
-    if (threadIdx.x == 0) {
-      const int unit = a.group_axis == FP8MOE_GROUP_ROWS ? 128 : 4;
-      const int64_t total = a.group_axis == FP8MOE_GROUP_ROWS ? a.R : a.Cs * 32;
-      int64_t p = 0, prev = 0;
-      int b = 0;
-      for (int e = 0; e < a.E; ++e) {
-        int64_t end = a.offs[e];
-        if (end < prev || end > total) b = 1;
-        if (a.group_axis == FP8MOE_GROUP_COLS) {
-          if (end % 32) b = 1;
-        }
-        const int64_t sz_el = end - prev;
-        const int64_t sz = a.group_axis == FP8MOE_GROUP_COLS ? sz_el / 32 : sz_el;
-        gp[e] = p;
-        gs[e] = a.group_axis == FP8MOE_GROUP_COLS ? prev / 32 : prev;
-        gz[e] = sz;
-        p += (sz + unit - 1) / unit * unit;
-        prev = end;
+  const bool gcols = a.group_axis == FP8MOE_GROUP_COLS, grows = a.group_axis == FP8MOE_GROUP_ROWS;
+  if (grouped) build_group_table(gt, a.offs, a.E, grows ? a.R : a.Cs * 32, grows ? GT_ROWS128 : GT_COLS, a.status);
+  const bool bad = grouped && gt.bad;
+  // source column position of padded column pc (GROUP_COLS): inside group g,
+  // or the end of g's source columns when pc lies in g's padding
+  auto src_pos = [&](int64_t pc, bool& valid) -> int64_t {
+    if (!gcols) {
+      valid = pc < a.Cs;
+      return pc < a.Cs ? pc : a.Cs;
+    }
+    const int g = find_last_le(gt.pad, a.E, pc);
+    const int64_t st = (g == 0 ? 0 : gt.end[g - 1]) / 32, sz = gt.end[g] / 32 - st, w = pc - gt.pad[g];
+    valid = w < sz;
+    return st + (w < sz ? w : sz);
+  };
+  const int64_t nrb = a.Rp / 128, ncc = (a.Cp + SW_CC - 1) / SW_CC;
+  const bool words = !gcols && (a.Cs % 4) == 0;  // 4-byte loads: rows and chunk starts are word-aligned
+  for (int64_t u = blockIdx.x; u < a.B * nrb * ncc; u += gridDim.x) {
+    const int64_t b = u / (nrb * ncc), rbk = (u / ncc) % nrb, cc = u % ncc;
+    const int64_t pc0 = cc * SW_CC;
+    const int pcn = (int)min((int64_t)SW_CC, a.Cp - pc0);
+    // source rows of this padded row block
+    int64_t r0 = rbk * 128, rn;
+    if (grows) {
+      const int g = find_last_le(gt.pad, a.E, rbk * 128);
+      const int64_t st = g == 0 ? 0 : gt.end[g - 1], w = rbk * 128 - gt.pad[g];
+      r0 = st + w;
+      rn = gt.end[g] - r0;
+    } else {
+      rn = a.R - r0;
+    }
+    rn = bad ? 0 : (rn < 0 ? 0 : (rn > 128 ? 128 : rn));
+    bool v_unused;
+    const int64_t s_lo = src_pos(pc0, v_unused), s_hi = src_pos(pc0 + pcn, v_unused);
+    const int span = bad ? 0 : (int)(s_hi - s_lo);
+    __syncthreads();  // the previous unit's reads of the staged rows are done
+    const uint8_t* src = a.s + (b * a.R + r0) * a.Cs + s_lo;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (words) {
+      // warp w stages rows w, w + 8, ...; lane j their word j (spans are at
+      // most 32 words), 16 loads in flight per lane
+      const int spw = span / 4;
+      uint32_t wv[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const int i = warp + 8 * t;
+        wv[t] = i < rn && lane < spw ? __ldg(reinterpret_cast<const uint32_t*>(src + (int64_t)i * a.Cs) + lane) : 0u;
       }
-      if (prev != total) b = 1;
-      gp[a.E] = p;
-      bad = b;
-      if (b) set_status(a.status, FP8MOE_ERR_DEVICE_OFFSETS);
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        const int i = warp + 8 * t;
+        if (i < rn && lane < spw) *reinterpret_cast<uint32_t*>(tile + i * SW_PITCH + lane * 4) = wv[t];
+      }
+    } else {
+      for (int i = warp; i < rn; i += 8)
+        for (int j = lane; j < span; j += 32) tile[i * SW_PITCH + j] = __ldg(src + (int64_t)i * a.Cs + j);
     }
     __syncthreads();
-  }
-  const int64_t per_batch = a.Rp * a.Cp / 16;
-  const int64_t total = a.B * per_batch;
-  const int64_t tiles_per_rb = a.Cp / 4;
-  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total;
-       k += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t b = k / per_batch;
-    const int64_t kk = k % per_batch;
-    const int64_t tile = kk / 32;
-    const int r32 = (int)(kk % 32);
-    const int64_t rbk = tile / tiles_per_rb, cbk = tile % tiles_per_rb;
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int64_t prow = rbk * 128 + q * 32 + r32;
-      uint32_t word = 0;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int64_t pcol = cbk * 4 + c4;
-        int64_t r = -1, c = -1;
-        if (!grouped) {
-          r = prow;
-          c = pcol;
-        } else if (!bad) {
-          const int64_t key = a.group_axis == FP8MOE_GROUP_ROWS ? prow : pcol;
-          // last group whose padded start is <= key (skips empty groups)
-          int lo = 0, hi = a.E - 1, g = -1;
-          while (lo <= hi) {
-            const int mid = (lo + hi) >> 1;
-            if (gp[mid] <= key) {
-              g = mid;
-              lo = mid + 1;
-            } else {
-              hi = mid - 1;
-            }
-          }
-          if (g >= 0) {
-            const int64_t within = key - gp[g];
-            if (within < gz[g]) {
-              if (a.group_axis == FP8MOE_GROUP_ROWS) {
-                r = gs[g] + within;
-                c = pcol;
-              } else {
-                r = prow;
-                c = gs[g] + within;
-              }
-            }
-          }
+    // tiles (rbk, pc0/4 ...) are consecutive 512-byte blocks of the output
+    uint4* dst = reinterpret_cast<uint4*>(a.out + b * a.Rp * a.Cp + (rbk * (a.Cp / 4) + pc0 / 4) * 512);
+    for (int k = threadIdx.x; k < (pcn / 4) * 32; k += 256) {
+      const int t = k >> 5, r32 = k & 31;
+      // the tile's 4 padded columns: first staged column and how many hold data
+      bool v0;
+      const int64_t sp = src_pos(pc0 + 4 * t, v0);
+      int nvalid = 0;
+      if (!bad) {
+        if (gcols) {
+          bool vv;
+          const int64_t e4 = src_pos(pc0 + 4 * t + 3, vv);
+          nvalid = v0 ? (int)(e4 - sp) + (vv ? 1 : 0) : 0;
+        } else {
+          nvalid = (int)min((int64_t)4, a.Cs - (pc0 + 4 * t));
+          nvalid = nvalid < 0 ? 0 : nvalid;
         }
-        uint32_t v = 0;
-        if (r >= 0 && r < a.R && c >= 0 && c < a.Cs) v = a.s[(b * a.R + r) * a.Cs + c];
-        word |= v << (8 * c4);
       }
-      w[q] = word;
+      const int lc = (int)(sp - s_lo);
+      uint32_t w[4];
+      if (nvalid == 4 && (lc & 3) == 0) {
+        // a whole aligned word of each of the four rows
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = r32 + 32 * q;
+          w[q] = i < rn ? *reinterpret_cast<const uint32_t*>(tile + i * SW_PITCH + lc) : 0u;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = r32 + 32 * q;
+          uint32_t word = 0;
+          if (i < rn) {
+            const uint8_t* row = tile + i * SW_PITCH + lc;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+              if (c4 < nvalid) word |= (uint32_t)row[c4] << (8 * c4);
+          }
+          w[q] = word;
+        }
+      }
+      dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    reinterpret_cast<uint4*>(a.out + b * a.Rp * a.Cp)[kk] = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -146,11 +181,10 @@ cudaError_t launch_swizzle(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, c
   a.Cp = g.Cp;
   a.out = out;
   a.status = status;
-  const int64_t total = B * g.Rp * g.Cp / 16;
-  if (total == 0) return cudaSuccess;
-  int64_t blocks = (total + 255) / 256;
-  const int64_t cap = (int64_t)num_sms * 8;
-  if (blocks > cap) blocks = cap;
+  const int64_t units = B * (g.Rp / 128) * ((g.Cp + SW_CC - 1) / SW_CC);
+  if (units == 0) return cudaSuccess;
+  const int64_t cap = (int64_t)num_sms * 4;
+  const int64_t blocks = units < cap ? units : cap;
   k_swizzle<<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }

@@ -7,9 +7,9 @@
 // Three stream-ordered launches around the caller's one-float scale buffer,
 // which holds the maximum's bf16 bit pattern until the last one replaces it
 // by the dequantization scale:
-//   1. k_tw_amax: grid-stride 16-byte loads, warp / block maxima, one
-//      atomicMax per block (bit patterns of non-negative values order like
-//      the values);
+//   1. k_tw_amax: grid-stride 16-byte loads (four in flight per thread),
+//      warp / block maxima, one atomicMax per block (bit patterns of
+//      non-negative values order like the values);
 //   2. the cast: k_tw_cast for the plain layout, or the colwise kernel in its
 //      fixed-scale mode for the transposed / jagged layouts;
 //   3. k_tw_finalize: one thread writes fl(1 / s).
@@ -28,14 +28,28 @@ FP8MOE_DEV uint4 ld_nc(const void* p) {
   return v;
 }
 
+// Four 16-byte chunks in flight per thread and loop trip.
+constexpr int TW_U = 4;
+
 __global__ void __launch_bounds__(256) k_tw_amax(const uint16_t* __restrict__ x, int64_t n,
                                                  uint32_t* __restrict__ amax_bits) {
   __shared__ uint32_t wmax[8];
   const int64_t nch = n / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   uint32_t m = 0;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nch; i += stride)
-    m = max(m, absmax8_bits(ld_nc(x + i * 8)));
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nch; i += stride * TW_U) {
+    uint4 v[TW_U];
+    if (i + (TW_U - 1) * stride < nch) {  // all in range: unconditional loads, all in flight
+#pragma unroll
+      for (int u = 0; u < TW_U; ++u) v[u] = ld_nc(x + (i + u * stride) * 8);
+    } else {
+#pragma unroll
+      for (int u = 0; u < TW_U; ++u)
+        v[u] = i + u * stride < nch ? ld_nc(x + (i + u * stride) * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < TW_U; ++u) m = max(m, absmax8_bits(v[u]));
+  }
   // tail elements (n % 8)
   for (int64_t i = nch * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
     m = max(m, (uint32_t)x[i] & 0x7FFFu);
@@ -55,8 +69,25 @@ __global__ void __launch_bounds__(256) k_tw_cast(const uint16_t* __restrict__ x,
   rowwise_scale<FNUZ>(bf16bits_to_float(*amax_bits), s, inv);
   const int64_t nch = n / 8;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nch; i += stride)
-    *reinterpret_cast<uint2*>(q + i * 8) = enc8_bf16<FNUZ>(ld_nc(x + i * 8), s);
+  // chunks in the reverse of the amax pass's order: the first reads find
+  // the tensor's tail still in L2
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nch; i += stride * TW_U) {
+    uint4 v[TW_U];
+    if (i + (TW_U - 1) * stride < nch) {
+#pragma unroll
+      for (int u = 0; u < TW_U; ++u) v[u] = ld_nc(x + (nch - 1 - (i + u * stride)) * 8);
+#pragma unroll
+      for (int u = 0; u < TW_U; ++u)
+        *reinterpret_cast<uint2*>(q + (nch - 1 - (i + u * stride)) * 8) = enc8_bf16<FNUZ>(v[u], s);
+    } else {
+#pragma unroll
+      for (int u = 0; u < TW_U; ++u)
+        if (i + u * stride < nch) {
+          v[u] = ld_nc(x + (nch - 1 - (i + u * stride)) * 8);
+          *reinterpret_cast<uint2*>(q + (nch - 1 - (i + u * stride)) * 8) = enc8_bf16<FNUZ>(v[u], s);
+        }
+    }
+  }
   for (int64_t i = nch * 8 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
     q[i] = (uint8_t)(enc2<FNUZ>(__fmul_rn(bf16bits_to_float(x[i]), s), 0.0f) & 0xFFu);
 }
