@@ -304,7 +304,7 @@ def cpu_baseline(wl, budget_s=20.0):
 # ----------------------------------------------------------------------------
 # --rows: every hot-path row timed at its configuration size
 # ----------------------------------------------------------------------------
-def bench_rows(F, iters=10):
+def bench_rows(F, iters=10, only=None):
     """One JSON line per kernel: each step of the path at the configuration
     sizes of the MoE layers (CUDA events on the launching stream, median of
     `iters` runs after warm-up, an L2 flush between runs), with the fraction
@@ -313,6 +313,11 @@ def bench_rows(F, iters=10):
     import torch
     import workloads as W
     dev = torch.device("cuda")
+    sections = set(only.split(",")) if only else None
+
+    def want(name):
+        return sections is None or name in sections
+
     peaks, peak_kind = load_peaks()
     hbm, fp8 = peaks["hbm_gbs"], 2.0 * peaks["bf16_tflops"]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -364,184 +369,202 @@ def bench_rows(F, iters=10):
     ll, ds, sc, v3 = (W.get_workload(n) for n in ("llama3_8b", "dsmoe_16b", "scout", "dsv3"))
     x = W.make_activations(ll, "A", device=dev)
     wll = W.make_weights(ll, "W1", device=dev).reshape(ll.N, ll.K)
-    for kind, tag in ((F.E4M3FN, "a1"), (F.E4M3FNUZ, "a10")):
+    if want("rowwise"):
+        for kind, tag in ((F.E4M3FN, "a1"), (F.E4M3FNUZ, "a10")):
+            for name, t in (("X [8192,4096]", x), ("W [14336,4096]", wll)):
+                q = torch.empty(t.shape, dtype=torch.uint8, device=dev)
+                inv = torch.empty(t.shape[0], dtype=torch.float32, device=dev)
+                ms = timed(lambda: F.fp8moe_quantize_rowwise(t, kind=kind, q=q, scale_inv=inv))
+                emit(tag, "k_quant_rowwise", f"llama3_8b {name}", ms, nbytes=t.numel() * 3 + t.shape[0] * 4)
+        ads = W.make_activations(ds, "A", device=dev)
+        qa = torch.empty(ads.shape, dtype=torch.uint8, device=dev)
+        ia = torch.empty(ds.M, dtype=torch.float32, device=dev)
+        ms = timed(lambda: F.fp8moe_quantize_rowwise(ads, q=qa, scale_inv=ia))
+        emit("a1", "k_quant_rowwise", f"dsmoe_16b A [{ds.M},{ds.K}]", ms, nbytes=ads.numel() * 3 + ds.M * 4)
+        del ads
+    if want("colwise"):
+        q = torch.empty(wll.shape[::-1], dtype=torch.uint8, device=dev)
+        inv = torch.empty(1, ll.K, dtype=torch.float32, device=dev)
+        ms = timed(lambda: F.fp8moe_quantize_colwise_3d(wll[None], None, True, q=q, scale_inv=inv))
+        emit("a2", "k_cw_amax + k_cw_cast", "llama3_8b W^T [1,14336,4096] transposed", ms, nbytes=wll.numel() * 3 + ll.K * 4)
+        dsoffs = torch.from_numpy(ds.offs()).to(dev)
+        for which in ("W1", "W2"):
+            wds = W.make_weights(ds, which, device=dev)
+            q = torch.empty((wds.shape[0], wds.shape[2], wds.shape[1]), dtype=torch.uint8, device=dev)
+            inv = torch.empty(wds.shape[0], wds.shape[2], dtype=torch.float32, device=dev)
+            ms = timed(lambda: F.fp8moe_quantize_colwise_3d(wds, None, True, q=q, scale_inv=inv))
+            emit("a2", "k_cw_amax + k_cw_cast", f"dsmoe_16b {which} {list(wds.shape)} transposed", ms,
+                 nbytes=wds.numel() * 3 + wds.shape[0] * wds.shape[2] * 4)
+            del wds
+        ads = W.make_activations(ds, "A", device=dev)
+        q = torch.empty((ds.K, F.fp8moe_jagged_t_cols(ds.M, ds.E)), dtype=torch.uint8, device=dev)
+        inv = torch.empty(ds.E, ds.K, dtype=torch.float32, device=dev)
+        ms = timed(lambda: F.fp8moe_quantize_colwise_3d(ads, dsoffs, True, q=q, scale_inv=inv))
+        emit("a2", "k_cw_amax + k_cw_cast", f"dsmoe_16b jagged A [{ds.M},{ds.K}] transposed", ms,
+             nbytes=ads.numel() * 3 + ds.E * ds.K * 4)
+        del ads
+    if want("tensorwise"):
         for name, t in (("X [8192,4096]", x), ("W [14336,4096]", wll)):
             q = torch.empty(t.shape, dtype=torch.uint8, device=dev)
-            inv = torch.empty(t.shape[0], dtype=torch.float32, device=dev)
-            ms = timed(lambda: F.fp8moe_quantize_rowwise(t, kind=kind, q=q, scale_inv=inv))
-            emit(tag, "k_quant_rowwise", f"llama3_8b {name}", ms, nbytes=t.numel() * 3 + t.shape[0] * 4)
-    q = torch.empty(wll.shape[::-1], dtype=torch.uint8, device=dev)
-    inv = torch.empty(1, ll.K, dtype=torch.float32, device=dev)
-    ms = timed(lambda: F.fp8moe_quantize_colwise_3d(wll[None], None, True, q=q, scale_inv=inv))
-    emit("a2", "k_cw_amax + k_cw_cast", "llama3_8b W^T [1,14336,4096] transposed", ms, nbytes=wll.numel() * 3 + ll.K * 4)
-    dsoffs = torch.from_numpy(ds.offs()).to(dev)
-    for which in ("W1", "W2"):
-        wds = W.make_weights(ds, which, device=dev)
-        q = torch.empty((wds.shape[0], wds.shape[2], wds.shape[1]), dtype=torch.uint8, device=dev)
-        inv = torch.empty(wds.shape[0], wds.shape[2], dtype=torch.float32, device=dev)
-        ms = timed(lambda: F.fp8moe_quantize_colwise_3d(wds, None, True, q=q, scale_inv=inv))
-        emit("a2", "k_cw_amax + k_cw_cast", f"dsmoe_16b {which} {list(wds.shape)} transposed", ms,
-             nbytes=wds.numel() * 3 + wds.shape[0] * wds.shape[2] * 4)
-        del wds
-    ads = W.make_activations(ds, "A", device=dev)
-    q = torch.empty((ds.K, F.fp8moe_jagged_t_cols(ds.M, ds.E)), dtype=torch.uint8, device=dev)
-    inv = torch.empty(ds.E, ds.K, dtype=torch.float32, device=dev)
-    ms = timed(lambda: F.fp8moe_quantize_colwise_3d(ads, dsoffs, True, q=q, scale_inv=inv))
-    emit("a2", "k_cw_amax + k_cw_cast", f"dsmoe_16b jagged A [{ds.M},{ds.K}] transposed", ms,
-         nbytes=ads.numel() * 3 + ds.E * ds.K * 4)
-    qa = torch.empty(ads.shape, dtype=torch.uint8, device=dev)
-    ia = torch.empty(ds.M, dtype=torch.float32, device=dev)
-    ms = timed(lambda: F.fp8moe_quantize_rowwise(ads, q=qa, scale_inv=ia))
-    emit("a1", "k_quant_rowwise", f"dsmoe_16b A [{ds.M},{ds.K}]", ms, nbytes=ads.numel() * 3 + ds.M * 4)
-    for name, t in (("X [8192,4096]", x), ("W [14336,4096]", wll)):
-        q = torch.empty(t.shape, dtype=torch.uint8, device=dev)
-        inv = torch.empty(1, dtype=torch.float32, device=dev)
-        ms = timed(lambda: F.fp8moe_quantize_tensorwise(t, q=q, scale_inv=inv))
-        emit("next4", "k_tw_amax + k_tw_cast", f"llama3_8b {name} tensorwise", ms, nbytes=t.numel() * 3)
-    del x, wll, ads
+            inv = torch.empty(1, dtype=torch.float32, device=dev)
+            ms = timed(lambda: F.fp8moe_quantize_tensorwise(t, q=q, scale_inv=inv))
+            emit("next4", "k_tw_amax + k_tw_cast", f"llama3_8b {name} tensorwise", ms, nbytes=t.numel() * 3)
+    del x, wll
 
     # ---- MXFP8 quantization rows (a3, a4, a5, fused dual) on Scout and DeepSeek-V3
     soffs = torch.from_numpy(sc.offs()).to(dev)
-    a = W.make_activations(sc, "A", device=dev)
-    w1 = W.make_weights(sc, "W1", device=dev)
-    for name, t, offs, l0, l1 in (("A [16640,5120]", a, soffs, F.GROUP_ROWS, F.GROUP_COLS),
-                                  ("W1 [16,8192,5120]", w1, None, F.NO_GROUPS, F.NO_GROUPS)):
-        o = F.fp8moe_mxfp8_quantize_dual(t, offs, l0, l1)
-        n = t.numel()
-        ms = timed(lambda: F.fp8moe_mxfp8_quantize_dim0(t, q=o[0]))
-        emit("a3", "k_mx_dim0", f"scout {name}", ms, nbytes=n * (3 + 1 / 32))
-        ms = timed(lambda: F.fp8moe_mxfp8_quantize_dim1(t, qt=o[2]))
-        emit("a4", "k_mx_dual<dim1>", f"scout {name}", ms, nbytes=n * (3 + 1 / 32))
-        ms = timed(lambda: F.fp8moe_mxfp8_quantize_dual(t, offs, l0, l1, q0=o[0], s0=o[1], q1=o[2], s1=o[3]))
-        emit("next1", "k_mx_dual (both directions, one read)", f"scout {name} final-layout scales", ms,
-             nbytes=n * (4 + 2 / 32))
-    s_rm = torch.empty(sc.E, sc.N, sc.K // 32, dtype=torch.uint8, device=dev)
-    F.fp8moe_mxfp8_quantize_dim0(w1, scale=s_rm)
-    s_sw = torch.zeros(F.fp8moe_swizzled_scales_bytes(sc.E, sc.N, sc.K // 32), dtype=torch.uint8, device=dev)
-    ms = timed(lambda: F.fp8moe_swizzle_scales_128x4(s_rm, out=s_sw))
-    emit("a5", "k_swizzle", "scout W1 scales [16,8192,160]", ms, nbytes=s_rm.numel() * 2)
-    del a, w1, s_rm, s_sw
-    w3 = W.make_weights(v3, "W1", device=dev)
-    o = F.fp8moe_mxfp8_quantize_dual(w3, None, F.NO_GROUPS, F.NO_GROUPS)
-    ms = timed(lambda: F.fp8moe_mxfp8_quantize_dual(w3, None, F.NO_GROUPS, F.NO_GROUPS, q0=o[0], s0=o[1], q1=o[2],
-                                                     s1=o[3]))
-    emit("next1", "k_mx_dual (both directions, one read)", "dsv3 W1 [256,2048,7168]", ms,
-         nbytes=w3.numel() * (4 + 2 / 32))
-    ms = timed(lambda: F.fp8moe_mxfp8_quantize_dim0(w3, q=o[0]))
-    emit("a3", "k_mx_dim0", "dsv3 W1 [256,2048,7168]", ms, nbytes=w3.numel() * (3 + 1 / 32))
-    del w3, o
+    if want("mx") or want("swizzle"):
+        a = W.make_activations(sc, "A", device=dev)
+        w1 = W.make_weights(sc, "W1", device=dev)
+    if want("mx"):
+        for name, t, offs, l0, l1 in (("A [16640,5120]", a, soffs, F.GROUP_ROWS, F.GROUP_COLS),
+                                      ("W1 [16,8192,5120]", w1, None, F.NO_GROUPS, F.NO_GROUPS)):
+            o = F.fp8moe_mxfp8_quantize_dual(t, offs, l0, l1)
+            n = t.numel()
+            ms = timed(lambda: F.fp8moe_mxfp8_quantize_dim0(t, q=o[0]))
+            emit("a3", "k_mx_dim0", f"scout {name}", ms, nbytes=n * (3 + 1 / 32))
+            ms = timed(lambda: F.fp8moe_mxfp8_quantize_dim1(t, qt=o[2]))
+            emit("a4", "k_mx_dual<dim1>", f"scout {name}", ms, nbytes=n * (3 + 1 / 32))
+            ms = timed(lambda: F.fp8moe_mxfp8_quantize_dual(t, offs, l0, l1, q0=o[0], s0=o[1], q1=o[2], s1=o[3]))
+            emit("next1", "k_mx_dual (both directions, one read)", f"scout {name} final-layout scales", ms,
+                 nbytes=n * (4 + 2 / 32))
+    if want("swizzle"):
+        s_rm = torch.empty(sc.E, sc.N, sc.K // 32, dtype=torch.uint8, device=dev)
+        F.fp8moe_mxfp8_quantize_dim0(w1, scale=s_rm)
+        s_sw = torch.zeros(F.fp8moe_swizzled_scales_bytes(sc.E, sc.N, sc.K // 32), dtype=torch.uint8, device=dev)
+        ms = timed(lambda: F.fp8moe_swizzle_scales_128x4(s_rm, out=s_sw))
+        emit("a5", "k_swizzle", "scout W1 scales [16,8192,160]", ms, nbytes=s_rm.numel() * 2)
+    if want("mx") or want("swizzle"):
+        del a, w1
+    if want("mx"):
+        w3 = W.make_weights(v3, "W1", device=dev)
+        o = F.fp8moe_mxfp8_quantize_dual(w3, None, F.NO_GROUPS, F.NO_GROUPS)
+        ms = timed(lambda: F.fp8moe_mxfp8_quantize_dual(w3, None, F.NO_GROUPS, F.NO_GROUPS, q0=o[0], s0=o[1], q1=o[2],
+                                                         s1=o[3]))
+        emit("next1", "k_mx_dual (both directions, one read)", "dsv3 W1 [256,2048,7168]", ms,
+             nbytes=w3.numel() * (4 + 2 / 32))
+        ms = timed(lambda: F.fp8moe_mxfp8_quantize_dim0(w3, q=o[0]))
+        emit("a3", "k_mx_dim0", "dsv3 W1 [256,2048,7168]", ms, nbytes=w3.numel() * (3 + 1 / 32))
+        del w3, o
 
     # ---- grouped GEMMs (a6-a8): MXFP8 on Scout and DeepSeek-V3, rowwise on
     # DeepSeek-MoE-16B and the dense Llama3 linear
-    for wl in (sc, v3):
-        offs = torch.from_numpy(wl.offs()).to(dev)
-        M, E, T = wl.M, wl.E, int(wl.group_plan()[0].sum())
-        live = int((wl.group_plan()[0] > 0).sum())
-        for (N, K, wname) in ((wl.N, wl.K, "W1"), (wl.K, wl.N, "W2")):
-            flops = 2.0 * T * N * K
-            qa, qw, qdy, qwt = codes(M, K), codes(E, N, K), codes(M, N), codes(E, K, N)
-            qdyt, qat = codes(N, M), codes(K, M)
+    if want("gemm"):
+        for wl in (sc, v3):
+            offs = torch.from_numpy(wl.offs()).to(dev)
+            M, E, T = wl.M, wl.E, int(wl.group_plan()[0].sum())
+            live = int((wl.group_plan()[0] > 0).sum())
+            for (N, K, wname) in ((wl.N, wl.K, "W1"), (wl.K, wl.N, "W2")):
+                flops = 2.0 * T * N * K
+                qa, qw, qdy, qwt = codes(M, K), codes(E, N, K), codes(M, N), codes(E, K, N)
+                qdyt, qat = codes(N, M), codes(K, M)
 
-            def sc_(n):
-                return torch.full((n,), 127, dtype=torch.uint8, device=dev)
-            sa = sc_(F.fp8moe_swizzled_scales_bytes(1, M, K // 32, E, F.GROUP_ROWS))
-            sw = sc_(F.fp8moe_swizzled_scales_bytes(E, N, K // 32))
-            sdy = sc_(F.fp8moe_swizzled_scales_bytes(1, M, N // 32, E, F.GROUP_ROWS))
-            swt = sc_(F.fp8moe_swizzled_scales_bytes(E, K, N // 32))
-            sdyt = sc_(F.fp8moe_swizzled_scales_bytes(1, N, M // 32, E, F.GROUP_COLS))
-            sat = sc_(F.fp8moe_swizzled_scales_bytes(1, K, M // 32, E, F.GROUP_COLS))
+                def sc_(n):
+                    return torch.full((n,), 127, dtype=torch.uint8, device=dev)
+                sa = sc_(F.fp8moe_swizzled_scales_bytes(1, M, K // 32, E, F.GROUP_ROWS))
+                sw = sc_(F.fp8moe_swizzled_scales_bytes(E, N, K // 32))
+                sdy = sc_(F.fp8moe_swizzled_scales_bytes(1, M, N // 32, E, F.GROUP_ROWS))
+                swt = sc_(F.fp8moe_swizzled_scales_bytes(E, K, N // 32))
+                sdyt = sc_(F.fp8moe_swizzled_scales_bytes(1, N, M // 32, E, F.GROUP_COLS))
+                sat = sc_(F.fp8moe_swizzled_scales_bytes(1, K, M // 32, E, F.GROUP_COLS))
+                out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+                da = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+                dw = torch.empty(E, N, K, dtype=torch.bfloat16, device=dev)
+                # HBM bytes: fp8 operands (weights of live experts) + bf16 output
+                fb = M * K + live * N * K + M * N * 2
+                db = M * N + live * N * K + M * K * 2
+                wb = (N + K) * M + E * N * K * 2
+                cfg = f"{wl.name} {wname} M={M} N={N} K={K} E={E}"
+                hb = wl.name == "dsv3"
+                ms = timed(lambda: F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, offs, out=out))
+                emit("a6", "k_grouped_mm<MX,fwd>", cfg, ms, nbytes=fb, flops=flops, roof_of_hbm=hb)
+                ms = timed(lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.MXFP8, qdy, sdy, qwt, swt, offs, out=da))
+                emit("a7", "k_grouped_mm<MX,dgrad>", cfg, ms, nbytes=db, flops=flops, roof_of_hbm=hb)
+                ms = timed(lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.MXFP8, qdyt, sdyt, qat, sat, offs, M, out=dw))
+                emit("a8", "k_grouped_mm<MX,wgrad>", cfg, ms, nbytes=wb, flops=flops, roof_of_hbm=hb)
+                del qa, qw, qdy, qwt, qdyt, qat, out, da, dw
+        for wl in (ds, ll):
+            offs = torch.from_numpy(wl.offs()).to(dev)
+            M, E, N, K = wl.M, wl.E, wl.N, wl.K
+            Mt = F.fp8moe_jagged_t_cols(M, E)
+            flops = 2.0 * M * N * K
+            qa, qw, qdy, qwt, qdyt, qat = codes(M, K), codes(E, N, K), codes(M, N), codes(E, K, N), codes(N, Mt), codes(K, Mt)
+            s_m = torch.ones(M, dtype=torch.float32, device=dev)
+            s_en = torch.ones(E, N, dtype=torch.float32, device=dev)
+            s_ek = torch.ones(E, K, dtype=torch.float32, device=dev)
+            cfg = f"{wl.name} M={M} N={N} K={K} E={E}"
             out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            ms = timed(lambda: F.fp8moe_scaled_grouped_mm_fwd(F.ROWWISE, qa, s_m, qw, s_en, offs, out=out))
+            emit("a6", "k_grouped_mm<rowwise,fwd>", cfg, ms, flops=flops)
             da = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+            ms = timed(lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.ROWWISE, qdy, s_m, qwt, s_ek, offs, out=da))
+            emit("a7", "k_grouped_mm<rowwise,dgrad>", cfg, ms, flops=flops)
             dw = torch.empty(E, N, K, dtype=torch.bfloat16, device=dev)
-            # HBM bytes: fp8 operands (weights of live experts) + bf16 output
-            fb = M * K + live * N * K + M * N * 2
-            db = M * N + live * N * K + M * K * 2
-            wb = (N + K) * M + E * N * K * 2
-            cfg = f"{wl.name} {wname} M={M} N={N} K={K} E={E}"
-            hb = wl.name == "dsv3"
-            ms = timed(lambda: F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, offs, out=out))
-            emit("a6", "k_grouped_mm<MX,fwd>", cfg, ms, nbytes=fb, flops=flops, roof_of_hbm=hb)
-            ms = timed(lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.MXFP8, qdy, sdy, qwt, swt, offs, out=da))
-            emit("a7", "k_grouped_mm<MX,dgrad>", cfg, ms, nbytes=db, flops=flops, roof_of_hbm=hb)
-            ms = timed(lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.MXFP8, qdyt, sdyt, qat, sat, offs, M, out=dw))
-            emit("a8", "k_grouped_mm<MX,wgrad>", cfg, ms, nbytes=wb, flops=flops, roof_of_hbm=hb)
+            ms = timed(lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.ROWWISE, qdyt, s_en, qat, s_ek, offs, M, out=dw))
+            emit("a8", "k_grouped_mm<rowwise,wgrad>", cfg, ms, flops=flops)
             del qa, qw, qdy, qwt, qdyt, qat, out, da, dw
-    for wl in (ds, ll):
-        offs = torch.from_numpy(wl.offs()).to(dev)
-        M, E, N, K = wl.M, wl.E, wl.N, wl.K
-        Mt = F.fp8moe_jagged_t_cols(M, E)
-        flops = 2.0 * M * N * K
-        qa, qw, qdy, qwt, qdyt, qat = codes(M, K), codes(E, N, K), codes(M, N), codes(E, K, N), codes(N, Mt), codes(K, Mt)
-        s_m = torch.ones(M, dtype=torch.float32, device=dev)
-        s_en = torch.ones(E, N, dtype=torch.float32, device=dev)
-        s_ek = torch.ones(E, K, dtype=torch.float32, device=dev)
-        cfg = f"{wl.name} M={M} N={N} K={K} E={E}"
-        out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-        ms = timed(lambda: F.fp8moe_scaled_grouped_mm_fwd(F.ROWWISE, qa, s_m, qw, s_en, offs, out=out))
-        emit("a6", "k_grouped_mm<rowwise,fwd>", cfg, ms, flops=flops)
-        da = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
-        ms = timed(lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.ROWWISE, qdy, s_m, qwt, s_ek, offs, out=da))
-        emit("a7", "k_grouped_mm<rowwise,dgrad>", cfg, ms, flops=flops)
-        dw = torch.empty(E, N, K, dtype=torch.bfloat16, device=dev)
-        ms = timed(lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.ROWWISE, qdyt, s_en, qat, s_ek, offs, M, out=dw))
-        emit("a8", "k_grouped_mm<rowwise,wgrad>", cfg, ms, flops=flops)
-        del qa, qw, qdy, qwt, qdyt, qat, out, da, dw
 
     # ---- MoE layer composites (next1) and blockwise scaling (next3) on the
     # Scout W1 layer
-    soffs = torch.from_numpy(sc.offs()).to(dev)
-    M, E, N, K = sc.M, sc.E, sc.N, sc.K
-    T = int(sc.group_plan()[0].sum())
-    flops = 2.0 * T * N * K
-    a = W.make_activations(sc, "A", device=dev)
-    w = W.make_weights(sc, "W1", device=dev)
-    dy = torch.randn(M, N, device=dev).to(torch.bfloat16)
-    ws = torch.empty(F.fp8moe_mxfp8_moe_workspace_bytes(E, M, N, K), dtype=torch.uint8, device=dev)
-    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-    da = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
-    dw = torch.empty(E, N, K, dtype=torch.bfloat16, device=dev)
-    cfg = f"scout W1 M={M} N={N} K={K} E={E}"
-    ms = timed(lambda: F.fp8moe_mxfp8_moe_fwd(a, w, soffs, workspace=ws, out=out))
-    emit("next1", "fp8moe_mxfp8_moe_fwd (2 dual quant + fwd GEMM)", cfg, ms, flops=flops)
-    ms = timed(lambda: F.fp8moe_mxfp8_moe_bwd(dy, soffs, ws, K, da=da, dw=dw))
-    emit("next1", "fp8moe_mxfp8_moe_bwd (dual quant + dgrad + wgrad)", cfg, ms, flops=2 * flops)
-    del ws
-    qa, sa = F.fp8moe_quantize_blockwise_rows(a)
-    ms = timed(lambda: F.fp8moe_quantize_blockwise_rows(a, q=qa, scale_inv=sa))
-    emit("next3", "k_bw_rows", f"scout A [{M},{K}] 1x128", ms, nbytes=a.numel() * (3 + 4 / 128))
-    qw, qwt, sw = F.fp8moe_quantize_blockwise_weight(w)
-    ms = timed(lambda: F.fp8moe_quantize_blockwise_weight(w, q=qw, qt=qwt, scale_inv=sw))
-    emit("next3", "k_bw_weight (both layouts)", f"scout W1 {list(w.shape)} 128x128", ms, nbytes=w.numel() * 4)
-    qat, sat = F.fp8moe_quantize_blockwise_tokens(a, soffs)
-    ms = timed(lambda: F.fp8moe_quantize_blockwise_tokens(a, soffs, qt=qat, scale_inv=sat))
-    emit("next3", "k_bw_tokens", f"scout A [{M},{K}] 128-token tiles", ms, nbytes=a.numel() * (3 + 4 / 128))
-    qdy, sdy = F.fp8moe_quantize_blockwise_rows(dy)
-    qdyt, sdyt = F.fp8moe_quantize_blockwise_tokens(dy, soffs)
-    ms = timed(lambda: F.fp8moe_scaled_grouped_mm_fwd(F.BLOCKWISE, qa, sa, qw, sw, soffs, out=out))
-    emit("next3", "k_blockwise_mm<fwd>", cfg, ms, flops=flops)
-    ms = timed(lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.BLOCKWISE, qdy, sdy, qwt, sw, soffs, out=da))
-    emit("next3", "k_blockwise_mm<dgrad>", cfg, ms, flops=flops)
-    ms = timed(lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.BLOCKWISE, qdyt, sdyt, qat, sat, soffs, M, out=dw))
-    emit("next3", "k_blockwise_mm<wgrad>", cfg, ms, flops=flops)
-    del a, w, dy, out, da, dw, qa, qw, qwt, qat, qdy, qdyt
+    if want("layer") or want("blockwise"):
+        soffs = torch.from_numpy(sc.offs()).to(dev)
+        M, E, N, K = sc.M, sc.E, sc.N, sc.K
+        T = int(sc.group_plan()[0].sum())
+        flops = 2.0 * T * N * K
+        a = W.make_activations(sc, "A", device=dev)
+        w = W.make_weights(sc, "W1", device=dev)
+        dy = torch.randn(M, N, device=dev).to(torch.bfloat16)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        da = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        dw = torch.empty(E, N, K, dtype=torch.bfloat16, device=dev)
+        cfg = f"scout W1 M={M} N={N} K={K} E={E}"
+    if want("layer"):
+        ws = torch.empty(F.fp8moe_mxfp8_moe_workspace_bytes(E, M, N, K), dtype=torch.uint8, device=dev)
+        ms = timed(lambda: F.fp8moe_mxfp8_moe_fwd(a, w, soffs, workspace=ws, out=out))
+        emit("next1", "fp8moe_mxfp8_moe_fwd (2 dual quant + fwd GEMM)", cfg, ms, flops=flops)
+        ms = timed(lambda: F.fp8moe_mxfp8_moe_bwd(dy, soffs, ws, K, da=da, dw=dw))
+        emit("next1", "fp8moe_mxfp8_moe_bwd (dual quant + dgrad + wgrad)", cfg, ms, flops=2 * flops)
+        del ws
+    if want("blockwise"):
+        qa, sa = F.fp8moe_quantize_blockwise_rows(a)
+        ms = timed(lambda: F.fp8moe_quantize_blockwise_rows(a, q=qa, scale_inv=sa))
+        emit("next3", "k_bw_rows", f"scout A [{M},{K}] 1x128", ms, nbytes=a.numel() * (3 + 4 / 128))
+        qw, qwt, sw = F.fp8moe_quantize_blockwise_weight(w)
+        ms = timed(lambda: F.fp8moe_quantize_blockwise_weight(w, q=qw, qt=qwt, scale_inv=sw))
+        emit("next3", "k_bw_weight (both layouts)", f"scout W1 {list(w.shape)} 128x128", ms, nbytes=w.numel() * 4)
+        qat, sat = F.fp8moe_quantize_blockwise_tokens(a, soffs)
+        ms = timed(lambda: F.fp8moe_quantize_blockwise_tokens(a, soffs, qt=qat, scale_inv=sat))
+        emit("next3", "k_bw_tokens", f"scout A [{M},{K}] 128-token tiles", ms, nbytes=a.numel() * (3 + 4 / 128))
+        qdy, sdy = F.fp8moe_quantize_blockwise_rows(dy)
+        qdyt, sdyt = F.fp8moe_quantize_blockwise_tokens(dy, soffs)
+        ms = timed(lambda: F.fp8moe_scaled_grouped_mm_fwd(F.BLOCKWISE, qa, sa, qw, sw, soffs, out=out))
+        emit("next3", "k_blockwise_mm<fwd>", cfg, ms, flops=flops)
+        ms = timed(lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.BLOCKWISE, qdy, sdy, qwt, sw, soffs, out=da))
+        emit("next3", "k_blockwise_mm<dgrad>", cfg, ms, flops=flops)
+        ms = timed(lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.BLOCKWISE, qdyt, sdyt, qat, sat, soffs, M, out=dw))
+        emit("next3", "k_blockwise_mm<wgrad>", cfg, ms, flops=flops)
+        del qa, qw, qwt, qat, qdy, qdyt
+    if want("layer") or want("blockwise"):
+        del a, w, dy, out, da, dw
 
     # ---- routing (next2) on the Scout and DeepSeek-V3 token counts
-    for wl, k in ((sc, 1), (v3, 8)):
-        T, E, H = wl.tokens, wl.E, wl.K
-        g = torch.Generator(device=dev).manual_seed(wl.seed)
-        idx = torch.stack([torch.randperm(E, device=dev, generator=g)[:k] for _ in range(T)]).to(torch.int32) \
-            if k > 1 else torch.randint(0, E, (T, 1), device=dev, generator=g, dtype=torch.int32)
-        xt = torch.randn(T, H, device=dev, generator=g).to(torch.bfloat16)
-        wt = torch.rand(T, k, device=dev, generator=g)
-        ws = torch.empty(max(F.fp8moe_route_workspace_bytes(T, k, E), 4), dtype=torch.uint8, device=dev)
-        a, offs, row_of = F.fp8moe_route_permute(xt, idx, E, workspace=ws)
-        ms = timed(lambda: F.fp8moe_route_permute(xt, idx, E, a=a, offs=offs, row_of=row_of, workspace=ws))
-        emit("next2", "route_permute (count, scan, rank, copy)", f"{wl.name} T={T} k={k} E={E} H={H}", ms,
-             nbytes=T * H * 2 + a.numel() * 2)
-        outt = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-        ms = timed(lambda: F.fp8moe_route_unpermute(a, row_of, wt, out=outt))
-        emit("next2", "k_route_unpermute", f"{wl.name} T={T} k={k} N={H}", ms, nbytes=T * k * H * 2 + T * H * 2)
-        del xt, a, outt
+    if want("routing"):
+        for wl, k in ((sc, 1), (v3, 8)):
+            T, E, H = wl.tokens, wl.E, wl.K
+            g = torch.Generator(device=dev).manual_seed(wl.seed)
+            idx = torch.stack([torch.randperm(E, device=dev, generator=g)[:k] for _ in range(T)]).to(torch.int32) \
+                if k > 1 else torch.randint(0, E, (T, 1), device=dev, generator=g, dtype=torch.int32)
+            xt = torch.randn(T, H, device=dev, generator=g).to(torch.bfloat16)
+            wt = torch.rand(T, k, device=dev, generator=g)
+            ws = torch.empty(max(F.fp8moe_route_workspace_bytes(T, k, E), 4), dtype=torch.uint8, device=dev)
+            a, offs, row_of = F.fp8moe_route_permute(xt, idx, E, workspace=ws)
+            ms = timed(lambda: F.fp8moe_route_permute(xt, idx, E, a=a, offs=offs, row_of=row_of, workspace=ws))
+            emit("next2", "route_permute (count, scan, rank, copy)", f"{wl.name} T={T} k={k} E={E} H={H}", ms,
+                 nbytes=T * H * 2 + a.numel() * 2)
+            outt = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            ms = timed(lambda: F.fp8moe_route_unpermute(a, row_of, wt, out=outt))
+            emit("next2", "k_route_unpermute", f"{wl.name} T={T} k={k} N={H}", ms, nbytes=T * k * H * 2 + T * H * 2)
+            del xt, a, outt
 
 
 def main():
@@ -556,6 +579,9 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="separate dim0 / dim1 / swizzle launches instead of the fused dual-direction kernel")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only", default=None,
+                    help="with --rows: comma-separated sections (rowwise, colwise, tensorwise, mx, swizzle, gemm, "
+                         "layer, blockwise, routing)")
     ap.add_argument("--rows", action="store_true",
                     help="time every hot-path kernel at its configuration size (one JSON line each) and exit")
     args = ap.parse_args()
@@ -597,7 +623,7 @@ def main():
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     if args.rows:
-        bench_rows(F)
+        bench_rows(F, only=args.only)
         return
     pg = None
     if world > 1:
