@@ -244,32 +244,61 @@ class ScoutStep:
                                                                  L["sat_sw"], offs, self.M, out=L["dw"]))
 
 
-def run_e2e(F, step, steps, warmup):
-    """Same step through host buffers: pinned host inputs are copied in and the
-    step's results (out, dA, dW of both weights) copied back every step."""
+def run_e2e(F, sets, steps, warmup):
+    """Same step through host buffers: every step copies its inputs (A, W, dY
+    of both weights) in from pinned host memory and its results (out, dA, dW)
+    back to pinned host memory.  The copies run on their own streams and the
+    steps alternate between the given buffer sets (``sets``: ScoutStep objects
+    of the same shapes), so that step i's download, step i+1's compute and
+    step i+2's upload overlap, as a training loop with a prefetching loader
+    would; every step's transfers are inside the timed region, which ends when
+    the last download has landed (one copy stream per direction: spreading
+    the transfers over four streams each way measured slower)."""
     import torch
     host_in, host_out = [], []
-    for L in step.layers:
-        for k in ("a", "w", "dy"):
-            host_in.append((L[k], torch.empty(L[k].shape, dtype=L[k].dtype, pin_memory=True).copy_(L[k].cpu())))
-        for k in ("out", "da", "dw"):
-            host_out.append((L[k], torch.empty(L[k].shape, dtype=L[k].dtype, pin_memory=True)))
-    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
-    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
+    for st in sets:
+        hi, ho = [], []
+        for L in st.layers:
+            for k in ("a", "w", "dy"):
+                hi.append((L[k], torch.empty(L[k].shape, dtype=L[k].dtype, pin_memory=True).copy_(L[k].cpu())))
+            for k in ("out", "da", "dw"):
+                ho.append((L[k], torch.empty(L[k].shape, dtype=L[k].dtype, pin_memory=True)))
+        host_in.append(hi)
+        host_out.append(ho)
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in[0])
+    d2h = sum(h.numel() * h.element_size() for _, h in host_out[0])
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ns = len(sets)
+    ev_in = [torch.cuda.Event() for _ in range(ns)]
+    ev_comp = [torch.cuda.Event() for _ in range(ns)]
+    ev_out = [torch.cuda.Event() for _ in range(ns)]
 
-    def one():
-        for d, h in host_in:
-            d.copy_(h, non_blocking=True)
-        step.run()
-        for d, h in host_out:
-            h.copy_(d, non_blocking=True)
+    def one(i):
+        k = i % ns
+        with torch.cuda.stream(s_in):
+            if i >= ns:
+                s_in.wait_event(ev_comp[k])   # the set's previous step has read its inputs
+            for d, h in host_in[k]:
+                d.copy_(h, non_blocking=True)
+            ev_in[k].record(s_in)
+        comp.wait_event(ev_in[k])
+        if i >= ns:
+            comp.wait_event(ev_out[k])        # the set's previous results have been copied out
+        sets[k].run()
+        ev_comp[k].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[k])
+            for d, h in host_out[k]:
+                h.copy_(d, non_blocking=True)
+            ev_out[k].record(s_out)
 
-    for _ in range(warmup):
-        one()
+    for i in range(warmup):
+        one(i)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    for i in range(steps):
+        one(warmup + i)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     return dt, h2d, d2h
@@ -683,7 +712,11 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        dt, h2d, d2h = run_e2e(F, step, max(2, args.steps // 3), 1)
+        # a second buffer set of the same shapes lets transfers and compute
+        # of neighbouring steps overlap
+        step2 = ScoutStep(F, wl, dev, layers=args.layers, fused=not args.unfused)
+        dt, h2d, d2h = run_e2e(F, [step, step2], max(4, args.steps // 3), 2)
+        del step2
         e2e = {"value": flops * world / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
     cpu = None
