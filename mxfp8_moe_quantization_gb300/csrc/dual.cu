@@ -150,6 +150,14 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
   }
   const int lane = threadIdx.x & 31, half = lane >> 4, cl = lane & 15;
   const uint32_t nwarps = gridDim.x * (blockDim.x >> 5);
+  // Grouped layouts (B == 1): a warp's tiles come in increasing row order and
+  // every 32-row sub-tile lies inside one routing group (offsets are
+  // multiples of 32), so a forward-only cursor per table replaces the
+  // binary searches: the group of row r is the first whose end exceeds r.
+  int g0c = 0, g1c = 0;
+  auto advance = [](const GroupTable& gt, int E, int& g, int64_t r) {
+    while (g < E - 1 && gt.end[g] <= r) ++g;
+  };
   for (uint32_t t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.tiles; t += nwarps) {
     const uint32_t ct = t % a.n_ct;
     const uint32_t rest = t / a.n_ct;
@@ -175,20 +183,23 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
       // 128x4 layout (offset step 16) or are consecutive rows (step C/32) --
       // unless a routing group ends inside them (grouped layout only).
       int64_t s0_base = 0, s0_step = 0;
-      if ((cl & 3) == 0 && ok) {
-        s0_base = scale_offset(a.s0, &gt0, b, r, c >> 5, a.R, a.C >> 5);
-        if (a.s0.layout == FP8MOE_SCALES_ROWMAJOR) {
-          s0_step = a.C >> 5;
-        } else if (a.s0.layout == FP8MOE_NO_GROUPS) {
+      if (a.s0.layout == FP8MOE_GROUP_ROWS) {
+        // the cursor follows the sub-tile's first row; this half's group is
+        // at most a few steps further.  When rows r .. r + 15 lie in one
+        // routing group and start a 16-row half of the layout's 32-row group
+        // (always, for 32-multiple groups) their offsets step by 16; else
+        // each row's offset is computed on its own
+        advance(gt0, a.s0.E, g0c, rt * 32);
+        int g = g0c;
+        advance(gt0, a.s0.E, g, r);
+        const int64_t gs = g == 0 ? 0 : gt0.end[g - 1];
+        if (gt0.end[g] >= r + 16 && ((r - gs) & 15) == 0) {
+          s0_base = tile_off(gt0.pad[g] + (r - gs), c >> 5, a.s0.Cp);
           s0_step = 16;
-        } else {
-          // grouped rows: rows r .. r + 15 lie in one routing group and in
-          // one 32-row group of the layout (the group starts on a 16-row
-          // boundary)
-          const int g = find_group(gt0.end, a.s0.E, r);
-          const int64_t gs = g == 0 ? 0 : gt0.end[g - 1];
-          if (gt0.end[g] >= r + 16 && ((r - gs) & 15) == 0) s0_step = 16;
         }
+      } else if ((cl & 3) == 0 && ok) {
+        s0_base = scale_offset(a.s0, &gt0, b, r, c >> 5, a.R, a.C >> 5);
+        s0_step = a.s0.layout == FP8MOE_SCALES_ROWMAJOR ? (a.C >> 5) : 16;
       }
       uint8_t* q0p = a.q0 + (b * a.R + r) * a.C + c;
 #pragma unroll
@@ -247,16 +258,23 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
       // [C, R/32] scales (step R/32)
       const int64_t c = (int64_t)ct * 128 + cl * 8;
       const int nv = (int)min((uint32_t)a.nsub, a.n_rt - rt0);
+      const bool gcols = a.s1.layout == FP8MOE_GROUP_COLS;
+      if (gcols) advance(gt1, a.s1.E, g1c, (int64_t)rt0 * 32);
       if (half == 0 && c < a.C) {
-        const int64_t base = scale_offset(a.s1, &gt1, b, c, rt0, a.C, a.R >> 5);
+        int64_t base;
+        if (gcols) {
+          const int64_t gs = g1c == 0 ? 0 : gt1.end[g1c - 1];
+          base = tile_off(c, gt1.pad[g1c] + (rt0 - gs / 32), a.s1.Cp);
+        } else {
+          base = scale_offset(a.s1, &gt1, b, c, rt0, a.C, a.R >> 5);
+        }
         const bool rowmajor = a.s1.layout == FP8MOE_SCALES_ROWMAJOR;
         const int64_t st1 = rowmajor ? (a.R >> 5) : 16;
         // the band's row blocks are consecutive scale bytes of each column:
         // always in row-major; in a 128x4 tile while they stay inside one
         // 4-column group of it (and, grouped, inside one routing group)
         bool contiguous = rowmajor || (base & 3) + nv <= 4;
-        if (contiguous && a.s1.layout == FP8MOE_GROUP_COLS && nv > 1)
-          contiguous = find_group(gt1.end, a.s1.E, rt0 * 32) == find_group(gt1.end, a.s1.E, (rt0 + nv - 1) * 32);
+        if (contiguous && gcols && nv > 1) contiguous = gt1.end[g1c] >= (int64_t)(rt0 + nv) * 32;
         uint8_t* p0 = a.s1.p + base;
         if (contiguous && nv == 4 && ((uintptr_t)p0 & 3) == 0 && (st1 & 3) == 0) {
 #pragma unroll
