@@ -53,9 +53,9 @@ constexpr uint32_t TMEM_COLS = 512;
 // one's TMA store still reads.
 template <int STAGES, int NSTG>
 struct Layout {
-  // full, empty, cs_full, cs_empty per stage; pfull[2], pempty[2]
+  // full, empty, cs_full, cs_empty per stage; pfull[2], pempty[2], drain
   static constexpr int bars = STAGES * STAGE_BYTES;
-  static constexpr int misc = bars + (4 * STAGES + 4) * 8;          // tmem base, abort flag, total tiles
+  static constexpr int misc = bars + (4 * STAGES + 6) * 8;          // tmem base, abort flag, total tiles
   static constexpr int colsc = misc + 16;                           // wgrad column scales [STAGES][BN]
   static constexpr int tiles_prefix = colsc + STAGES * BN * 4;
   static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* cs_empty = cs_full + STAGES;
   uint64_t* pfull = cs_empty + STAGES;
   uint64_t* pempty = pfull + 2;
+  uint64_t* drain = pempty + 2;  // the MMA thread's own work, awaited before TMEM is released
   uint32_t* tmem_holder = (uint32_t*)(smem + Layout::misc);
   volatile int* abort_flag = (volatile int*)(smem + Layout::misc + 4);
   int* total_s = (int*)(smem + Layout::misc + 8);
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&pfull[b], 1);
       mbar_init(&pempty[b], EPI_THREADS / 32);
     }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -233,6 +235,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ======================= TMA producer =======================
     int stage = 0;
     uint32_t phase = 0;
+    int filled[STAGES], cs_filled[STAGES];  // phase of each slot's last fill, -1: never
+    for (int s2 = 0; s2 < STAGES; ++s2) filled[s2] = cs_filled[s2] = -1;
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
       const BwTile tl = bw_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
       for (int ks = 0; ks < tl.nk; ++ks) {
@@ -241,6 +245,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           *abort_flag = 1;
           break;
         }
+        filled[stage] = (int)phase;
         uint8_t* sa = smem + stage * STAGE_BYTES;
         mbar_expect_tx(&full[stage], STAGE_BYTES);
         const int x = (int)(tl.x0 + (int64_t)ks * BK);
@@ -254,6 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           const uint32_t nbytes = (uint32_t)(tl.ncols * 4);
+          cs_filled[stage] = (int)phase;
           mbar_expect_tx(&cs_full[stage], nbytes);
           bulk_load(colsc + stage * BN, (const float*)g.b_scale + (tl.blk0 + ks) * g.cols + tl.col0, nbytes,
                     &cs_full[stage]);
@@ -277,6 +283,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (++stage == STAGES) {
         stage = 0;
         phase ^= 1;
+      }
+    }
+    // after a timeout: wait (bounded) until the copies in flight have landed
+    if (*abort_flag) {
+      for (int s2 = 0; s2 < STAGES; ++s2) {
+        if (filled[s2] >= 0) (void)mbar_wait(&full[s2], (uint32_t)filled[s2], nullptr);
+        if (WGRAD && cs_filled[s2] >= 0) (void)mbar_wait(&cs_full[s2], (uint32_t)cs_filled[s2], nullptr);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -321,6 +334,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
     }
+    // every MMA this thread issued has completed before TMEM is released
+    tc_commit(drain);
+    if (!mbar_wait(drain, 0, nullptr)) set_status(g.status, FP8MOE_ERR_TIMEOUT);
   } else if (warp >= 2) {
     // ======================= epilogue: promotion and stores =======================
     const int quarter = warp & 3;

@@ -68,8 +68,8 @@ struct SmemLayout {
   static constexpr int b = a + STAGES * A_STAGE_BYTES;
   static constexpr int sfa = b + STAGES * B_STAGE_BYTES;
   static constexpr int sfb = sfa + STAGES * SFA_STAGE_BYTES;
-  static constexpr int bars = sfb + STAGES * SFB_STAGE_BYTES;   // 3*STAGES + 2 mbarriers
-  static constexpr int misc = bars + (3 * STAGES + 2) * 8;      // tmem addr, abort, counts
+  static constexpr int bars = sfb + STAGES * SFB_STAGE_BYTES;   // 3*STAGES + 4 mbarriers
+  static constexpr int misc = bars + (3 * STAGES + 4) * 8;      // tmem addr, abort, counts
   static constexpr int colscale = misc + 64;                    // 256 floats
   static constexpr int tiles_prefix = colscale + BN * 4;        // MAXG + 1 ints
   static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
@@ -220,6 +220,7 @@ struct KParams {
   int n_units;        // column units: n-tiles per cluster pass (quad mode: 2 n-tiles)
   int m_tiles_w;      // wgrad: tiles along the output rows
   int tma_out;        // output stored by TMA (tmOut valid); else by thread stores
+  int stall_test;     // test hook (FP8MOE_TEST_STALL=1): one accumulator is never handed over
 };
 
 // Per-tile geometry, recomputed identically by every role.
@@ -316,6 +317,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* tmem_full = empty + STAGES;
   uint64_t* tmem_empty = tmem_full + 1;
   uint64_t* sf_full = tmem_empty + 1;  // per stage: scales are in TMEM (scale-copier commits)
+  // completion of the MMA / scale-copier thread's own tcgen05 work, awaited
+  // before the CTA releases TMEM (matters on the timeout path)
+  uint64_t* drain_mma = sf_full + STAGES;
+  uint64_t* drain_cp = drain_mma + 1;
   uint32_t* tmem_base_holder = (uint32_t*)(smem + L::misc);
   volatile int* abort_flag = (volatile int*)(smem + L::misc + 4);
   int* total_tiles_s = (int*)(smem + L::misc + 8);
@@ -340,6 +345,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&empty[s], TWO ? (QUAD ? 2 : 1) : 2);
     }
     for (int s = 0; s < STAGES; ++s) mbar_init(&sf_full[s], 1);
+    mbar_init(drain_mma, 1);
+    mbar_init(drain_cp, 1);
     mbar_init(tmem_full, 1);
     // 2-CTA: the leader's accumulator is free once both CTAs' epilogues drained
     mbar_init(tmem_empty, TWO ? 8 : 4);
@@ -440,6 +447,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     int stage = 0;
     uint32_t phase = 0;
+    int filled[STAGES];  // phase of each stage's last fill, -1: never filled
+    for (int s = 0; s < STAGES; ++s) filled[s] = -1;
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
       const Tile tl = get_tile<WGRAD, NQ>(p, tiles_prefix, blk_prefix, t, rank, pp);
       for (int ks = 0; ks < tl.nk; ++ks) {
@@ -448,6 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           *abort_flag = 1;
           break;
         }
+        filled[stage] = (int)phase;
         // 1-CTA: own A + both halves of B (one of them multicast by the peer);
         // 2-CTA: own A + own half of B
         uint32_t bytes = A_STAGE_BYTES + (TWO ? B_STAGE_BYTES : B_STAGE_BYTES);
@@ -521,6 +531,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         stage = 0;
         phase ^= 1;
       }
+    }
+    // after a timeout the stages may not have been consumed: wait (bounded)
+    // until the copies in flight have landed.  A full barrier completes when
+    // every byte of its fill arrived, whoever consumes it; in a 2-CTA pair
+    // the leader's barriers count the bytes of both CTAs.
+    if (*abort_flag && (!TWO || rank == 0)) {
+      for (int s = 0; s < STAGES; ++s)
+        if (filled[s] >= 0) (void)mbar_wait(&full[s], (uint32_t)filled[s], nullptr);
     }
   } else if (warp == 1 && lane == 0 && TWO && rank == 1) {
     // 2-CTA peer: the leader issues every MMA of the pair; nothing to do here
@@ -613,12 +631,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (!ok) break;
+      // test hook: the first tile of the first cluster never hands over its
+      // accumulator, so the epilogue's bounded wait runs out
+      if (p.stall_test && t == pair && pair == 0) continue;
       if constexpr (TWO) {
         tc_commit_pair<true>(tmem_full, pair_mask);
       } else {
         tc_commit(tmem_full);
       }
     }
+    // every MMA this thread issued has completed before TMEM is released
+    tc_commit_local<TWO>(drain_mma);
+    if (!mbar_wait(drain_mma, 0, nullptr)) set_status(g.status, FP8MOE_ERR_TIMEOUT);
   } else if (warp == 6) {
     // ======================= scale copier =======================
     // Stage s's scale columns are free once the MMAs of its previous use
@@ -654,6 +678,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
       }
+      // every scale copy this thread issued has completed
+      tc_commit_local<TWO>(drain_cp);
+      if (!mbar_wait(drain_cp, 0, nullptr)) set_status(g.status, FP8MOE_ERR_TIMEOUT);
     }
   } else if (warp >= 2) {
     // ======================= epilogue =======================
@@ -880,6 +907,11 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   const bool quad = two && want_quad;
   KParams p;
   p.g = g;
+  // fault-injection hook for the tests of the timeout path, read per launch
+  {
+    const char* v = getenv("FP8MOE_TEST_STALL");
+    p.stall_test = v && v[0] == '1';
+  }
   p.n_tiles = (int)((g.cols + BN - 1) / BN);
   p.n_units = quad ? (p.n_tiles + 1) / 2 : p.n_tiles;
   p.m_tiles_w = (int)((g.rows + BM - 1) / BM);

@@ -251,3 +251,23 @@ def test_pair_mode_variants(env):
                         os.path.abspath(__file__), "-k", "not pair_mode_variants"],
                        cwd=root, env=dict(os.environ, **env), capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+def test_pipeline_wait_timeout_sets_status(F, monkeypatch):
+    """Fault injection without a GPU fault: with the FP8MOE_TEST_STALL hook the
+    first cluster never hands its first accumulator to the epilogue, whose
+    bounded wait (2 s) runs out.  The kernel reports FP8MOE_ERR_TIMEOUT; every
+    CTA waits for its own copies and MMAs before releasing TMEM, so the
+    context stays usable and the next GEMM is exact again."""
+    offs = W.offsets_from_sizes([64, 0, 352, 32, 160])
+    a = _bf16((608, 256), 91)
+    w = _bf16((5, 512, 256), 92, 0.05)
+    (qa, sa, qw, sw), ref, bound = mx_fwd_case(a, w, offs)
+    d_offs = _d(offs)
+    monkeypatch.setenv("FP8MOE_TEST_STALL", "1")
+    F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, d_offs)
+    assert F.fp8moe_get_device_status() == 6          # FP8MOE_ERR_TIMEOUT
+    monkeypatch.delenv("FP8MOE_TEST_STALL")
+    out = F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, d_offs)
+    assert F.fp8moe_get_device_status() == 0
+    check(out, ref, bound, "fwd after a timed-out launch")
