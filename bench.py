@@ -41,8 +41,8 @@ METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)
 # from the ncu capture summarised in profiles/k_grouped_mm_scout.md.  It is
 # reported only while the kernel source is the one that was captured.
 GEMM_TRAFFIC = {"source": "mxfp8_moe_quantization_gb300/csrc/grouped_mm.cu",
-                "sha256": "c8c5f80c4714b0a9d43f8400cfb810f6a1f73a33023173519ecb6882dcda08c2",
-                "bytes_per_launch": (1029.789e6 + 1072.055e6 + 1563.509e6) / 3}
+                "sha256": "547c6b0dc0b06e00eea7d43a215ce467c060a82952e29dd59eeb02341b4c512b",
+                "bytes_per_launch": (1030.651e6 + 1077.764e6 + 1563.850e6) / 3}
 
 
 def gemm_traffic():
