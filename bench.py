@@ -55,6 +55,23 @@ def gemm_traffic():
     return GEMM_TRAFFIC["bytes_per_launch"] if h == GEMM_TRAFFIC["sha256"] else None
 
 
+def max_over_ranks(value, pg=None, device="cpu"):
+    """The largest of the ranks' values (a job takes as long as its slowest
+    rank); the value itself on one rank."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank, world, ms_step):
+    """Whole-job throughput: every rank runs the same step on its own batch
+    (weak scaling), so the job does world x the flops of one rank per step."""
+    return flops_per_rank * world / (ms_step * 1e-3) / 1e12
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -691,11 +708,7 @@ def main():
         torch.cuda.synchronize()
     if pg:
         pg.barrier()
-    ms_total = t_start.elapsed_time(t_end)
-    if pg:
-        t = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), pg, dev)
     ms_step = ms_total / args.steps
     gemm_ms = sum(s.elapsed_time(e) for s, e in ev["gemm"]) / args.steps
     quant_ms = sum(s.elapsed_time(e) for s, e in ev["quant"]) / args.steps
@@ -708,7 +721,7 @@ def main():
     fp8_peak = 2.0 * peaks["bf16_tflops"]          # nominal fp8:bf16 dense ratio 4.5 / 2.25
     gemm_launch_ms = gemm_ms / n_gemm
     achieved = flops / n_gemm / (gemm_launch_ms * 1e-3) / 1e12
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    value = job_tflops(flops, world, ms_step)
 
     e2e = None
     if not args.no_e2e:
@@ -717,7 +730,8 @@ def main():
         step2 = ScoutStep(F, wl, dev, layers=args.layers, fused=not args.unfused)
         dt, h2d, d2h = run_e2e(F, [step, step2], max(4, args.steps // 3), 2)
         del step2
-        e2e = {"value": flops * world / dt / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        dt = max_over_ranks(dt, pg, dev)
+        e2e = {"value": job_tflops(flops, world, dt * 1e3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
