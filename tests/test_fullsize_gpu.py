@@ -201,3 +201,100 @@ def test_rowwise_fullsize(F, name):
         dyc = OF.decode(dq[0]) * di[0][:, None].astype(np.float64)
         ac = OF.decode(aq[0]) * ai[0][:, None].astype(np.float64)
         _check_vals(got, dyc @ ac.T, np.abs(dyc) @ np.abs(ac).T, f"{name} wgrad e={e}")
+
+
+def test_blockwise_fullsize(F):
+    """Blockwise recipe on the Llama4-Scout layer (W1 [16, 8192, 5120], 16,640
+    routed rows): the GPU quantizes every operand and runs the three GEMMs;
+    the oracle recomputes sampled row tiles, weight tiles, token tiles and
+    sampled outputs from the bf16 inputs alone."""
+    from oracle import blockwise as OB
+    wl = W.get_workload("scout")
+    rng = np.random.default_rng(13)
+    M, E, N, K = wl.M, wl.E, wl.N, wl.K
+    offs_np = wl.offs()
+    offs = torch.from_numpy(offs_np).to(DEV)
+    a = W.make_activations(wl, "A", device=DEV)
+    dy = W.make_activations(wl, "dY", device=DEV)
+    w = W.make_weights(wl, "W1", device=DEV)
+    qa, sa = F.fp8moe_quantize_blockwise_rows(a)
+    qw, qwt, sw = F.fp8moe_quantize_blockwise_weight(w)
+    qdy, sdy = F.fp8moe_quantize_blockwise_rows(dy)
+    qdyt, sdyt = F.fp8moe_quantize_blockwise_tokens(dy, offs)
+    qat, sat = F.fp8moe_quantize_blockwise_tokens(a, offs)
+    out = F.fp8moe_scaled_grouped_mm_fwd(F.BLOCKWISE, qa, sa, qw, sw, offs)
+    da = F.fp8moe_scaled_grouped_mm_dgrad(F.BLOCKWISE, qdy, sdy, qwt, sw, offs)
+    dw = F.fp8moe_scaled_grouped_mm_wgrad(F.BLOCKWISE, qdyt, sdyt, qat, sat, offs, M)
+    torch.cuda.synchronize()
+    assert F.fp8moe_get_device_status() == 0
+
+    rows = _sample_rows(offs_np, rng, 1)
+    starts, ends = OQ.group_bounds(offs_np)
+    grp = np.searchsorted(ends, rows, side="right")
+    rt = torch.from_numpy(rows).to(DEV)
+    # row tiles of the sampled rows: codes and scales
+    rq, ri = OB.quantize_blockwise_rows(_np(a[rt]))
+    assert np.array_equal(qa[rt].cpu().numpy(), rq) and np.array_equal(sa[:, rt].cpu().numpy(), ri)
+    a_deq = OB.dequant_rows(rq, ri)
+    # weight slabs (128 output rows of one expert, every k tile) for sampled columns
+    ncols = np.array(sorted(set(rng.integers(0, N, size=6).tolist() + [N - 1])))
+    w_deq = {}
+    for e in np.unique(grp):
+        for nb in sorted(set(int(n) // 128 for n in ncols)):
+            slab = _np(w[int(e), nb * 128:(nb + 1) * 128])[None]
+            q, s = OB.quantize_blockwise_weight(slab)
+            assert np.array_equal(qw[int(e), nb * 128:(nb + 1) * 128].cpu().numpy(), q[0])
+            assert np.array_equal(sw[int(e), nb].cpu().numpy(), s[0, 0])
+            w_deq[(int(e), nb)] = OB.dequant_weight(q, s)[0]
+    got = _np(out[rt][:, torch.from_numpy(ncols).to(DEV)])
+    ref = np.zeros_like(got, dtype=np.float64)
+    bnd = np.zeros_like(ref)
+    for i, (r, e) in enumerate(zip(rows, grp)):
+        wr = np.stack([w_deq[(int(e), int(n) // 128)][int(n) % 128] for n in ncols])
+        ref[i] = wr @ a_deq[i]
+        bnd[i] = np.abs(wr) @ np.abs(a_deq[i])
+    _check_vals(got, ref, bnd, "blockwise fwd")
+
+    # dgrad: dY row tiles along N against W^T (the same 128x128 tiles)
+    kcols = np.array(sorted(set(rng.integers(0, K, size=4).tolist())))
+    dq, di = OB.quantize_blockwise_rows(_np(dy[rt]))
+    assert np.array_equal(qdy[rt].cpu().numpy(), dq) and np.array_equal(sdy[:, rt].cpu().numpy(), di)
+    dy_deq = OB.dequant_rows(dq, di)
+    got = _np(da[rt][:, torch.from_numpy(kcols).to(DEV)])
+    ref = np.zeros_like(got, dtype=np.float64)
+    bnd = np.zeros_like(ref)
+    for e in np.unique(grp):
+        sel = grp == e
+        cols = []
+        for k in kcols:
+            kb = int(k) // 128
+            slab = _np(w[int(e), :, kb * 128:(kb + 1) * 128])[None]       # [1, N, 128]
+            q, s = OB.quantize_blockwise_weight(slab)
+            assert np.array_equal(qwt[int(e), int(k)].cpu().numpy(), q[0][:, int(k) % 128])
+            cols.append(OB.dequant_weight(q, s)[0][:, int(k) % 128])       # W[e, :, k] over N
+        wt = np.stack(cols)                                               # [k, N]
+        ref[sel] = dy_deq[sel] @ wt.T
+        bnd[sel] = np.abs(dy_deq[sel]) @ np.abs(wt).T
+    _check_vals(got, ref, bnd, "blockwise dgrad")
+
+    # wgrad: token tiles of sampled columns (codes and scales), then a few
+    # (n, k) of every expert
+    nn = rng.integers(0, N, size=4)
+    kk = rng.integers(0, K, size=4)
+    nt, kt = torch.from_numpy(nn).to(DEV), torch.from_numpy(kk).to(DEV)
+    tq_dy, ts_dy = OB.quantize_blockwise_tokens(_np(dy[:, nt]), offs_np)
+    tq_a, ts_a = OB.quantize_blockwise_tokens(_np(a[:, kt]), offs_np)
+    nblk = len(ts_dy)
+    assert np.array_equal(qdyt[nt].cpu().numpy(), tq_dy) and np.array_equal(qat[kt].cpu().numpy(), tq_a)
+    assert np.array_equal(sdyt[:nblk][:, nt].cpu().numpy(), ts_dy)
+    assert np.array_equal(sat[:nblk][:, kt].cpu().numpy(), ts_a)
+    dyt = OB.dequant_tokens(tq_dy, ts_dy, offs_np)      # [4, M]
+    at = OB.dequant_tokens(tq_a, ts_a, offs_np)
+    for e in range(E):
+        s0, s1 = int(starts[e]), int(ends[e])
+        got = _np(dw[e][nt][:, kt])
+        if s1 == s0:
+            assert np.all(got == 0)
+            continue
+        ref = dyt[:, s0:s1] @ at[:, s0:s1].T
+        _check_vals(got, ref, np.abs(dyt[:, s0:s1]) @ np.abs(at[:, s0:s1]).T, f"blockwise wgrad e={e}")
