@@ -261,10 +261,14 @@ class ScoutStep:
                                                                  L["sat_sw"], offs, self.M, out=L["dw"]))
 
 
-def run_e2e(F, sets, steps, warmup):
-    """Same step through host buffers: every step copies its inputs (A, W, dY
-    of both weights) in from pinned host memory and its results (out, dA, dW)
-    back to pinned host memory.  The copies run on their own streams and the
+def run_e2e(F, sets, steps, warmup, stream_weights=False):
+    """Same step through host buffers: every step copies its per-step inputs
+    (the routed activations A and the output gradients dY of both weights)
+    in from pinned host memory and its results (the layer outputs and the
+    input gradients, out and dA) back to pinned host memory; the expert
+    weights and their gradients stay on the device, as model state does in
+    training.  ``stream_weights`` also moves W in and dW out every step (a
+    weight-streaming setup).  The copies run on their own streams and the
     steps alternate between the given buffer sets (``sets``: ScoutStep objects
     of the same shapes), so that step i's download, step i+1's compute and
     step i+2's upload overlap, as a training loop with a prefetching loader
@@ -276,9 +280,9 @@ def run_e2e(F, sets, steps, warmup):
     for st in sets:
         hi, ho = [], []
         for L in st.layers:
-            for k in ("a", "w", "dy"):
+            for k in ("a", "w", "dy") if stream_weights else ("a", "dy"):
                 hi.append((L[k], torch.empty(L[k].shape, dtype=L[k].dtype, pin_memory=True).copy_(L[k].cpu())))
-            for k in ("out", "da", "dw"):
+            for k in ("out", "da", "dw") if stream_weights else ("out", "da"):
                 ho.append((L[k], torch.empty(L[k].shape, dtype=L[k].dtype, pin_memory=True)))
         host_in.append(hi)
         host_out.append(ho)
@@ -723,16 +727,22 @@ def main():
     achieved = flops / n_gemm / (gemm_launch_ms * 1e-3) / 1e12
     value = job_tflops(flops, world, ms_step)
 
-    e2e = None
+    e2e = e2e_ws = None
     if not args.no_e2e:
         # a second buffer set of the same shapes lets transfers and compute
         # of neighbouring steps overlap
         step2 = ScoutStep(F, wl, dev, layers=args.layers, fused=not args.unfused)
         dt, h2d, d2h = run_e2e(F, [step, step2], max(4, args.steps // 3), 2)
-        del step2
         dt = max_over_ranks(dt, pg, dev)
         e2e = {"value": job_tflops(flops, world, dt * 1e3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
+               "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
+               "moves": "A, dY in; out, dA back (weights and weight gradients resident)"}
+        dt, h2d, d2h = run_e2e(F, [step, step2], max(4, args.steps // 6), 2, stream_weights=True)
+        del step2
+        dt = max_over_ranks(dt, pg, dev)
+        e2e_ws = {"value": job_tflops(flops, world, dt * 1e3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
+                  "moves": "A, W, dY in; out, dA, dW back"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         q_rate, g_rate, sample = cpu_baseline(wl)
@@ -760,6 +770,7 @@ def main():
                              f"{peak_kind}: 2 x bf16_tflops (nominal fp8/bf16 dense ratio)"},
             "clocks": clk.summary(),
             "e2e": e2e,
+            "e2e_weights_streamed": e2e_ws,
             "cpu_baseline": cpu,
             "gpu_launches": step.launches_per_step * args.steps,
         }))
