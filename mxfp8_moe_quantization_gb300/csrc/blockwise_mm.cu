@@ -9,19 +9,30 @@
 // core cannot accumulate across k-blocks: each k-block's product goes to its
 // own TMEM partial and is promoted into an fp32 accumulator held in
 // registers, scaled by (row scale x column scale) of that k-block.
-//  * persistent kernel, one 320-thread CTA per SM, output tiles 128 x 256;
-//  * warp 0: TMA producer (A 128 x 128 and B 256 x 128 byte tiles, 128-byte
-//    swizzle, 4-stage ring); warp 1: TMEM allocator and MMA issuer
-//    (kind::f8f6f4, M = 128, N = 256, four K = 32 steps per k-block);
-//  * two TMEM partials of 256 columns: the MMAs of k-block i + 1 run while
-//    the epilogue promotes k-block i;
-//  * warps 2-9: epilogue; warp w reads TMEM lanes 32 (w % 4) .. +31 and
-//    columns 128 ((w - 2) / 4) .. +127, holds 128 fp32 accumulators per
-//    thread (half of one output row) and writes bf16 at the end through a
-//    2 KB staging tile per warp (32 rows x 32 columns, 64-byte swizzle)
-//    handed to TMA stores, so the LSU is not the bottleneck.  Ten warps
-//    leave 168 registers a thread (each SM sub-partition holds 16K registers
-//    and three of the warps); the promotion reads TMEM 16 columns at a time;
+//  * persistent kernel, one CTA per SM; warp 0: TMA producer (A 128 x 128
+//    and B BN x 128 byte tiles, 128-byte swizzle, 4-stage ring); warp 1:
+//    TMEM allocator and MMA issuer (kind::f8f6f4, M = 128, N = BN, four
+//    K = 32 steps per k-block); the group offsets and per-group tile counts
+//    are copied to shared memory once;
+//  * two TMEM partials (columns 0 and 256): the MMAs of k-block i + 1 run
+//    while the epilogue promotes k-block i;
+//  * the other warps: epilogue; warp w reads TMEM lanes 32 (w % 4) .. +31
+//    and one column slice of the tile, holds its fp32 accumulators (part of
+//    one output row per thread) and writes bf16 at the end through 2 KB
+//    staging tiles (32 rows x 32 columns, 64-byte swizzle) handed to TMA
+//    stores, so the LSU is not the bottleneck;
+//  * forward / dgrad (tiles of K / 128 k-blocks, one scalar scale per
+//    k-block and warp): BN = 256, eight epilogue warps of 128 columns, ten
+//    warps in all, so 168 registers a thread (each SM sub-partition holds
+//    16K registers and three of the warps).  Here the operand feed is the
+//    bound: a 192-column tile moves more bytes per flop and ran 12% slower;
+//  * wgrad (tiles of ~8 k-blocks, a scale per row and per column of every
+//    k-block, so twice the promotion arithmetic): BN = 192, twelve epilogue
+//    warps of 64 columns, three per sub-partition, so that one warp's TMEM
+//    load latency hides behind the others' arithmetic; fourteen warps allow
+//    128 registers a thread.  The N = 192 MMA takes as long as an N = 256
+//    one (75% of the per-clock tensor peak at most); with 256 columns the
+//    promotion was the bound, 15% slower;
 //  * wgrad's per-column scales change with every k-block: the producer
 //    bulk-copies each k-block's 256 of them into a ring slot that the
 //    epilogue warps release;
@@ -37,37 +48,39 @@
 namespace fp8moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int THREADS = 320;
-constexpr int EPI_THREADS = 256;
-constexpr int EPI_COLS = 128;  // columns per epilogue thread
+constexpr int BM = 128, BK = 128;
+constexpr int PSTRIDE = 256;   // TMEM columns between the two partials
 constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MAXG = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 
-// Forward / dgrad: 4 stages and one staging tile per epilogue warp.  Wgrad
-// (tiles of ~8 k-blocks, so the stores recur 5x as often): 3 stages and two
-// staging tiles per warp, so that a slice is written while the previous
-// one's TMA store still reads.
-template <int STAGES, int NSTG>
-struct Layout {
-  // full, empty, cs_full, cs_empty per stage; pfull[2], pempty[2], drain
-  static constexpr int bars = STAGES * STAGE_BYTES;
-  static constexpr int misc = bars + (4 * STAGES + 6) * 8;          // tmem base, abort flag, total tiles
-  static constexpr int colsc = misc + 16;                           // wgrad column scales [STAGES][BN]
-  static constexpr int tiles_prefix = colsc + STAGES * BN * 4;
-  static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
-  static constexpr int stg = (blk_prefix + (MAXG + 1) * 4 + 1023) / 1024 * 1024;  // [8 warps][2 KB]
-  static constexpr int total = stg + (EPI_THREADS / 32) * 2048 * NSTG;
-};
+// Tile shape, warp roles and shared-memory layout of one mode.  Wgrad keeps
+// two staging tiles per warp, so that a slice is written while the previous
+// one's TMA store still reads (its stores recur 5x as often as forward's).
 template <int MODE>
 struct Cfg {
-  static constexpr int STAGES = MODE == GEMM_WGRAD ? 3 : 4;
-  static constexpr int NSTG = MODE == GEMM_WGRAD ? 2 : 1;
-  using L = Layout<STAGES, NSTG>;
-  static constexpr int SMEM_BYTES = L::total + 1024;
+  static constexpr bool WG = MODE == GEMM_WGRAD;
+  static constexpr int BN = WG ? 192 : 256;
+  static constexpr int EPI_WARPS = WG ? 12 : 8;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // columns per epilogue thread
+  static constexpr int LDW = WG ? 32 : 16;              // TMEM columns per load
+  static constexpr int STAGES = 4;
+  static constexpr int NSTG = WG ? 2 : 1;
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // full, empty, cs_full, cs_empty per stage; pfull[2], pempty[2], drain
+  static constexpr int bars = STAGES * STAGE_BYTES;
+  static constexpr int misc = bars + (4 * STAGES + 6) * 8;  // tmem base, abort flag, total tiles
+  static constexpr int colsc = misc + 16;                   // wgrad column scales [STAGES][BN]
+  static constexpr int offs = colsc + STAGES * BN * 4;      // group ends [MAXG]
+  static constexpr int tiles_prefix = offs + MAXG * 4;
+  static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
+  static constexpr int stg = (blk_prefix + (MAXG + 1) * 4 + 1023) / 1024 * 1024;  // [warps][NSTG][2 KB]
+  static constexpr int total = stg + EPI_WARPS * 2048 * NSTG;
+  static constexpr int SMEM_BYTES = total + 1024;
+  static_assert(EPI_COLS % LDW == 0 && EPI_COLS % 64 == 0, "epilogue column split");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 struct BwParams {
@@ -86,8 +99,10 @@ struct BwTile {
   int64_t blk0;          // wgrad: first token block of the group
 };
 
-template <bool WGRAD>
-FP8MOE_DEV BwTile bw_tile(const BwParams& p, const int* tiles_prefix, const int* blk_prefix, int t) {
+template <int MODE>
+FP8MOE_DEV BwTile bw_tile(const BwParams& p, const int* offs, const int* tiles_prefix, const int* blk_prefix, int t) {
+  constexpr bool WGRAD = MODE == GEMM_WGRAD;
+  constexpr int BN = Cfg<MODE>::BN;
   const GemmArgs& g = p.g;
   int lo = 0, hi = g.E - 1, e = 0;
   while (lo <= hi) {
@@ -100,8 +115,8 @@ FP8MOE_DEV BwTile bw_tile(const BwParams& p, const int* tiles_prefix, const int*
     }
   }
   const int local = t - tiles_prefix[e];
-  const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
-  const int64_t ge = g.offs[e];
+  const int64_t gs = e == 0 ? 0 : offs[e - 1];
+  const int64_t ge = offs[e];
   BwTile tl;
   tl.e = e;
   if (!WGRAD) {
@@ -129,28 +144,30 @@ FP8MOE_DEV BwTile bw_tile(const BwParams& p, const int* tiles_prefix, const int*
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
     k_blockwise_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmOut, BwParams p) {
-  constexpr bool WGRAD = MODE == GEMM_WGRAD;
-  constexpr int STAGES = Cfg<MODE>::STAGES;
-  constexpr int NSTG = Cfg<MODE>::NSTG;
-  using Layout = typename Cfg<MODE>::L;
+  using C = Cfg<MODE>;
+  constexpr bool WGRAD = C::WG;
+  constexpr int STAGES = C::STAGES, NSTG = C::NSTG, BN = C::BN, THREADS = C::THREADS;
+  constexpr int EPI_WARPS = C::EPI_WARPS, EPI_COLS = C::EPI_COLS, LDW = C::LDW;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = (uint64_t*)(smem + Layout::bars);
+  uint64_t* full = (uint64_t*)(smem + C::bars);
   uint64_t* empty = full + STAGES;
   uint64_t* cs_full = empty + STAGES;
   uint64_t* cs_empty = cs_full + STAGES;
   uint64_t* pfull = cs_empty + STAGES;
   uint64_t* pempty = pfull + 2;
   uint64_t* drain = pempty + 2;  // the MMA thread's own work, awaited before TMEM is released
-  uint32_t* tmem_holder = (uint32_t*)(smem + Layout::misc);
-  volatile int* abort_flag = (volatile int*)(smem + Layout::misc + 4);
-  int* total_s = (int*)(smem + Layout::misc + 8);
-  float* colsc = (float*)(smem + Layout::colsc);
-  int* tiles_prefix = (int*)(smem + Layout::tiles_prefix);
-  int* blk_prefix = (int*)(smem + Layout::blk_prefix);
+  uint32_t* tmem_holder = (uint32_t*)(smem + C::misc);
+  volatile int* abort_flag = (volatile int*)(smem + C::misc + 4);
+  int* total_s = (int*)(smem + C::misc + 8);
+  float* colsc = (float*)(smem + C::colsc);
+  int* offs_s = (int*)(smem + C::offs);
+  int* tiles_prefix = (int*)(smem + C::tiles_prefix);
+  int* blk_prefix = (int*)(smem + C::blk_prefix);
   const GemmArgs& g = p.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -159,11 +176,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&cs_full[s], 1);
-      mbar_init(&cs_empty[s], EPI_THREADS / 32);
+      mbar_init(&cs_empty[s], EPI_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&pfull[b], 1);
-      mbar_init(&pempty[b], EPI_THREADS / 32);
+      mbar_init(&pempty[b], EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -178,7 +195,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   // per-group tile and token-block counts, then one warp scans them and
   // validates the offsets
   for (int e = threadIdx.x; e < g.E; e += THREADS) {
-    const int64_t sz = (int64_t)g.offs[e] - (e == 0 ? 0 : g.offs[e - 1]);
+    const int32_t end = g.offs[e];
+    offs_s[e] = end;
+    const int64_t sz = (int64_t)end - (e == 0 ? 0 : g.offs[e - 1]);
     int nt, nb = 0;
     if (!WGRAD) {
       nt = (int)((sz + BM - 1) / BM) * p.n_tiles;
@@ -238,7 +257,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int filled[STAGES], cs_filled[STAGES];  // phase of each slot's last fill, -1: never
     for (int s2 = 0; s2 < STAGES; ++s2) filled[s2] = cs_filled[s2] = -1;
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-      const BwTile tl = bw_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+      const BwTile tl = bw_tile<MODE>(p, offs_s, tiles_prefix, blk_prefix, t);
       for (int ks = 0; ks < tl.nk; ++ks) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
           set_status(g.status, FP8MOE_ERR_TIMEOUT);
@@ -298,7 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t phase = 0;
     uint32_t np = 0;  // partials issued
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-      const BwTile tl = bw_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
+      const BwTile tl = bw_tile<MODE>(p, offs_s, tiles_prefix, blk_prefix, t);
       bool ok = true;
       for (int ks = 0; ks < tl.nk; ++ks) {
         const uint32_t buf = np & 1, use = np >> 1;
@@ -311,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
         const uint64_t adesc = sdesc_sw128(a_addr), bdesc = sdesc_sw128(a_addr + A_BYTES);
-        const uint32_t d = tmem_base + buf * BN;
+        const uint32_t d = tmem_base + buf * PSTRIDE;
         const int64_t rem = tl.kvalid - (int64_t)ks * BK;
         if (rem >= BK) {
 #pragma unroll
@@ -340,40 +359,50 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp >= 2) {
     // ======================= epilogue: promotion and stores =======================
     const int quarter = warp & 3;
-    const int part = (warp - 2) >> 2;  // 128-column half of the tile
+    const int part = (warp - 2) >> 2;  // column slice of the tile
     const int lrow = quarter * 32 + lane;
     const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + part * EPI_COLS;
-    uint8_t* stg0 = smem + Layout::stg + (warp - 2) * 2048 * NSTG;
+    uint8_t* stg0 = smem + C::stg + (warp - 2) * 2048 * NSTG;
     int slice = 0;  // slices staged by this warp (alternating tiles when NSTG == 2)
     const float* sa_p = (const float*)g.a_scale;
     const float* sb_p = (const float*)g.b_scale;
     uint32_t np = 0;
     for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-      const BwTile tl = bw_tile<WGRAD>(p, tiles_prefix, blk_prefix, t);
-      const bool row_ok = lrow < tl.rows;
       const int64_t c0 = part * EPI_COLS;  // first column of this thread inside the tile
-      uint16_t* orow = WGRAD ? g.out + ((int64_t)tl.e * g.rows + tl.row0 + lrow) * g.cols + tl.col0
-                             : g.out + (tl.row0 + lrow) * g.cols + tl.col0;
-      if (tl.nk == 0) {
-        // an empty group in wgrad: dW[e] = 0
-        if (row_ok)
-          for (int c = (int)c0; c < c0 + EPI_COLS && c < tl.ncols; c += 8)
-            *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
-        continue;
+      // only the scale pointers and the k-block count live through the
+      // promotion loop; the tile's geometry is recomputed for the stores
+      int nk;
+      const float* rsp;  // row scale of k-block 0 (nullptr: row past the tile)
+      const float* csp;  // forward / dgrad: column scale of k-block 0 (nullptr: columns past the output)
+      {
+        const BwTile tl = bw_tile<MODE>(p, offs_s, tiles_prefix, blk_prefix, t);
+        nk = tl.nk;
+        if (nk == 0) {
+          // an empty group in wgrad: dW[e] = 0
+          if (lrow < tl.rows) {
+            uint16_t* orow = g.out + ((int64_t)tl.e * g.rows + tl.row0 + lrow) * g.cols + tl.col0;
+            for (int c = (int)c0; c < c0 + EPI_COLS && c < tl.ncols; c += 8)
+              *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+          }
+          continue;
+        }
+        rsp = lrow >= tl.rows ? nullptr
+                              : WGRAD ? sa_p + tl.blk0 * g.rows + tl.row0 + lrow : sa_p + tl.row0 + lrow;
+        const int64_t cb = (tl.col0 + c0) / 128;
+        csp = WGRAD || cb * 128 >= g.cols ? nullptr
+              : MODE == GEMM_FWD          ? sb_p + ((int64_t)tl.e * (g.cols / 128) + cb) * (g.kk / 128)
+                                          : sb_p + (int64_t)tl.e * (g.kk / 128) * (g.cols / 128) + cb;
       }
       // scale of k-block ks: row part (per thread) and column part (one per
-      // 128-column half for forward / dgrad, per column for wgrad)
+      // warp's columns for forward / dgrad, per column for wgrad)
       auto row_scale = [&](int ks) -> float {
-        if (!row_ok) return 0.0f;
-        if (WGRAD) return sa_p[(tl.blk0 + ks) * g.rows + tl.row0 + lrow];
-        return sa_p[(int64_t)ks * g.M + tl.row0 + lrow];
+        if (rsp == nullptr) return 0.0f;
+        return rsp[(int64_t)ks * (WGRAD ? g.rows : g.M)];
       };
       auto col_scale = [&](int ks) -> float {
         if (WGRAD) return 1.0f;  // per column, from the ring
-        const int64_t cb = (tl.col0 + c0) / 128;
-        if (cb * 128 >= g.cols) return 0.0f;
-        if (MODE == GEMM_FWD) return sb_p[((int64_t)tl.e * (g.cols / 128) + cb) * (g.kk / 128) + ks];
-        return sb_p[((int64_t)tl.e * (g.kk / 128) + ks) * (g.cols / 128) + cb];   // dgrad: W^T tiles
+        if (csp == nullptr) return 0.0f;
+        return csp[MODE == GEMM_FWD ? (int64_t)ks : (int64_t)ks * (g.cols / 128)];   // dgrad: W^T tiles
       };
       // column pairs: the promotion runs on packed fp32x2 multiplies / FMAs
       float2 acc[EPI_COLS / 2];
@@ -381,9 +410,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int j = 0; j < EPI_COLS / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
       float rs_next = row_scale(0), cs_next = col_scale(0);
       bool ok = true;
-      for (int ks = 0; ks < tl.nk; ++ks) {
+      for (int ks = 0; ks < nk; ++ks) {
         const float rs = rs_next, cs = cs_next;
-        if (ks + 1 < tl.nk) {
+        if (ks + 1 < nk) {
           rs_next = row_scale(ks + 1);
           cs_next = col_scale(ks + 1);
         }
@@ -408,26 +437,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const float f = WGRAD ? rs : rs * cs;
 #pragma unroll
-        for (int c = 0; c < EPI_COLS; c += 16) {
-          uint32_t r[16];
-          tmem_ld16(taddr + pb * BN + c, r);
+        for (int c = 0; c < EPI_COLS; c += LDW) {
+          uint32_t r[LDW];
+          if constexpr (LDW == 32) {
+            tmem_ld32(taddr + pb * PSTRIDE + c, r);
+          } else {
+            tmem_ld16(taddr + pb * PSTRIDE + c, r);
+          }
           tmem_ld_wait();
           const float2 f2 = make_float2(f, f);
           if constexpr (WGRAD) {
             // the product times its column scale, then times the row scale
 #pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-              const float4 cv = *reinterpret_cast<const float4*>(csv + c + j);
-              const float2 p0 = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
-                                           make_float2(cv.x, cv.y));
-              const float2 p1 = __fmul2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
-                                           make_float2(cv.z, cv.w));
-              acc[(c + j) / 2] = __ffma2_rn(p0, f2, acc[(c + j) / 2]);
-              acc[(c + j) / 2 + 1] = __ffma2_rn(p1, f2, acc[(c + j) / 2 + 1]);
+            for (int j = 0; j < LDW; j += 2) {
+              const float2 cv = *reinterpret_cast<const float2*>(csv + c + j);
+              const float2 pr = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), cv);
+              acc[(c + j) / 2] = __ffma2_rn(pr, f2, acc[(c + j) / 2]);
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; j += 2)
+            for (int j = 0; j < LDW; j += 2)
               acc[(c + j) / 2] =
                   __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), f2, acc[(c + j) / 2]);
           }
@@ -441,6 +470,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         ++np;
       }
       if (!ok) break;
+      const BwTile tl = bw_tile<MODE>(p, offs_s, tiles_prefix, blk_prefix, t);
       // 32-column slices through the warp's staging tile: 16-byte chunk ch
       // of row r at r * 64 + ((ch ^ ((r >> 1) & 3)) << 4) (the 64-byte
       // swizzle of the output map; conflict-free for the row-per-lane writes
@@ -515,7 +545,7 @@ template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& to, const BwParams& p,
                         int64_t tiles, cudaStream_t st) {
   auto kern = k_blockwise_mm<MODE>;
-  constexpr int SMEM_BYTES = Cfg<MODE>::SMEM_BYTES;
+  constexpr int SMEM_BYTES = Cfg<MODE>::SMEM_BYTES, THREADS = Cfg<MODE>::THREADS;
   if (SMEM_BYTES > p.g.max_smem) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -530,9 +560,10 @@ cudaError_t launch_blockwise_mm(const GemmArgs& g, cudaStream_t st) {
   if (g.E > MAXG) return cudaErrorNotSupported;
   if (g.kk > INT32_MAX || g.rows > INT32_MAX || g.cols > INT32_MAX || g.M > INT32_MAX) return cudaErrorInvalidValue;
   const bool wgrad = g.mode == GEMM_WGRAD;
+  const int bn = wgrad ? Cfg<GEMM_WGRAD>::BN : Cfg<GEMM_FWD>::BN;
   BwParams p;
   p.g = g;
-  p.n_tiles = (int)((g.cols + BN - 1) / BN);
+  p.n_tiles = (int)((g.cols + bn - 1) / bn);
   p.m_tiles_w = (int)((g.rows + BM - 1) / BM);
   CUtensorMap ta, tb;
   {
@@ -545,12 +576,12 @@ cudaError_t launch_blockwise_mm(const GemmArgs& g, cudaStream_t st) {
   if (wgrad) {
     cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)g.cols};
     cuuint64_t strides[1] = {(cuuint64_t)g.kk};
-    cuuint32_t box[2] = {BK, BN};
+    cuuint32_t box[2] = {BK, (cuuint32_t)bn};
     if (!make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b, 2, dims, strides, box)) return cudaErrorInvalidValue;
   } else {
     cuuint64_t dims[3] = {(cuuint64_t)g.kk, (cuuint64_t)g.cols, (cuuint64_t)g.E};
     cuuint64_t strides[2] = {(cuuint64_t)g.kk, (cuuint64_t)(g.kk * g.cols)};
-    cuuint32_t box[3] = {BK, BN, 1};
+    cuuint32_t box[3] = {BK, (cuuint32_t)bn, 1};
     if (!make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.b, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
   // bf16 output slices of 32 columns x 32 rows, 64-byte swizzle; wgrad as
