@@ -33,9 +33,9 @@
 //    128 registers a thread.  The N = 192 MMA takes as long as an N = 256
 //    one (75% of the per-clock tensor peak at most); with 256 columns the
 //    promotion was the bound, 15% slower;
-//  * wgrad's per-column scales change with every k-block: the producer
-//    bulk-copies each k-block's 256 of them into a ring slot that the
-//    epilogue warps release;
+//  * wgrad's row and column scales change with every k-block: the producer
+//    bulk-copies each k-block's 128 + 192 of them into a ring slot that the
+//    epilogue warps release, so the promotion loop makes no global loads;
 //  * every wait is bounded; a timeout sets the device status word.
 #include <cuda.h>
 
@@ -73,7 +73,8 @@ struct Cfg {
   static constexpr int bars = STAGES * STAGE_BYTES;
   static constexpr int misc = bars + (4 * STAGES + 6) * 8;  // tmem base, abort flag, total tiles
   static constexpr int colsc = misc + 16;                   // wgrad column scales [STAGES][BN]
-  static constexpr int offs = colsc + STAGES * BN * 4;      // group ends [MAXG]
+  static constexpr int rowsc = colsc + STAGES * BN * 4;     // wgrad row scales [STAGES][BM]
+  static constexpr int offs = rowsc + (WG ? STAGES * BM * 4 : 0);  // group ends [MAXG]
   static constexpr int tiles_prefix = offs + MAXG * 4;
   static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
   static constexpr int stg = (blk_prefix + (MAXG + 1) * 4 + 1023) / 1024 * 1024;  // [warps][NSTG][2 KB]
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
   volatile int* abort_flag = (volatile int*)(smem + C::misc + 4);
   int* total_s = (int*)(smem + C::misc + 8);
   float* colsc = (float*)(smem + C::colsc);
+  float* rowsc = (float*)(smem + C::rowsc);
   int* offs_s = (int*)(smem + C::offs);
   int* tiles_prefix = (int*)(smem + C::tiles_prefix);
   int* blk_prefix = (int*)(smem + C::blk_prefix);
@@ -271,16 +273,20 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
         tma_load_2d(sa, &tmA, &full[stage], x, (int)tl.row0);
         if (WGRAD) {
           tma_load_2d(sa + A_BYTES, &tmB, &full[stage], x, (int)tl.col0);
-          // this k-block's column scales (the epilogue released the slot)
+          // this k-block's column and row scales (the epilogue released the
+          // slot); rows and columns are multiples of 128, the scale arrays
+          // 16-byte aligned
           if (!mbar_wait(&cs_empty[stage], phase ^ 1, abort_flag)) {
             set_status(g.status, FP8MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             break;
           }
-          const uint32_t nbytes = (uint32_t)(tl.ncols * 4);
+          const uint32_t cbytes = (uint32_t)(tl.ncols * 4), rbytes = (uint32_t)(tl.rows * 4);
           cs_filled[stage] = (int)phase;
-          mbar_expect_tx(&cs_full[stage], nbytes);
-          bulk_load(colsc + stage * BN, (const float*)g.b_scale + (tl.blk0 + ks) * g.cols + tl.col0, nbytes,
+          mbar_expect_tx(&cs_full[stage], cbytes + rbytes);
+          bulk_load(colsc + stage * BN, (const float*)g.b_scale + (tl.blk0 + ks) * g.cols + tl.col0, cbytes,
+                    &cs_full[stage]);
+          bulk_load(rowsc + stage * BM, (const float*)g.a_scale + (tl.blk0 + ks) * g.rows + tl.row0, rbytes,
                     &cs_full[stage]);
         } else {
           tma_load_3d(sa + A_BYTES, &tmB, &full[stage], x, (int)tl.col0, tl.e);
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
       // scale of k-block ks: row part (per thread) and column part (one per
       // warp's columns for forward / dgrad, per column for wgrad)
       auto row_scale = [&](int ks) -> float {
-        if (rsp == nullptr) return 0.0f;
+        if (WGRAD || rsp == nullptr) return 0.0f;  // wgrad: from the ring
         return rsp[(int64_t)ks * (WGRAD ? g.rows : g.M)];
       };
       auto col_scale = [&](int ks) -> float {
@@ -435,7 +441,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1)
           break;
         }
         tc_fence_after();
-        const float f = WGRAD ? rs : rs * cs;
+        const float f = WGRAD ? rowsc[slot * BM + lrow] : rs * cs;
 #pragma unroll
         for (int c = 0; c < EPI_COLS; c += LDW) {
           uint32_t r[LDW];
