@@ -7,7 +7,8 @@
 // Three stream-ordered launches around the caller's one-float scale buffer,
 // which holds the maximum's bf16 bit pattern until the last one replaces it
 // by the dequantization scale:
-//   1. k_tw_amax: grid-stride 16-byte loads (four in flight per thread),
+//   1. k_tw_amax: grid-stride 16-byte loads (four in flight per thread; six
+//      256-thread CTAs per SM, the grid one wave of them),
 //      warp / block maxima, one atomicMax per block (bit patterns of
 //      non-negative values order like the values);
 //   2. the cast: k_tw_cast for the plain layout, or the colwise kernel in its
@@ -31,7 +32,7 @@ FP8MOE_DEV uint4 ld_nc(const void* p) {
 // Four 16-byte chunks in flight per thread and loop trip.
 constexpr int TW_U = 4;
 
-__global__ void __launch_bounds__(256) k_tw_amax(const uint16_t* __restrict__ x, int64_t n,
+__global__ void __launch_bounds__(256, 6) k_tw_amax(const uint16_t* __restrict__ x, int64_t n,
                                                  uint32_t* __restrict__ amax_bits) {
   __shared__ uint32_t wmax[8];
   const int64_t nch = n / 8;
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(256) k_tw_amax(const uint16_t* __restrict__ x,
 }
 
 template <bool FNUZ>
-__global__ void __launch_bounds__(256) k_tw_cast(const uint16_t* __restrict__ x, int64_t n, uint8_t* __restrict__ q,
+__global__ void __launch_bounds__(256, 6) k_tw_cast(const uint16_t* __restrict__ x, int64_t n, uint8_t* __restrict__ q,
                                                  const uint32_t* __restrict__ amax_bits) {
   float s, inv;
   rowwise_scale<FNUZ>(bf16bits_to_float(*amax_bits), s, inv);
@@ -99,6 +100,18 @@ __global__ void k_tw_finalize(float* scale) {
   *scale = inv;
 }
 
+// CTAs of `kern` resident on the whole GPU at once: the grid-stride kernels
+// run as a single wave (a second wave would repeat the ramp and the tail)
+template <typename K>
+int resident_ctas(K kern, int num_sms) {
+  int per = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, 256, 0) != cudaSuccess || per < 1) {
+    (void)cudaGetLastError();
+    per = 4;
+  }
+  return per * num_sms;
+}
+
 }  // namespace
 
 cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
@@ -108,19 +121,24 @@ cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, co
   cudaError_t e = cudaMemsetAsync(scale_inv, 0, sizeof(float), st);
   if (e != cudaSuccess) return e;
   const bool fnuz = kind == FP8MOE_E4M3FNUZ;
-  const int64_t cap = (int64_t)num_sms * 8;
+  static int cap_amax = 0, cap_fn = 0, cap_fnuz = 0;
+  if (!cap_amax) {
+    cap_amax = resident_ctas(k_tw_amax, num_sms);
+    cap_fn = resident_ctas(k_tw_cast<false>, num_sms);
+    cap_fnuz = resident_ctas(k_tw_cast<true>, num_sms);
+  }
   if (n > 0) {
-    int64_t blocks = (n / 8 + 255) / 256;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    k_tw_amax<<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, n, (uint32_t*)scale_inv);
+    const int64_t want = (n / 8 + 255) / 256;
+    auto grid = [&](int cap) -> unsigned { return (unsigned)(want < 1 ? 1 : (want < cap ? want : cap)); };
+    k_tw_amax<<<grid(cap_amax), 256, 0, st>>>((const uint16_t*)x, n, (uint32_t*)scale_inv);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (!transpose_out) {
       if (fnuz) {
-        k_tw_cast<true><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, n, (uint8_t*)q, (const uint32_t*)scale_inv);
+        k_tw_cast<true><<<grid(cap_fnuz), 256, 0, st>>>((const uint16_t*)x, n, (uint8_t*)q,
+                                                        (const uint32_t*)scale_inv);
       } else {
-        k_tw_cast<false><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, n, (uint8_t*)q,
-                                                           (const uint32_t*)scale_inv);
+        k_tw_cast<false><<<grid(cap_fn), 256, 0, st>>>((const uint16_t*)x, n, (uint8_t*)q,
+                                                       (const uint32_t*)scale_inv);
       }
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
