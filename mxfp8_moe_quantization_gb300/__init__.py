@@ -85,7 +85,7 @@ def _lib_raw() -> ctypes.CDLL:
         if not os.path.exists(library_path):
             raise ImportError(
                 f"libfp8moe.so is not built ({library_path}); run "
-                "`python -c 'import __graft_entry__ as g; g.build()'`")
+                "`python -m mxfp8_moe_quantization_gb300.build`")
         l = ctypes.CDLL(library_path)
         for name, (res, args) in SYMBOLS.items():
             f = getattr(l, name)
