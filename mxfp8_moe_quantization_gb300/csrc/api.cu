@@ -254,7 +254,7 @@ fp8moe_status fp8moe_quantize_blockwise_tokens(const void* x, int64_t M, int64_t
   DevInfo* d;
   fp8moe_status st = device_info(&d);
   if (st) return st;
-  return cuda_result(fp8moe::launch_bw_tokens(x, M, C, offs, E, kind, qt, scale_inv, d->status,
+  return cuda_result(fp8moe::launch_bw_tokens(x, M, C, offs, E, kind, qt, scale_inv, d->num_sms, d->status,
                                               (cudaStream_t)stream));
 }
 

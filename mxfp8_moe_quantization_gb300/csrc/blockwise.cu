@@ -113,11 +113,12 @@ __global__ void __launch_bounds__(256) k_bw_weight(const uint16_t* __restrict__ 
   }
 }
 
-// One token block (<= 128 rows of one group) x 128 columns per CTA.  Warp w:
+// Units of one token block (<= 128 rows of one group) x 128 columns; a
+// persistent CTA builds the group table once and loops over units.  Warp w:
 // rows 32*(w&3) .. +31 of the block, columns 64*(w>>2) .. +63; lane: 8 rows x
 // 8 columns.
 template <bool FNUZ>
-__global__ void __launch_bounds__(256) k_bw_tokens(const uint16_t* __restrict__ x, int64_t M, int64_t C,
+__global__ void __launch_bounds__(256, 4) k_bw_tokens(const uint16_t* __restrict__ x, int64_t M, int64_t C,
                                                    const int32_t* __restrict__ offs, int E, int n_ct,
                                                    uint8_t* __restrict__ qt, float* __restrict__ inv, int* status) {
   __shared__ GroupTable gt;
@@ -126,84 +127,86 @@ __global__ void __launch_bounds__(256) k_bw_tokens(const uint16_t* __restrict__ 
   if (gt.bad) return;
   const int64_t last = gt.end[E - 1] - (E > 1 ? gt.end[E - 2] : 0);
   const int64_t total = gt.pad[E - 1] + (last + TILE - 1) / TILE;
-  const int64_t blk = blockIdx.x / n_ct;
-  if (blk >= total) return;
-  const int ct = (int)(blockIdx.x % n_ct);
-  // owner: the last group whose first block is <= blk
-  int lo = 0, hi = E - 1, g = 0;
-  while (lo <= hi) {
-    const int mid = (lo + hi) >> 1;
-    if (gt.pad[mid] <= blk) {
-      g = mid;
-      lo = mid + 1;
-    } else {
-      hi = mid - 1;
-    }
-  }
-  const int64_t r0 = (g == 0 ? 0 : gt.end[g - 1]) + (blk - gt.pad[g]) * TILE;
-  const int64_t r1 = min(gt.end[g], r0 + TILE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rq4 = warp & 3, ch = warp >> 2, cl = lane & 7, rq = lane >> 3;
-  const int64_t c = (int64_t)ct * TILE + ch * 64 + cl * 8;
-  const int64_t rr = r0 + rq4 * 32 + rq * 8;
-  // block sizes are multiples of 32: a lane's 8 rows are all in or all out
-  const bool rows_ok = rr < r1, col_ok = c < C;
-  uint4 v[8];
+  for (int64_t u = blockIdx.x; u < total * n_ct; u += gridDim.x) {
+    const int64_t blk = u / n_ct;
+    const int ct = (int)(u % n_ct);
+    // owner: the last group whose first block is <= blk
+    int lo = 0, hi = E - 1, g = 0;
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      if (gt.pad[mid] <= blk) {
+        g = mid;
+        lo = mid + 1;
+      } else {
+        hi = mid - 1;
+      }
+    }
+    const int64_t r0 = (g == 0 ? 0 : gt.end[g - 1]) + (blk - gt.pad[g]) * TILE;
+    const int64_t r1 = min(gt.end[g], r0 + TILE);
+    const int64_t c = (int64_t)ct * TILE + ch * 64 + cl * 8;
+    const int64_t rr = r0 + rq4 * 32 + rq * 8;
+    // block sizes are multiples of 32: a lane's 8 rows are all in or all out
+    const bool rows_ok = rr < r1, col_ok = c < C;
+    uint4 v[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) v[k] = rows_ok && col_ok ? ld_nc16(x + (rr + k) * C + c) : make_uint4(0, 0, 0, 0);
-  uint32_t m[4] = {0, 0, 0, 0};
+    for (int k = 0; k < 8; ++k) v[k] = rows_ok && col_ok ? ld_nc16(x + (rr + k) * C + c) : make_uint4(0, 0, 0, 0);
+    uint32_t m[4] = {0, 0, 0, 0};
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    m[0] = __vmaxu2(m[0], v[k].x & 0x7FFF7FFFu);
-    m[1] = __vmaxu2(m[1], v[k].y & 0x7FFF7FFFu);
-    m[2] = __vmaxu2(m[2], v[k].z & 0x7FFF7FFFu);
-    m[3] = __vmaxu2(m[3], v[k].w & 0x7FFF7FFFu);
-  }
+    for (int k = 0; k < 8; ++k) {
+      m[0] = __vmaxu2(m[0], v[k].x & 0x7FFF7FFFu);
+      m[1] = __vmaxu2(m[1], v[k].y & 0x7FFF7FFFu);
+      m[2] = __vmaxu2(m[2], v[k].z & 0x7FFF7FFFu);
+      m[3] = __vmaxu2(m[3], v[k].w & 0x7FFF7FFFu);
+    }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    m[i] = __vmaxu2(m[i], __shfl_xor_sync(0xffffffffu, m[i], 8));
-    m[i] = __vmaxu2(m[i], __shfl_xor_sync(0xffffffffu, m[i], 16));
-  }
-  if (rq == 0) red[rq4][ch][cl] = make_uint4(m[0], m[1], m[2], m[3]);
-  __syncthreads();
-  uint32_t cm[4];
+    for (int i = 0; i < 4; ++i) {
+      m[i] = __vmaxu2(m[i], __shfl_xor_sync(0xffffffffu, m[i], 8));
+      m[i] = __vmaxu2(m[i], __shfl_xor_sync(0xffffffffu, m[i], 16));
+    }
+    __syncthreads();  // the previous unit's reads of red are done
+    if (rq == 0) red[rq4][ch][cl] = make_uint4(m[0], m[1], m[2], m[3]);
+    __syncthreads();
+    uint32_t cm[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t* p0 = reinterpret_cast<const uint32_t*>(&red[0][ch][cl]);
-    const uint32_t* p1 = reinterpret_cast<const uint32_t*>(&red[1][ch][cl]);
-    const uint32_t* p2 = reinterpret_cast<const uint32_t*>(&red[2][ch][cl]);
-    const uint32_t* p3 = reinterpret_cast<const uint32_t*>(&red[3][ch][cl]);
-    cm[i] = __vmaxu2(__vmaxu2(p0[i], p1[i]), __vmaxu2(p2[i], p3[i]));
-  }
-  float sv[8], iv[8];
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t* p0 = reinterpret_cast<const uint32_t*>(&red[0][ch][cl]);
+      const uint32_t* p1 = reinterpret_cast<const uint32_t*>(&red[1][ch][cl]);
+      const uint32_t* p2 = reinterpret_cast<const uint32_t*>(&red[2][ch][cl]);
+      const uint32_t* p3 = reinterpret_cast<const uint32_t*>(&red[3][ch][cl]);
+      cm[i] = __vmaxu2(__vmaxu2(p0[i], p1[i]), __vmaxu2(p2[i], p3[i]));
+    }
+    float sv[8], iv[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    rowwise_scale<FNUZ>(bf16bits_to_float(cm[i] & 0xFFFFu), sv[2 * i], iv[2 * i]);
-    rowwise_scale<FNUZ>(bf16bits_to_float(cm[i] >> 16), sv[2 * i + 1], iv[2 * i + 1]);
-  }
-  if (rq4 == 0 && rq == 0 && col_ok) {
-    float* ip = inv + blk * C + c;
-    *reinterpret_cast<float4*>(ip) = make_float4(iv[0], iv[1], iv[2], iv[3]);
-    *reinterpret_cast<float4*>(ip + 4) = make_float4(iv[4], iv[5], iv[6], iv[7]);
-  }
-  if (!rows_ok || !col_ok) return;
-  uint32_t w0[8], w1[8];
+    for (int i = 0; i < 4; ++i) {
+      rowwise_scale<FNUZ>(bf16bits_to_float(cm[i] & 0xFFFFu), sv[2 * i], iv[2 * i]);
+      rowwise_scale<FNUZ>(bf16bits_to_float(cm[i] >> 16), sv[2 * i + 1], iv[2 * i + 1]);
+    }
+    if (rq4 == 0 && rq == 0 && col_ok) {
+      float* ip = inv + blk * C + c;
+      *reinterpret_cast<float4*>(ip) = make_float4(iv[0], iv[1], iv[2], iv[3]);
+      *reinterpret_cast<float4*>(ip + 4) = make_float4(iv[4], iv[5], iv[6], iv[7]);
+    }
+    if (!rows_ok || !col_ok) continue;
+    uint32_t w0[8], w1[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    w0[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v[k].x), sv[0]), __fmul_rn(bf16_hi(v[k].x), sv[1]),
-                       __fmul_rn(bf16_lo(v[k].y), sv[2]), __fmul_rn(bf16_hi(v[k].y), sv[3]));
-    w1[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v[k].z), sv[4]), __fmul_rn(bf16_hi(v[k].z), sv[5]),
-                       __fmul_rn(bf16_lo(v[k].w), sv[6]), __fmul_rn(bf16_hi(v[k].w), sv[7]));
-  }
-  uint8_t* dst = qt + c * M + rr;
+    for (int k = 0; k < 8; ++k) {
+      w0[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v[k].x), sv[0]), __fmul_rn(bf16_hi(v[k].x), sv[1]),
+                         __fmul_rn(bf16_lo(v[k].y), sv[2]), __fmul_rn(bf16_hi(v[k].y), sv[3]));
+      w1[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v[k].z), sv[4]), __fmul_rn(bf16_hi(v[k].z), sv[5]),
+                         __fmul_rn(bf16_lo(v[k].w), sv[6]), __fmul_rn(bf16_hi(v[k].w), sv[7]));
+    }
+    uint8_t* dst = qt + c * M + rr;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint32_t* W = h ? w1 : w0;
-    uint32_t a[4], b[4];
-    transpose4x4(W[0], W[1], W[2], W[3], a);
-    transpose4x4(W[4], W[5], W[6], W[7], b);
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t* W = h ? w1 : w0;
+      uint32_t a[4], b[4];
+      transpose4x4(W[0], W[1], W[2], W[3], a);
+      transpose4x4(W[4], W[5], W[6], W[7], b);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) *reinterpret_cast<uint2*>(dst + (h * 4 + j) * M) = make_uint2(a[j], b[j]);
+      for (int j = 0; j < 4; ++j) *reinterpret_cast<uint2*>(dst + (h * 4 + j) * M) = make_uint2(a[j], b[j]);
+    }
   }
 }
 
@@ -233,11 +236,25 @@ cudaError_t launch_bw_weight(const void* w, int64_t E, int64_t N, int64_t K, int
 }
 
 cudaError_t launch_bw_tokens(const void* x, int64_t M, int64_t C, const int32_t* offs, int64_t E, int kind,
-                             void* qt, float* inv, int* status, cudaStream_t st) {
+                             void* qt, float* inv, int num_sms, int* status, cudaStream_t st) {
   if (C == 0) return cudaSuccess;
   const int n_ct = (int)((C + TILE - 1) / TILE);
-  const int64_t blocks = ((M + TILE - 1) / TILE + E) * n_ct;   // an upper bound; extra CTAs leave at once
-  if (kind == FP8MOE_E4M3FNUZ) {
+  // persistent CTAs, one wave: as many as are resident, at most one per unit
+  // (the unit count is an upper bound here; the exact one needs the offsets)
+  static int per_sm[2] = {0, 0};
+  const bool fnuz = kind == FP8MOE_E4M3FNUZ;
+  if (!per_sm[fnuz]) {
+    const cudaError_t e = fnuz ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[1], k_bw_tokens<true>, 256, 0)
+                               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[0], k_bw_tokens<false>, 256, 0);
+    if (e != cudaSuccess || per_sm[fnuz] < 1) {
+      (void)cudaGetLastError();
+      per_sm[fnuz] = 4;
+    }
+  }
+  const int64_t units = ((M + TILE - 1) / TILE + E) * n_ct;
+  const int64_t cap = (int64_t)per_sm[fnuz] * num_sms;
+  const int64_t blocks = units < cap ? units : cap;
+  if (fnuz) {
     k_bw_tokens<true><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, M, C, offs, (int)E, n_ct,
                                                         (uint8_t*)qt, inv, status);
   } else {

@@ -43,7 +43,7 @@ cudaError_t launch_bw_rows(const void* x, int64_t R, int64_t C, int kind, void* 
 cudaError_t launch_bw_weight(const void* w, int64_t E, int64_t N, int64_t K, int kind, void* q, void* qt,
                              float* inv, cudaStream_t st);
 cudaError_t launch_bw_tokens(const void* x, int64_t M, int64_t C, const int32_t* offs, int64_t E, int kind,
-                             void* qt, float* inv, int* status, cudaStream_t st);
+                             void* qt, float* inv, int num_sms, int* status, cudaStream_t st);
 // token routing (routing.cu)
 int64_t route_workspace_bytes(int64_t T, int64_t k, int64_t E);
 cudaError_t launch_route_permute(const void* x, int64_t T, int64_t H, const int32_t* idx, const float* w, int64_t k,
