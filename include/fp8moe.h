@@ -370,12 +370,27 @@ fp8moe_status fp8moe_route_unpermute(const void* y, int64_t T, int64_t N, const 
                                      const float* topk_w, int64_t k, void* out, fp8moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Device status.  Synchronizes `stream`, returns the sticky device error
- * code (an fp8moe_status value, 0 if none) in *out_code and clears it.
- * The pages' failure mode is silent ([AMD-FP8] aixai.ru "Тихая порча
- * градиентов"); this makes device-side problems visible instead.
+ * Device status.  After the work already queued on `stream`, takes the
+ * sticky device error code of the current device (an fp8moe_status value, 0
+ * if none) and clears it in one atomic exchange on the device, then
+ * synchronizes `stream` and returns the code in *out_code.  An error that a
+ * kernel on another stream sets meanwhile is never lost: it is either taken
+ * by this call or left for the next one.  The pages' failure mode is silent
+ * ([AMD-FP8] aixai.ru "Тихая порча градиентов"); this makes device-side
+ * problems visible instead.
  * ------------------------------------------------------------------------ */
 fp8moe_status fp8moe_get_device_status(fp8moe_stream_t stream, int32_t* out_code);
+
+/* ------------------------------------------------------------------------
+ * Testing hook of the failure-detection path (no counterpart on the pages).
+ * Arms a one-shot flag: the next fp8moe_scaled_grouped_mm_* launch of the
+ * process (MXFP8, rowwise or tensorwise recipe) has its first pair of CTAs
+ * keep its first accumulator, so the epilogue's bounded wait (2 s) runs out
+ * and the launch sets FP8MOE_ERR_TIMEOUT.  Every CTA still waits for its own
+ * copies and MMAs before it releases its tensor memory, so the context stays
+ * usable.  No environment variable and no other call can stall a launch.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_testing_stall_next_gemm(void);
 
 /* Static string for a status code. */
 const char* fp8moe_status_string(int status);

@@ -24,6 +24,7 @@ __all__ = [
     "fp8moe_swizzled_scales_bytes", "fp8moe_swizzle_scales_128x4",
     "fp8moe_scaled_grouped_mm_fwd", "fp8moe_scaled_grouped_mm_dgrad",
     "fp8moe_scaled_grouped_mm_wgrad", "fp8moe_get_device_status", "fp8moe_status_string",
+    "fp8moe_testing_stall_next_gemm",
     "fp8moe_mxfp8_moe_workspace_bytes", "fp8moe_mxfp8_moe_fwd", "fp8moe_mxfp8_moe_bwd",
     "fp8moe_quantize_blockwise_rows", "fp8moe_quantize_blockwise_weight", "fp8moe_blockwise_token_blocks",
     "fp8moe_quantize_blockwise_tokens",
@@ -64,6 +65,7 @@ SYMBOLS = {
     "fp8moe_mxfp8_moe_fwd": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _vp]),
     "fp8moe_mxfp8_moe_bwd": (_i32, [_vp, _vp, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp]),
     "fp8moe_get_device_status": (_i32, [_vp, ctypes.POINTER(ctypes.c_int32)]),
+    "fp8moe_testing_stall_next_gemm": (_i32, []),
     "fp8moe_status_string": (ctypes.c_char_p, [_i32]),
     "fp8moe_version": (_i32, []),
 }
@@ -446,6 +448,12 @@ def fp8moe_get_device_status(stream=None) -> int:
     v = ctypes.c_int32(0)
     _check("fp8moe_get_device_status", _lib_raw().fp8moe_get_device_status(_stream(stream), ctypes.byref(v)))
     return int(v.value)
+
+
+def fp8moe_testing_stall_next_gemm() -> None:
+    """Arm the one-shot stall of the next grouped GEMM launch (tests of the
+    bounded-wait timeout path)."""
+    _check("fp8moe_testing_stall_next_gemm", _lib_raw().fp8moe_testing_stall_next_gemm())
 
 
 def fp8moe_status_string(code: int) -> str:

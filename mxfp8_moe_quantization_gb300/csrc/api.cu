@@ -7,15 +7,19 @@
 #include "launch.h"
 
 // Sticky device status word (static device memory: the library allocates
-// nothing).  Kernels receive its address; fp8moe_get_device_status reads and
-// clears it.
+// nothing).  Kernels receive its address; fp8moe_get_device_status takes it
+// (reads and clears it in one atomic exchange) into the take slot.
 static __device__ int g_fp8moe_status;
+static __device__ int g_fp8moe_status_take;
+
+static __global__ void k_take_status(int* status, int* take) { *take = atomicExch(status, 0); }
 
 namespace {
 
 struct DevInfo {
   bool init = false;
   int* status = nullptr;
+  int* take = nullptr;
   int num_sms = 0;
   int max_smem = 0;
 };
@@ -23,6 +27,7 @@ struct DevInfo {
 constexpr int kMaxDevices = 128;
 DevInfo g_dev[kMaxDevices];
 std::mutex g_mu;
+std::mutex g_take_mu;
 
 fp8moe_status device_info(DevInfo** out) {
   int dev = 0;
@@ -31,6 +36,7 @@ fp8moe_status device_info(DevInfo** out) {
   DevInfo& d = g_dev[dev];
   if (!d.init) {
     if (cudaGetSymbolAddress((void**)&d.status, g_fp8moe_status) != cudaSuccess) return FP8MOE_ERR_CUDA;
+    if (cudaGetSymbolAddress((void**)&d.take, g_fp8moe_status_take) != cudaSuccess) return FP8MOE_ERR_CUDA;
     if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return FP8MOE_ERR_CUDA;
     if (cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
@@ -383,12 +389,26 @@ fp8moe_status fp8moe_route_unpermute(const void* y, int64_t T, int64_t N, const 
 
 fp8moe_status fp8moe_get_device_status(fp8moe_stream_t stream, int32_t* out_code) {
   if (!out_code) return FP8MOE_ERR_INVALID_ARG;
-  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FP8MOE_ERR_CUDA;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  // The read and the clear are one atomic exchange on the device, ordered
+  // after the stream's work: a status that a kernel on another stream sets
+  // meanwhile is either taken here or stays for the next call.  The mutex
+  // keeps concurrent callers from sharing the take slot.
+  std::lock_guard<std::mutex> lk(g_take_mu);
+  k_take_status<<<1, 1, 0, (cudaStream_t)stream>>>(d->status, d->take);
+  if (cudaGetLastError() != cudaSuccess) return FP8MOE_ERR_CUDA;
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_fp8moe_status, sizeof(int)) != cudaSuccess) return FP8MOE_ERR_CUDA;
-  const int zero = 0;
-  if (cudaMemcpyToSymbol(g_fp8moe_status, &zero, sizeof(int)) != cudaSuccess) return FP8MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, d->take, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+    return FP8MOE_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FP8MOE_ERR_CUDA;
   *out_code = v;
+  return FP8MOE_OK;
+}
+
+fp8moe_status fp8moe_testing_stall_next_gemm(void) {
+  fp8moe::arm_gemm_stall_hook();
   return FP8MOE_OK;
 }
 

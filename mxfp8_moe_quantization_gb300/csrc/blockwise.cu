@@ -241,18 +241,12 @@ cudaError_t launch_bw_tokens(const void* x, int64_t M, int64_t C, const int32_t*
   const int n_ct = (int)((C + TILE - 1) / TILE);
   // persistent CTAs, one wave: as many as are resident, at most one per unit
   // (the unit count is an upper bound here; the exact one needs the offsets)
-  static int per_sm[2] = {0, 0};
+  static std::atomic<int> per_sm_fn{0}, per_sm_fnuz{0};
   const bool fnuz = kind == FP8MOE_E4M3FNUZ;
-  if (!per_sm[fnuz]) {
-    const cudaError_t e = fnuz ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[1], k_bw_tokens<true>, 256, 0)
-                               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[0], k_bw_tokens<false>, 256, 0);
-    if (e != cudaSuccess || per_sm[fnuz] < 1) {
-      (void)cudaGetLastError();
-      per_sm[fnuz] = 4;
-    }
-  }
+  const int per_sm = fnuz ? blocks_per_sm(per_sm_fnuz, k_bw_tokens<true>, 256, 0, 4)
+                          : blocks_per_sm(per_sm_fn, k_bw_tokens<false>, 256, 0, 4);
   const int64_t units = ((M + TILE - 1) / TILE + E) * n_ct;
-  const int64_t cap = (int64_t)per_sm[fnuz] * num_sms;
+  const int64_t cap = (int64_t)per_sm * num_sms;
   const int64_t blocks = units < cap ? units : cap;
   if (fnuz) {
     k_bw_tokens<true><<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, M, C, offs, (int)E, n_ct,

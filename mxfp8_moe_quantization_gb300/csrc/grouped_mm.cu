@@ -12,25 +12,32 @@
 //
 // Design (GB300-first; the pages' Triton / Composable-Kernel kernels are for
 // other hardware):
-//  * persistent kernel, one 192-thread CTA per SM, tiles of 128 x 256 outputs;
+//  * persistent kernel over clusters of two CTAs (one per SM): each pair runs
+//    cta_group::2 MMAs of M = 256 (128 rows per CTA) x N = 256, each CTA
+//    holding its own 128 rows of A and its own half of B, so every SM
+//    receives half of the B tile per MMA;
 //  * warp 0: TMA producer (A and B tiles with 128-byte swizzle, MXFP8 scale
-//    tiles as 512-byte bulk copies -- the 128x4 layout makes each one
-//    contiguous); warp 1: TMEM allocator and single-thread MMA issuer; warps
-//    2-5: epilogue (TMEM -> registers -> bf16 -> global); warp 6: scale-factor
-//    copier (MXFP8): moves each stage's scale tiles into TMEM with
-//    tcgen05.cp and signals the MMA thread through a second per-stage barrier.
-//    Issued from the MMA thread itself, the copies cost a quarter of the MMA
-//    rate (measured); from their own thread they overlap the MMAs;
-//  * 4-stage shared-memory ring with mbarriers; every wait is bounded and a
+//    tiles as 512-byte copies -- the 128x4 layout makes each one
+//    contiguous); both CTAs' loads complete on the leader's barrier (2-SM
+//    TMA); warp 1: TMEM allocator and, in the leader, the single-thread MMA
+//    issuer; warps 2-5: epilogue (TMEM -> registers -> bf16 -> global); warp
+//    6: scale-factor copier (MXFP8): moves each stage's scale tiles into TMEM
+//    with tcgen05.cp and signals the MMA thread through a second per-stage
+//    barrier.  Issued from the MMA thread itself, the copies cost a quarter
+//    of the MMA rate (measured); from their own thread they overlap the MMAs;
+//  * a 6-stage shared-memory ring with mbarriers (5 stages when more than 512
+//    groups need the larger group tables); every wait is bounded and a
 //    timeout sets the device status word instead of hanging;
-//  * accumulator in TMEM (128 lanes x 256 fp32 columns); MXFP8 scales copied
-//    into TMEM per stage with tcgen05.cp and consumed by the block-scaled MMA
-//    (kind::mxf8f6f4, one e8m0 scale per 32 elements of K); the rowwise recipe
-//    uses kind::f8f6f4 and applies row x column fp32 scales in the epilogue;
+//  * accumulator in TMEM (128 lanes x 256 fp32 columns per CTA); MXFP8 scales
+//    consumed by the block-scaled MMA (kind::mxf8f6f4, one e8m0 scale per 32
+//    elements of K); the rowwise recipe uses kind::f8f6f4 and applies row x
+//    column fp32 scales in the epilogue;
 //  * the epilogue drains the accumulator to registers and releases TMEM before
 //    its global stores, so the next tile's MMAs overlap the stores.
+//  Every load lands in the issuing CTA's own shared memory: no TMA multicast.
 #include <cuda.h>
-#include <stdlib.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -43,27 +50,22 @@ namespace fp8moe {
 constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int NUM_THREADS = 224;  // producer, MMA, 4 epilogue warps, scale copier
 constexpr int A_STAGE_BYTES = BM * BK;            // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK / 2;        // this CTA's half of the B tile, 16 KB
 constexpr int SFA_STAGE_BYTES = 512;              // one 128x4 scale tile
 constexpr int SFB_STAGE_BYTES = 1024;             // two 128x4 scale tiles (256 rows)
-constexpr int MAX_GROUPS = 1024;                  // 1-CTA variant; the 2-CTA one holds 512
+constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = 256;            // scale columns start after the accumulator
 constexpr int STG_COLS = 32;                      // output columns per staged store (64 bytes of bf16)
 constexpr int STG_BYTES = 32 * STG_COLS * 2;      // one staging tile: 32 rows x 64 B
 constexpr int STG_WARP_BYTES = 2 * STG_BYTES;     // double-buffered per epilogue warp
 
-// TWO = false: 1-CTA MMAs (M = 128 per CTA), the pair shares B tiles by TMA
-//               multicast; each CTA's shared memory holds the whole B tile.
-// TWO = true:  2-CTA MMAs (cta_group::2, M = 256 across the pair); each CTA
-//               holds its own 128 rows of A and its own half of B, halving the
-//               operand bytes each SM receives per MMA.
-template <bool TWO>
+// BIGE = false: a 6-deep ring and group tables of 512 groups;
+// BIGE = true:  a 5-deep ring, which leaves room for tables of 1024 groups.
+template <bool BIGE>
 struct SmemLayout {
-  // 2-CTA: 32 KB per stage buys a 6-deep ring; its group tables are capped at
-  // 512 groups to fit (larger E runs the 1-CTA variant)
-  static constexpr int STAGES = TWO ? 6 : 4;
-  static constexpr int MAXG = TWO ? 512 : MAX_GROUPS;
-  static constexpr int B_STAGE_BYTES = TWO ? BN * BK / 2 : BN * BK;
+  static constexpr int STAGES = BIGE ? 5 : 6;
+  static constexpr int MAXG = BIGE ? MAX_GROUPS : 512;
   static constexpr int a = 0;
   static constexpr int b = a + STAGES * A_STAGE_BYTES;
   static constexpr int sfa = b + STAGES * B_STAGE_BYTES;
@@ -78,40 +80,20 @@ struct SmemLayout {
   static constexpr int total = stg + 4 * STG_WARP_BYTES;
 };
 static_assert(SmemLayout<false>::stg % 1024 == 0 && SmemLayout<true>::stg % 1024 == 0, "staging alignment");
-template <bool TWO>
-constexpr int smem_bytes() { return SmemLayout<TWO>::total + 1024; }  // + alignment slack
+template <bool BIGE>
+constexpr int smem_bytes() { return SmemLayout<BIGE>::total + 1024; }  // + alignment slack
+static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
-FP8MOE_DEV void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+// completion of the pair's MMAs (issued by the leader) on the barrier at the
+// same offset in every CTA of `mask` (an arrive, not a load)
+FP8MOE_DEV void tc_commit_pair(uint64_t* bar, uint16_t mask) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
       "h"(mask)
-      : "memory");
-}
-// completion of this thread's MMAs on the barrier at the same offset in every
-// CTA of `mask`
-template <bool TWO>
-FP8MOE_DEV void tc_commit_pair(uint64_t* bar, uint16_t mask) {
-  if constexpr (TWO) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-  } else {
-    tc_commit_mc(bar, mask);
-  }
-}
-// 2-SM TMA load multicast to the CTAs of `mask`; each destination's bytes
-// complete on the barrier at `bar`'s offset in that destination's pair leader
-FP8MOE_DEV void tma_load_2d_cg2_mc(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2 "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(bar), "h"(mask)
       : "memory");
 }
 FP8MOE_DEV uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
@@ -147,16 +129,11 @@ FP8MOE_DEV bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* 
 FP8MOE_DEV void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// completion of this thread's earlier tcgen05 ops (of its own CTA group) on a
-// local barrier
-template <bool TWO>
+// completion of this thread's earlier tcgen05 ops (of the pair) on a local
+// barrier
 FP8MOE_DEV void tc_commit_local(uint64_t* bar) {
-  if constexpr (TWO) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-  } else {
-    tc_commit(bar);
-  }
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
 }
 
 // Descriptor of one 128x4 scale tile (32 rows of 16 bytes, no swizzle) as the
@@ -181,33 +158,17 @@ FP8MOE_DEV uint32_t idesc_f8() {
   return idesc_f8n<MM, BN>();
 }
 
-template <bool TWO>
 FP8MOE_DEV void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfa, uint32_t sfb,
                        uint32_t accum) {
-  if constexpr (TWO) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::
-            "r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb));
-  } else {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::
-            "r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb));
-  }
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}\n" ::
+          "r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum), "r"(sfa), "r"(sfb));
 }
-template <bool TWO>
 FP8MOE_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-  if constexpr (TWO) {
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
-  } else {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
-  }
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
 }
-
-
 
 // ---------------------------------------------------------------------------
 // kernel
@@ -217,10 +178,9 @@ struct KParams {
   int64_t cpb;        // 128x4 scale tiles per scale row block (A side and, fwd, B side)
   int64_t b_rows_pad; // fwd/dgrad: padded rows (cols of C) of one expert's scale matrix
   int n_tiles;        // tiles along the output columns
-  int n_units;        // column units: n-tiles per cluster pass (quad mode: 2 n-tiles)
   int m_tiles_w;      // wgrad: tiles along the output rows
   int tma_out;        // output stored by TMA (tmOut valid); else by thread stores
-  int stall_test;     // test hook (FP8MOE_TEST_STALL=1): one accumulator is never handed over
+  int stall_test;     // test hook (armed by fp8moe_testing_stall_next_gemm): one accumulator is never handed over
 };
 
 // Per-tile geometry, recomputed identically by every role.
@@ -237,15 +197,12 @@ struct Tile {
 };
 
 // Tiles come in pairs: the two CTAs of a pair take m-tiles 2i and 2i+1 of
-// the same group against the same B tile (1-CTA: shared through TMA multicast;
-// 2-CTA: one M = 256 MMA).  A pair whose second m-tile lies past the group
-// ("phantom", rows == 0) still loads and releases its share of the operands
-// but stores nothing.  In quad mode (NQ = 2) the two pairs of a 4-CTA cluster
-// take adjacent n-tiles 2j and 2j+1 of the same rows and share the A tile; an
-// n-tile past the output ("phantom", col0 >= cols) stores nothing either.
-// rank: CTA within its pair; pp: pair within the cluster.
-template <bool WGRAD, int NQ>
-FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* blk_prefix, int t, int rank, int pp) {
+// the same group against the same B tile (one M = 256 MMA).  When the second
+// m-tile lies past the group ("phantom", rows == 0) the pair still computes
+// it (its operand rows read the fill of the tensor map or the next group's
+// rows) but stores nothing.  rank: CTA within its pair.
+template <bool WGRAD>
+FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* blk_prefix, int t, int rank) {
   const GemmArgs& g = p.g;
   // last group whose tile prefix is <= t
   int lo = 0, hi = g.E - 1, e = 0;
@@ -266,7 +223,7 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
   if (!WGRAD) {
     const int mt = (int)((ge - gs + BM - 1) / BM);
     const int mp = (mt + 1) / 2;
-    const int ni = NQ * (local / mp) + pp, mi = 2 * (local % mp) + rank;   // n-major: neighbours share B tiles
+    const int ni = local / mp, mi = 2 * (local % mp) + rank;   // n-major: neighbours share B tiles
     tl.row0 = gs + (int64_t)mi * BM;
     tl.rows = (ge - tl.row0) < BM ? (ge - tl.row0) : BM;
     if (tl.rows < 0) tl.rows = 0;
@@ -277,7 +234,7 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
     tl.sf_kblk = 0;
   } else {
     const int pw = (p.m_tiles_w + 1) / 2;
-    const int ni = NQ * (local / pw) + pp, mi = 2 * (local % pw) + rank;
+    const int ni = local / pw, mi = 2 * (local % pw) + rank;
     tl.row0 = (int64_t)mi * BM;
     tl.rows = (g.rows - tl.row0) < BM ? (g.rows - tl.row0) : BM;
     if (tl.rows < 0) tl.rows = 0;
@@ -293,19 +250,14 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
   return tl;
 }
 
-template <bool MX, bool WGRAD, bool TWO, bool QUAD>
+template <bool MX, bool WGRAD, bool BIGE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_grouped_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                  const __grid_constant__ CUtensorMap tmOut, KParams p) {
-  static_assert(!QUAD || TWO, "quad mode pairs 2-CTA MMAs");
-  using L = SmemLayout<TWO>;
+  using L = SmemLayout<BIGE>;
   constexpr int STAGES = L::STAGES;
-  constexpr int CL = QUAD ? 4 : 2;          // cluster size
-  constexpr int NQ = QUAD ? 2 : 1;          // n-tiles per cluster pass
-  // MXFP8 scale copies run on their own warp (the 2-CTA leader's)
-  constexpr bool SFW = MX;
-  constexpr int B_STAGE_BYTES = L::B_STAGE_BYTES;
+  constexpr int CL = 2;  // cluster size: one pair
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem + L::a;
@@ -330,41 +282,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const GemmArgs& g = p.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int crank = (int)(blockIdx.x % CL);  // rank in the cluster
-  const int rank = crank & 1;                // rank in the pair
-  const int pp = crank >> 1;                 // pair in the cluster
-  const uint32_t lead = (uint32_t)(crank & ~1);
-  const uint16_t pair_mask = (uint16_t)(0x3u << (2 * pp));
+  const int rank = (int)(blockIdx.x % CL);  // rank in the pair
+  const uint32_t lead = 0;                  // the pair's leader issues the MMAs
+  const uint16_t pair_mask = 0x3;
 
   // ---- setup: barriers, TMEM, the device-side group schedule ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      // 1-CTA: released by the MMAs of both CTAs; 2-CTA: by the leader's MMA;
-      // quad: by both pairs' leaders (either pair writes A into this CTA)
-      mbar_init(&empty[s], TWO ? (QUAD ? 2 : 1) : 2);
+      // released by the leader's MMA commit
+      mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < STAGES; ++s) mbar_init(&sf_full[s], 1);
     mbar_init(drain_mma, 1);
     mbar_init(drain_cp, 1);
     mbar_init(tmem_full, 1);
-    // 2-CTA: the leader's accumulator is free once both CTAs' epilogues drained
-    mbar_init(tmem_empty, TWO ? 8 : 4);
+    // the leader's accumulator is free once both CTAs' epilogues drained
+    mbar_init(tmem_empty, 8);
     *abort_flag = 0;
     mbar_fence_init();
   }
   if (warp == 1) {
-    if constexpr (TWO) {
-      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                       smem_u32(tmem_base_holder)),
-                   "r"(TMEM_COLS));
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
-    } else {
-      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                       smem_u32(tmem_base_holder)),
-                   "r"(TMEM_COLS));
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_base_holder)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
     tc_fence_before();
   }
   // per-group tile counts and scale-block counts, then a scan
@@ -374,10 +315,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int64_t sz = ge - gs;
     int nt, nb;
     if (!WGRAD) {
-      nt = (int)(((sz + BM - 1) / BM + 1) / 2) * p.n_units;
+      nt = (int)(((sz + BM - 1) / BM + 1) / 2) * p.n_tiles;
       nb = (int)((sz + BM - 1) / BM);
     } else {
-      nt = ((p.m_tiles_w + 1) / 2) * p.n_units;
+      nt = ((p.m_tiles_w + 1) / 2) * p.n_tiles;
       nb = MX ? (int)((sz + 127) / 128) : (int)((sz + 31) / 32 * 32);
     }
     tiles_prefix[e + 1] = sz < 0 ? 0 : nt;
@@ -450,7 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int filled[STAGES];  // phase of each stage's last fill, -1: never filled
     for (int s = 0; s < STAGES; ++s) filled[s] = -1;
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = get_tile<WGRAD, NQ>(p, tiles_prefix, blk_prefix, t, rank, pp);
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
       for (int ks = 0; ks < tl.nk; ++ks) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
           set_status(g.status, FP8MOE_ERR_TIMEOUT);
@@ -458,9 +399,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         filled[stage] = (int)phase;
-        // 1-CTA: own A + both halves of B (one of them multicast by the peer);
-        // 2-CTA: own A + own half of B
-        uint32_t bytes = A_STAGE_BYTES + (TWO ? B_STAGE_BYTES : B_STAGE_BYTES);
+        // this CTA loads its own 128 rows of A and its own half of B
+        uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES;
         const uint8_t* sfa_src = nullptr;
         const uint8_t* sfb_src0 = nullptr;
         const uint8_t* sfb_src1 = nullptr;
@@ -470,49 +410,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const int x = (int)(tl.x0 + (int64_t)ks * BK);
         const int brow = (int)(tl.col0 + rank * (BN / 2));
-        if constexpr (TWO) {
-          // both CTAs' loads complete on the leader's full barrier, which
-          // expects the bytes of the pair (both CTAs load the same amounts)
-          const uint32_t fb = mapa_rank(smem_u32(&full[stage]), lead);
-          if (rank == 0) mbar_expect_tx(&full[stage], 2 * bytes);
-          if (QUAD) {
-            // this CTA's 64 rows of the A tile, multicast to the CTA of the
-            // other pair that holds the same rows
-            tma_load_2d_cg2_mc(sA + stage * A_STAGE_BYTES + pp * (A_STAGE_BYTES / 2), &tmA, fb, x,
-                               (int)tl.row0 + pp * (BM / 2), (uint16_t)((1u << crank) | (1u << (crank ^ 2))));
-          } else {
-            tma_load_2d_cg2(sA + stage * A_STAGE_BYTES, &tmA, fb, x, (int)tl.row0);
-          }
-          uint8_t* bdst = sB + stage * B_STAGE_BYTES;
-          if (WGRAD) {
-            tma_load_2d_cg2(bdst, &tmB, fb, x, brow);
-          } else {
-            tma_load_3d_cg2(bdst, &tmB, fb, x, brow, tl.e);
-          }
-          if (MX) {
-            // scale tiles as 1-D boxes of 128 u32 (= one 512-byte 128x4 tile)
-            const uint8_t* sa0 = (const uint8_t*)g.a_scale;
-            const uint8_t* sb0 = (const uint8_t*)g.b_scale;
-            tma_load_1d_cg2(sSFA + stage * SFA_STAGE_BYTES, &tmSFA, fb, (int)((sfa_src - sa0) / 4));
-            tma_load_1d_cg2(sSFB + stage * SFB_STAGE_BYTES, &tmSFB, fb, (int)((sfb_src0 - sb0) / 4));
-            if (sfb_src1)
-              tma_load_1d_cg2(sSFB + stage * SFB_STAGE_BYTES + 512, &tmSFB, fb, (int)((sfb_src1 - sb0) / 4));
-          }
+        // both CTAs' loads complete on the leader's full barrier, which
+        // expects the bytes of the pair (both CTAs load the same amounts)
+        const uint32_t fb = mapa_rank(smem_u32(&full[stage]), lead);
+        if (rank == 0) mbar_expect_tx(&full[stage], 2 * bytes);
+        tma_load_2d_cg2(sA + stage * A_STAGE_BYTES, &tmA, fb, x, (int)tl.row0);
+        uint8_t* bdst = sB + stage * B_STAGE_BYTES;
+        if (WGRAD) {
+          tma_load_2d_cg2(bdst, &tmB, fb, x, brow);
         } else {
-          mbar_expect_tx(&full[stage], bytes);
-          tma_load_2d(sA + stage * A_STAGE_BYTES, &tmA, &full[stage], x, (int)tl.row0);
-          // this CTA's half of the B tile goes to both CTAs of the pair
-          uint8_t* bdst = sB + stage * B_STAGE_BYTES + rank * (B_STAGE_BYTES / 2);
-          if (WGRAD) {
-            tma_load_2d_mc(bdst, &tmB, &full[stage], x, brow, 0x3);
-          } else {
-            tma_load_3d_mc(bdst, &tmB, &full[stage], x, brow, tl.e, 0x3);
-          }
-          if (MX) {
-            bulk_load(sSFA + stage * SFA_STAGE_BYTES, sfa_src, 512, &full[stage]);
-            bulk_load(sSFB + stage * SFB_STAGE_BYTES, sfb_src0, 512, &full[stage]);
-            if (sfb_src1) bulk_load(sSFB + stage * SFB_STAGE_BYTES + 512, sfb_src1, 512, &full[stage]);
-          }
+          tma_load_3d_cg2(bdst, &tmB, fb, x, brow, tl.e);
+        }
+        if (MX) {
+          // scale tiles as 1-D boxes of 128 u32 (= one 512-byte 128x4 tile)
+          const uint8_t* sa0 = (const uint8_t*)g.a_scale;
+          const uint8_t* sb0 = (const uint8_t*)g.b_scale;
+          tma_load_1d_cg2(sSFA + stage * SFA_STAGE_BYTES, &tmSFA, fb, (int)((sfa_src - sa0) / 4));
+          tma_load_1d_cg2(sSFB + stage * SFB_STAGE_BYTES, &tmSFB, fb, (int)((sfb_src0 - sb0) / 4));
+          if (sfb_src1)
+            tma_load_1d_cg2(sSFB + stage * SFB_STAGE_BYTES + 512, &tmSFB, fb, (int)((sfb_src1 - sb0) / 4));
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -534,49 +450,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     // after a timeout the stages may not have been consumed: wait (bounded)
     // until the copies in flight have landed.  A full barrier completes when
-    // every byte of its fill arrived, whoever consumes it; in a 2-CTA pair
-    // the leader's barriers count the bytes of both CTAs.
-    if (*abort_flag && (!TWO || rank == 0)) {
+    // every byte of its fill arrived, whoever consumes it; the leader's
+    // barriers count the bytes of both CTAs.
+    if (*abort_flag && rank == 0) {
       for (int s = 0; s < STAGES; ++s)
         if (filled[s] >= 0) (void)mbar_wait(&full[s], (uint32_t)filled[s], nullptr);
     }
-  } else if (warp == 1 && lane == 0 && TWO && rank == 1) {
-    // 2-CTA peer: the leader issues every MMA of the pair; nothing to do here
+  } else if (warp == 1 && lane == 0 && rank == 1) {
+    // the peer: the leader issues every MMA of the pair; nothing to do here
   } else if (warp == 1 && lane == 0) {
     // ======================= MMA issuer =======================
-    constexpr int MM = TWO ? 2 * BM : BM;
+    constexpr int MM = 2 * BM;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_phase = 0;
     auto stage_ready = [&]() -> bool {
       if (!mbar_wait(&full[stage], phase, abort_flag)) return false;
-      return !SFW || mbar_wait(&sf_full[stage], phase, abort_flag);
+      return !MX || mbar_wait(&sf_full[stage], phase, abort_flag);
     };
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = get_tile<WGRAD, NQ>(p, tiles_prefix, blk_prefix, t, rank, pp);
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
       if (tl.nk == 0) continue;
-      if (!TWO && tl.rows == 0) {
-        // phantom: release each stage for the pair without computing
-        bool ok = true;
-        for (int ks = 0; ks < tl.nk; ++ks) {
-          if (!stage_ready()) {
-            set_status(g.status, FP8MOE_ERR_TIMEOUT);
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          tc_commit_mc(&empty[stage], pair_mask);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (!ok) break;
-        continue;
-      }
-      const bool acc_ok = TWO ? mbar_wait_cluster(tmem_empty, acc_phase ^ 1, abort_flag)
-                              : mbar_wait(tmem_empty, acc_phase ^ 1, abort_flag);
-      if (!acc_ok) {
+      if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, abort_flag)) {
         set_status(g.status, FP8MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
@@ -595,20 +490,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t a_addr = smem_u32(sA + stage * A_STAGE_BYTES);
         const uint32_t b_addr = smem_u32(sB + stage * B_STAGE_BYTES);
         const uint32_t sf_col = tmem_base + TMEM_SF_BASE + stage * 16;
-        if (MX && !SFW) {
-          tc_cp_sf<TWO>(sf_col, sdesc_sf(smem_u32(sSFA + stage * SFA_STAGE_BYTES)));
-          tc_cp_sf<TWO>(sf_col + 4, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES)));
-          tc_cp_sf<TWO>(sf_col + 8, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES + 512)));
-        }
         const int64_t rem = tl.kvalid - (int64_t)ks * BK;
         const uint64_t adesc = sdesc_sw128(a_addr), bdesc = sdesc_sw128(b_addr);
         auto issue = [&](int k) {
           const uint32_t accum = (ks > 0 || k > 0) ? 1u : 0u;
           if (MX) {
-            mma_mx<TWO>(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_mx<MM>((uint32_t)k),
+            mma_mx(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_mx<MM>((uint32_t)k),
                         sf_col, sf_col + 4, accum);
           } else {
-            mma_f8<TWO>(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8<MM>(), accum);
+            mma_f8<true>(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8<MM>(), accum);
           }
         };
         // Full stages issue their four K=32 MMAs as straight-line code: behind a
@@ -624,7 +514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int k = 0; k < 4; ++k)
             if (k < nsub) issue(k);
         }
-        tc_commit_pair<TWO>(&empty[stage], QUAD ? (uint16_t)0xF : pair_mask);
+        tc_commit_pair(&empty[stage], pair_mask);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1;
@@ -634,14 +524,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // test hook: the first tile of the first cluster never hands over its
       // accumulator, so the epilogue's bounded wait runs out
       if (p.stall_test && t == pair && pair == 0) continue;
-      if constexpr (TWO) {
-        tc_commit_pair<true>(tmem_full, pair_mask);
-      } else {
-        tc_commit(tmem_full);
-      }
+      tc_commit_pair(tmem_full, pair_mask);
     }
     // every MMA this thread issued has completed before TMEM is released
-    tc_commit_local<TWO>(drain_mma);
+    tc_commit_local(drain_mma);
     if (!mbar_wait(drain_mma, 0, nullptr)) set_status(g.status, FP8MOE_ERR_TIMEOUT);
   } else if (warp == 6) {
     // ======================= scale copier =======================
@@ -649,11 +535,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // completed: the producer refilled the stage only after that release, and
     // the copies wait for the refill.  Phantom tiles copy nothing but still
     // complete sf_full, so that its phase follows full.
-    if (SFW && lane == 0 && (!TWO || rank == 0)) {
+    if (MX && lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-        const Tile tl = get_tile<WGRAD, NQ>(p, tiles_prefix, blk_prefix, t, rank, pp);
+        const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
         bool ok = true;
         for (int ks = 0; ks < tl.nk; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
@@ -663,14 +549,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          // (a 2-CTA pair computes both halves even when one is a phantom)
-          if (TWO || tl.rows > 0) {
-            const uint32_t sf_col = tmem_base + TMEM_SF_BASE + stage * 16;
-            tc_cp_sf<TWO>(sf_col, sdesc_sf(smem_u32(sSFA + stage * SFA_STAGE_BYTES)));
-            tc_cp_sf<TWO>(sf_col + 4, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES)));
-            tc_cp_sf<TWO>(sf_col + 8, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES + 512)));
-          }
-          tc_commit_local<TWO>(&sf_full[stage]);
+          // (the pair computes both halves even when one is a phantom)
+          const uint32_t sf_col = tmem_base + TMEM_SF_BASE + stage * 16;
+          tc_cp_sf(sf_col, sdesc_sf(smem_u32(sSFA + stage * SFA_STAGE_BYTES)));
+          tc_cp_sf(sf_col + 4, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES)));
+          tc_cp_sf(sf_col + 8, sdesc_sf(smem_u32(sSFB + stage * SFB_STAGE_BYTES + 512)));
+          tc_commit_local(&sf_full[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -679,7 +563,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
       }
       // every scale copy this thread issued has completed
-      tc_commit_local<TWO>(drain_cp);
+      tc_commit_local(drain_cp);
       if (!mbar_wait(drain_cp, 0, nullptr)) set_status(g.status, FP8MOE_ERR_TIMEOUT);
     }
   } else if (warp >= 2) {
@@ -692,7 +576,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (TWO && rank == 1) {
+        if (rank == 1) {
           mbar_arrive_remote(tmem_empty, lead);
         } else {
           mbar_arrive(tmem_empty);
@@ -700,8 +584,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     };
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = get_tile<WGRAD, NQ>(p, tiles_prefix, blk_prefix, t, rank, pp);
-      if (!TWO && tl.rows == 0) continue;  // phantom of a 1-CTA pair: nothing computed
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
       const int64_t lrow = quarter * 32 + lane;
       const bool row_ok = lrow < tl.rows;
       const int64_t ncols = (g.cols - tl.col0) < BN ? (g.cols - tl.col0) : BN;
@@ -738,7 +621,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       acc_phase ^= 1;
       tc_fence_after();
-      if (tl.rows == 0) {  // 2-CTA phantom half: nothing to store
+      if (tl.rows == 0) {  // phantom half: nothing to store
         release_acc();
         continue;
       }
@@ -824,11 +707,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    if constexpr (TWO) {
-      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
-    } else {
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
-    }
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
   }
 }
 
@@ -840,13 +719,18 @@ static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_
   return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, rank, dims, strides, box);
 }
 
-template <bool MX, bool WGRAD, bool TWO, bool QUAD>
+// One-shot test hook: armed by fp8moe_testing_stall_next_gemm, consumed by
+// the next grouped GEMM launch of the process.
+static std::atomic<int> g_stall_next{0};
+void arm_gemm_stall_hook() { g_stall_next.store(1, std::memory_order_relaxed); }
+
+template <bool MX, bool WGRAD, bool BIGE>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                             const CUtensorMap& tsb, const CUtensorMap& tout, const KParams& p, int64_t units,
                             cudaStream_t st) {
-  auto kern = k_grouped_mm<MX, WGRAD, TWO, QUAD>;
-  constexpr int CL = QUAD ? 4 : 2;
-  constexpr int SMEM = smem_bytes<TWO>();
+  auto kern = k_grouped_mm<MX, WGRAD, BIGE>;
+  constexpr int CL = 2;
+  constexpr int SMEM = smem_bytes<BIGE>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -861,21 +745,22 @@ static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // persistent grid: as many clusters as can be resident at once (4-CTA
-  // clusters of this size fit on fewer SMs than pairs do)
+  // persistent grid: as many pairs as can be resident at once on this device
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  static int max_clusters[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_clusters[dev] <= 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess || n <= 0) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> max_clusters[kMaxDev] = {};
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  int ncl = max_clusters[dev].load(std::memory_order_relaxed);
+  if (ncl <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&ncl, (void*)kern, &cfg) != cudaSuccess || ncl <= 0) {
       (void)cudaGetLastError();
-      n = p.g.num_sms / CL;
+      ncl = p.g.num_sms / CL;
     }
-    max_clusters[dev] = n > 0 ? n : 1;
+    if (ncl < 1) ncl = 1;
+    max_clusters[dev].store(ncl, std::memory_order_relaxed);
   }
-  int64_t nclu = units < max_clusters[dev] ? units : max_clusters[dev];
+  int64_t nclu = units < ncl ? units : ncl;
   if (nclu < 1) nclu = 1;
   cfg.gridDim = dim3((unsigned)(CL * nclu));
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, tsa, tsb, tout, p);
@@ -884,36 +769,16 @@ static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const 
 cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   if (g.E > MAX_GROUPS) return cudaErrorNotSupported;
   if (g.kk > INT32_MAX || g.rows > INT32_MAX || g.cols > INT32_MAX || g.M > INT32_MAX) return cudaErrorInvalidValue;
-  if (smem_bytes<true>() > g.max_smem || smem_bytes<false>() > g.max_smem) return cudaErrorNotSupported;
   const bool mx = g.recipe == FP8MOE_MXFP8;
   const bool wgrad = g.mode == GEMM_WGRAD;
-  // Pair modes.  Default: cta_group::2 MMAs (M = 256 per pair, 6-deep ring)
-  // in 2-CTA clusters.  FP8MOE_GEMM_CLUSTER=4 groups two pairs into a 4-CTA
-  // cluster that takes adjacent n-tiles and shares the A tile by multicast
-  // (24 KB loaded per SM and k-stage instead of 32); on the Scout shapes it
-  // measured slower (2,547 against 2,652 TFLOP/s fwd: the loads were not
-  // bandwidth-bound, and 4-CTA clusters fit on 144 of the 152 SMs).
-  // FP8MOE_GEMM_1CTA=1 selects 1-CTA MMAs with B multicast inside a pair,
-  // which also serves E > 512.
-  static const bool want_two = [] {
-    const char* v = getenv("FP8MOE_GEMM_1CTA");
-    return !(v && v[0] == '1');
-  }();
-  static const bool want_quad = [] {
-    const char* v = getenv("FP8MOE_GEMM_CLUSTER");
-    return v && v[0] == '4';
-  }();
-  const bool two = want_two && g.E <= SmemLayout<true>::MAXG;
-  const bool quad = two && want_quad;
+  // cta_group::2 pairs throughout; more than 512 groups take the variant
+  // with the larger group tables and a 5-deep ring
+  const bool bige = g.E > SmemLayout<false>::MAXG;
+  if ((bige ? smem_bytes<true>() : smem_bytes<false>()) > g.max_smem) return cudaErrorNotSupported;
   KParams p;
   p.g = g;
-  // fault-injection hook for the tests of the timeout path, read per launch
-  {
-    const char* v = getenv("FP8MOE_TEST_STALL");
-    p.stall_test = v && v[0] == '1';
-  }
+  p.stall_test = g_stall_next.exchange(0, std::memory_order_relaxed);
   p.n_tiles = (int)((g.cols + BN - 1) / BN);
-  p.n_units = quad ? (p.n_tiles + 1) / 2 : p.n_tiles;
   p.m_tiles_w = (int)((g.rows + BM - 1) / BM);
   if (!wgrad) {
     p.cpb = (g.kk / 32 + 3) / 4;
@@ -927,7 +792,7 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
     const int64_t arows = wgrad ? g.rows : g.M;
     cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)(arows > 0 ? arows : 1)};
     cuuint64_t strides[1] = {(cuuint64_t)g.kk};
-    cuuint32_t box[2] = {BK, (cuuint32_t)(quad ? BM / 2 : BM)};   // quad: each pair loads half of A
+    cuuint32_t box[2] = {BK, BM};
     if (!make_map(&ta, g.a, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   if (wgrad) {
@@ -945,9 +810,9 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   // the tile units (a unit is one pass of a cluster)
   int64_t units;
   if (!wgrad) {
-    units = ((g.M + 2 * BM - 1) / (2 * BM) + g.E) * p.n_units;
+    units = ((g.M + 2 * BM - 1) / (2 * BM) + g.E) * p.n_tiles;
   } else {
-    units = (int64_t)g.E * ((p.m_tiles_w + 1) / 2) * p.n_units;
+    units = (int64_t)g.E * ((p.m_tiles_w + 1) / 2) * p.n_tiles;
   }
   // MXFP8 scale buffers as 1-D u32 tensors (the 2-CTA producer loads scale
   // tiles with TMA so that they can complete on the leader's barrier)
@@ -989,14 +854,12 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
     }
     p.tma_out = ok ? 1 : 0;
   }
-#define FP8MOE_GMM_LAUNCH(TWO_, QUAD_)                                                                    \
-  (mx ? (wgrad ? launch_t<true, true, TWO_, QUAD_>(ta, tb, tsa, tsb, tout, p, units, st)                  \
-               : launch_t<true, false, TWO_, QUAD_>(ta, tb, tsa, tsb, tout, p, units, st))                \
-      : (wgrad ? launch_t<false, true, TWO_, QUAD_>(ta, tb, tsa, tsb, tout, p, units, st)                 \
-               : launch_t<false, false, TWO_, QUAD_>(ta, tb, tsa, tsb, tout, p, units, st)))
-  if (quad) return FP8MOE_GMM_LAUNCH(true, true);
-  if (two) return FP8MOE_GMM_LAUNCH(true, false);
-  return FP8MOE_GMM_LAUNCH(false, false);
+#define FP8MOE_GMM_LAUNCH(BIGE_)                                                                          \
+  (mx ? (wgrad ? launch_t<true, true, BIGE_>(ta, tb, tsa, tsb, tout, p, units, st)                        \
+               : launch_t<true, false, BIGE_>(ta, tb, tsa, tsb, tout, p, units, st))                      \
+      : (wgrad ? launch_t<false, true, BIGE_>(ta, tb, tsa, tsb, tout, p, units, st)                       \
+               : launch_t<false, false, BIGE_>(ta, tb, tsa, tsb, tout, p, units, st)))
+  return bige ? FP8MOE_GMM_LAUNCH(true) : FP8MOE_GMM_LAUNCH(false);
 #undef FP8MOE_GMM_LAUNCH
 }
 

@@ -3,7 +3,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace fp8moe {
+
+// Resident CTAs per SM of `kern` at `threads` threads and `smem` bytes of
+// dynamic shared memory, queried on the first call and kept in `slot`.  The
+// figure depends only on the kernel's resources and the SM architecture (one
+// per build), so one value serves every device; the relaxed atomic keeps
+// concurrent first calls from several host threads well defined.  A failed
+// query yields `fallback`.
+template <typename K>
+inline int blocks_per_sm(std::atomic<int>& slot, K kern, int threads, size_t smem, int fallback) {
+  int v = slot.load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, smem) != cudaSuccess || v < 1) {
+    (void)cudaGetLastError();
+    v = fallback;
+  }
+  slot.store(v, std::memory_order_relaxed);
+  return v;
+}
 
 // Padded geometry of one swizzled scale matrix.
 struct SwizzleGeom {
@@ -57,6 +77,8 @@ cudaError_t launch_swizzle(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, c
 
 struct GemmArgs;
 cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st);
+// arms the one-shot stall of the next grouped GEMM launch (timeout-path test)
+void arm_gemm_stall_hook();
 // blockwise-scaled grouped GEMM (blockwise_mm.cu)
 cudaError_t launch_blockwise_mm(const GemmArgs& g, cudaStream_t st);
 

@@ -185,14 +185,8 @@ cudaError_t launch_swizzle(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, c
   if (units == 0) return cudaSuccess;
   // as many CTAs as fit on the GPU at once (each unit is a load-then-store
   // round trip, so more units in flight hide more DRAM latency)
-  static int per_sm = 0;
-  if (!per_sm) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_swizzle, 256, 0) != cudaSuccess || per_sm < 1) {
-      (void)cudaGetLastError();
-      per_sm = 4;
-    }
-  }
-  const int64_t cap = (int64_t)num_sms * per_sm;
+  static std::atomic<int> per_sm{0};
+  const int64_t cap = (int64_t)num_sms * blocks_per_sm(per_sm, k_swizzle, 256, 0, 4);
   const int64_t blocks = units < cap ? units : cap;
   k_swizzle<<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();

@@ -65,23 +65,6 @@ FP8MOE_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, in
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
-// Multicast loads: the box lands at the same shared-memory offset in every CTA
-// of `mask` and completes bytes on the mbarrier at the same offset in each.
-FP8MOE_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-FP8MOE_DEV void tma_load_3d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
-                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
 // 2-SM forms: the box lands in this CTA's shared memory and completes its bytes
 // on the mbarrier at shared::cluster address `bar` (this CTA's or its peer's).
 FP8MOE_DEV void tma_load_1d_cg2(void* dst, const CUtensorMap* map, uint32_t bar, int x) {

@@ -220,11 +220,13 @@ def test_bad_offsets_set_status(F):
     assert F.fp8moe_get_device_status() == 0
 
 
-def test_many_groups_fwd(F):
-    """E = 600 groups (above the 2-CTA variant's 512-group table; the launch
-    falls back to the 1-CTA variant), many of them empty."""
-    rng = np.random.default_rng(5)
-    sizes = (rng.integers(0, 3, size=600) * 32).tolist()
+@pytest.mark.parametrize("E", [600, 1024])
+def test_many_groups_fwd(F, E):
+    """More groups than the 512-entry tables of the default variant: the
+    launch takes the variant with 1024-entry tables (a 5-deep ring, the same
+    cta_group::2 pairs); many groups are empty."""
+    rng = np.random.default_rng(5 + E)
+    sizes = (rng.integers(0, 3, size=E) * 32).tolist()
     offs = W.offsets_from_sizes(sizes)
     M, N, K = int(sum(sizes)), 256, 128
     a = _bf16((M, K), 81)
@@ -232,42 +234,72 @@ def test_many_groups_fwd(F):
     (qa, sa, qw, sw), ref, bound = mx_fwd_case(a, w, offs)
     out = F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, _d(offs))
     assert F.fp8moe_get_device_status() == 0
-    check(out, ref, bound, "mx fwd, 600 groups")
+    check(out, ref, bound, f"mx fwd, {E} groups")
 
 
-@pytest.mark.parametrize("env", [{"FP8MOE_GEMM_1CTA": "1"}, {"FP8MOE_GEMM_CLUSTER": "4"}],
-                         ids=["1cta_pairs", "2cta_quads"])
-def test_pair_mode_variants(env):
-    """The other pair modes (chosen per process: 1-CTA MMAs with B multicast,
-    or 2-CTA pairs grouped into 4-CTA clusters that share A) pass the same
-    parity cases."""
-    import os
-    import subprocess
-    import sys
-    if any(os.environ.get(k) for k in ("FP8MOE_GEMM_1CTA", "FP8MOE_GEMM_CLUSTER")):
-        pytest.skip("this process already runs a non-default variant")
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
-                        os.path.abspath(__file__), "-k", "not pair_mode_variants"],
-                       cwd=root, env=dict(os.environ, **env), capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+def test_many_groups_rowwise_fwd(F):
+    """The rowwise recipe with E = 1024 groups of odd sizes (many empty)."""
+    rng = np.random.default_rng(17)
+    sizes = rng.integers(0, 40, size=1024)
+    sizes[rng.random(1024) < 0.3] = 0
+    sizes = sizes.tolist()
+    offs = W.offsets_from_sizes(sizes)
+    M, N, K = int(sum(sizes)), 272, 144
+    a = _bf16((M, K), 83)
+    w = _bf16((len(sizes), N, K), 84, 0.05)
+    (qa, ia, qw, iw), ref, bound = rw_fwd_case(a, w, offs)
+    out = F.fp8moe_scaled_grouped_mm_fwd(F.ROWWISE, qa, ia, qw, iw, _d(offs))
+    assert F.fp8moe_get_device_status() == 0
+    check(out, ref, bound, "rowwise fwd, 1024 groups")
 
 
-def test_pipeline_wait_timeout_sets_status(F, monkeypatch):
-    """Fault injection without a GPU fault: with the FP8MOE_TEST_STALL hook the
-    first cluster never hands its first accumulator to the epilogue, whose
-    bounded wait (2 s) runs out.  The kernel reports FP8MOE_ERR_TIMEOUT; every
-    CTA waits for its own copies and MMAs before releasing TMEM, so the
-    context stays usable and the next GEMM is exact again."""
+def test_many_groups_wgrad(F):
+    """MXFP8 wgrad with 1024 groups (most empty, checked to be exactly 0)."""
+    rng = np.random.default_rng(23)
+    sizes = (rng.integers(0, 2, size=1024) * rng.integers(1, 3, size=1024) * 32).tolist()
+    offs = W.offsets_from_sizes(sizes)
+    M, N, K = int(sum(sizes)), 128, 256
+    dy = _bf16((M, N), 85)
+    a = _bf16((M, K), 86)
+    (qdyt, sdyt, qat, sat), ref, bound = mx_wgrad_case(dy, a, offs)
+    out = F.fp8moe_scaled_grouped_mm_wgrad(F.MXFP8, qdyt, sdyt, qat, sat, _d(offs), M)
+    assert F.fp8moe_get_device_status() == 0
+    check(out, ref, bound, "mx wgrad, 1024 groups")
+
+
+def test_pipeline_wait_timeout_sets_status(F):
+    """Fault injection without a GPU fault: the one-shot testing hook makes
+    the first pair of the next launch keep its first accumulator, so the
+    epilogue's bounded wait (2 s) runs out.  The kernel reports
+    FP8MOE_ERR_TIMEOUT; every CTA waits for its own copies and MMAs before
+    releasing TMEM, so the context stays usable and the next GEMM (the hook
+    is spent) is exact again."""
     offs = W.offsets_from_sizes([64, 0, 352, 32, 160])
     a = _bf16((608, 256), 91)
     w = _bf16((5, 512, 256), 92, 0.05)
     (qa, sa, qw, sw), ref, bound = mx_fwd_case(a, w, offs)
     d_offs = _d(offs)
-    monkeypatch.setenv("FP8MOE_TEST_STALL", "1")
+    F.fp8moe_testing_stall_next_gemm()
     F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, d_offs)
     assert F.fp8moe_get_device_status() == 6          # FP8MOE_ERR_TIMEOUT
-    monkeypatch.delenv("FP8MOE_TEST_STALL")
     out = F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, d_offs)
     assert F.fp8moe_get_device_status() == 0
     check(out, ref, bound, "fwd after a timed-out launch")
+
+
+def test_status_taken_on_another_stream(F):
+    """An offsets error set by a launch on one stream is read (and cleared)
+    through a status call on another stream once that stream has waited."""
+    sizes, N, K = SHAPES["tiny"]
+    offs = W.offsets_from_sizes(sizes)
+    M = int(sum(sizes))
+    a = _bf16((M, K), 93)
+    w = _bf16((len(sizes), N, K), 94, 0.05)
+    (qa, sa, qw, sw), _, _ = mx_fwd_case(a, w, offs)
+    bad = torch.tensor([96, 64, 96, 1024], dtype=torch.int32, device=DEV)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, bad, stream=s1)
+    s2.wait_stream(s1)
+    assert F.fp8moe_get_device_status(stream=s2) == 5
+    assert F.fp8moe_get_device_status(stream=s2) == 0
