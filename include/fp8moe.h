@@ -50,7 +50,8 @@ typedef enum {
   FP8MOE_ERR_UNSUPPORTED = 3,     /* e.g. e4m3fnuz with MXFP8 or with the GEMM */
   FP8MOE_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
   FP8MOE_ERR_DEVICE_OFFSETS = 5,  /* device: offsets invalid (read via get_device_status) */
-  FP8MOE_ERR_TIMEOUT = 6          /* device: a bounded pipeline wait ran out */
+  FP8MOE_ERR_TIMEOUT = 6,         /* device: a bounded pipeline wait ran out */
+  FP8MOE_ERR_SCRATCH_LIMIT = 7    /* host: the problem needs more than the static scratch */
 } fp8moe_status;
 
 typedef enum {
@@ -368,6 +369,36 @@ fp8moe_status fp8moe_route_permute(const void* x, int64_t T, int64_t H, const in
                                    fp8moe_stream_t stream);
 fp8moe_status fp8moe_route_unpermute(const void* y, int64_t T, int64_t N, const int32_t* row_of,
                                      const float* topk_w, int64_t k, void* out, fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * fp8moe_route_permute without a caller workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory when they route, such as a runtime whose device memory is
+ * planned up front into a fixed arena with no room set aside for the
+ * routing scratch, or code on a path where a cudaMalloc is not allowed
+ * (it can synchronize the device and can fail under memory pressure).
+ *
+ * Arguments, results, layouts and errors as fp8moe_route_permute, minus the
+ * workspace: the call uses the library's own scratch, a static device array
+ * of FP8MOE_ROUTE_STATIC_SCRATCH_BYTES (1 MiB) that every device loading
+ * the library holds until the process exits.  A problem whose scratch,
+ * fp8moe_route_workspace_bytes(T, k, E), exceeds it is rejected on the host
+ * with FP8MOE_ERR_SCRATCH_LIMIT before any launch (for E = 256 experts, up
+ * to about a million (token, slot) pairs fit).  The call allocates nothing:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call on a device shares the one array and leaves its
+ * contents behind; each call writes every scratch word it reads before
+ * reading it, so nothing needs to start at zero.  Calls whose work overlaps
+ * on the GPU (two streams, or two host threads) race on the array: order
+ * them on one stream, or synchronize between them.
+ * ------------------------------------------------------------------------ */
+enum { FP8MOE_ROUTE_STATIC_SCRATCH_BYTES = 1 << 20 };
+fp8moe_status fp8moe_route_permute_noalloc(const void* x, int64_t T, int64_t H, const int32_t* topk_idx,
+                                           const float* topk_w, int64_t k, int64_t E, void* a, int32_t* offs,
+                                           int32_t* row_of, fp8moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Device status.  After the work already queued on `stream`, takes the

@@ -19,7 +19,8 @@ __all__ = [
     "Fp8MoeError", "lib", "library_path", "SYMBOLS",
     "fp8moe_quantize_rowwise", "fp8moe_quantize_colwise_3d", "fp8moe_quantize_tensorwise",
     "fp8moe_jagged_t_cols", "fp8moe_route_rows", "fp8moe_route_workspace_bytes",
-    "fp8moe_route_permute", "fp8moe_route_unpermute",
+    "fp8moe_route_permute", "fp8moe_route_unpermute", "fp8moe_route_permute_noalloc",
+    "ROUTE_STATIC_SCRATCH_BYTES",
     "fp8moe_mxfp8_quantize_dim0", "fp8moe_mxfp8_quantize_dim1", "fp8moe_mxfp8_quantize_dual",
     "fp8moe_swizzled_scales_bytes", "fp8moe_swizzle_scales_128x4",
     "fp8moe_scaled_grouped_mm_fwd", "fp8moe_scaled_grouped_mm_dgrad",
@@ -33,6 +34,7 @@ __all__ = [
 E4M3FN, E4M3FNUZ = 0, 1
 ROWWISE, MXFP8, TENSORWISE, BLOCKWISE = 0, 1, 2, 3
 SCALES_ROWMAJOR, NO_GROUPS, GROUP_ROWS, GROUP_COLS = -2, -1, 0, 1
+ROUTE_STATIC_SCRATCH_BYTES = 1 << 20   # the static scratch of fp8moe_route_permute_noalloc
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(HERE, "libfp8moe.so")
@@ -49,6 +51,7 @@ SYMBOLS = {
     "fp8moe_route_workspace_bytes": (_i64, [_i64, _i64, _i64]),
     "fp8moe_route_permute": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _vp]),
     "fp8moe_route_unpermute": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp]),
+    "fp8moe_route_permute_noalloc": (_i32, [_vp, _i64, _i64, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp]),
     "fp8moe_mxfp8_quantize_dim0": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "fp8moe_mxfp8_quantize_dim1": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "fp8moe_mxfp8_quantize_dual": (_i32, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i32, _vp, _vp, _i32, _vp]),
@@ -227,6 +230,25 @@ def fp8moe_route_permute(x, topk_idx, E: int, topk_w=None, a=None, offs=None, ro
     _check("fp8moe_route_permute", _lib_raw().fp8moe_route_permute(
         _ptr(x), T, H, _ptr(topk_idx), _ptr(topk_w), k, E, _ptr(a), _ptr(offs), _ptr(row_of),
         _ptr(workspace), workspace.numel(), _stream(stream)))
+    return a, offs, row_of
+
+
+def fp8moe_route_permute_noalloc(x, topk_idx, E: int, topk_w=None, a=None, offs=None, row_of=None,
+                                 stream=None):
+    """fp8moe_route_permute without a workspace: the library routes through
+    its own static 1 MiB device scratch, so the C call allocates nothing.
+    For callers that cannot allocate device memory at routing time, pass
+    preallocated ``a``, ``offs`` and ``row_of`` as well.  Calls that overlap
+    on the GPU share the scratch and race."""
+    torch = _torch()
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    rows = fp8moe_route_rows(T, k, E)
+    a = _empty((rows, H), torch.bfloat16, x) if a is None else a
+    offs = _empty((E,), torch.int32, x) if offs is None else offs
+    row_of = _empty((T, k), torch.int32, x) if row_of is None else row_of
+    _check("fp8moe_route_permute_noalloc", _lib_raw().fp8moe_route_permute_noalloc(
+        _ptr(x), T, H, _ptr(topk_idx), _ptr(topk_w), k, E, _ptr(a), _ptr(offs), _ptr(row_of), _stream(stream)))
     return a, offs, row_of
 
 

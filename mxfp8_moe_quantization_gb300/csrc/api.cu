@@ -66,6 +66,7 @@ const char* fp8moe_status_string(int s) {
     case FP8MOE_ERR_CUDA: return "CUDA error";
     case FP8MOE_ERR_DEVICE_OFFSETS: return "invalid routing offsets (device)";
     case FP8MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case FP8MOE_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the library's static array holds";
     default: return "unknown status";
   }
 }
@@ -372,6 +373,27 @@ fp8moe_status fp8moe_route_permute(const void* x, int64_t T, int64_t H, const in
   if (st) return st;
   return cuda_result(fp8moe::launch_route_permute(x, T, H, topk_idx, topk_w, k, E, fp8moe_route_rows(T, k, E), a,
                                                   offs, row_of, workspace, d->num_sms, d->status,
+                                                  (cudaStream_t)stream));
+}
+
+fp8moe_status fp8moe_route_permute_noalloc(const void* x, int64_t T, int64_t H, const int32_t* topk_idx,
+                                           const float* topk_w, int64_t k, int64_t E, void* a, int32_t* offs,
+                                           int32_t* row_of, fp8moe_stream_t stream) {
+  if (T < 0 || H < 0 || k < 1 || E < 1 || E > 1024) return FP8MOE_ERR_INVALID_ARG;
+  if (T * k > ((int64_t)1 << 30)) return FP8MOE_ERR_INVALID_ARG;
+  // the scratch this problem needs must fit the library's static array
+  if (fp8moe::route_workspace_bytes(T, k, E) > fp8moe::route_static_scratch_bytes()) return FP8MOE_ERR_SCRATCH_LIMIT;
+  if (!a || !offs || (T > 0 && (!x || !topk_idx || !row_of))) return FP8MOE_ERR_INVALID_ARG;
+  if (H % 8 || (x && !al16(x)) || !al16(a)) return FP8MOE_ERR_ALIGNMENT;
+  if (((uintptr_t)topk_idx | (uintptr_t)offs | (uintptr_t)row_of | (uintptr_t)topk_w) & 3)
+    return FP8MOE_ERR_ALIGNMENT;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  void* scratch = nullptr;
+  if (fp8moe::route_static_scratch(&scratch) != cudaSuccess) return FP8MOE_ERR_CUDA;
+  return cuda_result(fp8moe::launch_route_permute(x, T, H, topk_idx, topk_w, k, E, fp8moe_route_rows(T, k, E), a,
+                                                  offs, row_of, scratch, d->num_sms, d->status,
                                                   (cudaStream_t)stream));
 }
 

@@ -69,6 +69,10 @@ int64_t route_workspace_bytes(int64_t T, int64_t k, int64_t E);
 cudaError_t launch_route_permute(const void* x, int64_t T, int64_t H, const int32_t* idx, const float* w, int64_t k,
                                  int64_t E, int64_t rows, void* a, int32_t* offs, int32_t* row_of, void* workspace,
                                  int num_sms, int* status, cudaStream_t st);
+// the static scratch of the no-allocation permute: its size, and its device
+// address on the current device (looked up on the first call per device)
+int64_t route_static_scratch_bytes();
+cudaError_t route_static_scratch(void** out);
 cudaError_t launch_route_unpermute(const void* y, int64_t N, const int32_t* row_of, const float* w, int64_t T,
                                    int64_t k, void* out, cudaStream_t st);
 cudaError_t launch_swizzle(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, const int32_t* offs,

@@ -17,10 +17,20 @@
 //      16-byte accesses, optionally weighted (bf16(fp32(w) * x)), and the
 //      padding rows of every group (and the slack of the last one) zeroed.
 // Unpermute: one warp per token sums its k rows in slot order in fp32.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
 namespace fp8moe {
+
+// Scratch of the routing permute for callers that cannot allocate device
+// memory (fp8moe_route_permute_noalloc): a file-scope device array that every
+// device loading the library holds until the process exits.  Its size is
+// ROUTE_STATIC_SCRATCH_BYTES (1 MiB, declared in include/fp8moe.h as
+// FP8MOE_ROUTE_STATIC_SCRATCH_BYTES); all calls on a device share it.
+constexpr int64_t ROUTE_STATIC_SCRATCH_BYTES = FP8MOE_ROUTE_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) int32_t g_route_scratch[ROUTE_STATIC_SCRATCH_BYTES / 4];
 
 namespace {
 
@@ -252,6 +262,30 @@ cudaError_t launch_route_permute(const void* x, int64_t T, int64_t H, const int3
   k_route_copy<<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)x, H, w, n, (int)k, (int)E, row_of, real_end,
                                                  pad_prefix, (uint16_t*)a);
   return cudaGetLastError();
+}
+
+int64_t route_static_scratch_bytes() { return ROUTE_STATIC_SCRATCH_BYTES; }
+
+// Device address of g_route_scratch on the current device.  Host code only
+// holds a stand-in for the array's name, so the address is looked up once
+// per device (with that device current) and cached.
+cudaError_t route_static_scratch(void** out) {
+  constexpr int kMaxDev = 128;
+  static std::mutex mu;
+  static void* addr[kMaxDev] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_route_unpermute(const void* y, int64_t N, const int32_t* row_of, const float* w, int64_t T,
