@@ -37,9 +37,9 @@ METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMM
-# kernel, averaged over one fwd, dgrad and wgrad launch of the Scout layer,
-# from the ncu capture summarised in profiles/k_grouped_mm_scout.md.  It is
-# reported only while the kernel source is the one that was captured.
+# kernel per launch, averaged over one fwd, dgrad and wgrad launch of the Scout
+# W1 layer, from an ncu capture of those two counters.  It is reported only
+# while the kernel source is the one that was captured (same SHA-256).
 GEMM_TRAFFIC = {"source": "mxfp8_moe_quantization_gb300/csrc/grouped_mm.cu",
                 "sha256": "547c6b0dc0b06e00eea7d43a215ce467c060a82952e29dd59eeb02341b4c512b",
                 "bytes_per_launch": (1030.651e6 + 1077.764e6 + 1563.850e6) / 3}
@@ -326,29 +326,154 @@ def run_e2e(F, sets, steps, warmup, stream_weights=False):
 
 
 # ----------------------------------------------------------------------------
+# DeepSeek-V3 layer: HBM-bound GEMMs and the standalone weight quantization
+# ----------------------------------------------------------------------------
+def dsv3_measure(F, dev, iters=5, warmup=2):
+    """The DeepSeek-V3-shaped MoE layer (256 experts, 7168 -> 2048, 36,448
+    routed rows, Zipf-skewed loads with empty experts), measured the way the
+    Scout step is (CUDA events around every launch on the launching stream,
+    inputs larger than L2): the standalone MXFP8 quantization of all expert
+    weights (W1 [256,2048,7168] and W2 [256,7168,2048], both directions, one
+    launch each) and the MXFP8 grouped GEMM forward, dgrad and wgrad of both
+    weights.  Every GEMM here is bound by HBM (arithmetic intensity 123-235
+    FLOP/B against a ridge near 570), so each is reported against the
+    measured copy bandwidth with its algorithmic bytes: fp8 codes and e8m0
+    scales of both operands (the weights of experts with tokens) plus the
+    bf16 output (wgrad: every expert's dW)."""
+    import torch
+    import workloads as W
+    wl = W.get_workload("dsv3")
+    offs = torch.from_numpy(wl.offs()).to(dev)
+    M, E = wl.M, wl.E
+    real = wl.group_plan()[0]
+    T, live = int(real.sum()), int((real > 0).sum())
+    stream = torch.cuda.current_stream()
+    layers = []
+    for wname, aname, dname in [("W1", "A", "dY"), ("W2", "A2", "dY2")]:
+        w = W.make_weights(wl, wname, device=dev)
+        a = W.make_activations(wl, aname, device=dev)
+        dy = W.make_activations(wl, dname, device=dev)
+        _, N, K = w.shape
+        qw, sw, qwt, swt = F.fp8moe_mxfp8_quantize_dual(w, None, F.NO_GROUPS, F.NO_GROUPS)
+        qa, sa, qat, sat = F.fp8moe_mxfp8_quantize_dual(a, offs, F.GROUP_ROWS, F.GROUP_COLS)
+        qdy, sdy, qdyt, sdyt = F.fp8moe_mxfp8_quantize_dual(dy, offs, F.GROUP_ROWS, F.GROUP_COLS)
+        del a, dy
+        L = dict(name=wname, N=N, K=K, w=w, qw=qw, sw=sw, qwt=qwt, swt=swt, qa=qa, sa=sa, qat=qat, sat=sat,
+                 qdy=qdy, sdy=sdy, qdyt=qdyt, sdyt=sdyt,
+                 out=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+                 da=torch.empty(M, K, dtype=torch.bfloat16, device=dev),
+                 dw=torch.empty(E, N, K, dtype=torch.bfloat16, device=dev))
+        layers.append(L)
+    # launches of one pass, with their algorithmic bytes and flops
+    c = 1 + 1 / 32                          # an fp8 code and its share of an e8m0 scale
+    runs = []
+    for L in layers:
+        N, K = L["N"], L["K"]
+        fl = 2.0 * T * N * K
+        runs.append((f"{L['name']}_weight_quant", L["w"].numel() * (4 + 2 / 32), 0.0,
+                     lambda L=L: F.fp8moe_mxfp8_quantize_dual(L["w"], None, F.NO_GROUPS, F.NO_GROUPS, q0=L["qw"],
+                                                              s0=L["sw"], q1=L["qwt"], s1=L["swt"])))
+        runs.append((f"{L['name']}_fwd", (M * K + live * N * K) * c + M * N * 2, fl,
+                     lambda L=L: F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, L["qa"], L["sa"], L["qw"], L["sw"], offs,
+                                                                out=L["out"])))
+        runs.append((f"{L['name']}_dgrad", (M * N + live * N * K) * c + M * K * 2, fl,
+                     lambda L=L: F.fp8moe_scaled_grouped_mm_dgrad(F.MXFP8, L["qdy"], L["sdy"], L["qwt"], L["swt"],
+                                                                  offs, out=L["da"])))
+        runs.append((f"{L['name']}_wgrad", (N + K) * M * c + E * N * K * 2, fl,
+                     lambda L=L: F.fp8moe_scaled_grouped_mm_wgrad(F.MXFP8, L["qdyt"], L["sdyt"], L["qat"], L["sat"],
+                                                                  offs, M, out=L["dw"])))
+    for _ in range(warmup):
+        for _, _, _, fn in runs:
+            fn()
+    torch.cuda.synchronize()
+    assert F.fp8moe_get_device_status() == 0
+    evs = {name: [] for name, _, _, _ in runs}
+    for _ in range(iters):
+        for name, _, _, fn in runs:
+            s0 = torch.cuda.Event(enable_timing=True)
+            e0 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            fn()
+            e0.record(stream)
+            evs[name].append((s0, e0))
+    torch.cuda.synchronize()
+    assert F.fp8moe_get_device_status() == 0
+    peaks, _ = load_peaks()
+    hbm, fp8 = peaks["hbm_gbs"], 2.0 * peaks["bf16_tflops"]
+    res = {}
+    for name, nbytes, fl, _ in runs:
+        ms = sum(s0.elapsed_time(e0) for s0, e0 in evs[name]) / iters
+        d = {"us": ms * 1e3, "gbs": nbytes / ms / 1e6, "frac_hbm": nbytes / ms / 1e6 / hbm}
+        if fl:
+            d["tflops"] = fl / ms / 1e9
+            d["frac_fp8_peak"] = fl / ms / 1e9 / fp8
+        res[name] = d
+    q_bytes = sum(nb for name, nb, _, _ in runs if name.endswith("weight_quant"))
+    q_ms = sum(res[n]["us"] for n in res if n.endswith("weight_quant")) / 1e3
+    out = {
+        "dsv3_gemm_frac_hbm": {L["name"]: {m: round(res[f"{L['name']}_{m}"]["frac_hbm"], 4)
+                                           for m in ("fwd", "dgrad", "wgrad")} for L in layers},
+        "dsv3_weight_quant_gbs": q_bytes / q_ms / 1e6,
+        "dsv3_weight_quant_frac_hbm": q_bytes / q_ms / 1e6 / hbm,
+        "dsv3": {"workload": f"dsv3: {wl.description}", "routed_rows_padded": M, "real_tokens_x_topk": T,
+                 "experts_with_tokens": live, "launches": res, "launches_per_pass": len(runs),
+                 "passes": iters, "bound": "hbm"},
+    }
+    del layers, runs
+    torch.cuda.empty_cache()
+    return out, len(evs) * iters
+
+
+# ----------------------------------------------------------------------------
 # CPU baseline: the oracle, as it stands, on a bounded sample
 # ----------------------------------------------------------------------------
-def cpu_baseline(wl, budget_s=20.0):
-    """Time the oracle's MXFP8 quantization and float64 grouped GEMM on a slice
-    of the workload and scale to one step's work."""
+def oracle_sample_step(wl):
+    """A fixed fraction of one step of the workload for the CPU oracle: the
+    MXFP8 quantization of a slice of the routed activations (both directions)
+    and a float64 grouped GEMM forward on a slice of one expert, sized so that
+    their elements and flops stand in the step's own proportion.  Returns
+    (fraction, the callable step, a description)."""
     import numpy as np
     from oracle import quant as OQ, grouped_mm as OG
-    rng = np.random.default_rng(0)
-    # quantization rate (elements / s) on a 2048 x 5120 slice
-    x = rng.standard_normal((2048, 5120)).astype(np.float32)
-    t0 = time.perf_counter()
-    OQ.mxfp8_quantize_dim0(x)
-    q_rate = x.size / (time.perf_counter() - t0)
-    # GEMM rate (flop / s) on one group of 256 rows against a 512 x 5120 slice
-    a = rng.standard_normal((256, 5120))
-    w = rng.standard_normal((1, 512, 5120))
+    import workloads as W
+    T = int(wl.group_plan()[0].sum())
+    M = wl.M
+    step_flops = sum(3 * 2.0 * T * n * k for n, k in [(wl.N, wl.K), (wl.K, wl.N)])
+    step_elems = sum(2 * (M * k + wl.E * n * k + M * n) for n, k in [(wl.N, wl.K), (wl.K, wl.N)])
+    rows_q = 256                                    # quantized rows of K columns, both directions
+    frac = 2.0 * rows_q * wl.K / step_elems
+    gemm_flops = frac * step_flops
+    rows_g = 256
+    cols_g = max(16, int(round(gemm_flops / (2.0 * rows_g * wl.K) / 16)) * 16)
+    frac_g = 2.0 * rows_g * cols_g * wl.K / step_flops
+    frac = 0.5 * (frac + frac_g)                    # the two parts' fractions agree to within rounding
+    x = W.make_activations(wl, "A").float().numpy()[:rows_q]
+    a = x[:rows_g].astype(np.float64)
+    w = (np.random.default_rng(0).standard_normal((1, cols_g, wl.K)) * 0.02)
+
+    def step():
+        OQ.mxfp8_quantize_dim0(x)
+        OQ.mxfp8_quantize_dim1(x)
+        OG.grouped_mm_fwd(a, w, np.array([rows_g]))
+
+    desc = (f"oracle: mxfp8_quantize_dim0 + dim1 of A[:{rows_q}] ([{rows_q},{wl.K}]) and float64 grouped_mm_fwd "
+            f"{rows_g}x{cols_g}x{wl.K}; {frac:.3g} of one step's quantized elements and GEMM flops")
+    return frac, step, desc
+
+
+def cpu_baseline(wl, budget_s=20.0):
+    """The oracle's step rate (GEMM flops of the step / time) from sample
+    steps run for about ``budget_s`` seconds; (TFLOP/s, description)."""
+    frac, step, desc = oracle_sample_step(wl)
+    step_flops = sum(3 * 2.0 * int(wl.group_plan()[0].sum()) * n * k for n, k in [(wl.N, wl.K), (wl.K, wl.N)])
+    step()
     t0 = time.perf_counter()
     reps = 0
-    while time.perf_counter() - t0 < max(1.0, budget_s / 4) and reps < 50:
-        OG.grouped_mm_fwd(a, w, np.array([256]))
+    while time.perf_counter() - t0 < budget_s and reps < 200:
+        step()
         reps += 1
-    g_rate = reps * 2.0 * 256 * 512 * 5120 / (time.perf_counter() - t0)
-    return q_rate, g_rate, "oracle mxfp8_quantize_dim0 on 2048x5120 and fp64 grouped_mm_fwd on 256x512x5120"
+    dt = (time.perf_counter() - t0) / reps
+    return frac * step_flops / dt / 1e12, desc + f"; {reps} sample steps"
 
 
 # ----------------------------------------------------------------------------
@@ -629,6 +754,7 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="separate dim0 / dim1 / swizzle launches instead of the fused dual-direction kernel")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-dsv3", action="store_true", help="skip the DeepSeek-V3 layer measurements")
     ap.add_argument("--only", default=None,
                     help="with --rows: comma-separated sections (rowwise, colwise, tensorwise, mx, swizzle, gemm, "
                          "layer, blockwise, routing)")
@@ -643,22 +769,30 @@ def main():
     wl = W.get_workload(WORKLOAD)
 
     if args.impl == "reference":
-        # the reference arm is the CPU oracle (the pages ship no runnable code)
+        # the reference arm is the CPU oracle (the pages ship no runnable
+        # code): every step runs the oracle on the same fixed fraction of one
+        # Scout step (its quantization and its GEMM work in the step's
+        # proportion), so the rate is measured, not projected
         if rank != 0:
             return
-        q_rate, g_rate, sample = cpu_baseline(wl)
-        import numpy as np
+        frac, sample_step, sample = oracle_sample_step(wl)
         step_flops = sum(3 * 2.0 * int(wl.group_plan()[0].sum()) * n * k
                          for n, k in [(wl.N, wl.K), (wl.K, wl.N)])
-        M = wl.M
-        elems = sum(2 * M * k + 2 * wl.E * n * k + 2 * M * n for n, k in [(wl.N, wl.K), (wl.K, wl.N)])
-        t_step = elems / q_rate + step_flops / g_rate
-        val = step_flops / t_step / 1e12
+        for _ in range(args.warmup):
+            sample_step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            sample_step()
+        t_sample = (time.perf_counter() - t0) / args.steps
+        val = frac * step_flops / t_sample / 1e12
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_sample * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{wl.name}: {wl.description}"},
+            "config": {"workload": f"{wl.name}: {wl.description}", "step": sample,
+                       "step_fraction_of_workload_step": frac},
+            "extrapolated": False,
+            "full_step_ms_estimate": t_sample / frac * 1e3,
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -743,12 +877,11 @@ def main():
         e2e_ws = {"value": job_tflops(flops, world, dt * 1e3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                   "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
                   "moves": "A, W, dY in; out, dA, dW back"}
+    extra, extra_launches = ({}, 0) if args.no_dsv3 else dsv3_measure(F, dev)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        q_rate, g_rate, sample = cpu_baseline(wl)
-        t_cpu = step.quant_elements() / q_rate + flops / g_rate
-        cpu = {"value": flops / t_cpu / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": sample, "ms_per_step_extrapolated": t_cpu * 1e3}
+        rate, sample = cpu_baseline(wl)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle", "sample": sample}
 
     if rank == 0:
         print(json.dumps({
@@ -773,6 +906,8 @@ def main():
             "e2e_weights_streamed": e2e_ws,
             "cpu_baseline": cpu,
             "gpu_launches": step.launches_per_step * args.steps,
+            **extra,
+            "gpu_launches_dsv3": extra_launches,
         }))
     if pg:
         pg.destroy_process_group()

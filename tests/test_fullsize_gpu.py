@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import workloads as W
-from oracle import formats as OF, quant as OQ
+from oracle import formats as OF, quant as OQ, swizzle as OS
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -59,16 +59,66 @@ def _sample_rows(offs, rng, per_group=2):
     return np.array(sorted(set(rows)))
 
 
+# the operands of each expert weight: (activation, gradient, weight); W1
+# [E, N, K] takes A [M, K] and dY [M, N]; W2 [E, K, N] takes A2 [M, N] and
+# dY2 [M, K]
+OPERANDS = {"W1": ("A", "dY", "W1"), "W2": ("A2", "dY2", "W2")}
+
+
+def _layer(wl, which, dev):
+    an, dn, wn = OPERANDS[which]
+    a = W.make_activations(wl, an, device=dev)
+    dy = W.make_activations(wl, dn, device=dev)
+    w = W.make_weights(wl, wn, device=dev)
+    return a, dy, w
+
+
+def _swz_rows_bytes(buf, offs_np, rows, ncols, E):
+    """Bytes of a row-grouped swizzled scale buffer (GROUP_ROWS) at the
+    given rows, all ``ncols`` scale columns: [len(rows), ncols]."""
+    R = int(offs_np[-1])
+    _, Cp = OS.swizzled_shape(R, ncols, E, OS.GROUP_ROWS)
+    starts, ends = OQ.group_bounds(offs_np)
+    P = OQ.padded_starts(offs_np, 128)
+    g = np.searchsorted(ends, rows, side="right")
+    prow = P[g] + (rows - starts[g])
+    o = OS.tile_offset(prow[:, None], np.arange(ncols)[None, :], Cp)
+    return buf.cpu().numpy()[o]
+
+
+def _swz_cols_bytes(buf, offs_np, rows, nscols, E):
+    """Bytes of a column-grouped swizzled scale buffer (GROUP_COLS, offsets
+    over the contracting elements) at the given rows, every real scale
+    column: [len(rows), nscols]."""
+    _, Cp = OS.swizzled_shape(len(rows), nscols, E, OS.GROUP_COLS)
+    sc = np.asarray(offs_np, dtype=np.int64) // 32
+    starts, ends = OQ.group_bounds(sc)
+    Q = OQ.padded_starts(sc, 4)
+    cols = np.arange(nscols)
+    g = np.searchsorted(ends, cols, side="right")
+    pcol = Q[g] + (cols - starts[g])
+    o = OS.tile_offset(np.asarray(rows)[:, None], pcol[None, :], Cp)
+    return buf.cpu().numpy()[o]
+
+
+def _swz_batch_bytes(buf, R, ncols, b, rows):
+    """Bytes of batch ``b`` of a plain per-batch swizzled buffer (NO_GROUPS)
+    at the given rows: [len(rows), ncols]."""
+    Rp, Cp = OS.swizzled_shape(R, ncols)
+    o = b * Rp * Cp + OS.tile_offset(np.asarray(rows)[:, None], np.arange(ncols)[None, :], Cp)
+    return buf.cpu().numpy()[o]
+
+
+@pytest.mark.parametrize("which", ["W1", "W2"])
 @pytest.mark.parametrize("name", ["scout", "dsv3"])
-def test_mxfp8_fullsize(F, name):
+def test_mxfp8_fullsize(F, name, which):
     wl = W.get_workload(name)
     rng = np.random.default_rng(7)
-    M, E, N, K = wl.M, wl.E, wl.N, wl.K
+    a, dy, w = _layer(wl, which, DEV)
+    M = wl.M
+    E, N, K = w.shape                       # this weight's GEMM: [M, K] x [E, N, K]^T
     offs_np = wl.offs()
     offs = torch.from_numpy(offs_np).to(DEV)
-    a = W.make_activations(wl, "A", device=DEV)
-    dy = W.make_activations(wl, "dY", device=DEV)
-    w = W.make_weights(wl, "W1", device=DEV)
     qa, sa, qat, sat = F.fp8moe_mxfp8_quantize_dual(a, offs, F.GROUP_ROWS, F.GROUP_COLS)
     qw, sw, qwt, swt = F.fp8moe_mxfp8_quantize_dual(w, None, F.NO_GROUPS, F.NO_GROUPS)
     qdy, sdy, qdyt, sdyt = F.fp8moe_mxfp8_quantize_dual(dy, offs, F.GROUP_ROWS, F.GROUP_COLS)
@@ -79,20 +129,38 @@ def test_mxfp8_fullsize(F, name):
     assert F.fp8moe_get_device_status() == 0
 
     rows = _sample_rows(offs_np, rng)
+    rt = torch.from_numpy(rows).to(DEV)
     starts, ends = OQ.group_bounds(offs_np)
     grp = np.searchsorted(ends, rows, side="right")
-    # quantized codes of sampled rows (dim0) and of a column slice (dim1)
-    a_rows = _np(a[torch.from_numpy(rows).to(DEV)])
-    rq, _ = OQ.mxfp8_quantize_dim0(a_rows)
-    assert np.array_equal(qa[torch.from_numpy(rows).to(DEV)].cpu().numpy(), rq)
-    c0 = int(rng.integers(0, K // 64)) * 64
-    rqt, _ = OQ.mxfp8_quantize_dim1(_np(a[:, c0:c0 + 64]))
-    assert np.array_equal(qat[c0:c0 + 64].cpu().numpy(), rqt)
+    # codes and e8m0 scale bytes of sampled rows (dim0, row-grouped 128x4
+    # layout) and of a column slice (dim1, column-grouped layout), for the
+    # activation and the gradient
+    for x, q0, s0, q1, s1, C in [(a, qa, sa, qat, sat, K), (dy, qdy, sdy, qdyt, sdyt, N)]:
+        rq, rs = OQ.mxfp8_quantize_dim0(_np(x[rt]))
+        assert np.array_equal(q0[rt].cpu().numpy(), rq)
+        assert np.array_equal(_swz_rows_bytes(s0, offs_np, rows, C // 32, E), rs)
+        c0 = int(rng.integers(0, C // 64)) * 64
+        rqt, rst = OQ.mxfp8_quantize_dim1(_np(x[:, c0:c0 + 64]))
+        assert np.array_equal(q1[c0:c0 + 64].cpu().numpy(), rqt)
+        got = _swz_cols_bytes(s1, offs_np, np.arange(c0, c0 + 64), M // 32, E)
+        assert np.array_equal(got, rst)
+    # weight codes and scales: sampled rows (dim0) and a column slice (dim1)
+    # of a few experts, the last one included
+    for e in sorted(set(rng.integers(0, E, size=2).tolist() + [E - 1])):
+        wr = np.array(sorted(set(rng.integers(0, N, size=8).tolist() + [0, N - 1])))
+        rq, rs = OQ.mxfp8_quantize_dim0(_np(w[e][torch.from_numpy(wr).to(DEV)]))
+        assert np.array_equal(qw[e][torch.from_numpy(wr).to(DEV)].cpu().numpy(), rq)
+        assert np.array_equal(_swz_batch_bytes(sw, N, K // 32, e, wr), rs)
+        k0 = int(rng.integers(0, K // 64)) * 64
+        rqt, rst = OQ.mxfp8_quantize_dim1(_np(w[e][:, k0:k0 + 64]))
+        assert np.array_equal(qwt[e][k0:k0 + 64].cpu().numpy(), rqt)
+        assert np.array_equal(_swz_batch_bytes(swt, K, N // 32, e, np.arange(k0, k0 + 64)), rst)
 
     # forward: sampled rows x sampled columns
+    a_rows = _np(a[rt])
     ncols = np.array(sorted(set(rng.integers(0, N, size=24).tolist() + [0, N - 1])))
     a_deq = _mx_rows(a_rows)
-    got = _np(out[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(ncols).to(DEV)])
+    got = _np(out[rt][:, torch.from_numpy(ncols).to(DEV)])
     ref = np.zeros_like(got, dtype=np.float64)
     bnd = np.zeros_like(ref)
     for e in np.unique(grp):
@@ -100,12 +168,12 @@ def test_mxfp8_fullsize(F, name):
         w_deq = _mx_rows(_np(w[int(e)][torch.from_numpy(ncols).to(DEV)]))
         ref[sel] = a_deq[sel] @ w_deq.T
         bnd[sel] = np.abs(a_deq[sel]) @ np.abs(w_deq).T
-    _check_vals(got, ref, bnd, f"{name} fwd")
+    _check_vals(got, ref, bnd, f"{name} {which} fwd")
 
     # dgrad: sampled rows x sampled K columns (W quantized along N)
     kcols = np.array(sorted(set(rng.integers(0, K, size=16).tolist() + [K - 1])))
-    dy_deq = _mx_rows(_np(dy[torch.from_numpy(rows).to(DEV)]))
-    got = _np(da[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(kcols).to(DEV)])
+    dy_deq = _mx_rows(_np(dy[rt]))
+    got = _np(da[rt][:, torch.from_numpy(kcols).to(DEV)])
     ref = np.zeros_like(got, dtype=np.float64)
     bnd = np.zeros_like(ref)
     for e in np.unique(grp):
@@ -113,7 +181,7 @@ def test_mxfp8_fullsize(F, name):
         wt_deq = _mx_cols(_np(w[int(e)][:, torch.from_numpy(kcols).to(DEV)]))   # [k, N]
         ref[sel] = dy_deq[sel] @ wt_deq.T
         bnd[sel] = np.abs(dy_deq[sel]) @ np.abs(wt_deq).T
-    _check_vals(got, ref, bnd, f"{name} dgrad")
+    _check_vals(got, ref, bnd, f"{name} {which} dgrad")
 
     # wgrad: a few (n, k) of every expert, empty experts exactly zero
     nn = rng.integers(0, N, size=6)
@@ -127,19 +195,48 @@ def test_mxfp8_fullsize(F, name):
             continue
         dyc = _mx_cols(_np(dy[s0:s1][:, nt]))      # [6, g]
         ac = _mx_cols(_np(a[s0:s1][:, kt]))        # [6, g]
-        _check_vals(got, dyc @ ac.T, np.abs(dyc) @ np.abs(ac).T, f"{name} wgrad e={e}")
+        _check_vals(got, dyc @ ac.T, np.abs(dyc) @ np.abs(ac).T, f"{name} {which} wgrad e={e}")
 
 
-@pytest.mark.parametrize("name", ["llama3_8b", "dsmoe_16b"])
-def test_rowwise_fullsize(F, name):
+def test_dsv3_expert_weight_quantization_fullsize(F):
+    """The DeepSeek-V3 layer's standalone MXFP8 quantization of all expert
+    weights (W1 [256, 2048, 7168] and W2 [256, 7168, 2048], both directions,
+    scales in the 128x4 layout per expert), as bench.py times it: every code
+    and scale byte of a seeded sample of whole experts of both weights is
+    compared bit for bit with the oracle."""
+    wl = W.get_workload("dsv3")
+    rng = np.random.default_rng(29)
+    for which in ["W1", "W2"]:
+        w = W.make_weights(wl, which, device=DEV)
+        E, R, C = w.shape
+        q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(w, None, F.NO_GROUPS, F.NO_GROUPS)
+        torch.cuda.synchronize()
+        assert F.fp8moe_get_device_status() == 0
+        Rp0, Cp0 = OS.swizzled_shape(R, C // 32)
+        Rp1, Cp1 = OS.swizzled_shape(C, R // 32)
+        for e in sorted(set(rng.integers(0, E - 1, size=1).tolist() + [E - 1])):
+            x = _np(w[e])
+            rq, rs = OQ.mxfp8_quantize_dim0(x)
+            assert np.array_equal(q0[e].cpu().numpy(), rq), (which, e, "dim0 codes")
+            assert np.array_equal(s0[e * Rp0 * Cp0:(e + 1) * Rp0 * Cp0].cpu().numpy(), OS.swizzle(rs)), \
+                (which, e, "dim0 scales")
+            rqt, rst = OQ.mxfp8_quantize_dim1(x)
+            assert np.array_equal(q1[e].cpu().numpy(), rqt), (which, e, "dim1 codes")
+            assert np.array_equal(s1[e * Rp1 * Cp1:(e + 1) * Rp1 * Cp1].cpu().numpy(), OS.swizzle(rst)), \
+                (which, e, "dim1 scales")
+        del w, q0, s0, q1, s1
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,which", [("llama3_8b", "W1"), ("dsmoe_16b", "W1"), ("dsmoe_16b", "W2")])
+def test_rowwise_fullsize(F, name, which):
     wl = W.get_workload(name)
     rng = np.random.default_rng(11)
-    M, E, N, K = wl.M, wl.E, wl.N, wl.K
+    a, dy, w = _layer(wl, which, DEV)
+    M = wl.M
+    E, N, K = w.shape
     offs_np = wl.offs()
     offs = torch.from_numpy(offs_np).to(DEV)
-    a = W.make_activations(wl, "A", device=DEV)
-    dy = W.make_activations(wl, "dY", device=DEV)
-    w = W.make_weights(wl, "W1", device=DEV)
     qa, ia = F.fp8moe_quantize_rowwise(a)
     qw, iw = F.fp8moe_quantize_rowwise(w.reshape(E * N, K))
     qdy, idy = F.fp8moe_quantize_rowwise(dy)
@@ -170,7 +267,7 @@ def test_rowwise_fullsize(F, name):
         wd = OQ.dequant_rows(wq, wi)
         ref[sel] = a_deq[sel] @ wd.T
         bnd[sel] = np.abs(a_deq[sel]) @ np.abs(wd).T
-    _check_vals(got, ref, bnd, f"{name} fwd")
+    _check_vals(got, ref, bnd, f"{name} {which} fwd")
 
     kcols = np.array(sorted(set(rng.integers(0, K, size=8).tolist())))
     kt = torch.from_numpy(kcols).to(DEV)
@@ -186,7 +283,7 @@ def test_rowwise_fullsize(F, name):
         assert np.array_equal(qwt[int(e)][kt].cpu().numpy(), cq[0])
         ref[sel] = dy_deq[sel] @ wt.T
         bnd[sel] = np.abs(dy_deq[sel]) @ np.abs(wt).T
-    _check_vals(got, ref, bnd, f"{name} dgrad")
+    _check_vals(got, ref, bnd, f"{name} {which} dgrad")
 
     nn = torch.from_numpy(rng.integers(0, N, size=4)).to(DEV)
     kk = torch.from_numpy(rng.integers(0, K, size=4)).to(DEV)
@@ -200,7 +297,7 @@ def test_rowwise_fullsize(F, name):
         aq, ai = OQ.quantize_colwise_3d(_np(a[s0:s1][:, kk])[None], transpose_out=True)
         dyc = OF.decode(dq[0]) * di[0][:, None].astype(np.float64)
         ac = OF.decode(aq[0]) * ai[0][:, None].astype(np.float64)
-        _check_vals(got, dyc @ ac.T, np.abs(dyc) @ np.abs(ac).T, f"{name} wgrad e={e}")
+        _check_vals(got, dyc @ ac.T, np.abs(dyc) @ np.abs(ac).T, f"{name} {which} wgrad e={e}")
 
 
 def test_blockwise_fullsize(F):
