@@ -48,7 +48,10 @@
 namespace fp8moe {
 
 constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int NUM_THREADS = 224;  // producer, MMA, 4 epilogue warps, scale copier
+// Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-5 epilogue, 6
+// scale copier; wgrad adds four epilogue warps (7-10).
+template <bool WG>
+constexpr int num_threads() { return WG ? 352 : 224; }
 constexpr int A_STAGE_BYTES = BM * BK;            // 16 KB
 constexpr int B_STAGE_BYTES = BN * BK / 2;        // this CTA's half of the B tile, 16 KB
 constexpr int SFA_STAGE_BYTES = 512;              // one 128x4 scale tile
@@ -56,16 +59,27 @@ constexpr int SFB_STAGE_BYTES = 1024;             // two 128x4 scale tiles (256 
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF_BASE = 256;            // scale columns start after the accumulator
-constexpr int STG_COLS = 32;                      // output columns per staged store (64 bytes of bf16)
-constexpr int STG_BYTES = 32 * STG_COLS * 2;      // one staging tile: 32 rows x 64 B
-constexpr int STG_WARP_BYTES = 2 * STG_BYTES;     // double-buffered per epilogue warp
 
-// BIGE = false: a 6-deep ring and group tables of 512 groups;
-// BIGE = true:  a 5-deep ring, which leaves room for tables of 1024 groups.
-template <bool BIGE>
+// BIGE = false: group tables of 512 groups; BIGE = true: of 1024 groups.
+// Forward / dgrad: a 6-deep operand ring (5 with the larger tables) and four
+// epilogue warps, one per TMEM lane quarter, each draining all 256 columns
+// and storing them in 32-column slices (32 rows x 64 B, 64-byte swizzle).
+// Wgrad tiles are short in K (one group's tokens) and store a whole 64 KB
+// accumulator per CTA every few k-stages, so wgrad trades a stage of the
+// ring for eight epilogue warps (two per lane quarter, 128 columns each).
+// Every epilogue warp stores through two staging tiles.  (64-column slices
+// with a 128-byte swizzle, half the store rows, measured slower for wgrad:
+// they cost a second stage of the ring.)
+template <bool BIGE, bool WG>
 struct SmemLayout {
-  static constexpr int STAGES = BIGE ? 5 : 6;
+  static constexpr int STAGES = (BIGE ? 5 : 6) - (WG ? 1 : 0);
   static constexpr int MAXG = BIGE ? MAX_GROUPS : 512;
+  static constexpr int NEPI = WG ? 8 : 4;                       // epilogue warps
+  static constexpr int EC = BN * 4 / NEPI;                      // accumulator columns per epilogue warp
+  static constexpr int STG_COLS = 32;                           // output columns per staged store
+  static constexpr int STG_BYTES = 32 * STG_COLS * 2;           // one staging tile: 32 rows
+  static constexpr int STG_DEPTH = 2;                           // staging tiles per epilogue warp
+  static constexpr int STG_WARP_BYTES = STG_DEPTH * STG_BYTES;
   static constexpr int a = 0;
   static constexpr int b = a + STAGES * A_STAGE_BYTES;
   static constexpr int sfa = b + STAGES * B_STAGE_BYTES;
@@ -75,14 +89,16 @@ struct SmemLayout {
   static constexpr int colscale = misc + 64;                    // 256 floats
   static constexpr int tiles_prefix = colscale + BN * 4;        // MAXG + 1 ints
   static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
-  // per epilogue warp two 32-row x 64-byte staging tiles (64-byte swizzle)
-  static constexpr int stg = (blk_prefix + (MAXG + 1) * 4 + 1023) / 1024 * 1024;
-  static constexpr int total = stg + 4 * STG_WARP_BYTES;
+  static constexpr int offs = blk_prefix + (MAXG + 1) * 4;      // MAXG + 1 ints: group bounds
+  // per epilogue warp STG_DEPTH 32-row x 64-byte staging tiles (64-byte swizzle)
+  static constexpr int stg = (offs + (MAXG + 1) * 4 + 1023) / 1024 * 1024;
+  static constexpr int total = stg + NEPI * STG_WARP_BYTES;
 };
-static_assert(SmemLayout<false>::stg % 1024 == 0 && SmemLayout<true>::stg % 1024 == 0, "staging alignment");
-template <bool BIGE>
-constexpr int smem_bytes() { return SmemLayout<BIGE>::total + 1024; }  // + alignment slack
-static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory");
+template <bool BIGE, bool WG>
+constexpr int smem_bytes() { return SmemLayout<BIGE, WG>::total + 1024; }  // + alignment slack
+static_assert(smem_bytes<false, false>() <= 227 * 1024 && smem_bytes<true, false>() <= 227 * 1024 &&
+                  smem_bytes<false, true>() <= 227 * 1024 && smem_bytes<true, true>() <= 227 * 1024,
+              "shared memory");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -101,9 +117,14 @@ FP8MOE_DEV uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-// arrive on the mbarrier at the same offset in CTA `rank` of the cluster
+// arrive on the mbarrier at the same offset in CTA `rank` of the cluster.
+// The release is CTA-scoped: what the arrive publishes is this thread's
+// completed TMEM reads (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync),
+// not memory the other CTA reads.  A cluster-scoped release made the arriving
+// thread wait for its CTA's outstanding output stores first (measured: 1.4-2.2
+// thousand cycles per arrive, on the accumulator hand-off's critical path).
 FP8MOE_DEV void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa_rank(smem_u32(bar), rank))
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(mapa_rank(smem_u32(bar), rank))
                : "memory");
 }
 FP8MOE_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -201,23 +222,19 @@ struct Tile {
 // m-tile lies past the group ("phantom", rows == 0) the pair still computes
 // it (its operand rows read the fill of the tensor map or the next group's
 // rows) but stores nothing.  rank: CTA within its pair.
+// Each role walks its tiles in increasing t, so the group of tile t is found
+// by advancing a cursor `e` (the last group whose tile prefix is <= t) from
+// the previous tile's group; the group bounds come from shared memory
+// (bounds[e] = start of group e, bounds[e + 1] = its end), so no tile start
+// waits on a global load.
 template <bool WGRAD>
-FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* blk_prefix, int t, int rank) {
+FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* blk_prefix, const int* bounds, int t,
+                         int rank, int& e) {
   const GemmArgs& g = p.g;
-  // last group whose tile prefix is <= t
-  int lo = 0, hi = g.E - 1, e = 0;
-  while (lo <= hi) {
-    const int mid = (lo + hi) >> 1;
-    if (tiles_prefix[mid] <= t) {
-      e = mid;
-      lo = mid + 1;
-    } else {
-      hi = mid - 1;
-    }
-  }
+  while (e + 1 < g.E && tiles_prefix[e + 1] <= t) ++e;
   const int local = t - tiles_prefix[e];
-  const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
-  const int64_t ge = g.offs[e];
+  const int64_t gs = bounds[e];
+  const int64_t ge = bounds[e + 1];
   Tile tl;
   tl.e = e;
   if (!WGRAD) {
@@ -251,11 +268,11 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
 }
 
 template <bool MX, bool WGRAD, bool BIGE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
     k_grouped_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                  const __grid_constant__ CUtensorMap tmOut, KParams p) {
-  using L = SmemLayout<BIGE>;
+  using L = SmemLayout<BIGE, WGRAD>;
   constexpr int STAGES = L::STAGES;
   constexpr int CL = 2;  // cluster size: one pair
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -279,6 +296,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   float* colscale = (float*)(smem + L::colscale);
   int* tiles_prefix = (int*)(smem + L::tiles_prefix);
   int* blk_prefix = (int*)(smem + L::blk_prefix);
+  int* bounds = (int*)(smem + L::offs);
 
   const GemmArgs& g = p.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -298,7 +316,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(drain_cp, 1);
     mbar_init(tmem_full, 1);
     // the leader's accumulator is free once both CTAs' epilogues drained
-    mbar_init(tmem_empty, 8);
+    mbar_init(tmem_empty, 2 * L::NEPI);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -309,7 +327,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_before();
   }
   // per-group tile counts and scale-block counts, then a scan
-  for (int e = threadIdx.x; e < g.E; e += NUM_THREADS) {
+  for (int e = threadIdx.x; e < g.E; e += num_threads<WGRAD>()) {
     const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
     const int64_t ge = g.offs[e];
     const int64_t sz = ge - gs;
@@ -323,7 +341,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     tiles_prefix[e + 1] = sz < 0 ? 0 : nt;
     blk_prefix[e + 1] = sz < 0 ? 0 : nb;
+    bounds[e + 1] = (int)ge;
   }
+  if (threadIdx.x == 0) bounds[0] = 0;
   __syncthreads();
   if (warp == 0) {
     // validate the offsets and scan (one warp, 32 groups per step)
@@ -390,8 +410,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t phase = 0;
     int filled[STAGES];  // phase of each stage's last fill, -1: never filled
     for (int s = 0; s < STAGES; ++s) filled[s] = -1;
+    int cur_e = 0;
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, bounds, t, rank, cur_e);
       for (int ks = 0; ks < tl.nk; ++ks) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
           set_status(g.status, FP8MOE_ERR_TIMEOUT);
@@ -468,8 +489,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!mbar_wait(&full[stage], phase, abort_flag)) return false;
       return !MX || mbar_wait(&sf_full[stage], phase, abort_flag);
     };
+    int cur_e = 0;
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, bounds, t, rank, cur_e);
       if (tl.nk == 0) continue;
       if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, abort_flag)) {
         set_status(g.status, FP8MOE_ERR_TIMEOUT);
@@ -538,8 +560,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (MX && lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-        const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+      int cur_e = 0;
+    for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
+        const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, bounds, t, rank, cur_e);
         bool ok = true;
         for (int ks = 0; ks < tl.nk; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
@@ -568,9 +591,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= 2) {
     // ======================= epilogue =======================
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    const int et = threadIdx.x - 64;
-    uint8_t* stg = smem + L::stg + (warp - 2) * STG_WARP_BYTES;
+    constexpr int NEPI = L::NEPI, EC = L::EC;
+    const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+    const int ew = warp < 6 ? warp - 2 : warp - 3;  // epilogue warp index
+    const int c_lo = NEPI == 8 ? (ew >> 2) * EC : 0;  // this warp's accumulator columns [c_lo, c_lo + EC)
+    const int et = ew * 32 + lane;
+    uint8_t* stg = smem + L::stg + ew * L::STG_WARP_BYTES;
     uint32_t acc_phase = 0;
     auto release_acc = [&]() {
       tc_fence_before();
@@ -583,8 +609,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     };
+    int cur_e = 0;
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
-      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, t, rank);
+      const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, bounds, t, rank, cur_e);
       const int64_t lrow = quarter * 32 + lane;
       const bool row_ok = lrow < tl.rows;
       const int64_t ncols = (g.cols - tl.col0) < BN ? (g.cols - tl.col0) : BN;
@@ -592,11 +619,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint16_t* obase = WGRAD ? g.out + ((int64_t)tl.e * g.rows + tl.row0) * g.cols + tl.col0
                               : g.out + tl.row0 * g.cols + tl.col0;
       if (tl.nk == 0) {  // empty group in wgrad: dW[e] = 0
-        const int nc8 = (int)(ncols / 8);
+        const int64_t wc = ncols - c_lo < EC ? ncols - c_lo : EC;   // this warp's columns
+        const int nc8 = wc > 0 ? (int)(wc / 8) : 0;
         for (int i = lane; i < 32 * nc8; i += 32) {
           const int64_t trow = quarter * 32 + i / nc8;
           if (trow < tl.rows)
-            *reinterpret_cast<uint4*>(obase + trow * g.cols + (i % nc8) * 8) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(obase + trow * g.cols + c_lo + (i % nc8) * 8) = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -605,10 +633,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // column scales of this tile into shared memory, row scale per thread
         // (tensorwise: one scale per operand)
         const bool tw = g.recipe == FP8MOE_TENSORWISE;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NEPI) : "memory");
         const float* cs = (const float*)g.b_scale + (tw ? 0 : (int64_t)tl.e * g.cols + tl.col0);
-        for (int c = et; c < BN; c += 128) colscale[c] = c < ncols ? cs[tw ? 0 : c] : 0.0f;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        for (int c = et; c < BN; c += 32 * NEPI) colscale[c] = c < ncols ? cs[tw ? 0 : c] : 0.0f;
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * NEPI) : "memory");
         if (row_ok) {
           const float* rs = (const float*)g.a_scale;
           rscale = tw ? rs[0] : (WGRAD ? rs[(int64_t)tl.e * g.rows + tl.row0 + lrow] : rs[tl.row0 + lrow]);
@@ -625,19 +653,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         release_acc();
         continue;
       }
-      uint32_t packed[BN / 2];
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16);
+      uint32_t packed[EC / 2];
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c_lo;
+      // four epilogue warps: two 32-column loads in flight per wait (half the
+      // load round trips); eight (a third fewer registers each): one
+      constexpr int LW = EC == 256 ? 64 : 32;   // columns per wait
 #pragma unroll
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c, r);
+      for (int c = 0; c < EC; c += LW) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(taddr + c, r0);
+        if constexpr (LW == 64) tmem_ld32(taddr + c + 32, r1);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float v0 = __uint_as_float(r[j]), v1 = __uint_as_float(r[j + 1]);
+        for (int j = 0; j < LW; j += 2) {
+          float v0 = __uint_as_float(j < 32 ? r0[j] : r1[j - 32]);
+          float v1 = __uint_as_float(j < 32 ? r0[j + 1] : r1[j - 31]);
           if (!MX) {
-            v0 = v0 * rscale * colscale[c + j];
-            v1 = v1 * rscale * colscale[c + j + 1];
+            v0 = v0 * rscale * colscale[c_lo + c + j];
+            v1 = v1 * rscale * colscale[c_lo + c + j + 1];
           }
           packed[(c + j) / 2] = pack_bf16(v0, v1);
         }
@@ -654,24 +687,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // the lanes with bounds checks.
       const bool tma = p.tma_out && (WGRAD ? (int64_t)quarter * 32 < tl.rows : (int64_t)(quarter + 1) * 32 <= tl.rows);
       if (!tma && (int64_t)quarter * 32 >= tl.rows) continue;
+      constexpr int SC = L::STG_COLS, RB = SC * 2, NCH = SC / 8;   // columns, bytes, 16-B chunks per row
+      // 16-byte chunk c of staging row r: 64-byte swizzle (64-byte rows) or
+      // 128-byte swizzle (128-byte rows), as the output tensor map expects;
+      // conflict-free for row-per-lane writes and row-group reads
+      auto swz = [](int c, int r) { return NCH == 4 ? (c ^ ((r >> 1) & 3)) : (c ^ (r & 7)); };
 #pragma unroll
-      for (int j = 0; j < BN / STG_COLS; ++j) {
-        const int cc = j * STG_COLS;
+      for (int j = 0; j < EC / SC; ++j) {
+        const int cc = c_lo + j * SC;
         if (cc < ncols) {
-          uint8_t* buf = stg + (j & 1) * STG_BYTES;
-          // the store that last read this buffer (two slices ago) is done reading
+          uint8_t* buf = stg + (j % L::STG_DEPTH) * L::STG_BYTES;
+          // the store that last read this buffer (STG_DEPTH slices ago) is
+          // done reading
           if (lane == 0) {
             if (tma) {
-              bulk_wait_read<1>();
+              bulk_wait_read<L::STG_DEPTH - 1>();
             } else {
               bulk_wait_read<0>();
             }
           }
           __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int w = (cc + c * 8) / 2;
-            *reinterpret_cast<uint4*>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) =
+          for (int c = 0; c < NCH; ++c) {
+            const int w = (j * SC + c * 8) / 2;
+            *reinterpret_cast<uint4*>(buf + lane * RB + (swz(c, lane) << 4)) =
                 make_uint4(packed[w], packed[w + 1], packed[w + 2], packed[w + 3]);
           }
           if (tma) {
@@ -688,9 +727,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = i * 8 + (lane >> 2), ch = lane & 3;
-              const uint4 v = *reinterpret_cast<const uint4*>(buf + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+            for (int i = 0; i < NCH; ++i) {
+              const int r = i * (32 / NCH) + lane / NCH, ch = lane % NCH;
+              const uint4 v = *reinterpret_cast<const uint4*>(buf + r * RB + (swz(ch, r) << 4));
               const int64_t trow = quarter * 32 + r;
               const int64_t col = cc + ch * 8;
               if (trow < tl.rows && col < ncols) *reinterpret_cast<uint4*>(obase + trow * g.cols + col) = v;
@@ -730,12 +769,12 @@ static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const 
                             cudaStream_t st) {
   auto kern = k_grouped_mm<MX, WGRAD, BIGE>;
   constexpr int CL = 2;
-  constexpr int SMEM = smem_bytes<BIGE>();
+  constexpr int SMEM = smem_bytes<BIGE, WGRAD>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)CL);
-  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.blockDim = dim3(num_threads<WGRAD>());
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -773,8 +812,10 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   const bool wgrad = g.mode == GEMM_WGRAD;
   // cta_group::2 pairs throughout; more than 512 groups take the variant
   // with the larger group tables and a 5-deep ring
-  const bool bige = g.E > SmemLayout<false>::MAXG;
-  if ((bige ? smem_bytes<true>() : smem_bytes<false>()) > g.max_smem) return cudaErrorNotSupported;
+  const bool bige = g.E > SmemLayout<false, false>::MAXG;
+  if (smem_bytes<true, true>() > g.max_smem || smem_bytes<true, false>() > g.max_smem ||
+      smem_bytes<false, true>() > g.max_smem || smem_bytes<false, false>() > g.max_smem)
+    return cudaErrorNotSupported;
   KParams p;
   p.g = g;
   p.stall_test = g_stall_next.exchange(0, std::memory_order_relaxed);
@@ -835,7 +876,7 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
                    CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
-  // bf16 output tiles stored by TMA: 32 columns x 32 rows per box, 64-byte
+  // bf16 output tiles stored by TMA: boxes of 32 rows x 32 columns, 64-byte
   // swizzle; wgrad as [E, rows, cols] so that rows past an expert are clipped
   CUtensorMap tout = ta;
   p.tma_out = 0;
@@ -844,12 +885,12 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
     if (wgrad) {
       cuuint64_t dims[3] = {(cuuint64_t)g.cols, (cuuint64_t)g.rows, (cuuint64_t)g.E};
       cuuint64_t strides[2] = {(cuuint64_t)(g.cols * 2), (cuuint64_t)(g.rows * g.cols * 2)};
-      cuuint32_t box[3] = {(cuuint32_t)STG_COLS, 32, 1};
+      cuuint32_t box[3] = {(cuuint32_t)SmemLayout<false, true>::STG_COLS, 32, 1};
       ok = make_tmap(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.out, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
     } else {
       cuuint64_t dims[2] = {(cuuint64_t)g.cols, (cuuint64_t)(g.M > 0 ? g.M : 1)};
       cuuint64_t strides[1] = {(cuuint64_t)(g.cols * 2)};
-      cuuint32_t box[2] = {(cuuint32_t)STG_COLS, 32};
+      cuuint32_t box[2] = {(cuuint32_t)SmemLayout<false, false>::STG_COLS, 32};
       ok = make_tmap(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.out, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
     }
     p.tma_out = ok ? 1 : 0;
