@@ -679,6 +679,43 @@ def bench_rows(F, iters=10, only=None):
             emit("a8", "k_grouped_mm<rowwise,wgrad>", cfg, ms, flops=flops)
             del qa, qw, qdy, qwt, qdyt, qat, out, da, dw
 
+    # ---- activation quantization fused into the GEMM prologue (a9 and its
+    # dgrad twin) against the unfused chain: the dim0 quantization of the
+    # bf16 operand (scales straight into the grouped layout) then the GEMM
+    if want("fused"):
+        for wl in (sc, v3):
+            offs = torch.from_numpy(wl.offs()).to(dev)
+            M, E, N, K = wl.M, wl.E, wl.N, wl.K
+            T = int(wl.group_plan()[0].sum())
+            flops = 2.0 * T * N * K
+            a = W.make_activations(wl, "A", device=dev)
+            dy = W.make_activations(wl, "dY", device=dev)
+            w = W.make_weights(wl, "W1", device=dev)
+            qw, sw, qwt, swt = F.fp8moe_mxfp8_quantize_dual(w, None, F.NO_GROUPS, F.NO_GROUPS)
+            del w
+            out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            da = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+            qa, sa, _, _ = F.fp8moe_mxfp8_quantize_dual(a, offs, F.GROUP_ROWS, dim1=False)
+            qd, sd, _, _ = F.fp8moe_mxfp8_quantize_dual(dy, offs, F.GROUP_ROWS, dim1=False)
+            cfg = f"{wl.name} W1 M={M} N={N} K={K} E={E}"
+
+            def chain_fwd():
+                F.fp8moe_mxfp8_quantize_dual(a, offs, F.GROUP_ROWS, dim1=False, q0=qa, s0=sa)
+                F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, offs, out=out)
+
+            def chain_dgrad():
+                F.fp8moe_mxfp8_quantize_dual(dy, offs, F.GROUP_ROWS, dim1=False, q0=qd, s0=sd)
+                F.fp8moe_scaled_grouped_mm_dgrad(F.MXFP8, qd, sd, qwt, swt, offs, out=da)
+            ms = timed(chain_fwd)
+            emit("a9", "k_mx_dim0 + k_grouped_mm<MX,fwd> (unfused)", cfg, ms, flops=flops)
+            ms = timed(lambda: F.fp8moe_mxfp8_grouped_mm_fwd_quant_a(a, qw, sw, offs, out=out))
+            emit("a9", "k_grouped_mm<MX,fwd,quant-A prologue>", cfg, ms, flops=flops)
+            ms = timed(chain_dgrad)
+            emit("next1", "k_mx_dim0 + k_grouped_mm<MX,dgrad> (unfused)", cfg, ms, flops=flops)
+            ms = timed(lambda: F.fp8moe_mxfp8_grouped_mm_dgrad_quant_a(dy, qwt, swt, offs, out=da))
+            emit("next1", "k_grouped_mm<MX,dgrad,quant-dY prologue>", cfg, ms, flops=flops)
+            del a, dy, qw, sw, qwt, swt, out, da, qa, sa, qd, sd
+
     # ---- MoE layer composites (next1) and blockwise scaling (next3) on the
     # Scout W1 layer
     if want("layer") or want("blockwise"):
@@ -757,7 +794,7 @@ def main():
     ap.add_argument("--no-dsv3", action="store_true", help="skip the DeepSeek-V3 layer measurements")
     ap.add_argument("--only", default=None,
                     help="with --rows: comma-separated sections (rowwise, colwise, tensorwise, mx, swizzle, gemm, "
-                         "layer, blockwise, routing)")
+                         "fused, layer, blockwise, routing)")
     ap.add_argument("--rows", action="store_true",
                     help="time every hot-path kernel at its configuration size (one JSON line each) and exit")
     args = ap.parse_args()

@@ -302,6 +302,36 @@ fp8moe_status fp8moe_scaled_grouped_mm_wgrad(int recipe, const void* dyt, const 
                                              fp8moe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * MXFP8 grouped GEMM with the activation quantized in the GEMM's prologue.
+ * [SCOUT] section details (the _to_mxfp8_then_scaled_grouped_mm primitive:
+ * bf16 activations are quantized to MXFP8 on the fly and fed to the scaled
+ * grouped GEMM); [AMD-FP8] aixai.ru "Три уровня оптимизации" (fewer passes
+ * through HBM).  Same results as fp8moe_mxfp8_quantize_dim0 of the bf16
+ * operand (scales swizzled with GROUP_ROWS) followed by the MXFP8
+ * fp8moe_scaled_grouped_mm_fwd / _dgrad, bit for bit: the kernel's
+ * producer stages the bf16 A tiles in shared memory and four warps turn each
+ * into e4m3 codes and e8m0 scales (the dim0 rule) right where the tensor
+ * cores read them, so the fp8 copy of A never goes through HBM.
+ *
+ * forward: a [M, K] bf16 routed rows (groups from offs, multiples of 32),
+ *   w [E, N, K] e4m3 with w_scale as for the MXFP8 forward; out [M, N] bf16.
+ * dgrad:   dy [M, N] bf16, wt [E, K, N] e4m3 with wt_scale as for the MXFP8
+ *   dgrad; out [M, K] bf16.
+ * a_q / a_s (dy_q / dy_s): optional (both NULL or both given) copies of the
+ * quantized operand, codes [M, K] ([M, N]) and row-major e8m0 scales
+ * [M, K/32] ([M, N/32]), written by the kernel (rows past M are not).
+ * The contracting dimension must be a multiple of 32; N % 16 == K % 16 == 0;
+ * 1 <= E <= FP8MOE_MAX_GROUPS; every pointer 16-byte aligned.  Device-side
+ * offset errors as the MXFP8 grouped GEMM.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_mxfp8_grouped_mm_fwd_quant_a(const void* a, const void* w, const void* w_scale,
+                                                  const int32_t* offs, int64_t E, int64_t M, int64_t N, int64_t K,
+                                                  void* out, void* a_q, uint8_t* a_s, fp8moe_stream_t stream);
+fp8moe_status fp8moe_mxfp8_grouped_mm_dgrad_quant_a(const void* dy, const void* wt, const void* wt_scale,
+                                                    const int32_t* offs, int64_t E, int64_t M, int64_t N, int64_t K,
+                                                    void* out, void* dy_q, uint8_t* dy_s, fp8moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * MXFP8 MoE expert layer as two composites: dynamic MXFP8 quantization of
  * the bf16 operands followed by the scaled grouped GEMMs.  [SCOUT] section
  * details (the _to_mxfp8_then_scaled_grouped_mm primitive quantizes the

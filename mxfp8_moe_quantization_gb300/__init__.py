@@ -25,6 +25,7 @@ __all__ = [
     "fp8moe_swizzled_scales_bytes", "fp8moe_swizzle_scales_128x4",
     "fp8moe_scaled_grouped_mm_fwd", "fp8moe_scaled_grouped_mm_dgrad",
     "fp8moe_scaled_grouped_mm_wgrad", "fp8moe_get_device_status", "fp8moe_status_string",
+    "fp8moe_mxfp8_grouped_mm_fwd_quant_a", "fp8moe_mxfp8_grouped_mm_dgrad_quant_a",
     "fp8moe_testing_stall_next_gemm",
     "fp8moe_mxfp8_moe_workspace_bytes", "fp8moe_mxfp8_moe_fwd", "fp8moe_mxfp8_moe_bwd",
     "fp8moe_quantize_blockwise_rows", "fp8moe_quantize_blockwise_weight", "fp8moe_blockwise_token_blocks",
@@ -60,6 +61,9 @@ SYMBOLS = {
     "fp8moe_scaled_grouped_mm_fwd": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "fp8moe_scaled_grouped_mm_dgrad": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
     "fp8moe_scaled_grouped_mm_wgrad": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp]),
+    "fp8moe_mxfp8_grouped_mm_fwd_quant_a": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "fp8moe_mxfp8_grouped_mm_dgrad_quant_a": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _vp, _vp, _vp,
+                                                     _vp]),
     "fp8moe_quantize_blockwise_rows": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp]),
     "fp8moe_quantize_blockwise_weight": (_i32, [_vp, _i64, _i64, _i64, _i32, _vp, _vp, _vp, _vp]),
     "fp8moe_blockwise_token_blocks": (_i64, [_i64, _i64]),
@@ -372,6 +376,43 @@ def fp8moe_scaled_grouped_mm_wgrad(recipe, dyt, dyt_scale, at, at_scale, offs, M
     E = offs.numel()
     return _gemm("fp8moe_scaled_grouped_mm_wgrad", recipe, dyt, dyt_scale, at, at_scale, offs, E, M, N, K,
                  out, (E, N, K), stream)
+
+
+def fp8moe_mxfp8_grouped_mm_fwd_quant_a(a, w, w_scale, offs, out=None, a_q=None, a_s=None, keep_quantized=False,
+                                        stream=None):
+    """a [M, K] bf16, w [E, N, K] e4m3 (uint8) with its swizzled scales ->
+    out [M, N] bf16; A is quantized to MXFP8 inside the GEMM.  With
+    ``keep_quantized`` (or given buffers) also returns the codes [M, K] and
+    row-major e8m0 scales [M, K/32] the kernel used: (out, a_q, a_s)."""
+    torch = _torch()
+    M, K = a.shape
+    E, N, _ = w.shape
+    if keep_quantized and a_q is None:
+        a_q = _empty((M, K), torch.uint8, a)
+        a_s = _empty((M, K // 32), torch.uint8, a)
+    out = _empty((M, N), torch.bfloat16, a) if out is None else out
+    _check("fp8moe_mxfp8_grouped_mm_fwd_quant_a", _lib_raw().fp8moe_mxfp8_grouped_mm_fwd_quant_a(
+        _ptr(a), _ptr(w), _ptr(w_scale), _ptr(offs), E, M, N, K, _ptr(out), _ptr(a_q), _ptr(a_s),
+        _stream(stream)))
+    return (out, a_q, a_s) if a_q is not None else out
+
+
+def fp8moe_mxfp8_grouped_mm_dgrad_quant_a(dy, wt, wt_scale, offs, out=None, dy_q=None, dy_s=None,
+                                          keep_quantized=False, stream=None):
+    """dy [M, N] bf16, wt [E, K, N] e4m3 with its swizzled scales -> dA
+    [M, K] bf16; dY is quantized to MXFP8 inside the GEMM (codes / scales
+    returned as for the forward when asked)."""
+    torch = _torch()
+    M, N = dy.shape
+    E, K, _ = wt.shape
+    if keep_quantized and dy_q is None:
+        dy_q = _empty((M, N), torch.uint8, dy)
+        dy_s = _empty((M, N // 32), torch.uint8, dy)
+    out = _empty((M, K), torch.bfloat16, dy) if out is None else out
+    _check("fp8moe_mxfp8_grouped_mm_dgrad_quant_a", _lib_raw().fp8moe_mxfp8_grouped_mm_dgrad_quant_a(
+        _ptr(dy), _ptr(wt), _ptr(wt_scale), _ptr(offs), E, M, N, K, _ptr(out), _ptr(dy_q), _ptr(dy_s),
+        _stream(stream)))
+    return (out, dy_q, dy_s) if dy_q is not None else out
 
 
 def fp8moe_quantize_blockwise_rows(x, kind: int = E4M3FN, q=None, scale_inv=None, stream=None):

@@ -347,6 +347,56 @@ fp8moe_status fp8moe_scaled_grouped_mm_wgrad(int recipe, const void* dyt, const 
   return grouped_mm(fp8moe::GEMM_WGRAD, recipe, dyt, dyt_scale, at, at_scale, offs, E, M, N, K, out, stream);
 }
 
+static fp8moe_status grouped_mm_quant_a(int mode, const void* a_bf16, const void* b, const void* b_scale,
+                                        const int32_t* offs, int64_t E, int64_t M, int64_t N, int64_t K, void* out,
+                                        void* a_q, uint8_t* a_s, fp8moe_stream_t stream) {
+  if (E < 1 || E > FP8MOE_MAX_GROUPS || M < 0 || N < 0 || K < 0) return FP8MOE_ERR_INVALID_ARG;
+  if (!offs || ((uintptr_t)offs & 3)) return FP8MOE_ERR_INVALID_ARG;
+  if ((a_q == nullptr) != (a_s == nullptr)) return FP8MOE_ERR_INVALID_ARG;
+  const int64_t kk = mode == fp8moe::GEMM_FWD ? K : N;      // the contracting dimension
+  const int64_t cols = mode == fp8moe::GEMM_FWD ? N : K;
+  if (N % 16 || K % 16 || kk % 32) return FP8MOE_ERR_ALIGNMENT;
+  if (!a_bf16 || !b || !b_scale || !out) return FP8MOE_ERR_INVALID_ARG;
+  if (!al16(a_bf16) || !al16(b) || !al16(b_scale) || !al16(out) || (a_q && !al16(a_q))) return FP8MOE_ERR_ALIGNMENT;
+  if (M == 0 || cols == 0) return FP8MOE_OK;
+  DevInfo* d;
+  fp8moe_status st = device_info(&d);
+  if (st) return st;
+  fp8moe::GemmArgs g{};
+  g.recipe = FP8MOE_MXFP8;
+  g.mode = mode;
+  g.E = (int)E;
+  g.offs = offs;
+  g.out = (uint16_t*)out;
+  g.status = d->status;
+  g.num_sms = d->num_sms;
+  g.max_smem = d->max_smem;
+  g.M = M;
+  g.a = (const uint8_t*)a_bf16;
+  g.b = (const uint8_t*)b;
+  g.a_scale = nullptr;
+  g.b_scale = b_scale;
+  g.rows = M, g.cols = cols, g.kk = kk;
+  g.quant_a = 1;
+  g.qa_out = (uint8_t*)a_q;
+  g.sa_out = a_s;
+  cudaError_t e = fp8moe::launch_grouped_mm(g, (cudaStream_t)stream);
+  if (e == cudaErrorNotSupported) return FP8MOE_ERR_UNSUPPORTED;
+  return cuda_result(e);
+}
+
+fp8moe_status fp8moe_mxfp8_grouped_mm_fwd_quant_a(const void* a, const void* w, const void* w_scale,
+                                                  const int32_t* offs, int64_t E, int64_t M, int64_t N, int64_t K,
+                                                  void* out, void* a_q, uint8_t* a_s, fp8moe_stream_t stream) {
+  return grouped_mm_quant_a(fp8moe::GEMM_FWD, a, w, w_scale, offs, E, M, N, K, out, a_q, a_s, stream);
+}
+
+fp8moe_status fp8moe_mxfp8_grouped_mm_dgrad_quant_a(const void* dy, const void* wt, const void* wt_scale,
+                                                    const int32_t* offs, int64_t E, int64_t M, int64_t N, int64_t K,
+                                                    void* out, void* dy_q, uint8_t* dy_s, fp8moe_stream_t stream) {
+  return grouped_mm_quant_a(fp8moe::GEMM_DGRAD, dy, wt, wt_scale, offs, E, M, N, K, out, dy_q, dy_s, stream);
+}
+
 int64_t fp8moe_route_rows(int64_t T, int64_t k, int64_t E) {
   if (T < 0 || k < 1 || E < 1) return -1;
   return (T * k + 31 * E + 31) / 32 * 32;

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "mxcvt.cuh"
 #include "scales.cuh"
 
 namespace fp8moe {
@@ -37,47 +38,6 @@ FP8MOE_DEV uint4 ld_nc16(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
-}
-
-// lane-wise max of two pairs of non-negative bf16 values (sign bits cleared):
-// the result is one of the inputs, so the maximum is exact.  Only an all-zero
-// or all-subnormal block could see a subnormal flushed, and its scale byte is
-// 0 either way (its exponent field is 0).
-FP8MOE_DEV uint32_t max_u16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-// The e8m0 byte of a block, clamp(floor(log2 amax) - 8, -127, 127) + 127, is
-// max(ef, 8) - 8 for the bf16 exponent field ef of the block maximum (a zero
-// or subnormal maximum has ef = 0 and gets byte 0, as the clamp gives); 2^-e
-// is then the bf16 with exponent field 262 - max(ef, 8), a normal number.
-// x * 2^-e on two bf16 values: exact (an 8-bit significand times a power of
-// two, below 2^9 in magnitude; only values far under the e4m3 range can
-// round, and they encode to a signed zero either way)
-FP8MOE_DEV uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-// four fp32 values -> four e4m3fn codes (RNE, saturating), byte i from the
-// i-th argument, packed in one word
-FP8MOE_DEV uint32_t cvt4(float a, float b, float c, float d) {
-  uint32_t r;
-  asm("{\n .reg .b16 l, h;\n cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n"
-      " mov.b32 %0, {l, h};\n}"
-      : "=r"(r)
-      : "f"(a), "f"(b), "f"(c), "f"(d));
-  return r;
-}
-FP8MOE_DEV float lo_f32(uint32_t y) { return __uint_as_float(y << 16); }
-FP8MOE_DEV float hi_f32(uint32_t y) { return __uint_as_float(y & 0xFFFF0000u); }
-// 8 codes of one row chunk (4 bf16 pairs) scaled by the pair p2
-FP8MOE_DEV uint2 enc_row8(const uint4& v, uint32_t p2) {
-  const uint32_t y0 = mul_bf16x2(v.x, p2), y1 = mul_bf16x2(v.y, p2);
-  const uint32_t y2 = mul_bf16x2(v.z, p2), y3 = mul_bf16x2(v.w, p2);
-  return make_uint2(cvt4(lo_f32(y0), hi_f32(y0), lo_f32(y1), hi_f32(y1)),
-                    cvt4(lo_f32(y2), hi_f32(y2), lo_f32(y3), hi_f32(y3)));
 }
 
 struct DualArgs {

@@ -26,6 +26,12 @@ struct GemmArgs {
   int64_t M;             // routed rows (fwd/dgrad: = rows of A; wgrad: tokens)
   int64_t rows, cols, kk;
   uint16_t* out;         // bf16
+  // MXFP8 forward / dgrad with the A operand given as bf16 [M, kk] and
+  // quantized in the kernel's prologue (a_scale unused); qa_out / sa_out:
+  // optional copies of its codes [M, kk] and row-major e8m0 scales [M, kk/32]
+  int quant_a;
+  uint8_t* qa_out;
+  uint8_t* sa_out;
   int* status;
   int num_sms;
   int max_smem;

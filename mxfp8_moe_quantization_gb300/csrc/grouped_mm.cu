@@ -42,6 +42,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "launch.h"
+#include "mxcvt.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
 
@@ -49,9 +50,11 @@ namespace fp8moe {
 
 constexpr int BM = 128, BN = 256, BK = 128;
 // Warps: 0 TMA producer, 1 TMEM allocator + MMA issuer, 2-5 epilogue, 6
-// scale copier; wgrad adds four epilogue warps (7-10).
-template <bool WG>
-constexpr int num_threads() { return WG ? 352 : 224; }
+// scale copier; wgrad adds four epilogue warps (7-10), the bf16-A variant
+// (QA) four A-quantization warps (7-10).
+template <bool WG, bool QA>
+constexpr int num_threads() { return WG || QA ? 352 : 224; }
+constexpr int QA_SLOT_BYTES = BM * BK * 2;        // one bf16 A stage: two 128-row x 64-column boxes
 constexpr int A_STAGE_BYTES = BM * BK;            // 16 KB
 constexpr int B_STAGE_BYTES = BN * BK / 2;        // this CTA's half of the B tile, 16 KB
 constexpr int SFA_STAGE_BYTES = 512;              // one 128x4 scale tile
@@ -70,9 +73,13 @@ constexpr uint32_t TMEM_SF_BASE = 256;            // scale columns start after t
 // Every epilogue warp stores through two staging tiles.  (64-column slices
 // with a 128-byte swizzle, half the store rows, measured slower for wgrad:
 // they cost a second stage of the ring.)
-template <bool BIGE, bool WG>
+//
+// QA (forward / dgrad with the A operand quantized in the prologue): a
+// 4-deep fp8 ring (3 with the larger tables) plus two bf16 A staging slots.
+template <bool BIGE, bool WG, bool QA = false>
 struct SmemLayout {
-  static constexpr int STAGES = (BIGE ? 5 : 6) - (WG ? 1 : 0);
+  static constexpr int STAGES = QA ? (BIGE ? 3 : 4) : (BIGE ? 5 : 6) - (WG ? 1 : 0);
+  static constexpr int QS = QA ? 2 : 0;                         // bf16 A slots
   static constexpr int MAXG = BIGE ? MAX_GROUPS : 512;
   static constexpr int NEPI = WG ? 8 : 4;                       // epilogue warps
   static constexpr int EC = BN * 4 / NEPI;                      // accumulator columns per epilogue warp
@@ -84,8 +91,11 @@ struct SmemLayout {
   static constexpr int b = a + STAGES * A_STAGE_BYTES;
   static constexpr int sfa = b + STAGES * B_STAGE_BYTES;
   static constexpr int sfb = sfa + STAGES * SFA_STAGE_BYTES;
-  static constexpr int bars = sfb + STAGES * SFB_STAGE_BYTES;   // 3*STAGES + 4 mbarriers
-  static constexpr int misc = bars + (3 * STAGES + 4) * 8;      // tmem addr, abort, counts
+  static constexpr int abf = (sfb + STAGES * SFB_STAGE_BYTES + 1023) / 1024 * 1024;
+  static constexpr int bars = abf + QS * QA_SLOT_BYTES;
+  // 3 per stage + 4, and for QA: afull per stage, abf_full / abf_empty per slot
+  static constexpr int NBARS = 3 * STAGES + 4 + (QA ? STAGES + 2 * QS : 0);
+  static constexpr int misc = bars + NBARS * 8;                 // tmem addr, abort, counts
   static constexpr int colscale = misc + 64;                    // 256 floats
   static constexpr int tiles_prefix = colscale + BN * 4;        // MAXG + 1 ints
   static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
@@ -94,10 +104,11 @@ struct SmemLayout {
   static constexpr int stg = (offs + (MAXG + 1) * 4 + 1023) / 1024 * 1024;
   static constexpr int total = stg + NEPI * STG_WARP_BYTES;
 };
-template <bool BIGE, bool WG>
-constexpr int smem_bytes() { return SmemLayout<BIGE, WG>::total + 1024; }  // + alignment slack
+template <bool BIGE, bool WG, bool QA = false>
+constexpr int smem_bytes() { return SmemLayout<BIGE, WG, QA>::total + 1024; }  // + alignment slack
 static_assert(smem_bytes<false, false>() <= 227 * 1024 && smem_bytes<true, false>() <= 227 * 1024 &&
-                  smem_bytes<false, true>() <= 227 * 1024 && smem_bytes<true, true>() <= 227 * 1024,
+                  smem_bytes<false, true>() <= 227 * 1024 && smem_bytes<true, true>() <= 227 * 1024 &&
+                  smem_bytes<false, false, true>() <= 227 * 1024 && smem_bytes<true, false, true>() <= 227 * 1024,
               "shared memory");
 
 // ---------------------------------------------------------------------------
@@ -125,6 +136,12 @@ FP8MOE_DEV uint32_t mapa_rank(uint32_t saddr, uint32_t rank) {
 // thousand cycles per arrive, on the accumulator hand-off's critical path).
 FP8MOE_DEV void mbar_arrive_remote(uint64_t* bar, uint32_t rank) {
   asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(mapa_rank(smem_u32(bar), rank))
+               : "memory");
+}
+// the same with a cluster-scoped release: publishes this thread's shared-memory
+// writes (after fence.proxy.async) that the other CTA's tensor-core work reads
+FP8MOE_DEV void mbar_arrive_remote_cluster(uint64_t* bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa_rank(smem_u32(bar), rank))
                : "memory");
 }
 FP8MOE_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -196,6 +213,8 @@ FP8MOE_DEV void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
 // ---------------------------------------------------------------------------
 struct KParams {
   GemmArgs g;
+  uint8_t* qa_out;    // QA: optional copy of the quantized A codes [M, kk]
+  uint8_t* sa_out;    // QA: optional copy of its e8m0 scales, row-major [M, kk / 32]
   int64_t cpb;        // 128x4 scale tiles per scale row block (A side and, fwd, B side)
   int64_t b_rows_pad; // fwd/dgrad: padded rows (cols of C) of one expert's scale matrix
   int n_tiles;        // tiles along the output columns
@@ -267,12 +286,13 @@ FP8MOE_DEV Tile get_tile(const KParams& p, const int* tiles_prefix, const int* b
   return tl;
 }
 
-template <bool MX, bool WGRAD, bool BIGE>
-__global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
+template <bool MX, bool WGRAD, bool BIGE, bool QA>
+__global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
     k_grouped_mm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                  const __grid_constant__ CUtensorMap tmOut, KParams p) {
-  using L = SmemLayout<BIGE, WGRAD>;
+  static_assert(!QA || (MX && !WGRAD), "the A-quantization prologue serves the MXFP8 forward / dgrad");
+  using L = SmemLayout<BIGE, WGRAD, QA>;
   constexpr int STAGES = L::STAGES;
   constexpr int CL = 2;  // cluster size: one pair
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -290,6 +310,12 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
   // before the CTA releases TMEM (matters on the timeout path)
   uint64_t* drain_mma = sf_full + STAGES;
   uint64_t* drain_cp = drain_mma + 1;
+  // QA: afull[s] (leader): the pair's quantized A stage and its scales are in
+  // shared memory; abf_full / abf_empty[j]: bf16 A slot j landed / was read
+  uint64_t* afull = drain_cp + 1;
+  uint64_t* abf_full = afull + STAGES;
+  uint64_t* abf_empty = abf_full + L::QS;
+  uint8_t* sAbf = smem + L::abf;
   uint32_t* tmem_base_holder = (uint32_t*)(smem + L::misc);
   volatile int* abort_flag = (volatile int*)(smem + L::misc + 4);
   int* total_tiles_s = (int*)(smem + L::misc + 8);
@@ -314,6 +340,13 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
     for (int s = 0; s < STAGES; ++s) mbar_init(&sf_full[s], 1);
     mbar_init(drain_mma, 1);
     mbar_init(drain_cp, 1);
+    if constexpr (QA) {
+      for (int s = 0; s < STAGES; ++s) mbar_init(&afull[s], 2 * 4);   // 4 quantization warps per CTA
+      for (int j = 0; j < L::QS; ++j) {
+        mbar_init(&abf_full[j], 1);
+        mbar_init(&abf_empty[j], 4);
+      }
+    }
     mbar_init(tmem_full, 1);
     // the leader's accumulator is free once both CTAs' epilogues drained
     mbar_init(tmem_empty, 2 * L::NEPI);
@@ -327,7 +360,7 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
     tc_fence_before();
   }
   // per-group tile counts and scale-block counts, then a scan
-  for (int e = threadIdx.x; e < g.E; e += num_threads<WGRAD>()) {
+  for (int e = threadIdx.x; e < g.E; e += num_threads<WGRAD, QA>()) {
     const int64_t gs = e == 0 ? 0 : g.offs[e - 1];
     const int64_t ge = g.offs[e];
     const int64_t sz = ge - gs;
@@ -410,6 +443,9 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
     uint32_t phase = 0;
     int filled[STAGES];  // phase of each stage's last fill, -1: never filled
     for (int s = 0; s < STAGES; ++s) filled[s] = -1;
+    int qslot = 0;                     // QA: bf16 A slot and its phase
+    uint32_t qphase = 0;
+    int qfilled[2] = {-1, -1};
     int cur_e = 0;
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
       const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, bounds, t, rank, cur_e);
@@ -420,14 +456,15 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
           break;
         }
         filled[stage] = (int)phase;
-        // this CTA loads its own 128 rows of A and its own half of B
-        uint32_t bytes = A_STAGE_BYTES + B_STAGE_BYTES;
+        // this CTA loads its own 128 rows of A and its own half of B (QA: the
+        // quantization warps fill A and its scales from the bf16 slot)
+        uint32_t bytes = (QA ? 0 : A_STAGE_BYTES) + B_STAGE_BYTES;
         const uint8_t* sfa_src = nullptr;
         const uint8_t* sfb_src0 = nullptr;
         const uint8_t* sfb_src1 = nullptr;
         if (MX) {
           sf_srcs(tl, ks, sfa_src, sfb_src0, sfb_src1);
-          bytes += 512 + 512 + (sfb_src1 ? 512 : 0);
+          bytes += (QA ? 0 : 512) + 512 + (sfb_src1 ? 512 : 0);
         }
         const int x = (int)(tl.x0 + (int64_t)ks * BK);
         const int brow = (int)(tl.col0 + rank * (BN / 2));
@@ -435,7 +472,7 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
         // expects the bytes of the pair (both CTAs load the same amounts)
         const uint32_t fb = mapa_rank(smem_u32(&full[stage]), lead);
         if (rank == 0) mbar_expect_tx(&full[stage], 2 * bytes);
-        tma_load_2d_cg2(sA + stage * A_STAGE_BYTES, &tmA, fb, x, (int)tl.row0);
+        if (!QA) tma_load_2d_cg2(sA + stage * A_STAGE_BYTES, &tmA, fb, x, (int)tl.row0);
         uint8_t* bdst = sB + stage * B_STAGE_BYTES;
         if (WGRAD) {
           tma_load_2d_cg2(bdst, &tmB, fb, x, brow);
@@ -446,10 +483,28 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
           // scale tiles as 1-D boxes of 128 u32 (= one 512-byte 128x4 tile)
           const uint8_t* sa0 = (const uint8_t*)g.a_scale;
           const uint8_t* sb0 = (const uint8_t*)g.b_scale;
-          tma_load_1d_cg2(sSFA + stage * SFA_STAGE_BYTES, &tmSFA, fb, (int)((sfa_src - sa0) / 4));
+          if (!QA) tma_load_1d_cg2(sSFA + stage * SFA_STAGE_BYTES, &tmSFA, fb, (int)((sfa_src - sa0) / 4));
           tma_load_1d_cg2(sSFB + stage * SFB_STAGE_BYTES, &tmSFB, fb, (int)((sfb_src0 - sb0) / 4));
           if (sfb_src1)
             tma_load_1d_cg2(sSFB + stage * SFB_STAGE_BYTES + 512, &tmSFB, fb, (int)((sfb_src1 - sb0) / 4));
+        }
+        if constexpr (QA) {
+          // the bf16 A tile of this k-stage (128 rows x 128 elements) into
+          // this CTA's slot, as two 64-column boxes with the 128-byte swizzle
+          if (!mbar_wait(&abf_empty[qslot], qphase ^ 1, abort_flag)) {
+            set_status(g.status, FP8MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          qfilled[qslot] = (int)qphase;
+          uint8_t* dst = sAbf + qslot * QA_SLOT_BYTES;
+          mbar_expect_tx(&abf_full[qslot], QA_SLOT_BYTES);
+          tma_load_2d(dst, &tmA, &abf_full[qslot], x, (int)tl.row0);
+          tma_load_2d(dst + QA_SLOT_BYTES / 2, &tmA, &abf_full[qslot], x + 64, (int)tl.row0);
+          if (++qslot == L::QS) {
+            qslot = 0;
+            qphase ^= 1;
+          }
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -477,6 +532,10 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
       for (int s = 0; s < STAGES; ++s)
         if (filled[s] >= 0) (void)mbar_wait(&full[s], (uint32_t)filled[s], nullptr);
     }
+    if (QA && *abort_flag) {
+      for (int j = 0; j < L::QS; ++j)
+        if (qfilled[j] >= 0) (void)mbar_wait(&abf_full[j], (uint32_t)qfilled[j], nullptr);
+    }
   } else if (warp == 1 && lane == 0 && rank == 1) {
     // the peer: the leader issues every MMA of the pair; nothing to do here
   } else if (warp == 1 && lane == 0) {
@@ -487,6 +546,7 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
     uint32_t acc_phase = 0;
     auto stage_ready = [&]() -> bool {
       if (!mbar_wait(&full[stage], phase, abort_flag)) return false;
+      if (QA && !mbar_wait_cluster(&afull[stage], phase, abort_flag)) return false;
       return !MX || mbar_wait(&sf_full[stage], phase, abort_flag);
     };
     int cur_e = 0;
@@ -565,7 +625,8 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
         const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, bounds, t, rank, cur_e);
         bool ok = true;
         for (int ks = 0; ks < tl.nk; ++ks) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag) ||
+              (QA && !mbar_wait_cluster(&afull[stage], phase, abort_flag))) {
             set_status(g.status, FP8MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             ok = false;
@@ -588,6 +649,90 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
       // every scale copy this thread issued has completed
       tc_commit_local(drain_cp);
       if (!mbar_wait(drain_cp, 0, nullptr)) set_status(g.status, FP8MOE_ERR_TIMEOUT);
+    }
+  } else if (QA && warp >= 7) {
+    // ================= A quantization (bf16 -> MXFP8) =================
+    // Each of the four warps takes 32 rows of the 128-row A tile, a lane one
+    // row: per k-stage the row's four 32-element blocks are read from the
+    // bf16 slot, their e8m0 scales taken from the block maxima, and the e4m3
+    // codes written into the fp8 stage the MMA reads (K-major, 128-byte
+    // swizzle: 16-byte chunk c of row r at r*128 + (c ^ (r % 8))*16) and the
+    // four scale bytes into the stage's 128x4 scale tile ((r % 32)*16 +
+    // (r / 32)*4 + block).  The arithmetic is the dim0 quantizer's.
+    const int cw = warp - 7;
+    const int r = cw * 32 + lane;
+    const uint32_t rx = (uint32_t)(r & 7);
+    int stage = 0, qslot = 0;
+    uint32_t phase = 0, qphase = 0;
+    int cur_e = 0;
+    for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
+      const Tile tl = get_tile<false>(p, tiles_prefix, blk_prefix, bounds, t, rank, cur_e);
+      // the optional copy of the codes and scales, written once per A row
+      // (by the pair on the first column tile)
+      const bool out_row = p.qa_out != nullptr && tl.col0 == 0 && r < tl.rows;
+      bool ok = true;
+      for (int ks = 0; ks < tl.nk; ++ks) {
+        if (!mbar_wait(&abf_full[qslot], qphase, abort_flag) || !mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+          set_status(g.status, FP8MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        const uint8_t* src = sAbf + qslot * QA_SLOT_BYTES + r * 128;
+        uint8_t* dst = sA + stage * A_STAGE_BYTES + r * 128;
+        uint32_t sbytes = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint8_t* hs = src + (b >> 1) * (QA_SLOT_BYTES / 2);
+          uint4 v[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            v[c] = *reinterpret_cast<const uint4*>(hs + ((((uint32_t)((b & 1) * 4 + c)) ^ rx) << 4));
+          uint32_t m2 = 0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            m2 = max_u16x2(m2, max_u16x2(max_u16x2(v[c].x & 0x7FFF7FFFu, v[c].y & 0x7FFF7FFFu),
+                                         max_u16x2(v[c].z & 0x7FFF7FFFu, v[c].w & 0x7FFF7FFFu)));
+          m2 = max_u16x2(m2, __byte_perm(m2, 0, 0x1032));   // both halves: the block's maximum
+          uint32_t p2;
+          const uint32_t sb = mx_block_scale(m2 & 0xFFFFu, p2);
+          const uint2 e0 = enc_row8(v[0], p2), e1 = enc_row8(v[1], p2);
+          const uint2 e2 = enc_row8(v[2], p2), e3 = enc_row8(v[3], p2);
+          const uint4 lo = make_uint4(e0.x, e0.y, e1.x, e1.y), hi = make_uint4(e2.x, e2.y, e3.x, e3.y);
+          *reinterpret_cast<uint4*>(dst + (((uint32_t)(2 * b) ^ rx) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((uint32_t)(2 * b + 1) ^ rx) << 4)) = hi;
+          sbytes |= sb << (8 * b);
+          const int64_t k0 = (int64_t)ks * BK + 32 * b;
+          if (out_row && k0 < g.kk) {
+            uint8_t* qo = p.qa_out + (tl.row0 + r) * g.kk + k0;
+            *reinterpret_cast<uint4*>(qo) = lo;
+            *reinterpret_cast<uint4*>(qo + 16) = hi;
+            p.sa_out[(tl.row0 + r) * (g.kk / 32) + k0 / 32] = (uint8_t)sb;
+          }
+        }
+        *reinterpret_cast<uint32_t*>(sSFA + stage * SFA_STAGE_BYTES + lane * 16 + cw * 4) = sbytes;
+        // the codes and scales are generic-proxy writes that the tensor core
+        // (async proxy) reads
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&abf_empty[qslot]);
+          if (rank == 0) {
+            mbar_arrive(&afull[stage]);
+          } else {
+            mbar_arrive_remote_cluster(&afull[stage], lead);
+          }
+        }
+        if (++qslot == L::QS) {
+          qslot = 0;
+          qphase ^= 1;
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
     }
   } else if (warp >= 2) {
     // ======================= epilogue =======================
@@ -657,7 +802,7 @@ __global__ void __launch_bounds__(num_threads<WGRAD>(), 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c_lo;
       // four epilogue warps: two 32-column loads in flight per wait (half the
       // load round trips); eight (a third fewer registers each): one
-      constexpr int LW = EC == 256 ? 64 : 32;   // columns per wait
+      constexpr int LW = EC == 256 && !QA ? 64 : 32;   // columns per wait
 #pragma unroll
       for (int c = 0; c < EC; c += LW) {
         uint32_t r0[32], r1[32];
@@ -763,18 +908,18 @@ static bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_
 static std::atomic<int> g_stall_next{0};
 void arm_gemm_stall_hook() { g_stall_next.store(1, std::memory_order_relaxed); }
 
-template <bool MX, bool WGRAD, bool BIGE>
+template <bool MX, bool WGRAD, bool BIGE, bool QA = false>
 static cudaError_t launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                             const CUtensorMap& tsb, const CUtensorMap& tout, const KParams& p, int64_t units,
                             cudaStream_t st) {
-  auto kern = k_grouped_mm<MX, WGRAD, BIGE>;
+  auto kern = k_grouped_mm<MX, WGRAD, BIGE, QA>;
   constexpr int CL = 2;
-  constexpr int SMEM = smem_bytes<BIGE, WGRAD>();
+  constexpr int SMEM = smem_bytes<BIGE, WGRAD, QA>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)CL);
-  cfg.blockDim = dim3(num_threads<WGRAD>());
+  cfg.blockDim = dim3(num_threads<WGRAD, QA>());
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -813,11 +958,16 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   // cta_group::2 pairs throughout; more than 512 groups take the variant
   // with the larger group tables and a 5-deep ring
   const bool bige = g.E > SmemLayout<false, false>::MAXG;
+  const bool qa = g.quant_a != 0;
+  if (qa && (!mx || wgrad)) return cudaErrorNotSupported;
   if (smem_bytes<true, true>() > g.max_smem || smem_bytes<true, false>() > g.max_smem ||
-      smem_bytes<false, true>() > g.max_smem || smem_bytes<false, false>() > g.max_smem)
+      smem_bytes<false, true>() > g.max_smem || smem_bytes<false, false>() > g.max_smem ||
+      smem_bytes<false, false, true>() > g.max_smem || smem_bytes<true, false, true>() > g.max_smem)
     return cudaErrorNotSupported;
   KParams p;
   p.g = g;
+  p.qa_out = qa ? g.qa_out : nullptr;
+  p.sa_out = qa ? g.sa_out : nullptr;
   p.stall_test = g_stall_next.exchange(0, std::memory_order_relaxed);
   p.n_tiles = (int)((g.cols + BN - 1) / BN);
   p.m_tiles_w = (int)((g.rows + BM - 1) / BM);
@@ -829,7 +979,13 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
     p.b_rows_pad = 0;
   }
   CUtensorMap ta, tb;
-  {
+  if (qa) {
+    // bf16 A [M, kk]: boxes of 64 elements (128 bytes) x 128 rows, 128-byte swizzle
+    cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)(g.M > 0 ? g.M : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)(g.kk * 2)};
+    cuuint32_t box[2] = {64, BM};
+    if (!make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.a, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  } else {
     const int64_t arows = wgrad ? g.rows : g.M;
     cuuint64_t dims[2] = {(cuuint64_t)g.kk, (cuuint64_t)(arows > 0 ? arows : 1)};
     cuuint64_t strides[1] = {(cuuint64_t)g.kk};
@@ -861,7 +1017,8 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   if (mx) {
     int64_t sa_bytes, sb_bytes;
     if (!wgrad) {
-      sa_bytes = ((g.M + 127) / 128 + g.E) * 128 * p.cpb * 4;
+      // (QA: the prologue makes the A scales; the map is not used)
+      sa_bytes = qa ? 512 : ((g.M + 127) / 128 + g.E) * 128 * p.cpb * 4;
       sb_bytes = (int64_t)g.E * p.b_rows_pad * p.cpb * 4;
     } else {
       sa_bytes = (g.rows + 127) / 128 * 128 * p.cpb * 4;
@@ -870,7 +1027,7 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
     cuuint64_t da[1] = {(cuuint64_t)(sa_bytes / 4)}, db[1] = {(cuuint64_t)(sb_bytes / 4)};
     cuuint64_t unused_stride[1] = {(cuuint64_t)16};
     cuuint32_t box[1] = {128};
-    if (!make_tmap(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.a_scale, 1, da, unused_stride, box,
+    if (!make_tmap(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, qa ? g.b_scale : g.a_scale, 1, da, unused_stride, box,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_tmap(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, g.b_scale, 1, db, unused_stride, box,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -900,6 +1057,9 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
                : launch_t<true, false, BIGE_>(ta, tb, tsa, tsb, tout, p, units, st))                      \
       : (wgrad ? launch_t<false, true, BIGE_>(ta, tb, tsa, tsb, tout, p, units, st)                       \
                : launch_t<false, false, BIGE_>(ta, tb, tsa, tsb, tout, p, units, st)))
+  if (qa)
+    return bige ? launch_t<true, false, true, true>(ta, tb, tsa, tsb, tout, p, units, st)
+                : launch_t<true, false, false, true>(ta, tb, tsa, tsb, tout, p, units, st);
   return bige ? FP8MOE_GMM_LAUNCH(true) : FP8MOE_GMM_LAUNCH(false);
 #undef FP8MOE_GMM_LAUNCH
 }
