@@ -38,11 +38,14 @@ METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMM
 # kernel per launch, averaged over one fwd, dgrad and wgrad launch of the Scout
-# W1 layer, from an ncu capture of those two counters.  It is reported only
-# while the kernel source is the one that was captured (same SHA-256).
+# W1 layer: an ncu capture of those counters on the first 8 experts, scaled to
+# the full layer by each mode's algorithmic bytes.  It is reported only while
+# the kernel source is the one that was captured (same SHA-256).
 GEMM_TRAFFIC = {"source": "mxfp8_moe_quantization_gb300/csrc/grouped_mm.cu",
-                "sha256": "547c6b0dc0b06e00eea7d43a215ce467c060a82952e29dd59eeb02341b4c512b",
-                "bytes_per_launch": (1030.651e6 + 1077.764e6 + 1563.850e6) / 3}
+                "sha256": "96564d8435f8c79ed97a4c57b2aedfe2f20959f71f402c8214965414a142e165",
+                # full-size Scout W1 fwd / dgrad / wgrad: algorithmic bytes x the
+                # traffic / algorithmic ratio of an 8-expert capture
+                "bytes_per_launch": (1030.4e6 + 1055.2e6 + 1486.9e6) / 3}
 
 
 def gemm_traffic():
@@ -779,6 +782,52 @@ def bench_rows(F, iters=10, only=None):
             del xt, a, outt
 
 
+def gemm_case(F, dev, n_experts):
+    """The Scout W1 grouped GEMMs restricted to the first ``n_experts`` experts
+    and their routed rows (fp8 codes of random bytes, unit e8m0 scales): a
+    reduced case of the same kernels for profiler captures.  Runs forward,
+    dgrad and wgrad once as warm-up and once timed, and prints the times."""
+    import torch
+    import workloads as W
+    E = n_experts
+    sizes = W.group_sizes("scout")[:E]
+    offs = torch.from_numpy(W.offsets_from_sizes(sizes)).to(dev)
+    M, N, K = int(sum(sizes)), W.get_workload("scout").N, W.get_workload("scout").K
+    g = torch.Generator(device=dev).manual_seed(0)
+
+    def codes(*shape):
+        return torch.randint(0, 120, shape, dtype=torch.uint8, device=dev, generator=g)
+
+    def unit(n):
+        return torch.full((n,), 127, dtype=torch.uint8, device=dev)
+    qa, qw, qdy, qwt, qdyt, qat = codes(M, K), codes(E, N, K), codes(M, N), codes(E, K, N), codes(N, M), codes(K, M)
+    sa = unit(F.fp8moe_swizzled_scales_bytes(1, M, K // 32, E, F.GROUP_ROWS))
+    sw = unit(F.fp8moe_swizzled_scales_bytes(E, N, K // 32))
+    sdy = unit(F.fp8moe_swizzled_scales_bytes(1, M, N // 32, E, F.GROUP_ROWS))
+    swt = unit(F.fp8moe_swizzled_scales_bytes(E, K, N // 32))
+    sdyt = unit(F.fp8moe_swizzled_scales_bytes(1, N, M // 32, E, F.GROUP_COLS))
+    sat = unit(F.fp8moe_swizzled_scales_bytes(1, K, M // 32, E, F.GROUP_COLS))
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    da = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    dw = torch.empty(E, N, K, dtype=torch.bfloat16, device=dev)
+    runs = [("fwd", lambda: F.fp8moe_scaled_grouped_mm_fwd(F.MXFP8, qa, sa, qw, sw, offs, out=out)),
+            ("dgrad", lambda: F.fp8moe_scaled_grouped_mm_dgrad(F.MXFP8, qdy, sdy, qwt, swt, offs, out=da)),
+            ("wgrad", lambda: F.fp8moe_scaled_grouped_mm_wgrad(F.MXFP8, qdyt, sdyt, qat, sat, offs, M, out=dw))]
+    for _, fn in runs:
+        fn()
+    torch.cuda.synchronize()
+    for name, fn in runs:
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        fn()
+        e0.record()
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(e0)
+        print(json.dumps({"case": f"scout W1, first {E} experts", "mode": name, "M": M, "N": N, "K": K,
+                          "us": round(ms * 1e3, 1), "tflops": round(2.0 * M * N * K / ms / 1e9, 1)}))
+    assert F.fp8moe_get_device_status() == 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -795,6 +844,9 @@ def main():
     ap.add_argument("--only", default=None,
                     help="with --rows: comma-separated sections (rowwise, colwise, tensorwise, mx, swizzle, gemm, "
                          "fused, layer, blockwise, routing)")
+    ap.add_argument("--gemm-case", type=int, default=0, metavar="E",
+                    help="run the Scout W1 grouped GEMMs on the first E experts only (a reduced case for "
+                         "profiler captures) and exit")
     ap.add_argument("--rows", action="store_true",
                     help="time every hot-path kernel at its configuration size (one JSON line each) and exit")
     args = ap.parse_args()
@@ -845,6 +897,9 @@ def main():
     torch.cuda.set_device(dev)
     if args.rows:
         bench_rows(F, only=args.only)
+        return
+    if args.gemm_case:
+        gemm_case(F, dev, args.gemm_case)
         return
     pg = None
     if world > 1:
