@@ -564,14 +564,14 @@ def bench_rows(F, iters=10, only=None):
         q = torch.empty(wll.shape[::-1], dtype=torch.uint8, device=dev)
         inv = torch.empty(1, ll.K, dtype=torch.float32, device=dev)
         ms = timed(lambda: F.fp8moe_quantize_colwise_3d(wll[None], None, True, q=q, scale_inv=inv))
-        emit("a2", "k_cw_amax + k_cw_cast", "llama3_8b W^T [1,14336,4096] transposed", ms, nbytes=wll.numel() * 3 + ll.K * 4)
+        emit("a2", "k_cw_cluster (one pass)", "llama3_8b W^T [1,14336,4096] transposed", ms, nbytes=wll.numel() * 3 + ll.K * 4)
         dsoffs = torch.from_numpy(ds.offs()).to(dev)
         for which in ("W1", "W2"):
             wds = W.make_weights(ds, which, device=dev)
             q = torch.empty((wds.shape[0], wds.shape[2], wds.shape[1]), dtype=torch.uint8, device=dev)
             inv = torch.empty(wds.shape[0], wds.shape[2], dtype=torch.float32, device=dev)
             ms = timed(lambda: F.fp8moe_quantize_colwise_3d(wds, None, True, q=q, scale_inv=inv))
-            emit("a2", "k_cw_amax + k_cw_cast", f"dsmoe_16b {which} {list(wds.shape)} transposed", ms,
+            emit("a2", "k_cw_cluster (one pass)", f"dsmoe_16b {which} {list(wds.shape)} transposed", ms,
                  nbytes=wds.numel() * 3 + wds.shape[0] * wds.shape[2] * 4)
             del wds
         ads = W.make_activations(ds, "A", device=dev)

@@ -385,6 +385,9 @@ static cudaError_t run_colwise(const void* x, int64_t E, int64_t R, int64_t C, c
 
 cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs, int transpose_out,
                            int kind, int64_t ldt, void* q, float* inv, int* status, int num_sms, cudaStream_t st) {
+  // dense weights with transposed output (the dgrad operand): one pass
+  if (!offs && transpose_out && colwise_cluster_supported(E, R, C))
+    return launch_colwise_cluster(x, E, R, C, kind, q, inv, status, num_sms, st);
   return run_colwise(x, E, R, C, offs, transpose_out, kind, ldt, q, inv, nullptr, status, num_sms, st);
 }
 

@@ -1,0 +1,385 @@
+// Colwise FP8 quantization of dense 3D expert weights with transposed
+// output, in one pass over HBM ("FP8-обучение на AMD", sections "MoE: почему
+// DeepSeek-V3 ломал пайплайн" (a column scale per expert) and "Три уровня
+// оптимизации Triton-ядер" (the backward colwise-scales kernel: the columns
+// staged on chip, a single pass, the transposed output written without a
+// separate copy)).
+//
+// x [E, R, C] bf16 -> q [E, C, R] codes, scale_inv [E, C].  A unit is one
+// expert's 64-column strip (128 bytes of every row).  A thread-block cluster
+// of CL CTAs owns a unit at a time, each CTA a slice of S rows (a multiple of
+// 32):
+//   1. the CTA's slice lands in shared memory by TMA (boxes of 128 rows x 64
+//      columns, 128-byte swizzle) and its column maxima are taken there;
+//   2. the cluster combines the CTAs' maxima through distributed shared
+//      memory, and every CTA derives the 64 scales;
+//   3. each CTA casts its slice from shared memory and writes the codes
+//      transposed: a lane turns 8 rows x 8 columns into 8-byte runs of its
+//      columns, four lanes complete a 32-byte sector of an output row.
+// A slice of more than CC_SR rows is processed in pieces: the maxima pass
+// loads every piece, the cast pass reloads them in reverse order (the last
+// piece is still resident; the others were read moments before and come
+// back from L2), so HBM still sees every input byte once.
+#include <cuda.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tma.cuh"
+
+namespace fp8moe {
+namespace {
+
+constexpr int CC_COLS = 64;                          // columns of a unit: 128 bytes of a bf16 row
+constexpr int CC_BOXR = 128;                         // rows of one TMA box
+constexpr int CC_BOX_BYTES = CC_BOXR * CC_COLS * 2;  // 16 KB
+constexpr int CC_NB_MAX = 6;                         // box slots of the larger ring: 96 KB, two CTAs per SM
+constexpr int CC_THREADS = 256;
+
+struct CcArgs {
+  int64_t E, R, C;
+  int64_t S;       // rows of a unit per CTA (a multiple of 32)
+  int64_t n_ct;    // 64-column tiles
+  int64_t units;   // E * n_ct
+  uint8_t* q;      // [E, C, R]
+  float* inv;      // [E, C]
+  int* status;
+};
+
+FP8MOE_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+FP8MOE_DEV uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+FP8MOE_DEV uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+FP8MOE_DEV void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+FP8MOE_DEV uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+  return a;
+}
+// a 32-bit store into CTA `rank`'s shared memory that completes 4 bytes of
+// the transaction count of the mbarrier at `bar` there (no fence: the peer
+// observes the data through its own barrier wait)
+FP8MOE_DEV void st_async_peer(const void* dst, const void* bar, uint32_t rank, uint32_t v) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(peer_addr(dst, rank)),
+               "r"(v), "r"(peer_addr(bar, rank))
+               : "memory");
+}
+
+// NB box slots.  PRE: a slice takes at most half of them, so the boxes of
+// the CTA's next units load while it casts the current one (a ring over the
+// sequence of its units' boxes); otherwise each unit's slice streams through
+// the ring on its own.
+template <int CL, int NB, bool PRE, bool FNUZ>
+__global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_constant__ CUtensorMap tmX, CcArgs a) {
+  constexpr int CC_NB = NB;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sx = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);  // CC_NB box slots
+  __shared__ uint64_t bars[NB];
+  // the cluster's column maxima (bf16 bits) by unit parity and source CTA,
+  // delivered by st.async; xbar[parity] completes when all CL x 64 landed
+  __shared__ uint32_t xmax[2][CL][CC_COLS];
+  __shared__ uint64_t xbar[2];
+  __shared__ uint4 wmax[8][8];           // per warp and 16-byte column chunk: 8 maxima as bf16 pairs
+  __shared__ float scol[CC_COLS];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
+  const int64_t cid = CL > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
+  const int64_t ncl = CL > 1 ? (int64_t)num_clusters_x() : (int64_t)gridDim.x;
+  if (tid == 0) {
+    for (int i = 0; i < CC_NB; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  // every CTA's barriers are initialised before a peer's st.async reaches them
+  if constexpr (CL > 1) cluster_barrier();
+  uint32_t xph = 0;  // phase bit of each exchange barrier
+  uint32_t phases = 0;     // phase bit of each slot's next completion
+  uint32_t pending = 0;    // slots with a load in flight (thread 0's view, for the exit path)
+  bool ok = true;          // false after a load that never completed: the CTA keeps
+                           // meeting its barriers but does no more work
+  int ub = 0;
+  const int cc = tid & 7, rp = tid >> 3;  // maxima pass: 16-byte column chunk, row phase (32)
+  const int cl = lane & 7, rq = lane >> 3;  // cast: 8 columns x 8 rows per lane in a 32-row sub-tile
+
+  const int64_t r0 = (int64_t)rank * a.S;  // this CTA's first row within each expert
+  const int nr = (int)(r0 < a.R ? (a.R - r0 < a.S ? a.R - r0 : a.S) : 0);
+  const int nbox = (nr + CC_BOXR - 1) / CC_BOXR;  // boxes of every unit's slice
+  // PRE: global box j (unit k = j / nbox of this CTA, box j % nbox) sits in
+  // slot j % NB; `issued` boxes have been requested so far
+  const int64_t my_units = cid < a.units ? (a.units - 1 - cid) / ncl + 1 : 0;
+  const int64_t total_boxes = my_units * nbox;
+  int64_t issued = 0;
+  auto unit_geom = [&](int64_t k, int64_t& g, int& col0) {
+    const int64_t u = cid + k * ncl;
+    g = u / a.n_ct;
+    col0 = (int)((u - g * a.n_ct) * CC_COLS);
+  };
+  // thread 0: global box j into its slot (PRE) / box `box` of the unit at
+  // (g, col0) into slot box % NB
+  auto issue_at = [&](int slot, int64_t g, int col0, int box) {
+    mbar_expect_tx(&bars[slot], CC_BOX_BYTES);
+    tma_load_2d(sx + slot * CC_BOX_BYTES, &tmX, &bars[slot], col0, (int)(g * a.R + r0 + (int64_t)box * CC_BOXR));
+    pending |= 1u << slot;
+  };
+  auto issue_global = [&](int64_t j) {
+    int64_t g;
+    int col0;
+    unit_geom(j / nbox, g, col0);
+    issue_at((int)(j % NB), g, col0, (int)(j % nbox));
+  };
+  auto wait_slot = [&](int slot) {
+    if (!mbar_wait(&bars[slot], (phases >> slot) & 1u, nullptr)) ok = false;
+    phases ^= 1u << slot;
+    if (tid == 0) pending &= ~(1u << slot);
+  };
+  // every thread is done with the slots before the ring refills them
+  auto refill_barrier = [&]() {
+    fence_proxy_async_smem();
+    ok = __syncthreads_and(ok) != 0;
+  };
+
+  int64_t k = 0;
+  for (int64_t u = cid; u < a.units; u += ncl, ub ^= 1, ++k) {
+    const int64_t g = u / a.n_ct;
+    const int col0 = (int)((u - g * a.n_ct) * CC_COLS);
+    // slot of box bx of this unit
+    auto slot_of = [&](int bx) { return PRE ? (int)((k * nbox + bx) % NB) : bx % NB; };
+    auto issue = [&](int box) { issue_at(box % NB, g, col0, box); };
+
+    // ---- 1. column maxima: the slice streams through the ring once
+    refill_barrier();
+    if (PRE) {
+      // the boxes whose slots are free: every box before this unit's has been cast
+      if (ok && tid == 0) {
+        const int64_t limit = k * nbox + NB < total_boxes ? k * nbox + NB : total_boxes;
+        for (; issued < limit; ++issued) issue_global(issued);
+      }
+    } else if (ok && tid == 0) {
+      for (int bx = 0; bx < nbox && bx < CC_NB; ++bx) issue(bx);
+    }
+    uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+    for (int bx = 0; bx < nbox && ok; ++bx) {
+      wait_slot(slot_of(bx));
+      const uint8_t* box = sx + slot_of(bx) * CC_BOX_BYTES;
+      const int n = nr - bx * CC_BOXR < CC_BOXR ? nr - bx * CC_BOXR : CC_BOXR;
+#pragma unroll 4
+      for (int r = rp; r < n; r += 32) {
+        const uint4 v = *reinterpret_cast<const uint4*>(box + (r & 127) * 128 + ((cc ^ (r & 7)) << 4));
+        m0 = __vmaxu2(m0, v.x & 0x7FFF7FFFu);
+        m1 = __vmaxu2(m1, v.y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+        m3 = __vmaxu2(m3, v.w & 0x7FFF7FFFu);
+      }
+      if (!PRE && bx + CC_NB < nbox) {
+        refill_barrier();
+        if (ok && tid == 0) issue(bx + CC_NB);
+      }
+    }
+    // lanes cc, cc + 8, cc + 16, cc + 24 hold the same columns
+#pragma unroll
+    for (int o = 8; o < 32; o <<= 1) {
+      m0 = __vmaxu2(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = __vmaxu2(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+      m3 = __vmaxu2(m3, __shfl_xor_sync(0xffffffffu, m3, o));
+    }
+    if (lane < 8) wmax[warp][lane] = make_uint4(m0, m1, m2, m3);
+    ok = __syncthreads_and(ok) != 0;
+    // ---- 2. the cluster's maxima -> scales
+    if (tid < CC_COLS) {
+      uint32_t mc = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const uint32_t pair = reinterpret_cast<const uint32_t*>(&wmax[w][tid >> 3])[(tid & 7) >> 1];
+        mc = max(mc, (tid & 1) ? pair >> 16 : pair & 0xFFFFu);
+      }
+      if constexpr (CL > 1) {
+        // to every CTA of the cluster (this one included), then wait for all
+        if (tid == 0) mbar_expect_tx(&xbar[ub], CL * CC_COLS * 4);
+#pragma unroll
+        for (int r = 0; r < CL; ++r) st_async_peer(&xmax[ub][rank][tid], &xbar[ub], (uint32_t)r, mc);
+        if (!mbar_wait(&xbar[ub], (xph >> ub) & 1u, nullptr)) ok = false;
+#pragma unroll
+        for (int r = 0; r < CL; ++r) mc = max(mc, xmax[ub][r][tid]);
+      }
+      float s, iv;
+      rowwise_scale<FNUZ>(bf16bits_to_float(mc), s, iv);
+      scol[tid] = s;
+      if (ok && rank == 0 && col0 + tid < a.C) a.inv[g * a.C + col0 + tid] = iv;
+    }
+    xph ^= 1u << ub;
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) continue;
+    // ---- 3. cast and transposed store
+    float sv[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) sv[t] = scol[cl * 8 + t];
+    const int64_t col = col0 + cl * 8;
+    // one 32-row x 64-column sub-tile: local row lr0 (a multiple of 8) of
+    // this lane, held in the slot at `box`
+    auto cast_sub = [&](const uint8_t* box, int lr0) {
+      if (lr0 >= nr || col >= a.C) return;  // R % 8 == 0: a lane's 8 rows are all in or all out
+      uint32_t w0[8], w1[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int r = (lr0 + k) & 127;
+        const uint4 v = *reinterpret_cast<const uint4*>(box + r * 128 + ((cl ^ (r & 7)) << 4));
+        w0[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v.x), sv[0]), __fmul_rn(bf16_hi(v.x), sv[1]),
+                           __fmul_rn(bf16_lo(v.y), sv[2]), __fmul_rn(bf16_hi(v.y), sv[3]));
+        w1[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
+                           __fmul_rn(bf16_lo(v.w), sv[6]), __fmul_rn(bf16_hi(v.w), sv[7]));
+      }
+      // q[g][col + t][row .. row + 7] for the 8 columns t
+      uint8_t* base = a.q + (g * a.C + col) * a.R + r0 + lr0;
+      uint32_t q0[4], q1[4];
+      transpose4x4(w0[0], w0[1], w0[2], w0[3], q0);
+      transpose4x4(w0[4], w0[5], w0[6], w0[7], q1);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)t * a.R) = make_uint2(q0[t], q1[t]);
+      transpose4x4(w1[0], w1[1], w1[2], w1[3], q0);
+      transpose4x4(w1[4], w1[5], w1[6], w1[7], q1);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)(4 + t) * a.R) = make_uint2(q0[t], q1[t]);
+    };
+    // the boxes still resident after the maxima pass (the last CC_NB), by
+    // all warps: sub-tile i of them is box first + i / 4, quarter i % 4
+    const int first = nbox > CC_NB ? nbox - CC_NB : 0;
+    for (int i = warp; i < (nbox - first) * 4; i += 8) {
+      const int bx = first + (i >> 2);
+      cast_sub(sx + slot_of(bx) * CC_BOX_BYTES, bx * CC_BOXR + (i & 3) * 32 + rq * 8);
+    }
+    // the earlier boxes come back through the ring (from L2: read moments ago)
+    if (first > 0) {
+      refill_barrier();
+      if (ok && tid == 0)
+        for (int bx = 0; bx < first && bx < CC_NB; ++bx) issue(bx);
+      for (int bx = 0; bx < first && ok; ++bx) {
+        wait_slot(bx % NB);
+        if (warp < 4) cast_sub(sx + (bx % CC_NB) * CC_BOX_BYTES, bx * CC_BOXR + warp * 32 + rq * 8);
+        if (bx + CC_NB < first) {
+          refill_barrier();
+          if (ok && tid == 0) issue(bx + CC_NB);
+        }
+      }
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok && tid == 0) set_status(a.status, FP8MOE_ERR_TIMEOUT);
+  }
+  // after a load that timed out, wait (bounded) for the loads still in flight
+  if (tid == 0)
+    for (int sl = 0; sl < CC_NB; ++sl)
+      if (pending & (1u << sl)) (void)mbar_wait(&bars[sl], (phases >> sl) & 1u, nullptr);
+  // no CTA leaves while its st.async to a peer may be in flight
+  if constexpr (CL > 1) cluster_barrier();
+}
+
+template <int CL, int NB, bool PRE, bool FNUZ>
+cudaError_t launch_cc(const CUtensorMap& tm, const CcArgs& a, int smem, int num_sms, cudaStream_t st) {
+  auto kern = k_cw_cluster<CL, NB, PRE, FNUZ>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(CC_THREADS);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)CL);
+  // persistent clusters: as many as are resident at once (per device and
+  // shared-memory size: this cache holds the size it was computed for)
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  constexpr int kMaxDev = 64;
+  static std::atomic<long long> cache[kMaxDev] = {};
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  long long c = cache[dev].load(std::memory_order_relaxed);
+  int ncl = (int)(c & 0xFFFFFFFF);
+  if ((int)(c >> 32) != smem || ncl <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&ncl, (void*)kern, &cfg) != cudaSuccess || ncl <= 0) {
+      (void)cudaGetLastError();
+      ncl = num_sms / CL;
+    }
+    if (ncl < 1) ncl = 1;
+    cache[dev].store(((long long)smem << 32) | (unsigned)ncl, std::memory_order_relaxed);
+  }
+  const int64_t nc = a.units < ncl ? a.units : ncl;
+  cfg.gridDim = dim3((unsigned)(CL * (nc < 1 ? 1 : nc)));
+  return cudaLaunchKernelEx(&cfg, kern, tm, a);
+}
+
+template <bool PRE, bool FNUZ>
+cudaError_t launch_cc_k(int CL, const CUtensorMap& tm, const CcArgs& a, int smem, int num_sms, cudaStream_t st) {
+  switch (CL) {
+    case 1: return launch_cc<1, CC_NB_MAX, PRE, FNUZ>(tm, a, smem, num_sms, st);
+    case 2: return launch_cc<2, CC_NB_MAX, PRE, FNUZ>(tm, a, smem, num_sms, st);
+    case 4: return launch_cc<4, CC_NB_MAX, PRE, FNUZ>(tm, a, smem, num_sms, st);
+    default: return launch_cc<8, CC_NB_MAX, PRE, FNUZ>(tm, a, smem, num_sms, st);
+  }
+}
+
+}  // namespace
+
+bool colwise_cluster_supported(int64_t E, int64_t R, int64_t C) {
+  return E > 0 && R > 0 && C > 0 && R % 8 == 0 && C % 16 == 0 && E * R < ((int64_t)1 << 31) &&
+         C < ((int64_t)1 << 31);
+}
+
+cudaError_t launch_colwise_cluster(const void* x, int64_t E, int64_t R, int64_t C, int kind, void* q, float* inv,
+                                   int* status, int num_sms, cudaStream_t st) {
+  // the smallest cluster whose CTAs' slices fit the ring (measured: every
+  // doubling of the cluster costs more in per-unit waiting for the slowest
+  // CTA than it saves), the largest one when none does (its CTAs then stream
+  // their slices through the ring); with room for two slices, the next
+  // unit's boxes load during the cast
+  auto rows_per_cta = [&](int cl) { return (((R + cl - 1) / cl) + 31) / 32 * 32; };
+  auto boxes_of = [&](int cl) { return (rows_per_cta(cl) + CC_BOXR - 1) / CC_BOXR; };
+  int CL = 0;
+  for (int cl = 1; cl <= 8 && !CL; cl *= 2)
+    if (boxes_of(cl) <= CC_NB_MAX) CL = cl;
+  if (!CL) CL = 8;
+  const bool pre = 2 * boxes_of(CL) <= CC_NB_MAX;
+  CcArgs a;
+  a.E = E;
+  a.R = R;
+  a.C = C;
+  a.S = rows_per_cta(CL);
+  a.n_ct = (C + CC_COLS - 1) / CC_COLS;
+  a.units = E * a.n_ct;
+  a.q = (uint8_t*)q;
+  a.inv = inv;
+  a.status = status;
+  const int smem = CC_NB_MAX * CC_BOX_BYTES + 1024;
+  CUtensorMap tm;
+  cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(E * R)};
+  cuuint64_t strides[1] = {(cuuint64_t)(C * 2)};
+  cuuint32_t box[2] = {CC_COLS, CC_BOXR};
+  if (!make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  const bool fnuz = kind == FP8MOE_E4M3FNUZ;
+  if (pre) return fnuz ? launch_cc_k<true, true>(CL, tm, a, smem, num_sms, st)
+                       : launch_cc_k<true, false>(CL, tm, a, smem, num_sms, st);
+  return fnuz ? launch_cc_k<false, true>(CL, tm, a, smem, num_sms, st)
+              : launch_cc_k<false, false>(CL, tm, a, smem, num_sms, st);
+}
+
+}  // namespace fp8moe

@@ -47,6 +47,11 @@ cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const
                            int transpose_out, int kind, int64_t ldt, void* q, float* inv, int* status,
                            int num_sms, cudaStream_t st);
 
+// colwise FP8 of dense [E, R, C] with transposed output in one HBM pass
+// (colwise_cluster.cu), for the sizes colwise_cluster_supported accepts
+bool colwise_cluster_supported(int64_t E, int64_t R, int64_t C);
+cudaError_t launch_colwise_cluster(const void* x, int64_t E, int64_t R, int64_t C, int kind, void* q, float* inv,
+                                   int* status, int num_sms, cudaStream_t st);
 // colwise transposed cast with one scale from the tensor's maximum (bf16
 // bits at amax_bits); no per-column scales
 cudaError_t launch_colwise_fixed(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs, int kind,

@@ -102,7 +102,12 @@ def test_rowwise_tiny_workload(F):
 
 @pytest.mark.parametrize("kind,okind", KINDS)
 @pytest.mark.parametrize("E,R,C", [(4, 256, 512), (2, 48, 32), (3, 64, 48), (1, 4096, 64),
-                                   (1, 14336, 32), (1, 24576, 16)])
+                                   (1, 14336, 32), (1, 24576, 16),
+                                   # transposed dense output runs one pass over clusters of 1-8
+                                   # CTAs: 2-CTA slices of 704 rows with a partial 64-column tile,
+                                   # 4-CTA slices with a ragged last one, 8-CTA slices of 800 rows
+                                   # (two pieces each, the second 32 rows)
+                                   (3, 1408, 80), (2, 2000, 48), (5, 6160, 16)])
 @pytest.mark.parametrize("trans", [True, False])
 def test_colwise_dense_parity(F, kind, okind, E, R, C, trans):
     x = _bf16((E, R, C), E * 1000 + R + C, 0.02)
