@@ -800,9 +800,9 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
       }
       uint32_t packed[EC / 2];
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c_lo;
-      // four epilogue warps: two 32-column loads in flight per wait (half the
-      // load round trips); eight (a third fewer registers each): one
-      constexpr int LW = EC == 256 && !QA ? 64 : 32;   // columns per wait
+      // two 32-column loads in flight per wait (half the load round trips);
+      // the A-quantization variant, which holds fewer registers, one
+      constexpr int LW = QA ? 32 : 64;   // columns per wait
 #pragma unroll
       for (int c = 0; c < EC; c += LW) {
         uint32_t r0[32], r1[32];
