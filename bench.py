@@ -586,7 +586,7 @@ def bench_rows(F, iters=10, only=None):
             q = torch.empty(t.shape, dtype=torch.uint8, device=dev)
             inv = torch.empty(1, dtype=torch.float32, device=dev)
             ms = timed(lambda: F.fp8moe_quantize_tensorwise(t, q=q, scale_inv=inv))
-            emit("next4", "k_tw_amax + k_tw_cast", f"llama3_8b {name} tensorwise", ms, nbytes=t.numel() * 3)
+            emit("next4", "k_tw_stream (one launch)", f"llama3_8b {name} tensorwise", ms, nbytes=t.numel() * 3)
     del x, wll
 
     # ---- MXFP8 quantization rows (a3, a4, a5, fused dual) on Scout and DeepSeek-V3

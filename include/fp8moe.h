@@ -130,6 +130,11 @@ fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, in
  * (4-byte aligned), the dequantization scale 1/s; it is used as scratch by
  * the call (stream-ordered).  Alignment: x, q 16 bytes; C % 16 == 0 when
  * transposed, (dense) R % 16 == 0 when transposed.  kind: e4m3fn or fnuz.
+ * The plain layout runs as one cooperative launch of one CTA per SM: it
+ * starts once every SM can take one of its CTAs (work on other streams
+ * that occupies SMs delays it), and each CTA holds the SM's whole TMEM.
+ * A wait inside it that exceeds 2 s sets FP8MOE_ERR_TIMEOUT in the device
+ * status.
  * ------------------------------------------------------------------------ */
 fp8moe_status fp8moe_quantize_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                                          int transpose_out, int kind, void* q, float* scale_inv,

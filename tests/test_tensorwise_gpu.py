@@ -35,7 +35,7 @@ def _kind(F, k):
 
 
 @pytest.mark.parametrize("kind", [OF.FN, OF.FNUZ])
-@pytest.mark.parametrize("shape", [(1024, 256), (7, 9), (3, 96, 160), (1, 5000, 48)])
+@pytest.mark.parametrize("shape", [(1024, 256), (7, 9), (3, 96, 160), (1, 5000, 48), (1023, 4099), (4096, 2048)])
 def test_tensorwise_plain(F, kind, shape):
     x = _bf16(shape, sum(shape) + 3, 2.0)
     q, inv = F.fp8moe_quantize_tensorwise(x.to(DEV), kind=_kind(F, kind))
