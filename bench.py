@@ -42,10 +42,10 @@ METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)
 # the full layer by each mode's algorithmic bytes.  It is reported only while
 # the kernel source is the one that was captured (same SHA-256).
 GEMM_TRAFFIC = {"source": "mxfp8_moe_quantization_gb300/csrc/grouped_mm.cu",
-                "sha256": "96564d8435f8c79ed97a4c57b2aedfe2f20959f71f402c8214965414a142e165",
+                "sha256": "02736c207b843f7e122025a08f91e37b44617fd12417b8bd461b5bd92dff0242",
                 # full-size Scout W1 fwd / dgrad / wgrad: algorithmic bytes x the
                 # traffic / algorithmic ratio of an 8-expert capture
-                "bytes_per_launch": (1030.4e6 + 1055.2e6 + 1486.9e6) / 3}
+                "bytes_per_launch": (1029.7e6 + 1053.4e6 + 1487.4e6) / 3}
 
 
 def gemm_traffic():
@@ -782,6 +782,31 @@ def bench_rows(F, iters=10, only=None):
             del xt, a, outt
 
 
+def dual_case(F, dev):
+    """The fused dual-direction MXFP8 quantization of the Scout activations
+    A [16640, 5120] (routing offsets of 16 experts, both code layouts with
+    grouped 128x4 scales): the step's first k_mx_dual launch on its own, a
+    case for profiler captures that holds under 1 GB on the device.  Runs
+    once as warm-up and once timed, and prints the time."""
+    import torch
+    import workloads as W
+    sc = W.get_workload("scout")
+    a = W.make_activations(sc, "A", device=dev)
+    offs = torch.from_numpy(sc.offs()).to(dev)
+    run = lambda: F.fp8moe_mxfp8_quantize_dual(a, offs, F.GROUP_ROWS, F.GROUP_COLS)
+    run()
+    torch.cuda.synchronize()
+    s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    run()
+    e0.record()
+    torch.cuda.synchronize()
+    ms = s0.elapsed_time(e0)
+    print(json.dumps({"case": "scout A dual-direction MXFP8", "shape": list(a.shape), "us": round(ms * 1e3, 1),
+                      "gbs": round(a.numel() * (2 + 2 + 2 / 32) / ms / 1e6, 1)}))
+    assert F.fp8moe_get_device_status() == 0
+
+
 def gemm_case(F, dev, n_experts):
     """The Scout W1 grouped GEMMs restricted to the first ``n_experts`` experts
     and their routed rows (fp8 codes of random bytes, unit e8m0 scales): a
@@ -847,6 +872,9 @@ def main():
     ap.add_argument("--gemm-case", type=int, default=0, metavar="E",
                     help="run the Scout W1 grouped GEMMs on the first E experts only (a reduced case for "
                          "profiler captures) and exit")
+    ap.add_argument("--dual-case", action="store_true",
+                    help="run the fused dual-direction quantization of the Scout activations once (a reduced "
+                         "case for profiler captures) and exit")
     ap.add_argument("--rows", action="store_true",
                     help="time every hot-path kernel at its configuration size (one JSON line each) and exit")
     args = ap.parse_args()
@@ -900,6 +928,9 @@ def main():
         return
     if args.gemm_case:
         gemm_case(F, dev, args.gemm_case)
+        return
+    if args.dual_case:
+        dual_case(F, dev)
         return
     pg = None
     if world > 1:
