@@ -7,13 +7,16 @@
 // forward and the two backward GEMMs); doing both from one read moves 4 bytes
 // per element instead of the 6 of two separate passes.
 //
-// Layout of the work (no shared-memory staging): a warp owns a band of up to
-// 128 rows x 128 columns and sweeps it in 32-row sub-tiles, so that every
-// 128-byte line of the transposed codes and of the scales is completed by one
-// warp within a short time (while it is still in L2); small tensors use lower
-// bands so that every warp gets work.  In a sub-tile, lane l
-// holds rows 16*(l/16) .. +15 of the 8 columns 8*(l%16) .. +7 in registers
-// (16 loads of 16 bytes, each warp load covering two 256-byte row segments).
+// Layout of the work: a warp owns a band of up to 128 rows x 128 columns and
+// sweeps it in 32-row sub-tiles, so that every 128-byte line of the
+// transposed codes and of the scales is completed by one warp within a short
+// time (while it is still in L2); small tensors use lower bands so that every
+// warp gets work.  Each warp has one 8 KB shared-memory buffer: a TMA load
+// brings the next sub-tile (32 rows x 128 columns) into it while the warp
+// works on the current one from registers, so every warp keeps a load in
+// flight through its arithmetic.  In a sub-tile, lane l holds rows
+// 16*(l/16) .. +15 of the 8 columns 8*(l%16) .. +7 in registers (16
+// conflict-free 16-byte shared loads).
 //   dim0: the 32-element block of a row spans 4 lanes: two shuffles give its
 //         absolute maximum; each lane encodes and stores its 8 codes, so a
 //         warp store writes two 128-byte row segments.
@@ -23,10 +26,15 @@
 //         32-byte output segment coming from the two lanes.
 #include <stdlib.h>
 
+#include <string.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "mxcvt.cuh"
 #include "scales.cuh"
+#include "tma.cuh"
 
 namespace fp8moe {
 
@@ -40,12 +48,26 @@ FP8MOE_DEV uint4 ld_nc16(const void* p) {
   return v;
 }
 
+FP8MOE_DEV uint4 lds16(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(saddr));
+  return v;
+}
+
+constexpr int DUAL_WARPS = 8;                 // warps per CTA
+constexpr int SUB_ROWS = 32;                  // rows of a sub-tile
+constexpr int SUB_BYTES = SUB_ROWS * 128 * 2; // one sub-tile of bf16 (128 columns at most)
+constexpr size_t DUAL_SMEM = (size_t)DUAL_WARPS * SUB_BYTES + DUAL_WARPS * sizeof(uint64_t);
+
 struct DualArgs {
   const uint16_t* x;    // [B, R, C] bf16
   int64_t B, R, C;
   uint32_t n_ct, n_band, tiles;  // 128 columns x bands of `nsub` 32-row sub-tiles
   uint32_t n_rt;
   int nsub;
+  int boxc;             // columns of the TMA box: min(128, C)
   uint8_t* q0;          // [B, R, C]
   uint8_t* q1;          // [B, C, R]
   ScaleSpec s0;         // [B, R, C/32] in its layout
@@ -72,7 +94,7 @@ template <int K>
 FP8MOE_DEV void dim1_pair(const uint4 (&v)[16], uint32_t mw, bool ok, uint8_t* q1c, int64_t R, uint32_t& b_lo,
                           uint32_t& b_hi) {
   // exponent fields of the two column maxima (sign bits are clear)
-  const uint32_t efl = max((mw >> 7) & 0xFFu, 8u), efh = max(mw >> 23, 8u);
+  const uint32_t efl = max((mw >> 7) & 0xFFu, 8u), efh = max((mw >> 23) & 0xFFu, 8u);
   const uint32_t blo = efl - 8u, bhi = efh - 8u;
   const uint32_t p2 = ((262u - efl) << 7) | ((262u - efh) << 23);
   uint32_t lo[4], hi[4];
@@ -96,10 +118,13 @@ FP8MOE_DEV void dim1_pair(const uint4 (&v)[16], uint32_t mw, bool ok, uint8_t* q
 }
 
 // D0 / D1: produce the dim0 / dim1 direction (the dim1-only instance serves
-// the standalone transposed quantization)
-template <bool D0, bool D1>
-__global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
+// the standalone transposed quantization).  PF: sub-tiles come through the
+// warp's shared-memory buffer, loaded one ahead by TMA; otherwise each lane
+// loads its 16 rows straight into registers when the sub-tile starts.
+template <bool D0, bool D1, bool PF>
+__global__ void __launch_bounds__(32 * DUAL_WARPS, 2) k_mx_dual(const __grid_constant__ CUtensorMap tx, DualArgs a) {
   __shared__ GroupTable gt0, gt1;
+  extern __shared__ __align__(1024) uint8_t dsm[];
   if (D0 && a.s0.layout == FP8MOE_GROUP_ROWS) {
     build_group_table(gt0, a.s0.offs, a.s0.E, a.R, GT_ROWS128, a.status);
     if (gt0.bad) return;
@@ -110,6 +135,46 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
   }
   const int lane = threadIdx.x & 31, half = lane >> 4, cl = lane & 15;
   const uint32_t nwarps = gridDim.x * (blockDim.x >> 5);
+  // this warp's sub-tile buffer and the barrier its loads complete on
+  const int wib = threadIdx.x >> 5;
+  uint8_t* wbuf = dsm + wib * SUB_BYTES;
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(dsm + DUAL_WARPS * SUB_BYTES) + wib;
+  if (PF && lane == 0) {
+    mbar_init(wbar, 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  const uint32_t box_bytes = (uint32_t)a.boxc * SUB_ROWS * 2;
+  // a band tile's column tile, first row block, batch and first row of x
+  struct Tile {
+    uint32_t ct, rt0;
+    int64_t b, row0;
+  };
+  auto tile_of = [&](uint32_t t) {
+    Tile u;
+    u.ct = t % a.n_ct;
+    const uint32_t rest = t / a.n_ct;
+    u.rt0 = (rest % a.n_band) * a.nsub;
+    u.b = rest / a.n_band;
+    u.row0 = u.b * a.R + (int64_t)u.rt0 * SUB_ROWS;
+    return u;
+  };
+  // load the sub-tile at (row, column) of x into the buffer (one lane)
+  auto issue = [&](int64_t row, uint32_t ct) {
+    mbar_expect_tx(wbar, box_bytes);
+    tma_load_2d(wbuf, &tx, wbar, (int)(ct * 128), (int)row);
+  };
+  uint32_t parity = 0;
+  bool live = true;  // false after a wait ran out: no further loads or waits
+  const uint32_t t_first = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  Tile cur;
+  if (t_first < a.tiles) {
+    cur = tile_of(t_first);
+    if (PF && lane == 0) issue(cur.row0, cur.ct);
+  }
+  // this lane's 16 rows x 16 bytes in the buffer
+  const uint32_t lbase = smem_u32(wbuf) + (uint32_t)(half * 16 * a.boxc * 2 + cl * 16);
+  const uint32_t lpitch = (uint32_t)a.boxc * 2;
   // Grouped layouts (B == 1): a warp's tiles come in increasing row order and
   // every 32-row sub-tile lies inside one routing group (offsets are
   // multiples of 32), so a forward-only cursor per table replaces the
@@ -118,11 +183,12 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
   auto advance = [](const GroupTable& gt, int E, int& g, int64_t r) {
     while (g < E - 1 && gt.end[g] <= r) ++g;
   };
-  for (uint32_t t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.tiles; t += nwarps) {
-    const uint32_t ct = t % a.n_ct;
-    const uint32_t rest = t / a.n_ct;
-    const uint32_t rt0 = (rest % a.n_band) * a.nsub;
-    const int64_t b = rest / a.n_band;
+  for (uint32_t t = t_first; t < a.tiles; t += nwarps) {
+    if (!PF) cur = tile_of(t);
+    const uint32_t ct = cur.ct, rt0 = cur.rt0;
+    const int64_t b = cur.b;
+    const bool more = PF && t + nwarps < a.tiles;
+    const Tile nxt = more ? tile_of(t + nwarps) : cur;
     // dim1 scale bytes of this lane's 8 columns over the band's row blocks
     // (byte `sub` of each word): the row blocks of a band are consecutive
     // scale bytes of a column in every layout, written as one word per column
@@ -132,10 +198,30 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
       const int64_t r = rt * 32 + half * 16;   // first of this lane's 16 rows
       const int64_t c = (int64_t)ct * 128 + cl * 8;   // first of this lane's 8 columns
       const bool ok = c < a.C;                 // C % 32 == 0: whole 4-lane groups are in or out
-      const uint16_t* xp = a.x + (b * a.R + r) * a.C + c;
       uint4 v[16];
+      if (!PF) {
+        const uint16_t* xp = a.x + (b * a.R + r) * a.C + c;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = ok ? ld_nc16(xp + i * a.C) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 16; ++i) v[i] = ok ? ld_nc16(xp + i * a.C) : make_uint4(0, 0, 0, 0);
+      } else {
+      if (live && !mbar_wait(wbar, parity, nullptr)) {
+        set_status(a.status, FP8MOE_ERR_TIMEOUT);
+        live = false;
+      }
+      parity ^= 1;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = ok ? lds16(lbase + i * lpitch) : make_uint4(0, 0, 0, 0);
+      // the buffer is free again: the next sub-tile of this warp's sequence
+      // starts loading while this one is worked on
+      __syncwarp();
+      }
+      if (PF && lane == 0 && live) {
+        fence_proxy_async_smem();
+        if (sub + 1 < a.nsub && rt0 + sub + 1 < a.n_rt)
+          issue(cur.row0 + (int64_t)(sub + 1) * SUB_ROWS, ct);
+        else if (more)
+          issue(nxt.row0, nxt.ct);
+      }
 
       if (D0) {
       // ---- dim0: blocks of 32 along each row (4 lanes x 8 columns).
@@ -164,11 +250,12 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
       uint8_t* q0p = a.q0 + (b * a.R + r) * a.C + c;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        uint32_t m2 = max_u16x2(max_u16x2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
-                                max_u16x2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
-        m2 = max_u16x2(m2, __byte_perm(m2, 0, 0x1032));   // both halves: the chunk's maximum
-        m2 = max_u16x2(m2, __shfl_xor_sync(FULL, m2, 1));
-        m2 = max_u16x2(m2, __shfl_xor_sync(FULL, m2, 2));
+        // magnitudes (the sign bits of m2 are meaningless; the exponent
+        // field below drops them)
+        uint32_t m2 = max_abs_bf16x2(max_abs_bf16x2(v[i].x, v[i].y), max_abs_bf16x2(v[i].z, v[i].w));
+        m2 = max_abs_bf16x2(m2, __byte_perm(m2, 0, 0x1032));   // both halves: the chunk's maximum
+        m2 = max_abs_bf16x2(m2, __shfl_xor_sync(FULL, m2, 1));
+        m2 = max_abs_bf16x2(m2, __shfl_xor_sync(FULL, m2, 2));
         const uint32_t ef = max((m2 >> 7) & 0xFFu, 8u);   // exponent field of the block maximum
         const uint32_t byte = ef - 8u;
         const uint32_t p2 = (262u - ef) * 0x00800080u;    // 2^-e in both bf16 halves
@@ -188,13 +275,13 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
       uint32_t mw[4] = {0, 0, 0, 0};   // column pairs (2k, 2k+1) as packed 16-bit maxima
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        mw[0] = max_u16x2(mw[0], v[i].x & 0x7FFF7FFFu);
-        mw[1] = max_u16x2(mw[1], v[i].y & 0x7FFF7FFFu);
-        mw[2] = max_u16x2(mw[2], v[i].z & 0x7FFF7FFFu);
-        mw[3] = max_u16x2(mw[3], v[i].w & 0x7FFF7FFFu);
+        mw[0] = max_abs_bf16x2(mw[0], v[i].x);
+        mw[1] = max_abs_bf16x2(mw[1], v[i].y);
+        mw[2] = max_abs_bf16x2(mw[2], v[i].z);
+        mw[3] = max_abs_bf16x2(mw[3], v[i].w);
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) mw[k] = max_u16x2(mw[k], __shfl_xor_sync(FULL, mw[k], 16));
+      for (int k = 0; k < 4; ++k) mw[k] = max_abs_bf16x2(mw[k], __shfl_xor_sync(FULL, mw[k], 16));
       // q1[b][c + j][r .. r + 15]
       uint8_t* q1c = a.q1 + (b * a.C + c) * a.R + r;
       uint32_t bl, bh;
@@ -255,6 +342,7 @@ __global__ void __launch_bounds__(256, 2) k_mx_dual(DualArgs a) {
         }
       }
     }
+    if (PF) cur = nxt;
   }
 }
 
@@ -288,18 +376,54 @@ cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void*
   const int64_t tiles = (int64_t)a.n_ct * a.n_band * B;
   if (tiles >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
   a.tiles = (uint32_t)tiles;
+  a.boxc = (int)(C < 128 ? C : 128);
   a.q0 = (uint8_t*)q0;
   a.q1 = (uint8_t*)q1;
   a.s0 = make_spec(s0, s0_layout, R, C / 32, offs, E);
   a.s1 = make_spec(s1, s1_layout, C, R / 32, offs, E);
   a.status = status;
-  int64_t grid = (a.tiles + 7) / 8;
+  static std::once_flag attr_once;
+  std::call_once(attr_once, [] {
+    cudaFuncSetAttribute(k_mx_dual<true, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DUAL_SMEM);
+    cudaFuncSetAttribute(k_mx_dual<false, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DUAL_SMEM);
+  });
+  int64_t grid = (a.tiles + DUAL_WARPS - 1) / DUAL_WARPS;
   const int64_t cap = (int64_t)num_sms * 2;
   if (grid > cap) grid = cap;
+  // the prefetching form for the dim1-only kernel and, for both directions,
+  // where every warp has few sub-tiles (its loads would otherwise wait in
+  // the open); plain loads where each warp has many sub-tiles of both
+  // directions' arithmetic (measured faster there: Scout W1 530 against 545
+  // us, DeepSeek-V3 W1 2951 against 3185 us; the activations 82 against 88).
+  // FP8MOE_DUAL_PREFETCH=0|1 fixes the form (tests cover both).
+  const int64_t subs_per_warp = (int64_t)a.tiles * a.nsub / (grid * DUAL_WARPS);
+  static const int pf_env = [] {
+    const char* v = getenv("FP8MOE_DUAL_PREFETCH");
+    return v ? atoi(v) : -1;
+  }();
+  const bool pf = pf_env >= 0 ? pf_env != 0 : (!q0 || subs_per_warp < 32);
+  // x as a 2D [B*R, C] bf16 tensor; one box is a sub-tile (columns past C
+  // read as zero)
+  CUtensorMap tx;
+  memset(&tx, 0, sizeof(tx));
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(B * R)};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)a.boxc, (cuuint32_t)SUB_ROWS};
+    if (pf && !make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
+  const size_t smem = pf ? DUAL_SMEM : 0;
   if (q0) {
-    k_mx_dual<true, true><<<(unsigned)grid, 256, 0, st>>>(a);
+    if (pf)
+      k_mx_dual<true, true, true><<<(unsigned)grid, 32 * DUAL_WARPS, smem, st>>>(tx, a);
+    else
+      k_mx_dual<true, true, false><<<(unsigned)grid, 32 * DUAL_WARPS, smem, st>>>(tx, a);
   } else {
-    k_mx_dual<false, true><<<(unsigned)grid, 256, 0, st>>>(a);
+    if (pf)
+      k_mx_dual<false, true, true><<<(unsigned)grid, 32 * DUAL_WARPS, smem, st>>>(tx, a);
+    else
+      k_mx_dual<false, true, false><<<(unsigned)grid, 32 * DUAL_WARPS, smem, st>>>(tx, a);
   }
   return cudaGetLastError();
 }

@@ -19,6 +19,16 @@ FP8MOE_DEV uint32_t max_u16x2(uint32_t a, uint32_t b) {
   asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
+// lane-wise max of the magnitudes of two bf16 pairs, in one instruction:
+// each half of the result has magnitude max(|a|, |b|) (NaN ignored unless
+// both are NaN, as in max_u16x2) and a sign bit that is the XOR of the
+// inputs' signs, which callers must not use (the exponent field, bits 7-14
+// of a half, is exact).
+FP8MOE_DEV uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 // The e8m0 byte of a block, clamp(floor(log2 amax) - 8, -127, 127) + 127, is
 // max(ef, 8) - 8 for the bf16 exponent field ef of the block maximum (a zero
 // or subnormal maximum has ef = 0 and gets byte 0, as the clamp gives); 2^-e

@@ -397,11 +397,30 @@ def test_mx_dual_band_heights(band):
     import os
     import subprocess
     import sys
-    if os.environ.get("FP8MOE_DUAL_BAND"):
-        pytest.skip("this process already fixes the band height")
+    if os.environ.get("FP8MOE_DUAL_BAND") or os.environ.get("FP8MOE_DUAL_PREFETCH"):
+        pytest.skip("this process already fixes the band height or the load form")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
                         os.path.abspath(__file__), "-k", "(mx_dual or mx_dim1) and not band_heights"],
                        cwd=root, env=dict(os.environ, FP8MOE_DUAL_BAND=band), capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("prefetch", ["0", "1"])
+def test_mx_dual_load_forms(prefetch):
+    """Both ways the fused kernel gets its sub-tiles (a TMA load into the
+    warp's buffer one sub-tile ahead, or plain loads into registers; chosen by
+    tensor size) give identical results: the dual / dim1 cases rerun with the
+    form fixed."""
+    import os
+    import subprocess
+    import sys
+    if os.environ.get("FP8MOE_DUAL_PREFETCH") or os.environ.get("FP8MOE_DUAL_BAND"):
+        pytest.skip("this process already fixes the load form or the band height")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
+                        os.path.abspath(__file__), "-k", "(mx_dual or mx_dim1) and not band_heights and not load_forms"],
+                       cwd=root, env=dict(os.environ, FP8MOE_DUAL_PREFETCH=prefetch), capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
