@@ -189,12 +189,14 @@ __global__ void __launch_bounds__(256, 4) k_bw_tokens(const uint16_t* __restrict
       *reinterpret_cast<float4*>(ip + 4) = make_float4(iv[4], iv[5], iv[6], iv[7]);
     }
     if (!rows_ok || !col_ok) continue;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) sv[t] = enc_mul<FNUZ>(sv[t]);
     uint32_t w0[8], w1[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      w0[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v[k].x), sv[0]), __fmul_rn(bf16_hi(v[k].x), sv[1]),
+      w0[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v[k].x), sv[0]), __fmul_rn(bf16_hi(v[k].x), sv[1]),
                          __fmul_rn(bf16_lo(v[k].y), sv[2]), __fmul_rn(bf16_hi(v[k].y), sv[3]));
-      w1[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v[k].z), sv[4]), __fmul_rn(bf16_hi(v[k].z), sv[5]),
+      w1[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v[k].z), sv[4]), __fmul_rn(bf16_hi(v[k].z), sv[5]),
                          __fmul_rn(bf16_lo(v[k].w), sv[6]), __fmul_rn(bf16_hi(v[k].w), sv[7]));
     }
     uint8_t* dst = qt + c * M + rr;

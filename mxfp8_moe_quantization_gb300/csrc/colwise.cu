@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(256) k_cw_cast(CwArgs a) {
       const uint32_t bits = fixed ? fixed_bits : a.amax[(int64_t)sb.g * a.C + c + t];
       float inv;
       rowwise_scale<FNUZ>(bf16bits_to_float(bits), sv[t], inv);
+      sv[t] = enc_mul<FNUZ>(sv[t]);
     }
     const int64_t rr = sb.r0 + rq * CW_LR;
     uint4 v[CW_LR];
@@ -220,9 +221,9 @@ __global__ void __launch_bounds__(256) k_cw_cast(CwArgs a) {
     uint32_t w0[CW_LR], w1[CW_LR];
 #pragma unroll
     for (int k = 0; k < CW_LR; ++k) {
-      w0[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v[k].x), sv[0]), __fmul_rn(bf16_hi(v[k].x), sv[1]),
+      w0[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v[k].x), sv[0]), __fmul_rn(bf16_hi(v[k].x), sv[1]),
                          __fmul_rn(bf16_lo(v[k].y), sv[2]), __fmul_rn(bf16_hi(v[k].y), sv[3]));
-      w1[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v[k].z), sv[4]), __fmul_rn(bf16_hi(v[k].z), sv[5]),
+      w1[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v[k].z), sv[4]), __fmul_rn(bf16_hi(v[k].z), sv[5]),
                          __fmul_rn(bf16_lo(v[k].w), sv[6]), __fmul_rn(bf16_hi(v[k].w), sv[7]));
     }
     if constexpr (!TRANS) {

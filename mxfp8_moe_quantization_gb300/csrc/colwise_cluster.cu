@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
     // ---- 3. cast and transposed store
     float sv[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) sv[t] = scol[cl * 8 + t];
+    for (int t = 0; t < 8; ++t) sv[t] = enc_mul<FNUZ>(scol[cl * 8 + t]);
     const int64_t col = col0 + cl * 8;
     // one 32-row x 64-column sub-tile: local row lr0 (a multiple of 8) of
     // this lane, held in the slot at `box`
@@ -240,9 +240,9 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
       for (int k = 0; k < 8; ++k) {
         const int r = (lr0 + k) & 127;
         const uint4 v = *reinterpret_cast<const uint4*>(box + r * 128 + ((cl ^ (r & 7)) << 4));
-        w0[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v.x), sv[0]), __fmul_rn(bf16_hi(v.x), sv[1]),
+        w0[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v.x), sv[0]), __fmul_rn(bf16_hi(v.x), sv[1]),
                            __fmul_rn(bf16_lo(v.y), sv[2]), __fmul_rn(bf16_hi(v.y), sv[3]));
-        w1[k] = enc4<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
+        w1[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
                            __fmul_rn(bf16_lo(v.w), sv[6]), __fmul_rn(bf16_hi(v.w), sv[7]));
       }
       // q[g][col + t][row .. row + 7] for the 8 columns t

@@ -49,37 +49,75 @@ FP8MOE_DEV uint32_t enc2(float lo, float hi) {
   }
 }
 
-// Four fp32 -> four codes packed little-endian into a 32-bit word.
-// fnuz, four at a time: the packed fn conversion of 2v, then two byte-wise
-// fix-ups.  A byte can need the 0x7F (= 240) code only where the fn
-// conversion gave +-448 (0x7E / 0xFE: |v| >= 216, within 10% of the fnuz
-// maximum), so the per-value check runs only when such a byte is present;
-// -0 (0x80) becomes the unsigned zero.
+// Four doubled values (2v) -> four fnuz codes packed little-endian: the
+// packed fn conversion of 2v, then two byte-wise fix-ups on the word (plain
+// bit arithmetic, exact per byte: no carry crosses a byte).  A byte can need
+// the 0x7F (= 240) code only where the fn conversion gave +-448 (0x7E /
+// 0xFE: |v| >= 216, within 10% of the fnuz maximum), so the per-value check
+// runs only when such a byte is present; -0 (0x80) becomes the unsigned zero.
+FP8MOE_DEV uint32_t enc4_fnuz_x2(float a, float b, float c, float d) {
+  uint32_t w = cvt_e4m3x2(a, b) | (cvt_e4m3x2(c, d) << 16);
+  const uint32_t y = (w & 0x7F7F7F7Fu) ^ 0x7E7E7E7Eu;   // a zero byte where the code is +-448
+  if ((y - 0x01010101u) & ~y & 0x80808080u) {            // some byte of y is zero
+    const float v2[4] = {a, b, c, d};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (fabsf(v2[i]) > 464.0f)
+        w = (w & ~(0xFFu << (8 * i))) | ((0x7Fu | (v2[i] < 0.0f ? 0x80u : 0u)) << (8 * i));
+  }
+  // bytes equal to 0x80: t = w ^ 0x80808080 has a zero byte there; nz has
+  // bit 7 set in every byte of t that is not zero
+  const uint32_t t = w ^ 0x80808080u;
+  const uint32_t z = ((((t & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | t) & 0x80808080u) ^ 0x80808080u;
+  return w & ~(z | (z - (z >> 7)));
+}
+
+// Four fp32 -> four codes packed little-endian into a 32-bit word (fnuz:
+// through the doubled values, see enc4_fnuz_x2).
 template <bool FNUZ>
 FP8MOE_DEV uint32_t enc4(float a, float b, float c, float d) {
   if constexpr (FNUZ) {
-    uint32_t w = cvt_e4m3x2(2.0f * a, 2.0f * b) | (cvt_e4m3x2(2.0f * c, 2.0f * d) << 16);
-    if (__vcmpeq4(w & 0x7F7F7F7Fu, 0x7E7E7E7Eu)) {
-      const float v[4] = {a, b, c, d};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (fabsf(2.0f * v[i]) > 464.0f)
-          w = (w & ~(0xFFu << (8 * i))) | ((0x7Fu | (v[i] < 0.0f ? 0x80u : 0u)) << (8 * i));
-    }
-    return w & ~__vcmpeq4(w, 0x80808080u);
+    return enc4_fnuz_x2(2.0f * a, 2.0f * b, 2.0f * c, 2.0f * d);
   } else {
     return enc2<false>(a, b) | (enc2<false>(c, d) << 16);
   }
 }
 
-// Encode 8 bf16 values (a uint4 of packed bf16 pairs) scaled by s.
+// The multiplier that enc4_pre takes: s itself, or 2s for fnuz (whose codes
+// come from the doubled values, see enc4_fnuz_x2 and enc8_bf16)
+template <bool FNUZ>
+FP8MOE_DEV float enc_mul(float s) {
+  return FNUZ ? 2.0f * s : s;
+}
+// Four products x * enc_mul(s) -> four codes
+template <bool FNUZ>
+FP8MOE_DEV uint32_t enc4_pre(float a, float b, float c, float d) {
+  if constexpr (FNUZ) {
+    return enc4_fnuz_x2(a, b, c, d);
+  } else {
+    return enc2<false>(a, b) | (enc2<false>(c, d) << 16);
+  }
+}
+
+// Encode 8 bf16 values (a uint4 of packed bf16 pairs) scaled by s.  fnuz
+// multiplies by 2s instead of doubling each product: x * 2s = 2 * (x * s)
+// exactly wherever the code can be non-zero (the two can differ only where
+// x * s is a subnormal fp32, far below the smallest fnuz code).
 template <bool FNUZ>
 FP8MOE_DEV uint2 enc8_bf16(uint4 v, float s) {
   uint2 r;
-  r.x = enc4<FNUZ>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s),
-                   __fmul_rn(bf16_lo(v.y), s), __fmul_rn(bf16_hi(v.y), s));
-  r.y = enc4<FNUZ>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s),
-                   __fmul_rn(bf16_lo(v.w), s), __fmul_rn(bf16_hi(v.w), s));
+  if constexpr (FNUZ) {
+    const float s2 = 2.0f * s;
+    r.x = enc4_fnuz_x2(__fmul_rn(bf16_lo(v.x), s2), __fmul_rn(bf16_hi(v.x), s2), __fmul_rn(bf16_lo(v.y), s2),
+                       __fmul_rn(bf16_hi(v.y), s2));
+    r.y = enc4_fnuz_x2(__fmul_rn(bf16_lo(v.z), s2), __fmul_rn(bf16_hi(v.z), s2), __fmul_rn(bf16_lo(v.w), s2),
+                       __fmul_rn(bf16_hi(v.w), s2));
+  } else {
+    r.x = enc4<false>(__fmul_rn(bf16_lo(v.x), s), __fmul_rn(bf16_hi(v.x), s), __fmul_rn(bf16_lo(v.y), s),
+                      __fmul_rn(bf16_hi(v.y), s));
+    r.y = enc4<false>(__fmul_rn(bf16_lo(v.z), s), __fmul_rn(bf16_hi(v.z), s), __fmul_rn(bf16_lo(v.w), s),
+                      __fmul_rn(bf16_hi(v.w), s));
+  }
   return r;
 }
 
