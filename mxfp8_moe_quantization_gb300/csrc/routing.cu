@@ -194,6 +194,9 @@ __global__ void __launch_bounds__(256) k_route_copy(const uint16_t* __restrict__
   }
 }
 
+// UK source rows at a time, VU 16-byte column chunks per lane and trip: UK x
+// VU loads in flight per lane (about 8 for every k).
+template <int UK, int VU>
 __global__ void __launch_bounds__(256) k_route_unpermute(const uint16_t* __restrict__ y, int64_t N,
                                                          const int32_t* __restrict__ row_of,
                                                          const float* __restrict__ w, int64_t T, int k,
@@ -202,27 +205,61 @@ __global__ void __launch_bounds__(256) k_route_unpermute(const uint16_t* __restr
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const int64_t nv = N / 8;
-  for (int64_t v = lane; v < nv; v += 32) {
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int j = 0; j < k; ++j) {
-      const int r = row_of[t * k + j];
-      if (r < 0) continue;
-      const float wt = w ? w[t * k + j] : 1.0f;
-      const uint4 s = reinterpret_cast<const uint4*>(y + (int64_t)r * N)[v];
-      const uint32_t q[4] = {s.x, s.y, s.z, s.w};
+  // the token's first UK source rows and weights, once (rows past k: -1)
+  int r0[UK];
+  float w0[UK];
+#pragma unroll
+  for (int j = 0; j < UK; ++j) {
+    r0[j] = j < k ? row_of[t * k + j] : -1;
+    w0[j] = (w && j < k) ? w[t * k + j] : 1.0f;
+  }
+  for (int64_t vb = lane; vb < nv; vb += 32 * VU) {
+    float acc[VU][8];
+#pragma unroll
+    for (int u = 0; u < VU; ++u)
+#pragma unroll
+      for (int h = 0; h < 8; ++h) acc[u][h] = 0.0f;
+    for (int j0 = 0; j0 < k; j0 += UK) {
+      int rj[UK];
+      float wj[UK];
+#pragma unroll
+      for (int j = 0; j < UK; ++j) {
+        rj[j] = j0 == 0 ? r0[j] : (j0 + j < k ? row_of[t * k + j0 + j] : -1);
+        wj[j] = j0 == 0 ? w0[j] : ((w && j0 + j < k) ? w[t * k + j0 + j] : 1.0f);
+      }
+      // every load of the group first, then the sums in slot order
+      uint4 sv[VU][UK];
+#pragma unroll
+      for (int u = 0; u < VU; ++u)
+#pragma unroll
+        for (int j = 0; j < UK; ++j)
+          sv[u][j] = (rj[j] >= 0 && vb + 32 * u < nv) ? ld_nc16(y + (int64_t)rj[j] * N + (vb + 32 * u) * 8)
+                                                      : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < VU; ++u)
+#pragma unroll
+        for (int j = 0; j < UK; ++j) {
+          if (rj[j] < 0) continue;
+          const uint32_t q[4] = {sv[u][j].x, sv[u][j].y, sv[u][j].z, sv[u][j].w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            acc[u][2 * h] = __fadd_rn(acc[u][2 * h], w ? __fmul_rn(wj[j], bf16_lo(q[h])) : bf16_lo(q[h]));
+            acc[u][2 * h + 1] =
+                __fadd_rn(acc[u][2 * h + 1], w ? __fmul_rn(wj[j], bf16_hi(q[h])) : bf16_hi(q[h]));
+          }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < VU; ++u) {
+      if (vb + 32 * u >= nv) break;
+      uint32_t o[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        acc[2 * h] = __fadd_rn(acc[2 * h], w ? __fmul_rn(wt, bf16_lo(q[h])) : bf16_lo(q[h]));
-        acc[2 * h + 1] = __fadd_rn(acc[2 * h + 1], w ? __fmul_rn(wt, bf16_hi(q[h])) : bf16_hi(q[h]));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[u][2 * h], acc[u][2 * h + 1]);
+        o[h] = *reinterpret_cast<const uint32_t*>(&b);
       }
+      reinterpret_cast<uint4*>(out + t * N)[vb + 32 * u] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    uint32_t o[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
-      o[h] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    reinterpret_cast<uint4*>(out + t * N)[v] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -292,7 +329,16 @@ cudaError_t launch_route_unpermute(const void* y, int64_t N, const int32_t* row_
                                    int64_t k, void* out, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int64_t blocks = (T + 7) / 8;
-  k_route_unpermute<<<(unsigned)blocks, 256, 0, st>>>((const uint16_t*)y, N, row_of, w, T, (int)k, (uint16_t*)out);
+  const uint16_t* yp = (const uint16_t*)y;
+  uint16_t* op = (uint16_t*)out;
+  if (k <= 1)
+    k_route_unpermute<1, 8><<<(unsigned)blocks, 256, 0, st>>>(yp, N, row_of, w, T, (int)k, op);
+  else if (k <= 2)
+    k_route_unpermute<2, 4><<<(unsigned)blocks, 256, 0, st>>>(yp, N, row_of, w, T, (int)k, op);
+  else if (k <= 4)
+    k_route_unpermute<4, 2><<<(unsigned)blocks, 256, 0, st>>>(yp, N, row_of, w, T, (int)k, op);
+  else
+    k_route_unpermute<8, 1><<<(unsigned)blocks, 256, 0, st>>>(yp, N, row_of, w, T, (int)k, op);
   return cudaGetLastError();
 }
 

@@ -55,9 +55,12 @@ def test_permute_parity(F, T, k, E, H, dup):
 
 
 @pytest.mark.parametrize("weighted", [False, True])
-def test_unpermute_parity(F, weighted):
-    T, k, E, N = 500, 3, 7, 96
-    idx, w = _topk(T, k, E, 9)
+@pytest.mark.parametrize("k,N", [(3, 96), (1, 2056), (2, 1032), (8, 520), (11, 264)])
+def test_unpermute_parity(F, weighted, k, N):
+    """Every shape of the combine kernel (source rows loaded 1, 2, 4 or 8 at a
+    time; k = 11 takes a second group) and ragged column chunk counts."""
+    T, E = 500, 13
+    idx, w = _topk(T, k, E, 9 + k)
     _, _, rrow = RT.route_permute(np.zeros((T, 8), np.float32), idx, E)
     y = _bf16((RT.route_rows(T, k, E), N), 10)
     out = F.fp8moe_route_unpermute(y.to(DEV), torch.from_numpy(rrow).to(DEV),
