@@ -578,7 +578,7 @@ def bench_rows(F, iters=10, only=None):
         q = torch.empty((ds.K, F.fp8moe_jagged_t_cols(ds.M, ds.E)), dtype=torch.uint8, device=dev)
         inv = torch.empty(ds.E, ds.K, dtype=torch.float32, device=dev)
         ms = timed(lambda: F.fp8moe_quantize_colwise_3d(ads, dsoffs, True, q=q, scale_inv=inv))
-        emit("a2", "k_cw_amax + k_cw_cast", f"dsmoe_16b jagged A [{ds.M},{ds.K}] transposed", ms,
+        emit("a2", "k_cw_cluster jagged (one pass)", f"dsmoe_16b jagged A [{ds.M},{ds.K}] transposed", ms,
              nbytes=ads.numel() * 3 + ds.E * ds.K * 4)
         del ads
     if want("tensorwise"):

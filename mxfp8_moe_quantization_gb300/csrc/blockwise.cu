@@ -155,15 +155,15 @@ __global__ void __launch_bounds__(256, 4) k_bw_tokens(const uint16_t* __restrict
     uint32_t m[4] = {0, 0, 0, 0};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      m[0] = __vmaxu2(m[0], v[k].x & 0x7FFF7FFFu);
-      m[1] = __vmaxu2(m[1], v[k].y & 0x7FFF7FFFu);
-      m[2] = __vmaxu2(m[2], v[k].z & 0x7FFF7FFFu);
-      m[3] = __vmaxu2(m[3], v[k].w & 0x7FFF7FFFu);
+      m[0] = umax16x2(m[0], v[k].x & 0x7FFF7FFFu);
+      m[1] = umax16x2(m[1], v[k].y & 0x7FFF7FFFu);
+      m[2] = umax16x2(m[2], v[k].z & 0x7FFF7FFFu);
+      m[3] = umax16x2(m[3], v[k].w & 0x7FFF7FFFu);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      m[i] = __vmaxu2(m[i], __shfl_xor_sync(0xffffffffu, m[i], 8));
-      m[i] = __vmaxu2(m[i], __shfl_xor_sync(0xffffffffu, m[i], 16));
+      m[i] = umax16x2(m[i], __shfl_xor_sync(0xffffffffu, m[i], 8));
+      m[i] = umax16x2(m[i], __shfl_xor_sync(0xffffffffu, m[i], 16));
     }
     __syncthreads();  // the previous unit's reads of red are done
     if (rq == 0) red[rq4][ch][cl] = make_uint4(m[0], m[1], m[2], m[3]);
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(256, 4) k_bw_tokens(const uint16_t* __restrict
       const uint32_t* p1 = reinterpret_cast<const uint32_t*>(&red[1][ch][cl]);
       const uint32_t* p2 = reinterpret_cast<const uint32_t*>(&red[2][ch][cl]);
       const uint32_t* p3 = reinterpret_cast<const uint32_t*>(&red[3][ch][cl]);
-      cm[i] = __vmaxu2(__vmaxu2(p0[i], p1[i]), __vmaxu2(p2[i], p3[i]));
+      cm[i] = umax16x2(umax16x2(p0[i], p1[i]), umax16x2(p2[i], p3[i]));
     }
     float sv[8], iv[8];
 #pragma unroll

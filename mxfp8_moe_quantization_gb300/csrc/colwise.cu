@@ -147,19 +147,19 @@ __global__ void __launch_bounds__(256) k_cw_amax(CwArgs a) {
       load_rows(a, sb.r0 + rq * CW_LR, sb.r1, c, v);
 #pragma unroll
       for (int k = 0; k < CW_LR; ++k) {
-        m0 = __vmaxu2(m0, v[k].x & 0x7FFF7FFFu);
-        m1 = __vmaxu2(m1, v[k].y & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, v[k].z & 0x7FFF7FFFu);
-        m3 = __vmaxu2(m3, v[k].w & 0x7FFF7FFFu);
+        m0 = umax16x2(m0, v[k].x & 0x7FFF7FFFu);
+        m1 = umax16x2(m1, v[k].y & 0x7FFF7FFFu);
+        m2 = umax16x2(m2, v[k].z & 0x7FFF7FFFu);
+        m3 = umax16x2(m3, v[k].w & 0x7FFF7FFFu);
       }
     }
     // the row groups of a column sit in lanes cl, cl + NCL, ...
 #pragma unroll
     for (int o = CW_NCL; o < 32; o <<= 1) {
-      m0 = __vmaxu2(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-      m1 = __vmaxu2(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-      m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, o));
-      m3 = __vmaxu2(m3, __shfl_xor_sync(0xffffffffu, m3, o));
+      m0 = umax16x2(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = umax16x2(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      m2 = umax16x2(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+      m3 = umax16x2(m3, __shfl_xor_sync(0xffffffffu, m3, o));
     }
     if (lane < CW_NCL) red[warp][lane] = make_uint4(m0, m1, m2, m3);
     if (lane == 0) gsel[warp] = sb.g;
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(256) k_cw_amax(CwArgs a) {
             cur = gw;
             acc = 0;
           }
-          acc = __vmaxu2(acc, reinterpret_cast<const uint32_t*>(&red[w][l])[wi]);
+          acc = umax16x2(acc, reinterpret_cast<const uint32_t*>(&red[w][l])[wi]);
         }
         flush_max(a, cur, col, acc);
       }
@@ -386,9 +386,12 @@ static cudaError_t run_colwise(const void* x, int64_t E, int64_t R, int64_t C, c
 
 cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs, int transpose_out,
                            int kind, int64_t ldt, void* q, float* inv, int* status, int num_sms, cudaStream_t st) {
-  // dense weights with transposed output (the dgrad operand): one pass
+  // transposed output (the dgrad operand of dense weights, the wgrad operand
+  // of routed rows): one pass
   if (!offs && transpose_out && colwise_cluster_supported(E, R, C))
     return launch_colwise_cluster(x, E, R, C, kind, q, inv, status, num_sms, st);
+  if (offs && transpose_out && R > 0 && colwise_cluster_jagged_supported(E, R, C))
+    return launch_colwise_cluster_jagged(x, E, R, C, offs, kind, ldt, q, inv, status, num_sms, st);
   return run_colwise(x, E, R, C, offs, transpose_out, kind, ldt, q, inv, nullptr, status, num_sms, st);
 }
 

@@ -1,12 +1,14 @@
-// Colwise FP8 quantization of dense 3D expert weights with transposed
-// output, in one pass over HBM ("FP8-обучение на AMD", sections "MoE: почему
-// DeepSeek-V3 ломал пайплайн" (a column scale per expert) and "Три уровня
-// оптимизации Triton-ядер" (the backward colwise-scales kernel: the columns
-// staged on chip, a single pass, the transposed output written without a
-// separate copy)).
+// Colwise FP8 quantization with transposed output, in one pass over HBM, of
+// dense 3D expert weights and of routed rows grouped by offsets
+// ("FP8-обучение на AMD", sections "MoE: почему DeepSeek-V3 ломал пайплайн"
+// (a column scale per expert) and "Три уровня оптимизации Triton-ядер" (the
+// backward colwise-scales kernel: the columns staged on chip, a single pass,
+// the transposed output written without a separate copy)).
 //
-// x [E, R, C] bf16 -> q [E, C, R] codes, scale_inv [E, C].  A unit is one
-// expert's 64-column strip (128 bytes of every row).  A thread-block cluster
+// Dense: x [E, R, C] bf16 -> q [E, C, R] codes, scale_inv [E, C].  Jagged:
+// x [R, C] in E groups -> q [C, ldt] (group-padded columns), scale_inv
+// [E, C].  A unit is one expert's (group's) 64-column strip (128 bytes of
+// every row).  A thread-block cluster
 // of CL CTAs owns a unit at a time, each CTA a slice of S rows (a multiple of
 // 32):
 //   1. the CTA's slice lands in shared memory by TMA (boxes of 128 rows x 64
@@ -23,9 +25,11 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
+#include "scales.cuh"
 #include "tma.cuh"
 
 namespace fp8moe {
@@ -38,12 +42,14 @@ constexpr int CC_NB_MAX = 6;                         // box slots of the larger 
 constexpr int CC_THREADS = 256;
 
 struct CcArgs {
-  int64_t E, R, C;
-  int64_t S;       // rows of a unit per CTA (a multiple of 32)
+  int64_t E, R, C;  // jagged: E groups of routed rows, R rows in all
+  int64_t S;       // dense: rows of a unit per CTA (a multiple of 32)
   int64_t n_ct;    // 64-column tiles
   int64_t units;   // E * n_ct
-  uint8_t* q;      // [E, C, R]
+  uint8_t* q;      // dense [E, C, R]; jagged [C, ldt]
   float* inv;      // [E, C]
+  const int32_t* offs;  // jagged: group ends
+  int64_t ldt;     // jagged: row length of q (group g at column 32 * its 32-row blocks before it)
   int* status;
 };
 
@@ -83,8 +89,19 @@ FP8MOE_DEV void st_async_peer(const void* dst, const void* bar, uint32_t rank, u
 // the CTA's next units load while it casts the current one (a ring over the
 // sequence of its units' boxes); otherwise each unit's slice streams through
 // the ring on its own.
-template <int CL, int NB, bool PRE, bool FNUZ>
+// JAG: routed rows [R, C] in E groups (offsets), codes in the group-padded
+// transposed layout [C, ldt] (group g's rows at columns 32 * pad[g] ..., its
+// padding up to the next multiple of 32 and the slack after the last group
+// zero).  A unit is a group's 64-column strip; the CTAs of a cluster split
+// the group's rows.  Units go to clusters largest group first, in a snake
+// order (round k forward for even k, backward for odd), so the clusters'
+// loads even out although group sizes vary widely.
+template <int CL, int NB, bool PRE, bool FNUZ, bool JAG>
 __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_constant__ CUtensorMap tmX, CcArgs a) {
+  static_assert(!(JAG && PRE), "jagged units stream on their own");
+  // jagged: the group table and the group order (largest first)
+  __shared__ std::conditional_t<JAG, GroupTable, char> gt_s;
+  __shared__ std::conditional_t<JAG, int[QG_MAX], char> order_s;
   constexpr int CC_NB = NB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sx = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);  // CC_NB box slots
@@ -106,6 +123,22 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
     mbar_fence_init();
   }
   __syncthreads();
+  if constexpr (JAG) {
+    // every CTA builds the same table, so a bad offsets vector sends every
+    // CTA home here (before any cluster barrier)
+    build_group_table(gt_s, a.offs, (int)a.E, a.R, GT_SUB32, a.status);
+    if (gt_s.bad) return;
+    for (int g = tid; g < (int)a.E; g += CC_THREADS) {
+      const int64_t sg = gt_s.end[g] - (g ? gt_s.end[g - 1] : 0);
+      int rk = 0;
+      for (int h = 0; h < (int)a.E; ++h) {
+        const int64_t sh = gt_s.end[h] - (h ? gt_s.end[h - 1] : 0);
+        rk += (sh > sg || (sh == sg && h < g)) ? 1 : 0;
+      }
+      order_s[rk] = g;
+    }
+    __syncthreads();
+  }
   // every CTA's barriers are initialised before a peer's st.async reaches them
   if constexpr (CL > 1) cluster_barrier();
   uint32_t xph = 0;  // phase bit of each exchange barrier
@@ -117,9 +150,14 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
   const int cc = tid & 7, rp = tid >> 3;  // maxima pass: 16-byte column chunk, row phase (32)
   const int cl = lane & 7, rq = lane >> 3;  // cast: 8 columns x 8 rows per lane in a 32-row sub-tile
 
-  const int64_t r0 = (int64_t)rank * a.S;  // this CTA's first row within each expert
-  const int nr = (int)(r0 < a.R ? (a.R - r0 < a.S ? a.R - r0 : a.S) : 0);
-  const int nbox = (nr + CC_BOXR - 1) / CC_BOXR;  // boxes of every unit's slice
+  // dense: this CTA's first row within each expert, its rows and boxes (the
+  // same for every unit); jagged: set per unit
+  int64_t r0 = (int64_t)rank * a.S;
+  int nr = (int)(r0 < a.R ? (a.R - r0 < a.S ? a.R - r0 : a.S) : 0);
+  int nbox = (nr + CC_BOXR - 1) / CC_BOXR;
+  int npad = nr;          // rows whose codes this CTA writes (jagged: padding included)
+  int64_t xrow0 = 0;      // row of x where this CTA's slice of the unit starts
+  int64_t qcol0 = 0;      // jagged: column of q where the unit's group starts
   // PRE: global box j (unit k = j / nbox of this CTA, box j % nbox) sits in
   // slot j % NB; `issued` boxes have been requested so far
   const int64_t my_units = cid < a.units ? (a.units - 1 - cid) / ncl + 1 : 0;
@@ -134,7 +172,8 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
   // (g, col0) into slot box % NB
   auto issue_at = [&](int slot, int64_t g, int col0, int box) {
     mbar_expect_tx(&bars[slot], CC_BOX_BYTES);
-    tma_load_2d(sx + slot * CC_BOX_BYTES, &tmX, &bars[slot], col0, (int)(g * a.R + r0 + (int64_t)box * CC_BOXR));
+    const int64_t row = JAG ? xrow0 + (int64_t)box * CC_BOXR : g * a.R + r0 + (int64_t)box * CC_BOXR;
+    tma_load_2d(sx + slot * CC_BOX_BYTES, &tmX, &bars[slot], col0, (int)row);
     pending |= 1u << slot;
   };
   auto issue_global = [&](int64_t j) {
@@ -154,13 +193,85 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
     ok = __syncthreads_and(ok) != 0;
   };
 
+  // Jagged: this CTA's part of the unit at snake position kk (false: no
+  // unit there).  Its boxes are numbered on across the CTA's units; box j
+  // sits in slot j % NB.  A unit whose boxes fit the ring has them loaded
+  // ahead by a cursor that runs over the following units' boxes while slots
+  // are free (it stops before a unit that does not fit: that one streams
+  // through the ring on its own, as the dense kernel does).
+  struct UG {
+    int64_t g, r0, xrow0, qcol0;
+    int col0, nr, nbox, npad;
+  };
+  auto jgeom = [&](int64_t kk, UG& o) -> bool {
+    if constexpr (!JAG) {
+      return false;
+    } else {
+    const int64_t u = kk * ncl + ((kk & 1) ? ncl - 1 - cid : cid);
+    if (u >= a.units) return false;
+    const int64_t gi = u / a.n_ct;
+    o.col0 = (int)((u - gi * a.n_ct) * CC_COLS);
+    o.g = order_s[gi];
+    const int64_t gs = o.g ? gt_s.end[o.g - 1] : 0, rg = gt_s.end[o.g] - gs;
+    const int64_t S = ((rg + CL - 1) / CL + 31) / 32 * 32;
+    o.r0 = (int64_t)rank * S;
+    o.nr = (int)(o.r0 < rg ? (rg - o.r0 < S ? rg - o.r0 : S) : 0);
+    o.nbox = (o.nr + CC_BOXR - 1) / CC_BOXR;
+    const int64_t rpad = (rg + 31) / 32 * 32;   // the group's rows with its padding
+    o.npad = (int)(o.r0 < rpad ? (rpad - o.r0 < S ? rpad - o.r0 : S) : 0);
+    o.xrow0 = gs + o.r0;
+    o.qcol0 = 32 * gt_s.pad[o.g];
+    return true;
+    }
+  };
+  int64_t base = 0;      // jagged: number of this unit's first box
+  // the cursor (thread 0): the next box to load is box pb of the unit at pkk
+  int64_t pkk = 0;
+  int pb = 0;
+  UG pu{};
+  bool pvalid = false;
+  auto seek = [&](int64_t from) {
+    pb = 0;
+    for (pkk = from; pkk * ncl < a.units; ++pkk)
+      if (jgeom(pkk, pu) && pu.nbox > 0) return true;
+    return false;
+  };
+  if (JAG && tid == 0) pvalid = seek(0);
+  auto issue_row = [&](int slot, int col0, int64_t row) {
+    mbar_expect_tx(&bars[slot], CC_BOX_BYTES);
+    tma_load_2d(sx + slot * CC_BOX_BYTES, &tmX, &bars[slot], col0, (int)row);
+    pending |= 1u << slot;
+  };
+
   int64_t k = 0;
-  for (int64_t u = cid; u < a.units; u += ncl, ub ^= 1, ++k) {
-    const int64_t g = u / a.n_ct;
-    const int col0 = (int)((u - g * a.n_ct) * CC_COLS);
+  for (int64_t kk = 0; JAG ? kk * ncl < a.units : cid + kk * ncl < a.units; ++kk) {
+    int64_t u = cid + kk * ncl;
+    int64_t g = u / a.n_ct;
+    int col0 = (int)((u - g * a.n_ct) * CC_COLS);
+    if constexpr (JAG) {
+      UG c;
+      if (!jgeom(kk, c)) continue;
+      g = c.g;
+      col0 = c.col0;
+      r0 = c.r0;
+      nr = c.nr;
+      nbox = c.nbox;
+      npad = c.npad;
+      xrow0 = c.xrow0;
+      qcol0 = c.qcol0;
+    }
+    const bool fits = nbox <= NB;
     // slot of box bx of this unit
-    auto slot_of = [&](int bx) { return PRE ? (int)((k * nbox + bx) % NB) : bx % NB; };
-    auto issue = [&](int box) { issue_at(box % NB, g, col0, box); };
+    auto slot_of = [&](int bx) {
+      return JAG ? (int)((base + bx) % NB) : (PRE ? (int)((k * nbox + bx) % NB) : bx % NB);
+    };
+    auto issue = [&](int box) {
+      if constexpr (JAG) {
+        issue_row(slot_of(box), col0, xrow0 + (int64_t)box * CC_BOXR);
+      } else {
+        issue_at(box % NB, g, col0, box);
+      }
+    };
 
     // ---- 1. column maxima: the slice streams through the ring once
     refill_barrier();
@@ -170,6 +281,15 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
         const int64_t limit = k * nbox + NB < total_boxes ? k * nbox + NB : total_boxes;
         for (; issued < limit; ++issued) issue_global(issued);
       }
+    } else if (JAG && fits) {
+      // this unit's boxes not yet loaded and the following units' while
+      // slots are free (every box before this unit's has been cast)
+      if (ok && tid == 0)
+        while (pvalid && issued < base + NB && pu.nbox <= NB) {
+          issue_row((int)(issued % NB), pu.col0, pu.xrow0 + (int64_t)pb * CC_BOXR);
+          ++issued;
+          if (++pb == pu.nbox) pvalid = seek(pkk + 1);
+        }
     } else if (ok && tid == 0) {
       for (int bx = 0; bx < nbox && bx < CC_NB; ++bx) issue(bx);
     }
@@ -181,10 +301,10 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
 #pragma unroll 4
       for (int r = rp; r < n; r += 32) {
         const uint4 v = *reinterpret_cast<const uint4*>(box + (r & 127) * 128 + ((cc ^ (r & 7)) << 4));
-        m0 = __vmaxu2(m0, v.x & 0x7FFF7FFFu);
-        m1 = __vmaxu2(m1, v.y & 0x7FFF7FFFu);
-        m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
-        m3 = __vmaxu2(m3, v.w & 0x7FFF7FFFu);
+        m0 = umax16x2(m0, v.x & 0x7FFF7FFFu);
+        m1 = umax16x2(m1, v.y & 0x7FFF7FFFu);
+        m2 = umax16x2(m2, v.z & 0x7FFF7FFFu);
+        m3 = umax16x2(m3, v.w & 0x7FFF7FFFu);
       }
       if (!PRE && bx + CC_NB < nbox) {
         refill_barrier();
@@ -194,10 +314,10 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
     // lanes cc, cc + 8, cc + 16, cc + 24 hold the same columns
 #pragma unroll
     for (int o = 8; o < 32; o <<= 1) {
-      m0 = __vmaxu2(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-      m1 = __vmaxu2(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-      m2 = __vmaxu2(m2, __shfl_xor_sync(0xffffffffu, m2, o));
-      m3 = __vmaxu2(m3, __shfl_xor_sync(0xffffffffu, m3, o));
+      m0 = umax16x2(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = umax16x2(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      m2 = umax16x2(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+      m3 = umax16x2(m3, __shfl_xor_sync(0xffffffffu, m3, o));
     }
     if (lane < 8) wmax[warp][lane] = make_uint4(m0, m1, m2, m3);
     ok = __syncthreads_and(ok) != 0;
@@ -225,7 +345,12 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
     }
     xph ^= 1u << ub;
     ok = __syncthreads_and(ok) != 0;
-    if (!ok) continue;
+    if (!ok) {
+      ub ^= 1;
+      ++k;
+      base += nbox;
+      continue;
+    }
     // ---- 3. cast and transposed store
     float sv[8];
 #pragma unroll
@@ -234,7 +359,9 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
     // one 32-row x 64-column sub-tile: local row lr0 (a multiple of 8) of
     // this lane, held in the slot at `box`
     auto cast_sub = [&](const uint8_t* box, int lr0) {
-      if (lr0 >= nr || col >= a.C) return;  // R % 8 == 0: a lane's 8 rows are all in or all out
+      // dense: R % 8 == 0, so a lane's 8 rows are all in or all out; jagged:
+      // rows from nr to npad are the group's padding (zero codes)
+      if (lr0 >= npad || col >= a.C) return;
       uint32_t w0[8], w1[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -244,18 +371,21 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
                            __fmul_rn(bf16_lo(v.y), sv[2]), __fmul_rn(bf16_hi(v.y), sv[3]));
         w1[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
                            __fmul_rn(bf16_lo(v.w), sv[6]), __fmul_rn(bf16_hi(v.w), sv[7]));
+        if (JAG && lr0 + k >= nr) w0[k] = w1[k] = 0u;
       }
-      // q[g][col + t][row .. row + 7] for the 8 columns t
-      uint8_t* base = a.q + (g * a.C + col) * a.R + r0 + lr0;
+      // q[g][col + t][row .. row + 7] (jagged: q[col + t][group column + row])
+      // for the 8 columns t
+      const int64_t pitch = JAG ? a.ldt : a.R;
+      uint8_t* base = JAG ? a.q + col * a.ldt + qcol0 + r0 + lr0 : a.q + (g * a.C + col) * a.R + r0 + lr0;
       uint32_t q0[4], q1[4];
       transpose4x4(w0[0], w0[1], w0[2], w0[3], q0);
       transpose4x4(w0[4], w0[5], w0[6], w0[7], q1);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)t * a.R) = make_uint2(q0[t], q1[t]);
+      for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)t * pitch) = make_uint2(q0[t], q1[t]);
       transpose4x4(w1[0], w1[1], w1[2], w1[3], q0);
       transpose4x4(w1[4], w1[5], w1[6], w1[7], q1);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)(4 + t) * a.R) = make_uint2(q0[t], q1[t]);
+      for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)(4 + t) * pitch) = make_uint2(q0[t], q1[t]);
     };
     // the boxes still resident after the maxima pass (the last CC_NB), by
     // all warps: sub-tile i of them is box first + i / 4, quarter i % 4
@@ -270,8 +400,8 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
       if (ok && tid == 0)
         for (int bx = 0; bx < first && bx < CC_NB; ++bx) issue(bx);
       for (int bx = 0; bx < first && ok; ++bx) {
-        wait_slot(bx % NB);
-        if (warp < 4) cast_sub(sx + (bx % CC_NB) * CC_BOX_BYTES, bx * CC_BOXR + warp * 32 + rq * 8);
+        wait_slot(slot_of(bx));
+        if (warp < 4) cast_sub(sx + slot_of(bx) * CC_BOX_BYTES, bx * CC_BOXR + warp * 32 + rq * 8);
         if (bx + CC_NB < first) {
           refill_barrier();
           if (ok && tid == 0) issue(bx + CC_NB);
@@ -280,6 +410,25 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
     }
     ok = __syncthreads_and(ok) != 0;
     if (!ok && tid == 0) set_status(a.status, FP8MOE_ERR_TIMEOUT);
+    if (JAG && !fits && tid == 0) {
+      // a unit that streamed on its own: the cursor resumes after it
+      issued = base + nbox;
+      pvalid = seek(kk + 1);
+    }
+    ub ^= 1;
+    ++k;
+    base += nbox;
+  }
+  if constexpr (JAG) {
+    // the slack of q after the last group: columns [32 * sub-tiles, ldt)
+    const int64_t E = a.E, last = gt_s.end[E - 1] - (E > 1 ? gt_s.end[E - 2] : 0);
+    const int64_t from = 32 * (gt_s.pad[E - 1] + (last + 31) / 32);
+    const int64_t chunks = (a.ldt - from) / 16;
+    if (chunks > 0)
+      for (int64_t i = (int64_t)blockIdx.x * CC_THREADS + tid; i < a.C * chunks; i += (int64_t)gridDim.x * CC_THREADS) {
+        const int64_t row = i / chunks, ch = i - row * chunks;
+        *reinterpret_cast<uint4*>(a.q + row * a.ldt + from + ch * 16) = make_uint4(0, 0, 0, 0);
+      }
   }
   // after a load that timed out, wait (bounded) for the loads still in flight
   if (tid == 0)
@@ -289,9 +438,9 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
   if constexpr (CL > 1) cluster_barrier();
 }
 
-template <int CL, int NB, bool PRE, bool FNUZ>
+template <int CL, int NB, bool PRE, bool FNUZ, bool JAG = false>
 cudaError_t launch_cc(const CUtensorMap& tm, const CcArgs& a, int smem, int num_sms, cudaStream_t st) {
-  auto kern = k_cw_cluster<CL, NB, PRE, FNUZ>;
+  auto kern = k_cw_cluster<CL, NB, PRE, FNUZ, JAG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -323,7 +472,8 @@ cudaError_t launch_cc(const CUtensorMap& tm, const CcArgs& a, int smem, int num_
     if (ncl < 1) ncl = 1;
     cache[dev].store(((long long)smem << 32) | (unsigned)ncl, std::memory_order_relaxed);
   }
-  const int64_t nc = a.units < ncl ? a.units : ncl;
+  // jagged: every resident cluster (the CTAs also zero the slack of q)
+  const int64_t nc = JAG ? ncl : (a.units < ncl ? a.units : ncl);
   cfg.gridDim = dim3((unsigned)(CL * (nc < 1 ? 1 : nc)));
   return cudaLaunchKernelEx(&cfg, kern, tm, a);
 }
@@ -339,6 +489,40 @@ cudaError_t launch_cc_k(int CL, const CUtensorMap& tm, const CcArgs& a, int smem
 }
 
 }  // namespace
+
+// Jagged: clusters of two, a five-slot ring (the group table takes the room
+// of the sixth at two CTAs per SM).
+constexpr int CCJ_CL = 2, CCJ_NB = 5;
+
+bool colwise_cluster_jagged_supported(int64_t E, int64_t R, int64_t C) {
+  return E > 0 && E <= QG_MAX && R >= 0 && C > 0 && C % 16 == 0 && R < ((int64_t)1 << 31) - CC_BOXR &&
+         C < ((int64_t)1 << 31);
+}
+
+cudaError_t launch_colwise_cluster_jagged(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                                          int kind, int64_t ldt, void* q, float* inv, int* status, int num_sms,
+                                          cudaStream_t st) {
+  CcArgs a;
+  a.E = E;
+  a.R = R;
+  a.C = C;
+  a.S = 0;
+  a.n_ct = (C + CC_COLS - 1) / CC_COLS;
+  a.units = E * a.n_ct;
+  a.q = (uint8_t*)q;
+  a.inv = inv;
+  a.offs = offs;
+  a.ldt = ldt;
+  a.status = status;
+  const int smem = CCJ_NB * CC_BOX_BYTES + 1024;
+  CUtensorMap tm;
+  cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(R > 0 ? R : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)(C * 2)};
+  cuuint32_t box[2] = {CC_COLS, CC_BOXR};
+  if (!make_tmap(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  return kind == FP8MOE_E4M3FNUZ ? launch_cc<CCJ_CL, CCJ_NB, false, true, true>(tm, a, smem, num_sms, st)
+                                 : launch_cc<CCJ_CL, CCJ_NB, false, false, true>(tm, a, smem, num_sms, st);
+}
 
 bool colwise_cluster_supported(int64_t E, int64_t R, int64_t C) {
   return E > 0 && R > 0 && C > 0 && R % 8 == 0 && C % 16 == 0 && E * R < ((int64_t)1 << 31) &&
@@ -363,6 +547,8 @@ cudaError_t launch_colwise_cluster(const void* x, int64_t E, int64_t R, int64_t 
   a.E = E;
   a.R = R;
   a.C = C;
+  a.offs = nullptr;
+  a.ldt = 0;
   a.S = rows_per_cta(CL);
   a.n_ct = (C + CC_COLS - 1) / CC_COLS;
   a.units = E * a.n_ct;

@@ -15,6 +15,15 @@ FP8MOE_DEV void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// lane-wise unsigned max of two pairs of 16-bit values, as __vmaxu2 gives it,
+// in one PTX instruction (applied to bf16 bit patterns with the sign bits
+// cleared it is the maximum magnitude, NaN patterns above every number)
+FP8MOE_DEV uint32_t umax16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 FP8MOE_DEV float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 FP8MOE_DEV float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

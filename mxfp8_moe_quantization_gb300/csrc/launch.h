@@ -49,6 +49,10 @@ cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const
 
 // colwise FP8 of dense [E, R, C] with transposed output in one HBM pass
 // (colwise_cluster.cu), for the sizes colwise_cluster_supported accepts
+bool colwise_cluster_jagged_supported(int64_t E, int64_t R, int64_t C);
+cudaError_t launch_colwise_cluster_jagged(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
+                                          int kind, int64_t ldt, void* q, float* inv, int* status, int num_sms,
+                                          cudaStream_t st);
 bool colwise_cluster_supported(int64_t E, int64_t R, int64_t C);
 cudaError_t launch_colwise_cluster(const void* x, int64_t E, int64_t R, int64_t C, int kind, void* q, float* inv,
                                    int* status, int num_sms, cudaStream_t st);
