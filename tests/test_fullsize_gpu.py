@@ -285,6 +285,24 @@ def test_rowwise_fullsize(F, name, which):
         bnd[sel] = np.abs(dy_deq[sel]) @ np.abs(wt).T
     _check_vals(got, ref, bnd, f"{name} {which} dgrad")
 
+    # the jagged transposed codes of the activation (the wgrad operand), bit
+    # for bit on sampled columns of every group: each group at its padded
+    # start, its padding and the slack after the last group zero
+    P = OQ.padded_starts(offs_np, 32)
+    kc = np.array(sorted(set([0, K - 1] + rng.integers(0, K, size=4).tolist())))
+    qat_np = qat[torch.from_numpy(kc).to(DEV)].cpu().numpy()
+    iat_np = iat.cpu().numpy()
+    for e in range(E):
+        s0, s1 = int(starts[e]), int(ends[e])
+        if s1 == s0:
+            continue
+        rq_, ri_ = OQ.quantize_colwise_3d(_np(a[s0:s1][:, torch.from_numpy(kc).to(DEV)])[None], transpose_out=True)
+        assert np.array_equal(qat_np[:, P[e]:P[e] + (s1 - s0)], rq_[0]), f"{name} jagged codes e={e}"
+        assert not qat_np[:, P[e] + (s1 - s0):P[e] + (s1 - s0 + 31) // 32 * 32].any(), f"padding e={e}"
+        assert np.array_equal(iat_np[e][kc], ri_[0]), f"{name} jagged scales e={e}"
+    last = int(ends[-1] - starts[-1])
+    assert not qat_np[:, P[-1] + (last + 31) // 32 * 32:].any(), "slack after the last group"
+
     nn = torch.from_numpy(rng.integers(0, N, size=4)).to(DEV)
     kk = torch.from_numpy(rng.integers(0, K, size=4)).to(DEV)
     for e in range(E):
