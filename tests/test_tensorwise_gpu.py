@@ -131,3 +131,20 @@ def test_tensorwise_gemms(F, sizes, N, K):
     ref, bound = OG.grouped_mm_wgrad(dyt, at, offs, col0=P)
     _check(dw, ref, bound, "tensorwise wgrad")
     assert F.fp8moe_get_device_status() == 0
+
+
+@pytest.mark.parametrize("which", ["A", "W1"])
+def test_tensorwise_llama3_fullsize(F, which):
+    """The bench's tensorwise workloads at full size (Llama3-8B X [8192,
+    4096] and W [14336, 4096], plain layout: the one-launch streaming
+    kernel with its grid-wide meeting), every code and the scale against the
+    oracle."""
+    wl = W.get_workload("llama3_8b")
+    t = (W.make_activations(wl, "A", device=DEV) if which == "A"
+         else W.make_weights(wl, "W1", device=DEV).reshape(wl.N, wl.K))
+    q, inv = F.fp8moe_quantize_tensorwise(t)
+    torch.cuda.synchronize()
+    assert F.fp8moe_get_device_status() == 0
+    rq, rinv = OQ.quantize_tensorwise(_np(t), OF.FN)
+    assert inv.cpu().numpy()[0] == rinv
+    assert np.array_equal(q.cpu().numpy(), rq)
