@@ -141,3 +141,28 @@ def test_routed_mxfp8_layer_end_to_end(F):
                                                     + 2.0 ** -8 * np.abs(ref_y[rrow[:, j]])) for j in range(k))
     got = _np(out)
     assert np.all(np.abs(got - ref) <= bound + 2.0 ** -8 * np.abs(ref))
+
+
+@pytest.mark.parametrize("name", ["scout", "dsv3"])
+def test_unpermute_model_shapes(F, name):
+    """The weighted combine at the layer shapes the bench times (Scout top-1
+    over 16 experts, hidden 5120; DeepSeek-V3 top-8 over 256, hidden 7168):
+    sampled tokens bit for bit against the oracle, which recombines them
+    from just the expert-output rows they read."""
+    wl = W.get_workload(name)
+    T, E, N = wl.tokens, wl.E, wl.K
+    k = 1 if name == "scout" else 8
+    idx, w = _topk(T, k, E, 21, 0.0 if name == "scout" else 1.2)
+    _, _, rrow = RT.route_permute(np.zeros((T, 8), np.float32), idx, E)
+    g = torch.Generator(device=DEV).manual_seed(22)
+    y = torch.randn(RT.route_rows(T, k, E), N, device=DEV, generator=g).to(torch.bfloat16)
+    out = F.fp8moe_route_unpermute(y, torch.from_numpy(rrow).to(DEV), torch.from_numpy(w).to(DEV))
+    torch.cuda.synchronize()
+    assert F.fp8moe_get_device_status() == 0
+    tok = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(23).integers(0, T, size=62)]))
+    sub = rrow[tok]
+    need = np.unique(sub)
+    local = np.searchsorted(need, sub)
+    ysub = _np(y[torch.from_numpy(need).to(DEV)])
+    ref = RT.route_unpermute(ysub, local, w[tok])
+    assert np.array_equal(_np(out[torch.from_numpy(tok).to(DEV)]), ref)
