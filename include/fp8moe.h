@@ -109,7 +109,10 @@ fp8moe_status fp8moe_quantize_rowwise(const void* x, int64_t R, int64_t C, int64
  *   columns [P_e, P_e + g_e), P_e = sum_{j<e} round_up(g_j, 32), every
  *   other column 0; else [R, C].  1 <= E <= FP8MOE_MAX_GROUPS.
  * C % 16 == 0; dense transposed output also needs R % 16 == 0.
- * scale_inv doubles as the scratch of the column maxima during the call
+ * Transposed output (dense or jagged) runs as one pass over x in
+ * thread-block clusters that exchange column maxima through distributed
+ * shared memory, and writes scale_inv directly.  Untransposed output uses
+ * scale_inv as the scratch of the column maxima during the call
  * (stream-ordered; it holds the scales when the call's work completes).
  * ------------------------------------------------------------------------ */
 fp8moe_status fp8moe_quantize_colwise_3d(const void* x, int64_t E, int64_t R, int64_t C,
