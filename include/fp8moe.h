@@ -461,6 +461,17 @@ fp8moe_status fp8moe_get_device_status(fp8moe_stream_t stream, int32_t* out_code
  * ------------------------------------------------------------------------ */
 fp8moe_status fp8moe_testing_stall_next_gemm(void);
 
+/* ------------------------------------------------------------------------
+ * Testing hook of the failure-detection path of fp8moe_quantize_tensorwise
+ * (no counterpart on the pages).  Arms a one-shot flag: the next plain-
+ * layout tensorwise launch of the process (the one-launch kernel) has its
+ * first CTA skip counting itself in at the grid-wide meeting, so every
+ * CTA's bounded wait (2 s) runs out and the launch sets FP8MOE_ERR_TIMEOUT
+ * (its codes and scale are then not valid).  Every CTA still waits for its
+ * own copies and releases its tensor memory, so the context stays usable.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_testing_stall_next_tensorwise(void);
+
 /* Static string for a status code. */
 const char* fp8moe_status_string(int status);
 

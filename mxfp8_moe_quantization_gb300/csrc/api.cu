@@ -484,4 +484,9 @@ fp8moe_status fp8moe_testing_stall_next_gemm(void) {
   return FP8MOE_OK;
 }
 
+fp8moe_status fp8moe_testing_stall_next_tensorwise(void) {
+  fp8moe::arm_tensorwise_stall_hook();
+  return FP8MOE_OK;
+}
+
 }  // extern "C"

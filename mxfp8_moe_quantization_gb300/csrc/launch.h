@@ -92,6 +92,9 @@ struct GemmArgs;
 cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st);
 // arms the one-shot stall of the next grouped GEMM launch (timeout-path test)
 void arm_gemm_stall_hook();
+// arms the one-shot stall of the next one-launch tensorwise kernel (its
+// grid-wide meeting; timeout-path test)
+void arm_tensorwise_stall_hook();
 // blockwise-scaled grouped GEMM (blockwise_mm.cu)
 cudaError_t launch_blockwise_mm(const GemmArgs& g, cudaStream_t st);
 

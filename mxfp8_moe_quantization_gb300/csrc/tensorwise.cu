@@ -23,6 +23,7 @@
 //   2. the cast: k_tw_cast for the plain layout, or the colwise kernel in its
 //      fixed-scale mode for the transposed / jagged layouts;
 //   3. k_tw_finalize: one thread writes fl(1 / s).
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -31,6 +32,11 @@
 #include "tma.cuh"
 
 namespace fp8moe {
+
+// One-shot test hook: armed by fp8moe_testing_stall_next_tensorwise,
+// consumed by the next launch of the one-launch tensorwise kernel.
+static std::atomic<int> g_tw_stall{0};
+void arm_tensorwise_stall_hook() { g_tw_stall.store(1, std::memory_order_relaxed); }
 
 namespace {
 
@@ -162,7 +168,8 @@ FP8MOE_DEV void tmem_ld8(uint32_t taddr, uint4& a, uint4& b) {
 // phase k / SLOTS and its release the empty barrier's phase k / SLOTS.
 template <bool FNUZ, int TWS_SLOTS, int TWS_TMEM_COLS, int MINB>
 __global__ void __launch_bounds__(TWS_THREADS, MINB)
-    k_tw_stream(const uint8_t* __restrict__ x, int64_t n, uint8_t* __restrict__ q, uint32_t* word, int* status) {
+    k_tw_stream(const uint8_t* __restrict__ x, int64_t n, uint8_t* __restrict__ q, uint32_t* word, int* status,
+                int stall_test) {
   constexpr int TWS_TMEM_TILES = TWS_TMEM_COLS / 32;
   extern __shared__ __align__(128) uint8_t sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + (size_t)TWS_SLOTS * TWS_TILE);
@@ -186,6 +193,8 @@ __global__ void __launch_bounds__(TWS_THREADS, MINB)
   };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // a ring wait that ran out: the pipeline is broken, later ring waits
+  // return at once
   auto fail = [&]() {
     set_status(status, FP8MOE_ERR_TIMEOUT);
     abort_s = 1;
@@ -269,7 +278,9 @@ __global__ void __launch_bounds__(TWS_THREADS, MINB)
     // maximum already there is at least this CTA's, a compare-and-swap
     // otherwise
     uint32_t seen = ld_acquire(word);
-    for (;;) {
+    // test hook: CTA 0 of this launch never counts itself in, so every
+    // CTA's bounded wait below runs out
+    for (; !(stall_test && blockIdx.x == 0);) {
       if ((seen & 0xFFFFu) >= mx) {
         atomicAdd(word, 1u << 16);
         break;
@@ -284,7 +295,10 @@ __global__ void __launch_bounds__(TWS_THREADS, MINB)
     uint32_t cur = ld_acquire(word);
     while ((cur >> 16) < gridDim.x) {
       if (globaltimer() - t0 > WAIT_LIMIT_NS) {
-        fail();
+        // the meeting ran out: the status says the result is not valid; the
+        // ring's loads do not depend on the meeting and still complete and
+        // are waited for, so no copy is in flight when the CTA exits
+        set_status(status, FP8MOE_ERR_TIMEOUT);
         break;
       }
       __nanosleep(32);
@@ -414,7 +428,8 @@ cudaError_t launch_tensorwise(const void* x, int64_t E, int64_t R, int64_t C, co
       uint8_t* qp = (uint8_t*)q;
       uint32_t* wp = (uint32_t*)scale_inv;
       int64_t nn = n;
-      void* args[] = {(void*)&xp, (void*)&nn, (void*)&qp, (void*)&wp, (void*)&status};
+      int stall = g_tw_stall.exchange(0, std::memory_order_relaxed);
+      void* args[] = {(void*)&xp, (void*)&nn, (void*)&qp, (void*)&wp, (void*)&status, (void*)&stall};
       return cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(TWS_THREADS), args, SMEM, st);
     }
   }

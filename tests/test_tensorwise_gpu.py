@@ -148,3 +148,20 @@ def test_tensorwise_llama3_fullsize(F, which):
     rq, rinv = OQ.quantize_tensorwise(_np(t), OF.FN)
     assert inv.cpu().numpy()[0] == rinv
     assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_tensorwise_meeting_timeout_sets_status(F):
+    """Fault injection without a GPU fault: the one-shot testing hook makes
+    the first CTA of the next one-launch tensorwise kernel skip counting
+    itself in at the grid-wide meeting, so every CTA's bounded wait (2 s)
+    runs out; the launch reports FP8MOE_ERR_TIMEOUT, every CTA still waits for
+    its own loads and releases its tensor memory, and the next call (the
+    hook is spent) is exact again."""
+    x = _bf16((2048, 1024), 77, 1.5)
+    F.fp8moe_testing_stall_next_tensorwise()
+    F.fp8moe_quantize_tensorwise(x.to(DEV))
+    assert F.fp8moe_get_device_status() == 6          # FP8MOE_ERR_TIMEOUT
+    q, inv = F.fp8moe_quantize_tensorwise(x.to(DEV))
+    assert F.fp8moe_get_device_status() == 0
+    rq, rinv = OQ.quantize_tensorwise(_np(x), OF.FN)
+    assert np.array_equal(q.cpu().numpy(), rq) and inv.cpu().numpy()[0] == rinv
