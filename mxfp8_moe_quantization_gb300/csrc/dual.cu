@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(32 * DUAL_WARPS, 2) k_mx_dual(const __grid_con
   };
   uint32_t parity = 0;
   bool live = true;  // false after a wait ran out: no further loads or waits
+  uint32_t lost = 0; // the phase whose wait ran out (its load may be in flight)
   const uint32_t t_first = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   Tile cur;
   if (t_first < a.tiles) {
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(32 * DUAL_WARPS, 2) k_mx_dual(const __grid_con
       if (live && !mbar_wait(wbar, parity, nullptr)) {
         set_status(a.status, FP8MOE_ERR_TIMEOUT);
         live = false;
+        lost = parity;
       }
       parity ^= 1;
 #pragma unroll
@@ -344,6 +346,9 @@ __global__ void __launch_bounds__(32 * DUAL_WARPS, 2) k_mx_dual(const __grid_con
     }
     if (PF) cur = nxt;
   }
+  // after a wait that ran out, wait (bounded) once more for that load, the
+  // only one that can be in flight, before the warp's buffer goes away
+  if (PF && !live && lane == 0) (void)mbar_wait(wbar, lost, nullptr);
 }
 
 }  // namespace

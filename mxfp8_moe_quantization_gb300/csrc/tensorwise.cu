@@ -200,9 +200,13 @@ __global__ void __launch_bounds__(TWS_THREADS, MINB)
     abort_s = 1;
   };
   // producer: fill the slot of item k once its previous occupant is released
+  // (filled / fill_par: the slots filled and the phase bit of their last fill)
+  uint32_t filled = 0, fill_par = 0;
   auto issue = [&](int k) {
     const int s = k % TWS_SLOTS;
     if (k >= TWS_SLOTS && !mbar_wait(&empty[s], (k / TWS_SLOTS - 1) & 1, &abort_s)) fail();
+    filled |= 1u << s;
+    fill_par = (fill_par & ~(1u << s)) | ((uint32_t)((k / TWS_SLOTS) & 1) << s);
     const int bytes = tile_bytes(k);
     mbar_expect_tx(&full[s], (uint32_t)bytes);
     bulk_load(sm + (size_t)s * TWS_TILE, x + gtile(local_tile(k)) * TWS_TILE, (uint32_t)bytes, &full[s]);
@@ -364,6 +368,13 @@ __global__ void __launch_bounds__(TWS_THREADS, MINB)
       *reinterpret_cast<volatile float*>(word) = inv;
     }
   }
+  // after a ring wait that ran out (in any thread: read after the barrier),
+  // the producer waits (bounded) for the last fill of every slot, so no copy
+  // is in flight when the CTA exits
+  __syncthreads();
+  if (threadIdx.x == 0 && abort_s)
+    for (int s = 0; s < TWS_SLOTS; ++s)
+      if (filled & (1u << s)) (void)mbar_wait(&full[s], (fill_par >> s) & 1u, nullptr);
   tc_fence_before();
   __syncthreads();
   if (warp == 1 && T > 0) {
