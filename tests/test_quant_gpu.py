@@ -120,7 +120,11 @@ def test_colwise_dense_parity(F, kind, okind, E, R, C, trans):
 
 @pytest.mark.parametrize("kind,okind", KINDS)
 @pytest.mark.parametrize("sizes", [[96, 0, 0, 928], [30, 0, 47, 23], [4000, 0, 1000], [1, 2, 3, 500, 7],
-                                   [0, 0, 64]])
+                                   [0, 0, 64],
+                                   # tall and small groups together: the transposed output
+                                   # streams slices past the ring (6000: 3000 rows per CTA)
+                                   # and fits the rest in it
+                                   [6000, 1281, 1280, 33, 0, 2500]])
 @pytest.mark.parametrize("trans", [True, False])
 def test_colwise_jagged_parity(F, kind, okind, sizes, trans):
     M = sum(sizes)
