@@ -30,8 +30,10 @@
 //    timeout sets the device status word instead of hanging;
 //  * accumulator in TMEM (128 lanes x 256 fp32 columns per CTA); MXFP8 scales
 //    consumed by the block-scaled MMA (kind::mxf8f6f4, one e8m0 scale per 32
-//    elements of K); the rowwise recipe uses kind::f8f6f4 and applies row x
-//    column fp32 scales in the epilogue;
+//    elements of K) from the other half of TMEM; the rowwise recipe uses
+//    kind::f8f6f4 and applies row x column fp32 scales in the epilogue, so
+//    its TMEM holds two accumulators and a tile's MMAs do not wait for the
+//    previous tile's drain;
 //  * the epilogue drains the accumulator to registers and releases TMEM before
 //    its global stores, so the next tile's MMAs overlap the stores.
 //  Every load lands in the issuing CTA's own shared memory: no TMA multicast.
@@ -93,8 +95,8 @@ struct SmemLayout {
   static constexpr int sfb = sfa + STAGES * SFA_STAGE_BYTES;
   static constexpr int abf = (sfb + STAGES * SFB_STAGE_BYTES + 1023) / 1024 * 1024;
   static constexpr int bars = abf + QS * QA_SLOT_BYTES;
-  // 3 per stage + 4, and for QA: afull per stage, abf_full / abf_empty per slot
-  static constexpr int NBARS = 3 * STAGES + 4 + (QA ? STAGES + 2 * QS : 0);
+  // 3 per stage + 6, and for QA: afull per stage, abf_full / abf_empty per slot
+  static constexpr int NBARS = 3 * STAGES + 6 + (QA ? STAGES + 2 * QS : 0);
   static constexpr int misc = bars + NBARS * 8;                 // tmem addr, abort, counts
   static constexpr int colscale = misc + 64;                    // 256 floats
   static constexpr int tiles_prefix = colscale + BN * 4;        // MAXG + 1 ints
@@ -303,9 +305,15 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
   uint8_t* sSFB = smem + L::sfb;
   uint64_t* full = (uint64_t*)(smem + L::bars);
   uint64_t* empty = full + STAGES;
+  // per accumulator: tmem_full[i] (the MMAs of its tile completed),
+  // tmem_empty[i] (both CTAs' epilogues drained it).  The rowwise and
+  // tensorwise recipes keep no scales in TMEM, so two 256-column
+  // accumulators fit and the MMAs of the next tile run while the epilogue
+  // drains the last one; MXFP8 keeps its block scales in the second half.
+  constexpr int NACC = MX ? 1 : 2;
   uint64_t* tmem_full = empty + STAGES;
-  uint64_t* tmem_empty = tmem_full + 1;
-  uint64_t* sf_full = tmem_empty + 1;  // per stage: scales are in TMEM (scale-copier commits)
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint64_t* sf_full = tmem_empty + 2;  // per stage: scales are in TMEM (scale-copier commits)
   // completion of the MMA / scale-copier thread's own tcgen05 work, awaited
   // before the CTA releases TMEM (matters on the timeout path)
   uint64_t* drain_mma = sf_full + STAGES;
@@ -347,9 +355,11 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
         mbar_init(&abf_empty[j], 4);
       }
     }
-    mbar_init(tmem_full, 1);
-    // the leader's accumulator is free once both CTAs' epilogues drained
-    mbar_init(tmem_empty, 2 * L::NEPI);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tmem_full[i], 1);
+      // the leader's accumulator is free once both CTAs' epilogues drained
+      mbar_init(&tmem_empty[i], 2 * L::NEPI);
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -543,7 +553,7 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
     constexpr int MM = 2 * BM;
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t acc_phase = 0;
+    uint32_t acc_i = 0;   // tiles with k-stages so far: accumulator acc_i % NACC, use acc_i / NACC
     auto stage_ready = [&]() -> bool {
       if (!mbar_wait(&full[stage], phase, abort_flag)) return false;
       if (QA && !mbar_wait_cluster(&afull[stage], phase, abort_flag)) return false;
@@ -553,13 +563,16 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
       const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, bounds, t, rank, cur_e);
       if (tl.nk == 0) continue;
-      if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, abort_flag)) {
+      const int abuf = (int)(acc_i % NACC);
+      const uint32_t use = acc_i / NACC;
+      ++acc_i;
+      if (!mbar_wait_cluster(&tmem_empty[abuf], (use & 1u) ^ 1u, abort_flag)) {
         set_status(g.status, FP8MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
       }
-      acc_phase ^= 1;
       tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(abuf * BN);
       bool ok = true;
       for (int ks = 0; ks < tl.nk; ++ks) {
         if (!stage_ready()) {
@@ -577,10 +590,10 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
         auto issue = [&](int k) {
           const uint32_t accum = (ks > 0 || k > 0) ? 1u : 0u;
           if (MX) {
-            mma_mx(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_mx<MM>((uint32_t)k),
-                        sf_col, sf_col + 4, accum);
+            mma_mx(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_mx<MM>((uint32_t)k),
+                   sf_col, sf_col + 4, accum);
           } else {
-            mma_f8<true>(tmem_base, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8<MM>(), accum);
+            mma_f8<true>(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc_f8<MM>(), accum);
           }
         };
         // Full stages issue their four K=32 MMAs as straight-line code: behind a
@@ -606,7 +619,7 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
       // test hook: the first tile of the first cluster never hands over its
       // accumulator, so the epilogue's bounded wait runs out
       if (p.stall_test && t == pair && pair == 0) continue;
-      tc_commit_pair(tmem_full, pair_mask);
+      tc_commit_pair(&tmem_full[abuf], pair_mask);
     }
     // every MMA this thread issued has completed before TMEM is released
     tc_commit_local(drain_mma);
@@ -742,15 +755,16 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
     const int c_lo = NEPI == 8 ? (ew >> 2) * EC : 0;  // this warp's accumulator columns [c_lo, c_lo + EC)
     const int et = ew * 32 + lane;
     uint8_t* stg = smem + L::stg + ew * L::STG_WARP_BYTES;
-    uint32_t acc_phase = 0;
+    uint32_t acc_i = 0;   // as the MMA issuer counts them
+    int abuf = 0;
     auto release_acc = [&]() {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         if (rank == 1) {
-          mbar_arrive_remote(tmem_empty, lead);
+          mbar_arrive_remote(&tmem_empty[abuf], lead);
         } else {
-          mbar_arrive(tmem_empty);
+          mbar_arrive(&tmem_empty[abuf]);
         }
       }
     };
@@ -787,19 +801,21 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
           rscale = tw ? rs[0] : (WGRAD ? rs[(int64_t)tl.e * g.rows + tl.row0 + lrow] : rs[tl.row0 + lrow]);
         }
       }
-      if (!mbar_wait(tmem_full, acc_phase, abort_flag)) {
+      abuf = (int)(acc_i % NACC);
+      const uint32_t use = acc_i / NACC;
+      ++acc_i;
+      if (!mbar_wait(&tmem_full[abuf], use & 1u, abort_flag)) {
         set_status(g.status, FP8MOE_ERR_TIMEOUT);
         *abort_flag = 1;
         break;
       }
-      acc_phase ^= 1;
       tc_fence_after();
       if (tl.rows == 0) {  // phantom half: nothing to store
         release_acc();
         continue;
       }
       uint32_t packed[EC / 2];
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c_lo;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(abuf * BN + c_lo);
       // two 32-column loads in flight per wait (half the load round trips);
       // the A-quantization variant, which holds fewer registers, one
       constexpr int LW = QA ? 32 : 64;   // columns per wait
