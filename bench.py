@@ -42,10 +42,10 @@ METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)
 # the full layer by each mode's algorithmic bytes.  It is reported only while
 # the kernel source is the one that was captured (same SHA-256).
 GEMM_TRAFFIC = {"source": "mxfp8_moe_quantization_gb300/csrc/grouped_mm.cu",
-                "sha256": "02736c207b843f7e122025a08f91e37b44617fd12417b8bd461b5bd92dff0242",
+                "sha256": "e690dbae6a9ef19065a86971406e0cc85ff5796b91086d61b7ffd4f7696d2017",
                 # full-size Scout W1 fwd / dgrad / wgrad: algorithmic bytes x the
                 # traffic / algorithmic ratio of an 8-expert capture
-                "bytes_per_launch": (1029.7e6 + 1053.4e6 + 1487.4e6) / 3}
+                "bytes_per_launch": (1030.3e6 + 1050.2e6 + 1491.4e6) / 3}
 
 
 def gemm_traffic():
