@@ -182,10 +182,15 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
     unit_geom(j / nbox, g, col0);
     issue_at((int)(j % NB), g, col0, (int)(j % nbox));
   };
+  // (a wait that runs out leaves the slot pending with its phase, for the
+  // exit path)
   auto wait_slot = [&](int slot) {
-    if (!mbar_wait(&bars[slot], (phases >> slot) & 1u, nullptr)) ok = false;
+    if (!mbar_wait(&bars[slot], (phases >> slot) & 1u, nullptr)) {
+      ok = false;
+      return;
+    }
     phases ^= 1u << slot;
-    if (tid == 0) pending &= ~(1u << slot);
+    if (tid == 0 || tid == 128) pending &= ~(1u << slot);
   };
   // every thread is done with the slots before the ring refills them
   auto refill_barrier = [&]() {
@@ -244,6 +249,7 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
   };
 
   int64_t k = 0;
+  int preloaded = 0;   // boxes of this unit already loading (issued during the last unit's cast)
   for (int64_t kk = 0; JAG ? kk * ncl < a.units : cid + kk * ncl < a.units; ++kk) {
     int64_t u = cid + kk * ncl;
     int64_t g = u / a.n_ct;
@@ -291,8 +297,9 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
           if (++pb == pu.nbox) pvalid = seek(pkk + 1);
         }
     } else if (ok && tid == 0) {
-      for (int bx = 0; bx < nbox && bx < CC_NB; ++bx) issue(bx);
+      for (int bx = preloaded; bx < nbox && bx < CC_NB; ++bx) issue(bx);
     }
+    preloaded = 0;
     uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
     for (int bx = 0; bx < nbox && ok; ++bx) {
       wait_slot(slot_of(bx));
@@ -387,26 +394,81 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
 #pragma unroll
       for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)(4 + t) * pitch) = make_uint2(q0[t], q1[t]);
     };
-    // the boxes still resident after the maxima pass (the last CC_NB), by
-    // all warps: sub-tile i of them is box first + i / 4, quarter i % 4
+    // the boxes still resident after the maxima pass (the last CC_NB)
     const int first = nbox > CC_NB ? nbox - CC_NB : 0;
-    for (int i = warp; i < (nbox - first) * 4; i += 8) {
-      const int bx = first + (i >> 2);
-      cast_sub(sx + slot_of(bx) * CC_BOX_BYTES, bx * CC_BOXR + (i & 3) * 32 + rq * 8);
-    }
-    // the earlier boxes come back through the ring (from L2: read moments ago)
-    if (first > 0) {
-      refill_barrier();
-      if (ok && tid == 0)
-        for (int bx = 0; bx < first && bx < CC_NB; ++bx) issue(bx);
-      for (int bx = 0; bx < first && ok; ++bx) {
-        wait_slot(slot_of(bx));
-        if (warp < 4) cast_sub(sx + slot_of(bx) * CC_BOX_BYTES, bx * CC_BOXR + warp * 32 + rq * 8);
-        if (bx + CC_NB < first) {
-          refill_barrier();
-          if (ok && tid == 0) issue(bx + CC_NB);
+    bool piped = false;
+    if constexpr (!JAG && !PRE && (NB % 2) == 0) piped = first > 0;
+    if (!piped) {
+      // by all warps: sub-tile i of them is box first + i / 4, quarter i % 4
+      for (int i = warp; i < (nbox - first) * 4; i += 8) {
+        const int bx = first + (i >> 2);
+        cast_sub(sx + slot_of(bx) * CC_BOX_BYTES, bx * CC_BOXR + (i & 3) * 32 + rq * 8);
+      }
+      // the earlier boxes come back through the ring (from L2: read moments ago)
+      if (first > 0) {
+        refill_barrier();
+        if (ok && tid == 0)
+          for (int bx = 0; bx < first && bx < CC_NB; ++bx) issue(bx);
+        for (int bx = 0; bx < first && ok; ++bx) {
+          wait_slot(slot_of(bx));
+          if (warp < 4) cast_sub(sx + slot_of(bx) * CC_BOX_BYTES, bx * CC_BOXR + warp * 32 + rq * 8);
+          if (bx + CC_NB < first) {
+            refill_barrier();
+            if (ok && tid == 0) issue(bx + CC_NB);
+          }
         }
       }
+    } else {
+      // A slice longer than the ring: two groups of four warps cast every
+      // other box of the sequence [the CC_NB resident boxes, then boxes
+      // 0 .. first - 1 again], a box's four 32-row quarters one per warp.
+      // The box at position p + CC_NB of the sequence reloads into the slot
+      // that position p frees (CC_NB is even: the same group), as soon as
+      // the group is done with it, so the reloads (from L2: read moments
+      // ago) overlap the casts of the resident boxes and both groups work
+      // throughout.
+      const int h = warp >> 2, wq = warp & 3;
+      const int itid = h * 128;   // the group's issuing thread
+      // the CTA's next unit, whose first CC_NB boxes load into the slots as
+      // they are freed for the last time here (box b into slot b, where its
+      // maxima pass expects it)
+      int64_t gn = 0;
+      int coln = 0;
+      const bool more = cid + (k + 1) * ncl < a.units;
+      if (more) unit_geom(k + 1, gn, coln);
+      for (int p = h; p < nbox; p += 2) {
+        const int bx = p < CC_NB ? first + p : p - CC_NB;
+        const int slot = (int)((first + p) % CC_NB);
+        if (p >= CC_NB && ok) {
+          if (mbar_wait(&bars[slot], (phases >> slot) & 1u, nullptr)) {
+            phases ^= 1u << slot;
+            if (tid == itid) pending &= ~(1u << slot);
+          } else {
+            ok = false;   // the load stays pending: the exit path waits for it
+          }
+        }
+        if (ok) cast_sub(sx + slot * CC_BOX_BYTES, bx * CC_BOXR + wq * 32 + rq * 8);
+        if (p + CC_NB < nbox || more) {
+          // the slot is free once the group's four warps are done with it
+          fence_proxy_async_smem();
+          if (h == 0) {
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+          } else {
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+          }
+          if (tid == itid && ok) {
+            if (p + CC_NB < nbox) {
+              issue_at(slot, g, col0, p);
+            } else {
+              issue_at(slot, gn, coln, slot);
+            }
+          }
+        }
+      }
+      preloaded = more ? CC_NB : 0;
+      // every thread follows every slot's phase: the other group's reloads
+      // (a slot serves one group here: positions p and p + CC_NB share it)
+      for (int p = CC_NB + (h ^ 1); p < nbox; p += 2) phases ^= 1u << ((first + p) % CC_NB);
     }
     ok = __syncthreads_and(ok) != 0;
     if (!ok && tid == 0) set_status(a.status, FP8MOE_ERR_TIMEOUT);
@@ -431,7 +493,8 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
       }
   }
   // after a load that timed out, wait (bounded) for the loads still in flight
-  if (tid == 0)
+  // (threads 0 and 128 issue loads)
+  if (tid == 0 || tid == 128)
     for (int sl = 0; sl < CC_NB; ++sl)
       if (pending & (1u << sl)) (void)mbar_wait(&bars[sl], (phases >> sl) & 1u, nullptr);
   // no CTA leaves while its st.async to a peer may be in flight

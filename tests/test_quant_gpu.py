@@ -107,7 +107,11 @@ def test_rowwise_tiny_workload(F):
                                    # CTAs: 2-CTA slices of 704 rows with a partial 64-column tile,
                                    # 4-CTA slices with a ragged last one, 8-CTA slices of 800 rows
                                    # (two pieces each, the second 32 rows)
-                                   (3, 1408, 80), (2, 2000, 48), (5, 6160, 16)])
+                                   (3, 1408, 80), (2, 2000, 48), (5, 6160, 16),
+                                   # 8-CTA slices of 1504 rows: 12 boxes through the 6-slot
+                                   # ring, 6 reloaded in the pipelined cast, a ragged last box
+                                   # and a partial 64-column tile
+                                   (2, 12000, 80)])
 @pytest.mark.parametrize("trans", [True, False])
 def test_colwise_dense_parity(F, kind, okind, E, R, C, trans):
     x = _bf16((E, R, C), E * 1000 + R + C, 0.02)
