@@ -482,12 +482,19 @@ def cpu_baseline(wl, budget_s=20.0):
 # ----------------------------------------------------------------------------
 # --rows: every hot-path row timed at its configuration size
 # ----------------------------------------------------------------------------
-def bench_rows(F, iters=10, only=None):
+def bench_rows(F, iters=30, only=None):
     """One JSON line per kernel: each step of the path at the configuration
-    sizes of the MoE layers (CUDA events on the launching stream, median of
+    sizes of the MoE layers (CUDA events on the launching stream, the mean of
     `iters` runs after warm-up, an L2 flush between runs), with the fraction
     of its roof: HBM bytes / measured copy bandwidth, or FLOPs / measured FP8
-    peak (2 x the bf16 burst), whichever the kernel is bound by."""
+    peak (2 x the bf16 burst), whichever the kernel is bound by.
+
+    The event clock of these GPUs advances in steps of about 2 us, so a
+    single reading of a short kernel is off by up to a step; the start of a
+    run falls at a random point between steps, which makes the mean of many
+    readings unbiased where a median would stay on the step grid.  Readings
+    more than twice the median (a run interrupted by something else) are
+    left out."""
     import torch
     import workloads as W
     dev = torch.device("cuda")
@@ -525,7 +532,9 @@ def bench_rows(F, iters=10, only=None):
             ts.append(s.elapsed_time(e))
         assert F.fp8moe_get_device_status() == 0
         ts.sort()
-        return ts[len(ts) // 2]
+        med = ts[len(ts) // 2]
+        kept = [t for t in ts if t <= 2.0 * med]
+        return sum(kept) / len(kept)
 
     def emit(row, kernel, config, ms, nbytes=None, flops=None, roof_of_hbm=False):
         d = {"row": row, "kernel": kernel, "config": config, "us": round(ms * 1e3, 1)}
@@ -611,7 +620,7 @@ def bench_rows(F, iters=10, only=None):
         F.fp8moe_mxfp8_quantize_dim0(w1, scale=s_rm)
         s_sw = torch.zeros(F.fp8moe_swizzled_scales_bytes(sc.E, sc.N, sc.K // 32), dtype=torch.uint8, device=dev)
         ms = timed(lambda: F.fp8moe_swizzle_scales_128x4(s_rm, out=s_sw))
-        emit("a5", "k_swizzle", "scout W1 scales [16,8192,160]", ms, nbytes=s_rm.numel() * 2)
+        emit("a5", "k_swizzle_rows (one bulk copy per 128-row block)", "scout W1 scales [16,8192,160]", ms, nbytes=s_rm.numel() * 2)
     if want("mx") or want("swizzle"):
         del a, w1
     if want("mx"):

@@ -17,6 +17,9 @@
 #include "common.cuh"
 #include "launch.h"
 #include "scales.cuh"
+#include "tma.cuh"
+
+#include <type_traits>
 
 namespace fp8moe {
 
@@ -165,6 +168,89 @@ __global__ void __launch_bounds__(256) k_swizzle(SwizzleArgs a) {
   }
 }
 
+// Rows of whole 16-byte chunks (Cs % 16 == 0), without column groups: the
+// source rows of a padded 128-row block are contiguous (groups are padded to
+// whole blocks), so one bulk copy brings the block into shared memory, and
+// every CTA has its block's load in flight at once (a 21 MB tiling is one
+// round of loads, where the staged kernel above takes two or three rounds of
+// load, then store).  A thread then takes the 16-byte chunk j of rows r32,
+// r32 + 32, r32 + 64 and r32 + 96: word s of each holds that row's columns
+// of tile 4j + s, so the four words make the tile's 16 output bytes at row
+// r32; a warp's stores cover a whole 512-byte tile.
+constexpr int SWR_THREADS = 128;
+constexpr int64_t SWR_MAX_CS = 384;   // a block of at most 48 KB
+
+template <bool GROWS>
+__global__ void __launch_bounds__(SWR_THREADS) k_swizzle_rows(SwizzleArgs a) {
+  extern __shared__ __align__(128) uint8_t rows[];
+  __shared__ uint64_t bar;
+  __shared__ std::conditional_t<GROWS, GroupTable, char> gt_s;
+  bool bad = false;
+  if constexpr (GROWS) {
+    build_group_table(gt_s, a.offs, a.E, a.R, GT_ROWS128, a.status);
+    bad = gt_s.bad;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const int64_t nrb = a.Rp / 128;
+  const int nch = (int)(a.Cs / 16);
+  uint32_t phase = 0;
+  bool ok = true;
+  int lost = -1;   // thread 0: the phase of a load whose wait ran out
+  for (int64_t u = blockIdx.x; u < a.B * nrb; u += gridDim.x) {
+    const int64_t b = u / nrb, rbk = u - b * nrb;
+    int64_t r0 = rbk * 128, rn;
+    if constexpr (GROWS) {
+      const int g = find_last_le(gt_s.pad, a.E, rbk * 128);
+      const int64_t st = g == 0 ? 0 : gt_s.end[g - 1];
+      r0 = st + (rbk * 128 - gt_s.pad[g]);
+      rn = gt_s.end[g] - r0;
+    } else {
+      rn = a.R - r0;
+    }
+    rn = bad ? 0 : (rn < 0 ? 0 : (rn > 128 ? 128 : rn));
+    const uint32_t bytes = (uint32_t)(rn * a.Cs);
+    // the previous block's reads (generic proxy) come before the copy's writes
+    fence_proxy_async_smem();
+    ok = __syncthreads_and(ok) != 0;
+    if (bytes > 0) {
+      if (threadIdx.x == 0 && ok) {
+        mbar_expect_tx(&bar, bytes);
+        bulk_load(rows, a.s + (b * a.R + r0) * a.Cs, bytes, &bar);
+      }
+      if (ok && !mbar_wait(&bar, phase, nullptr)) {
+        ok = false;
+        if (threadIdx.x == 0) {
+          set_status(a.status, FP8MOE_ERR_TIMEOUT);
+          lost = (int)phase;
+        }
+      }
+      phase ^= 1;
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.out + b * a.Rp * a.Cp + rbk * (a.Cp / 4) * 512);
+    for (int e = threadIdx.x; e < 32 * nch; e += SWR_THREADS) {
+      const int j = e >> 5, r32 = e & 31;
+      uint4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = r32 + 32 * q;
+        v[q] = i < rn && ok ? *reinterpret_cast<const uint4*>(rows + (int64_t)i * a.Cs + 16 * j)
+                            : make_uint4(0, 0, 0, 0);
+      }
+      dst[(4 * j + 0) * 32 + r32] = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+      dst[(4 * j + 1) * 32 + r32] = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+      dst[(4 * j + 2) * 32 + r32] = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+      dst[(4 * j + 3) * 32 + r32] = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+    }
+  }
+  // a load whose wait ran out may still land: wait for it (bounded) before
+  // the shared memory goes away
+  if (lost >= 0) (void)mbar_wait(&bar, (uint32_t)lost, nullptr);
+}
+
 cudaError_t launch_swizzle(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, const int32_t* offs,
                            int64_t E, int group_axis, uint8_t* out, int* status, int num_sms,
                            cudaStream_t st) {
@@ -181,6 +267,34 @@ cudaError_t launch_swizzle(const uint8_t* s, int64_t B, int64_t R, int64_t Cs, c
   a.Cp = g.Cp;
   a.out = out;
   a.status = status;
+  if (group_axis != FP8MOE_GROUP_COLS && Cs % 16 == 0 && Cs <= SWR_MAX_CS &&
+      (reinterpret_cast<uintptr_t>(s) & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+    const int64_t blocks_all = B * (g.Rp / 128);
+    if (blocks_all == 0) return cudaSuccess;
+    const size_t smem = (size_t)(128 * Cs);
+    const bool grows = group_axis == FP8MOE_GROUP_ROWS;
+    // resident CTAs per SM at this block size (cached per variant and size)
+    static std::atomic<long long> occ[2];
+    long long c = occ[grows].load(std::memory_order_relaxed);
+    int per = (int)(c & 0xFFFFFFFF);
+    if ((size_t)(c >> 32) != smem || per <= 0) {
+      auto kern = grows ? k_swizzle_rows<true> : k_swizzle_rows<false>;
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, kern, SWR_THREADS, smem) != cudaSuccess || per < 1) {
+        (void)cudaGetLastError();
+        per = 2;
+      }
+      occ[grows].store(((long long)smem << 32) | (unsigned)per, std::memory_order_relaxed);
+    }
+    const int64_t cap = (int64_t)num_sms * per;
+    const int64_t blocks = blocks_all < cap ? blocks_all : cap;
+    if (grows)
+      k_swizzle_rows<true><<<(unsigned)blocks, SWR_THREADS, smem, st>>>(a);
+    else
+      k_swizzle_rows<false><<<(unsigned)blocks, SWR_THREADS, smem, st>>>(a);
+    return cudaGetLastError();
+  }
   const int64_t units = B * (g.Rp / 128) * ((g.Cp + SW_CC - 1) / SW_CC);
   if (units == 0) return cudaSuccess;
   // as many CTAs as fit on the GPU at once (each unit is a load-then-store

@@ -232,7 +232,10 @@ def test_mx_tiny_workload(F):
 # swizzle
 # ----------------------------------------------------------------------------
 
-@pytest.mark.parametrize("B,R,Cs", [(1, 1024, 8), (4, 512, 8), (1, 1, 1), (2, 200, 7), (1, 300, 160)])
+@pytest.mark.parametrize("B,R,Cs", [(1, 1024, 8), (4, 512, 8), (1, 1, 1), (2, 200, 7), (1, 300, 160),
+                                    # rows of whole 16-byte chunks (the 16-byte staging path):
+                                    # batched with a ragged row block, two full column chunks
+                                    (3, 257, 48), (1, 128, 256)])
 def test_swizzle_plain(F, B, R, Cs):
     s = torch.randint(1, 255, (B, R, Cs), dtype=torch.uint8, generator=torch.Generator().manual_seed(R))
     out = F.fp8moe_swizzle_scales_128x4(s.to(DEV))
@@ -241,9 +244,10 @@ def test_swizzle_plain(F, B, R, Cs):
 
 
 @pytest.mark.parametrize("sizes", [[96, 0, 0, 928], [100, 0, 160, 40], [0, 0, 5], [300]])
-def test_swizzle_group_rows(F, sizes):
+@pytest.mark.parametrize("Cs", [6, 32])
+def test_swizzle_group_rows(F, sizes, Cs):
     R = sum(sizes)
-    s = torch.randint(1, 255, (R, 6), dtype=torch.uint8, generator=torch.Generator().manual_seed(R))
+    s = torch.randint(1, 255, (R, Cs), dtype=torch.uint8, generator=torch.Generator().manual_seed(R))
     offs = W.offsets_from_sizes(sizes)
     out = F.fp8moe_swizzle_scales_128x4(s.to(DEV), torch.from_numpy(offs).to(DEV), F.GROUP_ROWS)
     assert np.array_equal(out.cpu().numpy(), OS.swizzle(s.numpy(), offs, OS.GROUP_ROWS))
