@@ -7,7 +7,14 @@
 // forward and the two backward GEMMs); doing both from one read moves 4 bytes
 // per element instead of the 6 of two separate passes.
 //
-// Layout of the work: a warp owns a band of up to 128 rows x 128 columns and
+// Two forms.  Both directions with at least 128 columns run the
+// warp-specialised kernel (k_mx_dual_ws, described where it is defined): a
+// producer warp stages 32 x 128 sub-tiles in a shared-memory ring by TMA,
+// and dim0 and dim1 consumer warps each take one direction, a lane one
+// block.  Narrower tensors and the dim1-only call run the register-tile form
+// below (k_mx_dual), which was measured faster there.
+//
+// Register-tile form: a warp owns a band of up to 128 rows x 128 columns and
 // sweeps it in 32-row sub-tiles, so that every 128-byte line of the
 // transposed codes and of the scales is completed by one warp within a short
 // time (while it is still in L2); small tensors use lower bands so that every
@@ -28,6 +35,8 @@
 
 #include <string.h>
 
+#include <atomic>
+#include <type_traits>
 #include <mutex>
 
 #include "common.cuh"
@@ -351,6 +360,231 @@ __global__ void __launch_bounds__(32 * DUAL_WARPS, 2) k_mx_dual(const __grid_con
   if (PF && !live && lane == 0) (void)mbar_wait(wbar, lost, nullptr);
 }
 
+// ---------------------------------------------------------------------------
+// Warp-specialised form of both directions (C >= 128).  The CTA walks its
+// band tiles (the same enumeration as above, tiles blockIdx.x, + gridDim.x,
+// ...) sub-tile by sub-tile; a producer warp brings each 32-row x 128-column
+// sub-tile into a four-slot shared-memory ring by TMA (two 64-column boxes,
+// 128-byte swizzle: 16-byte chunk c of row r at r * 128 + (c ^ (r % 8)) * 16)
+// and eight consumer warps work on it from there:
+//   dim0 warps 0-3: a lane owns one 32-element block of a row (row
+//         8w + lane / 4, block lane % 4): four 16-byte reads, its maximum
+//         without shuffles, 32 codes as two 16-byte stores (the four lanes of
+//         a row write its 128 bytes) and the block's scale byte;
+//   dim1 warps 4-7: a lane owns a column pair for 16 rows (pair
+//         16 (w - 4) + lane % 16, rows 16 (lane / 16) ...): sixteen 4-byte
+//         reads, one shuffle with the lane holding the other 16 rows for the
+//         column maxima, and 16 codes per column as one 16-byte store.
+// Per element this is about half the instruction count of the register-tile
+// form (whose dim0 block spans four lanes: two shuffles and the scale work
+// four times per block), and with under 80 registers three CTAs fit per SM.
+constexpr int WS_SLOTS = 4;
+constexpr int WS_SUB_BYTES = 32 * 128 * 2;   // one sub-tile: two 64-column x 32-row boxes of 4 KB
+constexpr size_t WS_SMEM = (size_t)WS_SLOTS * WS_SUB_BYTES + 1024;   // + room to align the ring to 1 KB
+// consumer warps: 4 dim0 + 4 dim1, or (dim1 alone) 4 dim1; one producer warp
+template <bool D0>
+__host__ __device__ constexpr int ws_consumers() { return D0 ? 8 : 4; }
+template <bool D0>
+__host__ __device__ constexpr int ws_threads() { return 32 * (ws_consumers<D0>() + 1); }
+
+FP8MOE_DEV uint32_t lds32(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr));
+  return v;
+}
+
+template <bool D0>
+__global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid_constant__ CUtensorMap tx, DualArgs a) {
+  constexpr int WS_CONSUMERS = ws_consumers<D0>();
+  __shared__ std::conditional_t<D0, GroupTable, char> gt0_s;
+  __shared__ GroupTable gt1;
+  __shared__ uint64_t full[WS_SLOTS], empty[WS_SLOTS];
+  __shared__ int abort_s;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
+  if constexpr (D0) {
+    if (a.s0.layout == FP8MOE_GROUP_ROWS) {
+      build_group_table(gt0_s, a.s0.offs, a.s0.E, a.R, GT_ROWS128, a.status);
+      if (gt0_s.bad) return;
+    }
+  }
+  if (a.s1.layout == FP8MOE_GROUP_COLS) {
+    build_group_table(gt1, a.s1.offs, a.s1.E, a.R, GT_COLS, a.status);
+    if (gt1.bad) return;
+  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < WS_SLOTS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], WS_CONSUMERS);
+    }
+    abort_s = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  auto tile_of = [&](uint32_t t, uint32_t& ct, uint32_t& rt0, int64_t& b) {
+    ct = t % a.n_ct;
+    const uint32_t rest = t / a.n_ct;
+    rt0 = (rest % a.n_band) * a.nsub;
+    b = rest / a.n_band;
+  };
+  const uint32_t ring_s = smem_u32(ring);
+
+  if (warp == WS_CONSUMERS) {
+    // ======================= producer =======================
+    if (lane == 0) {
+      uint32_t k = 0;
+      for (uint32_t t = blockIdx.x; t < a.tiles && !abort_s; t += gridDim.x) {
+        uint32_t ct, rt0;
+        int64_t b;
+        tile_of(t, ct, rt0, b);
+        const int nv = (int)min((uint32_t)a.nsub, a.n_rt - rt0);
+        for (int sub = 0; sub < nv; ++sub, ++k) {
+          const uint32_t s = k % WS_SLOTS, round = k / WS_SLOTS;
+          if (k >= WS_SLOTS && !mbar_wait(&empty[s], (round - 1) & 1u, &abort_s)) {
+            if (!abort_s) set_status(a.status, FP8MOE_ERR_TIMEOUT);
+            abort_s = 1;
+            break;
+          }
+          const int row = (int)(b * a.R + (int64_t)(rt0 + sub) * 32);
+          mbar_expect_tx(&full[s], WS_SUB_BYTES);
+          tma_load_2d(ring + s * WS_SUB_BYTES, &tx, &full[s], (int)(ct * 128), row);
+          tma_load_2d(ring + s * WS_SUB_BYTES + WS_SUB_BYTES / 2, &tx, &full[s], (int)(ct * 128 + 64), row);
+        }
+      }
+      // the loads still in flight land before the CTA can leave: the last
+      // fill of each slot (the consumers may have stopped early)
+      for (uint32_t j = k > WS_SLOTS ? k - WS_SLOTS : 0; j < k; ++j)
+        (void)mbar_wait(&full[j % WS_SLOTS], (j / WS_SLOTS) & 1u, nullptr);
+    }
+    return;
+  }
+
+  // ======================= consumers =======================
+  const bool d0w = D0 && warp < 4;
+  // dim0 lane: row rl of the sub-tile, 32-column block bq
+  const int bq = lane & 3, rl = warp * 8 + (lane >> 2);
+  // dim1 lane: column pair cp (columns 2cp, 2cp + 1), rows 16 * half ...
+  const int half = lane >> 4, cp = (warp & 3) * 16 + (lane & 15);
+  int g0c = 0, g1c = 0;   // forward-only group cursors (the CTA's rows only grow within a batch)
+  auto advance = [](const GroupTable& gt, int E, int& g, int64_t r) {
+    while (g < E - 1 && gt.end[g] <= r) ++g;
+  };
+  uint32_t k = 0;
+  bool ok = true;
+  for (uint32_t t = blockIdx.x; t < a.tiles && ok; t += gridDim.x) {
+    uint32_t ct, rt0;
+    int64_t b;
+    tile_of(t, ct, rt0, b);
+    const int nv = (int)min((uint32_t)a.nsub, a.n_rt - rt0);
+    const int64_t c0 = (int64_t)ct * 128;
+    for (int sub = 0; sub < nv; ++sub, ++k) {
+      const uint32_t s = k % WS_SLOTS;
+      if (!mbar_wait(&full[s], (k / WS_SLOTS) & 1u, &abort_s)) {
+        if (!abort_s) set_status(a.status, FP8MOE_ERR_TIMEOUT);
+        abort_s = 1;
+        ok = false;
+        break;
+      }
+      const int64_t r = (int64_t)(rt0 + sub) * 32;   // first row of the sub-tile (in batch b)
+      const uint32_t slot = ring_s + s * WS_SUB_BYTES;
+      if constexpr (D0) {
+      if (d0w) {
+        const GroupTable& gt0 = gt0_s;
+        // ---- dim0: the block of 32 at (row r + rl, columns c0 + 32 bq ...)
+        const int64_t col = c0 + 32 * bq;
+        const uint32_t rb = slot + (uint32_t)((bq >> 1) * (WS_SUB_BYTES / 2) + rl * 128);
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = lds16(rb + (uint32_t)(((((bq & 1) * 4 + j) ^ (rl & 7))) << 4));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        uint32_t m2 = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          m2 = max_abs_bf16x2(m2, max_abs_bf16x2(max_abs_bf16x2(v[j].x, v[j].y), max_abs_bf16x2(v[j].z, v[j].w)));
+        m2 = max_abs_bf16x2(m2, __byte_perm(m2, 0, 0x1032));
+        uint32_t p2;
+        const uint32_t byte = mx_block_scale(m2 & 0xFFFFu, p2);
+        if (col < a.C) {
+          const uint2 e0 = enc_row8(v[0], p2), e1 = enc_row8(v[1], p2), e2 = enc_row8(v[2], p2),
+                      e3 = enc_row8(v[3], p2);
+          uint8_t* qp = a.q0 + (b * a.R + r + rl) * a.C + col;
+          *reinterpret_cast<uint4*>(qp) = make_uint4(e0.x, e0.y, e1.x, e1.y);
+          *reinterpret_cast<uint4*>(qp + 16) = make_uint4(e2.x, e2.y, e3.x, e3.y);
+          int64_t off;
+          if (a.s0.layout == FP8MOE_GROUP_ROWS) {
+            advance(gt0, a.s0.E, g0c, r + rl);
+            const int64_t gs = g0c == 0 ? 0 : gt0.end[g0c - 1];
+            off = tile_off(gt0.pad[g0c] + (r + rl - gs), col >> 5, a.s0.Cp);
+          } else if (a.s0.layout == FP8MOE_NO_GROUPS) {
+            off = b * a.s0.Rp * a.s0.Cp + tile_off(r + rl, col >> 5, a.s0.Cp);
+          } else {
+            off = (b * a.R + r + rl) * (a.C >> 5) + (col >> 5);
+          }
+          a.s0.p[off] = (uint8_t)byte;
+        }
+        continue;
+      }
+      }
+      {
+        // ---- dim1: columns (2cp, 2cp + 1) over rows r + 16 half ... + 15
+        const uint32_t cb = slot + (uint32_t)((cp >> 5) * (WS_SUB_BYTES / 2) + (cp & 3) * 4);
+        const uint32_t cc = (uint32_t)((cp & 31) >> 2);
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t row = (uint32_t)(half * 16 + i);
+          v[i] = lds32(cb + row * 128 + ((cc ^ (row & 7)) << 4));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        uint32_t mw = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mw = max_abs_bf16x2(mw, v[i]);
+        mw = max_abs_bf16x2(mw, __shfl_xor_sync(FULL, mw, 16));
+        const uint32_t efl = max((mw >> 7) & 0xFFu, 8u), efh = max((mw >> 23) & 0xFFu, 8u);
+        const uint32_t p2 = ((262u - efl) << 7) | ((262u - efh) << 23);
+        const int64_t col = c0 + 2 * cp;
+        if (col < a.C) {
+          if (half == 0) {
+            // the two columns' scale bytes of row block r / 32 (the sub-tile
+            // lies inside one routing group: offsets are multiples of 32)
+            const int64_t rb = r >> 5;
+            int64_t off, step;
+            if (a.s1.layout == FP8MOE_GROUP_COLS) {
+              advance(gt1, a.s1.E, g1c, r);
+              const int64_t gs = g1c == 0 ? 0 : gt1.end[g1c - 1];
+              off = tile_off(col, gt1.pad[g1c] + (rb - gs / 32), a.s1.Cp);
+              step = 16;
+            } else if (a.s1.layout == FP8MOE_NO_GROUPS) {
+              off = b * a.s1.Rp * a.s1.Cp + tile_off(col, rb, a.s1.Cp);
+              step = 16;
+            } else {
+              off = (b * a.C + col) * (a.R >> 5) + rb;
+              step = a.R >> 5;
+            }
+            a.s1.p[off] = (uint8_t)(efl - 8u);
+            a.s1.p[off + step] = (uint8_t)(efh - 8u);
+          }
+          uint32_t lo[4], hi[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t y0 = mul_bf16x2(v[4 * q], p2), y1 = mul_bf16x2(v[4 * q + 1], p2);
+            const uint32_t y2 = mul_bf16x2(v[4 * q + 2], p2), y3 = mul_bf16x2(v[4 * q + 3], p2);
+            lo[q] = cvt4(lo_f32(y0), lo_f32(y1), lo_f32(y2), lo_f32(y3));
+            hi[q] = cvt4(hi_f32(y0), hi_f32(y1), hi_f32(y2), hi_f32(y3));
+          }
+          uint8_t* qp = a.q1 + (b * a.C + col) * a.R + r + half * 16;
+          *reinterpret_cast<uint4*>(qp) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(qp + a.R) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        }
+      }
+    }
+    if (!ok) break;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void* q0, uint8_t* s0, int s0_layout,
@@ -365,10 +599,6 @@ cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void*
   a.C = C;
   a.n_ct = (uint32_t)((C + 127) / 128);
   a.n_rt = (uint32_t)(R / 32);
-  // bands of 4 sub-tiles when that leaves several bands per warp, else lower
-  const int64_t warps = (int64_t)num_sms * 2 * 8;
-  a.nsub = 4;
-  while (a.nsub > 1 && (int64_t)a.n_ct * ((a.n_rt + a.nsub - 1) / a.nsub) * B < 4 * warps) a.nsub >>= 1;
   // FP8MOE_DUAL_BAND=1|2|4 fixes the band height (tests use it to cover every
   // band shape on small inputs)
   static const int force_band = [] {
@@ -376,6 +606,58 @@ cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void*
     const int n = v ? atoi(v) : 0;
     return (n == 1 || n == 2 || n == 4) ? n : 0;
   }();
+  // both directions with at least one whole 128-column tile: the
+  // warp-specialised kernel (FP8MOE_DUAL_WS=0 keeps the register-tile form,
+  // for comparison).  Its dim1-only instance (four dim1 warps) measured
+  // slower than the register-tile form (Scout W1 412 against 387 us, the
+  // activation 57 against 49 us), which keeps that case; FP8MOE_DUAL_WS=1
+  // selects it anyway.
+  static const int ws_env = [] {
+    const char* v = getenv("FP8MOE_DUAL_WS");
+    return v ? atoi(v) : -1;
+  }();
+  if (C >= 128 && (q0 ? ws_env != 0 : ws_env == 1)) {
+    static std::atomic<int> per_sm_ws[2];
+    static std::once_flag ws_once;
+    std::call_once(ws_once, [] {
+      cudaFuncSetAttribute(k_mx_dual_ws<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)WS_SMEM);
+      cudaFuncSetAttribute(k_mx_dual_ws<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)WS_SMEM);
+    });
+    const bool both = q0 != nullptr;
+    const int per = both ? blocks_per_sm(per_sm_ws[1], k_mx_dual_ws<true>, ws_threads<true>(), WS_SMEM, 2)
+                         : blocks_per_sm(per_sm_ws[0], k_mx_dual_ws<false>, ws_threads<false>(), WS_SMEM, 2);
+    const int64_t ctas = (int64_t)num_sms * per;
+    // bands of 4 sub-tiles while every CTA gets 16 band tiles or more
+    a.nsub = 4;
+    while (a.nsub > 1 && (int64_t)a.n_ct * ((a.n_rt + a.nsub - 1) / a.nsub) * B < 16 * ctas) a.nsub >>= 1;
+    if (force_band) a.nsub = force_band;
+    a.n_band = (a.n_rt + a.nsub - 1) / a.nsub;
+    const int64_t tiles = (int64_t)a.n_ct * a.n_band * B;
+    if (tiles >= ((int64_t)1 << 31) || B * R >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
+    a.tiles = (uint32_t)tiles;
+    a.boxc = 64;
+    a.q0 = (uint8_t*)q0;
+    a.q1 = (uint8_t*)q1;
+    a.s0 = make_spec(s0, both ? s0_layout : FP8MOE_SCALES_ROWMAJOR, R, C / 32, offs, E);
+    a.s1 = make_spec(s1, s1_layout, C, R / 32, offs, E);
+    a.status = status;
+    CUtensorMap tx;
+    memset(&tx, 0, sizeof(tx));
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(B * R)};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {64, 32};
+    if (!make_tmap(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    const int64_t grid = tiles < ctas ? tiles : ctas;
+    if (both)
+      k_mx_dual_ws<true><<<(unsigned)grid, ws_threads<true>(), WS_SMEM, st>>>(tx, a);
+    else
+      k_mx_dual_ws<false><<<(unsigned)grid, ws_threads<false>(), WS_SMEM, st>>>(tx, a);
+    return cudaGetLastError();
+  }
+  // bands of 4 sub-tiles when that leaves several bands per warp, else lower
+  const int64_t warps = (int64_t)num_sms * 2 * 8;
+  a.nsub = 4;
+  while (a.nsub > 1 && (int64_t)a.n_ct * ((a.n_rt + a.nsub - 1) / a.nsub) * B < 4 * warps) a.nsub >>= 1;
   if (force_band) a.nsub = force_band;
   a.n_band = (a.n_rt + a.nsub - 1) / a.nsub;
   const int64_t tiles = (int64_t)a.n_ct * a.n_band * B;

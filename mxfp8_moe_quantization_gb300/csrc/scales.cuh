@@ -59,10 +59,12 @@ FP8MOE_DEV int find_group(const int64_t* ends, int E, int64_t key) {
 //               size must be a multiple of 32).
 enum { GT_ROWS128 = 0, GT_COLS = 1, GT_SUB32 = 2, GT_BLK128 = 3 };
 
-// Call with all threads of a block of 256; ends with __syncthreads.
+// Call with all threads of a block of at least 256 (a multiple of 32, at most
+// 1024); the groups are spread over the first 256 threads.  Ends with
+// __syncthreads.
 static __device__ void build_group_table(GroupTable& t, const int32_t* offs, int E, int64_t total, int mode,
                                   int* status) {
-  __shared__ int64_t wsum[8];
+  __shared__ int64_t wsum[32];   // per warp (warps past the eighth hold no groups)
   const int tid = threadIdx.x;
   const int per = (E + 255) / 256;  // <= 4
   int64_t u[4] = {0, 0, 0, 0};

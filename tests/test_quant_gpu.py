@@ -281,7 +281,9 @@ def _mx_ref(x_np):
     return q0, s0, q1, s1
 
 
-@pytest.mark.parametrize("shape", [(1024, 256), (96, 96), (32, 64), (160, 5120)])
+@pytest.mark.parametrize("shape", [(1024, 256), (96, 96), (32, 64), (160, 5120),
+                                   # a last 128-column tile with one 64-column box in range
+                                   (32, 192), (64, 448)])
 def test_mx_dual_rowmajor(F, shape):
     x = _bf16(shape, sum(shape) + 7, 2.0)
     q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), None, F.SCALES_ROWMAJOR, F.SCALES_ROWMAJOR)
@@ -413,18 +415,38 @@ def test_mx_dual_band_heights(band):
         pytest.skip("this process already fixes the band height or the load form")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
-                        os.path.abspath(__file__), "-k", "(mx_dual or mx_dim1) and not band_heights"],
+                        os.path.abspath(__file__), "-k",
+                        "(mx_dual or mx_dim1) and not band_heights and not warp_specialised"],
                        cwd=root, env=dict(os.environ, FP8MOE_DUAL_BAND=band), capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+def test_mx_dim1_warp_specialised_form():
+    """The warp-specialised kernel's dim1-only instance (selected with
+    FP8MOE_DUAL_WS=1; the register-tile form serves that case by default)
+    gives identical results: the dim1 and dual cases rerun with it."""
+    import os
+    import subprocess
+    import sys
+    if os.environ.get("FP8MOE_DUAL_WS") or os.environ.get("FP8MOE_DUAL_PREFETCH") or os.environ.get("FP8MOE_DUAL_BAND"):
+        pytest.skip("this process already fixes the kernel form")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
+                        os.path.abspath(__file__), "-k",
+                        "(mx_dual or mx_dim1) and not band_heights and not load_forms and not warp_specialised"],
+                       cwd=root, env=dict(os.environ, FP8MOE_DUAL_WS="1"), capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
 
 
 @pytest.mark.parametrize("prefetch", ["0", "1"])
 def test_mx_dual_load_forms(prefetch):
-    """Both ways the fused kernel gets its sub-tiles (a TMA load into the
-    warp's buffer one sub-tile ahead, or plain loads into registers; chosen by
-    tensor size) give identical results: the dual / dim1 cases rerun with the
-    form fixed."""
+    """The register-tile form of the fused kernel (the one for fewer than 128
+    columns; FP8MOE_DUAL_WS=0 selects it for every shape) in both ways it gets
+    its sub-tiles (a TMA load into the warp's buffer one sub-tile ahead, or
+    plain loads into registers; chosen by tensor size) gives identical
+    results: the dual / dim1 cases rerun with that form and the load fixed."""
     import os
     import subprocess
     import sys
@@ -432,7 +454,9 @@ def test_mx_dual_load_forms(prefetch):
         pytest.skip("this process already fixes the load form or the band height")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
-                        os.path.abspath(__file__), "-k", "(mx_dual or mx_dim1) and not band_heights and not load_forms"],
-                       cwd=root, env=dict(os.environ, FP8MOE_DUAL_PREFETCH=prefetch), capture_output=True, text=True,
+                        os.path.abspath(__file__), "-k",
+                        "(mx_dual or mx_dim1) and not band_heights and not load_forms and not warp_specialised"],
+                       cwd=root, env=dict(os.environ, FP8MOE_DUAL_PREFETCH=prefetch, FP8MOE_DUAL_WS="0"),
+                       capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
