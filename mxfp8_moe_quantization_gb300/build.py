@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp8moe.so")
 
-SOURCES = ["api.cu", "quant.cu", "colwise.cu", "colwise_cluster.cu", "dual.cu", "tensorwise.cu", "blockwise.cu", "routing.cu", "swizzle.cu",
+SOURCES = ["api.cu", "quant.cu", "colwise.cu", "colwise_cluster.cu", "colwise_jagged.cu", "dual.cu", "tensorwise.cu", "blockwise.cu", "routing.cu", "swizzle.cu",
            "grouped_mm.cu", "blockwise_mm.cu", "layer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

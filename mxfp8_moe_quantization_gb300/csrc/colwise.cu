@@ -24,6 +24,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <stdlib.h>
+#include <string.h>
+
 #include "common.cuh"
 #include "launch.h"
 #include "scales.cuh"
@@ -390,8 +393,16 @@ cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const
   // of routed rows): one pass
   if (!offs && transpose_out && colwise_cluster_supported(E, R, C))
     return launch_colwise_cluster(x, E, R, C, kind, q, inv, status, num_sms, st);
-  if (offs && transpose_out && R > 0 && colwise_cluster_jagged_supported(E, R, C))
-    return launch_colwise_cluster_jagged(x, E, R, C, offs, kind, ldt, q, inv, status, num_sms, st);
+  if (offs && transpose_out && R > 0 && colwise_cluster_jagged_supported(E, R, C)) {
+    // one persistent CTA per SM holding whole group strips; FP8MOE_CW_JAGGED=cluster
+    // selects the two-CTA cluster kernel instead (for comparison)
+    static const bool cluster = [] {
+      const char* v = getenv("FP8MOE_CW_JAGGED");
+      return v && strcmp(v, "cluster") == 0;
+    }();
+    if (cluster) return launch_colwise_cluster_jagged(x, E, R, C, offs, kind, ldt, q, inv, status, num_sms, st);
+    return launch_colwise_jagged_ws(x, E, R, C, offs, kind, ldt, q, inv, status, num_sms, st);
+  }
   return run_colwise(x, E, R, C, offs, transpose_out, kind, ldt, q, inv, nullptr, status, num_sms, st);
 }
 

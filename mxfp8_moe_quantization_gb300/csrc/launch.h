@@ -50,6 +50,10 @@ cudaError_t launch_colwise(const void* x, int64_t E, int64_t R, int64_t C, const
 // colwise FP8 of dense [E, R, C] with transposed output in one HBM pass
 // (colwise_cluster.cu), for the sizes colwise_cluster_supported accepts
 bool colwise_cluster_jagged_supported(int64_t E, int64_t R, int64_t C);
+// the same operation on one persistent CTA per SM (no cluster exchange);
+// takes the same arguments and the same supported shapes
+cudaError_t launch_colwise_jagged_ws(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs, int kind,
+                                     int64_t ldt, void* q, float* inv, int* status, int num_sms, cudaStream_t st);
 cudaError_t launch_colwise_cluster_jagged(const void* x, int64_t E, int64_t R, int64_t C, const int32_t* offs,
                                           int kind, int64_t ldt, void* q, float* inv, int* status, int num_sms,
                                           cudaStream_t st);
