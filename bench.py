@@ -587,7 +587,7 @@ def bench_rows(F, iters=30, only=None):
         q = torch.empty((ds.K, F.fp8moe_jagged_t_cols(ds.M, ds.E)), dtype=torch.uint8, device=dev)
         inv = torch.empty(ds.E, ds.K, dtype=torch.float32, device=dev)
         ms = timed(lambda: F.fp8moe_quantize_colwise_3d(ads, dsoffs, True, q=q, scale_inv=inv))
-        emit("a2", "k_cw_cluster jagged (one pass)", f"dsmoe_16b jagged A [{ds.M},{ds.K}] transposed", ms,
+        emit("a2", "k_cw_jag_ws (one pass, one CTA per group strip)", f"dsmoe_16b jagged A [{ds.M},{ds.K}] transposed", ms,
              nbytes=ads.numel() * 3 + ds.E * ds.K * 4)
         del ads
     if want("tensorwise"):
@@ -613,7 +613,7 @@ def bench_rows(F, iters=30, only=None):
             ms = timed(lambda: F.fp8moe_mxfp8_quantize_dim1(t, qt=o[2]))
             emit("a4", "k_mx_dual<dim1>", f"scout {name}", ms, nbytes=n * (3 + 1 / 32))
             ms = timed(lambda: F.fp8moe_mxfp8_quantize_dual(t, offs, l0, l1, q0=o[0], s0=o[1], q1=o[2], s1=o[3]))
-            emit("next1", "k_mx_dual (both directions, one read)", f"scout {name} final-layout scales", ms,
+            emit("next1", "k_mx_dual_ws (both directions, one read)", f"scout {name} final-layout scales", ms,
                  nbytes=n * (4 + 2 / 32))
     if want("swizzle"):
         s_rm = torch.empty(sc.E, sc.N, sc.K // 32, dtype=torch.uint8, device=dev)
@@ -628,7 +628,7 @@ def bench_rows(F, iters=30, only=None):
         o = F.fp8moe_mxfp8_quantize_dual(w3, None, F.NO_GROUPS, F.NO_GROUPS)
         ms = timed(lambda: F.fp8moe_mxfp8_quantize_dual(w3, None, F.NO_GROUPS, F.NO_GROUPS, q0=o[0], s0=o[1], q1=o[2],
                                                          s1=o[3]))
-        emit("next1", "k_mx_dual (both directions, one read)", "dsv3 W1 [256,2048,7168]", ms,
+        emit("next1", "k_mx_dual_ws (both directions, one read)", "dsv3 W1 [256,2048,7168]", ms,
              nbytes=w3.numel() * (4 + 2 / 32))
         ms = timed(lambda: F.fp8moe_mxfp8_quantize_dim0(w3, q=o[0]))
         emit("a3", "k_mx_dim0", "dsv3 W1 [256,2048,7168]", ms, nbytes=w3.numel() * (3 + 1 / 32))

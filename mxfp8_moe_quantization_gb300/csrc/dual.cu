@@ -400,6 +400,11 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
   __shared__ GroupTable gt1;
   __shared__ uint64_t full[WS_SLOTS], empty[WS_SLOTS];
   __shared__ int abort_s;
+  // grouped layouts, per slot: the row shift into the padded scale matrix of
+  // the sub-tile's group (dim0: padded row = row + shift0, or NO_SHIFT when
+  // a group ends inside the sub-tile; dim1: padded 32-block column = block +
+  // shift1), set by the producer before it issues the slot's load
+  __shared__ int64_t shift0_s[WS_SLOTS], shift1_s[WS_SLOTS];
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   if constexpr (D0) {
@@ -430,10 +435,12 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
   };
   const uint32_t ring_s = smem_u32(ring);
 
+  constexpr int64_t NO_SHIFT = -((int64_t)1 << 62);   // no shift: rows of two groups
   if (warp == WS_CONSUMERS) {
     // ======================= producer =======================
     if (lane == 0) {
       uint32_t k = 0;
+      int pg0 = 0, pg1 = 0;   // group cursors (the CTA's rows only grow: B == 1 for grouped layouts)
       for (uint32_t t = blockIdx.x; t < a.tiles && !abort_s; t += gridDim.x) {
         uint32_t ct, rt0;
         int64_t b;
@@ -446,7 +453,22 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
             abort_s = 1;
             break;
           }
-          const int row = (int)(b * a.R + (int64_t)(rt0 + sub) * 32);
+          const int64_t r = (int64_t)(rt0 + sub) * 32;
+          if constexpr (D0) {
+            if (a.s0.layout == FP8MOE_GROUP_ROWS) {
+              const GroupTable& gt0 = gt0_s;
+              while (pg0 < a.s0.E - 1 && gt0.end[pg0] <= r) ++pg0;
+              const int64_t gs = pg0 == 0 ? 0 : gt0.end[pg0 - 1];
+              shift0_s[s] = gt0.end[pg0] >= r + 32 ? gt0.pad[pg0] - gs : NO_SHIFT;
+            }
+          }
+          if (a.s1.layout == FP8MOE_GROUP_COLS) {
+            while (pg1 < a.s1.E - 1 && gt1.end[pg1] <= r) ++pg1;
+            const int64_t gs = pg1 == 0 ? 0 : gt1.end[pg1 - 1];
+            shift1_s[s] = gt1.pad[pg1] - gs / 32;
+          }
+          const int row = (int)(b * a.R + r);
+          // (the arrive below releases the shifts to the consumers' wait)
           mbar_expect_tx(&full[s], WS_SUB_BYTES);
           tma_load_2d(ring + s * WS_SUB_BYTES, &tx, &full[s], (int)(ct * 128), row);
           tma_load_2d(ring + s * WS_SUB_BYTES + WS_SUB_BYTES / 2, &tx, &full[s], (int)(ct * 128 + 64), row);
@@ -466,7 +488,7 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
   const int bq = lane & 3, rl = warp * 8 + (lane >> 2);
   // dim1 lane: column pair cp (columns 2cp, 2cp + 1), rows 16 * half ...
   const int half = lane >> 4, cp = (warp & 3) * 16 + (lane & 15);
-  int g0c = 0, g1c = 0;   // forward-only group cursors (the CTA's rows only grow within a batch)
+  int g0c = 0;   // forward-only group cursor for rows whose sub-tile holds two groups
   auto advance = [](const GroupTable& gt, int E, int& g, int64_t r) {
     while (g < E - 1 && gt.end[g] <= r) ++g;
   };
@@ -497,6 +519,7 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
         uint4 v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) v[j] = lds16(rb + (uint32_t)(((((bq & 1) * 4 + j) ^ (rl & 7))) << 4));
+        const int64_t sh0 = a.s0.layout == FP8MOE_GROUP_ROWS ? shift0_s[s] : 0;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         uint32_t m2 = 0;
@@ -514,9 +537,14 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
           *reinterpret_cast<uint4*>(qp + 16) = make_uint4(e2.x, e2.y, e3.x, e3.y);
           int64_t off;
           if (a.s0.layout == FP8MOE_GROUP_ROWS) {
-            advance(gt0, a.s0.E, g0c, r + rl);
-            const int64_t gs = g0c == 0 ? 0 : gt0.end[g0c - 1];
-            off = tile_off(gt0.pad[g0c] + (r + rl - gs), col >> 5, a.s0.Cp);
+            if (sh0 != NO_SHIFT) {
+              off = tile_off(r + rl + sh0, col >> 5, a.s0.Cp);
+            } else {
+              // a group ends inside this sub-tile: this row's own group
+              advance(gt0, a.s0.E, g0c, r + rl);
+              const int64_t gs = g0c == 0 ? 0 : gt0.end[g0c - 1];
+              off = tile_off(gt0.pad[g0c] + (r + rl - gs), col >> 5, a.s0.Cp);
+            }
           } else if (a.s0.layout == FP8MOE_NO_GROUPS) {
             off = b * a.s0.Rp * a.s0.Cp + tile_off(r + rl, col >> 5, a.s0.Cp);
           } else {
@@ -537,6 +565,7 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
           const uint32_t row = (uint32_t)(half * 16 + i);
           v[i] = lds32(cb + row * 128 + ((cc ^ (row & 7)) << 4));
         }
+        const int64_t sh1 = a.s1.layout == FP8MOE_GROUP_COLS ? shift1_s[s] : 0;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         uint32_t mw = 0;
@@ -553,9 +582,7 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
             const int64_t rb = r >> 5;
             int64_t off, step;
             if (a.s1.layout == FP8MOE_GROUP_COLS) {
-              advance(gt1, a.s1.E, g1c, r);
-              const int64_t gs = g1c == 0 ? 0 : gt1.end[g1c - 1];
-              off = tile_off(col, gt1.pad[g1c] + (rb - gs / 32), a.s1.Cp);
+              off = tile_off(col, rb + sh1, a.s1.Cp);
               step = 16;
             } else if (a.s1.layout == FP8MOE_NO_GROUPS) {
               off = b * a.s1.Rp * a.s1.Cp + tile_off(col, rb, a.s1.Cp);
