@@ -84,7 +84,11 @@ def test_weight_parity(F, kind, okind, E, N, K):
 
 @pytest.mark.parametrize("kind,okind", KINDS)
 @pytest.mark.parametrize("sizes,C", [([96, 0, 320, 32, 0, 160], 48), ([0, 0, 64], 256), ([4096], 144),
-                                     ([32] * 9, 16)])
+                                     ([32] * 9, 16),
+                                     # from 128 columns on, the TMA-ring kernel: enough units
+                                     # (81 token blocks x 16 column tiles) for every CTA's
+                                     # six-slot ring to wrap, blocks ending inside groups
+                                     ([3008, 0, 4992, 2016, 96], 2048)])
 def test_tokens_parity(F, kind, okind, sizes, C):
     offs = W.offsets_from_sizes(sizes)
     M = int(sum(sizes))
