@@ -143,6 +143,23 @@ def test_colwise_jagged_parity(F, kind, okind, sizes, trans):
     assert F.fp8moe_get_device_status() == 0
 
 
+def test_colwise_jagged_cluster_form():
+    """The two-CTA cluster kernel for routed rows (FP8MOE_CW_JAGGED=cluster;
+    the one-CTA-per-strip kernel serves them by default) gives identical
+    results: the jagged colwise cases rerun with it."""
+    import os
+    import subprocess
+    import sys
+    if os.environ.get("FP8MOE_CW_JAGGED"):
+        pytest.skip("this process already fixes the jagged kernel")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu",
+                        os.path.abspath(__file__), "-k", "colwise_jagged and not cluster_form"],
+                       cwd=root, env=dict(os.environ, FP8MOE_CW_JAGGED="cluster"), capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
 def test_colwise_jagged_tiny_workload(F):
     wl = W.get_workload("tiny")
     offs = wl.offs()
