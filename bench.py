@@ -277,7 +277,9 @@ def run_e2e(F, sets, steps, warmup, stream_weights=False):
     step i+2's upload overlap, as a training loop with a prefetching loader
     would; every step's transfers are inside the timed region, which ends when
     the last download has landed (one copy stream per direction: spreading
-    the transfers over four streams each way measured slower)."""
+    the transfers over four streams each way measured slower).  Before the
+    steps, the same buffers' copies are timed alone and both ways at once
+    (``host_link``): their rates and the per-step floor they set."""
     import torch
     host_in, host_out = [], []
     for st in sets:
@@ -289,11 +291,53 @@ def run_e2e(F, sets, steps, warmup, stream_weights=False):
                 ho.append((L[k], torch.empty(L[k].shape, dtype=L[k].dtype, pin_memory=True)))
         host_in.append(hi)
         host_out.append(ho)
-    h2d = sum(h.numel() * h.element_size() for _, h in host_in[0])
-    d2h = sum(h.numel() * h.element_size() for _, h in host_out[0])
+    def h2d_bytes(hs):
+        return sum(h.numel() * h.element_size() for _, h in hs[0])
+
+    d2h_bytes = h2d_bytes
+    h2d = h2d_bytes(host_in)
+    d2h = d2h_bytes(host_out)
     comp = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ns = len(sets)
+
+    # the host link on these buffers: one step's uploads alone, downloads
+    # alone, and both at once (their own streams, CUDA events), so that the
+    # end-to-end time can be read against the copies' own floor
+    def copies(up, down, reps=3):
+        for it in range(reps + 1):
+            e0 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e1 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            torch.cuda.synchronize()
+            if up:
+                with torch.cuda.stream(s_in):
+                    e0[0].record(s_in)
+                    for d, h in host_in[0]:
+                        d.copy_(h, non_blocking=True)
+                    e1[0].record(s_in)
+            if down:
+                with torch.cuda.stream(s_out):
+                    e0[1].record(s_out)
+                    for d, h in host_out[0]:
+                        h.copy_(d, non_blocking=True)
+                    e1[1].record(s_out)
+            torch.cuda.synchronize()
+            if it == 0:
+                ms = [0.0, 0.0]
+                continue
+            if up:
+                ms[0] += e0[0].elapsed_time(e1[0]) / reps
+            if down:
+                ms[1] += e0[1].elapsed_time(e1[1]) / reps
+        return ms
+
+    up_ms = copies(True, False)[0]
+    down_ms = copies(False, True)[1]
+    both = copies(True, True)
+    link = {"h2d_gbs": h2d_bytes(host_in) / up_ms / 1e6, "d2h_gbs": d2h_bytes(host_out) / down_ms / 1e6,
+            "h2d_gbs_concurrent": h2d_bytes(host_in) / both[0] / 1e6,
+            "d2h_gbs_concurrent": d2h_bytes(host_out) / both[1] / 1e6,
+            "copies_floor_ms_per_step": max(both)}
     ev_in = [torch.cuda.Event() for _ in range(ns)]
     ev_comp = [torch.cuda.Event() for _ in range(ns)]
     ev_out = [torch.cuda.Event() for _ in range(ns)]
@@ -325,7 +369,7 @@ def run_e2e(F, sets, steps, warmup, stream_weights=False):
         one(warmup + i)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
-    return dt, h2d, d2h
+    return dt, h2d, d2h, link
 
 
 # ----------------------------------------------------------------------------
@@ -998,17 +1042,17 @@ def main():
         # a second buffer set of the same shapes lets transfers and compute
         # of neighbouring steps overlap
         step2 = ScoutStep(F, wl, dev, layers=args.layers, fused=not args.unfused)
-        dt, h2d, d2h = run_e2e(F, [step, step2], max(4, args.steps // 3), 2)
+        dt, h2d, d2h, link = run_e2e(F, [step, step2], max(4, args.steps // 3), 2)
         dt = max_over_ranks(dt, pg, dev)
         e2e = {"value": job_tflops(flops, world, dt * 1e3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
-               "moves": "A, dY in; out, dA back (weights and weight gradients resident)"}
-        dt, h2d, d2h = run_e2e(F, [step, step2], max(4, args.steps // 6), 2, stream_weights=True)
+               "moves": "A, dY in; out, dA back (weights and weight gradients resident)", "host_link": link}
+        dt, h2d, d2h, link = run_e2e(F, [step, step2], max(4, args.steps // 6), 2, stream_weights=True)
         del step2
         dt = max_over_ranks(dt, pg, dev)
         e2e_ws = {"value": job_tflops(flops, world, dt * 1e3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                   "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3,
-                  "moves": "A, W, dY in; out, dA, dW back"}
+                  "moves": "A, W, dY in; out, dA, dW back", "host_link": link}
     extra, extra_launches = ({}, 0) if args.no_dsv3 else dsv3_measure(F, dev)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
