@@ -472,6 +472,19 @@ fp8moe_status fp8moe_testing_stall_next_gemm(void);
  * ------------------------------------------------------------------------ */
 fp8moe_status fp8moe_testing_stall_next_tensorwise(void);
 
+/* ------------------------------------------------------------------------
+ * Testing hook of the failure-detection path of the warp-specialised
+ * quantizers (no counterpart on the pages): fp8moe_mxfp8_quantize_dual with
+ * both directions and at least 128 columns, and fp8moe_quantize_colwise_3d of
+ * routed rows with transposed output.  Arms a one-shot flag: the next such
+ * launch of the process has its first CTA never load its first tile, so that
+ * CTA's consumer warps' bounded wait (2 s) runs out and the launch sets
+ * FP8MOE_ERR_TIMEOUT (its outputs are then not valid).  The CTA's producer
+ * still waits (bounded) for the loads it issued, so no copy is in flight when
+ * it exits and the context stays usable.
+ * ------------------------------------------------------------------------ */
+fp8moe_status fp8moe_testing_stall_next_quant_ring(void);
+
 /* Static string for a status code. */
 const char* fp8moe_status_string(int status);
 

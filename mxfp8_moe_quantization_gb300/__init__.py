@@ -28,6 +28,7 @@ __all__ = [
     "fp8moe_mxfp8_grouped_mm_fwd_quant_a", "fp8moe_mxfp8_grouped_mm_dgrad_quant_a",
     "fp8moe_testing_stall_next_gemm",
     "fp8moe_testing_stall_next_tensorwise",
+    "fp8moe_testing_stall_next_quant_ring",
     "fp8moe_mxfp8_moe_workspace_bytes", "fp8moe_mxfp8_moe_fwd", "fp8moe_mxfp8_moe_bwd",
     "fp8moe_quantize_blockwise_rows", "fp8moe_quantize_blockwise_weight", "fp8moe_blockwise_token_blocks",
     "fp8moe_quantize_blockwise_tokens",
@@ -75,6 +76,7 @@ SYMBOLS = {
     "fp8moe_get_device_status": (_i32, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "fp8moe_testing_stall_next_gemm": (_i32, []),
     "fp8moe_testing_stall_next_tensorwise": (_i32, []),
+    "fp8moe_testing_stall_next_quant_ring": (_i32, []),
     "fp8moe_status_string": (ctypes.c_char_p, [_i32]),
     "fp8moe_version": (_i32, []),
 }
@@ -525,6 +527,13 @@ def fp8moe_testing_stall_next_tensorwise() -> None:
     """Arm the one-shot stall of the next one-launch tensorwise kernel (tests
     of its grid-wide meeting's timeout path)."""
     _check("fp8moe_testing_stall_next_tensorwise", _lib_raw().fp8moe_testing_stall_next_tensorwise())
+
+
+def fp8moe_testing_stall_next_quant_ring() -> None:
+    """Arm the one-shot stall of the next warp-specialised quantization launch
+    (dual-direction MXFP8 or routed-rows transposed colwise; tests of their
+    rings' timeout path)."""
+    _check("fp8moe_testing_stall_next_quant_ring", _lib_raw().fp8moe_testing_stall_next_quant_ring())
 
 
 def fp8moe_status_string(code: int) -> str:

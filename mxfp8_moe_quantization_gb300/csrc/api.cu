@@ -489,4 +489,9 @@ fp8moe_status fp8moe_testing_stall_next_tensorwise(void) {
   return FP8MOE_OK;
 }
 
+fp8moe_status fp8moe_testing_stall_next_quant_ring(void) {
+  fp8moe::arm_ring_stall_hook();
+  return FP8MOE_OK;
+}
+
 }  // extern "C"

@@ -57,6 +57,7 @@ struct CjArgs {
   uint8_t* q;
   float* inv;
   int* status;
+  int stall_test;  // CTA 0 never loads its first box (timeout-path test)
 };
 
 FP8MOE_DEV void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
@@ -138,8 +139,12 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
               live = false;
               break;
             }
-            mbar_expect_tx(&full[s], CJ_BOX_BYTES);
-            tma_load_2d(ring + s * CJ_BOX_BYTES, &tmX, &full[s], u.col0, (int)(u.gs + (int64_t)b * CJ_BOXR));
+            // test hook: CTA 0's first box is never loaded (but counted as
+            // issued), so its consumers' bounded wait runs out
+            if (!(a.stall_test && blockIdx.x == 0 && f == 0)) {
+              mbar_expect_tx(&full[s], CJ_BOX_BYTES);
+              tma_load_2d(ring + s * CJ_BOX_BYTES, &tmX, &full[s], u.col0, (int)(u.gs + (int64_t)b * CJ_BOXR));
+            }
             // publish the fill (after the release of fill f - CJ_NS that it waited for)
             __threadfence_block();
             *reinterpret_cast<volatile uint32_t*>(&issued_s) = f + 1;
@@ -325,6 +330,7 @@ cudaError_t launch_colwise_jagged_ws(const void* x, int64_t E, int64_t R, int64_
   a.q = (uint8_t*)q;
   a.inv = inv;
   a.status = status;
+  a.stall_test = take_ring_stall_hook();
   CUtensorMap tm;
   cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(R > 0 ? R : 1)};
   cuuint64_t strides[1] = {(cuuint64_t)(C * 2)};

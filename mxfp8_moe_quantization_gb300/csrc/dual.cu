@@ -82,6 +82,7 @@ struct DualArgs {
   ScaleSpec s0;         // [B, R, C/32] in its layout
   ScaleSpec s1;         // [B, C, R/32] in its layout
   int* status;
+  int stall_test;       // warp-specialised form: CTA 0 never loads its first sub-tile (timeout-path test)
 };
 
 constexpr uint32_t FULL = 0xffffffffu;
@@ -468,6 +469,9 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
             shift1_s[s] = gt1.pad[pg1] - gs / 32;
           }
           const int row = (int)(b * a.R + r);
+          // test hook: CTA 0's first sub-tile is never loaded, so its
+          // consumers' bounded wait runs out
+          if (a.stall_test && blockIdx.x == 0 && k == 0) continue;
           // (the arrive below releases the shifts to the consumers' wait)
           mbar_expect_tx(&full[s], WS_SUB_BYTES);
           tma_load_2d(ring + s * WS_SUB_BYTES, &tx, &full[s], (int)(ct * 128), row);
@@ -614,6 +618,13 @@ __global__ void __launch_bounds__(ws_threads<D0>(), 3) k_mx_dual_ws(const __grid
 
 }  // namespace
 
+// One-shot test hook of the warp-specialised quantizers (this file and the
+// jagged colwise kernel): armed by fp8moe_testing_stall_next_quant_ring,
+// consumed by the next such launch.
+static std::atomic<int> g_ring_stall{0};
+void arm_ring_stall_hook() { g_ring_stall.store(1, std::memory_order_relaxed); }
+int take_ring_stall_hook() { return g_ring_stall.exchange(0, std::memory_order_relaxed); }
+
 cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void* q0, uint8_t* s0, int s0_layout,
                            void* q1, uint8_t* s1, int s1_layout, const int32_t* offs, int64_t E, int num_sms,
                            int* status, cudaStream_t st) {
@@ -668,6 +679,7 @@ cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void*
     a.s0 = make_spec(s0, both ? s0_layout : FP8MOE_SCALES_ROWMAJOR, R, C / 32, offs, E);
     a.s1 = make_spec(s1, s1_layout, C, R / 32, offs, E);
     a.status = status;
+    a.stall_test = take_ring_stall_hook();
     CUtensorMap tx;
     memset(&tx, 0, sizeof(tx));
     const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(B * R)};
@@ -696,6 +708,7 @@ cudaError_t launch_mx_dual(const void* x, int64_t B, int64_t R, int64_t C, void*
   a.s0 = make_spec(s0, s0_layout, R, C / 32, offs, E);
   a.s1 = make_spec(s1, s1_layout, C, R / 32, offs, E);
   a.status = status;
+  a.stall_test = 0;
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
     cudaFuncSetAttribute(k_mx_dual<true, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DUAL_SMEM);

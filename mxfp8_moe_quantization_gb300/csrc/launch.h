@@ -99,6 +99,11 @@ void arm_gemm_stall_hook();
 // arms the one-shot stall of the next one-launch tensorwise kernel (its
 // grid-wide meeting; timeout-path test)
 void arm_tensorwise_stall_hook();
+// arms the one-shot stall of the next warp-specialised quantization launch
+// (dual-direction MXFP8 or jagged colwise: its first CTA never loads its
+// first tile); take_ring_stall_hook reads and clears it at launch
+void arm_ring_stall_hook();
+int take_ring_stall_hook();
 // blockwise-scaled grouped GEMM (blockwise_mm.cu)
 cudaError_t launch_blockwise_mm(const GemmArgs& g, cudaStream_t st);
 

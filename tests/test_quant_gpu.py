@@ -477,3 +477,50 @@ def test_mx_dual_load_forms(prefetch):
                        capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+# ----------------------------------------------------------------------------
+# timeout path of the warp-specialised quantizers (no GPU fault: a load that
+# is never issued)
+# ----------------------------------------------------------------------------
+
+def test_quant_ring_timeout_dual(F):
+    """The one-shot testing hook makes the first CTA of the next
+    warp-specialised dual-direction launch never load its first sub-tile:
+    that CTA's consumer warps' bounded wait (2 s) runs out, the launch
+    reports FP8MOE_ERR_TIMEOUT, its producer still waits for the loads it
+    issued, and the next call (the hook is spent) is exact."""
+    import os
+    if os.environ.get("FP8MOE_DUAL_WS"):
+        pytest.skip("this process fixes the dual kernel form")
+    x = _bf16((256, 512), 91, 1.0)
+    F.fp8moe_testing_stall_next_quant_ring()
+    F.fp8moe_mxfp8_quantize_dual(x.to(DEV), None, F.SCALES_ROWMAJOR, F.SCALES_ROWMAJOR)
+    assert F.fp8moe_get_device_status() == 6          # FP8MOE_ERR_TIMEOUT
+    q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), None, F.SCALES_ROWMAJOR, F.SCALES_ROWMAJOR)
+    assert F.fp8moe_get_device_status() == 0
+    r0, rs0, r1, rs1 = _mx_ref(_np(x))
+    assert np.array_equal(q0.cpu().numpy(), r0) and np.array_equal(s0.cpu().numpy(), rs0)
+    assert np.array_equal(q1.cpu().numpy(), r1) and np.array_equal(s1.cpu().numpy(), rs1)
+
+
+def test_quant_ring_timeout_jagged(F):
+    """The same hook on the routed-rows transposed colwise kernel: the first
+    CTA's first box is counted as issued but never loaded, so the consumer
+    group waiting for it runs out (2 s) while the other group and the other
+    CTAs carry on; FP8MOE_ERR_TIMEOUT, then an exact call."""
+    import os
+    if os.environ.get("FP8MOE_CW_JAGGED"):
+        pytest.skip("this process fixes the jagged colwise kernel")
+    sizes = [96, 0, 320, 32, 160]
+    offs = W.offsets_from_sizes(sizes)
+    x = _bf16((int(sum(sizes)), 192), 17, 0.5)
+    ot = torch.from_numpy(offs).to(DEV)
+    F.fp8moe_testing_stall_next_quant_ring()
+    F.fp8moe_quantize_colwise_3d(x.to(DEV), ot, True, 0)
+    assert F.fp8moe_get_device_status() == 6          # FP8MOE_ERR_TIMEOUT
+    q, inv = F.fp8moe_quantize_colwise_3d(x.to(DEV), ot, True, 0)
+    assert F.fp8moe_get_device_status() == 0
+    rq, rinv = OQ.quantize_colwise_jagged(_np(x), offs, OF.FN, transpose_out=True)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+    assert np.array_equal(q.cpu().numpy(), rq)
