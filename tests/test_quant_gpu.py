@@ -388,12 +388,15 @@ def test_mx_dual_mixed_layouts(F, l0, l1):
     assert F.fp8moe_get_device_status() == 0
 
 
-def test_mx_dual_unaligned_row_groups(F):
+@pytest.mark.parametrize("C", [96, 256])
+def test_mx_dual_unaligned_row_groups(F, C):
     """dim0 scales grouped by rows whose groups start off 16-row boundaries
-    (allowed when dim1's scales are not grouped)."""
+    (allowed when dim1's scales are not grouped); 256 columns take the
+    warp-specialised kernel, where a 32-row sub-tile that holds two groups
+    gives each row its own group."""
     sizes = [40, 0, 200, 8, 72]          # sums to 320
     offs = W.offsets_from_sizes(sizes)
-    x = _bf16((320, 96), 41, 1.0)
+    x = _bf16((320, C), 41, 1.0)
     q0, s0, q1, s1 = F.fp8moe_mxfp8_quantize_dual(x.to(DEV), torch.from_numpy(offs).to(DEV), F.GROUP_ROWS,
                                                   F.SCALES_ROWMAJOR)
     r0, rs0, r1, rs1 = _mx_ref(_np(x))
