@@ -285,6 +285,10 @@ def test_swizzle_bad_offsets_set_status(F):
     assert F.fp8moe_get_device_status() == 5
     F.fp8moe_swizzle_scales_128x4(s, torch.tensor([40, 64], dtype=torch.int32, device=DEV), F.GROUP_COLS)
     assert F.fp8moe_get_device_status() == 5     # 40 is not a multiple of 32
+    # rows of whole 16-byte chunks: the bulk-copy kernel
+    s32 = torch.ones(64, 32, dtype=torch.uint8, device=DEV)
+    F.fp8moe_swizzle_scales_128x4(s32, torch.tensor([40, 30, 64], dtype=torch.int32, device=DEV), F.GROUP_ROWS)
+    assert F.fp8moe_get_device_status() == 5
     assert F.fp8moe_get_device_status() == 0
 
 
