@@ -279,7 +279,9 @@ def run_e2e(F, sets, steps, warmup, stream_weights=False):
     the last download has landed (one copy stream per direction: spreading
     the transfers over four streams each way measured slower).  Before the
     steps, the same buffers' copies are timed alone and both ways at once
-    (``host_link``): their rates and the per-step floor they set."""
+    (``host_link``): their rates and the per-step floor they set; inside the
+    timed steps, the mean duration of each step's uploads, compute and
+    downloads (``host_link.in_loop_ms_per_step``)."""
     import torch
     host_in, host_out = [], []
     for st in sets:
@@ -342,33 +344,58 @@ def run_e2e(F, sets, steps, warmup, stream_weights=False):
     ev_comp = [torch.cuda.Event() for _ in range(ns)]
     ev_out = [torch.cuda.Event() for _ in range(ns)]
 
-    def one(i):
+    # per timed step: start / end events of its uploads, compute and downloads
+    # (each on its own stream), to tell in the report whether the copies ran
+    # at the link's rate inside the loop
+    marks = []
+
+    def one(i, mark=False):
         k = i % ns
+        m = [torch.cuda.Event(enable_timing=True) for _ in range(6)] if mark else None
         with torch.cuda.stream(s_in):
             if i >= ns:
                 s_in.wait_event(ev_comp[k])   # the set's previous step has read its inputs
+            if m:
+                m[0].record(s_in)
             for d, h in host_in[k]:
                 d.copy_(h, non_blocking=True)
+            if m:
+                m[1].record(s_in)
             ev_in[k].record(s_in)
         comp.wait_event(ev_in[k])
         if i >= ns:
             comp.wait_event(ev_out[k])        # the set's previous results have been copied out
+        if m:
+            m[2].record(comp)
         sets[k].run()
+        if m:
+            m[3].record(comp)
         ev_comp[k].record(comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[k])
+            if m:
+                m[4].record(s_out)
             for d, h in host_out[k]:
                 h.copy_(d, non_blocking=True)
+            if m:
+                m[5].record(s_out)
             ev_out[k].record(s_out)
+        if m:
+            marks.append(m)
 
     for i in range(warmup):
         one(i)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
-        one(warmup + i)
+        one(warmup + i, mark=True)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
+    n = len(marks)
+    link["in_loop_ms_per_step"] = {
+        "h2d": sum(m[0].elapsed_time(m[1]) for m in marks) / n,
+        "compute": sum(m[2].elapsed_time(m[3]) for m in marks) / n,
+        "d2h": sum(m[4].elapsed_time(m[5]) for m in marks) / n}
     return dt, h2d, d2h, link
 
 
