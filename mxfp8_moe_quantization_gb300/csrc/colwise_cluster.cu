@@ -39,6 +39,7 @@ constexpr int CC_COLS = 64;                          // columns of a unit: 128 b
 constexpr int CC_BOXR = 128;                         // rows of one TMA box
 constexpr int CC_BOX_BYTES = CC_BOXR * CC_COLS * 2;  // 16 KB
 constexpr int CC_NB_MAX = 6;                         // box slots of the larger ring: 96 KB, two CTAs per SM
+constexpr int CC_STREAM_SLACK = 2;                    // boxes of a slice past the ring worth a smaller cluster
 constexpr int CC_THREADS = 256;
 
 struct CcArgs {
@@ -594,16 +595,19 @@ bool colwise_cluster_supported(int64_t E, int64_t R, int64_t C) {
 
 cudaError_t launch_colwise_cluster(const void* x, int64_t E, int64_t R, int64_t C, int kind, void* q, float* inv,
                                    int* status, int num_sms, cudaStream_t st) {
-  // the smallest cluster whose CTAs' slices fit the ring (measured: every
+  // the smallest cluster whose CTAs' slices hold at most CC_STREAM_SLACK
+  // boxes more than the ring (those few come back through it from L2),
+  // the largest one when none does (its CTAs then stream their slices
+  // through the ring); with room for two slices, the next unit's boxes load
+  // during the cast.  Measured over eleven expert-weight shapes: every
   // doubling of the cluster costs more in per-unit waiting for the slowest
-  // CTA than it saves), the largest one when none does (its CTAs then stream
-  // their slices through the ring); with room for two slices, the next
-  // unit's boxes load during the cast
+  // CTA than it saves, except where it takes a slice from more than
+  // CC_STREAM_SLACK boxes over the ring down to that or fewer
   auto rows_per_cta = [&](int cl) { return (((R + cl - 1) / cl) + 31) / 32 * 32; };
   auto boxes_of = [&](int cl) { return (rows_per_cta(cl) + CC_BOXR - 1) / CC_BOXR; };
   int CL = 0;
   for (int cl = 1; cl <= 8 && !CL; cl *= 2)
-    if (boxes_of(cl) <= CC_NB_MAX) CL = cl;
+    if (boxes_of(cl) <= CC_NB_MAX + CC_STREAM_SLACK) CL = cl;
   if (!CL) CL = 8;
   const bool pre = 2 * boxes_of(CL) <= CC_NB_MAX;
   CcArgs a;
