@@ -51,7 +51,8 @@ typedef enum {
   FP8MOE_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
   FP8MOE_ERR_DEVICE_OFFSETS = 5,  /* device: offsets invalid (read via get_device_status) */
   FP8MOE_ERR_TIMEOUT = 6,         /* device: a bounded pipeline wait ran out */
-  FP8MOE_ERR_SCRATCH_LIMIT = 7    /* host: the problem needs more than the static scratch */
+  FP8MOE_ERR_SCRATCH_LIMIT = 7,   /* host: the problem needs more than the static scratch */
+  FP8MOE_ERR_CONCURRENT = 8       /* device: launches in flight at once shared a work counter */
 } fp8moe_status;
 
 typedef enum {
@@ -109,9 +110,14 @@ fp8moe_status fp8moe_quantize_rowwise(const void* x, int64_t R, int64_t C, int64
  *   columns [P_e, P_e + g_e), P_e = sum_{j<e} round_up(g_j, 32), every
  *   other column 0; else [R, C].  1 <= E <= FP8MOE_MAX_GROUPS.
  * C % 16 == 0; dense transposed output also needs R % 16 == 0.
- * Transposed output (dense or jagged) runs as one pass over x in
- * thread-block clusters that exchange column maxima through distributed
- * shared memory, and writes scale_inv directly.  Untransposed output uses
+ * Transposed output runs as one pass over x and writes scale_inv directly:
+ * dense, in thread-block clusters that exchange column maxima through
+ * distributed shared memory; jagged, one CTA per group strip, the CTAs
+ * taking strips from a device work counter (one of 16 slots, chosen per
+ * launch in turn: 16 or more such launches in flight at once on different
+ * streams, or replays of one captured launch running concurrently, can
+ * meet in a slot, which sets FP8MOE_ERR_CONCURRENT in the device status and
+ * leaves the outputs invalid).  Untransposed output uses
  * scale_inv as the scratch of the column maxima during the call
  * (stream-ordered; it holds the scales when the call's work completes).
  * ------------------------------------------------------------------------ */
@@ -477,8 +483,10 @@ fp8moe_status fp8moe_testing_stall_next_tensorwise(void);
  * quantizers (no counterpart on the pages): fp8moe_mxfp8_quantize_dual with
  * both directions and at least 128 columns, and fp8moe_quantize_colwise_3d of
  * routed rows with transposed output.  Arms a one-shot flag: the next such
- * launch of the process has its first CTA never load its first tile, so that
- * CTA's consumer warps' bounded wait (2 s) runs out and the launch sets
+ * launch of the process never loads one tile (the dual quantizer: the first
+ * CTA's first tile; the routed-rows colwise kernel: the first tile of its
+ * first unit, whichever CTA takes it), so the consumer warps waiting for it
+ * run out of their bounded wait (2 s) and the launch sets
  * FP8MOE_ERR_TIMEOUT (its outputs are then not valid).  The CTA's producer
  * still waits (bounded) for the loads it issued, so no copy is in flight when
  * it exits and the context stays usable.

@@ -67,6 +67,7 @@ const char* fp8moe_status_string(int s) {
     case FP8MOE_ERR_DEVICE_OFFSETS: return "invalid routing offsets (device)";
     case FP8MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
     case FP8MOE_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the library's static array holds";
+    case FP8MOE_ERR_CONCURRENT: return "launches in flight at once shared a device work counter";
     default: return "unknown status";
   }
 }

@@ -10,8 +10,10 @@
 // multiple of 32 and the slack after the last group zero), scale_inv [E, C].
 //
 // A unit is one group's 64-column strip.  One persistent CTA per SM takes
-// its units (largest groups first, in a snake order over the CTAs so that
-// their loads even out) one after another:
+// units one after another from a device-wide counter over the units ordered
+// largest group first, so that the CTAs finish together whatever the group
+// sizes (a fixed assignment, e.g. a snake order over the CTAs, left the
+// slowest CTA ~20% above the mean on a skewed routing):
 //   * a producer warp streams the units' TMA boxes (128 rows x 64 columns,
 //     128-byte swizzle, 16 KB) through a ring of CJ_NS slots, running ahead
 //     into the next units while slots are free;
@@ -47,6 +49,19 @@ constexpr int CJ_CONS = 16;                          // consumer warps
 constexpr int CJ_GW = CJ_CONS / 2;                   // warps of each of the two consumer groups
 constexpr int CJ_THREADS = 32 * (CJ_CONS + 1);
 constexpr size_t CJ_SMEM = (size_t)CJ_NS * CJ_BOX_BYTES + 1024;   // + room to align the ring to 1 KB
+constexpr int CJ_UQ = 32;                            // entries of the producer's unit queue
+constexpr int CJ_SLOTS = 16;                         // work-counter slots, one per launch in flight
+
+// The work counters.  A launch with generation `gen` (a per-process launch
+// count, never 0) uses slot gen % CJ_SLOTS: word = gen << 32 | units taken.
+// Every CTA first raises the word to gen << 32 (a no-op once another CTA of
+// the launch has), then takes units with atomicAdd; a word whose top half
+// is not `gen` means that another launch in flight holds the slot, which
+// the launch reports as FP8MOE_ERR_CONCURRENT.  The `done` word counts the
+// CTAs that have finished taking units; the last one returns both words to
+// zero, so a replay of the same launch (a CUDA graph) starts clean.
+__device__ unsigned long long g_cj_work[CJ_SLOTS];
+__device__ unsigned long long g_cj_done[CJ_SLOTS];
 
 struct CjArgs {
   int64_t E, R, C;
@@ -57,7 +72,15 @@ struct CjArgs {
   uint8_t* q;
   float* inv;
   int* status;
-  int stall_test;  // CTA 0 never loads its first box (timeout-path test)
+  int stall_test;  // the first box of unit 0 is never loaded (timeout-path test)
+  uint32_t gen;    // launch generation (work-counter tag), slot = gen % CJ_SLOTS
+};
+
+// A unit queue entry: the unit's index in the size-ordered list (-1: no
+// more units, -2: the launch stopped) and the fill of its first box.
+struct CjEntry {
+  long long u;
+  uint32_t f0;
 };
 
 FP8MOE_DEV void mbar_arrive_cnt(uint64_t* bar, uint32_t n) {
@@ -73,6 +96,10 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
   __shared__ float scol[2][CJ_COLS];
   __shared__ int abort_s;
   __shared__ uint32_t issued_s;   // fills the producer has issued
+  __shared__ CjEntry uq[CJ_UQ];   // units in the order the producer took them
+  __shared__ int nq_s;            // entries published
+  __shared__ int read_s[2];       // per consumer group: 1 + the last entry it took
+  __shared__ CjEntry ubc[2];      // per consumer group: the entry its elected thread took
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -96,19 +123,18 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
     }
     abort_s = 0;
     issued_s = 0;
+    nq_s = 0;
+    read_s[0] = read_s[1] = 0;
     mbar_fence_init();
   }
   __syncthreads();
 
-  // the CTA's kk-th unit (snake order over the size-ordered units)
+  // unit u of the size-ordered list: group order[u / n_ct], strip u % n_ct
   struct U {
     int64_t g, gs, rg, rpad, qcol0;
     int col0, nbox;
   };
-  auto unit = [&](int64_t kk, U& o) -> bool {
-    const int64_t G = gridDim.x, cid = blockIdx.x;
-    const int64_t u = kk * G + ((kk & 1) ? G - 1 - cid : cid);
-    if (u >= a.units) return false;
+  auto unit_of = [&](int64_t u, U& o) {
     const int64_t gi = u / a.n_ct;
     o.col0 = (int)((u - gi * a.n_ct) * CJ_COLS);
     o.g = order[gi];
@@ -117,31 +143,72 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
     o.rpad = (o.rg + 31) / 32 * 32;
     o.qcol0 = 32 * gt.pad[o.g];
     o.nbox = (int)((o.rg + CJ_BOXR - 1) / CJ_BOXR);
-    return true;
   };
-  const int64_t rounds = (a.units + gridDim.x - 1) / gridDim.x;
 
   if (warp == CJ_CONS) {
     // ======================= producer =======================
     if (lane == 0) {
+      unsigned long long* wk = &g_cj_work[a.gen % CJ_SLOTS];
+      unsigned long long* dn = &g_cj_done[a.gen % CJ_SLOTS];
+      const unsigned long long tag = (unsigned long long)a.gen << 32;
+      atomicMax(wk, tag);
+      atomicMax(dn, tag);
+      // the next unit's index: taken one unit ahead, so that the atomic's
+      // round trip overlaps the issue of the current unit's boxes
+      unsigned long long taken = atomicAdd(wk, 1ull);
       uint32_t f = 0;   // boxes issued so far (fill f goes to slot f % CJ_NS)
       bool live = true;
-      for (int64_t kk = 0; kk < rounds && live; ++kk) {
+      auto stop = [&](int code) {
+        if (!abort_s) set_status(a.status, code);
+        abort_s = 1;
+        live = false;
+      };
+      // room for entry n: entry n - CJ_UQ has been taken by its group
+      auto room = [&](int n) -> bool {
+        if (n < CJ_UQ) return true;
+        const volatile int* rd = &read_s[(n - CJ_UQ) & 1];
+        const uint64_t t0 = globaltimer();
+        while (*rd <= n - CJ_UQ) {
+          if (abort_s || globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+        }
+        return true;
+      };
+      auto publish = [&](int n, long long u) {
+        volatile CjEntry* e = &uq[n % CJ_UQ];
+        e->u = u;
+        e->f0 = f;
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&nq_s) = n + 1;
+      };
+      int n = 0;
+      for (; live; ++n) {
+        long long k;
+        if ((taken >> 32) != a.gen) {
+          stop(FP8MOE_ERR_CONCURRENT);
+          break;
+        }
+        k = (long long)(taken & 0xFFFFFFFFull);
+        if (k >= a.units) break;
+        taken = atomicAdd(wk, 1ull);
+        if (!room(n)) {
+          stop(FP8MOE_ERR_TIMEOUT);
+          break;
+        }
         U u;
-        if (!unit(kk, u)) continue;
+        unit_of(k, u);
+        publish(n, k);
         const int passes = u.nbox <= CJ_NS ? 1 : 2;
         for (int p = 0; p < passes && live; ++p)
           for (int b = 0; b < u.nbox; ++b, ++f) {
             const uint32_t s = f % CJ_NS;
             if (f >= CJ_NS && !mbar_wait(&empty[s], ((f / CJ_NS) - 1) & 1u, &abort_s)) {
-              if (!abort_s) set_status(a.status, FP8MOE_ERR_TIMEOUT);
-              abort_s = 1;
-              live = false;
+              stop(FP8MOE_ERR_TIMEOUT);
               break;
             }
-            // test hook: CTA 0's first box is never loaded (but counted as
-            // issued), so its consumers' bounded wait runs out
-            if (!(a.stall_test && blockIdx.x == 0 && f == 0)) {
+            // test hook: the first box of unit 0 (whichever CTA takes it) is
+            // never loaded (but counted as issued), so its consumers'
+            // bounded wait runs out
+            if (!(a.stall_test && k == 0 && p == 0 && b == 0)) {
               mbar_expect_tx(&full[s], CJ_BOX_BYTES);
               tma_load_2d(ring + s * CJ_BOX_BYTES, &tmX, &full[s], u.col0, (int)(u.gs + (int64_t)b * CJ_BOXR));
             }
@@ -150,10 +217,24 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
             *reinterpret_cast<volatile uint32_t*>(&issued_s) = f + 1;
           }
       }
+      // no more units: one end entry for each group (after a stop the
+      // consumers leave on abort_s instead)
+      for (int e = 0; e < 2 && live; ++e) {
+        if (room(n + e))
+          publish(n + e, -1);
+        else
+          stop(FP8MOE_ERR_TIMEOUT);
+      }
       // the loads still in flight land before the CTA can leave (the
       // consumers may have stopped early): the last fill of each slot
       for (uint32_t j = f > CJ_NS ? f - CJ_NS : 0; j < f; ++j)
         (void)mbar_wait(&full[j % CJ_NS], (j / CJ_NS) & 1u, nullptr);
+      // the last CTA to finish taking units clears the slot
+      const unsigned long long d = atomicAdd(dn, 1ull);
+      if ((d >> 32) == a.gen && (d & 0xFFFFFFFFull) == gridDim.x - 1) {
+        atomicExch(wk, 0ull);
+        atomicExch(dn, 0ull);
+      }
     }
     return;
   }
@@ -187,16 +268,51 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
     __threadfence_block();
     return mbar_wait(&full[fb % CJ_NS], (fb / CJ_NS) & 1u, &abort_s);
   };
-  uint32_t f = 0;   // fills of the units before this one (the producer's sequence)
-  int nu = 0;       // units before this one
+  // the group's elected thread takes queue entry n and hands it to the
+  // group (one decision for all its warps, so that they meet the same
+  // barriers)
+  auto take = [&](int n) -> CjEntry {
+    if (gw == 0 && lane == 0) {
+      CjEntry e;
+      e.u = -2;
+      e.f0 = 0;
+      const volatile int* nq = &nq_s;
+      const uint64_t t0 = globaltimer();
+      bool got = true;
+      while (*nq <= n) {
+        if (abort_s) {
+          got = false;
+          break;
+        }
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+          set_status(a.status, FP8MOE_ERR_TIMEOUT);
+          abort_s = 1;
+          got = false;
+          break;
+        }
+      }
+      if (got) {
+        __threadfence_block();
+        const volatile CjEntry* q = &uq[n % CJ_UQ];
+        e.u = q->u;
+        e.f0 = q->f0;
+        __threadfence_block();
+        *reinterpret_cast<volatile int*>(&read_s[grp]) = n + 1;
+      }
+      ubc[grp] = e;
+    }
+    group_sync();
+    return ubc[grp];
+  };
   bool ok = true;   // false after a wait ran out: the warps keep meeting their barriers, no more work
-  for (int64_t kk = 0; kk < rounds; ++kk) {
+  // entries alternate between the groups: group grp takes grp, grp + 2, ...
+  for (int n = grp;; n += 2) {
+    const CjEntry e = take(n);
+    if (e.u < 0) break;
     U u;
-    if (!unit(kk, u)) continue;
+    unit_of(e.u, u);
     const bool res = u.nbox <= CJ_NS;
-    const uint32_t f0 = f;
-    f += res ? u.nbox : 2 * u.nbox;
-    if ((nu++ & 1) != grp) continue;
+    const uint32_t f0 = e.f0;
     ok = ok && !abort_s;
     // ---- 1. column maxima, box by box as they land
     uint32_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
@@ -331,6 +447,12 @@ cudaError_t launch_colwise_jagged_ws(const void* x, int64_t E, int64_t R, int64_
   a.inv = inv;
   a.status = status;
   a.stall_test = take_ring_stall_hook();
+  // units + one end-of-work take per CTA must fit the counter's 32 bits
+  if (a.units + num_sms >= ((int64_t)1 << 32)) return cudaErrorInvalidValue;
+  static std::atomic<uint32_t> gen{0};
+  uint32_t g = gen.fetch_add(1, std::memory_order_relaxed) + 1;
+  while (g == 0) g = gen.fetch_add(1, std::memory_order_relaxed) + 1;
+  a.gen = g;
   CUtensorMap tm;
   cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(R > 0 ? R : 1)};
   cuuint64_t strides[1] = {(cuuint64_t)(C * 2)};

@@ -160,6 +160,59 @@ def test_colwise_jagged_cluster_form():
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
 
 
+def test_colwise_jagged_work_counter(F):
+    """The routed-rows transposed kernel takes its units from a device work
+    counter (one of 16 slots per launch, cleared by the launch's last CTA):
+    40 launches in a row (every slot reused), three replays of one captured
+    launch (the same slot and tag each time) and two launches in flight at
+    once on two streams all give the oracle's codes and scales."""
+    import os
+    if os.environ.get("FP8MOE_CW_JAGGED"):
+        pytest.skip("this process fixes the jagged colwise kernel")
+    sizes = [700, 0, 130, 2000, 33, 1, 0, 1600]
+    C = 320
+    M = sum(sizes)
+    x = _bf16((M, C), 91, 1.0)
+    offs = W.offsets_from_sizes(sizes)
+    rq, rinv = OQ.quantize_colwise_jagged(_np(x), offs, OF.FN, transpose_out=True)
+    xd, ot = x.to(DEV), torch.from_numpy(offs).to(DEV)
+
+    def same(q, inv):
+        return np.array_equal(q.cpu().numpy(), rq) and np.array_equal(inv.cpu().numpy(), rinv)
+
+    outs = [F.fp8moe_quantize_colwise_3d(xd, ot, True, 0) for _ in range(40)]
+    assert F.fp8moe_get_device_status() == 0
+    assert all(same(q, inv) for q, inv in outs)
+    qs, invs = outs[0][0].clone(), outs[0][1].clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        F.fp8moe_quantize_colwise_3d(xd, ot, True, 0, q=qs, scale_inv=invs)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        F.fp8moe_quantize_colwise_3d(xd, ot, True, 0, q=qs, scale_inv=invs)
+    for _ in range(3):
+        qs.zero_()
+        invs.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert same(qs, invs)
+    assert F.fp8moe_get_device_status() == 0
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    q1, i1 = torch.empty_like(qs), torch.empty_like(invs)
+    q2, i2 = torch.empty_like(qs), torch.empty_like(invs)
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        F.fp8moe_quantize_colwise_3d(xd, ot, True, 0, q=q1, scale_inv=i1)
+    with torch.cuda.stream(s2):
+        F.fp8moe_quantize_colwise_3d(xd, ot, True, 0, q=q2, scale_inv=i2)
+    torch.cuda.synchronize()
+    assert F.fp8moe_get_device_status() == 0
+    assert same(q1, i1) and same(q2, i2)
+
+
 def test_colwise_jagged_tiny_workload(F):
     wl = W.get_workload("tiny")
     offs = wl.offs()
@@ -513,9 +566,10 @@ def test_quant_ring_timeout_dual(F):
 
 def test_quant_ring_timeout_jagged(F):
     """The same hook on the routed-rows transposed colwise kernel: the first
-    CTA's first box is counted as issued but never loaded, so the consumer
-    group waiting for it runs out (2 s) while the other group and the other
-    CTAs carry on; FP8MOE_ERR_TIMEOUT, then an exact call."""
+    box of unit 0 (the largest group's first strip, whichever CTA takes it)
+    is counted as issued but never loaded, so the consumer group waiting for
+    it runs out (2 s) while the other group and the other CTAs carry on;
+    FP8MOE_ERR_TIMEOUT, then an exact call."""
     import os
     if os.environ.get("FP8MOE_CW_JAGGED"):
         pytest.skip("this process fixes the jagged colwise kernel")
