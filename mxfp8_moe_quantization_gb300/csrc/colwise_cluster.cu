@@ -360,9 +360,9 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
       continue;
     }
     // ---- 3. cast and transposed store
-    float sv[8];
+    uint64_t mul2[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) sv[t] = enc_mul<FNUZ>(scol[cl * 8 + t]);
+    for (int t = 0; t < 8; ++t) mul2[t] = pair_f32(enc_mul<FNUZ>(scol[cl * 8 + t]));
     const int64_t col = col0 + cl * 8;
     // one 32-row x 64-column sub-tile: local row lr0 (a multiple of 8) of
     // this lane, held in the slot at `box`
@@ -370,30 +370,26 @@ __global__ void __launch_bounds__(CC_THREADS, 2) k_cw_cluster(const __grid_const
       // dense: R % 8 == 0, so a lane's 8 rows are all in or all out; jagged:
       // rows from nr to npad are the group's padding (zero codes)
       if (lr0 >= npad || col >= a.C) return;
-      uint32_t w0[8], w1[8];
+      uint4 v[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int r = (lr0 + k) & 127;
-        const uint4 v = *reinterpret_cast<const uint4*>(box + r * 128 + ((cl ^ (r & 7)) << 4));
-        w0[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v.x), sv[0]), __fmul_rn(bf16_hi(v.x), sv[1]),
-                           __fmul_rn(bf16_lo(v.y), sv[2]), __fmul_rn(bf16_hi(v.y), sv[3]));
-        w1[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
-                           __fmul_rn(bf16_lo(v.w), sv[6]), __fmul_rn(bf16_hi(v.w), sv[7]));
-        if (JAG && lr0 + k >= nr) w0[k] = w1[k] = 0u;
+        v[k] = *reinterpret_cast<const uint4*>(box + r * 128 + ((cl ^ (r & 7)) << 4));
+      }
+      uint2 cw[8];
+      cast8x8_cols<FNUZ>(v, mul2, cw);
+      if (JAG && nr - lr0 < 8) {
+        const int nv = nr - lr0;
+        const uint64_t keep = nv <= 0 ? 0ull : (1ull << (8 * nv)) - 1;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) cw[t] = make_uint2(cw[t].x & (uint32_t)keep, cw[t].y & (uint32_t)(keep >> 32));
       }
       // q[g][col + t][row .. row + 7] (jagged: q[col + t][group column + row])
       // for the 8 columns t
       const int64_t pitch = JAG ? a.ldt : a.R;
       uint8_t* base = JAG ? a.q + col * a.ldt + qcol0 + r0 + lr0 : a.q + (g * a.C + col) * a.R + r0 + lr0;
-      uint32_t q0[4], q1[4];
-      transpose4x4(w0[0], w0[1], w0[2], w0[3], q0);
-      transpose4x4(w0[4], w0[5], w0[6], w0[7], q1);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)t * pitch) = make_uint2(q0[t], q1[t]);
-      transpose4x4(w1[0], w1[1], w1[2], w1[3], q0);
-      transpose4x4(w1[4], w1[5], w1[6], w1[7], q1);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)(4 + t) * pitch) = make_uint2(q0[t], q1[t]);
+      for (int t = 0; t < 8; ++t) *reinterpret_cast<uint2*>(base + (int64_t)t * pitch) = cw[t];
     };
     // the boxes still resident after the maxima pass (the last CC_NB)
     const int first = nbox > CC_NB ? nbox - CC_NB : 0;

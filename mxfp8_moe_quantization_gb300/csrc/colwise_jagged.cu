@@ -372,9 +372,9 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
     // ---- 3. cast and transposed store: the unit's 32-row quarters of its
     // boxes over the group's warps (a box's four quarters on four warps,
     // which then release its slot together)
-    float sv[8];
+    uint64_t mul2[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) sv[t] = enc_mul<FNUZ>(scol[grp][cl * 8 + t]);
+    for (int t = 0; t < 8; ++t) mul2[t] = pair_f32(enc_mul<FNUZ>(scol[grp][cl * 8 + t]));
     const int64_t col = u.col0 + cl * 8;
     for (int i = gw; i < 4 * u.nbox && ok; i += CJ_GW) {
       const int b = i >> 2;
@@ -388,29 +388,25 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
       const uint8_t* box = ring + s * CJ_BOX_BYTES;
       const int64_t lr0 = (int64_t)b * CJ_BOXR + (i & 3) * 32 + rq * 8;   // this lane's first row in the group
       if (lr0 < u.rpad && col < a.C) {
-        uint32_t w0[8], w1[8];
+        uint4 v[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int r = (int)((lr0 + k) & 127);
-          const uint4 v = *reinterpret_cast<const uint4*>(box + r * 128 + ((cl ^ (r & 7)) << 4));
-          w0[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v.x), sv[0]), __fmul_rn(bf16_hi(v.x), sv[1]),
-                                 __fmul_rn(bf16_lo(v.y), sv[2]), __fmul_rn(bf16_hi(v.y), sv[3]));
-          w1[k] = enc4_pre<FNUZ>(__fmul_rn(bf16_lo(v.z), sv[4]), __fmul_rn(bf16_hi(v.z), sv[5]),
-                                 __fmul_rn(bf16_lo(v.w), sv[6]), __fmul_rn(bf16_hi(v.w), sv[7]));
-          if (lr0 + k >= u.rg) w0[k] = w1[k] = 0u;   // the group's padding rows
+          v[k] = *reinterpret_cast<const uint4*>(box + r * 128 + ((cl ^ (r & 7)) << 4));
+        }
+        uint2 cw[8];
+        cast8x8_cols<FNUZ>(v, mul2, cw);
+        // the group's padding rows (from rg to the next multiple of 32) get zero codes
+        const int64_t nv = u.rg - lr0;
+        if (nv < 8) {
+          const uint64_t keep = nv <= 0 ? 0ull : (1ull << (8 * nv)) - 1;
+#pragma unroll
+          for (int t = 0; t < 8; ++t) cw[t] = make_uint2(cw[t].x & (uint32_t)keep, cw[t].y & (uint32_t)(keep >> 32));
         }
         // q[col + t][group column + row] for the 8 columns t
         uint8_t* base = a.q + col * a.ldt + u.qcol0 + lr0;
-        uint32_t q0[4], q1[4];
-        transpose4x4(w0[0], w0[1], w0[2], w0[3], q0);
-        transpose4x4(w0[4], w0[5], w0[6], w0[7], q1);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) *reinterpret_cast<uint2*>(base + (int64_t)t * a.ldt) = make_uint2(q0[t], q1[t]);
-        transpose4x4(w1[0], w1[1], w1[2], w1[3], q0);
-        transpose4x4(w1[4], w1[5], w1[6], w1[7], q1);
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          *reinterpret_cast<uint2*>(base + (int64_t)(4 + t) * a.ldt) = make_uint2(q0[t], q1[t]);
+        for (int t = 0; t < 8; ++t) *reinterpret_cast<uint2*>(base + (int64_t)t * a.ldt) = cw[t];
       }
       // the box's slot: four warps x (CJ_GW / 4) arrivals
       __syncwarp();

@@ -155,6 +155,47 @@ FP8MOE_DEV uint4 ld_nc16(const void* p) {
   return v;
 }
 
+// (m, m) in one 64-bit register pair: the second operand of fmul2_rn
+FP8MOE_DEV uint64_t pair_f32(float m) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(m));
+  return r;
+}
+
+// x = a * m, y = b * m with (m, m) = m2: the packed fp32 multiply of sm_100
+// and later (two IEEE products, round to nearest even, subnormals kept:
+// bit-identical to two __fmul_rn)
+FP8MOE_DEV void fmul2_rn(float a, float b, uint64_t m2, float& x, float& y) {
+  asm("{\n .reg .b64 p, r;\n mov.b64 p, {%2, %3};\n mul.rn.f32x2 r, p, %4;\n mov.b64 {%0, %1}, r;\n}"
+      : "=f"(x), "=f"(y)
+      : "f"(a), "f"(b), "l"(m2));
+}
+
+// The codes of an 8-row x 8-column bf16 block scaled per column, column by
+// column: v[k] holds row k (columns 0..7 as bf16 pairs), m2[c] the pair
+// (enc_mul(s_c), enc_mul(s_c)), and col[c] receives column c's eight codes
+// with row k in byte k.  Each product pair and each packed conversion takes
+// one column from neighbouring rows, so the codes come out already in
+// column order: no byte transposes.
+template <bool FNUZ>
+FP8MOE_DEV void cast8x8_cols(const uint4 (&v)[8], const uint64_t (&m2)[8], uint2 (&col)[8]) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = w == 0 ? v[k].x : w == 1 ? v[k].y : w == 2 ? v[k].z : v[k].w;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float p[8];
+#pragma unroll
+      for (int k = 0; k < 8; k += 2)
+        fmul2_rn(h ? bf16_hi(x[k]) : bf16_lo(x[k]), h ? bf16_hi(x[k + 1]) : bf16_lo(x[k + 1]), m2[2 * w + h], p[k],
+                 p[k + 1]);
+      col[2 * w + h] = make_uint2(enc4_pre<FNUZ>(p[0], p[1], p[2], p[3]), enc4_pre<FNUZ>(p[4], p[5], p[6], p[7]));
+    }
+  }
+}
+
 // Column t (0..3) of four row words (byte t of each) as one word, rows in
 // byte order: a 4x4 byte transpose.
 FP8MOE_DEV void transpose4x4(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3, uint32_t (&col)[4]) {
