@@ -160,6 +160,30 @@ def test_colwise_jagged_cluster_form():
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
 
 
+@pytest.mark.parametrize("E", [640, 700])
+def test_colwise_jagged_many_groups(F, E):
+    """Hundreds of routed groups, most of them a fraction of a TMA box, with
+    empty and one-row groups among them and one group longer than the ring:
+    the transposed kernel's per-group tables, size order and padding."""
+    import os
+    if os.environ.get("FP8MOE_CW_JAGGED"):
+        pytest.skip("this process fixes the jagged colwise kernel")
+    rng = np.random.default_rng(E)
+    sizes = rng.integers(0, 60, size=E)
+    sizes[::7] = 0
+    sizes[3::11] = 1
+    sizes[5] = 1500
+    C = 64
+    M = int(sizes.sum())
+    x = _bf16((M, C), E, 1.0)
+    offs = W.offsets_from_sizes([int(v) for v in sizes])
+    q, inv = F.fp8moe_quantize_colwise_3d(x.to(DEV), torch.from_numpy(offs).to(DEV), True, 0)
+    assert F.fp8moe_get_device_status() == 0
+    rq, rinv = OQ.quantize_colwise_jagged(_np(x), offs, OF.FN, transpose_out=True)
+    assert np.array_equal(inv.cpu().numpy(), rinv)
+    assert np.array_equal(q.cpu().numpy(), rq)
+
+
 def test_colwise_jagged_work_counter(F):
     """The routed-rows transposed kernel takes its units from a device work
     counter (one of 16 slots per launch, cleared by the launch's last CTA):
