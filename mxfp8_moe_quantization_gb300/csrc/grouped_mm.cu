@@ -98,8 +98,10 @@ struct SmemLayout {
   // 3 per stage + 6, and for QA: afull per stage, abf_full / abf_empty per slot
   static constexpr int NBARS = 3 * STAGES + 6 + (QA ? STAGES + 2 * QS : 0);
   static constexpr int misc = bars + NBARS * 8;                 // tmem addr, abort, counts
-  static constexpr int colscale = misc + 64;                    // 256 floats
-  static constexpr int tiles_prefix = colscale + BN * 4;        // MAXG + 1 ints
+  // column scales (rowwise / tensorwise): fwd / dgrad one shared buffer of
+  // BN floats; wgrad two buffers of EC floats per epilogue warp
+  static constexpr int colscale = misc + 64;
+  static constexpr int tiles_prefix = colscale + (WG ? NEPI * 2 * EC : BN) * 4;   // MAXG + 1 ints
   static constexpr int blk_prefix = tiles_prefix + (MAXG + 1) * 4;
   static constexpr int offs = blk_prefix + (MAXG + 1) * 4;      // MAXG + 1 ints: group bounds
   // per epilogue warp STG_DEPTH 32-row x 64-byte staging tiles (64-byte swizzle)
@@ -769,6 +771,34 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
       }
     };
     int cur_e = 0;
+    // wgrad, rowwise / tensorwise: its tiles are short in K, so a tile's
+    // scales are loaded into registers one tile ahead (their global round
+    // trip overlaps the previous tile's drain and stores) and staged at the
+    // tile's start into one of the warp's own two buffers (the scales of its
+    // EC columns): no epilogue warp waits for another
+    constexpr int CPL = EC / 32;   // column scales per lane
+    float cs_pre[CPL];
+    float rs_pre = 1.0f;
+    int pre_e = 0;   // the look-ahead's group cursor
+    int sbuf = 0;
+    auto load_scales = [&](int tt) {
+      const Tile tn = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, bounds, tt, rank, pre_e);
+      const bool tw = g.recipe == FP8MOE_TENSORWISE;
+      const int64_t nc = (g.cols - tn.col0) < BN ? (g.cols - tn.col0) : BN;
+      const float* cs = (const float*)g.b_scale + (tw ? 0 : (int64_t)tn.e * g.cols + tn.col0);
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int c = c_lo + lane + 32 * i;
+        cs_pre[i] = c < nc ? cs[tw ? 0 : c] : 0.0f;
+      }
+      const int64_t lr = quarter * 32 + lane;
+      rs_pre = 1.0f;
+      if (lr < tn.rows) {
+        const float* rs = (const float*)g.a_scale;
+        rs_pre = tw ? rs[0] : rs[(int64_t)tn.e * g.rows + tn.row0 + lr];
+      }
+    };
+    if (!MX && WGRAD && pair < total_tiles) load_scales(pair);
     for (int t = pair; t < total_tiles && !*abort_flag; t += npairs) {
       const Tile tl = get_tile<WGRAD>(p, tiles_prefix, blk_prefix, bounds, t, rank, cur_e);
       const int64_t lrow = quarter * 32 + lane;
@@ -777,6 +807,20 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
       // first element of this tile in the output
       uint16_t* obase = WGRAD ? g.out + ((int64_t)tl.e * g.rows + tl.row0) * g.cols + tl.col0
                               : g.out + tl.row0 * g.cols + tl.col0;
+      // csb[c]: the scale of tile column c (for this warp's columns)
+      const float* csb = colscale;
+      float rscale = 1.0f;
+      if (!MX && WGRAD) {
+        // the buffer was last read by this warp two tiles ago
+        float* wbuf = colscale + (ew * 2 + sbuf) * EC;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) wbuf[lane + 32 * i] = cs_pre[i];
+        __syncwarp();
+        rscale = rs_pre;
+        csb = wbuf - c_lo;
+        if (t + npairs < total_tiles) load_scales(t + npairs);
+        sbuf ^= 1;
+      }
       if (tl.nk == 0) {  // empty group in wgrad: dW[e] = 0
         const int64_t wc = ncols - c_lo < EC ? ncols - c_lo : EC;   // this warp's columns
         const int nc8 = wc > 0 ? (int)(wc / 8) : 0;
@@ -787,8 +831,7 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
         }
         continue;
       }
-      float rscale = 1.0f;
-      if (!MX && tl.rows > 0) {
+      if (!MX && !WGRAD && tl.rows > 0) {
         // column scales of this tile into shared memory, row scale per thread
         // (tensorwise: one scale per operand)
         const bool tw = g.recipe == FP8MOE_TENSORWISE;
@@ -830,8 +873,8 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
           float v0 = __uint_as_float(j < 32 ? r0[j] : r1[j - 32]);
           float v1 = __uint_as_float(j < 32 ? r0[j + 1] : r1[j - 31]);
           if (!MX) {
-            v0 = v0 * rscale * colscale[c_lo + c + j];
-            v1 = v1 * rscale * colscale[c_lo + c + j + 1];
+            v0 = v0 * rscale * csb[c_lo + c + j];
+            v1 = v1 * rscale * csb[c_lo + c + j + 1];
           }
           packed[(c + j) / 2] = pack_bf16(v0, v1);
         }
