@@ -17,11 +17,14 @@
 //      memory, and every CTA derives the 64 scales;
 //   3. each CTA casts its slice from shared memory and writes the codes
 //      transposed: a lane turns 8 rows x 8 columns into 8-byte runs of its
-//      columns, four lanes complete a 32-byte sector of an output row.
-// A slice of more than CC_SR rows is processed in pieces: the maxima pass
-// loads every piece, the cast pass reloads them in reverse order (the last
-// piece is still resident; the others were read moments before and come
-// back from L2), so HBM still sees every input byte once.
+//      columns (each conversion pairs one column's values from two
+//      neighbouring rows, so the codes come out in column order), four
+//      lanes complete a 32-byte sector of an output row.
+// The boxes stream through a ring of NB slots: a slice of more boxes than
+// that keeps its last NB boxes for the cast and loads the earlier ones again
+// (read moments before, they come back from L2), so HBM still sees every
+// input byte once; the cast then runs in a pipeline over two groups of four
+// warps, each reload going into the slot its group has just freed.
 #include <cuda.h>
 
 #include <atomic>
