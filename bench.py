@@ -42,10 +42,10 @@ METRIC = "MXFP8 grouped-GEMM TFLOP/s (% FP8 peak); fused quant HBM GB/s (% peak)
 # the full layer by each mode's algorithmic bytes.  It is reported only while
 # the kernel source is the one that was captured (same SHA-256).
 GEMM_TRAFFIC = {"source": "mxfp8_moe_quantization_gb300/csrc/grouped_mm.cu",
-                "sha256": "67bfab9b87363805814d0b43f768def341a2eed6e1a462f1687c7ffcd88f8e94",
+                "sha256": "503e3ef16d9dc15f9d0b947bb3bd4d632d48e0ecca09219d9fef5ad1ae2d276e",
                 # full-size Scout W1 fwd / dgrad / wgrad: algorithmic bytes x the
                 # traffic / algorithmic ratio of an 8-expert capture
-                "bytes_per_launch": (1029.8e6 + 1052.6e6 + 1486.8e6) / 3}
+                "bytes_per_launch": (1030.3e6 + 1055.2e6 + 1474.9e6) / 3}
 
 
 def gemm_traffic():

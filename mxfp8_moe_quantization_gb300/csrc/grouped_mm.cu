@@ -40,6 +40,7 @@
 #include <cuda.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -224,6 +225,9 @@ struct KParams {
   int n_tiles;        // tiles along the output columns
   int m_tiles_w;      // wgrad: tiles along the output rows
   int tma_out;        // output stored by TMA (tmOut valid); else by thread stores
+  int wide_out;       // MXFP8 wgrad: 64-column store slices through one 4 KB staging tile per warp
+                      // (tmOut's box 64 columns, 128-byte swizzle); else 32-column slices
+                      // through two 2 KB tiles (box 32 columns, 64-byte swizzle)
   int stall_test;     // test hook (armed by fp8moe_testing_stall_next_gemm): one accumulator is never handed over
 };
 
@@ -884,64 +888,79 @@ __global__ void __launch_bounds__(num_threads<WGRAD, QA>(), 1)
       // Stores in 32-column slices through two 32-row x 64-byte staging tiles
       // per warp, laid out with the 64-byte swizzle (16-byte chunk c of row r
       // at r*64 + (c ^ ((r >> 1) & 3))*16: conflict-free for the row-per-lane
-      // writes and for the 2-rows-per-8-lanes reads).  A warp whose 32 rows
-      // are all in the output (always for MXFP8 fwd/dgrad, whose groups are
-      // multiples of 32, and for wgrad, whose 3-D map clips rows past the
-      // expert) hands each slice to a TMA store; a partial slice is written by
-      // the lanes with bounds checks.
+      // writes and for the 2-rows-per-8-lanes reads), or (wgrad, wide_out)
+      // in 64-column slices through one 32-row x 128-byte tile with the
+      // 128-byte swizzle: half the stores and their waits, which pays where
+      // the MMAs set the pace (long groups) and costs where the output writes
+      // do (many short groups keep more stores in flight with two tiles).  A
+      // warp whose 32 rows are all in the output (always for MXFP8 fwd/dgrad,
+      // whose groups are multiples of 32, and for wgrad, whose 3-D map clips
+      // rows past the expert) hands each slice to a TMA store; a partial
+      // slice is written by the lanes with bounds checks.
       const bool tma = p.tma_out && (WGRAD ? (int64_t)quarter * 32 < tl.rows : (int64_t)(quarter + 1) * 32 <= tl.rows);
       if (!tma && (int64_t)quarter * 32 >= tl.rows) continue;
-      constexpr int SC = L::STG_COLS, RB = SC * 2, NCH = SC / 8;   // columns, bytes, 16-B chunks per row
-      // 16-byte chunk c of staging row r: 64-byte swizzle (64-byte rows) or
-      // 128-byte swizzle (128-byte rows), as the output tensor map expects;
-      // conflict-free for row-per-lane writes and row-group reads
-      auto swz = [](int c, int r) { return NCH == 4 ? (c ^ ((r >> 1) & 3)) : (c ^ (r & 7)); };
+      auto store_slices = [&](auto sc_c, auto depth_c) {
+        constexpr int SC = decltype(sc_c)::value, DEPTH = decltype(depth_c)::value;
+        constexpr int RB = SC * 2, NCH = SC / 8, SBYTES = 32 * RB;   // row bytes, 16-B chunks per row, tile bytes
+        static_assert(DEPTH * SBYTES == L::STG_WARP_BYTES, "staging per warp");
+        // 16-byte chunk c of staging row r: 64-byte swizzle (64-byte rows) or
+        // 128-byte swizzle (128-byte rows), as the output tensor map expects;
+        // conflict-free for row-per-lane writes and row-group reads
+        auto swz = [](int c, int r) { return NCH == 4 ? (c ^ ((r >> 1) & 3)) : (c ^ (r & 7)); };
 #pragma unroll
-      for (int j = 0; j < EC / SC; ++j) {
-        const int cc = c_lo + j * SC;
-        if (cc < ncols) {
-          uint8_t* buf = stg + (j % L::STG_DEPTH) * L::STG_BYTES;
-          // the store that last read this buffer (STG_DEPTH slices ago) is
-          // done reading
-          if (lane == 0) {
-            if (tma) {
-              bulk_wait_read<L::STG_DEPTH - 1>();
-            } else {
-              bulk_wait_read<0>();
-            }
-          }
-          __syncwarp();
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            const int w = (j * SC + c * 8) / 2;
-            *reinterpret_cast<uint4*>(buf + lane * RB + (swz(c, lane) << 4)) =
-                make_uint4(packed[w], packed[w + 1], packed[w + 2], packed[w + 3]);
-          }
-          if (tma) {
-            fence_proxy_async_smem();
-            __syncwarp();
+        for (int j = 0; j < EC / SC; ++j) {
+          const int cc = c_lo + j * SC;
+          if (cc < ncols) {
+            uint8_t* buf = stg + (j % DEPTH) * SBYTES;
+            // the store that last read this buffer (DEPTH slices ago) is
+            // done reading
             if (lane == 0) {
-              if (WGRAD) {
-                tma_store_3d(&tmOut, buf, (int)(tl.col0 + cc), (int)(tl.row0 + quarter * 32), tl.e);
+              if (tma) {
+                bulk_wait_read<DEPTH - 1>();
               } else {
-                tma_store_2d(&tmOut, buf, (int)(tl.col0 + cc), (int)(tl.row0 + quarter * 32));
+                bulk_wait_read<0>();
               }
-              bulk_commit();
             }
-          } else {
             __syncwarp();
 #pragma unroll
-            for (int i = 0; i < NCH; ++i) {
-              const int r = i * (32 / NCH) + lane / NCH, ch = lane % NCH;
-              const uint4 v = *reinterpret_cast<const uint4*>(buf + r * RB + (swz(ch, r) << 4));
-              const int64_t trow = quarter * 32 + r;
-              const int64_t col = cc + ch * 8;
-              if (trow < tl.rows && col < ncols) *reinterpret_cast<uint4*>(obase + trow * g.cols + col) = v;
+            for (int c = 0; c < NCH; ++c) {
+              const int w = (j * SC + c * 8) / 2;
+              *reinterpret_cast<uint4*>(buf + lane * RB + (swz(c, lane) << 4)) =
+                  make_uint4(packed[w], packed[w + 1], packed[w + 2], packed[w + 3]);
             }
-            __syncwarp();
+            if (tma) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                if (WGRAD) {
+                  tma_store_3d(&tmOut, buf, (int)(tl.col0 + cc), (int)(tl.row0 + quarter * 32), tl.e);
+                } else {
+                  tma_store_2d(&tmOut, buf, (int)(tl.col0 + cc), (int)(tl.row0 + quarter * 32));
+                }
+                bulk_commit();
+              }
+            } else {
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < NCH; ++i) {
+                const int r = i * (32 / NCH) + lane / NCH, ch = lane % NCH;
+                const uint4 v = *reinterpret_cast<const uint4*>(buf + r * RB + (swz(ch, r) << 4));
+                const int64_t trow = quarter * 32 + r;
+                const int64_t col = cc + ch * 8;
+                if (trow < tl.rows && col < ncols) *reinterpret_cast<uint4*>(obase + trow * g.cols + col) = v;
+              }
+              __syncwarp();
+            }
           }
         }
+      };
+      if constexpr (WGRAD && MX) {
+        if (p.wide_out) {
+          store_slices(std::integral_constant<int, 64>{}, std::integral_constant<int, 1>{});
+          continue;
+        }
       }
+      store_slices(std::integral_constant<int, L::STG_COLS>{}, std::integral_constant<int, L::STG_DEPTH>{});
     }
     // the output stores have left shared memory and reached global memory
     if (lane == 0) bulk_wait_all();
@@ -1096,13 +1115,22 @@ cudaError_t launch_grouped_mm(const GemmArgs& g, cudaStream_t st) {
   // swizzle; wgrad as [E, rows, cols] so that rows past an expert are clipped
   CUtensorMap tout = ta;
   p.tma_out = 0;
+  p.wide_out = 0;
   if (((uintptr_t)g.out % 16) == 0 && (g.cols * 2) % 16 == 0) {
     bool ok;
     if (wgrad) {
       cuuint64_t dims[3] = {(cuuint64_t)g.cols, (cuuint64_t)g.rows, (cuuint64_t)g.E};
       cuuint64_t strides[2] = {(cuuint64_t)(g.cols * 2), (cuuint64_t)(g.rows * g.cols * 2)};
-      cuuint32_t box[3] = {(cuuint32_t)SmemLayout<false, true>::STG_COLS, 32, 1};
-      ok = make_tmap(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.out, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+      // 64-column slices (one 4 KB staging tile per epilogue warp) for MXFP8
+      // groups of 512 tokens or more on average, where the MMAs set the pace
+      // (Scout wgrad 584 against 601 us); 32-column slices in two tiles
+      // where the output writes do (DeepSeek-V3, ~142 tokens a group: 1,417
+      // against 1,527 us) and for the rowwise recipe (no difference measured
+      // on MoE-16B, 2% the other way on Llama3)
+      p.wide_out = g.recipe == FP8MOE_MXFP8 && g.E > 0 && g.M / g.E >= 512;
+      cuuint32_t box[3] = {(cuuint32_t)(p.wide_out ? 64 : SmemLayout<false, true>::STG_COLS), 32, 1};
+      ok = make_tmap(&tout, CU_TENSOR_MAP_DATA_TYPE_UINT16, g.out, 3, dims, strides, box,
+                     p.wide_out ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     } else {
       cuuint64_t dims[2] = {(cuuint64_t)g.cols, (cuuint64_t)(g.M > 0 ? g.M : 1)};
       cuuint64_t strides[1] = {(cuuint64_t)(g.cols * 2)};

@@ -115,6 +115,9 @@ SHAPES = {
     "ragged": ([64, 0, 352, 32, 160], 320, 384),
     "dense": ([512], 1024, 512),
     "wide_k": ([128, 96, 0, 288], 256, 1408 + 128),
+    # groups of 512 tokens or more on average: the wgrad stores 64-column
+    # slices; 352 columns leave a half slice, 288 rows a partial tile
+    "long_groups": ([704, 0, 896], 288, 352),
 }
 RW_SHAPES = {
     "tiny": (list(W.group_sizes("tiny")), 512, 256),
