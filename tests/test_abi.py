@@ -33,8 +33,15 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
-        assert lib.fp8moe_status_string(code)
+    """Every code of the header's fp8moe_status enum has its own message."""
+    hdr = open(os.path.join(ROOT, "include", "fp8moe.h")).read()
+    body = hdr[hdr.index("typedef enum {"):hdr.index("} fp8moe_status;")]
+    codes = {name: int(v) for name, v in re.findall(r"(FP8MOE_\w+)\s*=\s*(\d+)", body)}
+    assert codes["FP8MOE_OK"] == 0 and codes["FP8MOE_ERR_CONCURRENT"] == 8
+    unknown = lib.fp8moe_status_string(max(codes.values()) + 1)
+    msgs = [lib.fp8moe_status_string(c) for c in sorted(codes.values())]
+    assert all(m and m != unknown for m in msgs)
+    assert len(set(msgs)) == len(msgs)
     assert lib.fp8moe_version() >> 16 == 1
 
 
