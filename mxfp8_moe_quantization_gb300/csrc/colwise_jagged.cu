@@ -57,10 +57,15 @@ constexpr int CJ_SLOTS = 16;                         // work-counter slots, one 
 // Every CTA first raises the word to gen << 32 (a no-op once another CTA of
 // the launch has), then takes units with atomicAdd; a word whose top half
 // is not `gen` means that another launch in flight holds the slot, which
-// the launch reports as FP8MOE_ERR_CONCURRENT.  The `done` word counts the
-// CTAs that have finished taking units; the last one returns both words to
-// zero, so a replay of the same launch (a CUDA graph) starts clean.
+// the launch reports as FP8MOE_ERR_CONCURRENT.  The `units` word sums the
+// units each CTA handed to its consumers and the `done` word counts the
+// CTAs that have finished taking units (same tags); the last CTA checks that
+// the launch took every unit exactly once (another launch's takes from the
+// slot would have consumed some of its counts: FP8MOE_ERR_CONCURRENT, never
+// a silent gap) and returns the three words to zero, so a replay of the same
+// launch (a CUDA graph) starts clean.
 __device__ unsigned long long g_cj_work[CJ_SLOTS];
+__device__ unsigned long long g_cj_units[CJ_SLOTS];
 __device__ unsigned long long g_cj_done[CJ_SLOTS];
 
 struct CjArgs {
@@ -150,9 +155,12 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
     if (lane == 0) {
       unsigned long long* wk = &g_cj_work[a.gen % CJ_SLOTS];
       unsigned long long* dn = &g_cj_done[a.gen % CJ_SLOTS];
+      unsigned long long* pu = &g_cj_units[a.gen % CJ_SLOTS];
       const unsigned long long tag = (unsigned long long)a.gen << 32;
       atomicMax(wk, tag);
       atomicMax(dn, tag);
+      atomicMax(pu, tag);
+      uint32_t handed = 0;   // units this CTA published to its consumers
       // the next unit's index: taken one unit ahead, so that the atomic's
       // round trip overlaps the issue of the current unit's boxes
       unsigned long long taken = atomicAdd(wk, 1ull);
@@ -197,6 +205,7 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
         U u;
         unit_of(k, u);
         publish(n, k);
+        ++handed;
         const int passes = u.nbox <= CJ_NS ? 1 : 2;
         for (int p = 0; p < passes && live; ++p)
           for (int b = 0; b < u.nbox; ++b, ++f) {
@@ -229,11 +238,18 @@ __global__ void __launch_bounds__(CJ_THREADS, 1) k_cw_jag_ws(const __grid_consta
       // consumers may have stopped early): the last fill of each slot
       for (uint32_t j = f > CJ_NS ? f - CJ_NS : 0; j < f; ++j)
         (void)mbar_wait(&full[j % CJ_NS], (j / CJ_NS) & 1u, nullptr);
-      // the last CTA to finish taking units clears the slot
+      // the last CTA to finish taking units checks the sum and clears the slot
+      atomicAdd(pu, (unsigned long long)handed);
+      __threadfence();
       const unsigned long long d = atomicAdd(dn, 1ull);
       if ((d >> 32) == a.gen && (d & 0xFFFFFFFFull) == gridDim.x - 1) {
+        __threadfence();
+        const unsigned long long pv = atomicAdd(pu, 0ull);
+        if ((pv >> 32) != a.gen || (pv & 0xFFFFFFFFull) != (unsigned long long)a.units)
+          set_status(a.status, FP8MOE_ERR_CONCURRENT);
         atomicExch(wk, 0ull);
         atomicExch(dn, 0ull);
+        atomicExch(pu, 0ull);
       }
     }
     return;
